@@ -1,0 +1,144 @@
+"""Seeded synthetic inputs for the gated delta rule (shared by tests and bench).
+
+This module only draws random numbers and shapes them; it holds none of the
+method's arithmetic, so both the CUDA path and the float64 oracle can take
+their inputs from it without sharing any computation.
+
+Recipe (one per variant, drawn in fp32 on the CPU with a seeded
+``torch.Generator``, then cast to the compute dtype):
+
+* q, k ~ N(0, 1), each token-head vector L2-normalised over its channels
+  (the pages normalise q and k before the rule: Gated DeltaNet-2 notes,
+  training strategy; LLMs from scratch ch. 11 section 11.3). With
+  ``q_prescaled`` q is also multiplied by d_k^-1/2 and the read-out scale
+  is 1, otherwise the read-out scale is d_k^-1/2.
+* v ~ N(0, 1).
+* scalar log-decay g = -softplus(N(0, 1)) per token and head (Gated
+  DeltaNet, Q-Delta); channel log-decay g = -exp(N(-2, 0.5)) per key
+  channel (KDA, Gated DeltaNet-2). Gates stay fp32.
+* beta = sigmoid(N(0, 1)) per token and head.
+* Q-Delta: lambda ~ U[0, 1] per head, broadcast over batch and time; the
+  write strength is capped so that beta * k^T x < 2 with x = k + lambda q:
+  beta = sigmoid(N(0,1)) * min(1, 1.9 / (k^T x)) (factor 1 when k^T x <= 0),
+  which keeps Q-Delta's one-step contraction condition (its notes, key
+  design 4) true. k and q here are the values after the dtype cast.
+* Gated DeltaNet-2: erase gate b = sigmoid(N(0, 1)) per key channel, write
+  gate w = sigmoid(N(0, 1)) per value channel, in the compute dtype.
+* Initial state (when asked for) ~ N(0, std^2) in fp32, layout
+  [B, H, d_k, d_v].
+
+The five named workloads mirror the pages' 340M / 1.3B layer shapes.
+"""
+import math
+
+import torch
+
+DECAY_CHANNEL = 1
+ERASE_CHANNEL = 2
+WRITE_CHANNEL = 4
+QMIX = 8
+
+VARIANT_FLAGS = {
+    "gdn": 0,
+    "qdelta": QMIX,
+    "kda": DECAY_CHANNEL,
+    "gdn2": DECAY_CHANNEL | ERASE_CHANNEL | WRITE_CHANNEL,
+}
+
+# name -> recipe of the five workloads (the fifth also has a decode phase)
+CONFIGS = {
+    1: dict(name="gdn_fp32_b1_t256_h2_d64", variant="gdn", B=1, T=256, H=2, dk=64, dv=64,
+            dtype=torch.float32, q_prescaled=True, h0_std=None, seed=0),
+    2: dict(name="gdn_bf16_b4_t4096_h16_d128", variant="gdn", B=4, T=4096, H=16, dk=128,
+            dv=128, dtype=torch.bfloat16, q_prescaled=False, h0_std=0.02, seed=1),
+    3: dict(name="qdelta_bf16_b4_t8192_h16_d128", variant="qdelta", B=4, T=8192, H=16,
+            dk=128, dv=128, dtype=torch.bfloat16, q_prescaled=False, h0_std=None, seed=2),
+    4: dict(name="kda_bf16_b2_t16384_h32_d128", variant="kda", B=2, T=16384, H=32, dk=128,
+            dv=128, dtype=torch.bfloat16, q_prescaled=False, h0_std=None, seed=3),
+    5: dict(name="gdn2_bf16_b1_t65536_h32_d128", variant="gdn2", B=1, T=65536, H=32,
+            dk=128, dv=128, dtype=torch.bfloat16, q_prescaled=False, h0_std=None, seed=4,
+            decode=dict(steps=256, N=256, h_std=0.02)),
+}
+
+
+def _l2norm(x):
+    return x / x.norm(dim=-1, keepdim=True).clamp_min(1e-12)
+
+
+def make_inputs(variant, B, T, H, dk, dv, dtype=torch.bfloat16, seed=0,
+                q_prescaled=False, h0_std=None, device="cpu"):
+    """Seeded inputs of one variant in the [B, T, H, d] layout.
+
+    Returns a dict with q, k, v (dtype), g (fp32, [B,T,H] or [B,T,H,d_k]),
+    beta / lam (fp32 [B,T,H] or None), b / w (dtype or None), h0 (fp32 or
+    None), scale (float), flags (int) and variant.
+    """
+    if variant not in VARIANT_FLAGS:
+        raise ValueError("unknown variant %r" % variant)
+    flags = VARIANT_FLAGS[variant]
+    gen = torch.Generator().manual_seed(int(seed))
+
+    def normal(*shape, mean=0.0, std=1.0):
+        return torch.randn(*shape, generator=gen, dtype=torch.float32) * std + mean
+
+    q = _l2norm(normal(B, T, H, dk))
+    k = _l2norm(normal(B, T, H, dk))
+    if q_prescaled:
+        q = q * dk ** -0.5
+        scale = 1.0
+    else:
+        scale = dk ** -0.5
+    v = normal(B, T, H, dv)
+    q, k, v = q.to(dtype), k.to(dtype), v.to(dtype)
+
+    if flags & DECAY_CHANNEL:
+        g = -torch.exp(normal(B, T, H, dk, mean=-2.0, std=0.5))
+    else:
+        g = -torch.nn.functional.softplus(normal(B, T, H))
+    beta = lam = b = w = None
+    if not (flags & ERASE_CHANNEL and flags & WRITE_CHANNEL):
+        beta = torch.sigmoid(normal(B, T, H))
+    if flags & QMIX:
+        lam_h = torch.rand(H, generator=gen, dtype=torch.float32)
+        lam = lam_h.view(1, 1, H).expand(B, T, H).contiguous()
+        kf, qf = k.float(), q.float()
+        a = (kf * (kf + lam[..., None] * qf)).sum(-1)
+        cap = torch.where(a > 0, torch.clamp(1.9 / a.clamp_min(1e-30), max=1.0),
+                          torch.ones_like(a))
+        beta = beta * cap
+    if flags & ERASE_CHANNEL:
+        b = torch.sigmoid(normal(B, T, H, dk)).to(dtype)
+    if flags & WRITE_CHANNEL:
+        w = torch.sigmoid(normal(B, T, H, dv)).to(dtype)
+    h0 = None
+    if h0_std is not None:
+        h0 = normal(B, H, dk, dv, std=h0_std)
+    out = dict(q=q, k=k, v=v, g=g.contiguous(), beta=beta, lam=lam, b=b, w=w, h0=h0,
+               scale=float(scale), flags=flags, variant=variant)
+    if device != "cpu":
+        out = {key: (val.to(device) if torch.is_tensor(val) else val) for key, val in out.items()}
+    return out
+
+
+def config_inputs(cfg_id, device="cpu", **override):
+    """Inputs of one of the five named workloads (prefill part)."""
+    c = dict(CONFIGS[cfg_id])
+    c.update(override)
+    return make_inputs(c["variant"], c["B"], c["T"], c["H"], c["dk"], c["dv"], c["dtype"],
+                       c["seed"], c["q_prescaled"], c["h0_std"], device=device)
+
+
+def decode_inputs(variant, N, H, dk, dv, dtype=torch.bfloat16, seed=0, h_std=0.02,
+                  device="cpu"):
+    """One decode step's inputs: [N, 1, H, d] tensors plus a state [N, H, d_k, d_v]."""
+    x = make_inputs(variant, N, 1, H, dk, dv, dtype, seed, False, h_std, device)
+    return x
+
+
+def token_heads(cfg_id):
+    c = CONFIGS[cfg_id]
+    return c["B"] * c["T"] * c["H"]
+
+
+def n_chunks(T, C=64):
+    return math.ceil(T / C)
