@@ -1,0 +1,425 @@
+"""Throughput of the chunked gated-delta forward on one GB300 (JSON line out).
+
+One step = the whole hot path over one batch: the chunkwise forward of the
+Gated DeltaNet workload B=4, T=4096, H=16, d_k=d_v=128 (bf16 inputs, fp32
+state, random initial state, final state returned), then one decode step per
+(sequence, head) continuing from that final state. Unit: token-heads per
+second (prefill B*T*H plus decode B*H per step). Other workloads are selected
+with --workload (1..5; the decode phase applies where the workload has one).
+
+Timing: W untimed warm-up steps, then K steps, each bracketed by CUDA events
+on the launching stream with the L2 flushed (a 256 MiB write) before every
+step, outside the events. Per-kernel events give the roofline of the chunk
+kernel. Under torchrun each rank runs its own copy of the workload (weak
+scaling; no collective on the data path) and the time is the max over ranks.
+
+--impl reference times the float64 CPU oracle on the host cores instead (a
+bounded sample of the same workload per step).
+"""
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from gated_delta_rule_10_gb300 import workloads as wl  # noqa: E402
+
+METRIC = "gated-delta chunk fwd tokens·heads/s at 1 GB300; % of bf16 tensor/HBM roofline"
+UNIT = "token-heads/s"
+PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def parse():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=300)
+    p.add_argument("--warmup", type=int, default=5)
+    p.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    p.add_argument("--workload", type=int, default=2, choices=[1, 2, 3, 4, 5])
+    p.add_argument("--decode-steps", type=int, default=1)
+    p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    return p.parse_args()
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def peaks():
+    try:
+        with open(PEAKS_FILE) as f:
+            d = json.load(f)
+        return d, "measured"
+    except (OSError, ValueError):
+        return FALLBACK_PEAKS, "fallback"
+
+
+def algorithmic_flops_per_th(dk, dv, C=64):
+    """Minimal FLOPs per token-head of the chunk algorithm (triangles counted once):
+    6 dk dv (Y S, Q_gamma S, K_tail^T W) + (C-1)(2 dk + dv) (T, Y, U strictly lower)
+    + (C+1)(dk + dv) (A_qk and A_qk W with the diagonal) + C^2/3 (substitution)."""
+    return 6 * dk * dv + (C - 1) * (2 * dk + dv) + (C + 1) * (dk + dv) + C * C / 3.0
+
+
+def tensor_bytes(*ts):
+    return sum(t.numel() * t.element_size() for t in ts if t is not None)
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons, sampled while the timed loop runs."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.proc = None
+        self.file = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(gpu_index), "--query-gpu=" + self.FIELDS,
+                 "--format=csv,noheader,nounits", "-lms", "50"],
+                stdout=self.file, stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.file.flush()
+        rows = []
+        with open(self.file.name) as f:
+            for line in f:
+                parts = [x.strip() for x in line.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+        os.unlink(self.file.name)
+        if not rows:
+            return None
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i] == "Active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons,
+                "samples": len(rows)}
+
+
+def make_step_inputs(cfg_id, rank, dev):
+    c = wl.CONFIGS[cfg_id]
+    x = wl.config_inputs(cfg_id, seed=c["seed"] + 1000 * rank)
+    N, H = c["B"], c["H"]
+    if "decode" in c:
+        N = c["decode"]["N"]
+    y = wl.make_inputs(c["variant"], N, 1, H, c["dk"], c["dv"], c["dtype"],
+                       seed=c["seed"] + 1000 * rank + 1, q_prescaled=c["q_prescaled"])
+    return c, x, y
+
+
+def squeeze_t(t):
+    return None if t is None else t[:, 0].contiguous()
+
+
+def run_ours(args):
+    import gated_delta_rule_10_gb300 as gdr
+
+    rank, world, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    c, x, y = make_step_inputs(args.workload, rank, dev)
+    xd = {k: (v.to(dev) if torch.is_tensor(v) else v) for k, v in x.items()}
+    yd = {k: (squeeze_t(v).to(dev) if torch.is_tensor(v) else v) for k, v in y.items()}
+    B, T, H, dk, dv = c["B"], c["T"], c["H"], c["dk"], c["dv"]
+    N = y["q"].shape[0]
+    has_decode = args.decode_steps > 0
+    o = torch.empty(B, T, H, dv, dtype=c["dtype"], device=dev)
+    hT = torch.empty(B, H, dk, dv, dtype=torch.float32, device=dev)
+    # decode state: the prefill's final state when the batch matches, else its own
+    if N == B:
+        state = hT
+    else:
+        gen = torch.Generator().manual_seed(99 + rank)
+        state = (torch.randn(N, H, dk, dv, generator=gen) * c.get("decode", {}).get("h_std", 0.02)
+                 ).to(dev)
+    o_dec = torch.empty(N, H, dv, dtype=c["dtype"], device=dev)
+    stream = torch.cuda.current_stream(dev)
+    flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
+
+    def step():
+        gdr.chunk_fwd(xd["q"], xd["k"], xd["v"], xd["g"], xd["beta"], xd["lam"], xd["b"],
+                      xd["w"], xd["h0"], scale=x["scale"], flags=x["flags"], o=o, hT=hT)
+        for _ in range(args.decode_steps if has_decode else 0):
+            gdr.recurrent_step(yd["q"], yd["k"], yd["v"], yd["g"], state, yd["beta"], yd["lam"],
+                               yd["b"], yd["w"], scale=y["scale"], flags=y["flags"], o=o_dec)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+
+    K = args.steps
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    clocks = ClockSampler(local)
+    time.sleep(0.1)
+    for i in range(K):
+        flush.fill_(float(i))
+        ev[i][0].record(stream)
+        gdr.chunk_fwd(xd["q"], xd["k"], xd["v"], xd["g"], xd["beta"], xd["lam"], xd["b"],
+                      xd["w"], xd["h0"], scale=x["scale"], flags=x["flags"], o=o, hT=hT)
+        ev[i][1].record(stream)
+        for _ in range(args.decode_steps if has_decode else 0):
+            gdr.recurrent_step(yd["q"], yd["k"], yd["v"], yd["g"], state, yd["beta"], yd["lam"],
+                               yd["b"], yd["w"], scale=y["scale"], flags=y["flags"], o=o_dec)
+        ev[i][2].record(stream)
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    if world > 1:
+        torch.distributed.barrier()
+    chunk_ms = [ev[i][0].elapsed_time(ev[i][1]) for i in range(K)]
+    dec_ms = [ev[i][1].elapsed_time(ev[i][2]) for i in range(K)]
+    step_ms = [a + b for a, b in zip(chunk_ms, dec_ms)]
+    total_ms = sum(step_ms)
+    if world > 1:
+        t = torch.tensor([total_ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        total_ms = float(t.item())
+
+    th_prefill = B * T * H
+    th_decode = N * H * (args.decode_steps if has_decode else 0)
+    th_step = th_prefill + th_decode
+    value = th_step * K * world / (total_ms / 1e3)
+
+    # roofline of the dominant kernel (the chunked forward), algorithmic bytes
+    pk, pk_kind = peaks()
+    chunk_bytes = tensor_bytes(xd["q"], xd["k"], xd["v"], xd["g"], xd["beta"], xd["lam"],
+                               xd["b"], xd["w"], xd["h0"], o, hT)
+    mean_chunk_s = statistics.mean(chunk_ms) / 1e3
+    gbs = chunk_bytes / mean_chunk_s / 1e9
+    flops = algorithmic_flops_per_th(dk, dv) * th_prefill
+    tflops = flops / mean_chunk_s / 1e12
+    ridge = pk["bf16_tflops"] * 1e12 / (pk["hbm_gbs"] * 1e9)
+    bound = "hbm" if flops / chunk_bytes < ridge else "tensor"
+    if bound == "hbm":
+        roof = {"bound": "hbm", "achieved": round(gbs, 1), "peak": pk["hbm_gbs"], "unit": "GB/s",
+                "frac": round(gbs / pk["hbm_gbs"], 4)}
+    else:
+        roof = {"bound": "tensor", "achieved": round(tflops, 2), "peak": pk["bf16_tflops"],
+                "unit": "TFLOP/s", "frac": round(tflops / pk["bf16_tflops"], 4)}
+    roof.update({"traffic": None, "kernel": "chunk_fwd_kernel", "peak_source": pk_kind,
+                 "algorithmic_bytes_per_launch": chunk_bytes,
+                 "algorithmic_flops_per_launch": flops,
+                 "tensor_tflops_achieved": round(tflops, 2),
+                 "tensor_frac_of_bf16_peak": round(tflops / pk["bf16_tflops"], 4),
+                 "launch_ms_mean": round(statistics.mean(chunk_ms), 4)})
+    dec_bytes = tensor_bytes(yd["q"], yd["k"], yd["v"], yd["g"], yd["beta"], yd["lam"],
+                             yd["b"], yd["w"], o_dec) + 2 * tensor_bytes(state)
+    decode_info = None
+    if has_decode and statistics.mean(dec_ms) > 0:
+        dgbs = dec_bytes * args.decode_steps / (statistics.mean(dec_ms) / 1e3) / 1e9
+        decode_info = {"kernel": "recurrent_step_kernel", "N": N, "H": H,
+                       "ms_mean": round(statistics.mean(dec_ms), 4),
+                       "achieved_gbs": round(dgbs, 1), "frac_hbm": round(dgbs / pk["hbm_gbs"], 4)}
+
+    e2e = None if args.no_e2e else measure_e2e(gdr, x, y, c, dev, args, B, T, H, dk, dv, N)
+
+    result = {
+        "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world, "steps": K,
+        "warmup": args.warmup, "ms_per_step": round(total_ms / K, 5), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16" if c["dtype"] == torch.bfloat16
+        else "f32", "data": "synthetic",
+        "config": {"workload": c["name"] + (" + %d decode step(s) at N=%d" %
+                                            (args.decode_steps, N) if has_decode else ""),
+                   "variant": c["variant"], "B": B, "T": T, "H": H, "dk": dk, "dv": dv,
+                   "chunk": 64, "token_heads_per_step": th_step,
+                   "l2": "flushed before every timed step (256 MiB write, outside the events)",
+                   "parallelism": "replica per GPU" if world > 1 else "single GPU"},
+        "roofline": roof,
+        "decode": decode_info,
+        "gpu_launches": K * (1 + (args.decode_steps if has_decode else 0)),
+        "clocks": clk,
+        "e2e": e2e,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        result["cpu_baseline"] = cpu_baseline(x, y if N == B else None, th_step)
+    if rank == 0:
+        print(json.dumps(result), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+def measure_e2e(gdr, x, y, c, dev, args, B, T, H, dk, dv, N, steps=5):
+    """Same metric through the public API with pinned host buffers: every step
+    copies its inputs host->device, runs the path, and copies o, the decode
+    output and the final state back."""
+    names = ("q", "k", "v", "g", "beta", "lam", "b", "w", "h0")
+    hx = {n: x[n].pin_memory() for n in names if x[n] is not None}
+    hy = {n: squeeze_t(y[n]).pin_memory() for n in ("q", "k", "v", "g", "beta", "lam", "b", "w")
+          if y[n] is not None}
+    dx = {n: torch.empty_like(t, device=dev) for n, t in hx.items()}
+    dy = {n: torch.empty_like(t, device=dev) for n, t in hy.items()}
+    o = torch.empty(B, T, H, dv, dtype=c["dtype"], device=dev)
+    hT = torch.empty(B, H, dk, dv, dtype=torch.float32, device=dev)
+    state = hT if N == B else torch.zeros(N, H, dk, dv, device=dev)
+    o_dec = torch.empty(N, H, dv, dtype=c["dtype"], device=dev)
+    ho = torch.empty_like(o, device="cpu").pin_memory()
+    hhT = torch.empty_like(state, device="cpu").pin_memory()
+    ho_dec = torch.empty_like(o_dec, device="cpu").pin_memory()
+    stream = torch.cuda.current_stream(dev)
+    g = lambda d, n: d.get(n)
+
+    def one():
+        for n in hx:
+            dx[n].copy_(hx[n], non_blocking=True)
+        for n in hy:
+            dy[n].copy_(hy[n], non_blocking=True)
+        gdr.chunk_fwd(g(dx, "q"), g(dx, "k"), g(dx, "v"), g(dx, "g"), g(dx, "beta"),
+                      g(dx, "lam"), g(dx, "b"), g(dx, "w"), g(dx, "h0"), scale=x["scale"],
+                      flags=x["flags"], o=o, hT=hT)
+        for _ in range(args.decode_steps):
+            gdr.recurrent_step(g(dy, "q"), g(dy, "k"), g(dy, "v"), g(dy, "g"), state,
+                               g(dy, "beta"), g(dy, "lam"), g(dy, "b"), g(dy, "w"),
+                               scale=y["scale"], flags=y["flags"], o=o_dec)
+        ho.copy_(o, non_blocking=True)
+        ho_dec.copy_(o_dec, non_blocking=True)
+        hhT.copy_(state, non_blocking=True)
+
+    one()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(steps):
+        one()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / steps
+    th = B * T * H + N * H * args.decode_steps
+    h2d = sum(t.numel() * t.element_size() for t in hx.values()) + \
+        sum(t.numel() * t.element_size() for t in hy.values()) * args.decode_steps
+    d2h = tensor_bytes(ho, ho_dec, hhT)
+    return {"value": round(th / (ms / 1e3), 1), "unit": UNIT, "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h, "ms_per_step": round(ms, 4), "steps": steps}
+
+
+def oracle_step(x, y, seqs, nthreads):
+    """The oracle on `seqs` (batch, head) sequences of the step's workload: the
+    prefill tokens followed by the decode token (same math as the GPU step)."""
+    import numpy as np
+    from oracle import native
+
+    f64 = lambda t: None if t is None else t.double().numpy()
+    out_th = 0
+    t_total = 0.0
+    for (b, h) in seqs:
+        def pick(n):
+            t = x[n]
+            if t is None:
+                return None
+            t = t[b:b + 1, :, h:h + 1]
+            if y is not None and y[n] is not None:
+                t = torch.cat([t, y[n][b:b + 1, :, h:h + 1]], dim=1)
+            return f64(t.contiguous())
+        args = [pick(n) for n in ("q", "k", "v", "g", "beta", "lam", "b", "w")]
+        h0 = None if x["h0"] is None else f64(x["h0"][b:b + 1, h:h + 1].contiguous())
+        t0 = time.perf_counter()
+        native.recurrence(*args[:4], beta=args[4], lam=args[5], b=args[6], w=args[7], h0=h0,
+                          scale=x["scale"], flags=x["flags"], nthreads=1)
+        t_total += time.perf_counter() - t0
+        out_th += args[0].shape[1]
+    return out_th, t_total
+
+
+def cpu_baseline(x, y, th_step, budget_s=20.0):
+    """The oracle as it stands, timed on the host cores: every (batch, head)
+    sequence of the workload (each the prefill plus the decode token), spread
+    over all cores with OpenMP, repeated until ~budget_s or one pass."""
+    import numpy as np
+    from oracle import native
+
+    f64 = lambda t: None if t is None else t.double().numpy()
+    cat = lambda n: (torch.cat([x[n], y[n]], dim=1) if (y is not None and x[n] is not None)
+                     else x[n])
+    arrs = {n: f64(cat(n)) for n in ("q", "k", "v", "g", "beta", "lam", "b", "w")}
+    h0 = f64(x["h0"])
+    cores = native.max_threads()
+    th = arrs["q"].shape[0] * arrs["q"].shape[1] * arrs["q"].shape[2]
+    reps, t_total = 0, 0.0
+    while reps == 0 or (t_total < budget_s and reps < 3):
+        t0 = time.perf_counter()
+        native.recurrence(arrs["q"], arrs["k"], arrs["v"], arrs["g"], arrs["beta"], arrs["lam"],
+                          arrs["b"], arrs["w"], h0, x["scale"], x["flags"], nthreads=cores)
+        t_total += time.perf_counter() - t0
+        reps += 1
+    return {"value": round(th * reps / t_total, 1), "unit": UNIT, "cores": cores,
+            "kind": "oracle", "sample": "whole workload (%d token-heads incl. decode tokens), "
+            "%d pass(es), C fp64 token recurrence, OpenMP over (batch, head)" % (th, reps),
+            "seconds": round(t_total, 3)}
+
+
+def run_reference(args):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return
+    from oracle import native
+    c, x, y = make_step_inputs(args.workload, 0, "cpu")
+    N = y["q"].shape[0]
+    yy = y if N == c["B"] else None
+    B, H = c["B"], c["H"]
+    # bounded sample per step: 2 sequences (each ~0.5 GFLOP at T=4096)
+    seqs_all = [(b, h) for b in range(B) for h in range(H)]
+    per_step = 2
+    for i in range(args.warmup):
+        oracle_step(x, yy, seqs_all[:1], 1)
+    th_total, t_total = 0, 0.0
+    steps = max(1, min(args.steps, 8))
+    for i in range(steps):
+        seqs = [seqs_all[(i * per_step + j) % len(seqs_all)] for j in range(per_step)]
+        th, t = oracle_step(x, yy, seqs, 1)
+        th_total += th
+        t_total += t
+    value = th_total / t_total
+    res = {"metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world,
+           "steps": steps, "warmup": args.warmup, "ms_per_step": round(1e3 * t_total / steps, 3),
+           "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+           "data": "synthetic", "impl": "reference",
+           "config": {"workload": c["name"], "variant": c["variant"], "B": c["B"], "T": c["T"],
+                      "H": c["H"], "dk": c["dk"], "dv": c["dv"]},
+           "cpu_baseline": {"value": round(value, 1), "unit": UNIT, "cores": 1, "kind": "oracle",
+                            "sample": "%d (batch, head) sequences per step (prefill plus "
+                                      "decode token), single thread" % per_step},
+           "e2e": {"value": round(value, 1), "unit": UNIT, "h2d_bytes_per_step": 0,
+                   "d2h_bytes_per_step": 0}}
+    print(json.dumps(res), flush=True)
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

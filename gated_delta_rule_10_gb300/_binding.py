@@ -1,0 +1,220 @@
+"""ctypes binding of libgdr.so: argument marshalling only.
+
+Every step of the computation runs in the library's CUDA kernels; this module
+checks tensor devices, dtypes and layouts, allocates outputs with PyTorch and
+passes raw pointers plus the current CUDA stream through the C ABI declared in
+``include/gdr.h``. There is no fallback: if the library is missing or a call
+fails, an exception is raised.
+"""
+import ctypes
+import os
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libgdr.so")
+
+GDR_F32 = 0
+GDR_BF16 = 1
+DECAY_CHANNEL = 1
+ERASE_CHANNEL = 2
+WRITE_CHANNEL = 4
+QMIX = 8
+CHUNK = 64
+
+STATUS = {0: "GDR_OK", 1: "GDR_ERR_INVALID_ARG", 2: "GDR_ERR_UNSUPPORTED", 3: "GDR_ERR_CUDA",
+          4: "GDR_ERR_WORKSPACE", 5: "GDR_ERR_TIMEOUT"}
+
+
+class GdrError(RuntimeError):
+    def __init__(self, code, where):
+        self.code = code
+        super().__init__("%s failed: %s" % (where, status_string(code)))
+
+
+class Shape(ctypes.Structure):
+    """Mirror of ``gdr_shape``."""
+    _fields_ = [("B", ctypes.c_int), ("T", ctypes.c_int), ("H", ctypes.c_int),
+                ("dk", ctypes.c_int), ("dv", ctypes.c_int), ("dtype", ctypes.c_int),
+                ("flags", ctypes.c_uint), ("scale", ctypes.c_float)]
+
+
+_lib = None
+_vp = ctypes.c_void_p
+
+
+def lib():
+    """The loaded libgdr.so (raises if it has not been built)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError("libgdr.so is not built (%s); run __graft_entry__.build() or "
+                               "python -m gated_delta_rule_10_gb300.build" % LIB_PATH)
+        L = ctypes.CDLL(LIB_PATH)
+        sp = ctypes.POINTER(Shape)
+        L.gdr_chunk_fwd_workspace.argtypes = [sp, ctypes.POINTER(ctypes.c_size_t)]
+        L.gdr_chunk_fwd.argtypes = [sp] + [_vp] * 11 + [_vp, ctypes.c_size_t, _vp]
+        L.gdr_recurrent_step.argtypes = [sp] + [_vp] * 10 + [_vp]
+        L.gdr_gate_cumsum.argtypes = [ctypes.c_int] * 4 + [_vp, _vp, _vp]
+        L.gdr_status_string.argtypes = [ctypes.c_int]
+        L.gdr_status_string.restype = ctypes.c_char_p
+        L.gdr_abi_version.restype = ctypes.c_int
+        for name in ("gdr_chunk_fwd_workspace", "gdr_chunk_fwd", "gdr_recurrent_step",
+                     "gdr_gate_cumsum"):
+            getattr(L, name).restype = ctypes.c_int
+        _lib = L
+    return _lib
+
+
+def status_string(code):
+    return lib().gdr_status_string(int(code)).decode()
+
+
+def _ptr(t):
+    return None if t is None else _vp(t.data_ptr())
+
+
+def _stream(stream, device):
+    if stream is None:
+        stream = torch.cuda.current_stream(device)
+    return _vp(stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
+
+
+def _check(t, name, dtype, device, shape=None):
+    if t is None:
+        return
+    if not t.is_cuda or t.device != device:
+        raise ValueError("%s must be a CUDA tensor on %s" % (name, device))
+    if t.dtype != dtype:
+        raise ValueError("%s must be %s, got %s" % (name, dtype, t.dtype))
+    if not t.is_contiguous():
+        raise ValueError("%s must be contiguous" % name)
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError("%s has shape %s, expected %s" % (name, tuple(t.shape), tuple(shape)))
+
+
+def _infer_flags(channel_decay, b, w, lam):
+    """Variant flags implied by which gates the caller passed."""
+    flags = DECAY_CHANNEL if channel_decay else 0
+    if b is not None:
+        flags |= ERASE_CHANNEL
+    if w is not None:
+        flags |= WRITE_CHANNEL
+    if lam is not None:
+        flags |= QMIX
+    return flags
+
+
+def make_shape(B, T, H, dk, dv, dtype, flags, scale):
+    return Shape(B, T, H, dk, dv, GDR_BF16 if dtype == torch.bfloat16 else GDR_F32,
+                 flags, float(scale))
+
+
+def chunk_fwd_workspace_bytes(shape):
+    n = ctypes.c_size_t(0)
+    st = lib().gdr_chunk_fwd_workspace(ctypes.byref(shape), ctypes.byref(n))
+    if st:
+        raise GdrError(st, "gdr_chunk_fwd_workspace")
+    return n.value
+
+
+def chunk_fwd(q, k, v, g, beta=None, lam=None, b=None, w=None, h0=None, *, scale=None,
+              flags=None, output_final_state=True, o=None, hT=None, workspace=None,
+              stream=None):
+    """Chunkwise forward (``gdr_chunk_fwd``).
+
+    q, k: [B, T, H, d_k]; v: [B, T, H, d_v] (bf16 or fp32, one dtype);
+    g: [B, T, H] or [B, T, H, d_k] fp32 log-decay; beta / lam: [B, T, H] fp32;
+    b: [B, T, H, d_k]; w: [B, T, H, d_v]; h0: [B, H, d_k, d_v] fp32 or None.
+    ``flags`` defaults to what the given gates imply (channel g, b, w, lam);
+    ``scale`` to d_k^-1/2. Returns (o, hT) with hT None unless requested.
+    """
+    B, T, H, dk = q.shape
+    dv = v.shape[-1]
+    dev, dt = q.device, q.dtype
+    if dt not in (torch.bfloat16, torch.float32):
+        raise ValueError("q, k, v must be bf16 or fp32")
+    if flags is None:
+        flags = _infer_flags(g.dim() == 4, b, w, lam)
+    if scale is None:
+        scale = dk ** -0.5
+    _check(q, "q", dt, dev, (B, T, H, dk))
+    _check(k, "k", dt, dev, (B, T, H, dk))
+    _check(v, "v", dt, dev, (B, T, H, dv))
+    _check(g, "g", torch.float32, dev, (B, T, H, dk) if flags & DECAY_CHANNEL else (B, T, H))
+    _check(beta, "beta", torch.float32, dev, (B, T, H))
+    _check(lam, "lam", torch.float32, dev, (B, T, H))
+    _check(b, "b", dt, dev, (B, T, H, dk))
+    _check(w, "w", dt, dev, (B, T, H, dv))
+    _check(h0, "h0", torch.float32, dev, (B, H, dk, dv))
+    if o is None:
+        o = torch.empty(B, T, H, dv, dtype=dt, device=dev)
+    _check(o, "o", dt, dev, (B, T, H, dv))
+    if hT is None and output_final_state:
+        hT = torch.empty(B, H, dk, dv, dtype=torch.float32, device=dev)
+    _check(hT, "hT", torch.float32, dev, (B, H, dk, dv))
+    shape = make_shape(B, T, H, dk, dv, dt, flags, scale)
+    ws_bytes = chunk_fwd_workspace_bytes(shape)
+    if ws_bytes and workspace is None:
+        workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+    with torch.cuda.device(dev):
+        st = lib().gdr_chunk_fwd(ctypes.byref(shape), _ptr(q), _ptr(k), _ptr(v), _ptr(g),
+                                 _ptr(beta), _ptr(lam), _ptr(b), _ptr(w), _ptr(h0), _ptr(o),
+                                 _ptr(hT), _ptr(workspace),
+                                 ctypes.c_size_t(0 if workspace is None else workspace.numel()),
+                                 _stream(stream, dev))
+    if st:
+        raise GdrError(st, "gdr_chunk_fwd")
+    return o, hT
+
+
+def recurrent_step(q, k, v, g, state, beta=None, lam=None, b=None, w=None, *, scale=None,
+                   flags=None, o=None, stream=None):
+    """One decode step (``gdr_recurrent_step``); updates ``state`` in place.
+
+    q, k: [N, H, d_k] (or [N, 1, H, d_k]); v: [N, H, d_v]; g: [N, H] or
+    [N, H, d_k]; beta / lam: [N, H]; b: [N, H, d_k]; w: [N, H, d_v];
+    state: [N, H, d_k, d_v] fp32. Returns o [N, H, d_v].
+    """
+    N, H, dk, dv = state.shape
+    dev, dt = q.device, q.dtype
+    if flags is None:
+        flags = _infer_flags(g.numel() == N * H * dk, b, w, lam)
+    if scale is None:
+        scale = dk ** -0.5
+    for name, t, n in (("q", q, N * H * dk), ("k", k, N * H * dk), ("v", v, N * H * dv),
+                       ("b", b, N * H * dk), ("w", w, N * H * dv), ("beta", beta, N * H),
+                       ("lam", lam, N * H),
+                       ("g", g, N * H * dk if flags & DECAY_CHANNEL else N * H)):
+        if t is not None:
+            want = torch.float32 if name in ("beta", "lam", "g") else dt
+            _check(t, name, want, dev)
+            if t.numel() != n:
+                raise ValueError("%s has %d elements, expected %d" % (name, t.numel(), n))
+    _check(state, "state", torch.float32, dev)
+    if o is None:
+        o = torch.empty(N, H, dv, dtype=dt, device=dev)
+    _check(o, "o", dt, dev)
+    shape = make_shape(N, 1, H, dk, dv, dt, flags, scale)
+    with torch.cuda.device(dev):
+        st = lib().gdr_recurrent_step(ctypes.byref(shape), _ptr(q), _ptr(k), _ptr(v), _ptr(g),
+                                      _ptr(beta), _ptr(lam), _ptr(b), _ptr(w), _ptr(state),
+                                      _ptr(o), _stream(stream, dev))
+    if st:
+        raise GdrError(st, "gdr_recurrent_step")
+    return o
+
+
+def gate_cumsum(g, chunk=CHUNK, out=None, stream=None):
+    """Chunk-local inclusive cumsum of g ([B, T, H] or [B, T, H, d_k], fp32)."""
+    B, T = g.shape[0], g.shape[1]
+    X = g.numel() // max(B * T, 1)
+    _check(g, "g", torch.float32, g.device)
+    if out is None:
+        out = torch.empty_like(g)
+    _check(out, "out", torch.float32, g.device, tuple(g.shape))
+    with torch.cuda.device(g.device):
+        st = lib().gdr_gate_cumsum(B, T, X, chunk, _ptr(g), _ptr(out), _stream(stream, g.device))
+    if st:
+        raise GdrError(st, "gdr_gate_cumsum")
+    return out

@@ -1,0 +1,139 @@
+// The C ABI of the library (declared in include/gdr.h): argument checks and
+// kernel dispatch. Nothing here allocates memory or synchronises the stream.
+#include <stdint.h>
+
+#include <cmath>
+#include <limits>
+
+#include "gdr.h"
+#include "kernels.h"
+
+namespace {
+
+constexpr int kAbiVersion = 1;
+constexpr long long kMaxElems = std::numeric_limits<int>::max();
+
+bool aligned(const void* p, uintptr_t n) { return (reinterpret_cast<uintptr_t>(p) % n) == 0; }
+
+gdr_status check_shape(const gdr_shape* s, bool step) {
+  if (!s) return GDR_ERR_INVALID_ARG;
+  if (s->B < 1 || s->T < 1 || s->H < 1 || s->dk < 1 || s->dv < 1) return GDR_ERR_INVALID_ARG;
+  if (s->dtype != GDR_F32 && s->dtype != GDR_BF16) return GDR_ERR_INVALID_ARG;
+  if (s->flags & ~15u) return GDR_ERR_INVALID_ARG;
+  if (!std::isfinite(s->scale)) return GDR_ERR_INVALID_ARG;
+  if (step && s->T != 1) return GDR_ERR_INVALID_ARG;
+  if ((s->dk != 64 && s->dk != 128) || (s->dv != 64 && s->dv != 128)) return GDR_ERR_UNSUPPORTED;
+  const long long d = s->dk > s->dv ? s->dk : s->dv;
+  const long long elems = static_cast<long long>(s->B) * s->T * s->H * d;
+  const long long state = static_cast<long long>(s->B) * s->H * s->dk * s->dv;
+  if (elems > kMaxElems || state > kMaxElems) return GDR_ERR_UNSUPPORTED;
+  if (s->H > 65535 || s->B > 65535) return GDR_ERR_UNSUPPORTED;  // grid y / z extents
+  return GDR_OK;
+}
+
+// Pointer rules shared by the chunked forward and the recurrent step.
+gdr_status check_gates(const gdr_shape* s, const void* q, const void* k, const void* v,
+                       const float* g, const float* beta, const float* lam, const void* b,
+                       const void* w, const void* o) {
+  const unsigned f = s->flags;
+  if (!q || !k || !v || !g || !o) return GDR_ERR_INVALID_ARG;
+  const bool need_beta = !((f & GDR_ERASE_CHANNEL) && (f & GDR_WRITE_CHANNEL));
+  if (need_beta && !beta) return GDR_ERR_INVALID_ARG;
+  if ((f & GDR_QMIX) && !lam) return GDR_ERR_INVALID_ARG;
+  if ((f & GDR_ERASE_CHANNEL) && !b) return GDR_ERR_INVALID_ARG;
+  if ((f & GDR_WRITE_CHANNEL) && !w) return GDR_ERR_INVALID_ARG;
+  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16))
+    return GDR_ERR_INVALID_ARG;
+  if (!aligned(g, 4) || (beta && !aligned(beta, 4)) || (lam && !aligned(lam, 4)))
+    return GDR_ERR_INVALID_ARG;
+  if ((f & GDR_ERASE_CHANNEL) && !aligned(b, 16)) return GDR_ERR_INVALID_ARG;
+  if ((f & GDR_WRITE_CHANNEL) && !aligned(w, 16)) return GDR_ERR_INVALID_ARG;
+  return GDR_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int gdr_abi_version(void) { return kAbiVersion; }
+
+const char* gdr_status_string(gdr_status status) {
+  switch (status) {
+    case GDR_OK: return "GDR_OK";
+    case GDR_ERR_INVALID_ARG: return "GDR_ERR_INVALID_ARG: null or misaligned pointer, bad size or flag";
+    case GDR_ERR_UNSUPPORTED: return "GDR_ERR_UNSUPPORTED: request outside the supported set";
+    case GDR_ERR_CUDA: return "GDR_ERR_CUDA: the CUDA runtime reported an error";
+    case GDR_ERR_WORKSPACE: return "GDR_ERR_WORKSPACE: workspace missing or too small";
+    case GDR_ERR_TIMEOUT: return "GDR_ERR_TIMEOUT: a bounded device-side wait gave up";
+  }
+  return "unknown gdr_status";
+}
+
+gdr_status gdr_chunk_fwd_workspace(const gdr_shape* shape, size_t* bytes) {
+  if (!bytes) return GDR_ERR_INVALID_ARG;
+  const gdr_status st = check_shape(shape, false);
+  if (st != GDR_OK) return st;
+  *bytes = 0;  // the fused kernel keeps every intermediate on chip
+  return GDR_OK;
+}
+
+gdr_status gdr_chunk_fwd(const gdr_shape* shape, const void* q, const void* k, const void* v,
+                         const float* g, const float* beta, const float* lam, const void* b,
+                         const void* w, const float* h0, void* o, float* hT, void* workspace,
+                         size_t ws_bytes, gdr_stream_t stream) {
+  gdr_status st = check_shape(shape, false);
+  if (st != GDR_OK) return st;
+  st = check_gates(shape, q, k, v, g, beta, lam, b, w, o);
+  if (st != GDR_OK) return st;
+  if ((h0 && !aligned(h0, 16)) || (hT && !aligned(hT, 16))) return GDR_ERR_INVALID_ARG;
+  size_t need = 0;
+  gdr_chunk_fwd_workspace(shape, &need);
+  if (need > 0 && (!workspace || ws_bytes < need)) return GDR_ERR_WORKSPACE;
+  (void)workspace;
+
+  const bool f32 = shape->dtype == GDR_F32;
+  gdr::ChunkArgs a;
+  a.q = q; a.k = k; a.v = v; a.g = g; a.beta = beta; a.lam = lam; a.b = b; a.w = w;
+  a.h0 = h0; a.o = o; a.hT = hT;
+  a.B = shape->B; a.T = shape->T; a.H = shape->H; a.dv = shape->dv;
+  a.flags = shape->flags; a.scale = shape->scale;
+  const int nv = gdr::chunk_fwd_slice_width(shape->B, shape->H, shape->dk, shape->dv, f32);
+  const cudaError_t err =
+      gdr::launch_chunk_fwd(a, shape->dk, nv, f32, reinterpret_cast<cudaStream_t>(stream));
+  return err == cudaSuccess ? GDR_OK : GDR_ERR_CUDA;
+}
+
+gdr_status gdr_recurrent_step(const gdr_shape* shape, const void* q, const void* k,
+                              const void* v, const float* g, const float* beta,
+                              const float* lam, const void* b, const void* w, float* state,
+                              void* o, gdr_stream_t stream) {
+  gdr_status st = check_shape(shape, true);
+  if (st != GDR_OK) return st;
+  st = check_gates(shape, q, k, v, g, beta, lam, b, w, o);
+  if (st != GDR_OK) return st;
+  if (!state || !aligned(state, 16)) return GDR_ERR_INVALID_ARG;
+  const long long blocks = static_cast<long long>(shape->B) * shape->H;
+  if (blocks > 2147483647LL) return GDR_ERR_UNSUPPORTED;
+  gdr::StepArgs a;
+  a.q = q; a.k = k; a.v = v; a.g = g; a.beta = beta; a.lam = lam; a.b = b; a.w = w;
+  a.state = state; a.o = o; a.N = shape->B; a.H = shape->H;
+  a.flags = shape->flags; a.scale = shape->scale;
+  const cudaError_t err = gdr::launch_recurrent_step(a, shape->dk, shape->dv,
+                                                     shape->dtype == GDR_F32,
+                                                     reinterpret_cast<cudaStream_t>(stream));
+  return err == cudaSuccess ? GDR_OK : GDR_ERR_CUDA;
+}
+
+gdr_status gdr_gate_cumsum(int B, int T, int X, int chunk, const float* g, float* G,
+                           gdr_stream_t stream) {
+  if (B < 1 || T < 1 || X < 1 || !g || !G) return GDR_ERR_INVALID_ARG;
+  if (!aligned(g, 4) || !aligned(G, 4)) return GDR_ERR_INVALID_ARG;
+  if (chunk != gdr::kChunkLen) return GDR_ERR_UNSUPPORTED;
+  if (static_cast<long long>(B) * T * X > kMaxElems * 2LL) return GDR_ERR_UNSUPPORTED;
+  if (B > 65535) return GDR_ERR_UNSUPPORTED;
+  const cudaError_t err =
+      gdr::launch_gate_cumsum(g, G, B, T, X, reinterpret_cast<cudaStream_t>(stream));
+  return err == cudaSuccess ? GDR_OK : GDR_ERR_CUDA;
+}
+
+}  // extern "C"

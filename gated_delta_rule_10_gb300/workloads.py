@@ -67,15 +67,18 @@ def _l2norm(x):
 
 def make_inputs(variant, B, T, H, dk, dv, dtype=torch.bfloat16, seed=0,
                 q_prescaled=False, h0_std=None, device="cpu"):
-    """Seeded inputs of one variant in the [B, T, H, d] layout.
+    """Seeded inputs of one variant (a name or a flag bitmask), [B, T, H, d] layout.
 
     Returns a dict with q, k, v (dtype), g (fp32, [B,T,H] or [B,T,H,d_k]),
     beta / lam (fp32 [B,T,H] or None), b / w (dtype or None), h0 (fp32 or
     None), scale (float), flags (int) and variant.
     """
-    if variant not in VARIANT_FLAGS:
+    if isinstance(variant, int):
+        flags = variant                    # any flag combination, same recipe per gate
+    elif variant in VARIANT_FLAGS:
+        flags = VARIANT_FLAGS[variant]
+    else:
         raise ValueError("unknown variant %r" % variant)
-    flags = VARIANT_FLAGS[variant]
     gen = torch.Generator().manual_seed(int(seed))
 
     def normal(*shape, mean=0.0, std=1.0):
@@ -101,6 +104,7 @@ def make_inputs(variant, B, T, H, dk, dv, dtype=torch.bfloat16, seed=0,
     if flags & QMIX:
         lam_h = torch.rand(H, generator=gen, dtype=torch.float32)
         lam = lam_h.view(1, 1, H).expand(B, T, H).contiguous()
+    if flags & QMIX and beta is not None:
         kf, qf = k.float(), q.float()
         a = (kf * (kf + lam[..., None] * qf)).sum(-1)
         cap = torch.where(a > 0, torch.clamp(1.9 / a.clamp_min(1e-30), max=1.0),

@@ -1,0 +1,173 @@
+/*
+ * gdr.h -- C interface of the GB300 (sm_103a) gated delta rule library.
+ *
+ * The library computes the forward pass of the gated delta rule, the
+ * recurrence (state S in R^{d_k x d_v}, one per batch row and head)
+ *
+ *     S~_t = Diag(alpha_t) S_{t-1},  alpha_t = exp(g_t)
+ *     S_t  = S~_t + k_t (z_t - S~_t^T e_t)^T
+ *     o_t  = S_t^T (scale * q_t)
+ *
+ * (Gated DeltaNet-2 notes, key design 1, which names e_t and z_t; state
+ * orientation as in LLMs from scratch ch. 11, section 11.1) through the
+ * chunkwise WY/UT algorithm with chunks of C = 64 tokens (Gated DeltaNet-2
+ * notes, key design 2), plus a single-token recurrent step for decoding.
+ * The variant is chosen by flags:
+ *
+ *   flags                                   e_t                z_t
+ *   0                 Gated DeltaNet         beta_t k_t         beta_t v_t
+ *   GDR_DECAY_CHANNEL KDA                    beta_t k_t         beta_t v_t
+ *   GDR_QMIX          Q-Delta                beta_t (k_t + lam_t q_t)  beta_t v_t
+ *   DECAY|ERASE|WRITE Gated DeltaNet-2       b_t (.) k_t        w_t (.) v_t
+ *
+ * Flags combine independently: the erase input is x_t = k_t + lam_t q_t under
+ * GDR_QMIX and k_t otherwise; e_t = b_t (.) x_t under GDR_ERASE_CHANNEL and
+ * beta_t x_t otherwise; z_t = w_t (.) v_t under GDR_WRITE_CHANNEL and
+ * beta_t v_t otherwise. Gated DeltaNet is the recurrence of LLMs from scratch
+ * ch. 11, section 11.2; KDA that of "You could have come up with Kimi Delta
+ * Attention", section 4; Q-Delta the rewritten rule of the Q-Delta notes, key
+ * design 3.
+ *
+ * Conventions common to every call:
+ *  - Layouts are dense and row-major. Per-token tensors are [B, T, H, d] with
+ *    d fastest; scalar per-token gates are [B, T, H]; states are
+ *    [B, H, d_k, d_v] with d_v fastest (S's rows are key channels).
+ *  - q, k, v, o, b and w use the call's dtype (fp32 or bf16); g, beta, lam and
+ *    the states are always fp32. g is the natural-log decay (alpha = exp(g),
+ *    g <= 0 in the pages' usage; any finite value is accepted).
+ *  - Ownership: the caller owns and allocates every buffer, workspace
+ *    included. The library never allocates or frees device memory and keeps
+ *    no per-call state between calls.
+ *  - Execution: work is enqueued on `stream` (a cudaStream_t; NULL is the
+ *    legacy default stream) and the call returns without synchronising.
+ *    Input buffers must stay valid until the work completes.
+ *  - Errors: argument errors (null or misaligned pointers, bad sizes or
+ *    flags, too small a workspace) are reported synchronously, before
+ *    anything is enqueued, and the outputs are left untouched. A launch
+ *    failure reported by the CUDA runtime returns GDR_ERR_CUDA. Non-finite
+ *    inputs propagate to the outputs; they are not detected.
+ *  - Supported sizes: d_k, d_v in {64, 128}; any B, H >= 1 and T >= 1 with
+ *    B*T*H*max(d_k, d_v) < 2^31 elements per tensor; a ragged last chunk is
+ *    handled. 16-byte alignment is required for q, k, v, o, b, w, h0, hT and
+ *    state; 4-byte alignment for g, beta and lam.
+ *  - Decay range of the chunked path with per-channel gates
+ *    (GDR_DECAY_CHANNEL): within one 64-token chunk the summed log-decay of
+ *    any key channel must stay above -140 (beyond that the decay factors of
+ *    the chunk algebra approach the bottom of the fp32 normal range and lose
+ *    precision). Scalar gates and the recurrent step have no such limit.
+ */
+#ifndef GDR_H_
+#define GDR_H_
+
+#include <stddef.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same object as cudaStream_t / CUstream; NULL selects the default stream. */
+typedef struct CUstream_st* gdr_stream_t;
+
+typedef enum {
+  GDR_OK = 0,
+  GDR_ERR_INVALID_ARG = 1, /* null/misaligned pointer, bad size or flag */
+  GDR_ERR_UNSUPPORTED = 2, /* valid request outside the supported set  */
+  GDR_ERR_CUDA = 3,        /* the CUDA runtime reported an error        */
+  GDR_ERR_WORKSPACE = 4,   /* workspace missing or smaller than needed  */
+  GDR_ERR_TIMEOUT = 5      /* a bounded device-side wait gave up        */
+} gdr_status;
+
+typedef enum { GDR_F32 = 0, GDR_BF16 = 1 } gdr_dtype;
+
+enum {
+  GDR_DECAY_CHANNEL = 1, /* g is [B,T,H,d_k] (per key channel), else [B,T,H] */
+  GDR_ERASE_CHANNEL = 2, /* erase direction b (.) x, b is [B,T,H,d_k]        */
+  GDR_WRITE_CHANNEL = 4, /* write vector w (.) v, w is [B,T,H,d_v]           */
+  GDR_QMIX = 8           /* erase input x = k + lam q, lam is [B,T,H]         */
+};
+
+typedef struct {
+  int B, T, H;      /* batch, tokens, heads                                */
+  int dk, dv;       /* key and value widths (64 or 128)                    */
+  int dtype;        /* gdr_dtype of q, k, v, o, b, w                       */
+  unsigned flags;   /* GDR_DECAY_CHANNEL | GDR_ERASE_CHANNEL | ...         */
+  float scale;      /* read-out scale on q (d_k^-1/2 in the KDA derivation) */
+} gdr_shape;
+
+/* Device workspace bytes gdr_chunk_fwd needs for `shape` (may be 0).
+ * Returns GDR_ERR_INVALID_ARG / GDR_ERR_UNSUPPORTED for a bad shape. */
+gdr_status gdr_chunk_fwd_workspace(const gdr_shape* shape, size_t* bytes);
+
+/*
+ * Chunkwise-parallel forward (Gated DeltaNet-2 notes, key design 2; the
+ * same WY/UT machinery serves Q-Delta, Q-Delta notes key design 3). For each
+ * (batch, head) and each chunk of C = 64 tokens it forms the in-chunk
+ * cumulative decay gamma, T = tril(E_bar K_bar^T, -1), A = (I + T)^{-1} by
+ * forward substitution, Y = A E_bar and U = A Z, and passes the state across
+ * chunks with S_{n+1} = Diag(gamma_C) S_n + K_tail^T (U - Y S_n), reading out
+ * O_n = Q_gamma S_n + A_qk (U - Y S_n). The result equals the token
+ * recurrence above up to rounding.
+ *
+ *   q, k   [B,T,H,d_k] dtype      v, o  [B,T,H,d_v] dtype
+ *   g      [B,T,H] fp32, or [B,T,H,d_k] under GDR_DECAY_CHANNEL
+ *   beta   [B,T,H] fp32; required unless both ERASE and WRITE are set
+ *          (then ignored)
+ *   lam    [B,T,H] fp32; required under GDR_QMIX, ignored otherwise
+ *   b      [B,T,H,d_k] dtype; required under GDR_ERASE_CHANNEL, else ignored
+ *   w      [B,T,H,d_v] dtype; required under GDR_WRITE_CHANNEL, else ignored
+ *   h0     [B,H,d_k,d_v] fp32 initial state, or NULL for the zero state
+ *   hT     [B,H,d_k,d_v] fp32 final state (written), or NULL
+ *   workspace, ws_bytes: device memory of at least
+ *          gdr_chunk_fwd_workspace() bytes (NULL allowed when that is 0)
+ *
+ * h0 and hT may be the same buffer (streaming: the state read for a (batch,
+ * head) is consumed before that (batch, head)'s final state is written); no
+ * other output may overlap an input. o is written in dtype, rounded to
+ * nearest even for bf16; accumulation and the state are fp32.
+ */
+gdr_status gdr_chunk_fwd(const gdr_shape* shape, const void* q, const void* k,
+                         const void* v, const float* g, const float* beta,
+                         const float* lam, const void* b, const void* w,
+                         const float* h0, void* o, float* hT, void* workspace,
+                         size_t ws_bytes, gdr_stream_t stream);
+
+/*
+ * One recurrent step for decoding (LLMs from scratch ch. 11, section 11.2,
+ * in the general form above; section 11.3 for the streaming protocol: the
+ * prefill's final state is the first step's state). shape->T must be 1 and
+ * shape->B is the number of sequences N; tensors are the [N,1,H,d] (equally
+ * [N,H,d]) slices of the layouts above and the gates likewise.
+ *
+ *   state  [N,H,d_k,d_v] fp32, read as S_{t-1} and overwritten with S_t
+ *   o      [N,H,d_v] dtype, o_t = S_t^T (scale q_t)
+ *
+ * Each (sequence, head) reads and writes its state once.
+ */
+gdr_status gdr_recurrent_step(const gdr_shape* shape, const void* q,
+                              const void* k, const void* v, const float* g,
+                              const float* beta, const float* lam,
+                              const void* b, const void* w, float* state,
+                              void* o, gdr_stream_t stream);
+
+/*
+ * Chunk-local cumulative log-decay (Gated DeltaNet-2 notes, key design 2:
+ * gamma_r = exp(sum_{i<=r} g_i) restarts every chunk; the training-strategy
+ * paragraph keeps this sum in fp32). G[b, t, x] = sum of g[b, i, x] over the
+ * tokens i <= t of t's chunk (chunks of `chunk` tokens from t = 0), for
+ * g, G of shape [B, T, X] fp32 with X = H (scalar gates) or H * d_k
+ * (channel gates). chunk must be 64. G may alias g.
+ */
+gdr_status gdr_gate_cumsum(int B, int T, int X, int chunk, const float* g,
+                           float* G, gdr_stream_t stream);
+
+/* Static, human-readable name of a status code. */
+const char* gdr_status_string(gdr_status status);
+
+/* Interface version (incremented on any signature change). */
+int gdr_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GDR_H_ */

@@ -1,0 +1,156 @@
+"""The C-ABI library without a GPU: it loads, exports what include/gdr.h
+declares, and rejects bad arguments before touching the device.
+
+Only calls whose arguments fail validation are made here; they return before
+any CUDA runtime call, so no kernel is launched.
+"""
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+import torch
+
+import gated_delta_rule_10_gb300 as gdr
+from gated_delta_rule_10_gb300 import _binding
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "gdr.h")
+
+
+@pytest.fixture(scope="module")
+def L():
+    from gated_delta_rule_10_gb300 import build
+    build.build()
+    return gdr.lib()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(gdr_[a-z_0-9]+)\s*\(", text)))
+
+
+def test_header_declares_the_entry_points():
+    names = declared_functions()
+    for n in ("gdr_chunk_fwd", "gdr_chunk_fwd_workspace", "gdr_recurrent_step",
+              "gdr_gate_cumsum", "gdr_status_string", "gdr_abi_version"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(L):
+    out = subprocess.run(["nm", "-D", "--defined-only", _binding.LIB_PATH],
+                         capture_output=True, text=True, check=True).stdout
+    exported = set(re.findall(r"\sT\s(\w+)$", out, flags=re.M))
+    for name in declared_functions():
+        assert name in exported, name
+        assert getattr(L, name) is not None
+
+
+def test_header_compiles_as_c_and_cpp(tmp_path):
+    src = tmp_path / "use.c"
+    src.write_text('#include "gdr.h"\nint f(void){ gdr_shape s; (void)s; return GDR_OK; }\n')
+    for compiler in ("gcc", "g++"):
+        subprocess.run([compiler, "-fsyntax-only", "-Wall", "-Werror", "-I",
+                        os.path.join(ROOT, "include"), "-x", "c" if compiler == "gcc" else "c++",
+                        str(src)], check=True)
+
+
+def test_version_and_status_strings(L):
+    assert L.gdr_abi_version() >= 1
+    for code, name in _binding.STATUS.items():
+        assert gdr.status_string(code).startswith(name)
+    assert "unknown" in gdr.status_string(99)
+
+
+def _shape(**kw):
+    d = dict(B=1, T=64, H=1, dk=64, dv=64, dtype=_binding.GDR_BF16, flags=0, scale=0.125)
+    d.update(kw)
+    return _binding.Shape(**d)
+
+
+def test_workspace_query(L):
+    n = ctypes.c_size_t(123)
+    assert L.gdr_chunk_fwd_workspace(ctypes.byref(_shape()), ctypes.byref(n)) == 0
+    assert n.value == 0
+    assert L.gdr_chunk_fwd_workspace(None, ctypes.byref(n)) == 1
+    assert L.gdr_chunk_fwd_workspace(ctypes.byref(_shape()), None) == 1
+    assert L.gdr_chunk_fwd_workspace(ctypes.byref(_shape(dk=96)), ctypes.byref(n)) == 2
+    assert L.gdr_chunk_fwd_workspace(ctypes.byref(_shape(T=0)), ctypes.byref(n)) == 1
+    assert L.gdr_chunk_fwd_workspace(ctypes.byref(_shape(flags=16)), ctypes.byref(n)) == 1
+    assert L.gdr_chunk_fwd_workspace(ctypes.byref(_shape(dtype=7)), ctypes.byref(n)) == 1
+    assert L.gdr_chunk_fwd_workspace(ctypes.byref(_shape(scale=float("nan"))),
+                                     ctypes.byref(n)) == 1
+    big = _shape(B=65536, T=65536, H=64, dk=128, dv=128)
+    assert L.gdr_chunk_fwd_workspace(ctypes.byref(big), ctypes.byref(n)) == 2
+
+
+FAKE = 0x10000  # a 64 KiB-aligned address that is never dereferenced
+
+
+def _call_chunk(L, shape, **ptrs):
+    p = dict(q=FAKE, k=FAKE, v=FAKE, g=FAKE, beta=FAKE, lam=None, b=None, w=None, h0=None,
+             o=FAKE, hT=None, ws=None)
+    p.update(ptrs)
+    vp = ctypes.c_void_p
+    sp = None if shape is None else ctypes.byref(shape)
+    return L.gdr_chunk_fwd(sp, *(vp(p[n]) for n in
+                                                 ("q", "k", "v", "g", "beta", "lam", "b", "w",
+                                                  "h0", "o", "hT", "ws")),
+                           ctypes.c_size_t(0), None)
+
+
+def test_chunk_fwd_rejects_bad_arguments_synchronously(L):
+    s = _shape()
+    assert _call_chunk(L, s, q=None) == 1
+    assert _call_chunk(L, s, o=None) == 1
+    assert _call_chunk(L, s, g=None) == 1
+    assert _call_chunk(L, s, beta=None) == 1                       # beta needed for GDN
+    assert _call_chunk(L, _shape(flags=gdr.QMIX)) == 1              # lam missing
+    assert _call_chunk(L, _shape(flags=gdr.ERASE_CHANNEL)) == 1     # b missing
+    assert _call_chunk(L, _shape(flags=gdr.WRITE_CHANNEL)) == 1     # w missing
+    assert _call_chunk(L, s, q=FAKE + 8) == 1                       # 16-byte alignment
+    assert _call_chunk(L, s, h0=FAKE + 4) == 1
+    assert _call_chunk(L, s, g=FAKE + 2) == 1
+    assert _call_chunk(L, _shape(dk=32)) == 2
+    assert _call_chunk(L, _shape(dv=256)) == 2
+    assert _call_chunk(L, _shape(H=0)) == 1
+    assert _call_chunk(L, None) == 1
+
+
+def test_recurrent_step_rejects_bad_arguments(L):
+    vp = ctypes.c_void_p
+    s = _shape(T=2)
+    args = [vp(FAKE)] * 5 + [None, None, None, vp(FAKE), vp(FAKE), None]
+    assert L.gdr_recurrent_step(ctypes.byref(s), *args) == 1        # T must be 1
+    s = _shape(T=1)
+    bad_state = [vp(FAKE)] * 5 + [None, None, None, None, vp(FAKE), None]
+    assert L.gdr_recurrent_step(ctypes.byref(s), *bad_state) == 1
+    s = _shape(T=1, dk=80)
+    assert L.gdr_recurrent_step(ctypes.byref(s), *args) == 2
+
+
+def test_gate_cumsum_rejects_bad_arguments(L):
+    vp = ctypes.c_void_p
+    assert L.gdr_gate_cumsum(1, 64, 4, 32, vp(FAKE), vp(FAKE), None) == 2   # chunk must be 64
+    assert L.gdr_gate_cumsum(0, 64, 4, 64, vp(FAKE), vp(FAKE), None) == 1
+    assert L.gdr_gate_cumsum(1, 64, 4, 64, None, vp(FAKE), None) == 1
+    assert L.gdr_gate_cumsum(1, 64, 4, 64, vp(FAKE + 1), vp(FAKE), None) == 1
+
+
+def test_binding_refuses_cpu_tensors(L):
+    x = torch.zeros(1, 64, 1, 64)
+    with pytest.raises(ValueError):
+        gdr.chunk_fwd(x, x, x, torch.zeros(1, 64, 1), torch.zeros(1, 64, 1))
+
+
+def test_product_code_does_not_touch_the_oracle():
+    pkg = os.path.join(ROOT, "gated_delta_rule_10_gb300")
+    for dirpath, _, files in os.walk(pkg):
+        for f in files:
+            if f.endswith((".py", ".cu", ".cuh", ".h", ".cpp")):
+                text = open(os.path.join(dirpath, f)).read()
+                assert not re.search(r"\boracle\b\s*(import|\.)|from\s+oracle|import\s+oracle",
+                                     text), f
+                assert "gdr_oracle" not in text, f

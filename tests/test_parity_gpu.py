@@ -1,0 +1,256 @@
+"""GPU parity: the CUDA path (through the C ABI) against the float64 oracle.
+
+Bar (element by element on the same seeded inputs): max|d| / max|ref| <= 1e-4
+for fp32 inputs and <= 2e-2 for bf16 inputs, for both o and the final state.
+Small cases compare every output; the full-size workloads run in the launch
+configuration the benchmark times and compare sampled (batch, head)
+sequences, which the oracle computes one by one.
+"""
+import numpy as np
+import pytest
+import torch
+
+import gated_delta_rule_10_gb300 as gdr
+from gated_delta_rule_10_gb300 import workloads as wl
+from oracle import chunked as och
+from tests.gdr_testutil import TOL, f64, gpu_forward, oracle_forward, rel_err, select, to_dev
+
+pytestmark = pytest.mark.gpu
+
+VARIANTS = ["gdn", "qdelta", "kda", "gdn2"]
+DTYPES = [torch.float32, torch.bfloat16]
+
+
+def check(x, h0_std=None, tol=None, **kw):
+    o, hT = gpu_forward(x, **kw)
+    torch.cuda.synchronize()
+    ro, rh = oracle_forward(x)
+    tol = tol or TOL[x["q"].dtype]
+    eo, eh = rel_err(o.float().cpu(), ro), rel_err(hT.cpu(), rh)
+    assert eo <= tol and eh <= tol, (eo, eh)
+    return eo, eh
+
+
+@pytest.mark.parametrize("dtype", DTYPES, ids=["f32", "bf16"])
+@pytest.mark.parametrize("dk,dv", [(64, 64), (128, 128), (64, 128), (128, 64)])
+@pytest.mark.parametrize("T", [1, 63, 64, 65, 130])
+@pytest.mark.parametrize("variant", VARIANTS)
+def test_variants_small_shapes(variant, T, dk, dv, dtype):
+    x = wl.make_inputs(variant, 2, T, 3, dk, dv, dtype, seed=T + dk + 7 * dv, h0_std=0.05)
+    check(x)
+
+
+@pytest.mark.parametrize("dtype", DTYPES, ids=["f32", "bf16"])
+@pytest.mark.parametrize("flags", range(16))
+def test_every_flag_combination(flags, dtype):
+    x = wl.make_inputs(flags, 1, 130, 2, 128, 64, dtype, seed=100 + flags, h0_std=0.05)
+    check(x)
+
+
+def test_zero_initial_state_and_no_final_state():
+    x = wl.make_inputs("kda", 1, 200, 2, 128, 128, torch.bfloat16, seed=5)
+    o, hT = gpu_forward(x, output_final_state=False)
+    assert hT is None
+    ro, _ = oracle_forward(x)
+    assert rel_err(o.float().cpu(), ro) <= TOL[torch.bfloat16]
+
+
+@pytest.mark.parametrize("cfg", [1, 2, 3, 4, 5])
+def test_workload_recipes_reduced_length(cfg):
+    """Each named workload's recipe at a length the oracle finishes in seconds."""
+    c = wl.CONFIGS[cfg]
+    x = wl.config_inputs(cfg, T=min(c["T"], 320), B=min(c["B"], 2), H=min(c["H"], 4))
+    check(x)
+
+
+def test_config1_full_size():
+    check(wl.config_inputs(1))
+
+
+@pytest.mark.parametrize("cfg", [2, 3, 4, 5])
+def test_workload_full_size_sampled(cfg):
+    """Full size, the benchmark's launch configuration; two sequences checked."""
+    x = wl.config_inputs(cfg)
+    o, hT = gpu_forward(x)
+    torch.cuda.synchronize()
+    B, H = wl.CONFIGS[cfg]["B"], wl.CONFIGS[cfg]["H"]
+    picks = [(0, 0), (B - 1, H - 1)]
+    for b, h in picks:
+        xs = select(x, batches=[b], heads=[h])
+        ro, rh = oracle_forward(xs)
+        eo = rel_err(o[b:b + 1, :, h:h + 1].float().cpu(), ro)
+        eh = rel_err(hT[b:b + 1, h:h + 1].cpu(), rh)
+        assert eo <= TOL[torch.bfloat16] and eh <= TOL[torch.bfloat16], (cfg, b, h, eo, eh)
+    assert torch.isfinite(o).all() and torch.isfinite(hT).all()
+
+
+def test_scalar_decay_far_below_channel_limit():
+    # scalar gates have no in-chunk range limit: sum over a chunk ~ -320
+    x = wl.make_inputs("gdn", 1, 192, 2, 64, 64, torch.float32, seed=3, h0_std=0.1)
+    x["g"] = torch.full_like(x["g"], -5.0)
+    check(x)
+
+
+def test_channel_decay_near_documented_limit():
+    x = wl.make_inputs("kda", 1, 128, 2, 128, 128, torch.float32, seed=4, h0_std=0.1)
+    x["g"] = torch.full_like(x["g"], -2.15)    # -137.6 over a full chunk
+    x["g"][..., ::2] = -0.01
+    check(x)
+
+
+def test_unnormalised_keys_and_extended_erase_range():
+    # b in [0, 2] (the extended erase range of the Gated DeltaNet-2 ablations)
+    x = wl.make_inputs("gdn2", 1, 130, 2, 64, 64, torch.float32, seed=9, h0_std=0.1)
+    x["b"] = 2.0 * x["b"]
+    check(x)
+
+
+def test_streaming_split_prefill_equals_whole():
+    x = wl.make_inputs("qdelta", 2, 300, 3, 128, 128, torch.float32, seed=21, h0_std=0.05)
+    o_full, h_full = gpu_forward(x)
+    cut = 100   # not a chunk boundary
+    p1 = {n: (t[:, :cut].contiguous() if torch.is_tensor(t) and n in
+              ("q", "k", "v", "g", "beta", "lam", "b", "w") else t) for n, t in x.items()}
+    p2 = {n: (t[:, cut:].contiguous() if torch.is_tensor(t) and n in
+              ("q", "k", "v", "g", "beta", "lam", "b", "w") else t) for n, t in x.items()}
+    o1, h1 = gpu_forward(p1)
+    p2["h0"] = h1.cpu()
+    o2, h2 = gpu_forward(p2)
+    torch.cuda.synchronize()
+    o_split = torch.cat([o1, o2], dim=1)
+    assert rel_err(o_split.cpu(), o_full.cpu().numpy()) <= 1e-4
+    assert rel_err(h2.cpu(), h_full.cpu().numpy()) <= 1e-4
+
+
+def test_h0_and_hT_may_alias():
+    x = wl.make_inputs("gdn", 2, 130, 2, 64, 128, torch.bfloat16, seed=31, h0_std=0.05)
+    d = to_dev(x)
+    state = d["h0"].clone()
+    o, _ = gdr.chunk_fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], h0=state, hT=state,
+                         scale=x["scale"], flags=x["flags"])
+    torch.cuda.synchronize()
+    ro, rh = oracle_forward(x)
+    assert rel_err(o.float().cpu(), ro) <= 2e-2
+    assert rel_err(state.cpu(), rh) <= 2e-2
+
+
+def test_bitwise_deterministic():
+    x = wl.make_inputs("gdn2", 1, 500, 4, 128, 128, torch.bfloat16, seed=41, h0_std=0.02)
+    o1, h1 = gpu_forward(x)
+    o2, h2 = gpu_forward(x)
+    torch.cuda.synchronize()
+    assert torch.equal(o1, o2) and torch.equal(h1, h2)
+
+
+def test_outputs_only_where_expected():
+    # the kernel writes o only for the given tokens: a sentinel around it survives
+    x = wl.make_inputs("gdn", 1, 70, 2, 64, 64, torch.bfloat16, seed=51)
+    d = to_dev(x)
+    buf = torch.full((2 * 70 * 2 * 64,), 7.0, dtype=torch.bfloat16, device="cuda")
+    o = buf[:70 * 2 * 64].view(1, 70, 2, 64)
+    gdr.chunk_fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], scale=x["scale"], o=o,
+                  output_final_state=False)
+    torch.cuda.synchronize()
+    assert torch.all(buf[70 * 2 * 64:] == 7.0)
+
+
+# ---------------------------------------------------------------- decode step
+def _step_inputs(variant, N, H, dk, dv, dtype, seed):
+    y = wl.make_inputs(variant, N, 1, H, dk, dv, dtype, seed=seed)
+    return y
+
+
+def _gpu_step(y, state):
+    d = to_dev(y)
+    sq = lambda t: None if t is None else t[:, 0].contiguous()
+    return gdr.recurrent_step(sq(d["q"]), sq(d["k"]), sq(d["v"]), sq(d["g"]), state,
+                              beta=sq(d["beta"]), lam=sq(d["lam"]), b=sq(d["b"]),
+                              w=sq(d["w"]), scale=y["scale"], flags=y["flags"])
+
+
+@pytest.mark.parametrize("dtype", DTYPES, ids=["f32", "bf16"])
+@pytest.mark.parametrize("dk,dv", [(64, 64), (128, 128), (64, 128), (128, 64)])
+@pytest.mark.parametrize("flags", range(16))
+def test_recurrent_step_every_variant(flags, dk, dv, dtype):
+    N, H, steps = 3, 2, 3
+    gen = torch.Generator().manual_seed(flags)
+    h0 = torch.randn(N, H, dk, dv, generator=gen) * 0.05
+    state = h0.cuda()
+    ys = [_step_inputs(flags, N, H, dk, dv, dtype, seed=1000 * flags + s) for s in range(steps)]
+    outs = [_gpu_step(y, state) for y in ys]
+    torch.cuda.synchronize()
+    cat = {n: (torch.cat([y[n] for y in ys], dim=1) if ys[0][n] is not None else None)
+           for n in ("q", "k", "v", "g", "beta", "lam", "b", "w")}
+    cat.update(h0=h0, scale=ys[0]["scale"], flags=flags)
+    ro, rh = oracle_forward(cat)
+    got = torch.stack([o.float().cpu() for o in outs], dim=1)
+    tol = TOL[dtype]
+    assert rel_err(got, ro) <= tol and rel_err(state.cpu(), rh) <= tol
+
+
+def test_decode_workload_launch_configuration_sampled():
+    """The Gated DeltaNet-2 decode workload's launch (N=256, H=32, d=128)."""
+    c = wl.CONFIGS[5]
+    N, H, d = c["decode"]["N"], c["H"], c["dk"]
+    gen = torch.Generator().manual_seed(77)
+    h0 = torch.randn(N, H, d, d, generator=gen) * c["decode"]["h_std"]
+    state = h0.cuda()
+    ys = [_step_inputs("gdn2", N, H, d, d, torch.bfloat16, seed=500 + s) for s in range(4)]
+    outs = [_gpu_step(y, state) for y in ys]
+    torch.cuda.synchronize()
+    for n, h in [(0, 0), (N - 1, H - 1), (123, 17)]:
+        cat = {nm: (torch.cat([y[nm][n:n + 1, :, h:h + 1] for y in ys], dim=1)
+                    if ys[0][nm] is not None else None)
+               for nm in ("q", "k", "v", "g", "beta", "lam", "b", "w")}
+        cat.update(h0=h0[n:n + 1, h:h + 1], scale=ys[0]["scale"], flags=ys[0]["flags"])
+        ro, rh = oracle_forward(cat)
+        got = torch.stack([o[n:n + 1, h:h + 1].float().cpu() for o in outs], dim=1)
+        assert rel_err(got, ro) <= 2e-2
+        assert rel_err(state[n:n + 1, h:h + 1].cpu(), rh) <= 2e-2
+
+
+def test_prefill_then_decode_equals_longer_prefill():
+    x = wl.make_inputs("kda", 2, 130, 2, 128, 128, torch.float32, seed=61, h0_std=0.05)
+    o, hT = gpu_forward(x)
+    y = wl.make_inputs("kda", 2, 1, 2, 128, 128, torch.float32, seed=62)
+    o1 = _gpu_step(y, hT)
+    torch.cuda.synchronize()
+    cat = {n: (torch.cat([x[n], y[n]], dim=1) if x[n] is not None else None)
+           for n in ("q", "k", "v", "g", "beta", "lam", "b", "w")}
+    cat.update(h0=x["h0"], scale=x["scale"], flags=x["flags"])
+    ro, rh = oracle_forward(cat)
+    assert rel_err(o1.float().cpu(), ro[:, -1]) <= 1e-4
+    assert rel_err(hT.cpu(), rh) <= 1e-4
+
+
+# ------------------------------------------------------------ gate cumsum
+@pytest.mark.parametrize("shape", [(2, 130, 3), (1, 200, 4, 128), (2, 64, 5, 64), (1, 1, 7)])
+def test_gate_cumsum(shape):
+    gen = torch.Generator().manual_seed(len(shape))
+    g = -torch.nn.functional.softplus(torch.randn(*shape, generator=gen))
+    G = gdr.gate_cumsum(g.cuda())
+    torch.cuda.synchronize()
+    ref = np.stack([och.chunk_local_cumsum(f64(g[b]), 64) for b in range(shape[0])])
+    assert np.max(np.abs(G.cpu().numpy() - ref)) <= 1e-5 * max(1.0, np.abs(ref).max())
+
+
+def test_gate_cumsum_in_place():
+    g = -torch.rand(2, 100, 8, 64, device="cuda")
+    ref = gdr.gate_cumsum(g.clone())
+    gdr.gate_cumsum(g, out=g)
+    torch.cuda.synchronize()
+    assert torch.equal(g, ref)
+
+
+# ------------------------------------------------------------ error paths
+def test_binding_errors_on_gpu():
+    x = to_dev(wl.make_inputs("gdn", 1, 64, 1, 64, 64, torch.bfloat16, seed=1))
+    with pytest.raises(ValueError):
+        gdr.chunk_fwd(x["q"], x["k"], x["v"].float(), x["g"], x["beta"])
+    with pytest.raises(gdr.GdrError) as e:
+        gdr.chunk_fwd(x["q"], x["k"], x["v"], x["g"], None, flags=0)
+    assert e.value.code == 1
+    q = torch.zeros(1, 64, 1, 32, dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(gdr.GdrError) as e:
+        gdr.chunk_fwd(q, q, q, x["g"], x["beta"])
+    assert e.value.code == 2
