@@ -56,11 +56,12 @@ def lib():
         L.gdr_chunk_fwd.argtypes = [sp] + [_vp] * 11 + [_vp, ctypes.c_size_t, _vp]
         L.gdr_recurrent_step.argtypes = [sp] + [_vp] * 10 + [_vp]
         L.gdr_gate_cumsum.argtypes = [ctypes.c_int] * 4 + [_vp, _vp, _vp]
+        L.gdr_chunk_fwd_check.argtypes = [_vp, _vp, ctypes.POINTER(ctypes.c_int)]
         L.gdr_status_string.argtypes = [ctypes.c_int]
         L.gdr_status_string.restype = ctypes.c_char_p
         L.gdr_abi_version.restype = ctypes.c_int
         for name in ("gdr_chunk_fwd_workspace", "gdr_chunk_fwd", "gdr_recurrent_step",
-                     "gdr_gate_cumsum"):
+                     "gdr_gate_cumsum", "gdr_chunk_fwd_check"):
             getattr(L, name).restype = ctypes.c_int
         _lib = L
     return _lib
@@ -166,6 +167,22 @@ def chunk_fwd(q, k, v, g, beta=None, lam=None, b=None, w=None, h0=None, *, scale
     if st:
         raise GdrError(st, "gdr_chunk_fwd")
     return o, hT
+
+
+def chunk_fwd_check(workspace, stream=None):
+    """Status a chunk_fwd call left in its workspace (synchronises the stream).
+
+    Returns None when the call completed; raises GdrError(GDR_ERR_TIMEOUT) when a
+    bounded device-side wait gave up.
+    """
+    if workspace is None:
+        return None
+    detail = (ctypes.c_int * 2)()
+    with torch.cuda.device(workspace.device):
+        st = lib().gdr_chunk_fwd_check(_ptr(workspace), _stream(stream, workspace.device), detail)
+    if st:
+        raise GdrError(st, "gdr_chunk_fwd (CTA %d, wait %d)" % (detail[0], detail[1]))
+    return None
 
 
 def recurrent_step(q, k, v, g, state, beta=None, lam=None, b=None, w=None, *, scale=None,

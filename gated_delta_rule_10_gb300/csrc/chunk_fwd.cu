@@ -1,4 +1,5 @@
-// Chunkwise-parallel forward of the gated delta rule, fused into one kernel.
+// Chunkwise-parallel forward of the gated delta rule for fp32 inputs, fused
+// into one kernel (bf16 inputs take the tcgen05 kernel of chunk_fwd_tc.cu).
 //
 // Algorithm: Gated DeltaNet-2 notes, key design 2 (the chunkwise WY form with
 // the cumulative decay absorbed into the rank-one factors), which the Q-Delta
@@ -16,9 +17,10 @@
 //   O_n     = Q_gamma S_n + A_qk W
 //   S_{n+1} = Diag(gamma_C) S_n + K_tail^T W,  K_tail_r = gamma_C/gamma_r (.) k_r
 //
-// The products run on tensor cores (bf16 operands, fp32 accumulation). For
-// fp32 inputs every operand is split into a bf16 pair hi + lo and each
-// product takes hi*hi + hi*lo + lo*hi, which keeps ~2^-16 relative accuracy.
+// The products run on warp-level tensor-core MMA with bf16 operands and fp32
+// accumulation. Every fp32 operand is split into a bf16 pair hi + lo and each
+// product takes hi*hi + hi*lo + lo*hi, which keeps ~2^-16 relative accuracy
+// (the template keeps a one-plane mode, SPLIT = false, for bf16 operands).
 // S stays fp32 in registers across all chunks of the scan.
 //
 // Decay factors of T and A_qk. Scalar gates: T_ri = (e_r . k_i) exp(G_r - G_i)
@@ -517,25 +519,11 @@ cudaError_t launch_one(const ChunkArgs& a, cudaStream_t stream) {
 
 }  // namespace
 
-int chunk_fwd_slice_width(int B, int H, int dk, int dv, bool f32) {
-  if (f32) return dk == 128 ? 16 : 32;
-  // two value slices per SM-sized wave are enough; narrower slices double
-  // the scans when there are few (batch, head) pairs
-  (void)dv;
-  return (long long)B * H * 2 >= 120 ? 64 : 32;
-}
-
-cudaError_t launch_chunk_fwd(const ChunkArgs& a, int dk, int nv, bool f32,
-                             cudaStream_t stream) {
-  if (f32) {
-    if (dk == 64 && nv == 32) return launch_one<64, 32, true, float>(a, stream);
-    if (dk == 128 && nv == 16) return launch_one<128, 16, true, float>(a, stream);
-  } else {
-    if (dk == 64 && nv == 32) return launch_one<64, 32, false, __nv_bfloat16>(a, stream);
-    if (dk == 64 && nv == 64) return launch_one<64, 64, false, __nv_bfloat16>(a, stream);
-    if (dk == 128 && nv == 32) return launch_one<128, 32, false, __nv_bfloat16>(a, stream);
-    if (dk == 128 && nv == 64) return launch_one<128, 64, false, __nv_bfloat16>(a, stream);
-  }
+cudaError_t launch_chunk_fwd_f32(const ChunkArgs& a, int dk, cudaStream_t stream) {
+  // value slices of 16 (d_k = 128) or 32 (d_k = 64) columns keep the hi/lo
+  // operand planes within one CTA's shared memory
+  if (dk == 64 && a.dv % 32 == 0) return launch_one<64, 32, true, float>(a, stream);
+  if (dk == 128 && a.dv % 16 == 0) return launch_one<128, 16, true, float>(a, stream);
   return cudaErrorInvalidValue;
 }
 

@@ -1,0 +1,635 @@
+// Pipelined chunkwise forward for scalar gates (Gated DeltaNet and Q-Delta),
+// bf16 inputs, on tcgen05 tensor cores fed by TMA.
+//
+// Same algorithm as chunk_fwd_tc.cu (Gated DeltaNet-2 notes, key design 2;
+// Q-Delta notes, key design 3), rearranged so that Q, K and V go from HBM to
+// the tensor cores untouched: with a scalar decay and scalar beta every gate is
+// a per-row factor and folds into the small 64x64 matrices:
+//
+//   T_ri  = beta_r (k_r.k_i + lam_r q_r.k_i) exp(G_r - G_i)   (i < r)
+//   A_qk  = s (q_r.k_i) exp(G_r - G_i)                         (i <= r)
+//   A     = (I + T)^{-1}
+//   Y     = A diag(beta e^G) K + A diag(beta lam e^G) Q        (= A E_abs)
+//   U     = A diag(beta) V                                     (= A Z)
+//   W     = U - Y S_n
+//   O_n   = s diag(e^G) Q S_n + A_qk W                         (= Q_gamma S_n + A_qk W)
+//   S_n+1 = e^{G_C} S_n + K^T diag(e^{G_C - G}) W              (= Diag(gamma_C) S_n + K_tail^T W)
+//
+// Roles (288 threads): warps 0-3 run the state pass of chunk n (S in fp32
+// registers, one key channel per thread), warps 4-7 run the intra-chunk work
+// of chunk n+1 (T, A_qk, the inverse, Y and U), warp 8 streams the next chunks'
+// Q, K, V tiles with TMA and their gates with plain loads into a two-stage
+// ring. Hand-offs go through mbarriers; every wait is bounded, and a wait that
+// gives up makes all roles leave their loops together, release tensor memory
+// and report GDR_ERR_TIMEOUT in the status words.
+#include <cuda.h>
+
+#include "common.cuh"
+#include "kernels.h"
+#include "tc.cuh"
+
+namespace gdr {
+namespace {
+
+constexpr int kThreads = 288;
+constexpr int kNV = 64;
+constexpr uint32_t kPolls = 1u << 20;
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kScanBar = 1, kIntraBar = 2;
+
+template <int DK>
+struct PipeLayout {
+  static constexpr uint32_t kKQ = DK * 256;               // K/Q blocks interleaved
+  static constexpr uint32_t kStage = kKQ + 8192 + 1024;   // + V + gates (g, beta, lam)
+  static constexpr uint32_t oStage = 0;                   // two stages
+  static constexpr uint32_t oY = 2 * kStage;              // -Y, 64 x DK (A, K-major)
+  static constexpr uint32_t oAqk = oY + DK * 128;         // two 64 x 64 (A, K-major)
+  static constexpr uint32_t oRows = oAqk + 2 * 8192;      // two {e^G, e^{G_C-G}, e^{G_C}}
+  static constexpr uint32_t oAy = oRows + 2 * 1024;       // A diag(beta e^G)
+  static constexpr uint32_t oAyl = oAy + 8192;            // A diag(beta lam e^G)
+  static constexpr uint32_t oAu = oAyl + 8192;            // A diag(beta)
+  static constexpr uint32_t oS = oAu + 8192;              // S_n, DK x 64 (B, MN-major)
+  static constexpr uint32_t oW = oS + DK * 128;           // W (B, MN-major)
+  static constexpr uint32_t oW2 = oW + 8192;              // diag(e^{G_C-G}) W
+  static constexpr uint32_t oT = oW2 + 8192;              // fp32 [64][65]
+  static constexpr uint32_t oAf = oT + 64 * 65 * 4;       // fp32 [64][65] (also q.k for QMIX)
+  static constexpr uint32_t oP = oAf + 64 * 65 * 4;       // fp32 [4][256] per-warp scratch
+  static constexpr uint32_t oVec = oP + 4 * 256 * 4;      // intra: G, e^G, beta, lam [64]
+  static constexpr uint32_t oBar = oVec + 4 * 64 * 4;     // mbarriers
+  static constexpr int kBars = 15;
+  static constexpr uint32_t oSlot = oBar + kBars * 8;
+  static constexpr uint32_t oAbort = oSlot + 4;
+  static constexpr uint32_t bytes = oAbort + 12;
+  static constexpr uint32_t launch_bytes = bytes + 1024;
+};
+
+// barrier indices
+enum : uint32_t {
+  kFull0 = 0, kFree0 = 2, kReady0 = 4, kDuFree0 = 6, kAqkFree0 = 8, kTyFree = 10,
+  kM1 = 11, kM2 = 12, kM3 = 13, kM4 = 14
+};
+
+template <int DK>
+struct PipeTmem {
+  static constexpr uint32_t D1 = 0;
+  static constexpr uint32_t DY = 64;
+  static constexpr uint32_t DU0 = 64 + DK;
+  static constexpr uint32_t DQ = DU0 + 2 * kNV;
+  static constexpr uint32_t DA = DQ + kNV;
+  static constexpr uint32_t DS = DA + kNV;
+};
+
+__device__ __forceinline__ uint4 pack8f(const float* x) {
+  uint4 u;
+  u.x = pack_bf16x2(x[0], x[1]);
+  u.y = pack_bf16x2(x[2], x[3]);
+  u.z = pack_bf16x2(x[4], x[5]);
+  u.w = pack_bf16x2(x[6], x[7]);
+  return u;
+}
+
+// fp32 pair -> bf16 pair hi + lo (x ~= hi + lo to ~2^-17 relative)
+__device__ __forceinline__ void split2(float x, float y, uint32_t& hi, uint32_t& lo) {
+  const __nv_bfloat162 h = __floats2bfloat162_rn(x, y);
+  const float2 hf = __bfloat1622float2(h);
+  const __nv_bfloat162 l = __floats2bfloat162_rn(x - hf.x, y - hf.y);
+  hi = *reinterpret_cast<const uint32_t*>(&h);
+  lo = *reinterpret_cast<const uint32_t*>(&l);
+}
+
+// One 16x8 tile C += M[r0.., mk0..mk0+15] * N[nk0..nk0+15, n0..n0+7] from
+// row-major fp32 shared matrices, with both operands split into bf16 hi + lo
+// and the products hi*hi + hi*lo + lo*hi (warp-level MMA, fp32 accumulation).
+__device__ __forceinline__ void mma16x8x16_f32(float (&c)[4], const float* M, int ldm, int r0,
+                                               int mk0, const float* N, int ldn, int nk0, int n0) {
+  const int l = threadIdx.x & 31;
+  const int r = r0 + (l >> 2), kc = mk0 + 2 * (l & 3), n = n0 + (l >> 2), kr = nk0 + 2 * (l & 3);
+  uint32_t ah[4], al[4], bh0, bl0, bh1, bl1;
+  split2(M[r * ldm + kc], M[r * ldm + kc + 1], ah[0], al[0]);
+  split2(M[(r + 8) * ldm + kc], M[(r + 8) * ldm + kc + 1], ah[1], al[1]);
+  split2(M[r * ldm + kc + 8], M[r * ldm + kc + 9], ah[2], al[2]);
+  split2(M[(r + 8) * ldm + kc + 8], M[(r + 8) * ldm + kc + 9], ah[3], al[3]);
+  split2(N[kr * ldn + n], N[(kr + 1) * ldn + n], bh0, bl0);
+  split2(N[(kr + 8) * ldn + n], N[(kr + 9) * ldn + n], bh1, bl1);
+  mma_bf16_16816(c, ah, bh0, bh1);
+  mma_bf16_16816(c, ah, bl0, bl1);
+  mma_bf16_16816(c, al, bh0, bh1);
+}
+
+// Stores sign * C of a 16x8 accumulator tile at (r0, n0) of a row-major fp32
+// matrix.
+__device__ __forceinline__ void store_tile(float* D, int ld, int r0, int n0, const float (&c)[4],
+                                           float sign) {
+  const int l = threadIdx.x & 31;
+  const int r = r0 + (l >> 2), n = n0 + 2 * (l & 3);
+  D[r * ld + n] = sign * c[0];
+  D[r * ld + n + 1] = sign * c[1];
+  D[(r + 8) * ld + n] = sign * c[2];
+  D[(r + 8) * ld + n + 1] = sign * c[3];
+}
+
+// Bounded mbarrier wait that also gives up early once another role aborted.
+__device__ __forceinline__ bool wait_or_abort(uint32_t mbar, uint32_t parity,
+                                              volatile int* abort_flag) {
+  for (uint32_t i = 0; i < kPolls; ++i) {
+    uint32_t done;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+        " selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(done)
+        : "r"(mbar), "r"(parity)
+        : "memory");
+    if (done) return true;
+    if ((i & 255) == 255 && *abort_flag) return false;
+  }
+  *abort_flag = 1;
+  return false;
+}
+
+template <int DK>
+__global__ void __launch_bounds__(kThreads, 1)
+    chunk_fwd_pipe_kernel(const ChunkArgs a, const __grid_constant__ CUtensorMap tm_q,
+                          const __grid_constant__ CUtensorMap tm_k,
+                          const __grid_constant__ CUtensorMap tm_v, int* status) {
+  using L = PipeLayout<DK>;
+  using TM = PipeTmem<DK>;
+  constexpr uint32_t kStageTx = static_cast<uint32_t>(DK / 64) * 2 * 8192 + 8192;
+  extern __shared__ unsigned char smem_raw[];
+  unsigned char* smem = reinterpret_cast<unsigned char*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  const uint32_t sb = smem_u32(smem);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int h = blockIdx.y, bb = blockIdx.z;
+  const int col0 = blockIdx.x * kNV;
+  const int T = a.T, H = a.H, DV = a.dv;
+  const bool QM = a.flags & 8u;
+  const int n_chunks = (T + kChunk - 1) / kChunk;
+  auto bar = [&](uint32_t i) { return sb + L::oBar + 8 * i; };
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::oAbort);
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(smem + L::oSlot);
+
+  if (warp == 0) tc::tmem_alloc(smem_u32(tslot), kTmemCols);
+  if (tid == 32) {
+    for (int s = 0; s < 2; ++s) {
+      tc::mbar_init(bar(kFull0 + s), 2);     // expect_tx arrive + gates arrive
+      tc::mbar_init(bar(kFree0 + s), 1);
+      tc::mbar_init(bar(kReady0 + s), 1);
+      tc::mbar_init(bar(kDuFree0 + s), 1);
+      tc::mbar_init(bar(kAqkFree0 + s), 1);
+    }
+    tc::mbar_init(bar(kTyFree), 1);
+    for (uint32_t i = kM1; i <= kM4; ++i) tc::mbar_init(bar(i), 1);
+    *abort_flag = 0;
+    tc::fence_mbar_init();
+  }
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  const uint32_t tmem = *tslot;
+  const uint32_t tlane = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);
+  int fail = -1;
+
+  if (warp == 8) {
+    // ------------------------------------------------------------ producer
+    int issued = 0;
+    for (int n = 0; n < n_chunks; ++n) {
+      const int s = n & 1;
+      if (n >= 2 && !wait_or_abort(bar(kFree0 + s), ((n - 2) >> 1) & 1, abort_flag)) {
+        fail = 4 * n;
+        break;
+      }
+      const uint32_t st = sb + L::oStage + s * L::kStage;
+      const int t0 = n * kChunk;
+      if (lane == 0) {
+        tc::mbar_arrive_expect_tx(bar(kFull0 + s), kStageTx);
+#pragma unroll
+        for (int blk = 0; blk < DK / 64; ++blk) {
+          tc::tma_load_4d(st + (2 * blk) * 8192, &tm_k, blk * 64, h, t0, bb, bar(kFull0 + s));
+          tc::tma_load_4d(st + (2 * blk + 1) * 8192, &tm_q, blk * 64, h, t0, bb, bar(kFull0 + s));
+        }
+        tc::tma_load_4d(st + L::kKQ, &tm_v, col0, h, t0, bb, bar(kFull0 + s));
+      }
+      issued = n + 1;
+      float* gst = reinterpret_cast<float*>(smem + L::oStage + s * L::kStage + L::kKQ + 8192);
+      const int Lr = min(kChunk, T - t0);
+#pragma unroll
+      for (int half = 0; half < 2; ++half) {
+        const int r = lane + 32 * half;
+        const size_t ti = (size_t(bb) * T + t0 + r) * H + h;
+        gst[r] = r < Lr ? __ldg(a.g + ti) : 0.f;
+        gst[64 + r] = r < Lr ? __ldg(a.beta + ti) : 0.f;
+        gst[128 + r] = (r < Lr && QM) ? __ldg(a.lam + ti) : 0.f;
+      }
+      __syncwarp();
+      if (lane == 0) tc::mbar_arrive(bar(kFull0 + s));
+    }
+    // let the loads already issued land before the CTA can exit
+    for (int n = max(0, issued - 2); n < issued; ++n)
+      wait_or_abort(bar(kFull0 + (n & 1)), (n >> 1) & 1, abort_flag);
+  } else if (warp >= 4) {
+    // ------------------------------------------------------------ intra-chunk
+    const int it = tid - 128, w4 = warp - 4;
+    float* sT = reinterpret_cast<float*>(smem + L::oT);
+    float* sAf = reinterpret_cast<float*>(smem + L::oAf);
+    float* sQK = sAf;
+    float* sP = reinterpret_cast<float*>(smem + L::oP);
+    float* vG = reinterpret_cast<float*>(smem + L::oVec);
+    float* vEG = vG + 64;
+    float* vBeta = vEG + 64;
+    float* vLam = vBeta + 64;
+    for (int n = 0; n < n_chunks; ++n) {
+      const int s = n & 1;
+      const uint32_t st = sb + L::oStage + s * L::kStage;
+      const float* gst = reinterpret_cast<const float*>(smem + L::oStage + s * L::kStage + L::kKQ + 8192);
+      bool ok = wait_or_abort(bar(kFull0 + s), (n >> 1) & 1, abort_flag);
+      if (tc::named_any(kIntraBar, 128, !ok)) { fail = 4 * n; break; }
+
+      // gates of the chunk: G (in-chunk cumsum), per-row factors
+      if (w4 == 0) {
+        float g0 = gst[lane], g1 = gst[lane + 32];
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+          const float u0 = __shfl_up_sync(0xffffffffu, g0, off);
+          const float u1 = __shfl_up_sync(0xffffffffu, g1, off);
+          if (lane >= off) { g0 += u0; g1 += u1; }
+        }
+        g1 += __shfl_sync(0xffffffffu, g0, 31);
+        const float GL = __shfl_sync(0xffffffffu, g1, 31);
+        float* rows = reinterpret_cast<float*>(smem + L::oRows + s * 1024);
+        vG[lane] = g0;
+        vG[lane + 32] = g1;
+        const float e0 = __expf(g0), e1 = __expf(g1);
+        vEG[lane] = e0;
+        vEG[lane + 32] = e1;
+        vBeta[lane] = gst[64 + lane];
+        vBeta[lane + 32] = gst[96 + lane];
+        vLam[lane] = gst[128 + lane];
+        vLam[lane + 32] = gst[160 + lane];
+        rows[lane] = e0;
+        rows[lane + 32] = e1;
+        rows[64 + lane] = __expf(GL - g0);
+        rows[96 + lane] = __expf(GL - g1);
+        if (lane == 0) rows[128] = __expf(GL);
+      }
+      tc::named_sync(kIntraBar, 128);
+
+      // M1: [K; Q] K^T  (M = 128, N = 64, K = DK), raw TMA tiles
+      if (it == 0) {
+        tc::fence_after_sync();
+        constexpr uint32_t id = tc::idesc_bf16(128, 64, 0, 0);
+#pragma unroll
+        for (int k0 = 0; k0 < DK; k0 += 16) {
+          const uint32_t kb = (k0 >> 6) * 16384 + (k0 & 63) * 2;
+          tc::mma_bf16(tmem + TM::D1, tc::smem_desc(st + kb, 16, 1024),
+                       tc::smem_desc(st + kb, 16, 1024), id, k0 > 0);
+        }
+        tc::commit(bar(kM1));
+      }
+      ok = wait_or_abort(bar(kM1), n & 1, abort_flag);
+      if (tc::named_any(kIntraBar, 128, !ok)) { fail = 4 * n + 1; break; }
+      tc::fence_after_sync();
+
+      // T (fp32) and A_qk (bf16): rows r of K K^T sit in lanes 0..63,
+      // rows r of Q K^T in lanes 64..127
+      {
+        const int r = it & 63;
+        const bool isK = it < 64;
+        const float Gr = vG[r];
+        if (!isK) {
+          // A_qk[n%2] is free once the state pass of chunk n-2 has used it
+          ok = n < 2 || wait_or_abort(bar(kAqkFree0 + s), ((n - 2) >> 1) & 1, abort_flag);
+        }
+        if (tc::named_any(kIntraBar, 128, !ok)) { fail = 4 * n + 2; break; }
+        const uint32_t aqk = L::oAqk + s * 8192;
+        const float br = vBeta[r], lr = vLam[r];
+#pragma unroll
+        for (int c = 0; c < 64; c += 16) {
+          float x[16];
+          tc::tmem_ld16(tlane + TM::D1 + c, x);
+          if (isK) {
+            if (QM) {
+#pragma unroll
+              for (int j = 0; j < 16; ++j) sT[r * 65 + c + j] = x[j];
+            } else {
+#pragma unroll
+              for (int j = 0; j < 16; ++j) {
+                const int i = c + j;
+                sT[r * 65 + i] = i < r ? br * __expf(Gr - vG[i]) * x[j] : 0.f;
+              }
+            }
+          } else {
+            float y[16];
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+              const int i = c + j;
+              y[j] = i <= r ? a.scale * __expf(Gr - vG[i]) * x[j] : 0.f;
+              if (QM) sQK[r * 65 + i] = lr * x[j];
+            }
+            *reinterpret_cast<uint4*>(smem + aqk + tc::tile_off(64, r, c)) = pack8f(y);
+            *reinterpret_cast<uint4*>(smem + aqk + tc::tile_off(64, r, c + 8)) = pack8f(y + 8);
+          }
+        }
+        tc::fence_before_sync();
+        if (QM) {
+          tc::named_sync(kIntraBar, 128);
+          if (isK) {
+#pragma unroll 16
+            for (int i = 0; i < 64; ++i) {
+              const float t = sT[r * 65 + i] + sQK[r * 65 + i];
+              sT[r * 65 + i] = i < r ? br * __expf(Gr - vG[i]) * t : 0.f;
+            }
+          }
+        }
+      }
+      tc::named_sync(kIntraBar, 128);
+
+      // A = (I + T)^{-1}: diagonal 16x16 blocks, then blocks by distance
+      if (lane < 16) {
+        const int base = w4 * 16;
+        float col[16];
+#pragma unroll
+        for (int r = 0; r < 16; ++r) {
+          float acc = 0.f;
+#pragma unroll
+          for (int i = 0; i < r; ++i) acc += sT[(base + r) * 65 + base + i] * col[i];
+          col[r] = (r == lane ? 1.f : 0.f) - acc;
+        }
+#pragma unroll
+        for (int r = 0; r < 16; ++r) sAf[(base + r) * 65 + base + lane] = col[r];
+      }
+      tc::named_sync(kIntraBar, 128);
+      // 16-row blocks (1,0) and (3,2): A_IJ = -Dinv_I T_IJ Dinv_J. Warp w takes
+      // block (1,0) for w < 2, else (3,2), value columns 8 (w & 1) .. +7.
+      {
+        float* sX = sP + w4 * 256;                     // per-warp 32 x 8 scratch
+        const int I = w4 < 2 ? 1 : 3, J = I - 1, n0 = 16 * J + 8 * (w4 & 1);
+        float c[4] = {0.f, 0.f, 0.f, 0.f};
+        mma16x8x16_f32(c, sT, 65, 16 * I, 16 * J, sAf, 65, 16 * J, n0);
+        store_tile(sX, 8, 0, 0, c, -1.f);              // X = -T_IJ Dinv_J (16 x 8)
+        __syncwarp();
+        float d[4] = {0.f, 0.f, 0.f, 0.f};
+        mma16x8x16_f32(d, sAf, 65, 16 * I, 16 * I, sX, 8, 0, 0);
+        store_tile(sAf, 65, 16 * I, n0, d, 1.f);       // A_IJ = Dinv_I X
+      }
+      tc::named_sync(kIntraBar, 128);
+      // 32-row blocks: A[32:64, 0:32] = -A2 T[32:64, 0:32] A1 with
+      // A1 = A[0:32, 0:32], A2 = A[32:64, 32:64]; warp w: columns 8w .. 8w+7.
+      {
+        float* sX = sP + w4 * 256;
+        const int n0 = 8 * w4;
+        float c0[4] = {0.f, 0.f, 0.f, 0.f}, c1[4] = {0.f, 0.f, 0.f, 0.f};
+        if (n0 < 16) {                                  // A1 rows 0..15 vanish past column 15
+          mma16x8x16_f32(c0, sT, 65, 32, 0, sAf, 65, 0, n0);
+          mma16x8x16_f32(c1, sT, 65, 48, 0, sAf, 65, 0, n0);
+        }
+        mma16x8x16_f32(c0, sT, 65, 32, 16, sAf, 65, 16, n0);
+        mma16x8x16_f32(c1, sT, 65, 48, 16, sAf, 65, 16, n0);
+        store_tile(sX, 8, 0, 0, c0, -1.f);             // X = -T[32:64, 0:32] A1 (32 x 8)
+        store_tile(sX, 8, 16, 0, c1, -1.f);
+        __syncwarp();
+        float d0[4] = {0.f, 0.f, 0.f, 0.f}, d1[4] = {0.f, 0.f, 0.f, 0.f};
+        mma16x8x16_f32(d0, sAf, 65, 32, 32, sX, 8, 0, 0);    // A2 rows 0..15 vanish past col 15
+        mma16x8x16_f32(d1, sAf, 65, 48, 32, sX, 8, 0, 0);
+        mma16x8x16_f32(d1, sAf, 65, 48, 48, sX, 8, 16, 0);
+        store_tile(sAf, 65, 32, n0, d0, 1.f);
+        store_tile(sAf, 65, 48, n0, d1, 1.f);
+      }
+      tc::named_sync(kIntraBar, 128);
+      // A with the gates folded into its columns, as bf16 operands
+      for (int e = it; e < 64 * 8; e += 128) {
+        const int r = e >> 3, c0 = (e & 7) * 8;
+        float ay[8], ayl[8], au[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          const int m = c0 + j;
+          const float x = m <= r ? sAf[r * 65 + m] : 0.f;
+          au[j] = x * vBeta[m];
+          ay[j] = au[j] * vEG[m];
+          ayl[j] = ay[j] * vLam[m];
+        }
+        *reinterpret_cast<uint4*>(smem + L::oAy + tc::tile_off(64, r, c0)) = pack8f(ay);
+        *reinterpret_cast<uint4*>(smem + L::oAu + tc::tile_off(64, r, c0)) = pack8f(au);
+        if (QM) *reinterpret_cast<uint4*>(smem + L::oAyl + tc::tile_off(64, r, c0)) = pack8f(ayl);
+      }
+      tc::fence_proxy_async();
+      tc::named_sync(kIntraBar, 128);
+
+      // M2: Y = A_y K (+ A_yl Q); U = A_u V into D_U[n%2]
+      if (it == 0) {
+        ok = n < 2 || wait_or_abort(bar(kDuFree0 + s), ((n - 2) >> 1) & 1, abort_flag);
+        if (ok) {
+          tc::fence_after_sync();
+          constexpr uint32_t idY = tc::idesc_bf16(64, DK, 0, 1);
+          constexpr uint32_t idU = tc::idesc_bf16(64, kNV, 0, 1);
+#pragma unroll
+          for (int k0 = 0; k0 < 64; k0 += 16) {
+            const uint32_t kr = (k0 / 8) * 1024;   // next 8 chunk rows (MN-major B)
+            tc::mma_bf16(tmem + TM::DY, tc::smem_desc(sb + L::oAy + k0 * 2, 16, 1024),
+                         tc::smem_desc(st + kr, 16384, 1024), idY, k0 > 0);
+            tc::mma_bf16(tmem + TM::DU0 + s * kNV, tc::smem_desc(sb + L::oAu + k0 * 2, 16, 1024),
+                         tc::smem_desc(st + L::kKQ + kr, 8192, 1024), idU, k0 > 0);
+          }
+          if (QM) {
+#pragma unroll
+            for (int k0 = 0; k0 < 64; k0 += 16)
+              tc::mma_bf16(tmem + TM::DY, tc::smem_desc(sb + L::oAyl + k0 * 2, 16, 1024),
+                           tc::smem_desc(st + 8192 + (k0 / 8) * 1024, 16384, 1024), idY, 1);
+          }
+          tc::commit(bar(kM2));
+        }
+      }
+      if (tc::named_any(kIntraBar, 128, !ok)) { fail = 4 * n + 3; break; }
+      ok = wait_or_abort(bar(kM2), n & 1, abort_flag);
+      // -Y goes to the hand-off tile once the state pass of chunk n-1 has read it
+      if (ok && n >= 1) ok = wait_or_abort(bar(kTyFree), (n - 1) & 1, abort_flag);
+      if (tc::named_any(kIntraBar, 128, !ok)) { fail = 4 * n + 3; break; }
+      tc::fence_after_sync();
+#pragma unroll
+      for (int c = 0; c < DK; c += 16) {
+        float x[16];
+        tc::tmem_ld16(tlane + TM::DY + c, x);
+#pragma unroll
+        for (int j = 0; j < 16; ++j) x[j] = -x[j];
+        if (lane < 16) {
+          const int r = w4 * 16 + lane;
+          *reinterpret_cast<uint4*>(smem + L::oY + tc::tile_off(64, r, c)) = pack8f(x);
+          *reinterpret_cast<uint4*>(smem + L::oY + tc::tile_off(64, r, c + 8)) = pack8f(x + 8);
+        }
+      }
+      tc::fence_proxy_async();
+      tc::fence_before_sync();
+      tc::named_sync(kIntraBar, 128);
+      if (it == 0) tc::mbar_arrive(bar(kReady0 + s));
+    }
+  } else {
+    // ------------------------------------------------------------ state pass
+    const bool owner = (DK == 128) || (lane < 16);
+    const int srow = (DK == 128) ? tid : warp * 16 + (lane & 15);
+    float S[kNV];
+    {
+      const size_t base = ((size_t(bb) * H + h) * DK + srow) * DV + col0;
+#pragma unroll
+      for (int j = 0; j < kNV; j += 4) {
+        float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (a.h0 && owner) x = *reinterpret_cast<const float4*>(a.h0 + base + j);
+        S[j] = x.x; S[j + 1] = x.y; S[j + 2] = x.z; S[j + 3] = x.w;
+      }
+      if (owner) {
+#pragma unroll
+        for (int j = 0; j < kNV; j += 8)
+          *reinterpret_cast<uint4*>(smem + L::oS + tc::tile_off(DK, srow, j)) = pack8f(S + j);
+      }
+      tc::fence_proxy_async();
+      tc::named_sync(kScanBar, 128);
+    }
+    const int orow = warp * 16 + (lane & 15);   // output row held by this thread
+    for (int n = 0; n < n_chunks; ++n) {
+      const int s = n & 1;
+      const uint32_t st = sb + L::oStage + s * L::kStage;
+      const int t0 = n * kChunk;
+      const int Lr = min(kChunk, T - t0);
+      bool ok = wait_or_abort(bar(kReady0 + s), (n >> 1) & 1, abort_flag);
+      if (tc::named_any(kScanBar, 128, !ok)) { fail = 4 * n; break; }
+      const float* rows = reinterpret_cast<const float*>(smem + L::oRows + s * 1024);
+      const float eg = rows[orow], egl = rows[64 + orow], gc = rows[128];
+
+      // M3: W = U - Y S_n (onto D_U), D_Q = Q S_n
+      if (tid == 0) {
+        tc::fence_after_sync();
+        constexpr uint32_t idN = tc::idesc_bf16(64, kNV, 0, 1);
+#pragma unroll
+        for (int k0 = 0; k0 < DK; k0 += 16) {
+          const uint64_t bd = tc::smem_desc(sb + L::oS + (k0 / 8) * 1024, DK * 128, 1024);
+          const uint32_t ky = (k0 >> 6) * 8192 + (k0 & 63) * 2;
+          const uint32_t kq = (k0 >> 6) * 16384 + 8192 + (k0 & 63) * 2;
+          tc::mma_bf16(tmem + TM::DU0 + s * kNV, tc::smem_desc(sb + L::oY + ky, 16, 1024), bd, idN, 1);
+          tc::mma_bf16(tmem + TM::DQ, tc::smem_desc(st + kq, 16, 1024), bd, idN, k0 > 0);
+        }
+        tc::commit(bar(kM3));
+      }
+      ok = wait_or_abort(bar(kM3), n & 1, abort_flag);
+      if (tc::named_any(kScanBar, 128, !ok)) { fail = 4 * n + 1; break; }
+      tc::fence_after_sync();
+      if (tid == 0) tc::mbar_arrive(bar(kTyFree));
+
+#pragma unroll
+      for (int c = 0; c < kNV; c += 16) {
+        float x[16];
+        tc::tmem_ld16(tlane + TM::DU0 + s * kNV + c, x);
+        if (lane < 16) {
+          *reinterpret_cast<uint4*>(smem + L::oW + tc::tile_off(64, orow, c)) = pack8f(x);
+          *reinterpret_cast<uint4*>(smem + L::oW + tc::tile_off(64, orow, c + 8)) = pack8f(x + 8);
+#pragma unroll
+          for (int j = 0; j < 16; ++j) x[j] *= egl;
+          *reinterpret_cast<uint4*>(smem + L::oW2 + tc::tile_off(64, orow, c)) = pack8f(x);
+          *reinterpret_cast<uint4*>(smem + L::oW2 + tc::tile_off(64, orow, c + 8)) = pack8f(x + 8);
+        }
+      }
+      tc::fence_proxy_async();
+      tc::fence_before_sync();
+      tc::named_sync(kScanBar, 128);
+
+      // M4: D_A = A_qk W; D_S = K^T W2
+      if (tid == 0) {
+        tc::mbar_arrive(bar(kDuFree0 + s));
+        tc::fence_after_sync();
+        constexpr uint32_t idO = tc::idesc_bf16(64, kNV, 0, 1);
+        constexpr uint32_t idS = tc::idesc_bf16(DK, kNV, 1, 1);
+#pragma unroll
+        for (int k0 = 0; k0 < 64; k0 += 16) {
+          const uint32_t kr = (k0 / 8) * 1024;
+          tc::mma_bf16(tmem + TM::DA, tc::smem_desc(sb + L::oAqk + s * 8192 + k0 * 2, 16, 1024),
+                       tc::smem_desc(sb + L::oW + kr, 8192, 1024), idO, k0 > 0);
+          tc::mma_bf16(tmem + TM::DS, tc::smem_desc(st + kr, 16384, 1024),
+                       tc::smem_desc(sb + L::oW2 + kr, 8192, 1024), idS, k0 > 0);
+        }
+        tc::commit(bar(kM4));
+      }
+      ok = wait_or_abort(bar(kM4), n & 1, abort_flag);
+      if (tc::named_any(kScanBar, 128, !ok)) { fail = 4 * n + 2; break; }
+      tc::fence_after_sync();
+      if (tid == 0) {
+        tc::mbar_arrive(bar(kFree0 + s));
+        tc::mbar_arrive(bar(kAqkFree0 + s));
+      }
+
+      // O_n = s e^{G_r} (Q S_n)_r + (A_qk W)_r
+      {
+        __nv_bfloat16* op = static_cast<__nv_bfloat16*>(a.o) +
+                            ((size_t(bb) * T + t0 + orow) * H + h) * DV + col0;
+        const float sq = a.scale * eg;
+#pragma unroll
+        for (int c = 0; c < kNV; c += 16) {
+          float xq[16], xa[16];
+          tc::tmem_ld16(tlane + TM::DQ + c, xq);
+          tc::tmem_ld16(tlane + TM::DA + c, xa);
+#pragma unroll
+          for (int j = 0; j < 16; ++j) xq[j] = sq * xq[j] + xa[j];
+          if (lane < 16 && orow < Lr) {
+            *reinterpret_cast<uint4*>(op + c) = pack8f(xq);
+            *reinterpret_cast<uint4*>(op + c + 8) = pack8f(xq + 8);
+          }
+        }
+      }
+      // S_{n+1} = e^{G_C} S_n + K^T diag(e^{G_C - G}) W
+#pragma unroll
+      for (int c = 0; c < kNV; c += 16) {
+        float x[16];
+        tc::tmem_ld16(tlane + TM::DS + c, x);
+#pragma unroll
+        for (int j = 0; j < 16; ++j) S[c + j] = gc * S[c + j] + x[j];
+        if (owner) {
+          *reinterpret_cast<uint4*>(smem + L::oS + tc::tile_off(DK, srow, c)) = pack8f(S + c);
+          *reinterpret_cast<uint4*>(smem + L::oS + tc::tile_off(DK, srow, c + 8)) = pack8f(S + c + 8);
+        }
+      }
+      tc::fence_proxy_async();
+      tc::fence_before_sync();
+      tc::named_sync(kScanBar, 128);
+    }
+    if (fail < 0 && a.hT && owner) {
+      const size_t base = ((size_t(bb) * H + h) * DK + srow) * DV + col0;
+#pragma unroll
+      for (int j = 0; j < kNV; j += 4)
+        *reinterpret_cast<float4*>(a.hT + base + j) = make_float4(S[j], S[j + 1], S[j + 2], S[j + 3]);
+    }
+  }
+
+  if (fail >= 0 && status && (lane == 0)) {
+    if (atomicCAS(status, 0, 5) == 0) {  // GDR_ERR_TIMEOUT
+      status[1] = static_cast<int>((blockIdx.z * gridDim.y + blockIdx.y) * gridDim.x + blockIdx.x);
+      status[2] = fail;
+    }
+  }
+  tc::fence_before_sync();
+  __syncthreads();
+  if (warp == 0) tc::tmem_dealloc(tmem, kTmemCols);
+}
+
+template <int DK>
+cudaError_t launch_pipe(const ChunkArgs& a, const CUtensorMap& tq, const CUtensorMap& tk,
+                        const CUtensorMap& tv, int* status, cudaStream_t stream) {
+  using L = PipeLayout<DK>;
+  static_assert(L::launch_bytes <= 232448, "shared memory budget of one CTA");
+  auto kern = chunk_fwd_pipe_kernel<DK>;
+  cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(L::launch_bytes));
+  if (err != cudaSuccess) return err;
+  dim3 grid(a.dv / kNV, a.H, a.B);
+  kern<<<grid, kThreads, L::launch_bytes, stream>>>(a, tq, tk, tv, status);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+bool chunk_fwd_pipe_supports(unsigned flags) { return (flags & 7u) == 0; }
+
+cudaError_t launch_chunk_fwd_pipe(const ChunkArgs& a, int dk, const CUtensorMap& tq,
+                                  const CUtensorMap& tk, const CUtensorMap& tv, int* status,
+                                  cudaStream_t stream) {
+  if (dk == 64) return launch_pipe<64>(a, tq, tk, tv, status, stream);
+  if (dk == 128) return launch_pipe<128>(a, tq, tk, tv, status, stream);
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace gdr

@@ -1,5 +1,6 @@
 // The C ABI of the library (declared in include/gdr.h): argument checks and
-// kernel dispatch. Nothing here allocates memory or synchronises the stream.
+// kernel dispatch. Nothing here allocates memory; only gdr_chunk_fwd_check
+// synchronises the stream.
 #include <stdint.h>
 
 #include <cmath>
@@ -7,6 +8,7 @@
 
 #include "gdr.h"
 #include "kernels.h"
+#include "tma.h"
 
 namespace {
 
@@ -73,7 +75,9 @@ gdr_status gdr_chunk_fwd_workspace(const gdr_shape* shape, size_t* bytes) {
   if (!bytes) return GDR_ERR_INVALID_ARG;
   const gdr_status st = check_shape(shape, false);
   if (st != GDR_OK) return st;
-  *bytes = 0;  // the fused kernel keeps every intermediate on chip
+  // the fused kernels keep every intermediate on chip; the tensor-core kernel
+  // only needs its status words
+  *bytes = shape->dtype == GDR_BF16 ? gdr::kChunkWorkspaceBytes : 0;
   return GDR_OK;
 }
 
@@ -88,8 +92,8 @@ gdr_status gdr_chunk_fwd(const gdr_shape* shape, const void* q, const void* k, c
   if ((h0 && !aligned(h0, 16)) || (hT && !aligned(hT, 16))) return GDR_ERR_INVALID_ARG;
   size_t need = 0;
   gdr_chunk_fwd_workspace(shape, &need);
-  if (need > 0 && (!workspace || ws_bytes < need)) return GDR_ERR_WORKSPACE;
-  (void)workspace;
+  if (need > 0 && (!workspace || ws_bytes < need || !aligned(workspace, 16)))
+    return GDR_ERR_WORKSPACE;
 
   const bool f32 = shape->dtype == GDR_F32;
   gdr::ChunkArgs a;
@@ -97,10 +101,42 @@ gdr_status gdr_chunk_fwd(const gdr_shape* shape, const void* q, const void* k, c
   a.h0 = h0; a.o = o; a.hT = hT;
   a.B = shape->B; a.T = shape->T; a.H = shape->H; a.dv = shape->dv;
   a.flags = shape->flags; a.scale = shape->scale;
-  const int nv = gdr::chunk_fwd_slice_width(shape->B, shape->H, shape->dk, shape->dv, f32);
-  const cudaError_t err =
-      gdr::launch_chunk_fwd(a, shape->dk, nv, f32, reinterpret_cast<cudaStream_t>(stream));
+  const cudaStream_t st_ = reinterpret_cast<cudaStream_t>(stream);
+  cudaError_t err;
+  if (f32) {
+    err = gdr::launch_chunk_fwd_f32(a, shape->dk, st_);
+  } else {
+    int* status = static_cast<int*>(workspace);
+    err = cudaMemsetAsync(status, 0, gdr::kStatusWords * sizeof(int), st_);
+    if (err == cudaSuccess) {
+      if (gdr::chunk_fwd_pipe_supports(shape->flags)) {
+        CUtensorMap tq, tk, tv;
+        if (!gdr::make_bthd_tmap(&tq, q, shape->B, shape->T, shape->H, shape->dk) ||
+            !gdr::make_bthd_tmap(&tk, k, shape->B, shape->T, shape->H, shape->dk) ||
+            !gdr::make_bthd_tmap(&tv, v, shape->B, shape->T, shape->H, shape->dv))
+          return GDR_ERR_CUDA;
+        err = gdr::launch_chunk_fwd_pipe(a, shape->dk, tq, tk, tv, status, st_);
+      } else {
+        err = gdr::launch_chunk_fwd_tc(a, shape->dk, status, st_);
+      }
+    }
+  }
   return err == cudaSuccess ? GDR_OK : GDR_ERR_CUDA;
+}
+
+gdr_status gdr_chunk_fwd_check(const void* workspace, gdr_stream_t stream, int* detail) {
+  if (!workspace || !aligned(workspace, 16)) return GDR_ERR_INVALID_ARG;
+  int words[gdr::kStatusWords] = {0, 0, 0, 0};
+  const cudaStream_t st_ = reinterpret_cast<cudaStream_t>(stream);
+  if (cudaMemcpyAsync(words, workspace, sizeof(words), cudaMemcpyDeviceToHost, st_) !=
+          cudaSuccess ||
+      cudaStreamSynchronize(st_) != cudaSuccess)
+    return GDR_ERR_CUDA;
+  if (detail) {
+    detail[0] = words[1];
+    detail[1] = words[2];
+  }
+  return words[0] == 0 ? GDR_OK : static_cast<gdr_status>(words[0]);
 }
 
 gdr_status gdr_recurrent_step(const gdr_shape* shape, const void* q, const void* k,

@@ -1,6 +1,7 @@
 // Launch interface between the C ABI (gdr_api.cu) and the kernels.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 namespace gdr {
@@ -42,11 +43,23 @@ struct StepArgs {
   float scale;
 };
 
-// Value-column slice width of one chunk-forward CTA for this problem.
-int chunk_fwd_slice_width(int B, int H, int dk, int dv, bool f32);
+// Device status words the tensor-core chunk kernel reports into (in the
+// caller's workspace): [0] = 0 or a gdr_status code, [1] = CTA index,
+// [2] = 4 * chunk + which wait gave up.
+constexpr int kStatusWords = 4;
+constexpr size_t kChunkWorkspaceBytes = 256;
 
-cudaError_t launch_chunk_fwd(const ChunkArgs& a, int dk, int nv, bool f32,
-                             cudaStream_t stream);
+// fp32 inputs: split-precision warp-MMA kernel (value slice width chosen
+// inside). bf16 inputs: tcgen05 kernel, 64-wide value slices.
+cudaError_t launch_chunk_fwd_f32(const ChunkArgs& a, int dk, cudaStream_t stream);
+cudaError_t launch_chunk_fwd_tc(const ChunkArgs& a, int dk, int* status, cudaStream_t stream);
+
+// bf16 inputs with scalar gates (no channel decay, erase or write gate): the
+// pipelined TMA + tcgen05 kernel; tq, tk, tv from make_bthd_tmap.
+bool chunk_fwd_pipe_supports(unsigned flags);
+cudaError_t launch_chunk_fwd_pipe(const ChunkArgs& a, int dk, const CUtensorMap& tq,
+                                  const CUtensorMap& tk, const CUtensorMap& tv, int* status,
+                                  cudaStream_t stream);
 cudaError_t launch_recurrent_step(const StepArgs& a, int dk, int dv, bool f32,
                                   cudaStream_t stream);
 cudaError_t launch_gate_cumsum(const float* g, float* G, int B, int T, int X,

@@ -118,7 +118,10 @@ gdr_status gdr_chunk_fwd_workspace(const gdr_shape* shape, size_t* bytes);
  *   h0     [B,H,d_k,d_v] fp32 initial state, or NULL for the zero state
  *   hT     [B,H,d_k,d_v] fp32 final state (written), or NULL
  *   workspace, ws_bytes: device memory of at least
- *          gdr_chunk_fwd_workspace() bytes (NULL allowed when that is 0)
+ *          gdr_chunk_fwd_workspace() bytes, 16-byte aligned (NULL allowed
+ *          when that is 0). It holds the call's status words, which are
+ *          cleared on `stream` before the kernel runs: calls sharing one
+ *          workspace must be ordered on the stream.
  *
  * h0 and hT may be the same buffer (streaming: the state read for a (batch,
  * head) is consumed before that (batch, head)'s final state is written); no
@@ -130,6 +133,17 @@ gdr_status gdr_chunk_fwd(const gdr_shape* shape, const void* q, const void* k,
                          const float* lam, const void* b, const void* w,
                          const float* h0, void* o, float* hT, void* workspace,
                          size_t ws_bytes, gdr_stream_t stream);
+
+/*
+ * Reads the status a gdr_chunk_fwd call left in `workspace` once the work
+ * enqueued on `stream` has finished (this call synchronises the stream). It
+ * returns GDR_OK, or GDR_ERR_TIMEOUT when a bounded device-side wait of that
+ * call gave up (the affected outputs are then incomplete); with a non-NULL
+ * `detail`, detail[0] receives the index of the CTA that gave up and
+ * detail[1] 4 * chunk + the wait. Workspaces of 0 bytes need no check.
+ */
+gdr_status gdr_chunk_fwd_check(const void* workspace, gdr_stream_t stream,
+                               int* detail);
 
 /*
  * One recurrent step for decoding (LLMs from scratch ch. 11, section 11.2,

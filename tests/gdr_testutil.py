@@ -53,7 +53,13 @@ def rel_err(got, ref):
 
 
 def gpu_forward(x, **kw):
+    """The chunked forward through the C ABI; checks the call's status words."""
     import gated_delta_rule_10_gb300 as gdr
     d = to_dev(x)
-    return gdr.chunk_fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], d["lam"], d["b"], d["w"],
-                         d["h0"], scale=x["scale"], flags=x["flags"], **kw)
+    shape = gdr.make_shape(*d["q"].shape, d["v"].shape[-1], d["q"].dtype, x["flags"], x["scale"])
+    n = gdr.chunk_fwd_workspace_bytes(shape)
+    ws = torch.empty(n, dtype=torch.uint8, device="cuda") if n else None
+    out = gdr.chunk_fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], d["lam"], d["b"], d["w"],
+                        d["h0"], scale=x["scale"], flags=x["flags"], workspace=ws, **kw)
+    gdr.chunk_fwd_check(ws)
+    return out

@@ -73,6 +73,9 @@ def _shape(**kw):
 def test_workspace_query(L):
     n = ctypes.c_size_t(123)
     assert L.gdr_chunk_fwd_workspace(ctypes.byref(_shape()), ctypes.byref(n)) == 0
+    assert n.value == 256                      # bf16: the tensor-core kernel's status words
+    assert L.gdr_chunk_fwd_workspace(ctypes.byref(_shape(dtype=_binding.GDR_F32)),
+                                     ctypes.byref(n)) == 0
     assert n.value == 0
     assert L.gdr_chunk_fwd_workspace(None, ctypes.byref(n)) == 1
     assert L.gdr_chunk_fwd_workspace(ctypes.byref(_shape()), None) == 1
@@ -129,6 +132,19 @@ def test_recurrent_step_rejects_bad_arguments(L):
     assert L.gdr_recurrent_step(ctypes.byref(s), *bad_state) == 1
     s = _shape(T=1, dk=80)
     assert L.gdr_recurrent_step(ctypes.byref(s), *args) == 2
+
+
+def test_workspace_rules(L):
+    s = _shape()
+    vp = ctypes.c_void_p
+    # bf16 needs a workspace of at least 256 bytes, 16-byte aligned
+    assert _call_chunk(L, s, ws=None) == 4
+    p = dict(q=FAKE, k=FAKE, v=FAKE, g=FAKE, beta=FAKE, o=FAKE)
+    args = [vp(p.get(n)) if p.get(n) else None for n in
+            ("q", "k", "v", "g", "beta", "lam", "b", "w", "h0", "o", "hT")]
+    assert L.gdr_chunk_fwd(ctypes.byref(s), *args, vp(FAKE), ctypes.c_size_t(128), None) == 4
+    assert L.gdr_chunk_fwd(ctypes.byref(s), *args, vp(FAKE + 8), ctypes.c_size_t(256), None) == 4
+    assert L.gdr_chunk_fwd_check(None, None, None) == 1
 
 
 def test_gate_cumsum_rejects_bad_arguments(L):
