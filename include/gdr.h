@@ -146,6 +146,29 @@ gdr_status gdr_chunk_fwd_check(const void* workspace, gdr_stream_t stream,
                                int* detail);
 
 /*
+ * gdr_chunk_fwd without a workspace argument, for callers that cannot
+ * allocate device memory when they run the forward pass (a plugin whose host
+ * framework owns every allocation, a loop where cudaMalloc could block or
+ * synchronise the device). It has no counterpart on the pages: it exists for
+ * such callers only. The library compiles in a small scratch area (256
+ * bytes; a shape that would need more is rejected with GDR_ERR_WORKSPACE)
+ * that every GPU using the library holds until the process exits, and passes
+ * it where gdr_chunk_fwd takes a workspace; arguments, layouts and results
+ * are otherwise those of gdr_chunk_fwd. All calls on a device share that
+ * scratch, which keeps what the last call left; each call clears the status
+ * words it needs on `stream` first. Calls whose work overlaps on the GPU race
+ * on the scratch, so order them on one stream. A device-side timeout is
+ * recorded in the scratch but not returned; use gdr_chunk_fwd with
+ * gdr_chunk_fwd_check when that report matters. The first call on each
+ * device looks up the scratch address; make it before any stream capture.
+ */
+gdr_status gdr_chunk_fwd_static(const gdr_shape* shape, const void* q,
+                                const void* k, const void* v, const float* g,
+                                const float* beta, const float* lam,
+                                const void* b, const void* w, const float* h0,
+                                void* o, float* hT, gdr_stream_t stream);
+
+/*
  * One recurrent step for decoding (LLMs from scratch ch. 11, section 11.2,
  * in the general form above; section 11.3 for the streaming protocol: the
  * prefill's final state is the first step's state). shape->T must be 1 and
