@@ -33,7 +33,6 @@ namespace {
 
 constexpr int kThreads = 288;
 constexpr int kNV = 64;
-constexpr uint32_t kPolls = 1u << 20;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kScanBar = 1, kIntraBar = 2;
 
@@ -46,6 +45,8 @@ struct PipeLayout {
   static constexpr uint32_t oAqk = oY + DK * 128;         // two 64 x 64 (A, K-major)
   static constexpr uint32_t oRows = oAqk + 2 * 8192;      // two {e^G, e^{G_C-G}, e^{G_C}}
   static constexpr uint32_t oAy = oRows + 2 * 1024;       // A diag(beta e^G)
+                                                          // (before the inverse, the three
+                                                          // A tiles hold the decay matrix)
   static constexpr uint32_t oAyl = oAy + 8192;            // A diag(beta lam e^G)
   static constexpr uint32_t oAu = oAyl + 8192;            // A diag(beta)
   static constexpr uint32_t oS = oAu + 8192;              // S_n, DK x 64 (B, MN-major)
@@ -54,8 +55,8 @@ struct PipeLayout {
   static constexpr uint32_t oT = oW2 + 8192;              // fp32 [64][65]
   static constexpr uint32_t oAf = oT + 64 * 65 * 4;       // fp32 [64][65] (also q.k for QMIX)
   static constexpr uint32_t oP = oAf + 64 * 65 * 4;       // fp32 [4][256] per-warp scratch
-  static constexpr uint32_t oVec = oP + 4 * 256 * 4;      // intra: G, e^G, beta, lam [64]
-  static constexpr uint32_t oBar = oVec + 4 * 64 * 4;     // mbarriers
+  static constexpr uint32_t oVec = oP + 4 * 256 * 4;      // intra: G, e^G, beta, lam, e^g [64]
+  static constexpr uint32_t oBar = oVec + 5 * 64 * 4;     // mbarriers
   static constexpr int kBars = 15;
   static constexpr uint32_t oSlot = oBar + kBars * 8;
   static constexpr uint32_t oAbort = oSlot + 4;
@@ -128,19 +129,13 @@ __device__ __forceinline__ void store_tile(float* D, int ld, int r0, int n0, con
   D[(r + 8) * ld + n + 1] = sign * c[3];
 }
 
-// Bounded mbarrier wait that also gives up early once another role aborted.
+// Bounded mbarrier wait (sleeping between polls) that also gives up early once
+// another role has aborted.
 __device__ __forceinline__ bool wait_or_abort(uint32_t mbar, uint32_t parity,
                                               volatile int* abort_flag) {
-  for (uint32_t i = 0; i < kPolls; ++i) {
-    uint32_t done;
-    asm volatile(
-        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
-        " selp.u32 %0, 1, 0, p;\n}\n"
-        : "=r"(done)
-        : "r"(mbar), "r"(parity)
-        : "memory");
-    if (done) return true;
-    if ((i & 255) == 255 && *abort_flag) return false;
+  for (uint32_t i = 0; i < tc::kMaxPolls; ++i) {
+    if (tc::mbar_try_wait(mbar, parity, tc::kSuspendNs)) return true;
+    if (*abort_flag) return false;
   }
   *abort_flag = 1;
   return false;
@@ -155,8 +150,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   using TM = PipeTmem<DK>;
   constexpr uint32_t kStageTx = static_cast<uint32_t>(DK / 64) * 2 * 8192 + 8192;
   extern __shared__ unsigned char smem_raw[];
-  unsigned char* smem = reinterpret_cast<unsigned char*>(
-      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  // aligned by pointer arithmetic on the shared array, so the compiler keeps
+  // every access below in the shared state space
+  unsigned char* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   const uint32_t sb = smem_u32(smem);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int h = blockIdx.y, bb = blockIdx.z;
@@ -237,6 +233,19 @@ __global__ void __launch_bounds__(kThreads, 1)
     float* vEG = vG + 64;
     float* vBeta = vEG + 64;
     float* vLam = vBeta + 64;
+    float* vAl = vLam + 64;     // exp(g_r)
+    const float* sD = reinterpret_cast<const float*>(smem + L::oAy);
+    auto issue_m1 = [&](uint32_t stage) {   // M1: [K; Q] K^T (M=128, N=64, K=DK), raw tiles
+      tc::fence_after_sync();
+      constexpr uint32_t id = tc::idesc_bf16(128, 64, 0, 0);
+#pragma unroll
+      for (int k0 = 0; k0 < DK; k0 += 16) {
+        const uint32_t kb = (k0 >> 6) * 16384 + (k0 & 63) * 2;
+        tc::mma_bf16(tmem + TM::D1, tc::smem_desc(stage + kb, 16, 1024),
+                     tc::smem_desc(stage + kb, 16, 1024), id, k0 > 0);
+      }
+      tc::commit(bar(kM1));
+    };
     for (int n = 0; n < n_chunks; ++n) {
       const int s = n & 1;
       const uint32_t st = sb + L::oStage + s * L::kStage;
@@ -265,6 +274,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         vBeta[lane + 32] = gst[96 + lane];
         vLam[lane] = gst[128 + lane];
         vLam[lane + 32] = gst[160 + lane];
+        vAl[lane] = __expf(gst[lane]);
+        vAl[lane + 32] = __expf(gst[lane + 32]);
         rows[lane] = e0;
         rows[lane + 32] = e1;
         rows[64 + lane] = __expf(GL - g0);
@@ -273,18 +284,29 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       tc::named_sync(kIntraBar, 128);
 
-      // M1: [K; Q] K^T  (M = 128, N = 64, K = DK), raw TMA tiles
-      if (it == 0) {
-        tc::fence_after_sync();
-        constexpr uint32_t id = tc::idesc_bf16(128, 64, 0, 0);
+      // decay matrix D[r][i] = exp(G_r - G_i) = prod_{i < j <= r} exp(g_j) for
+      // i <= r, one column per thread (64 exps per chunk instead of one per entry)
+      if (it < 64) {
+        float* sDw = reinterpret_cast<float*>(smem + L::oAy);
+        const int i = it;
+        float d = 1.f;
 #pragma unroll
-        for (int k0 = 0; k0 < DK; k0 += 16) {
-          const uint32_t kb = (k0 >> 6) * 16384 + (k0 & 63) * 2;
-          tc::mma_bf16(tmem + TM::D1, tc::smem_desc(st + kb, 16, 1024),
-                       tc::smem_desc(st + kb, 16, 1024), id, k0 > 0);
+        for (int r0 = 0; r0 < 64; r0 += 16) {
+          float al[16];
+#pragma unroll
+          for (int j = 0; j < 16; j += 4) {
+            const float4 a4 = *reinterpret_cast<const float4*>(vAl + r0 + j);
+            al[j] = a4.x; al[j + 1] = a4.y; al[j + 2] = a4.z; al[j + 3] = a4.w;
+          }
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            d = select_f32(r0 + j > i, d * al[j], d);
+            sDw[(r0 + j) * 68 + i] = d;
+          }
         }
-        tc::commit(bar(kM1));
       }
+      // M1 of chunk 0 (later chunks are issued one chunk ahead, below)
+      if (n == 0 && it == 0) issue_m1(st);
       ok = wait_or_abort(bar(kM1), n & 1, abort_flag);
       if (tc::named_any(kIntraBar, 128, !ok)) { fail = 4 * n + 1; break; }
       tc::fence_after_sync();
@@ -294,7 +316,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       {
         const int r = it & 63;
         const bool isK = it < 64;
-        const float Gr = vG[r];
         if (!isK) {
           // A_qk[n%2] is free once the state pass of chunk n-2 has used it
           ok = n < 2 || wait_or_abort(bar(kAqkFree0 + s), ((n - 2) >> 1) & 1, abort_flag);
@@ -304,44 +325,65 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float br = vBeta[r], lr = vLam[r];
 #pragma unroll
         for (int c = 0; c < 64; c += 16) {
-          float x[16];
+          float x[16], dr[16], y[16];
+#pragma unroll
+          for (int j = 0; j < 16; j += 4) {       // decay row first, then the stores
+            const float4 d4 = *reinterpret_cast<const float4*>(sD + r * 68 + c + j);
+            dr[j] = d4.x; dr[j + 1] = d4.y; dr[j + 2] = d4.z; dr[j + 3] = d4.w;
+          }
           tc::tmem_ld16(tlane + TM::D1 + c, x);
-          if (isK) {
-            if (QM) {
+          // warp-uniform cases outside the element loop, only selects inside
+          if (isK && QM) {
 #pragma unroll
-              for (int j = 0; j < 16; ++j) sT[r * 65 + c + j] = x[j];
-            } else {
-#pragma unroll
-              for (int j = 0; j < 16; ++j) {
-                const int i = c + j;
-                sT[r * 65 + i] = i < r ? br * __expf(Gr - vG[i]) * x[j] : 0.f;
-              }
-            }
+            for (int j = 0; j < 16; ++j) y[j] = x[j];
           } else {
-            float y[16];
+            const float f = isK ? br : a.scale;
+            const int lim = isK ? r : r + 1;     // T strictly lower, A_qk with diagonal
 #pragma unroll
-            for (int j = 0; j < 16; ++j) {
-              const int i = c + j;
-              y[j] = i <= r ? a.scale * __expf(Gr - vG[i]) * x[j] : 0.f;
-              if (QM) sQK[r * 65 + i] = lr * x[j];
-            }
+            for (int j = 0; j < 16; ++j) y[j] = select_f32(c + j < lim, f * dr[j] * x[j], 0.f);
+          }
+          if (isK) {
+#pragma unroll
+            for (int j = 0; j < 16; ++j) sT[r * 65 + c + j] = y[j];
+          } else {
             *reinterpret_cast<uint4*>(smem + aqk + tc::tile_off(64, r, c)) = pack8f(y);
             *reinterpret_cast<uint4*>(smem + aqk + tc::tile_off(64, r, c + 8)) = pack8f(y + 8);
+            if (QM) {
+#pragma unroll
+              for (int j = 0; j < 16; ++j) sQK[r * 65 + c + j] = lr * x[j];
+            }
           }
         }
         tc::fence_before_sync();
         if (QM) {
           tc::named_sync(kIntraBar, 128);
           if (isK) {
-#pragma unroll 16
-            for (int i = 0; i < 64; ++i) {
-              const float t = sT[r * 65 + i] + sQK[r * 65 + i];
-              sT[r * 65 + i] = i < r ? br * __expf(Gr - vG[i]) * t : 0.f;
+#pragma unroll
+            for (int c = 0; c < 64; c += 16) {
+              float t[16], dr[16];
+#pragma unroll
+              for (int j = 0; j < 16; ++j) {
+                t[j] = sT[r * 65 + c + j] + sQK[r * 65 + c + j];
+                dr[j] = sD[r * 68 + c + j];
+              }
+#pragma unroll
+              for (int j = 0; j < 16; ++j)
+                sT[r * 65 + c + j] = select_f32(c + j < r, br * dr[j] * t[j], 0.f);
             }
           }
         }
       }
       tc::named_sync(kIntraBar, 128);
+      // every read of D1 is done: start M1 of the next chunk now, so that its
+      // latency hides behind the inverse of this one
+      if (n + 1 < n_chunks) {
+        if (it == 0) {
+          const int s1 = (n + 1) & 1;
+          ok = wait_or_abort(bar(kFull0 + s1), ((n + 1) >> 1) & 1, abort_flag);
+          if (ok) issue_m1(sb + L::oStage + s1 * L::kStage);
+        }
+        if (tc::named_any(kIntraBar, 128, !ok)) { fail = 4 * n + 2; break; }
+      }
 
       // A = (I + T)^{-1}: diagonal 16x16 blocks, then blocks by distance
       if (lane < 16) {
@@ -396,16 +438,24 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       tc::named_sync(kIntraBar, 128);
       // A with the gates folded into its columns, as bf16 operands
-      for (int e = it; e < 64 * 8; e += 128) {
+#pragma unroll
+      for (int rep = 0; rep < 4; ++rep) {
+        const int e = it + 128 * rep;
         const int r = e >> 3, c0 = (e & 7) * 8;
-        float ay[8], ayl[8], au[8];
+        float ay[8], ayl[8], au[8], xa[8], vb[8], ve[8], vl[8];
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
-          const int m = c0 + j;
-          const float x = m <= r ? sAf[r * 65 + m] : 0.f;
-          au[j] = x * vBeta[m];
-          ay[j] = au[j] * vEG[m];
-          ayl[j] = ay[j] * vLam[m];
+          xa[j] = sAf[r * 65 + c0 + j];
+          vb[j] = vBeta[c0 + j];
+          ve[j] = vEG[c0 + j];
+          vl[j] = vLam[c0 + j];
+        }
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          const float x = select_f32(c0 + j <= r, xa[j], 0.f);
+          au[j] = x * vb[j];
+          ay[j] = au[j] * ve[j];
+          ayl[j] = ay[j] * vl[j];
         }
         *reinterpret_cast<uint4*>(smem + L::oAy + tc::tile_off(64, r, c0)) = pack8f(ay);
         *reinterpret_cast<uint4*>(smem + L::oAu + tc::tile_off(64, r, c0)) = pack8f(au);

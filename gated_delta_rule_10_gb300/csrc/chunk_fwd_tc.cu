@@ -35,7 +35,6 @@ namespace {
 
 constexpr int kTcThreads = 128;
 constexpr int kNV = 64;                    // value columns per CTA
-constexpr uint32_t kWaitPolls = 1u << 22;  // bound on each mbarrier wait
 constexpr uint32_t kTmemCols = 512;
 
 template <int DK>
@@ -96,8 +95,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   using TM = TmemMap<DK>;
   constexpr int VK = DK / 8;
   extern __shared__ unsigned char smem_raw[];
-  unsigned char* smem = reinterpret_cast<unsigned char*>(
-      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  // aligned by pointer arithmetic on the shared array, so the compiler keeps
+  // every access below in the shared state space
+  unsigned char* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   const uint32_t sbase = smem_u32(smem);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -286,7 +286,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       }
       tc::commit(bar0);
     }
-    if (__syncthreads_or(!tc::mbar_wait(bar0, par, kWaitPolls))) { fail_at = 4 * n; break; }
+    if (__syncthreads_or(!tc::mbar_wait(bar0, par))) { fail_at = 4 * n; break; }
     tc::fence_after_sync();
 
     // ---- T (fp32) and A_qk (bf16 operand) with masks and scalar decay ----
@@ -298,11 +298,14 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       for (int c = 0; c < 64; c += 16) {
         float x[16];
         tc::tmem_ld16(tlane + TM::D1 + c, x);
+        const int lim = isT ? r : r + 1;   // T strictly lower, A_qk with diagonal
+        if (CH) {
 #pragma unroll
-        for (int j = 0; j < 16; ++j) {
-          const int i = c + j;
-          const float d = CH ? 1.f : __expf(Gr - sGs[i]);
-          x[j] = (isT ? i < r : i <= r) ? d * x[j] : 0.f;
+          for (int j = 0; j < 16; ++j) x[j] = select_f32(c + j < lim, x[j], 0.f);
+        } else {
+#pragma unroll
+          for (int j = 0; j < 16; ++j)
+            x[j] = select_f32(c + j < lim, __expf(fminf(Gr - sGs[c + j], 0.f)) * x[j], 0.f);
         }
         if (isT) {
 #pragma unroll
@@ -385,7 +388,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       }
       tc::commit(bar0 + 8);
     }
-    if (__syncthreads_or(!tc::mbar_wait(bar0 + 8, par, kWaitPolls))) { fail_at = 4 * n + 1; break; }
+    if (__syncthreads_or(!tc::mbar_wait(bar0 + 8, par))) { fail_at = 4 * n + 1; break; }
     tc::fence_after_sync();
 
     // ---- -Y to shared memory (M=64 accumulator: lanes 0..15 of each quadrant) ----
@@ -417,7 +420,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       }
       tc::commit(bar0 + 16);
     }
-    if (__syncthreads_or(!tc::mbar_wait(bar0 + 16, par, kWaitPolls))) { fail_at = 4 * n + 2; break; }
+    if (__syncthreads_or(!tc::mbar_wait(bar0 + 16, par))) { fail_at = 4 * n + 2; break; }
     tc::fence_after_sync();
 
 #pragma unroll
@@ -448,7 +451,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       }
       tc::commit(bar0 + 24);
     }
-    if (__syncthreads_or(!tc::mbar_wait(bar0 + 24, par, kWaitPolls))) { fail_at = 4 * n + 3; break; }
+    if (__syncthreads_or(!tc::mbar_wait(bar0 + 24, par))) { fail_at = 4 * n + 3; break; }
     tc::fence_after_sync();
 
     // ---- outputs and the next state ----

@@ -37,6 +37,16 @@ __device__ __forceinline__ void mma_bf16_16816(float (&d)[4], const uint32_t (&a
       : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 
+// p ? a : b as one predicated select. Written out so that a lane-dependent
+// mask around an expensive expression (exp) cannot become a divergent branch.
+__device__ __forceinline__ float select_f32(bool p, float a, float b) {
+  float r;
+  asm("{\n .reg .pred q;\n setp.ne.u32 q, %3, 0;\n selp.f32 %0, %1, %2, q;\n}\n"
+      : "=f"(r)
+      : "f"(a), "f"(b), "r"(static_cast<unsigned>(p)));
+  return r;
+}
+
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<uint32_t*>(&v);

@@ -67,19 +67,29 @@ __device__ __forceinline__ void fence_mbar_init() {
   asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
 }
 
-// Bounded wait for the phase with parity `parity` to complete. Returns false
-// after `limit` polls (each poll may suspend the thread for a short while).
-__device__ __forceinline__ bool mbar_wait(uint32_t mbar, uint32_t parity, uint32_t limit) {
-  for (uint32_t i = 0; i < limit; ++i) {
-    uint32_t done;
-    asm volatile(
-        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
-        " selp.u32 %0, 1, 0, p;\n}\n"
-        : "=r"(done)
-        : "r"(mbar), "r"(parity)
-        : "memory");
-    if (done) return true;
-  }
+// One poll of the phase with parity `parity`: the thread sleeps until the
+// phase completes or about `suspend_ns` nanoseconds pass (no busy spinning, so
+// waiting warps leave the issue slots to working ones). True once complete.
+__device__ __forceinline__ bool mbar_try_wait(uint32_t mbar, uint32_t parity, uint32_t suspend_ns) {
+  uint32_t done;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n"
+      " selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(done)
+      : "r"(mbar), "r"(parity), "r"(suspend_ns)
+      : "memory");
+  return done != 0;
+}
+
+constexpr uint32_t kSuspendNs = 200000;   // 0.2 ms per poll
+constexpr uint32_t kMaxPolls = 10000;     // at most ~2 s per wait
+
+// Bounded wait for the phase with parity `parity` to complete; false when it
+// gave up.
+__device__ __forceinline__ bool mbar_wait(uint32_t mbar, uint32_t parity,
+                                          uint32_t limit = kMaxPolls) {
+  for (uint32_t i = 0; i < limit; ++i)
+    if (mbar_try_wait(mbar, parity, kSuspendNs)) return true;
   return false;
 }
 
