@@ -27,6 +27,7 @@
 #include "common.cuh"
 #include "kernels.h"
 #include "tc.cuh"
+#include "tri_inverse.cuh"
 
 namespace gdr {
 namespace {
@@ -87,46 +88,6 @@ __device__ __forceinline__ uint4 pack8f(const float* x) {
   u.z = pack_bf16x2(x[4], x[5]);
   u.w = pack_bf16x2(x[6], x[7]);
   return u;
-}
-
-// fp32 pair -> bf16 pair hi + lo (x ~= hi + lo to ~2^-17 relative)
-__device__ __forceinline__ void split2(float x, float y, uint32_t& hi, uint32_t& lo) {
-  const __nv_bfloat162 h = __floats2bfloat162_rn(x, y);
-  const float2 hf = __bfloat1622float2(h);
-  const __nv_bfloat162 l = __floats2bfloat162_rn(x - hf.x, y - hf.y);
-  hi = *reinterpret_cast<const uint32_t*>(&h);
-  lo = *reinterpret_cast<const uint32_t*>(&l);
-}
-
-// One 16x8 tile C += M[r0.., mk0..mk0+15] * N[nk0..nk0+15, n0..n0+7] from
-// row-major fp32 shared matrices, with both operands split into bf16 hi + lo
-// and the products hi*hi + hi*lo + lo*hi (warp-level MMA, fp32 accumulation).
-__device__ __forceinline__ void mma16x8x16_f32(float (&c)[4], const float* M, int ldm, int r0,
-                                               int mk0, const float* N, int ldn, int nk0, int n0) {
-  const int l = threadIdx.x & 31;
-  const int r = r0 + (l >> 2), kc = mk0 + 2 * (l & 3), n = n0 + (l >> 2), kr = nk0 + 2 * (l & 3);
-  uint32_t ah[4], al[4], bh0, bl0, bh1, bl1;
-  split2(M[r * ldm + kc], M[r * ldm + kc + 1], ah[0], al[0]);
-  split2(M[(r + 8) * ldm + kc], M[(r + 8) * ldm + kc + 1], ah[1], al[1]);
-  split2(M[r * ldm + kc + 8], M[r * ldm + kc + 9], ah[2], al[2]);
-  split2(M[(r + 8) * ldm + kc + 8], M[(r + 8) * ldm + kc + 9], ah[3], al[3]);
-  split2(N[kr * ldn + n], N[(kr + 1) * ldn + n], bh0, bl0);
-  split2(N[(kr + 8) * ldn + n], N[(kr + 9) * ldn + n], bh1, bl1);
-  mma_bf16_16816(c, ah, bh0, bh1);
-  mma_bf16_16816(c, ah, bl0, bl1);
-  mma_bf16_16816(c, al, bh0, bh1);
-}
-
-// Stores sign * C of a 16x8 accumulator tile at (r0, n0) of a row-major fp32
-// matrix.
-__device__ __forceinline__ void store_tile(float* D, int ld, int r0, int n0, const float (&c)[4],
-                                           float sign) {
-  const int l = threadIdx.x & 31;
-  const int r = r0 + (l >> 2), n = n0 + 2 * (l & 3);
-  D[r * ld + n] = sign * c[0];
-  D[r * ld + n + 1] = sign * c[1];
-  D[(r + 8) * ld + n] = sign * c[2];
-  D[(r + 8) * ld + n + 1] = sign * c[3];
 }
 
 // Bounded mbarrier wait (sleeping between polls) that also gives up early once
@@ -385,58 +346,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (tc::named_any(kIntraBar, 128, !ok)) { fail = 4 * n + 2; break; }
       }
 
-      // A = (I + T)^{-1}: diagonal 16x16 blocks, then blocks by distance
-      if (lane < 16) {
-        const int base = w4 * 16;
-        float col[16];
-#pragma unroll
-        for (int r = 0; r < 16; ++r) {
-          float acc = 0.f;
-#pragma unroll
-          for (int i = 0; i < r; ++i) acc += sT[(base + r) * 65 + base + i] * col[i];
-          col[r] = (r == lane ? 1.f : 0.f) - acc;
-        }
-#pragma unroll
-        for (int r = 0; r < 16; ++r) sAf[(base + r) * 65 + base + lane] = col[r];
-      }
-      tc::named_sync(kIntraBar, 128);
-      // 16-row blocks (1,0) and (3,2): A_IJ = -Dinv_I T_IJ Dinv_J. Warp w takes
-      // block (1,0) for w < 2, else (3,2), value columns 8 (w & 1) .. +7.
-      {
-        float* sX = sP + w4 * 256;                     // per-warp 32 x 8 scratch
-        const int I = w4 < 2 ? 1 : 3, J = I - 1, n0 = 16 * J + 8 * (w4 & 1);
-        float c[4] = {0.f, 0.f, 0.f, 0.f};
-        mma16x8x16_f32(c, sT, 65, 16 * I, 16 * J, sAf, 65, 16 * J, n0);
-        store_tile(sX, 8, 0, 0, c, -1.f);              // X = -T_IJ Dinv_J (16 x 8)
-        __syncwarp();
-        float d[4] = {0.f, 0.f, 0.f, 0.f};
-        mma16x8x16_f32(d, sAf, 65, 16 * I, 16 * I, sX, 8, 0, 0);
-        store_tile(sAf, 65, 16 * I, n0, d, 1.f);       // A_IJ = Dinv_I X
-      }
-      tc::named_sync(kIntraBar, 128);
-      // 32-row blocks: A[32:64, 0:32] = -A2 T[32:64, 0:32] A1 with
-      // A1 = A[0:32, 0:32], A2 = A[32:64, 32:64]; warp w: columns 8w .. 8w+7.
-      {
-        float* sX = sP + w4 * 256;
-        const int n0 = 8 * w4;
-        float c0[4] = {0.f, 0.f, 0.f, 0.f}, c1[4] = {0.f, 0.f, 0.f, 0.f};
-        if (n0 < 16) {                                  // A1 rows 0..15 vanish past column 15
-          mma16x8x16_f32(c0, sT, 65, 32, 0, sAf, 65, 0, n0);
-          mma16x8x16_f32(c1, sT, 65, 48, 0, sAf, 65, 0, n0);
-        }
-        mma16x8x16_f32(c0, sT, 65, 32, 16, sAf, 65, 16, n0);
-        mma16x8x16_f32(c1, sT, 65, 48, 16, sAf, 65, 16, n0);
-        store_tile(sX, 8, 0, 0, c0, -1.f);             // X = -T[32:64, 0:32] A1 (32 x 8)
-        store_tile(sX, 8, 16, 0, c1, -1.f);
-        __syncwarp();
-        float d0[4] = {0.f, 0.f, 0.f, 0.f}, d1[4] = {0.f, 0.f, 0.f, 0.f};
-        mma16x8x16_f32(d0, sAf, 65, 32, 32, sX, 8, 0, 0);    // A2 rows 0..15 vanish past col 15
-        mma16x8x16_f32(d1, sAf, 65, 48, 32, sX, 8, 0, 0);
-        mma16x8x16_f32(d1, sAf, 65, 48, 48, sX, 8, 16, 0);
-        store_tile(sAf, 65, 32, n0, d0, 1.f);
-        store_tile(sAf, 65, 48, n0, d1, 1.f);
-      }
-      tc::named_sync(kIntraBar, 128);
+      // A = (I + T)^{-1}
+      invert_unit_lower_64(sT, sAf, sP, w4, lane, [&] { tc::named_sync(kIntraBar, 128); });
       // A with the gates folded into its columns, as bf16 operands
 #pragma unroll
       for (int rep = 0; rep < 4; ++rep) {

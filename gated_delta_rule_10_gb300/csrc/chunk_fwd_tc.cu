@@ -29,6 +29,7 @@
 #include "common.cuh"
 #include "kernels.h"
 #include "tc.cuh"
+#include "tri_inverse.cuh"
 
 namespace gdr {
 namespace {
@@ -56,10 +57,10 @@ struct TcLayout {
   static constexpr uint32_t kG = 64 * DK * 4;              // [64][DK] G (channel gates)
   static constexpr uint32_t kAf = 64 * 65 * 4;             // [64][65] A (aliases G)
   static constexpr uint32_t oGA = oT + 64 * 65 * 4;
-  static constexpr uint32_t oP = oGA + (kG > kAf ? kG : kAf);  // [3][256]
-  static constexpr uint32_t oVec = oP + 3 * 256 * 4;       // beta, lam, Gs, eG, eGL [64] each
-  static constexpr uint32_t oCh = oVec + 5 * 64 * 4;       // GL, gC [DK] each
-  static constexpr uint32_t oBar = (oCh + 2 * DK * 4 + 7) & ~7u;  // 4 mbarriers
+  static constexpr uint32_t oP = oGA + (kG > kAf ? kG : kAf);  // [4][256] inverse scratch
+  static constexpr uint32_t oVec = oP + 4 * 256 * 4;       // beta, lam, Gs, eG, eGL [64] each
+  static constexpr uint32_t oCh = oVec + 5 * 64 * 4;       // GL, gC, e^rho [DK] each
+  static constexpr uint32_t oBar = (oCh + 3 * DK * 4 + 7) & ~7u;  // 4 mbarriers
   static constexpr uint32_t oSlot = oBar + 4 * 8;          // TMEM base address
   static constexpr uint32_t bytes = oSlot + 16;
   static constexpr uint32_t launch_bytes = bytes + 1024;   // slack to align the base
@@ -86,6 +87,118 @@ __device__ __forceinline__ uint4 pack8(const float* x) {
   u.z = pack_bf16x2(x[4], x[5]);
   u.w = pack_bf16x2(x[6], x[7]);
   return u;
+}
+
+// Operand tiles of one chunk from the raw rows (flags as template parameters,
+// so no per-element branch on them). Each thread takes 8-channel vectors of
+// rows it, it + 16, ...; all its global loads are issued before any use.
+// Channel gates: f = e^{G-rho}, fi = e^{rho-G} per element and, with
+// rho = G_C / 2, e^G = f e^rho and e^{G_C - G} = fi e^rho (two exps each).
+template <int DK, bool CH, bool ER, bool QM>
+__device__ __forceinline__ void prep_tiles(unsigned char* smem, const ChunkArgs& a,
+                                           const __nv_bfloat16* q, const __nv_bfloat16* k,
+                                           const __nv_bfloat16* gb, size_t row0, int H, int h,
+                                           int Lr, const float* sG, const float* sGL,
+                                           const float* sER, const float* sBeta,
+                                           const float* sLam, const float* sEG,
+                                           const float* sEGL) {
+  using L = TcLayout<DK>;
+  constexpr int VK = DK / 8;
+  constexpr int kIter = 4;                                  // vectors in flight per thread
+  constexpr int kPasses = kChunk * VK / kTcThreads / kIter;
+  const int tid = threadIdx.x;
+#pragma unroll 1
+  for (int pass = 0; pass < kPasses; ++pass) {
+  float qv[kIter][8], kv[kIter][8], bv[ER ? kIter : 1][8];
+#pragma unroll
+  for (int u = 0; u < kIter; ++u) {
+    const int it = tid + (pass * kIter + u) * kTcThreads;
+    const int r = it / VK, c0 = (it % VK) * 8;
+    const size_t off = ((row0 + r) * H + h) * DK + c0;
+    if (r < Lr) {
+      load8(q + off, qv[u]);
+      load8(k + off, kv[u]);
+      if (ER) load8(gb + off, bv[ER ? u : 0]);
+    } else {
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        qv[u][j] = 0.f;
+        kv[u][j] = 0.f;
+        if (ER) bv[ER ? u : 0][j] = 0.f;
+      }
+    }
+  }
+#pragma unroll
+  for (int u = 0; u < kIter; ++u) {
+    const int it = tid + (pass * kIter + u) * kTcThreads;
+    const int r = it / VK, c0 = (it % VK) * 8;
+    const float lam = sLam[r], beta = sBeta[r];
+    const float ear = CH ? 0.f : sEG[r], ktr = CH ? 0.f : sEGL[r];
+    float Eb[8], Qr[8], Kb[8], Ea[8], Qg[8], Kt[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const int c = c0 + j;
+      const float x = QM ? kv[u][j] + lam * qv[u][j] : kv[u][j];
+      const float e = ER ? bv[ER ? u : 0][j] * x : beta * x;
+      float f = 1.f, fi = 1.f, ea = ear, kt = ktr;
+      if (CH) {
+        const float G = sG[r * DK + c], rho = 0.5f * sGL[c], er = sER[c];
+        f = __expf(G - rho);
+        fi = __expf(rho - G);
+        ea = f * er;
+        kt = fi * er;
+      }
+      Eb[j] = f * e;
+      Qr[j] = a.scale * f * qv[u][j];
+      Kb[j] = fi * kv[u][j];
+      Ea[j] = ea * e;
+      Qg[j] = a.scale * ea * qv[u][j];
+      Kt[j] = kt * kv[u][j];
+    }
+    st_shared_16(smem, L::oEQ + tc::tile_off(128, r, c0), pack8(Eb));
+    st_shared_16(smem, L::oEQ + tc::tile_off(128, 64 + r, c0), pack8(Qr));
+    st_shared_16(smem, L::oKb + tc::tile_off(64, r, c0), pack8(Kb));
+    st_shared_16(smem, L::oEa + tc::tile_off(64, r, c0), pack8(Ea));
+    st_shared_16(smem, L::oQg + tc::tile_off(64, r, c0), pack8(Qg));
+    st_shared_16(smem, L::oKt + tc::tile_off(64, r, c0), pack8(Kt));
+  }
+  }
+}
+
+template <int DK, bool WR>
+__device__ __forceinline__ void prep_z(unsigned char* smem, const __nv_bfloat16* v,
+                                       const __nv_bfloat16* gw, size_t row0, int H, int h,
+                                       int DV, int col0, int Lr, const float* sBeta) {
+  using L = TcLayout<DK>;
+  constexpr int kIter = kChunk * (kNV / 8) / kTcThreads;
+  const int tid = threadIdx.x;
+  float vv[kIter][8], wv[WR ? kIter : 1][8];
+#pragma unroll
+  for (int u = 0; u < kIter; ++u) {
+    const int it = tid + u * kTcThreads;
+    const int r = it / (kNV / 8), c0 = (it % (kNV / 8)) * 8;
+    const size_t off = ((row0 + r) * H + h) * DV + col0 + c0;
+    if (r < Lr) {
+      load8(v + off, vv[u]);
+      if (WR) load8(gw + off, wv[WR ? u : 0]);
+    } else {
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        vv[u][j] = 0.f;
+        if (WR) wv[WR ? u : 0][j] = 0.f;
+      }
+    }
+  }
+#pragma unroll
+  for (int u = 0; u < kIter; ++u) {
+    const int it = tid + u * kTcThreads;
+    const int r = it / (kNV / 8), c0 = (it % (kNV / 8)) * 8;
+    const float beta = sBeta[r];
+    float z[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) z[j] = WR ? wv[WR ? u : 0][j] * vv[u][j] : beta * vv[u][j];
+    st_shared_16(smem, L::oZ + tc::tile_off(64, r, c0), pack8(z));
+  }
 }
 
 template <int DK>
@@ -117,6 +230,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   float* sEGL = sEG + 64;    // scalar gates: exp(G_C - G_r)
   float* sGL = reinterpret_cast<float*>(smem + L::oCh);  // [DK] G_C
   float* sGC = sGL + DK;                                 // [DK] gamma_C
+  float* sER = sGC + DK;                                 // [DK] e^{rho}, rho = G_C / 2
   const uint32_t bar0 = sbase + L::oBar;
   uint32_t* tslot = reinterpret_cast<uint32_t*>(smem + L::oSlot);
 
@@ -180,6 +294,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         }
         sGL[c] = acc;
         sGC[c] = __expf(acc);
+        sER[c] = __expf(0.5f * acc);
       }
     } else if (warp == 0) {
       float g0 = lane < Lr ? __ldg(a.g + (row0 + lane) * H + h) : 0.f;
@@ -209,67 +324,22 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     __syncthreads();
 
     // ---- operand tiles of the chunk ----
-    for (int it = tid; it < kChunk * VK; it += kTcThreads) {
-      const int r = it / VK, c0 = (it % VK) * 8;
-      const bool valid = r < Lr;
-      const size_t off = ((row0 + r) * H + h) * DK + c0;
-      float qv[8], kv[8], bv[8];
-      if (valid) {
-        load8(q + off, qv);
-        load8(k + off, kv);
-        if (ER) load8(gb + off, bv);
-      } else {
-#pragma unroll
-        for (int j = 0; j < 8; ++j) { qv[j] = 0.f; kv[j] = 0.f; bv[j] = 0.f; }
-      }
-      float Eb[8], Qr[8], Kb[8], Ea[8], Qg[8], Kt[8];
-#pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        const int c = c0 + j;
-        const float x = QM ? kv[j] + sLam[r] * qv[j] : kv[j];
-        const float e = ER ? bv[j] * x : sBeta[r] * x;
-        float f, fi, ea, kt;
-        if (CH) {
-          const float G = sG[r * DK + c], rho = 0.5f * sGL[c];
-          f = __expf(G - rho);
-          fi = __expf(rho - G);
-          ea = __expf(G);
-          kt = __expf(sGL[c] - G);
-        } else {
-          f = 1.f;
-          fi = 1.f;
-          ea = sEG[r];
-          kt = sEGL[r];
-        }
-        Eb[j] = f * e;
-        Qr[j] = a.scale * f * qv[j];
-        Kb[j] = fi * kv[j];
-        Ea[j] = ea * e;
-        Qg[j] = a.scale * ea * qv[j];
-        Kt[j] = kt * kv[j];
-      }
-      st_shared_16(smem, L::oEQ + tc::tile_off(128, r, c0), pack8(Eb));
-      st_shared_16(smem, L::oEQ + tc::tile_off(128, 64 + r, c0), pack8(Qr));
-      st_shared_16(smem, L::oKb + tc::tile_off(64, r, c0), pack8(Kb));
-      st_shared_16(smem, L::oEa + tc::tile_off(64, r, c0), pack8(Ea));
-      st_shared_16(smem, L::oQg + tc::tile_off(64, r, c0), pack8(Qg));
-      st_shared_16(smem, L::oKt + tc::tile_off(64, r, c0), pack8(Kt));
+    switch (a.flags & 11u) {   // CH | ER | QM select the key-side tiles
+#define GDR_PREP(F)                                                                        \
+  case F:                                                                                  \
+    prep_tiles<DK, (F & 1u) != 0, (F & 2u) != 0, (F & 8u) != 0>(smem, a, q, k, gb, row0, H, h, \
+                                                                Lr, sG, sGL, sER, sBeta, sLam, \
+                                                                sEG, sEGL);                \
+    break;
+      GDR_PREP(0) GDR_PREP(1) GDR_PREP(2) GDR_PREP(3)
+      GDR_PREP(8) GDR_PREP(9) GDR_PREP(10) GDR_PREP(11)
+#undef GDR_PREP
+      default: break;
     }
-    for (int it = tid; it < kChunk * (kNV / 8); it += kTcThreads) {
-      const int r = it / (kNV / 8), c0 = (it % (kNV / 8)) * 8;
-      const size_t off = ((row0 + r) * H + h) * DV + col0 + c0;
-      float vv[8], wv[8], z[8];
-      if (r < Lr) {
-        load8(v + off, vv);
-        if (WR) load8(gw + off, wv);
-      } else {
-#pragma unroll
-        for (int j = 0; j < 8; ++j) { vv[j] = 0.f; wv[j] = 0.f; }
-      }
-#pragma unroll
-      for (int j = 0; j < 8; ++j) z[j] = WR ? wv[j] * vv[j] : sBeta[r] * vv[j];
-      st_shared_16(smem, L::oZ + tc::tile_off(64, r, c0), pack8(z));
-    }
+    if (WR)
+      prep_z<DK, true>(smem, v, gw, row0, H, h, DV, col0, Lr, sBeta);
+    else
+      prep_z<DK, false>(smem, v, gw, row0, H, h, DV, col0, Lr, sBeta);
     tc::fence_proxy_async();
     __syncthreads();
 
@@ -318,49 +388,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     }
     __syncthreads();
 
-    // ---- A = (I + T)^{-1}: 16x16 diagonal blocks per warp, then by distance ----
-    if (lane < 16) {
-      const int base = warp * 16;
-      float col[16];
-#pragma unroll
-      for (int r = 0; r < 16; ++r) {
-        float acc = 0.f;
-#pragma unroll
-        for (int i = 0; i < r; ++i) acc += sT[(base + r) * 65 + base + i] * col[i];
-        col[r] = (r == lane ? 1.f : 0.f) - acc;
-      }
-#pragma unroll
-      for (int r = 0; r < 16; ++r) sAf[(base + r) * 65 + base + lane] = col[r];
-    }
-    __syncthreads();
-#pragma unroll 1
-    for (int d = 1; d < 4; ++d) {
-      const int nb = 4 - d;
-      for (int e = tid; e < nb * 256; e += kTcThreads) {
-        const int J = e >> 8, r = (e >> 4) & 15, c = e & 15, I = J + d;
-        float acc = 0.f;
-        for (int Kb = J; Kb < I; ++Kb) {
-#pragma unroll
-          for (int m = 0; m < 16; ++m)
-            acc += sT[(16 * I + r) * 65 + 16 * Kb + m] * sAf[(16 * Kb + m) * 65 + 16 * J + c];
-        }
-        sP[J * 256 + r * 16 + c] = acc;
-      }
-      __syncthreads();
-      for (int e = tid; e < nb * 256; e += kTcThreads) {
-        const int J = e >> 8, r = (e >> 4) & 15, c = e & 15, I = J + d;
-        float acc = 0.f;
-        for (int m = 0; m <= r; ++m)
-          acc += sAf[(16 * I + r) * 65 + 16 * I + m] * sP[J * 256 + m * 16 + c];
-        sAf[(16 * I + r) * 65 + 16 * J + c] = -acc;
-      }
-      __syncthreads();
-    }
+    // ---- A = (I + T)^{-1} ----
+    invert_unit_lower_64(sT, sAf, sP, warp, lane, [] { __syncthreads(); });
     for (int it = tid; it < 64 * 8; it += kTcThreads) {
       const int r = it >> 3, c0 = (it & 7) * 8;
       float x[8];
 #pragma unroll
-      for (int j = 0; j < 8; ++j) x[j] = (c0 + j <= r) ? sAf[r * 65 + c0 + j] : 0.f;
+      for (int j = 0; j < 8; ++j) x[j] = select_f32(c0 + j <= r, sAf[r * 65 + c0 + j], 0.f);
       st_shared_16(smem, L::oA + tc::tile_off(64, r, c0), pack8(x));
     }
     tc::fence_proxy_async();
