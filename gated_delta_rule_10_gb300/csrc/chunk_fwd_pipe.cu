@@ -15,11 +15,13 @@
 //   O_n   = s diag(e^G) Q S_n + A_qk W                         (= Q_gamma S_n + A_qk W)
 //   S_n+1 = e^{G_C} S_n + K^T diag(e^{G_C - G}) W              (= Diag(gamma_C) S_n + K_tail^T W)
 //
-// Roles (288 threads): warps 0-3 run the state pass of chunk n (S in fp32
-// registers, one key channel per thread), warps 4-7 run the intra-chunk work
-// of chunk n+1 (T, A_qk, the inverse, Y and U), warp 8 streams the next chunks'
-// Q, K, V tiles with TMA and their gates with plain loads into a two-stage
-// ring. Hand-offs go through mbarriers; every wait is bounded, and a wait that
+// Roles (416 threads): warps 0-3 run the state pass of chunk n (S in fp32
+// registers, one key channel per thread), warps 4-11 run the intra-chunk work
+// of chunk n+1 (T, A_qk, the inverse, Y and U; two warps per tensor-memory lane
+// quadrant split the columns), warp 12 streams the next chunks' Q, K, V tiles
+// with TMA and their gates with plain loads into a two-stage ring. Groups of
+// MMAs are issued from two threads in different warps, since issue, not the
+// tensor core, bounds these small products. Hand-offs go through mbarriers; every wait is bounded, and a wait that
 // gives up makes all roles leave their loops together, release tensor memory
 // and report GDR_ERR_TIMEOUT in the status words.
 #include <cuda.h>
@@ -32,10 +34,11 @@
 namespace gdr {
 namespace {
 
-constexpr int kThreads = 288;
+constexpr int kThreads = 416;   // 4 scan warps, 8 intra-chunk warps, 1 producer warp
 constexpr int kNV = 64;
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kScanBar = 1, kIntraBar = 2;
+constexpr uint32_t kScanBar = 1, kIntraBar = 2, kInvBar = 3;
+constexpr uint32_t kIntraThreads = 256;
 
 template <int DK>
 struct PipeLayout {
@@ -135,7 +138,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc::mbar_init(bar(kAqkFree0 + s), 1);
     }
     tc::mbar_init(bar(kTyFree), 1);
-    for (uint32_t i = kM1; i <= kM4; ++i) tc::mbar_init(bar(i), 1);
+    tc::mbar_init(bar(kM1), 1);
+    for (uint32_t i = kM2; i <= kM4; ++i) tc::mbar_init(bar(i), 2);   // two issuing threads
     *abort_flag = 0;
     tc::fence_mbar_init();
   }
@@ -146,7 +150,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tlane = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);
   int fail = -1;
 
-  if (warp == 8) {
+  if (warp == 12) {
     // ------------------------------------------------------------ producer
     int issued = 0;
     for (int n = 0; n < n_chunks; ++n) {
@@ -185,7 +189,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       wait_or_abort(bar(kFull0 + (n & 1)), (n >> 1) & 1, abort_flag);
   } else if (warp >= 4) {
     // ------------------------------------------------------------ intra-chunk
-    const int it = tid - 128, w4 = warp - 4;
+    const int it = tid - 128;          // 0 .. 255
+    const int half = it >> 7;          // which of the two warps sharing a lane quadrant
+    const int w4 = warp & 3;           // lane quadrant of this warp
     float* sT = reinterpret_cast<float*>(smem + L::oT);
     float* sAf = reinterpret_cast<float*>(smem + L::oAf);
     float* sQK = sAf;
@@ -199,11 +205,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     auto issue_m1 = [&](uint32_t stage) {   // M1: [K; Q] K^T (M=128, N=64, K=DK), raw tiles
       tc::fence_after_sync();
       constexpr uint32_t id = tc::idesc_bf16(128, 64, 0, 0);
+      // descriptors built once per group; K steps advance the address field
+      const uint64_t dst = tc::smem_desc(stage, 16, 1024);
 #pragma unroll
       for (int k0 = 0; k0 < DK; k0 += 16) {
         const uint32_t kb = (k0 >> 6) * 16384 + (k0 & 63) * 2;
-        tc::mma_bf16(tmem + TM::D1, tc::smem_desc(stage + kb, 16, 1024),
-                     tc::smem_desc(stage + kb, 16, 1024), id, k0 > 0);
+        tc::mma_bf16(tmem + TM::D1, dst + (kb >> 4), dst + (kb >> 4), id, k0 > 0);
       }
       tc::commit(bar(kM1));
     };
@@ -212,80 +219,76 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t st = sb + L::oStage + s * L::kStage;
       const float* gst = reinterpret_cast<const float*>(smem + L::oStage + s * L::kStage + L::kKQ + 8192);
       bool ok = wait_or_abort(bar(kFull0 + s), (n >> 1) & 1, abort_flag);
-      if (tc::named_any(kIntraBar, 128, !ok)) { fail = 4 * n; break; }
+      if (tc::named_any(kIntraBar, kIntraThreads, !ok)) { fail = 4 * n; break; }
 
-      // gates of the chunk: G (in-chunk cumsum), per-row factors
-      if (w4 == 0) {
-        float g0 = gst[lane], g1 = gst[lane + 32];
-#pragma unroll
-        for (int off = 1; off < 32; off <<= 1) {
-          const float u0 = __shfl_up_sync(0xffffffffu, g0, off);
-          const float u1 = __shfl_up_sync(0xffffffffu, g1, off);
-          if (lane >= off) { g0 += u0; g1 += u1; }
-        }
-        g1 += __shfl_sync(0xffffffffu, g0, 31);
-        const float GL = __shfl_sync(0xffffffffu, g1, 31);
-        float* rows = reinterpret_cast<float*>(smem + L::oRows + s * 1024);
-        vG[lane] = g0;
-        vG[lane + 32] = g1;
-        const float e0 = __expf(g0), e1 = __expf(g1);
-        vEG[lane] = e0;
-        vEG[lane + 32] = e1;
-        vBeta[lane] = gst[64 + lane];
-        vBeta[lane + 32] = gst[96 + lane];
-        vLam[lane] = gst[128 + lane];
-        vLam[lane + 32] = gst[160 + lane];
-        vAl[lane] = __expf(gst[lane]);
-        vAl[lane + 32] = __expf(gst[lane + 32]);
-        rows[lane] = e0;
-        rows[lane + 32] = e1;
-        rows[64 + lane] = __expf(GL - g0);
-        rows[96 + lane] = __expf(GL - g1);
-        if (lane == 0) rows[128] = __expf(GL);
-      }
-      tc::named_sync(kIntraBar, 128);
-
-      // decay matrix D[r][i] = exp(G_r - G_i) = prod_{i < j <= r} exp(g_j) for
-      // i <= r, one column per thread (64 exps per chunk instead of one per entry)
+      // gates of the chunk: G (in-chunk cumsum), per-row factors. Thread r of
+      // the first 64 sums g_0 .. g_r itself from broadcast shared-memory reads
+      // (warp shuffles measured far slower here while the tensor memory is busy).
       if (it < 64) {
-        float* sDw = reinterpret_cast<float*>(smem + L::oAy);
-        const int i = it;
-        float d = 1.f;
+        const int r = it;
+        float G = 0.f, GL = 0.f;
 #pragma unroll
-        for (int r0 = 0; r0 < 64; r0 += 16) {
+        for (int j = 0; j < 64; j += 4) {
+          const float4 g4 = *reinterpret_cast<const float4*>(gst + j);
+          G += select_f32(j <= r, g4.x, 0.f) + select_f32(j + 1 <= r, g4.y, 0.f) +
+               select_f32(j + 2 <= r, g4.z, 0.f) + select_f32(j + 3 <= r, g4.w, 0.f);
+          GL += (g4.x + g4.y) + (g4.z + g4.w);
+        }
+        float* rows = reinterpret_cast<float*>(smem + L::oRows + s * 1024);
+        const float e = __expf(G);
+        vG[r] = G;
+        vEG[r] = e;
+        vBeta[r] = gst[64 + r];
+        vLam[r] = gst[128 + r];
+        vAl[r] = __expf(gst[r]);
+        rows[r] = e;
+        rows[64 + r] = __expf(GL - G);
+        if (r == 0) rows[128] = __expf(GL);
+      }
+      tc::named_sync(kIntraBar, kIntraThreads);
+
+      // decay matrix D[r][i] = exp(G_r - G_i) for i <= r: thread (i, p) fills
+      // column i over rows 16p .. 16p+15 as a running product of exp(g_j),
+      // started from exp(G_{16p-1} - G_i) (one exponential per thread)
+      {
+        float* sDw = reinterpret_cast<float*>(smem + L::oAy);
+        const int i = it & 63, p = it >> 6, bi = i >> 4;
+        if (p >= bi) {
+          float d = p == bi ? 1.f : __expf(vG[max(16 * p - 1, 0)] - vG[i]);
           float al[16];
 #pragma unroll
           for (int j = 0; j < 16; j += 4) {
-            const float4 a4 = *reinterpret_cast<const float4*>(vAl + r0 + j);
+            const float4 a4 = *reinterpret_cast<const float4*>(vAl + 16 * p + j);
             al[j] = a4.x; al[j + 1] = a4.y; al[j + 2] = a4.z; al[j + 3] = a4.w;
           }
 #pragma unroll
           for (int j = 0; j < 16; ++j) {
-            d = select_f32(r0 + j > i, d * al[j], d);
-            sDw[(r0 + j) * 68 + i] = d;
+            d = select_f32(16 * p + j > i, d * al[j], d);
+            sDw[(16 * p + j) * 68 + i] = d;
           }
         }
       }
       // M1 of chunk 0 (later chunks are issued one chunk ahead, below)
       if (n == 0 && it == 0) issue_m1(st);
       ok = wait_or_abort(bar(kM1), n & 1, abort_flag);
-      if (tc::named_any(kIntraBar, 128, !ok)) { fail = 4 * n + 1; break; }
+      if (tc::named_any(kIntraBar, kIntraThreads, !ok)) { fail = 4 * n + 1; break; }
       tc::fence_after_sync();
 
       // T (fp32) and A_qk (bf16): rows r of K K^T sit in lanes 0..63,
       // rows r of Q K^T in lanes 64..127
       {
         const int r = it & 63;
-        const bool isK = it < 64;
+        const bool isK = w4 < 2;           // lanes 0..63: K K^T, lanes 64..127: Q K^T
+        const int cbeg = 32 * half;        // this warp's half of the 64 columns
         if (!isK) {
           // A_qk[n%2] is free once the state pass of chunk n-2 has used it
           ok = n < 2 || wait_or_abort(bar(kAqkFree0 + s), ((n - 2) >> 1) & 1, abort_flag);
         }
-        if (tc::named_any(kIntraBar, 128, !ok)) { fail = 4 * n + 2; break; }
+        if (tc::named_any(kIntraBar, kIntraThreads, !ok)) { fail = 4 * n + 2; break; }
         const uint32_t aqk = L::oAqk + s * 8192;
         const float br = vBeta[r], lr = vLam[r];
 #pragma unroll
-        for (int c = 0; c < 64; c += 16) {
+        for (int c = cbeg; c < cbeg + 32; c += 16) {
           float x[16], dr[16], y[16];
 #pragma unroll
           for (int j = 0; j < 16; j += 4) {       // decay row first, then the stores
@@ -317,10 +320,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         tc::fence_before_sync();
         if (QM) {
-          tc::named_sync(kIntraBar, 128);
+          tc::named_sync(kIntraBar, kIntraThreads);
           if (isK) {
 #pragma unroll
-            for (int c = 0; c < 64; c += 16) {
+            for (int c = cbeg; c < cbeg + 32; c += 16) {
               float t[16], dr[16];
 #pragma unroll
               for (int j = 0; j < 16; ++j) {
@@ -334,24 +337,22 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       }
-      tc::named_sync(kIntraBar, 128);
-      // every read of D1 is done: start M1 of the next chunk now, so that its
-      // latency hides behind the inverse of this one
-      if (n + 1 < n_chunks) {
-        if (it == 0) {
-          const int s1 = (n + 1) & 1;
-          ok = wait_or_abort(bar(kFull0 + s1), ((n + 1) >> 1) & 1, abort_flag);
-          if (ok) issue_m1(sb + L::oStage + s1 * L::kStage);
-        }
-        if (tc::named_any(kIntraBar, 128, !ok)) { fail = 4 * n + 2; break; }
+      tc::named_sync(kIntraBar, kIntraThreads);
+      // A = (I + T)^{-1} on the first four intra warps. Meanwhile one thread of
+      // the other four starts M1 of the next chunk (every read of D1 is done),
+      // so that its issue and latency hide behind the inverse.
+      if (half == 0) {
+        invert_unit_lower_64(sT, sAf, sP, w4, lane, [] { tc::named_sync(kInvBar, 128); });
+      } else if (it == 128 && n + 1 < n_chunks) {
+        const int s1 = (n + 1) & 1;
+        ok = wait_or_abort(bar(kFull0 + s1), ((n + 1) >> 1) & 1, abort_flag);
+        if (ok) issue_m1(sb + L::oStage + s1 * L::kStage);
       }
-
-      // A = (I + T)^{-1}
-      invert_unit_lower_64(sT, sAf, sP, w4, lane, [&] { tc::named_sync(kIntraBar, 128); });
+      if (tc::named_any(kIntraBar, kIntraThreads, !ok)) { fail = 4 * n + 2; break; }
       // A with the gates folded into its columns, as bf16 operands
 #pragma unroll
-      for (int rep = 0; rep < 4; ++rep) {
-        const int e = it + 128 * rep;
+      for (int rep = 0; rep < 2; ++rep) {
+        const int e = it + 256 * rep;
         const int r = e >> 3, c0 = (e & 7) * 8;
         float ay[8], ayl[8], au[8], xa[8], vb[8], ve[8], vl[8];
 #pragma unroll
@@ -373,40 +374,50 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (QM) *reinterpret_cast<uint4*>(smem + L::oAyl + tc::tile_off(64, r, c0)) = pack8f(ayl);
       }
       tc::fence_proxy_async();
-      tc::named_sync(kIntraBar, 128);
+      tc::named_sync(kIntraBar, kIntraThreads);
 
-      // M2: Y = A_y K (+ A_yl Q); U = A_u V into D_U[n%2]
+      // M2: Y = A_y K (+ A_yl Q) from one thread; U = A_u V into D_U[n%2] from
+      // another, once the state pass of chunk n-2 has released D_U[n%2]
       if (it == 0) {
+        tc::fence_after_sync();
+        constexpr uint32_t idY = tc::idesc_bf16(64, DK, 0, 1);
+        const uint64_t dAy = tc::smem_desc(sb + L::oAy, 16, 1024);
+        const uint64_t dAyl = tc::smem_desc(sb + L::oAyl, 16, 1024);
+        const uint64_t dK = tc::smem_desc(st, 16384, 1024);          // K as MN-major B
+        const uint64_t dQ = tc::smem_desc(st + 8192, 16384, 1024);   // Q as MN-major B
+#pragma unroll
+        for (int k0 = 0; k0 < 64; k0 += 16)
+          tc::mma_bf16(tmem + TM::DY, dAy + ((k0 * 2) >> 4), dK + (((k0 / 8) * 1024) >> 4), idY,
+                       k0 > 0);
+        if (QM) {
+#pragma unroll
+          for (int k0 = 0; k0 < 64; k0 += 16)
+            tc::mma_bf16(tmem + TM::DY, dAyl + ((k0 * 2) >> 4), dQ + (((k0 / 8) * 1024) >> 4),
+                         idY, 1);
+        }
+        tc::commit(bar(kM2));
+      } else if (it == 128) {
         ok = n < 2 || wait_or_abort(bar(kDuFree0 + s), ((n - 2) >> 1) & 1, abort_flag);
         if (ok) {
           tc::fence_after_sync();
-          constexpr uint32_t idY = tc::idesc_bf16(64, DK, 0, 1);
           constexpr uint32_t idU = tc::idesc_bf16(64, kNV, 0, 1);
+          const uint64_t dAu = tc::smem_desc(sb + L::oAu, 16, 1024);
+          const uint64_t dV = tc::smem_desc(st + L::kKQ, 8192, 1024);
 #pragma unroll
-          for (int k0 = 0; k0 < 64; k0 += 16) {
-            const uint32_t kr = (k0 / 8) * 1024;   // next 8 chunk rows (MN-major B)
-            tc::mma_bf16(tmem + TM::DY, tc::smem_desc(sb + L::oAy + k0 * 2, 16, 1024),
-                         tc::smem_desc(st + kr, 16384, 1024), idY, k0 > 0);
-            tc::mma_bf16(tmem + TM::DU0 + s * kNV, tc::smem_desc(sb + L::oAu + k0 * 2, 16, 1024),
-                         tc::smem_desc(st + L::kKQ + kr, 8192, 1024), idU, k0 > 0);
-          }
-          if (QM) {
-#pragma unroll
-            for (int k0 = 0; k0 < 64; k0 += 16)
-              tc::mma_bf16(tmem + TM::DY, tc::smem_desc(sb + L::oAyl + k0 * 2, 16, 1024),
-                           tc::smem_desc(st + 8192 + (k0 / 8) * 1024, 16384, 1024), idY, 1);
-          }
+          for (int k0 = 0; k0 < 64; k0 += 16)
+            tc::mma_bf16(tmem + TM::DU0 + s * kNV, dAu + ((k0 * 2) >> 4),
+                         dV + (((k0 / 8) * 1024) >> 4), idU, k0 > 0);
           tc::commit(bar(kM2));
         }
       }
-      if (tc::named_any(kIntraBar, 128, !ok)) { fail = 4 * n + 3; break; }
+      if (tc::named_any(kIntraBar, kIntraThreads, !ok)) { fail = 4 * n + 3; break; }
       ok = wait_or_abort(bar(kM2), n & 1, abort_flag);
       // -Y goes to the hand-off tile once the state pass of chunk n-1 has read it
       if (ok && n >= 1) ok = wait_or_abort(bar(kTyFree), (n - 1) & 1, abort_flag);
-      if (tc::named_any(kIntraBar, 128, !ok)) { fail = 4 * n + 3; break; }
+      if (tc::named_any(kIntraBar, kIntraThreads, !ok)) { fail = 4 * n + 3; break; }
       tc::fence_after_sync();
 #pragma unroll
-      for (int c = 0; c < DK; c += 16) {
+      for (int c = half * (DK / 2); c < (half + 1) * (DK / 2); c += 16) {
         float x[16];
         tc::tmem_ld16(tlane + TM::DY + c, x);
 #pragma unroll
@@ -419,7 +430,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       tc::fence_proxy_async();
       tc::fence_before_sync();
-      tc::named_sync(kIntraBar, 128);
+      tc::named_sync(kIntraBar, kIntraThreads);
       if (it == 0) tc::mbar_arrive(bar(kReady0 + s));
     }
   } else {
@@ -454,17 +465,27 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float* rows = reinterpret_cast<const float*>(smem + L::oRows + s * 1024);
       const float eg = rows[orow], egl = rows[64 + orow], gc = rows[128];
 
-      // M3: W = U - Y S_n (onto D_U), D_Q = Q S_n
-      if (tid == 0) {
+      // M3: W = U - Y S_n (onto D_U) from thread 0, D_Q = Q S_n from thread 32
+      if (tid == 0 || tid == 32) {
         tc::fence_after_sync();
         constexpr uint32_t idN = tc::idesc_bf16(64, kNV, 0, 1);
+        const uint64_t dS = tc::smem_desc(sb + L::oS, DK * 128, 1024);
+        if (tid == 0) {
+          const uint64_t dY = tc::smem_desc(sb + L::oY, 16, 1024);
 #pragma unroll
-        for (int k0 = 0; k0 < DK; k0 += 16) {
-          const uint64_t bd = tc::smem_desc(sb + L::oS + (k0 / 8) * 1024, DK * 128, 1024);
-          const uint32_t ky = (k0 >> 6) * 8192 + (k0 & 63) * 2;
-          const uint32_t kq = (k0 >> 6) * 16384 + 8192 + (k0 & 63) * 2;
-          tc::mma_bf16(tmem + TM::DU0 + s * kNV, tc::smem_desc(sb + L::oY + ky, 16, 1024), bd, idN, 1);
-          tc::mma_bf16(tmem + TM::DQ, tc::smem_desc(st + kq, 16, 1024), bd, idN, k0 > 0);
+          for (int k0 = 0; k0 < DK; k0 += 16) {
+            const uint32_t ky = (k0 >> 6) * 8192 + (k0 & 63) * 2;
+            tc::mma_bf16(tmem + TM::DU0 + s * kNV, dY + (ky >> 4), dS + (((k0 / 8) * 1024) >> 4),
+                         idN, 1);
+          }
+        } else {
+          const uint64_t dQ = tc::smem_desc(st, 16, 1024);
+#pragma unroll
+          for (int k0 = 0; k0 < DK; k0 += 16) {
+            const uint32_t kq = (k0 >> 6) * 16384 + 8192 + (k0 & 63) * 2;
+            tc::mma_bf16(tmem + TM::DQ, dQ + (kq >> 4), dS + (((k0 / 8) * 1024) >> 4), idN,
+                         k0 > 0);
+          }
         }
         tc::commit(bar(kM3));
       }
@@ -490,19 +511,27 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc::fence_before_sync();
       tc::named_sync(kScanBar, 128);
 
-      // M4: D_A = A_qk W; D_S = K^T W2
-      if (tid == 0) {
-        tc::mbar_arrive(bar(kDuFree0 + s));
+      // M4: D_A = A_qk W from thread 0; D_S = K^T W2 from thread 32
+      if (tid == 0) tc::mbar_arrive(bar(kDuFree0 + s));
+      if (tid == 0 || tid == 32) {
         tc::fence_after_sync();
-        constexpr uint32_t idO = tc::idesc_bf16(64, kNV, 0, 1);
-        constexpr uint32_t idS = tc::idesc_bf16(DK, kNV, 1, 1);
+        if (tid == 0) {
+          constexpr uint32_t idO = tc::idesc_bf16(64, kNV, 0, 1);
+          const uint64_t dAqk = tc::smem_desc(sb + L::oAqk + s * 8192, 16, 1024);
+          const uint64_t dW = tc::smem_desc(sb + L::oW, 8192, 1024);
 #pragma unroll
-        for (int k0 = 0; k0 < 64; k0 += 16) {
-          const uint32_t kr = (k0 / 8) * 1024;
-          tc::mma_bf16(tmem + TM::DA, tc::smem_desc(sb + L::oAqk + s * 8192 + k0 * 2, 16, 1024),
-                       tc::smem_desc(sb + L::oW + kr, 8192, 1024), idO, k0 > 0);
-          tc::mma_bf16(tmem + TM::DS, tc::smem_desc(st + kr, 16384, 1024),
-                       tc::smem_desc(sb + L::oW2 + kr, 8192, 1024), idS, k0 > 0);
+          for (int k0 = 0; k0 < 64; k0 += 16)
+            tc::mma_bf16(tmem + TM::DA, dAqk + ((k0 * 2) >> 4), dW + (((k0 / 8) * 1024) >> 4),
+                         idO, k0 > 0);
+        } else {
+          constexpr uint32_t idS = tc::idesc_bf16(DK, kNV, 1, 1);
+          const uint64_t dW2 = tc::smem_desc(sb + L::oW2, 8192, 1024);
+          const uint64_t dK = tc::smem_desc(st, 16384, 1024);   // K as MN-major A
+#pragma unroll
+          for (int k0 = 0; k0 < 64; k0 += 16) {
+            const uint32_t kr = ((k0 / 8) * 1024) >> 4;
+            tc::mma_bf16(tmem + TM::DS, dK + kr, dW2 + kr, idS, k0 > 0);
+          }
         }
         tc::commit(bar(kM4));
       }

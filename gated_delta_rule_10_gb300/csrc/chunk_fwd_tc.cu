@@ -347,12 +347,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     if (tid == 0) {
       tc::fence_after_sync();
       constexpr uint32_t id = tc::idesc_bf16(128, 64, 0, 0);
+      const uint64_t dEQ = tc::smem_desc(sbase + L::oEQ, 16, 1024);
+      const uint64_t dKb = tc::smem_desc(sbase + L::oKb, 16, 1024);
 #pragma unroll
       for (int k0 = 0; k0 < DK; k0 += 16) {
         const uint32_t ka = (k0 >> 6) * (128 * 128) + (k0 & 63) * 2;
         const uint32_t kb = (k0 >> 6) * (64 * 128) + (k0 & 63) * 2;
-        tc::mma_bf16(tmem + TM::D1, tc::smem_desc(sbase + L::oEQ + ka, 16, 1024),
-                     tc::smem_desc(sbase + L::oKb + kb, 16, 1024), id, k0 > 0);
+        tc::mma_bf16(tmem + TM::D1, dEQ + (ka >> 4), dKb + (kb >> 4), id, k0 > 0);
       }
       tc::commit(bar0);
     }
@@ -406,19 +407,21 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       tc::fence_after_sync();
       constexpr uint32_t idY = tc::idesc_bf16(64, DK, 0, 1);
       constexpr uint32_t idN = tc::idesc_bf16(64, kNV, 0, 1);
+      const uint64_t dA = tc::smem_desc(sbase + L::oA, 16, 1024);
+      const uint64_t dEa = tc::smem_desc(sbase + L::oEa, 64 * 128, 1024);
+      const uint64_t dZ = tc::smem_desc(sbase + L::oZ, 64 * 128, 1024);
+      const uint64_t dQg = tc::smem_desc(sbase + L::oQg, 16, 1024);
+      const uint64_t dS = tc::smem_desc(sbase + L::oS, DK * 128, 1024);
 #pragma unroll
       for (int k0 = 0; k0 < 64; k0 += 16) {
-        const uint64_t ad = tc::smem_desc(sbase + L::oA + k0 * 2, 16, 1024);
-        tc::mma_bf16(tmem + TM::DY, ad, tc::smem_desc(sbase + L::oEa + (k0 / 8) * 1024, 64 * 128, 1024),
-                     idY, k0 > 0);
-        tc::mma_bf16(tmem + TM::DU, ad, tc::smem_desc(sbase + L::oZ + (k0 / 8) * 1024, 64 * 128, 1024),
-                     idN, k0 > 0);
+        const uint32_t kr = ((k0 / 8) * 1024) >> 4;
+        tc::mma_bf16(tmem + TM::DY, dA + ((k0 * 2) >> 4), dEa + kr, idY, k0 > 0);
+        tc::mma_bf16(tmem + TM::DU, dA + ((k0 * 2) >> 4), dZ + kr, idN, k0 > 0);
       }
 #pragma unroll
       for (int k0 = 0; k0 < DK; k0 += 16) {
         const uint32_t ka = (k0 >> 6) * (64 * 128) + (k0 & 63) * 2;
-        tc::mma_bf16(tmem + TM::DO, tc::smem_desc(sbase + L::oQg + ka, 16, 1024),
-                     tc::smem_desc(sbase + L::oS + (k0 / 8) * 1024, DK * 128, 1024), idN, k0 > 0);
+        tc::mma_bf16(tmem + TM::DO, dQg + (ka >> 4), dS + (((k0 / 8) * 1024) >> 4), idN, k0 > 0);
       }
       tc::commit(bar0 + 8);
     }
@@ -446,11 +449,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     if (tid == 0) {
       tc::fence_after_sync();
       constexpr uint32_t idN = tc::idesc_bf16(64, kNV, 0, 1);
+      const uint64_t dY = tc::smem_desc(sbase + L::oY, 16, 1024);
+      const uint64_t dS = tc::smem_desc(sbase + L::oS, DK * 128, 1024);
 #pragma unroll
       for (int k0 = 0; k0 < DK; k0 += 16) {
         const uint32_t ka = (k0 >> 6) * (64 * 128) + (k0 & 63) * 2;
-        tc::mma_bf16(tmem + TM::DU, tc::smem_desc(sbase + L::oY + ka, 16, 1024),
-                     tc::smem_desc(sbase + L::oS + (k0 / 8) * 1024, DK * 128, 1024), idN, 1);
+        tc::mma_bf16(tmem + TM::DU, dY + (ka >> 4), dS + (((k0 / 8) * 1024) >> 4), idN, 1);
       }
       tc::commit(bar0 + 16);
     }
@@ -476,12 +480,14 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       tc::fence_after_sync();
       constexpr uint32_t idO = tc::idesc_bf16(64, kNV, 0, 1);
       constexpr uint32_t idS = tc::idesc_bf16(DK, kNV, 1, 1);
+      const uint64_t dW = tc::smem_desc(sbase + L::oW, 64 * 128, 1024);
+      const uint64_t dAqk = tc::smem_desc(sbase + L::oAqk, 16, 1024);
+      const uint64_t dKt = tc::smem_desc(sbase + L::oKt, 64 * 128, 1024);
 #pragma unroll
       for (int k0 = 0; k0 < 64; k0 += 16) {
-        const uint64_t bd = tc::smem_desc(sbase + L::oW + (k0 / 8) * 1024, 64 * 128, 1024);
-        tc::mma_bf16(tmem + TM::DO, tc::smem_desc(sbase + L::oAqk + k0 * 2, 16, 1024), bd, idO, 1);
-        tc::mma_bf16(tmem + TM::DS, tc::smem_desc(sbase + L::oKt + (k0 / 8) * 1024, 64 * 128, 1024),
-                     bd, idS, k0 > 0);
+        const uint32_t kr = ((k0 / 8) * 1024) >> 4;
+        tc::mma_bf16(tmem + TM::DO, dAqk + ((k0 * 2) >> 4), dW + kr, idO, 1);
+        tc::mma_bf16(tmem + TM::DS, dKt + kr, dW + kr, idS, k0 > 0);
       }
       tc::commit(bar0 + 24);
     }

@@ -36,6 +36,11 @@ __device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t lbo, uint
   return d;
 }
 
+// A descriptor plus a byte offset: the address field holds addr >> 4 in 14
+// bits and shared addresses stay below 2^18, so adding offset >> 4 to the
+// whole descriptor never carries into the other fields. Callers build one
+// descriptor per tile and advance it by constants along K.
+
 // Instruction descriptor of kind::f16: bf16 x bf16 -> fp32, M x N, operand
 // majors (0 = K-major, 1 = MN-major).
 __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, int a_mn, int b_mn) {
