@@ -164,10 +164,14 @@ def run_ours(args):
     o_dec = torch.empty(N, H, dv, dtype=c["dtype"], device=dev)
     stream = torch.cuda.current_stream(dev)
     flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
+    shape = gdr.make_shape(B, T, H, dk, dv, c["dtype"], x["flags"], x["scale"])
+    ws_bytes = gdr.chunk_fwd_workspace_bytes(shape)
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev) if ws_bytes else None
 
     def step():
         gdr.chunk_fwd(xd["q"], xd["k"], xd["v"], xd["g"], xd["beta"], xd["lam"], xd["b"],
-                      xd["w"], xd["h0"], scale=x["scale"], flags=x["flags"], o=o, hT=hT)
+                      xd["w"], xd["h0"], scale=x["scale"], flags=x["flags"], o=o, hT=hT,
+                      workspace=ws)
         for _ in range(args.decode_steps if has_decode else 0):
             gdr.recurrent_step(yd["q"], yd["k"], yd["v"], yd["g"], state, yd["beta"], yd["lam"],
                                yd["b"], yd["w"], scale=y["scale"], flags=y["flags"], o=o_dec)
@@ -187,7 +191,8 @@ def run_ours(args):
         flush.fill_(float(i))
         ev[i][0].record(stream)
         gdr.chunk_fwd(xd["q"], xd["k"], xd["v"], xd["g"], xd["beta"], xd["lam"], xd["b"],
-                      xd["w"], xd["h0"], scale=x["scale"], flags=x["flags"], o=o, hT=hT)
+                      xd["w"], xd["h0"], scale=x["scale"], flags=x["flags"], o=o, hT=hT,
+                      workspace=ws)
         ev[i][1].record(stream)
         for _ in range(args.decode_steps if has_decode else 0):
             gdr.recurrent_step(yd["q"], yd["k"], yd["v"], yd["g"], state, yd["beta"], yd["lam"],

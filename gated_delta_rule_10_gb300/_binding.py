@@ -53,6 +53,7 @@ def lib():
         L = ctypes.CDLL(LIB_PATH)
         sp = ctypes.POINTER(Shape)
         L.gdr_chunk_fwd_workspace.argtypes = [sp, ctypes.POINTER(ctypes.c_size_t)]
+        L.gdr_chunk_fwd_workspace_min.argtypes = [sp, ctypes.POINTER(ctypes.c_size_t)]
         L.gdr_chunk_fwd.argtypes = [sp] + [_vp] * 11 + [_vp, ctypes.c_size_t, _vp]
         L.gdr_recurrent_step.argtypes = [sp] + [_vp] * 10 + [_vp]
         L.gdr_gate_cumsum.argtypes = [ctypes.c_int] * 4 + [_vp, _vp, _vp]
@@ -60,7 +61,8 @@ def lib():
         L.gdr_status_string.argtypes = [ctypes.c_int]
         L.gdr_status_string.restype = ctypes.c_char_p
         L.gdr_abi_version.restype = ctypes.c_int
-        for name in ("gdr_chunk_fwd_workspace", "gdr_chunk_fwd", "gdr_recurrent_step",
+        for name in ("gdr_chunk_fwd_workspace", "gdr_chunk_fwd_workspace_min", "gdr_chunk_fwd",
+                     "gdr_recurrent_step",
                      "gdr_gate_cumsum", "gdr_chunk_fwd_check"):
             getattr(L, name).restype = ctypes.c_int
         _lib = L
@@ -111,11 +113,14 @@ def make_shape(B, T, H, dk, dv, dtype, flags, scale):
                  flags, float(scale))
 
 
-def chunk_fwd_workspace_bytes(shape):
+def chunk_fwd_workspace_bytes(shape, minimum=False):
+    """Workspace bytes for a chunk_fwd call on `shape`: the size that selects the
+    two-kernel path, or with minimum=True the least the call accepts."""
+    name = "gdr_chunk_fwd_workspace_min" if minimum else "gdr_chunk_fwd_workspace"
     n = ctypes.c_size_t(0)
-    st = lib().gdr_chunk_fwd_workspace(ctypes.byref(shape), ctypes.byref(n))
+    st = getattr(lib(), name)(ctypes.byref(shape), ctypes.byref(n))
     if st:
-        raise GdrError(st, "gdr_chunk_fwd_workspace")
+        raise GdrError(st, name)
     return n.value
 
 

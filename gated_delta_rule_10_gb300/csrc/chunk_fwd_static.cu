@@ -64,7 +64,7 @@ extern "C" gdr_status gdr_chunk_fwd_static(const gdr_shape* shape, const void* q
                                            const float* h0, void* o, float* hT,
                                            gdr_stream_t stream) {
   size_t need = 0;
-  const gdr_status st = gdr_chunk_fwd_workspace(shape, &need);
+  const gdr_status st = gdr_chunk_fwd_workspace_min(shape, &need);
   if (st != GDR_OK) return st;
   if (need > kStaticScratchBytes) return GDR_ERR_WORKSPACE;
   void* scratch = nullptr;

@@ -1,0 +1,334 @@
+// Chunk scan kernel of the two-kernel chunkwise forward (bf16 inputs, every
+// gate variant): the cross-chunk state pass of the Gated DeltaNet-2 notes,
+// key design 2, fed by the packets of chunk_prep.cu:
+//
+//   W_n     = U_n - Y_n S_n
+//   O_n     = Q_gamma,n S_n + A_qk,n W_n
+//   S_{n+1} = Diag(gamma_C,n) S_n + K_tail,n^T W_n
+//
+// One CTA owns one (batch, head) and a 64-wide slice of value columns, and
+// walks the chunks in order with S_n (d_k x 64, fp32) in registers, one key
+// channel per thread. Roles (288 threads):
+//   warps 0-3  the state chain: W (tensor memory + U) -> bf16 operand,
+//              S_{n+1} = gamma_C S_n + K_tail^T W -> bf16 operand; thread 0
+//              issues every MMA
+//   warps 4-7  the output: O_n from tensor memory (double-buffered) to o
+//   warp 8     the loader: each chunk's packet into a three-stage ring with
+//              plain bulk copies
+// MMA order per chunk: -Y S_n (commit), Q_gamma S_n, then after W:
+// K_tail^T W (commit), A_qk W (commit), so the chain waits for nothing it
+// does not need. Every wait is bounded; a wait that gives up makes all roles
+// leave together, release tensor memory and report GDR_ERR_TIMEOUT.
+#include "common.cuh"
+#include "kernels.h"
+#include "packet.h"
+#include "tc.cuh"
+
+namespace gdr {
+namespace {
+
+constexpr int kThreads = 288;
+constexpr int kNV = 64;
+constexpr int kStages = 3;
+constexpr uint32_t kTmemCols = 256;
+constexpr uint32_t kChainBar = 1, kOutBar = 2;
+
+// TMEM columns: W = -Y S + ..., S update, two output accumulators
+constexpr uint32_t DW = 0, DS = 64, DO0 = 128;
+
+enum : uint32_t { kFull0 = 0, kEmpty0 = 3, kBW = 6, kBS = 7, kBO0 = 8, kOFree0 = 10, kBars = 12 };
+
+template <int DK>
+struct ScanLayout {
+  using P = Packet<DK, 128>;
+  static constexpr uint32_t kStage = P::kCommon + P::kUSlice;   // common part + U slice
+  static constexpr uint32_t oStage = 0;
+  static constexpr uint32_t oS = kStages * kStage;              // S_n, K=DK x 64 (B, MN-major)
+  static constexpr uint32_t oW = oS + DK * 128;                 // W,   K=64 x 64 (B, MN-major)
+  static constexpr uint32_t oBar = oW + 8192;
+  static constexpr uint32_t oSlot = oBar + kBars * 8;
+  static constexpr uint32_t oAbort = oSlot + 4;
+  static constexpr uint32_t bytes = oAbort + 12;
+  static constexpr uint32_t launch_bytes = bytes + 1024;
+};
+
+__device__ __forceinline__ uint4 pack8(const float* x) {
+  uint4 u;
+  u.x = pack_bf16x2(x[0], x[1]);
+  u.y = pack_bf16x2(x[2], x[3]);
+  u.z = pack_bf16x2(x[4], x[5]);
+  u.w = pack_bf16x2(x[6], x[7]);
+  return u;
+}
+
+__device__ __forceinline__ void unpack8(uint4 u, float* x) {
+  const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&u);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float2 f = __bfloat1622float2(h[i]);
+    x[2 * i] = f.x;
+    x[2 * i + 1] = f.y;
+  }
+}
+
+// Bounded mbarrier wait that also gives up once another role has aborted.
+__device__ __forceinline__ bool wait_or_abort(uint32_t mbar, uint32_t parity,
+                                              volatile int* abort_flag) {
+  for (uint32_t i = 0; i < tc::kMaxPolls; ++i) {
+    if (tc::mbar_try_wait(mbar, parity, tc::kSuspendNs)) return true;
+    if (*abort_flag) return false;
+  }
+  *abort_flag = 1;
+  return false;
+}
+
+template <int DK, int DV>
+__global__ void __launch_bounds__(kThreads, 1)
+    chunk_scan_kernel(const ChunkArgs a, const unsigned char* packets, int* status) {
+  using L = ScanLayout<DK>;
+  using P = Packet<DK, DV>;
+  extern __shared__ unsigned char smem_raw[];
+  unsigned char* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+  const uint32_t sb = smem_u32(smem);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int slice = blockIdx.x, h = blockIdx.y, bb = blockIdx.z;
+  const int T = a.T, H = a.H;
+  const int col0 = slice * kNV;
+  const int n_chunks = (T + kChunk - 1) / kChunk;
+  const unsigned char* pk0 = packets + (size_t(bb) * H + h) * n_chunks * P::bytes;
+  auto bar = [&](uint32_t i) { return sb + L::oBar + 8 * i; };
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::oAbort);
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(smem + L::oSlot);
+
+  if (warp == 0) tc::tmem_alloc(smem_u32(tslot), kTmemCols);
+  if (tid == 32) {
+    for (int s = 0; s < kStages; ++s) {
+      tc::mbar_init(bar(kFull0 + s), 1);
+      tc::mbar_init(bar(kEmpty0 + s), 1);
+    }
+    tc::mbar_init(bar(kBW), 1);
+    tc::mbar_init(bar(kBS), 1);
+    for (int i = 0; i < 2; ++i) {
+      tc::mbar_init(bar(kBO0 + i), 1);
+      tc::mbar_init(bar(kOFree0 + i), 1);
+    }
+    *abort_flag = 0;
+    tc::fence_mbar_init();
+  }
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  const uint32_t tmem = *tslot;
+  const uint32_t tlane = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);
+  int fail = -1;
+
+  if (warp == 8) {
+    // ------------------------------------------------------------ loader
+    int issued = 0;
+    if (lane == 0) {
+      for (int n = 0; n < n_chunks; ++n) {
+        const int s = n % kStages;
+        if (n >= kStages &&
+            !wait_or_abort(bar(kEmpty0 + s), ((n - kStages) / kStages) & 1, abort_flag)) {
+          fail = 4 * n;
+          break;
+        }
+        const uint32_t st = sb + L::oStage + s * L::kStage;
+        const unsigned char* pk = pk0 + size_t(n) * P::bytes;
+        tc::mbar_arrive_expect_tx(bar(kFull0 + s), P::kCommon + P::kUSlice);
+        tc::bulk_load(st, pk, P::kCommon, bar(kFull0 + s));
+        tc::bulk_load(st + P::kCommon, pk + P::oU + slice * P::kUSlice, P::kUSlice,
+                      bar(kFull0 + s));
+        issued = n + 1;
+      }
+      // let the copies already issued land before the CTA can exit
+      for (int n = max(0, issued - kStages); n < issued; ++n)
+        wait_or_abort(bar(kFull0 + n % kStages), (n / kStages) & 1, abort_flag);
+    }
+  } else if (warp < 4) {
+    // ------------------------------------------------------------ state chain
+    const bool owner = (DK == 128) || (lane < 16);
+    const int srow = (DK == 128) ? tid : warp * 16 + (lane & 15);
+    const int wrow = warp * 16 + (lane & 15);   // row of the M=64 accumulators (lanes < 16)
+    float S[kNV];
+    {
+      const size_t base = ((size_t(bb) * H + h) * DK + srow) * DV + col0;
+#pragma unroll
+      for (int j = 0; j < kNV; j += 4) {
+        float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (a.h0 && owner) x = *reinterpret_cast<const float4*>(a.h0 + base + j);
+        S[j] = x.x; S[j + 1] = x.y; S[j + 2] = x.z; S[j + 3] = x.w;
+      }
+      if (owner) {
+#pragma unroll
+        for (int j = 0; j < kNV; j += 8)
+          *reinterpret_cast<uint4*>(smem + L::oS + tc::tile_off(DK, srow, j)) = pack8(S + j);
+      }
+      tc::fence_proxy_async();
+      tc::named_sync(kChainBar, 128);
+    }
+    const uint64_t dS = tc::smem_desc(sb + L::oS, DK * 128, 1024);
+    const uint64_t dW = tc::smem_desc(sb + L::oW, 64 * 128, 1024);
+    for (int n = 0; n < n_chunks; ++n) {
+      const int s = n % kStages;
+      const uint32_t st = sb + L::oStage + s * L::kStage;
+      const unsigned char* sst = smem + L::oStage + s * L::kStage;
+      bool ok = true;
+      // -Y S_n onto D_W (commit), then Q_gamma S_n into D_O[n % 2]
+      if (tid == 0) {
+        ok = wait_or_abort(bar(kFull0 + s), (n / kStages) & 1, abort_flag);
+        if (ok && n >= 2) ok = wait_or_abort(bar(kOFree0 + (n & 1)), ((n - 2) >> 1) & 1, abort_flag);
+        if (ok) {
+          tc::fence_after_sync();
+          constexpr uint32_t idN = tc::idesc_bf16(64, kNV, 0, 1);
+          const uint64_t dY = tc::smem_desc(st + P::oY, 16, 1024);
+          const uint64_t dQ = tc::smem_desc(st + P::oQg, 16, 1024);
+#pragma unroll
+          for (int k0 = 0; k0 < DK; k0 += 16) {
+            const uint32_t ka = (k0 >> 6) * 8192 + (k0 & 63) * 2;
+            tc::mma_bf16(tmem + DW, dY + (ka >> 4), dS + (((k0 / 8) * 1024) >> 4), idN, k0 > 0);
+          }
+          tc::commit(bar(kBW));
+#pragma unroll
+          for (int k0 = 0; k0 < DK; k0 += 16) {
+            const uint32_t ka = (k0 >> 6) * 8192 + (k0 & 63) * 2;
+            tc::mma_bf16(tmem + DO0 + (n & 1) * 64, dQ + (ka >> 4), dS + (((k0 / 8) * 1024) >> 4),
+                         idN, k0 > 0);
+          }
+        }
+      }
+      if (tc::named_any(kChainBar, 128, !ok)) { fail = 4 * n; break; }
+      ok = wait_or_abort(bar(kBW), n & 1, abort_flag);
+      if (tc::named_any(kChainBar, 128, !ok)) { fail = 4 * n + 1; break; }
+      tc::fence_after_sync();
+      const float gc = reinterpret_cast<const float*>(sst + P::oGc)[srow];
+      // W = U + (-Y S_n) -> bf16 operand
+#pragma unroll
+      for (int c = 0; c < kNV; c += 32) {
+        float x[32];
+        tc::tmem_ld32(tlane + DW + c, x);
+        if (lane < 16) {
+#pragma unroll
+          for (int j = 0; j < 32; j += 8) {
+            float u[8];
+            unpack8(*reinterpret_cast<const uint4*>(sst + P::kCommon + tc::tile_off(64, wrow, c + j)), u);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) x[j + i] += u[i];
+            *reinterpret_cast<uint4*>(smem + L::oW + tc::tile_off(64, wrow, c + j)) = pack8(x + j);
+          }
+        }
+      }
+      tc::fence_proxy_async();
+      tc::fence_before_sync();
+      tc::named_sync(kChainBar, 128);
+      // K_tail^T W into D_S (commit), then A_qk W onto D_O[n % 2] (commit)
+      if (tid == 0) {
+        tc::fence_after_sync();
+        constexpr uint32_t idS = tc::idesc_bf16(DK, kNV, 1, 1);
+        constexpr uint32_t idO = tc::idesc_bf16(64, kNV, 0, 1);
+        const uint64_t dKt = tc::smem_desc(st + P::oKt, 64 * 128, 1024);
+        const uint64_t dAqk = tc::smem_desc(st + P::oAqk, 16, 1024);
+#pragma unroll
+        for (int k0 = 0; k0 < 64; k0 += 16) {
+          const uint32_t kr = ((k0 / 8) * 1024) >> 4;
+          tc::mma_bf16(tmem + DS, dKt + kr, dW + kr, idS, k0 > 0);
+        }
+        tc::commit(bar(kBS));
+#pragma unroll
+        for (int k0 = 0; k0 < 64; k0 += 16)
+          tc::mma_bf16(tmem + DO0 + (n & 1) * 64, dAqk + ((k0 * 2) >> 4),
+                       dW + (((k0 / 8) * 1024) >> 4), idO, 1);
+        tc::commit(bar(kBO0 + (n & 1)));
+      }
+      ok = wait_or_abort(bar(kBS), n & 1, abort_flag);
+      if (tc::named_any(kChainBar, 128, !ok)) { fail = 4 * n + 2; break; }
+      tc::fence_after_sync();
+      // S_{n+1} = Diag(gamma_C) S_n + K_tail^T W
+#pragma unroll
+      for (int c = 0; c < kNV; c += 32) {
+        float x[32];
+        tc::tmem_ld32(tlane + DS + c, x);
+#pragma unroll
+        for (int j = 0; j < 32; ++j) S[c + j] = gc * S[c + j] + x[j];
+        if (owner) {
+#pragma unroll
+          for (int j = 0; j < 32; j += 8)
+            *reinterpret_cast<uint4*>(smem + L::oS + tc::tile_off(DK, srow, c + j)) = pack8(S + c + j);
+        }
+      }
+      tc::fence_proxy_async();
+      tc::fence_before_sync();
+      tc::named_sync(kChainBar, 128);
+    }
+    if (fail < 0 && a.hT && owner) {
+      const size_t base = ((size_t(bb) * H + h) * DK + srow) * DV + col0;
+#pragma unroll
+      for (int j = 0; j < kNV; j += 4)
+        *reinterpret_cast<float4*>(a.hT + base + j) = make_float4(S[j], S[j + 1], S[j + 2], S[j + 3]);
+    }
+  } else {
+    // ------------------------------------------------------------ output
+    const int orow = (warp & 3) * 16 + (lane & 15);
+    for (int n = 0; n < n_chunks; ++n) {
+      const bool ok = wait_or_abort(bar(kBO0 + (n & 1)), (n >> 1) & 1, abort_flag);
+      if (tc::named_any(kOutBar, 128, !ok)) { fail = 4 * n + 3; break; }
+      tc::fence_after_sync();
+      const int t0 = n * kChunk;
+      const int Lr = min(kChunk, T - t0);
+      __nv_bfloat16* op = static_cast<__nv_bfloat16*>(a.o) +
+                          ((size_t(bb) * T + t0 + orow) * H + h) * DV + col0;
+#pragma unroll
+      for (int c = 0; c < kNV; c += 32) {
+        float x[32];
+        tc::tmem_ld32(tlane + DO0 + (n & 1) * 64 + c, x);
+        if (lane < 16 && orow < Lr) {
+#pragma unroll
+          for (int j = 0; j < 32; j += 8) *reinterpret_cast<uint4*>(op + c + j) = pack8(x + j);
+        }
+      }
+      tc::fence_before_sync();
+      tc::named_sync(kOutBar, 128);
+      if (tid == 128) {
+        tc::mbar_arrive(bar(kOFree0 + (n & 1)));
+        tc::mbar_arrive(bar(kEmpty0 + n % kStages));
+      }
+    }
+  }
+
+  if (fail >= 0 && status && lane == 0) {
+    if (atomicCAS(status, 0, 5) == 0) {  // GDR_ERR_TIMEOUT
+      status[1] = static_cast<int>((blockIdx.z * gridDim.y + blockIdx.y) * gridDim.x + blockIdx.x);
+      status[2] = fail;
+    }
+  }
+  tc::fence_before_sync();
+  __syncthreads();
+  if (warp == 0) tc::tmem_dealloc(tmem, kTmemCols);
+}
+
+template <int DK, int DV>
+cudaError_t launch_scan(const ChunkArgs& a, const unsigned char* packets, int* status,
+                        cudaStream_t stream) {
+  using L = ScanLayout<DK>;
+  static_assert(L::launch_bytes <= 232448, "shared memory budget of one CTA");
+  auto kern = chunk_scan_kernel<DK, DV>;
+  cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(L::launch_bytes));
+  if (err != cudaSuccess) return err;
+  dim3 grid(DV / kNV, a.H, a.B);
+  kern<<<grid, kThreads, L::launch_bytes, stream>>>(a, packets, status);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_chunk_scan(const ChunkArgs& a, int dk, const unsigned char* packets,
+                              int* status, cudaStream_t stream) {
+  if (dk == 64 && a.dv == 64) return launch_scan<64, 64>(a, packets, status, stream);
+  if (dk == 64 && a.dv == 128) return launch_scan<64, 128>(a, packets, status, stream);
+  if (dk == 128 && a.dv == 64) return launch_scan<128, 64>(a, packets, status, stream);
+  if (dk == 128 && a.dv == 128) return launch_scan<128, 128>(a, packets, status, stream);
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace gdr

@@ -8,6 +8,7 @@
 
 #include "gdr.h"
 #include "kernels.h"
+#include "packet.h"
 #include "tma.h"
 
 namespace {
@@ -48,6 +49,7 @@ gdr_status check_gates(const gdr_shape* s, const void* q, const void* k, const v
     return GDR_ERR_INVALID_ARG;
   if (!aligned(g, 4) || (beta && !aligned(beta, 4)) || (lam && !aligned(lam, 4)))
     return GDR_ERR_INVALID_ARG;
+  if ((f & GDR_DECAY_CHANNEL) && !aligned(g, 16)) return GDR_ERR_INVALID_ARG;   // vector loads
   if ((f & GDR_ERASE_CHANNEL) && !aligned(b, 16)) return GDR_ERR_INVALID_ARG;
   if ((f & GDR_WRITE_CHANNEL) && !aligned(w, 16)) return GDR_ERR_INVALID_ARG;
   return GDR_OK;
@@ -75,8 +77,22 @@ gdr_status gdr_chunk_fwd_workspace(const gdr_shape* shape, size_t* bytes) {
   if (!bytes) return GDR_ERR_INVALID_ARG;
   const gdr_status st = check_shape(shape, false);
   if (st != GDR_OK) return st;
-  // the fused kernels keep every intermediate on chip; the tensor-core kernel
-  // only needs its status words
+  // bf16: the status words, then one packet per chunk of every (batch, head)
+  // for the two-kernel path; fp32 needs nothing
+  if (shape->dtype != GDR_BF16) {
+    *bytes = 0;
+    return GDR_OK;
+  }
+  const size_t chunks = static_cast<size_t>(shape->B) * shape->H *
+                        static_cast<size_t>((shape->T + gdr::kChunkLen - 1) / gdr::kChunkLen);
+  *bytes = gdr::kChunkWorkspaceBytes + chunks * gdr::packet_bytes(shape->dk, shape->dv);
+  return GDR_OK;
+}
+
+gdr_status gdr_chunk_fwd_workspace_min(const gdr_shape* shape, size_t* bytes) {
+  if (!bytes) return GDR_ERR_INVALID_ARG;
+  const gdr_status st = check_shape(shape, false);
+  if (st != GDR_OK) return st;
   *bytes = shape->dtype == GDR_BF16 ? gdr::kChunkWorkspaceBytes : 0;
   return GDR_OK;
 }
@@ -90,9 +106,10 @@ gdr_status gdr_chunk_fwd(const gdr_shape* shape, const void* q, const void* k, c
   st = check_gates(shape, q, k, v, g, beta, lam, b, w, o);
   if (st != GDR_OK) return st;
   if ((h0 && !aligned(h0, 16)) || (hT && !aligned(hT, 16))) return GDR_ERR_INVALID_ARG;
-  size_t need = 0;
-  gdr_chunk_fwd_workspace(shape, &need);
-  if (need > 0 && (!workspace || ws_bytes < need || !aligned(workspace, 16)))
+  size_t need_min = 0, need_full = 0;
+  gdr_chunk_fwd_workspace_min(shape, &need_min);
+  gdr_chunk_fwd_workspace(shape, &need_full);
+  if (need_min > 0 && (!workspace || ws_bytes < need_min || !aligned(workspace, 16)))
     return GDR_ERR_WORKSPACE;
 
   const bool f32 = shape->dtype == GDR_F32;
@@ -109,7 +126,12 @@ gdr_status gdr_chunk_fwd(const gdr_shape* shape, const void* q, const void* k, c
     int* status = static_cast<int*>(workspace);
     err = cudaMemsetAsync(status, 0, gdr::kStatusWords * sizeof(int), st_);
     if (err == cudaSuccess) {
-      if (gdr::chunk_fwd_pipe_supports(shape->flags)) {
+      if (ws_bytes >= need_full) {
+        // two kernels: every chunk's intra-chunk work in parallel, then the state pass
+        unsigned char* packets = static_cast<unsigned char*>(workspace) + gdr::kChunkWorkspaceBytes;
+        err = gdr::launch_chunk_prep(a, shape->dk, packets, status, st_);
+        if (err == cudaSuccess) err = gdr::launch_chunk_scan(a, shape->dk, packets, status, st_);
+      } else if (gdr::chunk_fwd_pipe_supports(shape->flags)) {
         CUtensorMap tq, tk, tv;
         if (!gdr::make_bthd_tmap(&tq, q, shape->B, shape->T, shape->H, shape->dk) ||
             !gdr::make_bthd_tmap(&tk, k, shape->B, shape->T, shape->H, shape->dk) ||

@@ -60,6 +60,13 @@ bool chunk_fwd_pipe_supports(unsigned flags);
 cudaError_t launch_chunk_fwd_pipe(const ChunkArgs& a, int dk, const CUtensorMap& tq,
                                   const CUtensorMap& tk, const CUtensorMap& tv, int* status,
                                   cudaStream_t stream);
+// bf16 inputs, two-kernel path: the chunk preparation kernel writes one packet
+// per chunk (packet.h) into `packets`, then the chunk scan kernel runs the
+// state pass over them. `packets` holds B * H * ceil(T / 64) packets.
+cudaError_t launch_chunk_prep(const ChunkArgs& a, int dk, unsigned char* packets, int* status,
+                              cudaStream_t stream);
+cudaError_t launch_chunk_scan(const ChunkArgs& a, int dk, const unsigned char* packets,
+                              int* status, cudaStream_t stream);
 cudaError_t launch_recurrent_step(const StepArgs& a, int dk, int dv, bool f32,
                                   cudaStream_t stream);
 cudaError_t launch_gate_cumsum(const float* g, float* G, int B, int T, int X,

@@ -94,9 +94,25 @@ typedef struct {
   float scale;      /* read-out scale on q (d_k^-1/2 in the KDA derivation) */
 } gdr_shape;
 
-/* Device workspace bytes gdr_chunk_fwd needs for `shape` (may be 0).
- * Returns GDR_ERR_INVALID_ARG / GDR_ERR_UNSUPPORTED for a bad shape. */
+/* Device workspace bytes for gdr_chunk_fwd on `shape` (may be 0).
+ *
+ * gdr_chunk_fwd_workspace gives the size that selects the fastest path. For
+ * bf16 inputs that is the two-kernel path: one kernel does the intra-chunk
+ * work of every chunk of every (batch, head) in parallel and writes a packet
+ * per chunk (Q_gamma, -Y, K_tail, A_qk, gamma_C, U: 3 * 128 d_k + 128 d_v +
+ * 9216 bytes, 74752 at d_k = d_v = 128) into the workspace; a second kernel
+ * runs the state pass over the packets. Total: 256 + B * H * ceil(T / 64) *
+ * packet bytes.
+ *
+ * gdr_chunk_fwd_workspace_min gives the least a call accepts (256 bytes for
+ * bf16: the status words). A bf16 call whose workspace is at least that but
+ * smaller than the full size runs the single-kernel path, which keeps every
+ * intermediate on chip and is slower when B * H is small. Both paths compute
+ * the same result up to rounding. fp32 inputs need no workspace.
+ *
+ * Both return GDR_ERR_INVALID_ARG / GDR_ERR_UNSUPPORTED for a bad shape. */
 gdr_status gdr_chunk_fwd_workspace(const gdr_shape* shape, size_t* bytes);
+gdr_status gdr_chunk_fwd_workspace_min(const gdr_shape* shape, size_t* bytes);
 
 /*
  * Chunkwise-parallel forward (Gated DeltaNet-2 notes, key design 2; the
@@ -109,7 +125,8 @@ gdr_status gdr_chunk_fwd_workspace(const gdr_shape* shape, size_t* bytes);
  * recurrence above up to rounding.
  *
  *   q, k   [B,T,H,d_k] dtype      v, o  [B,T,H,d_v] dtype
- *   g      [B,T,H] fp32, or [B,T,H,d_k] under GDR_DECAY_CHANNEL
+ *   g      [B,T,H] fp32, or [B,T,H,d_k] under GDR_DECAY_CHANNEL (then
+ *          16-byte aligned)
  *   beta   [B,T,H] fp32; required unless both ERASE and WRITE are set
  *          (then ignored)
  *   lam    [B,T,H] fp32; required under GDR_QMIX, ignored otherwise
@@ -118,10 +135,11 @@ gdr_status gdr_chunk_fwd_workspace(const gdr_shape* shape, size_t* bytes);
  *   h0     [B,H,d_k,d_v] fp32 initial state, or NULL for the zero state
  *   hT     [B,H,d_k,d_v] fp32 final state (written), or NULL
  *   workspace, ws_bytes: device memory of at least
- *          gdr_chunk_fwd_workspace() bytes, 16-byte aligned (NULL allowed
- *          when that is 0). It holds the call's status words, which are
- *          cleared on `stream` before the kernel runs: calls sharing one
- *          workspace must be ordered on the stream.
+ *          gdr_chunk_fwd_workspace_min() bytes, 16-byte aligned (NULL allowed
+ *          when that is 0); gdr_chunk_fwd_workspace() bytes select the
+ *          two-kernel path. It holds the call's status words, which are
+ *          cleared on `stream` before the kernels run, and the packets:
+ *          calls sharing one workspace must be ordered on the stream.
  *
  * h0 and hT may be the same buffer (streaming: the state read for a (batch,
  * head) is consumed before that (batch, head)'s final state is written); no
@@ -151,10 +169,11 @@ gdr_status gdr_chunk_fwd_check(const void* workspace, gdr_stream_t stream,
  * framework owns every allocation, a loop where cudaMalloc could block or
  * synchronise the device). It has no counterpart on the pages: it exists for
  * such callers only. The library compiles in a small scratch area (256
- * bytes; a shape that would need more is rejected with GDR_ERR_WORKSPACE)
- * that every GPU using the library holds until the process exits, and passes
- * it where gdr_chunk_fwd takes a workspace; arguments, layouts and results
- * are otherwise those of gdr_chunk_fwd. All calls on a device share that
+ * bytes, the minimum workspace; a shape whose minimum is larger is rejected
+ * with GDR_ERR_WORKSPACE) that every GPU using the library holds until the
+ * process exits, and passes it where gdr_chunk_fwd takes a workspace, so bf16
+ * calls run the single-kernel path; arguments, layouts and results are
+ * otherwise those of gdr_chunk_fwd. All calls on a device share that
  * scratch, which keeps what the last call left; each call clears the status
  * words it needs on `stream` first. Calls whose work overlaps on the GPU race
  * on the scratch, so order them on one stream. A device-side timeout is

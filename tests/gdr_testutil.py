@@ -52,12 +52,14 @@ def rel_err(got, ref):
     return float(np.max(np.abs(got - ref)) / max(np.max(np.abs(ref)), 1e-30))
 
 
-def gpu_forward(x, **kw):
-    """The chunked forward through the C ABI; checks the call's status words."""
+def gpu_forward(x, single_kernel=False, **kw):
+    """The chunked forward through the C ABI; checks the call's status words.
+    bf16 runs the two-kernel path, or with single_kernel=True the minimum
+    workspace and so the single-kernel path."""
     import gated_delta_rule_10_gb300 as gdr
     d = to_dev(x)
     shape = gdr.make_shape(*d["q"].shape, d["v"].shape[-1], d["q"].dtype, x["flags"], x["scale"])
-    n = gdr.chunk_fwd_workspace_bytes(shape)
+    n = gdr.chunk_fwd_workspace_bytes(shape, minimum=single_kernel)
     ws = torch.empty(n, dtype=torch.uint8, device="cuda") if n else None
     out = gdr.chunk_fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], d["lam"], d["b"], d["w"],
                         d["h0"], scale=x["scale"], flags=x["flags"], workspace=ws, **kw)

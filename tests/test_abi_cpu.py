@@ -73,7 +73,18 @@ def _shape(**kw):
 def test_workspace_query(L):
     n = ctypes.c_size_t(123)
     assert L.gdr_chunk_fwd_workspace(ctypes.byref(_shape()), ctypes.byref(n)) == 0
-    assert n.value == 256                      # bf16: the tensor-core kernel's status words
+    # bf16: status words + one packet per chunk: Q_gamma, -Y, K_tail (64 x d_k bf16 each),
+    # A_qk (64 x 64 bf16), gamma_C (1 KB), U (64 x d_v bf16)
+    assert n.value == 256 + 3 * 64 * 64 * 2 + 8192 + 1024 + 64 * 64 * 2
+    s = _shape(B=2, T=130, H=3, dk=128, dv=128)
+    assert L.gdr_chunk_fwd_workspace(ctypes.byref(s), ctypes.byref(n)) == 0
+    assert n.value == 256 + 2 * 3 * 3 * 74752
+    assert L.gdr_chunk_fwd_workspace_min(ctypes.byref(s), ctypes.byref(n)) == 0
+    assert n.value == 256                      # the single-kernel path: status words only
+    assert L.gdr_chunk_fwd_workspace_min(ctypes.byref(_shape(dtype=_binding.GDR_F32)),
+                                         ctypes.byref(n)) == 0
+    assert n.value == 0
+    assert L.gdr_chunk_fwd_workspace_min(ctypes.byref(_shape(dk=96)), ctypes.byref(n)) == 2
     assert L.gdr_chunk_fwd_workspace(ctypes.byref(_shape(dtype=_binding.GDR_F32)),
                                      ctypes.byref(n)) == 0
     assert n.value == 0
@@ -116,6 +127,7 @@ def test_chunk_fwd_rejects_bad_arguments_synchronously(L):
     assert _call_chunk(L, s, q=FAKE + 8) == 1                       # 16-byte alignment
     assert _call_chunk(L, s, h0=FAKE + 4) == 1
     assert _call_chunk(L, s, g=FAKE + 2) == 1
+    assert _call_chunk(L, _shape(flags=gdr.DECAY_CHANNEL), g=FAKE + 4) == 1   # vector loads
     assert _call_chunk(L, _shape(dk=32)) == 2
     assert _call_chunk(L, _shape(dv=256)) == 2
     assert _call_chunk(L, _shape(H=0)) == 1

@@ -47,6 +47,34 @@ def test_every_flag_combination(flags, dtype):
     check(x)
 
 
+# bf16 has two paths: the two-kernel one (full workspace, used above) and the
+# single-kernel one (minimum workspace); both must meet the same bar.
+@pytest.mark.parametrize("dk,dv", [(64, 64), (128, 128), (64, 128), (128, 64)])
+@pytest.mark.parametrize("T", [1, 65, 130])
+@pytest.mark.parametrize("variant", VARIANTS)
+def test_single_kernel_path_small_shapes(variant, T, dk, dv):
+    x = wl.make_inputs(variant, 2, T, 3, dk, dv, torch.bfloat16, seed=T + dk + 7 * dv + 1,
+                       h0_std=0.05)
+    check(x, single_kernel=True)
+
+
+@pytest.mark.parametrize("flags", range(16))
+def test_single_kernel_path_every_flag_combination(flags):
+    x = wl.make_inputs(flags, 1, 200, 2, 128, 128, torch.bfloat16, seed=300 + flags, h0_std=0.05)
+    check(x, single_kernel=True)
+
+
+@pytest.mark.parametrize("variant", VARIANTS)
+def test_two_paths_agree(variant):
+    """Same inputs through both bf16 paths: each within the bar of the other."""
+    x = wl.make_inputs(variant, 2, 333, 4, 128, 128, torch.bfloat16, seed=77, h0_std=0.02)
+    o1, h1 = gpu_forward(x)
+    o2, h2 = gpu_forward(x, single_kernel=True)
+    torch.cuda.synchronize()
+    assert rel_err(o1.float().cpu(), o2.float().cpu().double().numpy()) <= TOL[torch.bfloat16]
+    assert rel_err(h1.cpu(), h2.cpu().double().numpy()) <= TOL[torch.bfloat16]
+
+
 def test_zero_initial_state_and_no_final_state():
     x = wl.make_inputs("kda", 1, 200, 2, 128, 128, torch.bfloat16, seed=5)
     o, hT = gpu_forward(x, output_final_state=False)
