@@ -184,9 +184,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       __syncwarp();
       if (lane == 0) tc::mbar_arrive(bar(kFull0 + s));
     }
-    // let the loads already issued land before the CTA can exit
+    // let the loads already issued land before the CTA can exit (a plain
+    // bounded wait: an abort elsewhere does not stop a copy in flight)
     for (int n = max(0, issued - 2); n < issued; ++n)
-      wait_or_abort(bar(kFull0 + (n & 1)), (n >> 1) & 1, abort_flag);
+      tc::mbar_wait(bar(kFull0 + (n & 1)), (n >> 1) & 1);
   } else if (warp >= 4) {
     // ------------------------------------------------------------ intra-chunk
     const int it = tid - 128;          // 0 .. 255

@@ -16,6 +16,7 @@
 //           T = tril(D1[0:64], -1) (fp32), A_qk = tril(D1[64:128], 0) -> packet
 //   UT      A = (I + T)^{-1}                   (blocked forward substitution)
 //   M2      Y = A E_abs, U = A Z                (M=64, N=d_k and d_v) -> packet (-Y, U)
+// The packet layout is in packet.h.
 // Operands live in shared memory in the 128-byte swizzle of tc.cuh; packet
 // tiles go from registers straight to global memory in the same byte layout.
 #include "common.cuh"
@@ -189,7 +190,7 @@ __device__ __forceinline__ void prep_keys(unsigned char* smem, unsigned char* pk
       st16(smem, L::oEQ + tc::tile_off(128, 64 + r, c0), pack8(Qr));
       st16(smem, L::oKb + tc::tile_off(64, r, c0), pack8(Kb));
       st16(smem, L::oEa + tc::tile_off(64, r, c0), pack8(Ea));
-      st16(pkt, P::oQg + tc::tile_off(64, r, c0), pack8(Qg));
+      st16(pkt, P::oQY + tc::tile_off(128, r, c0), pack8(Qg));
       st16(pkt, P::oKt + tc::tile_off(64, r, c0), pack8(Kt));
     }
   }
@@ -410,7 +411,8 @@ __global__ void __launch_bounds__(kThreads, 2)
         for (int j = 0; j < 32; ++j) x[j] = -x[j];
         if (lane < 16) {
 #pragma unroll
-          for (int j = 0; j < 32; j += 8) st16(pkt, P::oY + tc::tile_off(64, r, c + j), pack8(x + j));
+          for (int j = 0; j < 32; j += 8)
+            st16(pkt, P::oQY + tc::tile_off(128, 64 + r, c + j), pack8(x + j));
         }
       }
 #pragma unroll

@@ -8,17 +8,24 @@
 //
 // One CTA owns one (batch, head) and a 64-wide slice of value columns, and
 // walks the chunks in order with S_n (d_k x 64, fp32) in registers, one key
-// channel per thread. Roles (288 threads):
-//   warps 0-3  the state chain: W (tensor memory + U) -> bf16 operand,
-//              S_{n+1} = gamma_C S_n + K_tail^T W -> bf16 operand; thread 0
-//              issues every MMA
-//   warps 4-7  the output: O_n from tensor memory (double-buffered) to o
-//   warp 8     the loader: each chunk's packet into a three-stage ring with
-//              plain bulk copies
-// MMA order per chunk: -Y S_n (commit), Q_gamma S_n, then after W:
-// K_tail^T W (commit), A_qk W (commit), so the chain waits for nothing it
-// does not need. Every wait is bounded; a wait that gives up makes all roles
-// leave together, release tensor memory and report GDR_ERR_TIMEOUT.
+// channel per thread. Issuing a tensor-core instruction costs far more than
+// these small products take to run, so each chunk uses three MMA groups:
+//   MMA1  [Q_gamma; -Y] S_n  -> D1[n%2]   (M=128: Q_gamma S_n in lanes 0..63,
+//                                          -Y S_n in lanes 64..127)
+//   MMA2  K_tail^T W         -> D_S       (after W = U + lanes 64..127)
+//   MMA3  [A_qk; *] W        += D1[n%2]   (lanes 0..63 become O_n; the rows
+//                                          below A_qk read the U block that
+//                                          follows it in the stage and only
+//                                          touch lanes 64..127, already consumed
+//                                          and overwritten by the next MMA1)
+// Roles (192 threads):
+//   warps 0-3  the state chain; thread 0 issues MMA1 and MMA2; warps 2-3 form
+//              W; all four update S_{n+1} = gamma_C S_n + D_S
+//   warps 4-5  the output: thread 128 issues MMA3, both warps move O_n from
+//              D1[n%2] to o, and thread 128 refills the three-stage packet
+//              ring with plain bulk copies
+// Every wait is bounded; a wait that gives up makes all roles leave together,
+// release tensor memory and report GDR_ERR_TIMEOUT.
 #include "common.cuh"
 #include "kernels.h"
 #include "packet.h"
@@ -27,16 +34,18 @@
 namespace gdr {
 namespace {
 
-constexpr int kThreads = 288;
+constexpr int kThreads = 192;
 constexpr int kNV = 64;
 constexpr int kStages = 3;
 constexpr uint32_t kTmemCols = 256;
 constexpr uint32_t kChainBar = 1, kOutBar = 2;
 
-// TMEM columns: W = -Y S + ..., S update, two output accumulators
-constexpr uint32_t DW = 0, DS = 64, DO0 = 128;
+// TMEM columns: two stacked [O; W] accumulators (M=128), the state update
+constexpr uint32_t D10 = 0, DS = 128;
 
-enum : uint32_t { kFull0 = 0, kEmpty0 = 3, kBW = 6, kBS = 7, kBO0 = 8, kOFree0 = 10, kBars = 12 };
+enum : uint32_t {
+  kFull0 = 0, kEmpty0 = 3, kBW = 6, kWReady = 7, kBS = 8, kBO0 = 9, kOFree0 = 11, kBars = 13
+};
 
 template <int DK>
 struct ScanLayout {
@@ -74,6 +83,7 @@ __device__ __forceinline__ void unpack8(uint4 u, float* x) {
 // Bounded mbarrier wait that also gives up once another role has aborted.
 __device__ __forceinline__ bool wait_or_abort(uint32_t mbar, uint32_t parity,
                                               volatile int* abort_flag) {
+  if (tc::mbar_test(mbar, parity)) return true;
   for (uint32_t i = 0; i < tc::kMaxPolls; ++i) {
     if (tc::mbar_try_wait(mbar, parity, tc::kSuspendNs)) return true;
     if (*abort_flag) return false;
@@ -104,9 +114,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (tid == 32) {
     for (int s = 0; s < kStages; ++s) {
       tc::mbar_init(bar(kFull0 + s), 1);
-      tc::mbar_init(bar(kEmpty0 + s), 1);
+      tc::mbar_init(bar(kEmpty0 + s), 2);   // chain and output each release the stage
     }
     tc::mbar_init(bar(kBW), 1);
+    tc::mbar_init(bar(kWReady), 1);
     tc::mbar_init(bar(kBS), 1);
     for (int i = 0; i < 2; ++i) {
       tc::mbar_init(bar(kBO0 + i), 1);
@@ -122,34 +133,22 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tlane = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);
   int fail = -1;
 
-  if (warp == 8) {
-    // ------------------------------------------------------------ loader
-    int issued = 0;
-    if (lane == 0) {
-      for (int n = 0; n < n_chunks; ++n) {
-        const int s = n % kStages;
-        if (n >= kStages &&
-            !wait_or_abort(bar(kEmpty0 + s), ((n - kStages) / kStages) & 1, abort_flag)) {
-          fail = 4 * n;
-          break;
-        }
-        const uint32_t st = sb + L::oStage + s * L::kStage;
-        const unsigned char* pk = pk0 + size_t(n) * P::bytes;
-        tc::mbar_arrive_expect_tx(bar(kFull0 + s), P::kCommon + P::kUSlice);
-        tc::bulk_load(st, pk, P::kCommon, bar(kFull0 + s));
-        tc::bulk_load(st + P::kCommon, pk + P::oU + slice * P::kUSlice, P::kUSlice,
-                      bar(kFull0 + s));
-        issued = n + 1;
-      }
-      // let the copies already issued land before the CTA can exit
-      for (int n = max(0, issued - kStages); n < issued; ++n)
-        wait_or_abort(bar(kFull0 + n % kStages), (n / kStages) & 1, abort_flag);
-    }
-  } else if (warp < 4) {
+  // packet of chunk n into its ring stage (thread 128 only)
+  auto load_chunk = [&](int n) {
+    const int s = n % kStages;
+    const uint32_t st = sb + L::oStage + s * L::kStage;
+    const unsigned char* pk = pk0 + size_t(n) * P::bytes;
+    tc::mbar_arrive_expect_tx(bar(kFull0 + s), P::kCommon + P::kUSlice);
+    tc::bulk_load(st, pk, P::kCommon, bar(kFull0 + s));
+    tc::bulk_load(st + P::kCommon, pk + P::oU + slice * P::kUSlice, P::kUSlice, bar(kFull0 + s));
+  };
+
+  if (warp < 4) {
     // ------------------------------------------------------------ state chain
     const bool owner = (DK == 128) || (lane < 16);
     const int srow = (DK == 128) ? tid : warp * 16 + (lane & 15);
-    const int wrow = warp * 16 + (lane & 15);   // row of the M=64 accumulators (lanes < 16)
+    const bool wrole = warp >= 2;               // warps 2-3 hold lanes 64..127 = -Y S_n
+    const int wrow = tid - 64;                  // token row of W for those warps
     float S[kNV];
     {
       const size_t base = ((size_t(bb) * H + h) * DK + srow) * DV + col0;
@@ -173,92 +172,88 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int s = n % kStages;
       const uint32_t st = sb + L::oStage + s * L::kStage;
       const unsigned char* sst = smem + L::oStage + s * L::kStage;
+      const uint32_t d1 = tmem + D10 + (n & 1) * 64;
       bool ok = true;
-      // -Y S_n onto D_W (commit), then Q_gamma S_n into D_O[n % 2]
       if (tid == 0) {
+        // MMA1 once the packet has landed and D1[n%2] has been read out (chunk n-2)
         ok = wait_or_abort(bar(kFull0 + s), (n / kStages) & 1, abort_flag);
-        if (ok && n >= 2) ok = wait_or_abort(bar(kOFree0 + (n & 1)), ((n - 2) >> 1) & 1, abort_flag);
+        if (ok && n >= 2)
+          ok = wait_or_abort(bar(kOFree0 + (n & 1)), ((n - 2) >> 1) & 1, abort_flag);
         if (ok) {
           tc::fence_after_sync();
-          constexpr uint32_t idN = tc::idesc_bf16(64, kNV, 0, 1);
-          const uint64_t dY = tc::smem_desc(st + P::oY, 16, 1024);
-          const uint64_t dQ = tc::smem_desc(st + P::oQg, 16, 1024);
+          constexpr uint32_t id1 = tc::idesc_bf16(128, kNV, 0, 1);
+          const uint64_t dQY = tc::smem_desc(st + P::oQY, 16, 1024);
 #pragma unroll
           for (int k0 = 0; k0 < DK; k0 += 16) {
-            const uint32_t ka = (k0 >> 6) * 8192 + (k0 & 63) * 2;
-            tc::mma_bf16(tmem + DW, dY + (ka >> 4), dS + (((k0 / 8) * 1024) >> 4), idN, k0 > 0);
+            const uint32_t ka = (k0 >> 6) * 16384 + (k0 & 63) * 2;
+            tc::mma_bf16(d1, dQY + (ka >> 4), dS + (((k0 / 8) * 1024) >> 4), id1, k0 > 0);
           }
           tc::commit(bar(kBW));
-#pragma unroll
-          for (int k0 = 0; k0 < DK; k0 += 16) {
-            const uint32_t ka = (k0 >> 6) * 8192 + (k0 & 63) * 2;
-            tc::mma_bf16(tmem + DO0 + (n & 1) * 64, dQ + (ka >> 4), dS + (((k0 / 8) * 1024) >> 4),
-                         idN, k0 > 0);
-          }
         }
       }
       if (tc::named_any(kChainBar, 128, !ok)) { fail = 4 * n; break; }
-      ok = wait_or_abort(bar(kBW), n & 1, abort_flag);
+      // gamma_C and this thread's row of U, read while MMA1 runs; W is
+      // rewritten below only after MMA3 of chunk n-1 (which reads it) is done
+      const float gc = reinterpret_cast<const float*>(sst + P::oGc)[srow];
+      uint4 ur[kNV / 8];
+      if (wrole) {
+#pragma unroll
+        for (int j = 0; j < kNV / 8; ++j)
+          ur[j] = *reinterpret_cast<const uint4*>(sst + P::kCommon + tc::tile_off(64, wrow, 8 * j));
+      }
+      if (n >= 1) ok = wait_or_abort(bar(kBO0 + ((n - 1) & 1)), ((n - 1) >> 1) & 1, abort_flag);
+      if (ok) ok = wait_or_abort(bar(kBW), n & 1, abort_flag);
       if (tc::named_any(kChainBar, 128, !ok)) { fail = 4 * n + 1; break; }
       tc::fence_after_sync();
-      const float gc = reinterpret_cast<const float*>(sst + P::oGc)[srow];
       // W = U + (-Y S_n) -> bf16 operand
+      if (wrole) {
+        float x[kNV];
+        tc::tmem_ld64(tlane + D10 + (n & 1) * 64, x);
 #pragma unroll
-      for (int c = 0; c < kNV; c += 32) {
-        float x[32];
-        tc::tmem_ld32(tlane + DW + c, x);
-        if (lane < 16) {
+        for (int j = 0; j < kNV / 8; ++j) {
+          float u[8];
+          unpack8(ur[j], u);
 #pragma unroll
-          for (int j = 0; j < 32; j += 8) {
-            float u[8];
-            unpack8(*reinterpret_cast<const uint4*>(sst + P::kCommon + tc::tile_off(64, wrow, c + j)), u);
-#pragma unroll
-            for (int i = 0; i < 8; ++i) x[j + i] += u[i];
-            *reinterpret_cast<uint4*>(smem + L::oW + tc::tile_off(64, wrow, c + j)) = pack8(x + j);
-          }
+          for (int i = 0; i < 8; ++i) x[8 * j + i] += u[i];
+          *reinterpret_cast<uint4*>(smem + L::oW + tc::tile_off(64, wrow, 8 * j)) = pack8(x + 8 * j);
         }
       }
       tc::fence_proxy_async();
       tc::fence_before_sync();
       tc::named_sync(kChainBar, 128);
-      // K_tail^T W into D_S (commit), then A_qk W onto D_O[n % 2] (commit)
+      // MMA2: K_tail^T W into D_S; then let the output role issue MMA3
       if (tid == 0) {
         tc::fence_after_sync();
-        constexpr uint32_t idS = tc::idesc_bf16(DK, kNV, 1, 1);
-        constexpr uint32_t idO = tc::idesc_bf16(64, kNV, 0, 1);
+        constexpr uint32_t id2 = tc::idesc_bf16(DK, kNV, 1, 1);
         const uint64_t dKt = tc::smem_desc(st + P::oKt, 64 * 128, 1024);
-        const uint64_t dAqk = tc::smem_desc(st + P::oAqk, 16, 1024);
 #pragma unroll
         for (int k0 = 0; k0 < 64; k0 += 16) {
           const uint32_t kr = ((k0 / 8) * 1024) >> 4;
-          tc::mma_bf16(tmem + DS, dKt + kr, dW + kr, idS, k0 > 0);
+          tc::mma_bf16(tmem + DS, dKt + kr, dW + kr, id2, k0 > 0);
         }
         tc::commit(bar(kBS));
-#pragma unroll
-        for (int k0 = 0; k0 < 64; k0 += 16)
-          tc::mma_bf16(tmem + DO0 + (n & 1) * 64, dAqk + ((k0 * 2) >> 4),
-                       dW + (((k0 / 8) * 1024) >> 4), idO, 1);
-        tc::commit(bar(kBO0 + (n & 1)));
+        tc::mbar_arrive(bar(kWReady));
       }
       ok = wait_or_abort(bar(kBS), n & 1, abort_flag);
       if (tc::named_any(kChainBar, 128, !ok)) { fail = 4 * n + 2; break; }
       tc::fence_after_sync();
       // S_{n+1} = Diag(gamma_C) S_n + K_tail^T W
+      {
+        float x[kNV];
+        tc::tmem_ld64(tlane + DS, x);
 #pragma unroll
-      for (int c = 0; c < kNV; c += 32) {
-        float x[32];
-        tc::tmem_ld32(tlane + DS + c, x);
-#pragma unroll
-        for (int j = 0; j < 32; ++j) S[c + j] = gc * S[c + j] + x[j];
+        for (int j = 0; j < kNV; ++j) S[j] = gc * S[j] + x[j];
         if (owner) {
 #pragma unroll
-          for (int j = 0; j < 32; j += 8)
-            *reinterpret_cast<uint4*>(smem + L::oS + tc::tile_off(DK, srow, c + j)) = pack8(S + c + j);
+          for (int j = 0; j < kNV; j += 8)
+            *reinterpret_cast<uint4*>(smem + L::oS + tc::tile_off(DK, srow, j)) = pack8(S + j);
         }
       }
       tc::fence_proxy_async();
       tc::fence_before_sync();
       tc::named_sync(kChainBar, 128);
+      // the chain is done with chunk n's stage (its MMAs completed with D_S)
+      if (tid == 0) tc::mbar_arrive(bar(kEmpty0 + s));
     }
     if (fail < 0 && a.hT && owner) {
       const size_t base = ((size_t(bb) * H + h) * DK + srow) * DV + col0;
@@ -268,31 +263,68 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else {
     // ------------------------------------------------------------ output
-    const int orow = (warp & 3) * 16 + (lane & 15);
+    const int orow = tid - 128;                 // lanes 0..63 of D1 = rows of O_n
+    int issued = 0;
+    if (tid == 128) {
+      for (int n = 0; n < min(kStages, n_chunks); ++n) load_chunk(n);
+      issued = min(kStages, n_chunks);
+    }
     for (int n = 0; n < n_chunks; ++n) {
-      const bool ok = wait_or_abort(bar(kBO0 + (n & 1)), (n >> 1) & 1, abort_flag);
-      if (tc::named_any(kOutBar, 128, !ok)) { fail = 4 * n + 3; break; }
+      const int s = n % kStages;
+      const uint32_t st = sb + L::oStage + s * L::kStage;
+      bool ok = true;
+      if (tid == 128) {
+        // MMA3: [A_qk; *] W onto D1[n%2] once W is in shared memory
+        ok = wait_or_abort(bar(kWReady), n & 1, abort_flag);
+        if (ok) {
+          tc::fence_after_sync();
+          constexpr uint32_t id3 = tc::idesc_bf16(128, kNV, 0, 1);
+          const uint64_t dA = tc::smem_desc(st + P::oAqk, 16, 1024);
+          const uint64_t dW = tc::smem_desc(sb + L::oW, 64 * 128, 1024);
+#pragma unroll
+          for (int k0 = 0; k0 < 64; k0 += 16)
+            tc::mma_bf16(tmem + D10 + (n & 1) * 64, dA + ((k0 * 2) >> 4),
+                         dW + (((k0 / 8) * 1024) >> 4), id3, 1);
+          tc::commit(bar(kBO0 + (n & 1)));
+        }
+      }
+      if (tc::named_any(kOutBar, 64, !ok)) { fail = 4 * n + 3; break; }
+      ok = wait_or_abort(bar(kBO0 + (n & 1)), (n >> 1) & 1, abort_flag);
+      if (tc::named_any(kOutBar, 64, !ok)) { fail = 4 * n + 3; break; }
       tc::fence_after_sync();
       const int t0 = n * kChunk;
       const int Lr = min(kChunk, T - t0);
-      __nv_bfloat16* op = static_cast<__nv_bfloat16*>(a.o) +
-                          ((size_t(bb) * T + t0 + orow) * H + h) * DV + col0;
+      {
+        float x[kNV];
+        tc::tmem_ld64(tlane + D10 + (n & 1) * 64, x);
+        if (orow < Lr) {
+          __nv_bfloat16* op = static_cast<__nv_bfloat16*>(a.o) +
+                              ((size_t(bb) * T + t0 + orow) * H + h) * DV + col0;
 #pragma unroll
-      for (int c = 0; c < kNV; c += 32) {
-        float x[32];
-        tc::tmem_ld32(tlane + DO0 + (n & 1) * 64 + c, x);
-        if (lane < 16 && orow < Lr) {
-#pragma unroll
-          for (int j = 0; j < 32; j += 8) *reinterpret_cast<uint4*>(op + c + j) = pack8(x + j);
+          for (int j = 0; j < kNV; j += 8) *reinterpret_cast<uint4*>(op + j) = pack8(x + j);
         }
       }
       tc::fence_before_sync();
-      tc::named_sync(kOutBar, 128);
+      tc::named_sync(kOutBar, 64);
       if (tid == 128) {
         tc::mbar_arrive(bar(kOFree0 + (n & 1)));
-        tc::mbar_arrive(bar(kEmpty0 + n % kStages));
+        tc::mbar_arrive(bar(kEmpty0 + s));
+        // refill the stage once the chain has released it too
+        if (n + kStages < n_chunks) {
+          ok = wait_or_abort(bar(kEmpty0 + s), (n / kStages) & 1, abort_flag);
+          if (ok) {
+            load_chunk(n + kStages);
+            issued = n + kStages + 1;
+          }
+        }
       }
+      if (tc::named_any(kOutBar, 64, !ok)) { fail = 4 * n + 3; break; }
     }
+    // let the copies already issued land before the CTA can exit (a plain
+    // bounded wait: an abort elsewhere does not stop a copy in flight)
+    if (tid == 128)
+      for (int n = max(0, issued - kStages); n < issued; ++n)
+        tc::mbar_wait(bar(kFull0 + n % kStages), (n / kStages) & 1);
   }
 
   if (fail >= 0 && status && lane == 0) {

@@ -6,12 +6,15 @@
 // design 2 (S_{n+1} = Diag(gamma_C) S_n + K_tail^T (U - Y S_n),
 // O_n = Q_gamma S_n + A_qk (U - Y S_n)):
 //
-//   Q_gamma  64 x d_k  bf16, s gamma_r (.) q_r           (A operand, K-major)
-//   -Y       64 x d_k  bf16, -(A E_abs)                  (A operand, K-major)
+//   [Q_gamma; -Y]  128 x d_k bf16: rows 0..63 s gamma_r (.) q_r, rows 64..127
+//                  -(A E_abs); one M=128 A operand (K-major), so a single MMA
+//                  group gives Q_gamma S_n and -Y S_n
 //   K_tail   64 x d_k  bf16, (gamma_C / gamma_r) (.) k_r  (A operand, MN-major)
-//   A_qk     64 x 64   bf16, tril(Q_gamma K_bar^T)       (A operand, K-major)
 //   gamma_C  d_k fp32 (padded to 1 KB)
+//   A_qk     64 x 64   bf16, tril(Q_gamma K_bar^T)       (A operand, K-major)
 //   U        64 x d_v  bf16, A Z                         (64-column blocks)
+// U follows A_qk directly (also in the scan's shared-memory stage), so an M=128
+// operand starting at A_qk reads finite bf16 values in its lower half.
 //
 // Tiles are stored as byte images of the 128-byte-swizzled shared-memory
 // layout (tc::tile_off), so one plain bulk copy to a 1024-aligned shared
@@ -26,12 +29,11 @@ namespace gdr {
 
 template <int DK, int DV>
 struct Packet {
-  static constexpr uint32_t oQg = 0;
-  static constexpr uint32_t oY = oQg + 128 * DK;
-  static constexpr uint32_t oKt = oY + 128 * DK;
-  static constexpr uint32_t oAqk = oKt + 128 * DK;
-  static constexpr uint32_t oGc = oAqk + 8192;
-  static constexpr uint32_t kCommon = oGc + 1024;   // Q_gamma .. gamma_C
+  static constexpr uint32_t oQY = 0;                 // [Q_gamma; -Y], 128 rows
+  static constexpr uint32_t oKt = oQY + 256 * DK;
+  static constexpr uint32_t oGc = oKt + 128 * DK;
+  static constexpr uint32_t oAqk = oGc + 1024;
+  static constexpr uint32_t kCommon = oAqk + 8192;  // [Q_gamma; -Y] .. A_qk
   static constexpr uint32_t oU = kCommon;
   static constexpr uint32_t kUSlice = 8192;         // one 64-column block of U
   static constexpr uint32_t bytes = oU + 128 * DV;
