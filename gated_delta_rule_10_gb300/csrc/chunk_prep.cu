@@ -6,8 +6,9 @@
 // B * H * ceil(T / 64) independent CTAs and fills the GPU even when B * H is
 // small.
 //
-// One CTA takes one chunk (256 threads, two CTAs per SM):
-//   load    TMA brings the chunk's q, k, v (and b, w) tiles in at once
+// Persistent CTAs (256 threads, two per SM) walk the chunks; per chunk:
+//   load    TMA brings the chunk's q, k, v (and b, w) tiles in at once, and
+//           the CTA's next chunk is prefetched into L2 meanwhile
 //   gates   G = in-chunk cumsum of g (per key channel or per row), gamma_C
 //   tiles   gated in place: Z = z over v; E_bar = f (.) e, Q' = s f (.) q,
 //           K_bar = f^-1 (.) k over b (or a free slot), q and k; E_abs = gamma (.) e
@@ -237,13 +238,10 @@ __global__ void __launch_bounds__(kThreads, 2)
   unsigned char* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   const uint32_t sbase = smem_u32(smem);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int n = blockIdx.x, h = blockIdx.y, bb = blockIdx.z;
-  const int T = a.T, H = a.H;
-  const int n_chunks = gridDim.x;
-  const int t0 = n * kChunk, Lr = min(kChunk, T - t0);
-  const size_t row0 = size_t(bb) * T + t0;
+  const int T = a.T, H = a.H, B = a.B;
+  const int n_chunks = (T + kChunk - 1) / kChunk;
+  const int total = n_chunks * B * H;
   const bool CH = a.flags & 1u, ER = a.flags & 2u, WR = a.flags & 4u, QM = a.flags & 8u;
-  unsigned char* pkt = packets + ((size_t(bb) * H + h) * n_chunks + n) * P::bytes;
 
   float* sT = reinterpret_cast<float*>(smem + L::oT);
   float* sAf = reinterpret_cast<float*>(smem + L::oAf);
@@ -266,66 +264,110 @@ __global__ void __launch_bounds__(kThreads, 2)
   __syncthreads();
   tc::fence_after_sync();
   const uint32_t tmem = *tslot;
-  if (tid == 64) {
-    // every input tile of the chunk at once: v (and w) first, then q, k (and b)
-    tc::mbar_arrive_expect_tx(bar(kBarV), (WR ? 2u : 1u) * 128u * DV);
-#pragma unroll
-    for (int blk = 0; blk < DV / 64; ++blk) {
-      tc::tma_load_4d(sbase + L::oV + blk * 8192, &tm_v, blk * 64, h, t0, bb, bar(kBarV));
-      if (WR) tc::tma_load_4d(sbase + L::oEa + blk * 8192, &tm_w, blk * 64, h, t0, bb, bar(kBarV));
-    }
-    tc::mbar_arrive_expect_tx(bar(kBarK), (ER ? 3u : 2u) * 128u * DK);
-#pragma unroll
-    for (int blk = 0; blk < DK / 64; ++blk) {
-      tc::tma_load_4d(sbase + L::oEQ + blk * 16384 + 8192, &tm_q, blk * 64, h, t0, bb, bar(kBarK));
-      tc::tma_load_4d(sbase + L::oK + blk * 8192, &tm_k, blk * 64, h, t0, bb, bar(kBarK));
-      if (ER) tc::tma_load_4d(sbase + L::oEQ + blk * 16384, &tm_b, blk * 64, h, t0, bb, bar(kBarK));
-    }
-  }
 
-  // per-row gates while the tiles are in flight: beta, lam; scalar decay cumsum
-  if (tid < kChunk) {
-    const size_t ti = (row0 + tid) * H + h;
-    sBeta[tid] = (tid < Lr && a.beta) ? __ldg(a.beta + ti) : 0.f;
-    sLam[tid] = (tid < Lr && QM) ? __ldg(a.lam + ti) : 0.f;
-  }
-  if (!CH && warp == 3) {
-    float g0 = lane < Lr ? __ldg(a.g + (row0 + lane) * H + h) : 0.f;
-    float g1 = lane + 32 < Lr ? __ldg(a.g + (row0 + lane + 32) * H + h) : 0.f;
-#pragma unroll
-    for (int off = 1; off < 32; off <<= 1) {
-      const float u0 = __shfl_up_sync(0xffffffffu, g0, off);
-      const float u1 = __shfl_up_sync(0xffffffffu, g1, off);
-      if (lane >= off) { g0 += u0; g1 += u1; }
-    }
-    g1 += __shfl_sync(0xffffffffu, g0, 31);
-    const float tot = __shfl_sync(0xffffffffu, g1, 31);
-    sGs[lane] = g0;
-    sGs[lane + 32] = g1;
-    sEG[lane] = __expf(g0);
-    sEG[lane + 32] = __expf(g1);
-    sEGL[lane] = __expf(tot - g0);
-    sEGL[lane + 32] = __expf(tot - g1);
-    const float gc = __expf(tot);
-    float* dst = reinterpret_cast<float*>(pkt + P::oGc);
-    for (int c = lane; c < DK; c += 32) dst[c] = gc;
-  }
-  float gv[64 * DK / 8 / kThreads][8];
-  if (CH) load_channel_gates<DK>(a, row0, h, Lr, sPart, gv);
-  __syncthreads();
+  // work item w -> (chunk n, batch b, head h), heads fastest so that
+  // neighbouring CTAs read neighbouring bytes of each token row
+  auto decode = [&](int w, int& n, int& bb, int& h) {
+    h = w % H;
+    const int rest = w / H;
+    bb = rest % B;
+    n = rest / B;
+  };
+  int fail_at = -1, iter = 0;
+  for (int w = blockIdx.x; w < total; w += gridDim.x, ++iter) {
+    const uint32_t par = static_cast<uint32_t>(iter & 1);
+    int n, bb, h;
+    decode(w, n, bb, h);
+    const int t0 = n * kChunk, Lr = min(kChunk, T - t0);
+    const size_t row0 = size_t(bb) * T + t0;
+    unsigned char* pkt = packets + ((size_t(bb) * H + h) * n_chunks + n) * P::bytes;
+    const int wn = w + gridDim.x;   // this CTA's next chunk, prefetched into L2 below
+    int nn = 0, nb = 0, nh = 0;
+    if (wn < total) decode(wn, nn, nb, nh);
 
-  int fail_at = -1;
-  if (__syncthreads_or(!tc::mbar_wait(bar(kBarV), 0))) {
-    fail_at = 4 * n;
-  } else {
+    if (tid == 64) {
+      // every input tile of the chunk at once: v (and w) first, then q, k (and b)
+      tc::fence_proxy_async();
+      tc::mbar_arrive_expect_tx(bar(kBarV), (WR ? 2u : 1u) * 128u * DV);
+#pragma unroll
+      for (int blk = 0; blk < DV / 64; ++blk) {
+        tc::tma_load_4d(sbase + L::oV + blk * 8192, &tm_v, blk * 64, h, t0, bb, bar(kBarV));
+        if (WR) tc::tma_load_4d(sbase + L::oEa + blk * 8192, &tm_w, blk * 64, h, t0, bb, bar(kBarV));
+      }
+      tc::mbar_arrive_expect_tx(bar(kBarK), (ER ? 3u : 2u) * 128u * DK);
+#pragma unroll
+      for (int blk = 0; blk < DK / 64; ++blk) {
+        tc::tma_load_4d(sbase + L::oEQ + blk * 16384 + 8192, &tm_q, blk * 64, h, t0, bb, bar(kBarK));
+        tc::tma_load_4d(sbase + L::oK + blk * 8192, &tm_k, blk * 64, h, t0, bb, bar(kBarK));
+        if (ER) tc::tma_load_4d(sbase + L::oEQ + blk * 16384, &tm_b, blk * 64, h, t0, bb, bar(kBarK));
+      }
+      if (wn < total) {
+        const int nt0 = nn * kChunk;
+#pragma unroll
+        for (int blk = 0; blk < DV / 64; ++blk) {
+          tc::tma_prefetch_4d(&tm_v, blk * 64, nh, nt0, nb);
+          if (WR) tc::tma_prefetch_4d(&tm_w, blk * 64, nh, nt0, nb);
+        }
+#pragma unroll
+        for (int blk = 0; blk < DK / 64; ++blk) {
+          tc::tma_prefetch_4d(&tm_q, blk * 64, nh, nt0, nb);
+          tc::tma_prefetch_4d(&tm_k, blk * 64, nh, nt0, nb);
+          if (ER) tc::tma_prefetch_4d(&tm_b, blk * 64, nh, nt0, nb);
+        }
+      }
+    }
+    // gates of the next chunk into L2 (one row each for threads 128..191)
+    if (wn < total && tid >= 128 && tid < 128 + kChunk) {
+      const int r = tid - 128, nt = nn * kChunk + r;
+      if (nt < T) {
+        const size_t ti = (size_t(nb) * T + nt) * H + nh;
+        if (CH)
+          tc::bulk_prefetch(a.g + ti * DK, DK * 4);
+        else
+          tc::prefetch_l2(a.g + ti);
+        if (a.beta) tc::prefetch_l2(a.beta + ti);
+        if (QM) tc::prefetch_l2(a.lam + ti);
+      }
+    }
+
+    // per-row gates while the tiles are in flight: beta, lam; scalar decay cumsum
+    if (tid < kChunk) {
+      const size_t ti = (row0 + tid) * H + h;
+      sBeta[tid] = (tid < Lr && a.beta) ? __ldg(a.beta + ti) : 0.f;
+      sLam[tid] = (tid < Lr && QM) ? __ldg(a.lam + ti) : 0.f;
+    }
+    if (!CH && warp == 3) {
+      float g0 = lane < Lr ? __ldg(a.g + (row0 + lane) * H + h) : 0.f;
+      float g1 = lane + 32 < Lr ? __ldg(a.g + (row0 + lane + 32) * H + h) : 0.f;
+#pragma unroll
+      for (int off = 1; off < 32; off <<= 1) {
+        const float u0 = __shfl_up_sync(0xffffffffu, g0, off);
+        const float u1 = __shfl_up_sync(0xffffffffu, g1, off);
+        if (lane >= off) { g0 += u0; g1 += u1; }
+      }
+      g1 += __shfl_sync(0xffffffffu, g0, 31);
+      const float tot = __shfl_sync(0xffffffffu, g1, 31);
+      sGs[lane] = g0;
+      sGs[lane + 32] = g1;
+      sEG[lane] = __expf(g0);
+      sEG[lane + 32] = __expf(g1);
+      sEGL[lane] = __expf(tot - g0);
+      sEGL[lane + 32] = __expf(tot - g1);
+      const float gc = __expf(tot);
+      float* dst = reinterpret_cast<float*>(pkt + P::oGc);
+      for (int c = lane; c < DK; c += 32) dst[c] = gc;
+    }
+    float gv[64 * DK / 8 / kThreads][8];
+    if (CH) load_channel_gates<DK>(a, row0, h, Lr, sPart, gv);
+    __syncthreads();
+
+    if (__syncthreads_or(!tc::mbar_wait(bar(kBarV), par))) { fail_at = 4 * n; break; }
     if (WR)
       prep_z<DK, DV, true>(smem, sBeta);
     else
       prep_z<DK, DV, false>(smem, sBeta);
     __syncthreads();   // w has been read: its slot takes E_abs below
-    if (__syncthreads_or(!tc::mbar_wait(bar(kBarK), 0))) fail_at = 4 * n;
-  }
-  if (fail_at < 0) {
+    if (__syncthreads_or(!tc::mbar_wait(bar(kBarK), par))) { fail_at = 4 * n; break; }
     switch (a.flags & 11u) {   // CH | ER | QM select the key-side tiles
 #define GDR_PREP(F)                                                                       \
   case F:                                                                                 \
@@ -354,9 +396,7 @@ __global__ void __launch_bounds__(kThreads, 2)
       }
       tc::commit(bar(kBarM1));
     }
-    if (__syncthreads_or(!tc::mbar_wait(bar(kBarM1), 0))) fail_at = 4 * n + 1;
-  }
-  if (fail_at < 0) {
+    if (__syncthreads_or(!tc::mbar_wait(bar(kBarM1), par))) { fail_at = 4 * n + 1; break; }
     tc::fence_after_sync();
     // ---- T (fp32, shared) and A_qk (bf16, packet): warp w reads lane quadrant
     // w % 4 (quadrants 0-1: E_bar K_bar^T rows, 2-3: Q' K_bar^T rows), columns
@@ -418,10 +458,9 @@ __global__ void __launch_bounds__(kThreads, 2)
       }
       tc::commit(bar(kBarM2));
     }
-    if (__syncthreads_or(!tc::mbar_wait(bar(kBarM2), 0))) {
-      fail_at = 4 * n + 2;
-    } else {
-      tc::fence_after_sync();
+    if (__syncthreads_or(!tc::mbar_wait(bar(kBarM2), par))) { fail_at = 4 * n + 2; break; }
+    tc::fence_after_sync();
+    {
       // M=64 accumulators: row 16 q + l in lane l < 16 of quadrant q; warp w
       // takes quadrant w % 4 and half w / 4 of the columns
       const int q = warp & 3, half = warp >> 2;
@@ -449,16 +488,20 @@ __global__ void __launch_bounds__(kThreads, 2)
         }
       }
     }
+    // the next chunk reuses every shared tile and the tensor memory
+    tc::fence_before_sync();
+    __syncthreads();
+    tc::fence_after_sync();
   }
 
   if (fail_at >= 0) {
     // no TMA copy may still be writing this CTA's shared memory when it exits
     if (tid == 64) {
-      tc::mbar_wait(bar(kBarV), 0);
-      tc::mbar_wait(bar(kBarK), 0);
+      tc::mbar_wait(bar(kBarV), static_cast<uint32_t>(iter & 1));
+      tc::mbar_wait(bar(kBarK), static_cast<uint32_t>(iter & 1));
     }
     if (tid == 0 && status && atomicCAS(status, 0, 5) == 0) {  // GDR_ERR_TIMEOUT
-      status[1] = static_cast<int>((blockIdx.z * gridDim.y + blockIdx.y) * gridDim.x + blockIdx.x);
+      status[1] = static_cast<int>(blockIdx.x);
       status[2] = fail_at;
     }
   }
@@ -484,8 +527,13 @@ cudaError_t launch_prep(const ChunkArgs& a, unsigned char* packets, int* status,
   cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(L::launch_bytes));
   if (err != cudaSuccess) return err;
-  const int n_chunks = (a.T + kChunk - 1) / kChunk;
-  dim3 grid(n_chunks, a.H, a.B);
+  // persistent: two CTAs per SM walk the B * H * ceil(T / 64) chunks
+  int dev = 0, sms = 0;
+  if ((err = cudaGetDevice(&dev)) != cudaSuccess) return err;
+  if ((err = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
+    return err;
+  const long long total = static_cast<long long>((a.T + kChunk - 1) / kChunk) * a.B * a.H;
+  const int grid = static_cast<int>(total < 2LL * sms ? total : 2LL * sms);
   kern<<<grid, kThreads, L::launch_bytes, stream>>>(a, tq, tk, tv, tb, tw, packets, status);
   return cudaGetLastError();
 }
