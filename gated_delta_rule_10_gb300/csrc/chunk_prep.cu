@@ -7,8 +7,10 @@
 // small.
 //
 // Persistent CTAs (256 threads, two per SM) walk the chunks; per chunk:
-//   load    TMA brings the chunk's q, k, v (and b, w) tiles in at once, and
-//           the CTA's next chunk is prefetched into L2 meanwhile
+//   load    TMA brings the chunk's q, k, v (and b, w) tiles in: the key side as
+//           soon as the previous chunk's inverse is done with their shared
+//           memory, the value side as soon as its M2 is; the chunk after is
+//           prefetched into L2 meanwhile
 //   gates   G = in-chunk cumsum of g (per key channel or per row), gamma_C
 //   tiles   gated in place: Z = z over v; E_bar = f (.) e, Q' = s f (.) q,
 //           K_bar = f^-1 (.) k over b (or a free slot), q and k; E_abs = gamma (.) e
@@ -18,8 +20,8 @@
 //           scalar gates: f = 1 and exp(G_r - G_i) <= 1 multiplies T and A_qk afterwards)
 //   M1      D1 = [E_bar; Q'] K_bar^T            (tcgen05, M=128, N=64, K=d_k)
 //           T = tril(D1[0:64], -1) (fp32), A_qk = tril(D1[64:128], 0) -> packet
-//   UT      A = (I + T)^{-1}                   (blocked forward substitution)
-//   M2      Y = A E_abs, U = A Z                (M=64, N=d_k and d_v) -> packet (-Y, U)
+//   UT      A = (I + T)^{-1}                   (blocked forward substitution, 8 warps)
+//   M2      [U | Y] = A [Z | E_abs]             (M=64, N=d_v+d_k) -> packet (U, -Y)
 // The packet layout is in packet.h. Operands live in shared memory in the
 // 128-byte swizzle of tc.cuh (the TMA boxes land in it directly); packet tiles
 // go from registers straight to global memory in the same byte layout.
@@ -42,19 +44,22 @@ constexpr uint32_t cmax(uint32_t a, uint32_t b) { return a > b ? a : b; }
 template <int DK, int DV>
 struct PrepLayout {
   // region 1: [E; Q] (128 x DK, 16 KB per 64-column block: E rows, then Q rows)
-  // and K (64 x DK) until M1 completes, then T and A (fp32 [64][65] each)
-  static constexpr uint32_t kR1 = align1k(cmax(384 * DK, 2 * 64 * 65 * 4));
+  // and K (64 x DK) until M1 completes, then T and A (fp32 [64][65] each) and
+  // the inverse's [32][33] scratch
+  static constexpr uint32_t kR1 = align1k(cmax(384 * DK, 2 * 64 * 65 * 4 + 32 * 33 * 4));
   static constexpr uint32_t oEQ = 0;
   static constexpr uint32_t oK = 256 * DK;
   static constexpr uint32_t oT = 0;
   static constexpr uint32_t oAf = 64 * 65 * 4;
-  static constexpr uint32_t oV = kR1;                       // v -> Z, K=64 x DV (B, MN-major)
-  static constexpr uint32_t oEa = oV + 128 * DV;            // w -> E_abs, K=64 x DK (B, MN-major)
+  static constexpr uint32_t oX = 2 * 64 * 65 * 4;          // [32][33] inverse scratch
+  // v -> Z and w -> E_abs, adjacent: one B operand [Z | E_abs] of N = DV + DK
+  static constexpr uint32_t oV = kR1;                       // K=64 x DV (B, MN-major)
+  static constexpr uint32_t oEa = oV + 128 * DV;            // K=64 x DK (B, MN-major)
   static constexpr uint32_t oA = oEa + 128 * cmax(DK, DV);  // A 64 x 64 (A, K-major)
   static constexpr uint32_t oP = oA + 8192;                 // [4][256] inverse scratch
   static constexpr uint32_t oPart = oP + 4096;              // per-row-block gate sums
-  static constexpr uint32_t oVec = oPart + 8192;            // beta, lam, G, e^G, e^{G_C-G} [64]
-  static constexpr uint32_t oBar = oVec + 5 * 64 * 4;       // 4 mbarriers
+  static constexpr uint32_t oVec = oPart + 8192;            // beta, lam, G, e^G, e^{G_C-G}, e^-G [64]
+  static constexpr uint32_t oBar = oVec + 6 * 64 * 4 + 16;  // 4 mbarriers (after a flag word)
   static constexpr uint32_t oSlot = oBar + 32;
   static constexpr uint32_t bytes = oSlot + 16;
   static constexpr uint32_t launch_bytes = bytes + 1024;
@@ -252,6 +257,8 @@ __global__ void __launch_bounds__(kThreads, 2)
   float* sGs = sLam + 64;
   float* sEG = sGs + 64;
   float* sEGL = sEG + 64;
+  float* sEGn = sEGL + 64;   // scalar gates: exp(-G_r)
+  volatile int* sFactor = reinterpret_cast<volatile int*>(sEGn + 64);
   auto bar = [&](uint32_t i) { return sbase + L::oBar + 8 * i; };
   uint32_t* tslot = reinterpret_cast<uint32_t*>(smem + L::oSlot);
 
@@ -273,6 +280,58 @@ __global__ void __launch_bounds__(kThreads, 2)
     bb = rest % B;
     n = rest / B;
   };
+  // TMA loads of one chunk's input tiles (thread 64): the value side (v, w) and
+  // the key side (q, k, b) each complete one phase of their barrier; the
+  // CTA's chunk after that one is prefetched into L2 along with them
+  auto load_values = [&](int w) {
+    int n, bb, h;
+    decode(w, n, bb, h);
+    tc::fence_proxy_async();
+    tc::mbar_arrive_expect_tx(bar(kBarV), (WR ? 2u : 1u) * 128u * DV);
+#pragma unroll
+    for (int blk = 0; blk < DV / 64; ++blk) {
+      tc::tma_load_4d(sbase + L::oV + blk * 8192, &tm_v, blk * 64, h, n * kChunk, bb, bar(kBarV));
+      if (WR)
+        tc::tma_load_4d(sbase + L::oEa + blk * 8192, &tm_w, blk * 64, h, n * kChunk, bb, bar(kBarV));
+    }
+    if (w + gridDim.x < total) {
+      decode(w + gridDim.x, n, bb, h);
+#pragma unroll
+      for (int blk = 0; blk < DV / 64; ++blk) {
+        tc::tma_prefetch_4d(&tm_v, blk * 64, h, n * kChunk, bb);
+        if (WR) tc::tma_prefetch_4d(&tm_w, blk * 64, h, n * kChunk, bb);
+      }
+    }
+  };
+  auto load_keys = [&](int w) {
+    int n, bb, h;
+    decode(w, n, bb, h);
+    tc::fence_proxy_async();
+    tc::mbar_arrive_expect_tx(bar(kBarK), (ER ? 3u : 2u) * 128u * DK);
+#pragma unroll
+    for (int blk = 0; blk < DK / 64; ++blk) {
+      tc::tma_load_4d(sbase + L::oEQ + blk * 16384 + 8192, &tm_q, blk * 64, h, n * kChunk, bb, bar(kBarK));
+      tc::tma_load_4d(sbase + L::oK + blk * 8192, &tm_k, blk * 64, h, n * kChunk, bb, bar(kBarK));
+      if (ER) tc::tma_load_4d(sbase + L::oEQ + blk * 16384, &tm_b, blk * 64, h, n * kChunk, bb, bar(kBarK));
+    }
+    if (w + gridDim.x < total) {
+      decode(w + gridDim.x, n, bb, h);
+#pragma unroll
+      for (int blk = 0; blk < DK / 64; ++blk) {
+        tc::tma_prefetch_4d(&tm_q, blk * 64, h, n * kChunk, bb);
+        tc::tma_prefetch_4d(&tm_k, blk * 64, h, n * kChunk, bb);
+        if (ER) tc::tma_prefetch_4d(&tm_b, blk * 64, h, n * kChunk, bb);
+      }
+    }
+  };
+  // loads issued and waited for, to drain what is in flight on the way out
+  int v_issued = 0, k_issued = 0, v_done = 0, k_done = 0;
+  if (tid == 64 && blockIdx.x < total) {
+    load_values(blockIdx.x);
+    load_keys(blockIdx.x);
+  }
+  if (blockIdx.x < total) { v_issued = 1; k_issued = 1; }
+
   int fail_at = -1, iter = 0;
   for (int w = blockIdx.x; w < total; w += gridDim.x, ++iter) {
     const uint32_t par = static_cast<uint32_t>(iter & 1);
@@ -281,41 +340,10 @@ __global__ void __launch_bounds__(kThreads, 2)
     const int t0 = n * kChunk, Lr = min(kChunk, T - t0);
     const size_t row0 = size_t(bb) * T + t0;
     unsigned char* pkt = packets + ((size_t(bb) * H + h) * n_chunks + n) * P::bytes;
-    const int wn = w + gridDim.x;   // this CTA's next chunk, prefetched into L2 below
+    const int wn = w + gridDim.x;   // this CTA's next chunk
     int nn = 0, nb = 0, nh = 0;
     if (wn < total) decode(wn, nn, nb, nh);
 
-    if (tid == 64) {
-      // every input tile of the chunk at once: v (and w) first, then q, k (and b)
-      tc::fence_proxy_async();
-      tc::mbar_arrive_expect_tx(bar(kBarV), (WR ? 2u : 1u) * 128u * DV);
-#pragma unroll
-      for (int blk = 0; blk < DV / 64; ++blk) {
-        tc::tma_load_4d(sbase + L::oV + blk * 8192, &tm_v, blk * 64, h, t0, bb, bar(kBarV));
-        if (WR) tc::tma_load_4d(sbase + L::oEa + blk * 8192, &tm_w, blk * 64, h, t0, bb, bar(kBarV));
-      }
-      tc::mbar_arrive_expect_tx(bar(kBarK), (ER ? 3u : 2u) * 128u * DK);
-#pragma unroll
-      for (int blk = 0; blk < DK / 64; ++blk) {
-        tc::tma_load_4d(sbase + L::oEQ + blk * 16384 + 8192, &tm_q, blk * 64, h, t0, bb, bar(kBarK));
-        tc::tma_load_4d(sbase + L::oK + blk * 8192, &tm_k, blk * 64, h, t0, bb, bar(kBarK));
-        if (ER) tc::tma_load_4d(sbase + L::oEQ + blk * 16384, &tm_b, blk * 64, h, t0, bb, bar(kBarK));
-      }
-      if (wn < total) {
-        const int nt0 = nn * kChunk;
-#pragma unroll
-        for (int blk = 0; blk < DV / 64; ++blk) {
-          tc::tma_prefetch_4d(&tm_v, blk * 64, nh, nt0, nb);
-          if (WR) tc::tma_prefetch_4d(&tm_w, blk * 64, nh, nt0, nb);
-        }
-#pragma unroll
-        for (int blk = 0; blk < DK / 64; ++blk) {
-          tc::tma_prefetch_4d(&tm_q, blk * 64, nh, nt0, nb);
-          tc::tma_prefetch_4d(&tm_k, blk * 64, nh, nt0, nb);
-          if (ER) tc::tma_prefetch_4d(&tm_b, blk * 64, nh, nt0, nb);
-        }
-      }
-    }
     // gates of the next chunk into L2 (one row each for threads 128..191)
     if (wn < total && tid >= 128 && tid < 128 + kChunk) {
       const int r = tid - 128, nt = nn * kChunk + r;
@@ -356,18 +384,24 @@ __global__ void __launch_bounds__(kThreads, 2)
       const float gc = __expf(tot);
       float* dst = reinterpret_cast<float*>(pkt + P::oGc);
       for (int c = lane; c < DK; c += 32) dst[c] = gc;
+      // exp(G_r - G_i) = e^{G_r} e^{-G_i} stays exact in fp32 while G_C >= -80
+      sEGn[lane] = __expf(-g0);
+      sEGn[lane + 32] = __expf(-g1);
+      if (lane == 0) *sFactor = tot >= -80.f ? 1 : 0;
     }
     float gv[64 * DK / 8 / kThreads][8];
     if (CH) load_channel_gates<DK>(a, row0, h, Lr, sPart, gv);
     __syncthreads();
 
     if (__syncthreads_or(!tc::mbar_wait(bar(kBarV), par))) { fail_at = 4 * n; break; }
+    v_done = v_issued;
     if (WR)
       prep_z<DK, DV, true>(smem, sBeta);
     else
       prep_z<DK, DV, false>(smem, sBeta);
     __syncthreads();   // w has been read: its slot takes E_abs below
     if (__syncthreads_or(!tc::mbar_wait(bar(kBarK), par))) { fail_at = 4 * n; break; }
+    k_done = k_issued;
     switch (a.flags & 11u) {   // CH | ER | QM select the key-side tiles
 #define GDR_PREP(F)                                                                       \
   case F:                                                                                 \
@@ -411,6 +445,10 @@ __global__ void __launch_bounds__(kThreads, 2)
       if (CH) {
 #pragma unroll
         for (int j = 0; j < 32; ++j) x[j] = select_f32(c + j < lim, x[j], 0.f);
+      } else if (*sFactor) {
+        const float er = sEG[r];
+#pragma unroll
+        for (int j = 0; j < 32; ++j) x[j] = select_f32(c + j < lim, er * sEGn[c + j] * x[j], 0.f);
       } else {
         const float Gr = sGs[r];
 #pragma unroll
@@ -428,9 +466,9 @@ __global__ void __launch_bounds__(kThreads, 2)
     tc::fence_before_sync();
     __syncthreads();
 
-    // ---- A = (I + T)^{-1} on warps 0-3, then the bf16 operand tile ----
-    if (warp < 4) invert_unit_lower_64(sT, sAf, sP, warp, lane, [] { tc::named_sync(kInvBar, 128); });
-    __syncthreads();
+    // ---- A = (I + T)^{-1} (all 8 warps), then the bf16 operand tile ----
+    invert_unit_lower_64_w8(sT, sAf, sP, reinterpret_cast<float*>(smem + L::oX), warp, lane,
+                            [] { tc::named_sync(kInvBar, 128); }, [] { __syncthreads(); });
 #pragma unroll
     for (int u = 0; u < 2; ++u) {
       const int it = tid + u * kThreads, r = it >> 3, c0 = (it & 7) * 8;
@@ -441,25 +479,31 @@ __global__ void __launch_bounds__(kThreads, 2)
     }
     tc::fence_proxy_async();
     __syncthreads();
+    // T and A are consumed: the key-side tiles of the next chunk may land now
+    if (wn < total) {
+      if (tid == 64) load_keys(wn);
+      ++k_issued;
+    }
 
-    // ---- M2: Y = A E_abs (columns 0..DK-1), U = A Z (columns DK..DK+DV-1) ----
+    // ---- M2: [U | Y] = A [Z | E_abs] (N = DV + DK): U in columns 0..DV-1,
+    // Y in columns DV..DV+DK-1 ----
     if (tid == 0) {
       tc::fence_after_sync();
-      constexpr uint32_t idY = tc::idesc_bf16(64, DK, 0, 1);
-      constexpr uint32_t idU = tc::idesc_bf16(64, DV, 0, 1);
+      constexpr uint32_t id2 = tc::idesc_bf16(64, DV + DK, 0, 1);
       const uint64_t dA = tc::smem_desc(sbase + L::oA, 16, 1024);
-      const uint64_t dEa = tc::smem_desc(sbase + L::oEa, 64 * 128, 1024);
-      const uint64_t dZ = tc::smem_desc(sbase + L::oV, 64 * 128, 1024);
+      const uint64_t dZE = tc::smem_desc(sbase + L::oV, 64 * 128, 1024);
 #pragma unroll
-      for (int k0 = 0; k0 < 64; k0 += 16) {
-        const uint32_t kr = ((k0 / 8) * 1024) >> 4;
-        tc::mma_bf16(tmem, dA + ((k0 * 2) >> 4), dEa + kr, idY, k0 > 0);
-        tc::mma_bf16(tmem + DK, dA + ((k0 * 2) >> 4), dZ + kr, idU, k0 > 0);
-      }
+      for (int k0 = 0; k0 < 64; k0 += 16)
+        tc::mma_bf16(tmem, dA + ((k0 * 2) >> 4), dZE + (((k0 / 8) * 1024) >> 4), id2, k0 > 0);
       tc::commit(bar(kBarM2));
     }
     if (__syncthreads_or(!tc::mbar_wait(bar(kBarM2), par))) { fail_at = 4 * n + 2; break; }
     tc::fence_after_sync();
+    // Z and E_abs are consumed: the value-side tiles of the next chunk may land now
+    if (wn < total) {
+      if (tid == 64) load_values(wn);
+      ++v_issued;
+    }
     {
       // M=64 accumulators: row 16 q + l in lane l < 16 of quadrant q; warp w
       // takes quadrant w % 4 and half w / 4 of the columns
@@ -469,7 +513,7 @@ __global__ void __launch_bounds__(kThreads, 2)
 #pragma unroll
       for (int c = half * (DK / 2); c < (half + 1) * (DK / 2); c += 32) {
         float x[32];
-        tc::tmem_ld32(tl + c, x);
+        tc::tmem_ld32(tl + DV + c, x);
 #pragma unroll
         for (int j = 0; j < 32; ++j) x[j] = -x[j];
         if (lane < 16) {
@@ -481,7 +525,7 @@ __global__ void __launch_bounds__(kThreads, 2)
 #pragma unroll
       for (int c = half * (DV / 2); c < (half + 1) * (DV / 2); c += 32) {
         float x[32];
-        tc::tmem_ld32(tl + DK + c, x);
+        tc::tmem_ld32(tl + c, x);
         if (lane < 16) {
 #pragma unroll
           for (int j = 0; j < 32; j += 8) st16(pkt, P::oU + tc::tile_off(64, r, c + j), pack8(x + j));
@@ -497,8 +541,8 @@ __global__ void __launch_bounds__(kThreads, 2)
   if (fail_at >= 0) {
     // no TMA copy may still be writing this CTA's shared memory when it exits
     if (tid == 64) {
-      tc::mbar_wait(bar(kBarV), static_cast<uint32_t>(iter & 1));
-      tc::mbar_wait(bar(kBarK), static_cast<uint32_t>(iter & 1));
+      if (v_issued > v_done) tc::mbar_wait(bar(kBarV), static_cast<uint32_t>((v_issued - 1) & 1));
+      if (k_issued > k_done) tc::mbar_wait(bar(kBarK), static_cast<uint32_t>((k_issued - 1) & 1));
     }
     if (tid == 0 && status && atomicCAS(status, 0, 5) == 0) {  // GDR_ERR_TIMEOUT
       status[1] = static_cast<int>(blockIdx.x);

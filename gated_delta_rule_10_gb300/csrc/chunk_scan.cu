@@ -44,7 +44,7 @@ constexpr uint32_t kChainBar = 1, kOutBar = 2;
 constexpr uint32_t D10 = 0, DS = 128;
 
 enum : uint32_t {
-  kFull0 = 0, kEmpty0 = 3, kBW = 6, kWReady = 7, kBS = 8, kBO0 = 9, kOFree0 = 11, kBars = 13
+  kFull0 = 0, kEmpty0 = 3, kBW = 6, kBS = 7, kBO0 = 8, kOFree0 = 10, kBars = 12
 };
 
 template <int DK>
@@ -117,7 +117,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc::mbar_init(bar(kEmpty0 + s), 2);   // chain and output each release the stage
     }
     tc::mbar_init(bar(kBW), 1);
-    tc::mbar_init(bar(kWReady), 1);
     tc::mbar_init(bar(kBS), 1);
     for (int i = 0; i < 2; ++i) {
       tc::mbar_init(bar(kBO0 + i), 1);
@@ -221,7 +220,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc::fence_proxy_async();
       tc::fence_before_sync();
       tc::named_sync(kChainBar, 128);
-      // MMA2: K_tail^T W into D_S; then let the output role issue MMA3
+      // MMA2: K_tail^T W into D_S (the output role issues MMA3 once it completes)
       if (tid == 0) {
         tc::fence_after_sync();
         constexpr uint32_t id2 = tc::idesc_bf16(DK, kNV, 1, 1);
@@ -232,7 +231,6 @@ __global__ void __launch_bounds__(kThreads, 1)
           tc::mma_bf16(tmem + DS, dKt + kr, dW + kr, id2, k0 > 0);
         }
         tc::commit(bar(kBS));
-        tc::mbar_arrive(bar(kWReady));
       }
       ok = wait_or_abort(bar(kBS), n & 1, abort_flag);
       if (tc::named_any(kChainBar, 128, !ok)) { fail = 4 * n + 2; break; }
@@ -274,8 +272,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t st = sb + L::oStage + s * L::kStage;
       bool ok = true;
       if (tid == 128) {
-        // MMA3: [A_qk; *] W onto D1[n%2] once W is in shared memory
-        ok = wait_or_abort(bar(kWReady), n & 1, abort_flag);
+        // MMA3: [A_qk; *] W onto D1[n%2] once MMA2 (which reads the same W) has
+        // completed, so that MMA3 runs while the chain updates S instead of
+        // delaying MMA2 in the tensor pipe
+        ok = wait_or_abort(bar(kBS), n & 1, abort_flag);
         if (ok) {
           tc::fence_after_sync();
           constexpr uint32_t id3 = tc::idesc_bf16(128, kNV, 0, 1);

@@ -114,4 +114,58 @@ __device__ __forceinline__ void invert_unit_lower_64(const float* sT, float* sAf
   sync();
 }
 
+// The same inverse on two warpgroups (8 warps, `w` = 0..7): the diagonal
+// blocks and the 16-row level as above on warps 0-3 (warps 4-7 wait), the
+// 32-row level split over all 8 warps, one 16 x 8 output tile each:
+//   X = -T[32:64, 0:32] A1          (warp w: rows 32 + 16 (w >> 2), columns 8 (w & 3))
+//   A[32:64, 0:32] = A2 X           (same tile), after a barrier over the 8 warps.
+// `sync4` is a barrier over warps 0-3, `sync8` over all 8. X goes to sX
+// ([32][33] fp32, shared).
+template <typename Sync4, typename Sync8>
+__device__ __forceinline__ void invert_unit_lower_64_w8(const float* sT, float* sAf, float* sP,
+                                                        float* sX, int w, int lane, Sync4 sync4,
+                                                        Sync8 sync8) {
+  if (w < 4) {
+    if (lane < 16) {
+      const int base = w * 16;
+      float col[16];
+#pragma unroll
+      for (int r = 0; r < 16; ++r) {
+        float acc = 0.f;
+#pragma unroll
+        for (int i = 0; i < r; ++i) acc += sT[(base + r) * 65 + base + i] * col[i];
+        col[r] = (r == lane ? 1.f : 0.f) - acc;
+      }
+#pragma unroll
+      for (int r = 0; r < 16; ++r) sAf[(base + r) * 65 + base + lane] = col[r];
+    }
+    sync4();
+    float* sY = sP + w * 256;                      // per-warp 16 x 8 scratch
+    const int I = w < 2 ? 1 : 3, J = I - 1, n0 = 16 * J + 8 * (w & 1);
+    float c[4] = {0.f, 0.f, 0.f, 0.f};
+    mma16x8x16_f32(c, sT, 65, 16 * I, 16 * J, sAf, 65, 16 * J, n0);
+    store_tile(sY, 8, 0, 0, c, -1.f);              // -T_IJ Dinv_J
+    __syncwarp();
+    float d[4] = {0.f, 0.f, 0.f, 0.f};
+    mma16x8x16_f32(d, sAf, 65, 16 * I, 16 * I, sY, 8, 0, 0);
+    store_tile(sAf, 65, 16 * I, n0, d, 1.f);       // A_IJ
+  }
+  sync8();
+  const int r0 = 32 + 16 * (w >> 2), n0 = 8 * (w & 3);
+  {
+    float c[4] = {0.f, 0.f, 0.f, 0.f};
+    if (n0 < 16) mma16x8x16_f32(c, sT, 65, r0, 0, sAf, 65, 0, n0);   // A1 rows 0..15 vanish past column 15
+    mma16x8x16_f32(c, sT, 65, r0, 16, sAf, 65, 16, n0);
+    store_tile(sX, 33, r0 - 32, n0, c, -1.f);
+  }
+  sync8();
+  {
+    float d[4] = {0.f, 0.f, 0.f, 0.f};
+    mma16x8x16_f32(d, sAf, 65, r0, 32, sX, 33, 0, n0);                // A2 columns 32..47
+    if (r0 == 48) mma16x8x16_f32(d, sAf, 65, r0, 48, sX, 33, 16, n0);  // rows 48.. also see 48..63
+    store_tile(sAf, 65, r0, n0, d, 1.f);
+  }
+  sync8();
+}
+
 }  // namespace gdr
