@@ -188,38 +188,41 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc::mma_bf16(d1, dQY + (ka >> 4), dS + (((k0 / 8) * 1024) >> 4), id1, k0 > 0);
           }
           tc::commit(bar(kBW));
+        } else {
+          *abort_flag = 1;   // the waits of the W warps below give up at once
         }
       }
-      if (tc::named_any(kChainBar, 128, !ok)) { fail = 4 * n; break; }
-      // gamma_C and this thread's row of U, read while MMA1 runs; W is
-      // rewritten below only after MMA3 of chunk n-1 (which reads it) is done
-      const float gc = reinterpret_cast<const float*>(sst + P::oGc)[srow];
-      uint4 ur[kNV / 8];
+      // Two barriers per chunk (after W, after S_{n+1}); a wait that fails
+      // skips the work behind it and votes in the next barrier, which every
+      // chain thread reaches, so all leave together.
+      // W = U + (-Y S_n) -> bf16 operand (warps 2-3), once MMA1 has completed
+      // and MMA3 of chunk n-1 (which reads the previous W) is done.
+      float gc = 0.f;
       if (wrole) {
+        ok = wait_or_abort(bar(kBW), n & 1, abort_flag);
+        if (ok && n >= 1) ok = wait_or_abort(bar(kBO0 + ((n - 1) & 1)), ((n - 1) >> 1) & 1, abort_flag);
+        if (ok) {
+          tc::fence_after_sync();
+          gc = reinterpret_cast<const float*>(sst + P::oGc)[srow];
+          uint4 ur[kNV / 8];
 #pragma unroll
-        for (int j = 0; j < kNV / 8; ++j)
-          ur[j] = *reinterpret_cast<const uint4*>(sst + P::kCommon + tc::tile_off(64, wrow, 8 * j));
-      }
-      if (n >= 1) ok = wait_or_abort(bar(kBO0 + ((n - 1) & 1)), ((n - 1) >> 1) & 1, abort_flag);
-      if (ok) ok = wait_or_abort(bar(kBW), n & 1, abort_flag);
-      if (tc::named_any(kChainBar, 128, !ok)) { fail = 4 * n + 1; break; }
-      tc::fence_after_sync();
-      // W = U + (-Y S_n) -> bf16 operand
-      if (wrole) {
-        float x[kNV];
-        tc::tmem_ld64(tlane + D10 + (n & 1) * 64, x);
+          for (int j = 0; j < kNV / 8; ++j)
+            ur[j] = *reinterpret_cast<const uint4*>(sst + P::kCommon + tc::tile_off(64, wrow, 8 * j));
+          float x[kNV];
+          tc::tmem_ld64(tlane + D10 + (n & 1) * 64, x);
 #pragma unroll
-        for (int j = 0; j < kNV / 8; ++j) {
-          float u[8];
-          unpack8(ur[j], u);
+          for (int j = 0; j < kNV / 8; ++j) {
+            float u[8];
+            unpack8(ur[j], u);
 #pragma unroll
-          for (int i = 0; i < 8; ++i) x[8 * j + i] += u[i];
-          *reinterpret_cast<uint4*>(smem + L::oW + tc::tile_off(64, wrow, 8 * j)) = pack8(x + 8 * j);
+            for (int i = 0; i < 8; ++i) x[8 * j + i] += u[i];
+            *reinterpret_cast<uint4*>(smem + L::oW + tc::tile_off(64, wrow, 8 * j)) = pack8(x + 8 * j);
+          }
+          tc::fence_proxy_async();
         }
       }
-      tc::fence_proxy_async();
       tc::fence_before_sync();
-      tc::named_sync(kChainBar, 128);
+      if (tc::named_any(kChainBar, 128, !ok)) { fail = 4 * n + 1; break; }
       // MMA2: K_tail^T W into D_S (the output role issues MMA3 once it completes)
       if (tid == 0) {
         tc::fence_after_sync();
@@ -232,11 +235,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         tc::commit(bar(kBS));
       }
+      // S_{n+1} = Diag(gamma_C) S_n + K_tail^T W (MMA2 completing implies that
+      // MMA1 ran, so the stage had landed for the gamma_C read)
       ok = wait_or_abort(bar(kBS), n & 1, abort_flag);
-      if (tc::named_any(kChainBar, 128, !ok)) { fail = 4 * n + 2; break; }
-      tc::fence_after_sync();
-      // S_{n+1} = Diag(gamma_C) S_n + K_tail^T W
-      {
+      if (ok) {
+        tc::fence_after_sync();
+        if (!wrole) gc = reinterpret_cast<const float*>(sst + P::oGc)[srow];
         float x[kNV];
         tc::tmem_ld64(tlane + DS, x);
 #pragma unroll
@@ -246,10 +250,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int j = 0; j < kNV; j += 8)
             *reinterpret_cast<uint4*>(smem + L::oS + tc::tile_off(DK, srow, j)) = pack8(S + j);
         }
+        tc::fence_proxy_async();
       }
-      tc::fence_proxy_async();
       tc::fence_before_sync();
-      tc::named_sync(kChainBar, 128);
+      if (tc::named_any(kChainBar, 128, !ok)) { fail = 4 * n + 2; break; }
       // the chain is done with chunk n's stage (its MMAs completed with D_S)
       if (tid == 0) tc::mbar_arrive(bar(kEmpty0 + s));
     }
