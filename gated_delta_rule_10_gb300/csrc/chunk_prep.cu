@@ -12,7 +12,8 @@
 //           memory, the value side as soon as its M2 is; the chunk after is
 //           prefetched into L2 meanwhile
 //   gates   G = in-chunk cumsum of g (per key channel or per row), gamma_C
-//   tiles   gated in place: Z = z over v; E_bar = f (.) e, Q' = s f (.) q,
+//   tiles   (scalar gates: see prep_keys_scalar) gated in place: Z = z over v;
+//           E_bar = f (.) e, Q' = s f (.) q,
 //           K_bar = f^-1 (.) k over b (or a free slot), q and k; E_abs = gamma (.) e
 //           over w (after Z has used it); Q_gamma = s gamma (.) q and
 //           K_tail = gamma_C / gamma (.) k straight to the packet
@@ -203,6 +204,45 @@ __device__ __forceinline__ void prep_keys(unsigned char* smem, unsigned char* pk
   }
 }
 
+// Scalar gates (no channel decay, erase or write gate): beta folds into the rows
+// of T and the columns of A, the scale into A_qk, so q, k and v stay as
+// loaded and only three tiles are formed per element: E_abs' = e^{G_r} x_r
+// (x = k, or k + lam q), Q_gamma and K_tail (packet). k sits in the E slot;
+// under QMIX x replaces it there and k moves to the K slot.
+template <int DK, int DV, bool QM>
+__device__ __forceinline__ void prep_keys_scalar(unsigned char* smem, unsigned char* pkt,
+                                                 const ChunkArgs& a, const float* sLam,
+                                                 const float* sEG, const float* sEGL) {
+  using L = PrepLayout<DK, DV>;
+  using P = Packet<DK, DV>;
+  constexpr int VK = DK / 8, RB = kThreads / VK, RPB = 64 / RB;
+  const int tid = threadIdx.x, rb = tid / VK, c0 = (tid % VK) * 8, r0 = rb * RPB;
+#pragma unroll
+  for (int i = 0; i < RPB; ++i) {
+    const int r = r0 + i;
+    float qv[8], kv[8];
+    unpack8(ld16(smem, L::oEQ + tc::tile_off(128, 64 + r, c0)), qv);
+    const uint4 kraw = ld16(smem, L::oEQ + tc::tile_off(128, r, c0));
+    unpack8(kraw, kv);
+    const float lam = sLam[r], eg = sEG[r], egl = sEGL[r], sq = a.scale * eg;
+    float x[8], Ea[8], Qg[8], Kt[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      x[j] = QM ? kv[j] + lam * qv[j] : kv[j];
+      Ea[j] = eg * x[j];
+      Qg[j] = sq * qv[j];
+      Kt[j] = egl * kv[j];
+    }
+    if (QM) {
+      st16(smem, L::oEQ + tc::tile_off(128, r, c0), pack8(x));
+      st16(smem, L::oK + tc::tile_off(64, r, c0), kraw);
+    }
+    st16(smem, L::oEa + tc::tile_off(64, r, c0), pack8(Ea));
+    st16(pkt, P::oQY + tc::tile_off(128, r, c0), pack8(Qg));
+    st16(pkt, P::oKt + tc::tile_off(64, r, c0), pack8(Kt));
+  }
+}
+
 // Z = beta v (or w (.) v with the write gate), in place over v.
 template <int DK, int DV, bool WR>
 __device__ __forceinline__ void prep_z(unsigned char* smem, const float* sBeta) {
@@ -229,7 +269,7 @@ __device__ __forceinline__ void prep_z(unsigned char* smem, const float* sBeta) 
   }
 }
 
-template <int DK, int DV>
+template <int DK, int DV, bool SC>
 __global__ void __launch_bounds__(kThreads, 2)
     chunk_prep_kernel(const ChunkArgs a, const __grid_constant__ CUtensorMap tm_q,
                       const __grid_constant__ CUtensorMap tm_k,
@@ -311,7 +351,10 @@ __global__ void __launch_bounds__(kThreads, 2)
 #pragma unroll
     for (int blk = 0; blk < DK / 64; ++blk) {
       tc::tma_load_4d(sbase + L::oEQ + blk * 16384 + 8192, &tm_q, blk * 64, h, n * kChunk, bb, bar(kBarK));
-      tc::tma_load_4d(sbase + L::oK + blk * 8192, &tm_k, blk * 64, h, n * kChunk, bb, bar(kBarK));
+      if (SC)
+        tc::tma_load_4d(sbase + L::oEQ + blk * 16384, &tm_k, blk * 64, h, n * kChunk, bb, bar(kBarK));
+      else
+        tc::tma_load_4d(sbase + L::oK + blk * 8192, &tm_k, blk * 64, h, n * kChunk, bb, bar(kBarK));
       if (ER) tc::tma_load_4d(sbase + L::oEQ + blk * 16384, &tm_b, blk * 64, h, n * kChunk, bb, bar(kBarK));
     }
     if (w + gridDim.x < total) {
@@ -395,14 +438,21 @@ __global__ void __launch_bounds__(kThreads, 2)
 
     if (__syncthreads_or(!tc::mbar_wait(bar(kBarV), par))) { fail_at = 4 * n; break; }
     v_done = v_issued;
-    if (WR)
-      prep_z<DK, DV, true>(smem, sBeta);
-    else
-      prep_z<DK, DV, false>(smem, sBeta);
-    __syncthreads();   // w has been read: its slot takes E_abs below
+    if (!SC) {
+      if (WR)
+        prep_z<DK, DV, true>(smem, sBeta);
+      else
+        prep_z<DK, DV, false>(smem, sBeta);
+      __syncthreads();   // w has been read: its slot takes E_abs below
+    }
     if (__syncthreads_or(!tc::mbar_wait(bar(kBarK), par))) { fail_at = 4 * n; break; }
     k_done = k_issued;
-    switch (a.flags & 11u) {   // CH | ER | QM select the key-side tiles
+    if (SC) {
+      if (QM)
+        prep_keys_scalar<DK, DV, true>(smem, pkt, a, sLam, sEG, sEGL);
+      else
+        prep_keys_scalar<DK, DV, false>(smem, pkt, a, sLam, sEG, sEGL);
+    } else switch (a.flags & 11u) {   // CH | ER | QM select the key-side tiles
 #define GDR_PREP(F)                                                                       \
   case F:                                                                                 \
     prep_keys<DK, DV, (F & 1u) != 0, (F & 2u) != 0, (F & 8u) != 0>(smem, pkt, a, sPart, sBeta, \
@@ -421,11 +471,14 @@ __global__ void __launch_bounds__(kThreads, 2)
       tc::fence_after_sync();
       constexpr uint32_t id = tc::idesc_bf16(128, 64, 0, 0);
       const uint64_t dEQ = tc::smem_desc(sbase + L::oEQ, 16, 1024);
-      const uint64_t dKb = tc::smem_desc(sbase + L::oK, 16, 1024);
+      // K_bar: the K slot, or for scalar gates without QMIX k itself in the E slot
+      const bool kInE = SC && !QM;
+      const uint64_t dKb = tc::smem_desc(sbase + (kInE ? L::oEQ : L::oK), 16, 1024);
+      const uint32_t kBlk = kInE ? 16384u : 8192u;
 #pragma unroll
       for (int k0 = 0; k0 < DK; k0 += 16) {
         const uint32_t ka = (k0 >> 6) * 16384 + (k0 & 63) * 2;
-        const uint32_t kb = (k0 >> 6) * 8192 + (k0 & 63) * 2;
+        const uint32_t kb = (k0 >> 6) * kBlk + (k0 & 63) * 2;
         tc::mma_bf16(tmem, dEQ + (ka >> 4), dKb + (kb >> 4), id, k0 > 0);
       }
       tc::commit(bar(kBarM1));
@@ -442,6 +495,11 @@ __global__ void __launch_bounds__(kThreads, 2)
       const int lim = isT ? r : r + 1;       // T strictly lower, A_qk with the diagonal
       float x[32];
       tc::tmem_ld32(tmem + (static_cast<uint32_t>(32 * q) << 16) + c, x);
+      if (SC) {   // the row factors the scalar-gate tiles left out: beta_r (T), s (A_qk)
+        const float f = isT ? sBeta[r] : a.scale;
+#pragma unroll
+        for (int j = 0; j < 32; ++j) x[j] *= f;
+      }
       if (CH) {
 #pragma unroll
         for (int j = 0; j < 32; ++j) x[j] = select_f32(c + j < lim, x[j], 0.f);
@@ -475,6 +533,10 @@ __global__ void __launch_bounds__(kThreads, 2)
       float x[8];
 #pragma unroll
       for (int j = 0; j < 8; ++j) x[j] = select_f32(c0 + j <= r, sAf[r * 65 + c0 + j], 0.f);
+      if (SC) {   // A diag(beta): U = A diag(beta) V, Y = A diag(beta) (e^G x)
+#pragma unroll
+        for (int j = 0; j < 8; ++j) x[j] *= sBeta[c0 + j];
+      }
       st16(smem, L::oA + tc::tile_off(64, r, c0), pack8(x));
     }
     tc::fence_proxy_async();
@@ -554,9 +616,9 @@ __global__ void __launch_bounds__(kThreads, 2)
   if (warp == 0) tc::tmem_dealloc(tmem, L::kTmemCols);
 }
 
-template <int DK, int DV>
-cudaError_t launch_prep(const ChunkArgs& a, unsigned char* packets, int* status,
-                        cudaStream_t stream) {
+template <int DK, int DV, bool SC>
+cudaError_t launch_prep_kernel(const ChunkArgs& a, unsigned char* packets, int* status,
+                               cudaStream_t stream) {
   using L = PrepLayout<DK, DV>;
   static_assert(2 * (L::launch_bytes + 1024) <= 233472, "two CTAs per SM");
   CUtensorMap tq, tk, tv, tb, tw;
@@ -567,7 +629,7 @@ cudaError_t launch_prep(const ChunkArgs& a, unsigned char* packets, int* status,
   tw = tq;
   if ((a.flags & 2u) && !make_bthd_tmap(&tb, a.b, a.B, a.T, a.H, DK)) return cudaErrorInvalidValue;
   if ((a.flags & 4u) && !make_bthd_tmap(&tw, a.w, a.B, a.T, a.H, DV)) return cudaErrorInvalidValue;
-  auto kern = chunk_prep_kernel<DK, DV>;
+  auto kern = chunk_prep_kernel<DK, DV, SC>;
   cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(L::launch_bytes));
   if (err != cudaSuccess) return err;
@@ -580,6 +642,13 @@ cudaError_t launch_prep(const ChunkArgs& a, unsigned char* packets, int* status,
   const int grid = static_cast<int>(total < 2LL * sms ? total : 2LL * sms);
   kern<<<grid, kThreads, L::launch_bytes, stream>>>(a, tq, tk, tv, tb, tw, packets, status);
   return cudaGetLastError();
+}
+
+template <int DK, int DV>
+cudaError_t launch_prep(const ChunkArgs& a, unsigned char* packets, int* status,
+                        cudaStream_t stream) {
+  if ((a.flags & 7u) == 0) return launch_prep_kernel<DK, DV, true>(a, packets, status, stream);
+  return launch_prep_kernel<DK, DV, false>(a, packets, status, stream);
 }
 
 }  // namespace
