@@ -7,8 +7,8 @@
 //   S_{n+1} = Diag(gamma_C,n) S_n + K_tail,n^T W_n
 //
 // One CTA owns one (batch, head) and a 64-wide slice of value columns, and
-// walks the chunks in order with S_n (d_k x 64, fp32) in registers, one key
-// channel per thread. Issuing a tensor-core instruction costs far more than
+// walks the chunks in order with S_n (d_k x 64, fp32) in registers: one key
+// channel and 32 value columns per thread. Issuing a tensor-core instruction costs far more than
 // these small products take to run, so each chunk uses three MMA groups:
 //   MMA1  [Q_gamma; -Y] S_n  -> D1[n%2]   (M=128: Q_gamma S_n in lanes 0..63,
 //                                          -Y S_n in lanes 64..127)
@@ -18,11 +18,13 @@
 //                                          follows it in the stage and only
 //                                          touch lanes 64..127, already consumed
 //                                          and overwritten by the next MMA1)
-// Roles (192 threads):
-//   warps 0-3  the state chain; thread 0 issues MMA1 and MMA2; warps 2-3 form
-//              W; all four update S_{n+1} = gamma_C S_n + D_S
-//   warps 4-5  the output: thread 128 issues MMA3, both warps move O_n from
-//              D1[n%2] to o, and thread 128 refills the three-stage packet
+// Roles (320 threads):
+//   warps 0-7  the state chain, two warps per tensor-memory lane quadrant
+//              (value columns 0..31 and 32..63); thread 0 issues MMA1 and
+//              MMA2; warps 2, 3, 6, 7 form W; all eight update
+//              S_{n+1} = gamma_C S_n + D_S
+//   warps 8-9  the output: thread 256 issues MMA3, both warps move O_n from
+//              D1[n%2] to o, and thread 256 refills the three-stage packet
 //              ring with plain bulk copies
 // Every wait is bounded; a wait that gives up makes all roles leave together,
 // release tensor memory and report GDR_ERR_TIMEOUT.
@@ -34,11 +36,14 @@
 namespace gdr {
 namespace {
 
-constexpr int kThreads = 192;
+constexpr int kThreads = 320;
+constexpr int kOut = 256;       // first thread of the output role
 constexpr int kNV = 64;
 constexpr int kStages = 3;
 constexpr uint32_t kTmemCols = 256;
 constexpr uint32_t kChainBar = 1, kOutBar = 2;
+constexpr uint32_t kChainThreads = 256;
+constexpr int kHalf = 32;        // value columns per chain thread
 
 // TMEM columns: two stacked [O; W] accumulators (M=128), the state update
 constexpr uint32_t D10 = 0, DS = 128;
@@ -132,7 +137,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tlane = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);
   int fail = -1;
 
-  // packet of chunk n into its ring stage (thread 128 only)
+  // packet of chunk n into its ring stage (thread kOut only)
   auto load_chunk = [&](int n) {
     const int s = n % kStages;
     const uint32_t st = sb + L::oStage + s * L::kStage;
@@ -142,28 +147,30 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc::bulk_load(st + P::kCommon, pk + P::oU + slice * P::kUSlice, P::kUSlice, bar(kFull0 + s));
   };
 
-  if (warp < 4) {
+  if (warp < 8) {
     // ------------------------------------------------------------ state chain
+    // warp w: tensor-memory lane quadrant w % 4, value columns 32 (w / 4) .. +31
+    const int q = warp & 3, cb = 32 * (warp >> 2);
     const bool owner = (DK == 128) || (lane < 16);
-    const int srow = (DK == 128) ? tid : warp * 16 + (lane & 15);
-    const bool wrole = warp >= 2;               // warps 2-3 hold lanes 64..127 = -Y S_n
-    const int wrow = tid - 64;                  // token row of W for those warps
-    float S[kNV];
+    const int srow = (DK == 128) ? 32 * q + lane : 16 * q + (lane & 15);
+    const bool wrole = q >= 2;                  // lanes 64..127 of D1 = -Y S_n
+    const int wrow = 32 * (q - 2) + lane;       // token row of W for those warps
+    float S[kHalf];
     {
-      const size_t base = ((size_t(bb) * H + h) * DK + srow) * DV + col0;
+      const size_t base = ((size_t(bb) * H + h) * DK + srow) * DV + col0 + cb;
 #pragma unroll
-      for (int j = 0; j < kNV; j += 4) {
+      for (int j = 0; j < kHalf; j += 4) {
         float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
         if (a.h0 && owner) x = *reinterpret_cast<const float4*>(a.h0 + base + j);
         S[j] = x.x; S[j + 1] = x.y; S[j + 2] = x.z; S[j + 3] = x.w;
       }
       if (owner) {
 #pragma unroll
-        for (int j = 0; j < kNV; j += 8)
-          *reinterpret_cast<uint4*>(smem + L::oS + tc::tile_off(DK, srow, j)) = pack8(S + j);
+        for (int j = 0; j < kHalf; j += 8)
+          *reinterpret_cast<uint4*>(smem + L::oS + tc::tile_off(DK, srow, cb + j)) = pack8(S + j);
       }
       tc::fence_proxy_async();
-      tc::named_sync(kChainBar, 128);
+      tc::named_sync(kChainBar, kChainThreads);
     }
     const uint64_t dS = tc::smem_desc(sb + L::oS, DK * 128, 1024);
     const uint64_t dW = tc::smem_desc(sb + L::oW, 64 * 128, 1024);
@@ -204,25 +211,25 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (ok) {
           tc::fence_after_sync();
           gc = reinterpret_cast<const float*>(sst + P::oGc)[srow];
-          uint4 ur[kNV / 8];
+          uint4 ur[kHalf / 8];
 #pragma unroll
-          for (int j = 0; j < kNV / 8; ++j)
-            ur[j] = *reinterpret_cast<const uint4*>(sst + P::kCommon + tc::tile_off(64, wrow, 8 * j));
-          float x[kNV];
-          tc::tmem_ld64(tlane + D10 + (n & 1) * 64, x);
+          for (int j = 0; j < kHalf / 8; ++j)
+            ur[j] = *reinterpret_cast<const uint4*>(sst + P::kCommon + tc::tile_off(64, wrow, cb + 8 * j));
+          float x[kHalf];
+          tc::tmem_ld32(tlane + D10 + (n & 1) * 64 + cb, x);
 #pragma unroll
-          for (int j = 0; j < kNV / 8; ++j) {
+          for (int j = 0; j < kHalf / 8; ++j) {
             float u[8];
             unpack8(ur[j], u);
 #pragma unroll
             for (int i = 0; i < 8; ++i) x[8 * j + i] += u[i];
-            *reinterpret_cast<uint4*>(smem + L::oW + tc::tile_off(64, wrow, 8 * j)) = pack8(x + 8 * j);
+            *reinterpret_cast<uint4*>(smem + L::oW + tc::tile_off(64, wrow, cb + 8 * j)) = pack8(x + 8 * j);
           }
           tc::fence_proxy_async();
         }
       }
       tc::fence_before_sync();
-      if (tc::named_any(kChainBar, 128, !ok)) { fail = 4 * n + 1; break; }
+      if (tc::named_any(kChainBar, kChainThreads, !ok)) { fail = 4 * n + 1; break; }
       // MMA2: K_tail^T W into D_S (the output role issues MMA3 once it completes)
       if (tid == 0) {
         tc::fence_after_sync();
@@ -241,33 +248,33 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (ok) {
         tc::fence_after_sync();
         if (!wrole) gc = reinterpret_cast<const float*>(sst + P::oGc)[srow];
-        float x[kNV];
-        tc::tmem_ld64(tlane + DS, x);
+        float x[kHalf];
+        tc::tmem_ld32(tlane + DS + cb, x);
 #pragma unroll
-        for (int j = 0; j < kNV; ++j) S[j] = gc * S[j] + x[j];
+        for (int j = 0; j < kHalf; ++j) S[j] = gc * S[j] + x[j];
         if (owner) {
 #pragma unroll
-          for (int j = 0; j < kNV; j += 8)
-            *reinterpret_cast<uint4*>(smem + L::oS + tc::tile_off(DK, srow, j)) = pack8(S + j);
+          for (int j = 0; j < kHalf; j += 8)
+            *reinterpret_cast<uint4*>(smem + L::oS + tc::tile_off(DK, srow, cb + j)) = pack8(S + j);
         }
         tc::fence_proxy_async();
       }
       tc::fence_before_sync();
-      if (tc::named_any(kChainBar, 128, !ok)) { fail = 4 * n + 2; break; }
+      if (tc::named_any(kChainBar, kChainThreads, !ok)) { fail = 4 * n + 2; break; }
       // the chain is done with chunk n's stage (its MMAs completed with D_S)
       if (tid == 0) tc::mbar_arrive(bar(kEmpty0 + s));
     }
     if (fail < 0 && a.hT && owner) {
-      const size_t base = ((size_t(bb) * H + h) * DK + srow) * DV + col0;
+      const size_t base = ((size_t(bb) * H + h) * DK + srow) * DV + col0 + cb;
 #pragma unroll
-      for (int j = 0; j < kNV; j += 4)
+      for (int j = 0; j < kHalf; j += 4)
         *reinterpret_cast<float4*>(a.hT + base + j) = make_float4(S[j], S[j + 1], S[j + 2], S[j + 3]);
     }
   } else {
     // ------------------------------------------------------------ output
-    const int orow = tid - 128;                 // lanes 0..63 of D1 = rows of O_n
+    const int orow = tid - kOut;                // lanes 0..63 of D1 = rows of O_n
     int issued = 0;
-    if (tid == 128) {
+    if (tid == kOut) {
       for (int n = 0; n < min(kStages, n_chunks); ++n) load_chunk(n);
       issued = min(kStages, n_chunks);
     }
@@ -275,7 +282,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int s = n % kStages;
       const uint32_t st = sb + L::oStage + s * L::kStage;
       bool ok = true;
-      if (tid == 128) {
+      if (tid == kOut) {
         // MMA3: [A_qk; *] W onto D1[n%2] once MMA2 (which reads the same W) has
         // completed, so that MMA3 runs while the chain updates S instead of
         // delaying MMA2 in the tensor pipe
@@ -310,7 +317,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       tc::fence_before_sync();
       tc::named_sync(kOutBar, 64);
-      if (tid == 128) {
+      if (tid == kOut) {
         tc::mbar_arrive(bar(kOFree0 + (n & 1)));
         tc::mbar_arrive(bar(kEmpty0 + s));
         // refill the stage once the chain has released it too
@@ -326,7 +333,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     // let the copies already issued land before the CTA can exit (a plain
     // bounded wait: an abort elsewhere does not stop a copy in flight)
-    if (tid == 128)
+    if (tid == kOut)
       for (int n = max(0, issued - kStages); n < issued; ++n)
         tc::mbar_wait(bar(kFull0 + n % kStages), (n / kStages) & 1);
   }
