@@ -181,10 +181,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t d1 = tmem + D10 + (n & 1) * 64;
       bool ok = true;
       if (tid == 0) {
-        // MMA1 once the packet has landed and D1[n%2] has been read out (chunk n-2)
-        ok = wait_or_abort(bar(kFull0 + s), (n / kStages) & 1, abort_flag);
-        if (ok && n >= 2)
-          ok = wait_or_abort(bar(kOFree0 + (n & 1)), ((n - 2) >> 1) & 1, abort_flag);
+        // MMA1 once the packet has landed and D1[n%2] has been read out (chunk
+        // n-2); for n > 0 thread 0 waited for both while chunk n-1 formed W
+        if (n == 0) ok = wait_or_abort(bar(kFull0), 0, abort_flag);
         if (ok) {
           tc::fence_after_sync();
           constexpr uint32_t id1 = tc::idesc_bf16(128, kNV, 0, 1);
@@ -227,6 +226,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           tc::fence_proxy_async();
         }
+      }
+      if (tid == 0 && n + 1 < n_chunks) {
+        // meanwhile: the next chunk's packet and its D1 buffer (read out for chunk n-1)
+        ok = wait_or_abort(bar(kFull0 + (n + 1) % kStages), ((n + 1) / kStages) & 1, abort_flag);
+        if (ok && n >= 1)
+          ok = wait_or_abort(bar(kOFree0 + ((n + 1) & 1)), ((n - 1) >> 1) & 1, abort_flag);
       }
       tc::fence_before_sync();
       if (tc::named_any(kChainBar, kChainThreads, !ok)) { fail = 4 * n + 1; break; }
