@@ -275,6 +275,8 @@ def run_ours(args):
                        "ms_mean": round(statistics.mean(dec_ms), 4),
                        "achieved_gbs": round(dgbs, 1), "frac_hbm": round(dgbs / pk["hbm_gbs"], 4)}
 
+    epilogue_info = measure_epilogue(gdr, o, c, dev, stream, flush, K, pk)
+
     e2e = None if args.no_e2e else measure_e2e(gdr, x, y, c, dev, args, B, T, H, dk, dv, N)
 
     result = {
@@ -290,6 +292,7 @@ def run_ours(args):
                    "parallelism": "replica per GPU" if world > 1 else "single GPU"},
         "roofline": roof,
         "decode": decode_info,
+        "epilogue": epilogue_info,
         # this library's kernels per timed step: the two-kernel chunked forward
         # (bf16 with the full workspace) or one fused kernel (fp32), then the
         # decode steps
@@ -303,6 +306,34 @@ def run_ours(args):
         print(json.dumps(result), flush=True)
     if world > 1:
         torch.distributed.destroy_process_group()
+
+
+def measure_epilogue(gdr, o, c, dev, stream, flush, K, pk, eps=1e-6):
+    """The output epilogue (RMSNorm, gain, SiLU output gate) on the step's
+    read-out o, timed alone: K launches, L2 flushed before each, CUDA events on
+    the launching stream. Not part of the step or its metric."""
+    from gated_delta_rule_10_gb300 import workloads as wl
+    rows = o.numel() // c["dv"]
+    e = wl.epilogue_inputs(rows, c["dv"], c["dtype"], seed=11, device=dev)
+    y = torch.empty_like(e["z"])
+    o2 = o.reshape(rows, c["dv"])
+    for _ in range(3):
+        gdr.rmsnorm_gate(o2, e["z"], e["weight"], eps, out=y)
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(K)]
+    torch.cuda.synchronize()
+    for i in range(K):
+        flush.fill_(float(i))
+        ev[i][0].record(stream)
+        gdr.rmsnorm_gate(o2, e["z"], e["weight"], eps, out=y)
+        ev[i][1].record(stream)
+    torch.cuda.synchronize()
+    ms = statistics.mean(ev[i][0].elapsed_time(ev[i][1]) for i in range(K))
+    nbytes = tensor_bytes(o2, e["z"], y, e["weight"])
+    gbs = nbytes / (ms / 1e3) / 1e9
+    return {"kernel": "rmsnorm_gate_kernel", "rows": rows, "dv": c["dv"], "launches": K,
+            "ms_mean": round(ms, 4), "algorithmic_bytes_per_launch": nbytes,
+            "achieved_gbs": round(gbs, 1), "frac_hbm": round(gbs / pk["hbm_gbs"], 4),
+            "l2": "flushed before every launch"}
 
 
 def measure_e2e(gdr, x, y, c, dev, args, B, T, H, dk, dv, N, steps=5):

@@ -58,12 +58,14 @@ def lib():
         L.gdr_recurrent_step.argtypes = [sp] + [_vp] * 10 + [_vp]
         L.gdr_gate_cumsum.argtypes = [ctypes.c_int] * 4 + [_vp, _vp, _vp]
         L.gdr_chunk_fwd_check.argtypes = [_vp, _vp, ctypes.POINTER(ctypes.c_int)]
+        L.gdr_rmsnorm_gate.argtypes = [ctypes.c_longlong, ctypes.c_int, ctypes.c_int, _vp, _vp,
+                                       _vp, ctypes.c_float, _vp, _vp]
         L.gdr_status_string.argtypes = [ctypes.c_int]
         L.gdr_status_string.restype = ctypes.c_char_p
         L.gdr_abi_version.restype = ctypes.c_int
         for name in ("gdr_chunk_fwd_workspace", "gdr_chunk_fwd_workspace_min", "gdr_chunk_fwd",
                      "gdr_recurrent_step",
-                     "gdr_gate_cumsum", "gdr_chunk_fwd_check"):
+                     "gdr_gate_cumsum", "gdr_chunk_fwd_check", "gdr_rmsnorm_gate"):
             getattr(L, name).restype = ctypes.c_int
         _lib = L
     return _lib
@@ -239,4 +241,31 @@ def gate_cumsum(g, chunk=CHUNK, out=None, stream=None):
         st = lib().gdr_gate_cumsum(B, T, X, chunk, _ptr(g), _ptr(out), _stream(stream, g.device))
     if st:
         raise GdrError(st, "gdr_gate_cumsum")
+    return out
+
+
+def rmsnorm_gate(o, z, weight, eps=1e-6, *, out=None, stream=None):
+    """Output epilogue (``gdr_rmsnorm_gate``): RMSNorm of o over its last axis
+    (d_v), times ``weight``, times silu(z).
+
+    o, z: [..., d_v] bf16 or fp32 (one dtype, contiguous); weight: [d_v] fp32.
+    ``out`` may be o or z itself (in place); by default a new tensor.
+    """
+    dv = o.shape[-1]
+    dev, dt = o.device, o.dtype
+    if dt not in (torch.bfloat16, torch.float32):
+        raise ValueError("o and z must be bf16 or fp32")
+    _check(o, "o", dt, dev)
+    _check(z, "z", dt, dev, tuple(o.shape))
+    _check(weight, "weight", torch.float32, dev, (dv,))
+    if out is None:
+        out = torch.empty_like(o)
+    _check(out, "out", dt, dev, tuple(o.shape))
+    rows = o.numel() // dv if dv else 0
+    with torch.cuda.device(dev):
+        st = lib().gdr_rmsnorm_gate(rows, dv, GDR_BF16 if dt == torch.bfloat16 else GDR_F32,
+                                    _ptr(o), _ptr(z), _ptr(weight), ctypes.c_float(eps),
+                                    _ptr(out), _stream(stream, dev))
+    if st:
+        raise GdrError(st, "gdr_rmsnorm_gate")
     return out

@@ -13,7 +13,7 @@
 
 namespace {
 
-constexpr int kAbiVersion = 1;
+constexpr int kAbiVersion = 2;
 constexpr long long kMaxElems = std::numeric_limits<int>::max();
 
 bool aligned(const void* p, uintptr_t n) { return (reinterpret_cast<uintptr_t>(p) % n) == 0; }
@@ -191,6 +191,31 @@ gdr_status gdr_gate_cumsum(int B, int T, int X, int chunk, const float* g, float
   if (B > 65535) return GDR_ERR_UNSUPPORTED;
   const cudaError_t err =
       gdr::launch_gate_cumsum(g, G, B, T, X, reinterpret_cast<cudaStream_t>(stream));
+  return err == cudaSuccess ? GDR_OK : GDR_ERR_CUDA;
+}
+
+gdr_status gdr_rmsnorm_gate(long long rows, int dv, gdr_dtype dtype, const void* o,
+                            const void* z, const float* weight, float eps, void* y,
+                            gdr_stream_t stream) {
+  if (rows < 0 || dv < 1) return GDR_ERR_INVALID_ARG;
+  if (dtype != GDR_F32 && dtype != GDR_BF16) return GDR_ERR_INVALID_ARG;
+  if (!std::isfinite(eps) || eps < 0.f) return GDR_ERR_INVALID_ARG;
+  if (dv != 64 && dv != 128 && dv != 256) return GDR_ERR_UNSUPPORTED;
+  if (rows > (1LL << 40)) return GDR_ERR_UNSUPPORTED;
+  if (rows == 0) return GDR_OK;
+  if (!o || !z || !weight || !y) return GDR_ERR_INVALID_ARG;
+  if (!aligned(o, 16) || !aligned(z, 16) || !aligned(weight, 16) || !aligned(y, 16))
+    return GDR_ERR_INVALID_ARG;
+  // y is o itself, z itself, or apart from both
+  const uintptr_t bytes = static_cast<uintptr_t>(rows) * dv * (dtype == GDR_F32 ? 4 : 2);
+  const uintptr_t py = reinterpret_cast<uintptr_t>(y);
+  for (const void* src : {o, z}) {
+    const uintptr_t ps = reinterpret_cast<uintptr_t>(src);
+    if (ps != py && ps < py + bytes && py < ps + bytes) return GDR_ERR_INVALID_ARG;
+  }
+  const cudaError_t err = gdr::launch_rmsnorm_gate(o, z, weight, eps, y, rows, dv,
+                                                   dtype == GDR_F32,
+                                                   reinterpret_cast<cudaStream_t>(stream));
   return err == cudaSuccess ? GDR_OK : GDR_ERR_CUDA;
 }
 

@@ -69,6 +69,11 @@ cudaError_t launch_chunk_scan(const ChunkArgs& a, int dk, const unsigned char* p
                               int* status, cudaStream_t stream);
 cudaError_t launch_recurrent_step(const StepArgs& a, int dk, int dv, bool f32,
                                   cudaStream_t stream);
+// Output epilogue over `rows` rows of d_v channels (dv 64, 128 or 256):
+// y = o rsqrt(mean(o^2) + eps) weight silu(z); fp32 or bf16 rows, fp32 weight.
+cudaError_t launch_rmsnorm_gate(const void* o, const void* z, const float* weight, float eps,
+                                void* y, long long rows, int dv, bool f32,
+                                cudaStream_t stream);
 cudaError_t launch_gate_cumsum(const float* g, float* G, int B, int T, int X,
                                cudaStream_t stream);
 

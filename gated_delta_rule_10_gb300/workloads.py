@@ -26,6 +26,9 @@ Recipe (one per variant, drawn in fp32 on the CPU with a seeded
   gate w = sigmoid(N(0, 1)) per value channel, in the compute dtype.
 * Initial state (when asked for) ~ N(0, std^2) in fp32, layout
   [B, H, d_k, d_v].
+* Output epilogue: read-out rows o ~ N(0, 0.05^2) (RMSNorm makes the scale
+  immaterial), output-gate input z ~ N(0, 1), both in the compute dtype, and
+  a near-unit gain weight = 1 + 0.1 N(0, 1) per value channel in fp32.
 
 The five named workloads mirror the pages' 340M / 1.3B layer shapes.
 """
@@ -137,6 +140,15 @@ def decode_inputs(variant, N, H, dk, dv, dtype=torch.bfloat16, seed=0, h_std=0.0
     """One decode step's inputs: [N, 1, H, d] tensors plus a state [N, H, d_k, d_v]."""
     x = make_inputs(variant, N, 1, H, dk, dv, dtype, seed, False, h_std, device)
     return x
+
+
+def epilogue_inputs(rows, dv, dtype=torch.bfloat16, seed=0, device="cpu"):
+    """Inputs of the output epilogue: o, z [rows, d_v] and weight [d_v]."""
+    gen = torch.Generator().manual_seed(seed)
+    o = (0.05 * torch.randn(rows, dv, generator=gen)).to(dtype)
+    z = torch.randn(rows, dv, generator=gen).to(dtype)
+    weight = 1.0 + 0.1 * torch.randn(dv, generator=gen)
+    return {"o": o.to(device), "z": z.to(device), "weight": weight.to(device)}
 
 
 def token_heads(cfg_id):

@@ -216,6 +216,34 @@ gdr_status gdr_recurrent_step(const gdr_shape* shape, const void* q,
 gdr_status gdr_gate_cumsum(int B, int T, int X, int chunk, const float* g,
                            float* G, gdr_stream_t stream);
 
+/*
+ * Output epilogue after the read-out (Gated DeltaNet-2 notes, overall
+ * framework, the last stage of its flow chart; LLMs from scratch ch. 11,
+ * section 11.3: RMSNorm, then the SiLU output gate, before the heads merge).
+ * For each of `rows` rows of dv channels (rows = B * T * H for o of shape
+ * [B,T,H,dv], row-major, no padding):
+ *
+ *   y[r, c] = o[r, c] / sqrt(mean_c'(o[r, c']^2) + eps) * weight[c]
+ *             * z[r, c] * sigmoid(z[r, c])
+ *
+ *   o, z, y  [rows, dv] in `dtype` (GDR_BF16 or GDR_F32), device, 16-byte
+ *            aligned; the arithmetic is fp32 and y is rounded once
+ *   weight   [dv] fp32 device, 16-byte aligned: the RMSNorm gain, one value
+ *            per value channel, shared by every row
+ *   eps      finite, >= 0, added to the mean square (a row of zeros with
+ *            eps = 0 yields NaN)
+ *
+ * y may be o (in place) or z; any other overlap with them returns
+ * GDR_ERR_INVALID_ARG, as do null or misaligned pointers (when rows > 0),
+ * rows < 0, a bad dtype or a negative or non-finite eps. dv other than 64,
+ * 128 or 256 returns GDR_ERR_UNSUPPORTED. rows = 0 launches nothing. The
+ * caller owns every buffer; nothing is allocated and the stream is not
+ * synchronised.
+ */
+gdr_status gdr_rmsnorm_gate(long long rows, int dv, gdr_dtype dtype, const void* o,
+                            const void* z, const float* weight, float eps, void* y,
+                            gdr_stream_t stream);
+
 /* Static, human-readable name of a status code. */
 const char* gdr_status_string(gdr_status status);
 

@@ -182,3 +182,31 @@ def test_product_code_does_not_touch_the_oracle():
                 assert not re.search(r"\boracle\b\s*(import|\.)|from\s+oracle|import\s+oracle",
                                      text), f
                 assert "gdr_oracle" not in text, f
+
+
+def test_rmsnorm_gate_rejects_bad_arguments(L):
+    vp, F = ctypes.c_void_p, ctypes.c_float
+
+    def call(rows=4, dv=128, dtype=_binding.GDR_BF16, o=FAKE, z=FAKE + 0x4000, w=FAKE + 0x8000,
+             eps=1e-6, y=FAKE + 0xC000):
+        return L.gdr_rmsnorm_gate(rows, dv, dtype, vp(o) if o else None, vp(z) if z else None,
+                                  vp(w) if w else None, F(eps), vp(y) if y else None, None)
+
+    assert call(rows=0) == 0                       # nothing to do, nothing launched
+    assert call(rows=0, o=None, z=None, w=None, y=None) == 0
+    assert call(rows=-1) == 1
+    assert call(dv=0) == 1
+    assert call(dv=96) == 2
+    assert call(dv=512) == 2
+    assert call(dtype=5) == 1
+    assert call(eps=-1e-6) == 1
+    assert call(eps=float("inf")) == 1
+    assert call(eps=float("nan")) == 1
+    assert call(o=None) == 1
+    assert call(w=None) == 1
+    assert call(y=FAKE + 8) == 1                   # 16-byte alignment
+    assert call(w=FAKE + 0x8004) == 1
+    # 4 rows of 128 bf16 are 1 KiB: y overlapping o by part is refused
+    assert call(y=FAKE + 0x200) == 1
+    assert call(y=FAKE + 0x4000 - 0x200) == 1      # overlaps z
+    assert call(rows=1 << 41) == 2

@@ -112,6 +112,23 @@ def test_workload_full_size_sampled(cfg):
     assert torch.isfinite(o).all() and torch.isfinite(hT).all()
 
 
+@pytest.mark.parametrize("variant", ["gdn", "gdn2"])
+def test_many_chunks_with_ragged_tail(variant):
+    """More chunks than the persistent preparation grid holds at once (two CTAs
+    per SM), a ragged last chunk, and both value slices of the scan; sampled
+    (batch, head) pairs against the oracle."""
+    B, H, T = 2, 6, 64 * 40 + 23          # 2 * 6 * 41 = 492 chunks
+    x = wl.make_inputs(variant, B, T, H, 128, 128, torch.bfloat16, seed=55, h0_std=0.02)
+    o, hT = gpu_forward(x)
+    torch.cuda.synchronize()
+    for b, h in [(0, 0), (1, 5), (0, 3)]:
+        xs = select(x, batches=[b], heads=[h])
+        ro, rh = oracle_forward(xs)
+        eo = rel_err(o[b:b + 1, :, h:h + 1].float().cpu(), ro)
+        eh = rel_err(hT[b:b + 1, h:h + 1].cpu(), rh)
+        assert eo <= TOL[torch.bfloat16] and eh <= TOL[torch.bfloat16], (b, h, eo, eh)
+
+
 def test_scalar_decay_far_below_channel_limit():
     # scalar gates have no in-chunk range limit: sum over a chunk ~ -320
     x = wl.make_inputs("gdn", 1, 192, 2, 64, 64, torch.float32, seed=3, h0_std=0.1)
