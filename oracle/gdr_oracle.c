@@ -19,6 +19,11 @@
  * x_t = k_t; e_t = b_t (.) x_t under ERASE_CHANNEL, else beta_t x_t;
  * z_t = w_t (.) v_t under WRITE_CHANNEL, else beta_t v_t.
  *
+ * Under BETA_CHANNEL (the README variant of LLMs from scratch ch. 11, section
+ * 11.3: a write strength per value channel scaling the prediction error)
+ * beta is [B, T, H, d_v], e_t = k_t, z_t = v_t and the write is
+ * S_t = S~ + k_t (beta_t (.) (v_t - r_t))^T.
+ *
  * Layout: every per-token array is [B, T, H, d] row-major (d fastest); scalar
  * gates are [B, T, H]; states are [B, H, d_k, d_v] (d_v fastest). All double.
  * Each (batch, head) sequence is independent; OpenMP runs them in parallel.
@@ -34,6 +39,7 @@
 #define OR_ERASE_CHANNEL 2u
 #define OR_WRITE_CHANNEL 4u
 #define OR_QMIX 8u
+#define OR_BETA_CHANNEL 16u
 
 static void one_sequence(int B, int T, int H, int dk, int dv, unsigned flags,
                          double scale, int bi, int h, const double* q,
@@ -61,10 +67,18 @@ static void one_sequence(int B, int T, int H, int dk, int dv, unsigned flags,
     /* erase direction and write vector */
     for (int i = 0; i < dk; ++i)
       x[i] = (flags & OR_QMIX) ? kt[i] + lam[tok] * qt[i] : kt[i];
-    for (int i = 0; i < dk; ++i)
-      e[i] = (flags & OR_ERASE_CHANNEL) ? b[tok * dk + i] * x[i] : beta[tok] * x[i];
-    for (int j = 0; j < dv; ++j)
-      z[j] = (flags & OR_WRITE_CHANNEL) ? w[tok * dv + j] * vt[j] : beta[tok] * vt[j];
+    for (int i = 0; i < dk; ++i) {
+      if (flags & OR_BETA_CHANNEL)
+        e[i] = kt[i];
+      else
+        e[i] = (flags & OR_ERASE_CHANNEL) ? b[tok * dk + i] * x[i] : beta[tok] * x[i];
+    }
+    for (int j = 0; j < dv; ++j) {
+      if (flags & OR_BETA_CHANNEL)
+        z[j] = vt[j];
+      else
+        z[j] = (flags & OR_WRITE_CHANNEL) ? w[tok * dv + j] * vt[j] : beta[tok] * vt[j];
+    }
 
     /* forget: S~ = Diag(alpha) S */
     for (int i = 0; i < dk; ++i)
@@ -75,9 +89,14 @@ static void one_sequence(int B, int T, int H, int dk, int dv, unsigned flags,
     for (int i = 0; i < dk; ++i)
       for (int j = 0; j < dv; ++j) r[j] += S[i * dv + j] * e[i];
 
-    /* correct and write: S = S~ + k (z - r)^T */
+    /* correct and write: S = S~ + k (z - r)^T, the error scaled per value
+     * channel under BETA_CHANNEL */
+    if (flags & OR_BETA_CHANNEL)
+      for (int j = 0; j < dv; ++j) r[j] = beta[tok * dv + j] * (z[j] - r[j]);
+    else
+      for (int j = 0; j < dv; ++j) r[j] = z[j] - r[j];
     for (int i = 0; i < dk; ++i)
-      for (int j = 0; j < dv; ++j) S[i * dv + j] += kt[i] * (z[j] - r[j]);
+      for (int j = 0; j < dv; ++j) S[i * dv + j] += kt[i] * r[j];
 
     /* read: o = S^T (scale q) */
     double* ot = o + tok * dv;

@@ -29,6 +29,7 @@ DECAY_CHANNEL = 1   # g / alpha per key channel (KDA, GDN-2)
 ERASE_CHANNEL = 2   # erase direction e_t = b_t (.) x_t   (GDN-2)
 WRITE_CHANNEL = 4   # write vector   z_t = w_t (.) v_t   (GDN-2)
 QMIX = 8            # erase input x_t = k_t + lam_t q_t  (Q-Delta)
+BETA_CHANNEL = 16   # beta_t per value channel, scaling the error (ch. 11 README)
 
 
 def _f64(a):
@@ -54,6 +55,31 @@ def gdn_llms_ch11(q, k, v, alpha, beta, S0=None, scale=1.0):
         S_tilde = alpha[t] * S
         v_hat = S_tilde.T @ k[t]
         S = S_tilde + beta[t] * np.outer(k[t], v[t] - v_hat)
+        o[t] = S.T @ (scale * q[t])
+    return o, S
+
+
+def gdn_value_beta_ch11(q, k, v, alpha, beta_v, S0=None, scale=1.0):
+    """Gated DeltaNet with a write strength per value channel; S in R^{d_k x d_v}.
+
+    LLMs from scratch, ch. 11 "Gated DeltaNet", section 11.3: the chapter's
+    README module draws its write gate per value channel and scales the
+    prediction error channel by channel, while the forget gate stays one
+    scalar per head; the decay comes before the prediction. So with
+    beta_v in R^{d_v}: S~ = alpha_t S_{t-1}, v^_t = S~^T k_t,
+    S_t = S~ + k_t (beta_v,t (.) (v_t - v^_t))^T, y_t = S_t^T q_t.
+    Section 11.4 adds that each column of the state then follows its own
+    affine update, which the pins use.
+    """
+    q, k, v, alpha, beta_v = map(_f64, (q, k, v, alpha, beta_v))
+    T, dk = k.shape
+    dv = v.shape[1]
+    S = np.zeros((dk, dv)) if S0 is None else _f64(S0).copy()
+    o = np.zeros((T, dv))
+    for t in range(T):
+        S_tilde = alpha[t] * S
+        v_hat = S_tilde.T @ k[t]
+        S = S_tilde + np.outer(k[t], beta_v[t] * (v[t] - v_hat))
         o[t] = S.T @ (scale * q[t])
     return o, S
 
@@ -140,7 +166,13 @@ def erase_write_vectors(q, k, v, beta, lam, b, w, flags):
     ablation table uses channel b with scalar w and the reverse):
     x = k + lam q if QMIX else k; e = b (.) x if ERASE_CHANNEL else beta x;
     z = w (.) v if WRITE_CHANNEL else beta v.
+    Under BETA_CHANNEL (ch. 11 section 11.3's README variant) beta is
+    [T, d_v] and scales the error per value channel instead; the vectors
+    returned are then the unscaled e = k and z = v, and ``unified`` applies
+    beta to z - r.
     """
+    if flags & BETA_CHANNEL:
+        return k, v
     x = k + lam[:, None] * q if flags & QMIX else k
     e = b * x if flags & ERASE_CHANNEL else beta[:, None] * x
     z = w * v if flags & WRITE_CHANNEL else beta[:, None] * v
@@ -159,7 +191,10 @@ def unified(q, k, v, g, beta=None, lam=None, b=None, w=None, S0=None,
         r_t     = S~^T e_t
         S_t     = S~ + k_t (z_t - r_t)^T
         o_t     = S_t^T (scale q_t)
-    g is the log-decay; g = -inf gives alpha = 0 exactly.
+    g is the log-decay; g = -inf gives alpha = 0 exactly. Under
+    BETA_CHANNEL (README variant of ch. 11 section 11.3) beta is [T, d_v],
+    e_t = k_t, z_t = v_t and the write becomes
+        S_t     = S~ + k_t (beta_t (.) (v_t - r_t))^T.
     Returns (o [T, d_v], S_T [d_k, d_v]).
     """
     q, k, v, g = map(_f64, (q, k, v, g))
@@ -176,7 +211,10 @@ def unified(q, k, v, g, beta=None, lam=None, b=None, w=None, S0=None,
         alpha = np.exp(g[t])
         S_tilde = (alpha[:, None] if np.ndim(alpha) else alpha) * S
         r = S_tilde.T @ e[t]
-        S = S_tilde + np.outer(k[t], z[t] - r)
+        err = z[t] - r
+        if flags & BETA_CHANNEL:
+            err = beta[t] * err
+        S = S_tilde + np.outer(k[t], err)
         o[t] = S.T @ (scale * q[t])
     return o, S
 
