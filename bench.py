@@ -48,6 +48,8 @@ def parse():
     p.add_argument("--decode-steps", type=int, default=1)
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--no-value-beta", action="store_true",
+                   help="skip the per-value-channel write strength measurement")
     return p.parse_args()
 
 
@@ -72,7 +74,7 @@ def peaks():
 # and chunk_scan_kernel), per workload, with the hash of the kernel sources they
 # were taken on: a changed kernel reports null traffic until it is profiled
 # again. Source: profiles/chunk_fwd_two_kernel_gdn_b4_t4096_h16_d128.md.
-TRAFFIC = {2: {"bytes": 818.2e6, "sources": "eafec0e678bce8a2"}}
+TRAFFIC = {2: {"bytes": 817.9e6, "sources": "abc75c03ac7ac8c3"}}
 KERNEL_SOURCES = ("chunk_prep.cu", "chunk_scan.cu", "packet.h", "tc.cuh", "tri_inverse.cuh",
                   "common.cuh")
 
@@ -276,6 +278,8 @@ def run_ours(args):
                        "achieved_gbs": round(dgbs, 1), "frac_hbm": round(dgbs / pk["hbm_gbs"], 4)}
 
     epilogue_info = measure_epilogue(gdr, o, c, dev, stream, flush, K, pk)
+    value_beta_info = None if args.no_value_beta else measure_value_beta(gdr, dev, stream, flush,
+                                                                         K, pk, clk)
 
     e2e = None if args.no_e2e else measure_e2e(gdr, x, y, c, dev, args, B, T, H, dk, dv, N)
 
@@ -293,6 +297,7 @@ def run_ours(args):
         "roofline": roof,
         "decode": decode_info,
         "epilogue": epilogue_info,
+        "value_beta": value_beta_info,
         # this library's kernels per timed step: the two-kernel chunked forward
         # (bf16 with the full workspace) or one fused kernel (fp32), then the
         # decode steps
@@ -334,6 +339,57 @@ def measure_epilogue(gdr, o, c, dev, stream, flush, K, pk, eps=1e-6):
             "ms_mean": round(ms, 4), "algorithmic_bytes_per_launch": nbytes,
             "achieved_gbs": round(gbs, 1), "frac_hbm": round(gbs / pk["hbm_gbs"], 4),
             "l2": "flushed before every launch"}
+
+
+def fp32_alu_peak_tflops(sm_mhz):
+    """FP32 (non-tensor) FMA peak of one GB300: 152 SMs x 128 FP32 lanes x 2 flops
+    per FMA x the SM clock seen under load."""
+    return 152 * 128 * 2 * sm_mhz * 1e6 / 1e12
+
+
+def measure_value_beta(gdr, dev, stream, flush, K, pk, clk):
+    """The write strength per value channel (flag BETA_CHANNEL) on the 4 x 4096 x 16
+    x 128 bf16 workload, timed alone like the step: K calls, L2 flushed before
+    each, CUDA events on the launching stream. Not part of the step or its metric.
+    Bound by the FP32 pipe: 7 d_k d_v flops per token-head (decay, the two
+    column sums, the rank-1 write)."""
+    from gated_delta_rule_10_gb300 import workloads as wl
+    c = wl.CONFIGS["vbeta"]
+    x = wl.config_inputs("vbeta", device=dev)
+    B, T, H, dk, dv = c["B"], c["T"], c["H"], c["dk"], c["dv"]
+    o = torch.empty(B, T, H, dv, dtype=c["dtype"], device=dev)
+    hT = torch.empty(B, H, dk, dv, dtype=torch.float32, device=dev)
+
+    def call():
+        gdr.chunk_fwd(x["q"], x["k"], x["v"], x["g"], x["beta"], h0=x["h0"], scale=x["scale"],
+                      flags=x["flags"], o=o, hT=hT)
+
+    for _ in range(3):
+        call()
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(K)]
+    torch.cuda.synchronize()
+    for i in range(K):
+        flush.fill_(float(i))
+        ev[i][0].record(stream)
+        call()
+        ev[i][1].record(stream)
+    torch.cuda.synchronize()
+    ms = statistics.mean(ev[i][0].elapsed_time(ev[i][1]) for i in range(K))
+    th = B * T * H
+    flops = 7.0 * dk * dv * th
+    sm_mhz = (clk or {}).get("sm_mhz") or 2070.0
+    peak = fp32_alu_peak_tflops(sm_mhz)
+    tf = flops / (ms / 1e3) / 1e12
+    nbytes = tensor_bytes(x["q"], x["k"], x["v"], x["g"], x["beta"], x["h0"], o, hT)
+    gbs = nbytes / (ms / 1e3) / 1e9
+    return {"kernel": "value_beta_scan_kernel", "workload": c["name"], "launches": K,
+            "ms_mean": round(ms, 4), "token_heads_per_s": round(th / (ms / 1e3), 1),
+            "roofline": {"bound": "alu", "achieved": round(tf, 2), "peak": round(peak, 2),
+                         "unit": "TFLOP/s", "frac": round(tf / peak, 4),
+                         "peak_source": "derived: 152 SMs x 128 FP32 lanes x 2 x SM clock"},
+            "algorithmic_flops_per_launch": flops, "algorithmic_bytes_per_launch": nbytes,
+            "achieved_gbs": round(gbs, 1), "frac_hbm": round(gbs / pk["hbm_gbs"], 4),
+            "l2": "flushed before every call"}
 
 
 def measure_e2e(gdr, x, y, c, dev, args, B, T, H, dk, dv, N, steps=5):

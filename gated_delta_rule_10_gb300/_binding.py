@@ -20,6 +20,7 @@ DECAY_CHANNEL = 1
 ERASE_CHANNEL = 2
 WRITE_CHANNEL = 4
 QMIX = 8
+BETA_CHANNEL = 16
 CHUNK = 64
 
 STATUS = {0: "GDR_OK", 1: "GDR_ERR_INVALID_ARG", 2: "GDR_ERR_UNSUPPORTED", 3: "GDR_ERR_CUDA",
@@ -98,9 +99,11 @@ def _check(t, name, dtype, device, shape=None):
         raise ValueError("%s has shape %s, expected %s" % (name, tuple(t.shape), tuple(shape)))
 
 
-def _infer_flags(channel_decay, b, w, lam):
+def _infer_flags(channel_decay, b, w, lam, channel_beta=False):
     """Variant flags implied by which gates the caller passed."""
     flags = DECAY_CHANNEL if channel_decay else 0
+    if channel_beta:
+        flags |= BETA_CHANNEL
     if b is not None:
         flags |= ERASE_CHANNEL
     if w is not None:
@@ -132,7 +135,8 @@ def chunk_fwd(q, k, v, g, beta=None, lam=None, b=None, w=None, h0=None, *, scale
     """Chunkwise forward (``gdr_chunk_fwd``).
 
     q, k: [B, T, H, d_k]; v: [B, T, H, d_v] (bf16 or fp32, one dtype);
-    g: [B, T, H] or [B, T, H, d_k] fp32 log-decay; beta / lam: [B, T, H] fp32;
+    g: [B, T, H] or [B, T, H, d_k] fp32 log-decay; beta / lam: [B, T, H] fp32
+    (beta [B, T, H, d_v] selects the write strength per value channel);
     b: [B, T, H, d_k]; w: [B, T, H, d_v]; h0: [B, H, d_k, d_v] fp32 or None.
     ``flags`` defaults to what the given gates imply (channel g, b, w, lam);
     ``scale`` to d_k^-1/2. Returns (o, hT) with hT None unless requested.
@@ -143,14 +147,15 @@ def chunk_fwd(q, k, v, g, beta=None, lam=None, b=None, w=None, h0=None, *, scale
     if dt not in (torch.bfloat16, torch.float32):
         raise ValueError("q, k, v must be bf16 or fp32")
     if flags is None:
-        flags = _infer_flags(g.dim() == 4, b, w, lam)
+        flags = _infer_flags(g.dim() == 4, b, w, lam, beta is not None and beta.dim() == 4)
     if scale is None:
         scale = dk ** -0.5
     _check(q, "q", dt, dev, (B, T, H, dk))
     _check(k, "k", dt, dev, (B, T, H, dk))
     _check(v, "v", dt, dev, (B, T, H, dv))
     _check(g, "g", torch.float32, dev, (B, T, H, dk) if flags & DECAY_CHANNEL else (B, T, H))
-    _check(beta, "beta", torch.float32, dev, (B, T, H))
+    _check(beta, "beta", torch.float32, dev,
+           (B, T, H, dv) if flags & BETA_CHANNEL else (B, T, H))
     _check(lam, "lam", torch.float32, dev, (B, T, H))
     _check(b, "b", dt, dev, (B, T, H, dk))
     _check(w, "w", dt, dev, (B, T, H, dv))
@@ -203,11 +208,13 @@ def recurrent_step(q, k, v, g, state, beta=None, lam=None, b=None, w=None, *, sc
     N, H, dk, dv = state.shape
     dev, dt = q.device, q.dtype
     if flags is None:
-        flags = _infer_flags(g.numel() == N * H * dk, b, w, lam)
+        flags = _infer_flags(g.numel() == N * H * dk, b, w, lam,
+                             beta is not None and beta.numel() == N * H * dv)
     if scale is None:
         scale = dk ** -0.5
+    nbeta = N * H * dv if flags & BETA_CHANNEL else N * H
     for name, t, n in (("q", q, N * H * dk), ("k", k, N * H * dk), ("v", v, N * H * dv),
-                       ("b", b, N * H * dk), ("w", w, N * H * dv), ("beta", beta, N * H),
+                       ("b", b, N * H * dk), ("w", w, N * H * dv), ("beta", beta, nbeta),
                        ("lam", lam, N * H),
                        ("g", g, N * H * dk if flags & DECAY_CHANNEL else N * H)):
         if t is not None:

@@ -22,7 +22,10 @@ gdr_status check_shape(const gdr_shape* s, bool step) {
   if (!s) return GDR_ERR_INVALID_ARG;
   if (s->B < 1 || s->T < 1 || s->H < 1 || s->dk < 1 || s->dv < 1) return GDR_ERR_INVALID_ARG;
   if (s->dtype != GDR_F32 && s->dtype != GDR_BF16) return GDR_ERR_INVALID_ARG;
-  if (s->flags & ~15u) return GDR_ERR_INVALID_ARG;
+  if (s->flags & ~31u) return GDR_ERR_INVALID_ARG;
+  // the write strength per value channel comes with one scalar decay per head
+  // and no other gate
+  if ((s->flags & GDR_BETA_CHANNEL) && (s->flags & 15u)) return GDR_ERR_UNSUPPORTED;
   if (!std::isfinite(s->scale)) return GDR_ERR_INVALID_ARG;
   if (step && s->T != 1) return GDR_ERR_INVALID_ARG;
   if ((s->dk != 64 && s->dk != 128) || (s->dv != 64 && s->dv != 128)) return GDR_ERR_UNSUPPORTED;
@@ -31,6 +34,8 @@ gdr_status check_shape(const gdr_shape* s, bool step) {
   const long long state = static_cast<long long>(s->B) * s->H * s->dk * s->dv;
   if (elems > kMaxElems || state > kMaxElems) return GDR_ERR_UNSUPPORTED;
   if (s->H > 65535 || s->B > 65535) return GDR_ERR_UNSUPPORTED;  // grid y / z extents
+  if ((s->flags & GDR_BETA_CHANNEL) && static_cast<long long>(s->B) * s->H > 65535)
+    return GDR_ERR_UNSUPPORTED;                                     // grid y extent
   return GDR_OK;
 }
 
@@ -52,7 +57,17 @@ gdr_status check_gates(const gdr_shape* s, const void* q, const void* k, const v
   if ((f & GDR_DECAY_CHANNEL) && !aligned(g, 16)) return GDR_ERR_INVALID_ARG;   // vector loads
   if ((f & GDR_ERASE_CHANNEL) && !aligned(b, 16)) return GDR_ERR_INVALID_ARG;
   if ((f & GDR_WRITE_CHANNEL) && !aligned(w, 16)) return GDR_ERR_INVALID_ARG;
+  if ((f & GDR_BETA_CHANNEL) && !aligned(beta, 16)) return GDR_ERR_INVALID_ARG;
   return GDR_OK;
+}
+
+gdr::ValueBetaArgs value_beta_args(const gdr_shape* s, const void* q, const void* k,
+                                   const void* v, const float* g, const float* beta,
+                                   const float* h0, void* o, float* hT) {
+  gdr::ValueBetaArgs a;
+  a.q = q; a.k = k; a.v = v; a.g = g; a.beta = beta; a.h0 = h0; a.o = o; a.hT = hT;
+  a.B = s->B; a.T = s->T; a.H = s->H; a.scale = s->scale;
+  return a;
 }
 
 }  // namespace
@@ -78,8 +93,8 @@ gdr_status gdr_chunk_fwd_workspace(const gdr_shape* shape, size_t* bytes) {
   const gdr_status st = check_shape(shape, false);
   if (st != GDR_OK) return st;
   // bf16: the status words, then one packet per chunk of every (batch, head)
-  // for the two-kernel path; fp32 needs nothing
-  if (shape->dtype != GDR_BF16) {
+  // for the two-kernel path; fp32 and the value-channel scan need nothing
+  if (shape->dtype != GDR_BF16 || (shape->flags & GDR_BETA_CHANNEL)) {
     *bytes = 0;
     return GDR_OK;
   }
@@ -93,7 +108,9 @@ gdr_status gdr_chunk_fwd_workspace_min(const gdr_shape* shape, size_t* bytes) {
   if (!bytes) return GDR_ERR_INVALID_ARG;
   const gdr_status st = check_shape(shape, false);
   if (st != GDR_OK) return st;
-  *bytes = shape->dtype == GDR_BF16 ? gdr::kChunkWorkspaceBytes : 0;
+  *bytes = (shape->dtype == GDR_BF16 && !(shape->flags & GDR_BETA_CHANNEL))
+               ? gdr::kChunkWorkspaceBytes
+               : 0;
   return GDR_OK;
 }
 
@@ -113,6 +130,12 @@ gdr_status gdr_chunk_fwd(const gdr_shape* shape, const void* q, const void* k, c
     return GDR_ERR_WORKSPACE;
 
   const bool f32 = shape->dtype == GDR_F32;
+  if (shape->flags & GDR_BETA_CHANNEL) {
+    const cudaError_t err = gdr::launch_value_beta_scan(
+        value_beta_args(shape, q, k, v, g, beta, h0, o, hT), shape->dk, shape->dv, f32,
+        reinterpret_cast<cudaStream_t>(stream));
+    return err == cudaSuccess ? GDR_OK : GDR_ERR_CUDA;
+  }
   gdr::ChunkArgs a;
   a.q = q; a.k = k; a.v = v; a.g = g; a.beta = beta; a.lam = lam; a.b = b; a.w = w;
   a.h0 = h0; a.o = o; a.hT = hT;
@@ -170,6 +193,12 @@ gdr_status gdr_recurrent_step(const gdr_shape* shape, const void* q, const void*
   st = check_gates(shape, q, k, v, g, beta, lam, b, w, o);
   if (st != GDR_OK) return st;
   if (!state || !aligned(state, 16)) return GDR_ERR_INVALID_ARG;
+  if (shape->flags & GDR_BETA_CHANNEL) {   // one token of the token-order scan, in place
+    const cudaError_t err = gdr::launch_value_beta_scan(
+        value_beta_args(shape, q, k, v, g, beta, state, o, state), shape->dk, shape->dv,
+        shape->dtype == GDR_F32, reinterpret_cast<cudaStream_t>(stream));
+    return err == cudaSuccess ? GDR_OK : GDR_ERR_CUDA;
+  }
   const long long blocks = static_cast<long long>(shape->B) * shape->H;
   if (blocks > 2147483647LL) return GDR_ERR_UNSUPPORTED;
   gdr::StepArgs a;

@@ -43,6 +43,20 @@ struct StepArgs {
   float scale;
 };
 
+// Arguments of the token-order scan with a write strength per value channel.
+struct ValueBetaArgs {
+  const void* q;
+  const void* k;
+  const void* v;
+  const float* g;      // [B, T, H] log-decay
+  const float* beta;   // [B, T, H, d_v]
+  const float* h0;     // [B, H, d_k, d_v] or null (zero state)
+  void* o;
+  float* hT;           // [B, H, d_k, d_v] or null; may equal h0
+  int B, T, H;
+  float scale;
+};
+
 // Device status words the tensor-core chunk kernel reports into (in the
 // caller's workspace): [0] = 0 or a gdr_status code, [1] = CTA index,
 // [2] = 4 * chunk + which wait gave up.
@@ -74,6 +88,9 @@ cudaError_t launch_recurrent_step(const StepArgs& a, int dk, int dv, bool f32,
 cudaError_t launch_rmsnorm_gate(const void* o, const void* z, const float* weight, float eps,
                                 void* y, long long rows, int dv, bool f32,
                                 cudaStream_t stream);
+// Write strength per value channel (flag 16): token-order scan, fp32 state.
+cudaError_t launch_value_beta_scan(const ValueBetaArgs& a, int dk, int dv, bool f32,
+                                   cudaStream_t stream);
 cudaError_t launch_gate_cumsum(const float* g, float* G, int B, int T, int X,
                                cudaStream_t stream);
 

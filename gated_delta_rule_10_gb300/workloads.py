@@ -16,7 +16,9 @@ Recipe (one per variant, drawn in fp32 on the CPU with a seeded
 * scalar log-decay g = -softplus(N(0, 1)) per token and head (Gated
   DeltaNet, Q-Delta); channel log-decay g = -exp(N(-2, 0.5)) per key
   channel (KDA, Gated DeltaNet-2). Gates stay fp32.
-* beta = sigmoid(N(0, 1)) per token and head.
+* beta = sigmoid(N(0, 1)) per token and head; for the write strength per
+  value channel (flag BETA_CHANNEL) beta = sigmoid(N(0, 1)) per token, head
+  and value channel.
 * Q-Delta: lambda ~ U[0, 1] per head, broadcast over batch and time; the
   write strength is capped so that beta * k^T x < 2 with x = k + lambda q:
   beta = sigmoid(N(0,1)) * min(1, 1.9 / (k^T x)) (factor 1 when k^T x <= 0),
@@ -30,7 +32,8 @@ Recipe (one per variant, drawn in fp32 on the CPU with a seeded
   immaterial), output-gate input z ~ N(0, 1), both in the compute dtype, and
   a near-unit gain weight = 1 + 0.1 N(0, 1) per value channel in fp32.
 
-The five named workloads mirror the pages' 340M / 1.3B layer shapes.
+The five numbered workloads mirror the pages' 340M / 1.3B layer shapes; the
+"vbeta" workload runs the per-value-channel write strength on workload 2's.
 """
 import math
 
@@ -40,12 +43,14 @@ DECAY_CHANNEL = 1
 ERASE_CHANNEL = 2
 WRITE_CHANNEL = 4
 QMIX = 8
+BETA_CHANNEL = 16
 
 VARIANT_FLAGS = {
     "gdn": 0,
     "qdelta": QMIX,
     "kda": DECAY_CHANNEL,
     "gdn2": DECAY_CHANNEL | ERASE_CHANNEL | WRITE_CHANNEL,
+    "vbeta": BETA_CHANNEL,
 }
 
 # name -> recipe of the five workloads (the fifth also has a decode phase)
@@ -61,6 +66,10 @@ CONFIGS = {
     5: dict(name="gdn2_bf16_b1_t65536_h32_d128", variant="gdn2", B=1, T=65536, H=32,
             dk=128, dv=128, dtype=torch.bfloat16, q_prescaled=False, h0_std=None, seed=4,
             decode=dict(steps=256, N=256, h_std=0.02)),
+    # the write strength per value channel on workload 2's shapes
+    "vbeta": dict(name="vbeta_bf16_b4_t4096_h16_d128", variant="vbeta", B=4, T=4096, H=16,
+                  dk=128, dv=128, dtype=torch.bfloat16, q_prescaled=False, h0_std=0.02,
+                  seed=6),
 }
 
 
@@ -102,7 +111,9 @@ def make_inputs(variant, B, T, H, dk, dv, dtype=torch.bfloat16, seed=0,
     else:
         g = -torch.nn.functional.softplus(normal(B, T, H))
     beta = lam = b = w = None
-    if not (flags & ERASE_CHANNEL and flags & WRITE_CHANNEL):
+    if flags & BETA_CHANNEL:
+        beta = torch.sigmoid(normal(B, T, H, dv))
+    elif not (flags & ERASE_CHANNEL and flags & WRITE_CHANNEL):
         beta = torch.sigmoid(normal(B, T, H))
     if flags & QMIX:
         lam_h = torch.rand(H, generator=gen, dtype=torch.float32)

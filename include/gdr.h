@@ -28,6 +28,19 @@
  * Attention", section 4; Q-Delta the rewritten rule of the Q-Delta notes, key
  * design 3.
  *
+ * GDR_BETA_CHANNEL selects the README variant of LLMs from scratch ch. 11,
+ * section 11.3: the write strength is one value per value channel, beta is
+ * [B, T, H, d_v] fp32 (16-byte aligned) and scales the prediction error
+ * channel by channel,
+ *
+ *     S_t = S~_t + k_t (beta_t (.) (v_t - S~_t^T k_t))^T,
+ *
+ * with one scalar decay per head (g is [B, T, H]). It combines with no other
+ * flag (GDR_ERR_UNSUPPORTED) and needs B * H <= 65535. Every column of S then
+ * follows its own affine map, so there is no shared (I + T)^{-1}: both
+ * gdr_chunk_fwd and gdr_recurrent_step run it as a token-order scan with the
+ * state in fp32 registers, and it needs no workspace.
+ *
  * Conventions common to every call:
  *  - Layouts are dense and row-major. Per-token tensors are [B, T, H, d] with
  *    d fastest; scalar per-token gates are [B, T, H]; states are
@@ -83,7 +96,8 @@ enum {
   GDR_DECAY_CHANNEL = 1, /* g is [B,T,H,d_k] (per key channel), else [B,T,H] */
   GDR_ERASE_CHANNEL = 2, /* erase direction b (.) x, b is [B,T,H,d_k]        */
   GDR_WRITE_CHANNEL = 4, /* write vector w (.) v, w is [B,T,H,d_v]           */
-  GDR_QMIX = 8           /* erase input x = k + lam q, lam is [B,T,H]         */
+  GDR_QMIX = 8,          /* erase input x = k + lam q, lam is [B,T,H]         */
+  GDR_BETA_CHANNEL = 16  /* beta is [B,T,H,d_v], scales the error per channel */
 };
 
 typedef struct {
@@ -108,7 +122,8 @@ typedef struct {
  * bf16: the status words). A bf16 call whose workspace is at least that but
  * smaller than the full size runs the single-kernel path, which keeps every
  * intermediate on chip and is slower when B * H is small. Both paths compute
- * the same result up to rounding. fp32 inputs need no workspace.
+ * the same result up to rounding. fp32 inputs and GDR_BETA_CHANNEL need no
+ * workspace.
  *
  * Both return GDR_ERR_INVALID_ARG / GDR_ERR_UNSUPPORTED for a bad shape. */
 gdr_status gdr_chunk_fwd_workspace(const gdr_shape* shape, size_t* bytes);
@@ -128,7 +143,8 @@ gdr_status gdr_chunk_fwd_workspace_min(const gdr_shape* shape, size_t* bytes);
  *   g      [B,T,H] fp32, or [B,T,H,d_k] under GDR_DECAY_CHANNEL (then
  *          16-byte aligned)
  *   beta   [B,T,H] fp32; required unless both ERASE and WRITE are set
- *          (then ignored)
+ *          (then ignored); [B,T,H,d_v], 16-byte aligned, under
+ *          GDR_BETA_CHANNEL
  *   lam    [B,T,H] fp32; required under GDR_QMIX, ignored otherwise
  *   b      [B,T,H,d_k] dtype; required under GDR_ERASE_CHANNEL, else ignored
  *   w      [B,T,H,d_v] dtype; required under GDR_WRITE_CHANNEL, else ignored
@@ -192,7 +208,8 @@ gdr_status gdr_chunk_fwd_static(const gdr_shape* shape, const void* q,
  * in the general form above; section 11.3 for the streaming protocol: the
  * prefill's final state is the first step's state). shape->T must be 1 and
  * shape->B is the number of sequences N; tensors are the [N,1,H,d] (equally
- * [N,H,d]) slices of the layouts above and the gates likewise.
+ * [N,H,d]) slices of the layouts above and the gates likewise (beta is
+ * [N,H,d_v] under GDR_BETA_CHANNEL).
  *
  *   state  [N,H,d_k,d_v] fp32, read as S_{t-1} and overwritten with S_t
  *   o      [N,H,d_v] dtype, o_t = S_t^T (scale q_t)

@@ -92,7 +92,7 @@ def test_workspace_query(L):
     assert L.gdr_chunk_fwd_workspace(ctypes.byref(_shape()), None) == 1
     assert L.gdr_chunk_fwd_workspace(ctypes.byref(_shape(dk=96)), ctypes.byref(n)) == 2
     assert L.gdr_chunk_fwd_workspace(ctypes.byref(_shape(T=0)), ctypes.byref(n)) == 1
-    assert L.gdr_chunk_fwd_workspace(ctypes.byref(_shape(flags=16)), ctypes.byref(n)) == 1
+    assert L.gdr_chunk_fwd_workspace(ctypes.byref(_shape(flags=32)), ctypes.byref(n)) == 1
     assert L.gdr_chunk_fwd_workspace(ctypes.byref(_shape(dtype=7)), ctypes.byref(n)) == 1
     assert L.gdr_chunk_fwd_workspace(ctypes.byref(_shape(scale=float("nan"))),
                                      ctypes.byref(n)) == 1
@@ -210,3 +210,19 @@ def test_rmsnorm_gate_rejects_bad_arguments(L):
     assert call(y=FAKE + 0x200) == 1
     assert call(y=FAKE + 0x4000 - 0x200) == 1      # overlaps z
     assert call(rows=1 << 41) == 2
+
+
+def test_value_beta_flag_rules(L):
+    n = ctypes.c_size_t(7)
+    BC = gdr.BETA_CHANNEL
+    assert L.gdr_chunk_fwd_workspace(ctypes.byref(_shape(flags=BC)), ctypes.byref(n)) == 0
+    assert n.value == 0                                   # no workspace
+    assert L.gdr_chunk_fwd_workspace_min(ctypes.byref(_shape(flags=BC)), ctypes.byref(n)) == 0
+    assert n.value == 0
+    for other in (gdr.DECAY_CHANNEL, gdr.ERASE_CHANNEL, gdr.WRITE_CHANNEL, gdr.QMIX):
+        assert _call_chunk(L, _shape(flags=BC | other), b=FAKE, w=FAKE, lam=FAKE) == 2
+    assert _call_chunk(L, _shape(flags=32)) == 1
+    assert _call_chunk(L, _shape(flags=BC), beta=FAKE + 4) == 1     # 16-byte beta rows
+    assert _call_chunk(L, _shape(flags=BC), beta=None) == 1
+    big = _shape(B=1024, H=128, T=1, flags=BC)                       # grid y extent
+    assert _call_chunk(L, big) == 2
