@@ -50,6 +50,8 @@ def parse():
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-value-beta", action="store_true",
                    help="skip the per-value-channel write strength measurement")
+    p.add_argument("--no-split", action="store_true",
+                   help="skip the sequence-split measurement")
     return p.parse_args()
 
 
@@ -280,6 +282,7 @@ def run_ours(args):
     epilogue_info = measure_epilogue(gdr, o, c, dev, stream, flush, K, pk)
     value_beta_info = None if args.no_value_beta else measure_value_beta(gdr, dev, stream, flush,
                                                                          K, pk, clk)
+    split_info = None if args.no_split else measure_split(gdr, dev, stream, flush, K, pk)
 
     e2e = None if args.no_e2e else measure_e2e(gdr, x, y, c, dev, args, B, T, H, dk, dv, N)
 
@@ -298,6 +301,7 @@ def run_ours(args):
         "decode": decode_info,
         "epilogue": epilogue_info,
         "value_beta": value_beta_info,
+        "sequence_split": split_info,
         # this library's kernels per timed step: the two-kernel chunked forward
         # (bf16 with the full workspace) or one fused kernel (fp32), then the
         # decode steps
@@ -390,6 +394,51 @@ def measure_value_beta(gdr, dev, stream, flush, K, pk, clk):
             "algorithmic_flops_per_launch": flops, "algorithmic_bytes_per_launch": nbytes,
             "achieved_gbs": round(gbs, 1), "frac_hbm": round(gbs / pk["hbm_gbs"], 4),
             "l2": "flushed before every call"}
+
+
+def measure_split(gdr, dev, stream, flush, K, pk, H=4):
+    """The sequence split where it engages: the GDN-2 recipe of workload 5 (65536
+    tokens, d = 128) with B * H = 4, through gdr_chunk_fwd's default (split into
+    runs) and with one run (the plain two-kernel path), each timed alone: K calls,
+    L2 flushed before each, CUDA events on the launching stream. Not part of the
+    step or its metric."""
+    from gated_delta_rule_10_gb300 import workloads as wl
+    c = dict(wl.CONFIGS[5], H=H)
+    x = wl.config_inputs(5, device=dev, H=H)
+    B, T, dk, dv = c["B"], c["T"], c["dk"], c["dv"]
+    o = torch.empty(B, T, H, dv, dtype=c["dtype"], device=dev)
+    hT = torch.empty(B, H, dk, dv, dtype=torch.float32, device=dev)
+    shape = gdr.make_shape(B, T, H, dk, dv, c["dtype"], x["flags"], x["scale"])
+    ws = torch.empty(gdr.chunk_fwd_workspace_bytes(shape), dtype=torch.uint8, device=dev)
+    plain = gdr.chunk_fwd_workspace_bytes(shape, segments=1)
+    out = {"workload": "gdn2_bf16_b1_t65536_h%d_d128" % H}
+    for name, segments in (("split", None), ("one_run", 1)):
+        def call():
+            gdr.chunk_fwd(x["q"], x["k"], x["v"], x["g"], x["beta"], x["lam"], x["b"], x["w"],
+                          x["h0"], scale=x["scale"], flags=x["flags"], o=o, hT=hT, workspace=ws,
+                          segments=segments)
+        for _ in range(3):
+            call()
+        ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(K)]
+        torch.cuda.synchronize()
+        for i in range(K):
+            flush.fill_(float(i))
+            ev[i][0].record(stream)
+            call()
+            ev[i][1].record(stream)
+        torch.cuda.synchronize()
+        ms = statistics.mean(ev[i][0].elapsed_time(ev[i][1]) for i in range(K))
+        nbytes = tensor_bytes(x["q"], x["k"], x["v"], x["g"], x["beta"], x["lam"], x["b"], x["w"],
+                              x["h0"], o, hT)
+        gbs = nbytes / (ms / 1e3) / 1e9
+        out[name] = {"ms_mean": round(ms, 4), "token_heads_per_s": round(B * T * H / (ms / 1e3), 1),
+                     "achieved_gbs": round(gbs, 1), "frac_hbm": round(gbs / pk["hbm_gbs"], 4)}
+    out["runs_per_sequence"] = next(P for P in (64, 32, 16, 8, 4, 2, 1)
+                                    if gdr.chunk_fwd_workspace_bytes(shape, segments=P) == ws.numel()
+                                    ) if ws.numel() > plain else 1
+    out["launches_per_call"] = {"split": 4, "one_run": 2}
+    out["l2"] = "flushed before every call"
+    return out
 
 
 def measure_e2e(gdr, x, y, c, dev, args, B, T, H, dk, dv, N, steps=5):

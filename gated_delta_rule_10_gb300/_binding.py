@@ -56,6 +56,10 @@ def lib():
         L.gdr_chunk_fwd_workspace.argtypes = [sp, ctypes.POINTER(ctypes.c_size_t)]
         L.gdr_chunk_fwd_workspace_min.argtypes = [sp, ctypes.POINTER(ctypes.c_size_t)]
         L.gdr_chunk_fwd.argtypes = [sp] + [_vp] * 11 + [_vp, ctypes.c_size_t, _vp]
+        L.gdr_chunk_fwd_split.argtypes = ([sp, ctypes.c_int] + [_vp] * 11 +
+                                          [_vp, ctypes.c_size_t, _vp])
+        L.gdr_chunk_fwd_workspace_split.argtypes = [sp, ctypes.c_int,
+                                                    ctypes.POINTER(ctypes.c_size_t)]
         L.gdr_recurrent_step.argtypes = [sp] + [_vp] * 10 + [_vp]
         L.gdr_gate_cumsum.argtypes = [ctypes.c_int] * 4 + [_vp, _vp, _vp]
         L.gdr_chunk_fwd_check.argtypes = [_vp, _vp, ctypes.POINTER(ctypes.c_int)]
@@ -65,6 +69,7 @@ def lib():
         L.gdr_status_string.restype = ctypes.c_char_p
         L.gdr_abi_version.restype = ctypes.c_int
         for name in ("gdr_chunk_fwd_workspace", "gdr_chunk_fwd_workspace_min", "gdr_chunk_fwd",
+                     "gdr_chunk_fwd_split", "gdr_chunk_fwd_workspace_split",
                      "gdr_recurrent_step",
                      "gdr_gate_cumsum", "gdr_chunk_fwd_check", "gdr_rmsnorm_gate"):
             getattr(L, name).restype = ctypes.c_int
@@ -118,11 +123,17 @@ def make_shape(B, T, H, dk, dv, dtype, flags, scale):
                  flags, float(scale))
 
 
-def chunk_fwd_workspace_bytes(shape, minimum=False):
+def chunk_fwd_workspace_bytes(shape, minimum=False, segments=None):
     """Workspace bytes for a chunk_fwd call on `shape`: the size that selects the
-    two-kernel path, or with minimum=True the least the call accepts."""
-    name = "gdr_chunk_fwd_workspace_min" if minimum else "gdr_chunk_fwd_workspace"
+    fastest path, with minimum=True the least the call accepts, or with
+    `segments` the size a split into that many runs needs."""
     n = ctypes.c_size_t(0)
+    if segments is not None:
+        st = lib().gdr_chunk_fwd_workspace_split(ctypes.byref(shape), int(segments), ctypes.byref(n))
+        if st:
+            raise GdrError(st, "gdr_chunk_fwd_workspace_split")
+        return n.value
+    name = "gdr_chunk_fwd_workspace_min" if minimum else "gdr_chunk_fwd_workspace"
     st = getattr(lib(), name)(ctypes.byref(shape), ctypes.byref(n))
     if st:
         raise GdrError(st, name)
@@ -131,7 +142,7 @@ def chunk_fwd_workspace_bytes(shape, minimum=False):
 
 def chunk_fwd(q, k, v, g, beta=None, lam=None, b=None, w=None, h0=None, *, scale=None,
               flags=None, output_final_state=True, o=None, hT=None, workspace=None,
-              stream=None):
+              segments=None, stream=None):
     """Chunkwise forward (``gdr_chunk_fwd``).
 
     q, k: [B, T, H, d_k]; v: [B, T, H, d_v] (bf16 or fp32, one dtype);
@@ -139,7 +150,9 @@ def chunk_fwd(q, k, v, g, beta=None, lam=None, b=None, w=None, h0=None, *, scale
     (beta [B, T, H, d_v] selects the write strength per value channel);
     b: [B, T, H, d_k]; w: [B, T, H, d_v]; h0: [B, H, d_k, d_v] fp32 or None.
     ``flags`` defaults to what the given gates imply (channel g, b, w, lam);
-    ``scale`` to d_k^-1/2. Returns (o, hT) with hT None unless requested.
+    ``scale`` to d_k^-1/2. ``segments`` cuts every sequence into that many runs
+    (``gdr_chunk_fwd_split``); by default the library decides. Returns (o, hT)
+    with hT None unless requested.
     """
     B, T, H, dk = q.shape
     dv = v.shape[-1]
@@ -167,17 +180,19 @@ def chunk_fwd(q, k, v, g, beta=None, lam=None, b=None, w=None, h0=None, *, scale
         hT = torch.empty(B, H, dk, dv, dtype=torch.float32, device=dev)
     _check(hT, "hT", torch.float32, dev, (B, H, dk, dv))
     shape = make_shape(B, T, H, dk, dv, dt, flags, scale)
-    ws_bytes = chunk_fwd_workspace_bytes(shape)
+    ws_bytes = chunk_fwd_workspace_bytes(shape, segments=segments)
     if ws_bytes and workspace is None:
         workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+    args = (_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(lam), _ptr(b), _ptr(w),
+            _ptr(h0), _ptr(o), _ptr(hT), _ptr(workspace),
+            ctypes.c_size_t(0 if workspace is None else workspace.numel()), _stream(stream, dev))
     with torch.cuda.device(dev):
-        st = lib().gdr_chunk_fwd(ctypes.byref(shape), _ptr(q), _ptr(k), _ptr(v), _ptr(g),
-                                 _ptr(beta), _ptr(lam), _ptr(b), _ptr(w), _ptr(h0), _ptr(o),
-                                 _ptr(hT), _ptr(workspace),
-                                 ctypes.c_size_t(0 if workspace is None else workspace.numel()),
-                                 _stream(stream, dev))
+        if segments is None:
+            st = lib().gdr_chunk_fwd(ctypes.byref(shape), *args)
+        else:
+            st = lib().gdr_chunk_fwd_split(ctypes.byref(shape), int(segments), *args)
     if st:
-        raise GdrError(st, "gdr_chunk_fwd")
+        raise GdrError(st, "gdr_chunk_fwd" if segments is None else "gdr_chunk_fwd_split")
     return o, hT
 
 

@@ -28,6 +28,14 @@
 //              ring with plain bulk copies
 // Every wait is bounded; a wait that gives up makes all roles leave together,
 // release tensor memory and report GDR_ERR_TIMEOUT.
+//
+// Sequence split (ScanSegments): the chunks of each (batch, head) may be cut
+// into P runs, one CTA per run, each starting from its own state. Run p starts
+// from h0 (per run, or for run 0 only) or zero and writes its end state; with
+// `homogeneous` slices the state is the identity (d_k columns), U is taken as
+// zero and nothing is read out, so the end state is the run's transition M in
+// S_end = M S_start + H_local (LLMs from scratch ch. 11, section 11.4: the
+// affine maps of consecutive runs compose, in order).
 #include "common.cuh"
 #include "kernels.h"
 #include "packet.h"
@@ -99,18 +107,32 @@ __device__ __forceinline__ bool wait_or_abort(uint32_t mbar, uint32_t parity,
 
 template <int DK, int DV>
 __global__ void __launch_bounds__(kThreads, 1)
-    chunk_scan_kernel(const ChunkArgs a, const unsigned char* packets, int* status) {
+    chunk_scan_kernel(const ChunkArgs a, const unsigned char* packets, int* status,
+                      const ScanSegments sg) {
   using L = ScanLayout<DK>;
   using P = Packet<DK, DV>;
   extern __shared__ unsigned char smem_raw[];
   unsigned char* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   const uint32_t sb = smem_u32(smem);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int slice = blockIdx.x, h = blockIdx.y, bb = blockIdx.z;
+  const int h = blockIdx.y, bb = blockIdx.z / sg.segments, seg = blockIdx.z % sg.segments;
   const int T = a.T, H = a.H;
+  // value slices 0 .. DV/64-1, then (homogeneous) identity slices over d_k
+  const bool hom = static_cast<int>(blockIdx.x) >= DV / kNV;
+  const int slice = hom ? blockIdx.x - DV / kNV : blockIdx.x;
+  const int SW = hom ? DK : DV;               // width of this CTA's state
   const int col0 = slice * kNV;
   const int n_chunks = (T + kChunk - 1) / kChunk;
-  const unsigned char* pk0 = packets + (size_t(bb) * H + h) * n_chunks * P::bytes;
+  const int c_begin = seg * sg.seg_chunks;
+  const int cnt = max(0, min(n_chunks, c_begin + sg.seg_chunks) - c_begin);   // chunks of this run
+  const unsigned char* pk0 = packets + ((size_t(bb) * H + h) * n_chunks + c_begin) * P::bytes;
+  const size_t run = (size_t(bb) * H + h) * sg.segments + seg;   // per-run state index
+  float* const hT = hom ? sg.hT_hom
+                        : (sg.hT_per_seg ? a.hT : (seg == sg.segments - 1 ? a.hT : nullptr));
+  const size_t hT_idx = (hom || sg.hT_per_seg) ? run : (size_t(bb) * H + h);
+  const float* const h0 = hom ? nullptr : (sg.h0_per_seg ? a.h0 : (seg == 0 ? a.h0 : nullptr));
+  const size_t h0_idx = sg.h0_per_seg ? run : (size_t(bb) * H + h);
+  void* const out = hom ? nullptr : a.o;
   auto bar = [&](uint32_t i) { return sb + L::oBar + 8 * i; };
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::oAbort);
   uint32_t* tslot = reinterpret_cast<uint32_t*>(smem + L::oSlot);
@@ -144,7 +166,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const unsigned char* pk = pk0 + size_t(n) * P::bytes;
     tc::mbar_arrive_expect_tx(bar(kFull0 + s), P::kCommon + P::kUSlice);
     tc::bulk_load(st, pk, P::kCommon, bar(kFull0 + s));
-    tc::bulk_load(st + P::kCommon, pk + P::oU + slice * P::kUSlice, P::kUSlice, bar(kFull0 + s));
+    tc::bulk_load(st + P::kCommon, pk + P::oU + (hom ? 0 : slice) * P::kUSlice, P::kUSlice,
+                  bar(kFull0 + s));
   };
 
   if (warp < 8) {
@@ -157,12 +180,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int wrow = 32 * (q - 2) + lane;       // token row of W for those warps
     float S[kHalf];
     {
-      const size_t base = ((size_t(bb) * H + h) * DK + srow) * DV + col0 + cb;
+      const size_t base = (h0_idx * DK + srow) * SW + col0 + cb;
 #pragma unroll
       for (int j = 0; j < kHalf; j += 4) {
         float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (a.h0 && owner) x = *reinterpret_cast<const float4*>(a.h0 + base + j);
+        if (h0 && owner) x = *reinterpret_cast<const float4*>(h0 + base + j);
         S[j] = x.x; S[j + 1] = x.y; S[j + 2] = x.z; S[j + 3] = x.w;
+      }
+      if (hom) {   // the identity: row srow has its 1 in column srow
+#pragma unroll
+        for (int j = 0; j < kHalf; ++j) S[j] = (col0 + cb + j == srow) ? 1.f : 0.f;
       }
       if (owner) {
 #pragma unroll
@@ -174,7 +201,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     const uint64_t dS = tc::smem_desc(sb + L::oS, DK * 128, 1024);
     const uint64_t dW = tc::smem_desc(sb + L::oW, 64 * 128, 1024);
-    for (int n = 0; n < n_chunks; ++n) {
+    for (int n = 0; n < cnt; ++n) {   // n counts this run's chunks
       const int s = n % kStages;
       const uint32_t st = sb + L::oStage + s * L::kStage;
       const unsigned char* sst = smem + L::oStage + s * L::kStage;
@@ -213,7 +240,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           uint4 ur[kHalf / 8];
 #pragma unroll
           for (int j = 0; j < kHalf / 8; ++j)
-            ur[j] = *reinterpret_cast<const uint4*>(sst + P::kCommon + tc::tile_off(64, wrow, cb + 8 * j));
+            ur[j] = hom ? make_uint4(0, 0, 0, 0)   // U = 0: the transition alone
+                        : *reinterpret_cast<const uint4*>(sst + P::kCommon +
+                                                          tc::tile_off(64, wrow, cb + 8 * j));
           float x[kHalf];
           tc::tmem_ld32(tlane + D10 + (n & 1) * 64 + cb, x);
 #pragma unroll
@@ -227,7 +256,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           tc::fence_proxy_async();
         }
       }
-      if (tid == 0 && n + 1 < n_chunks) {
+      if (tid == 0 && n + 1 < cnt) {
         // meanwhile: the next chunk's packet and its D1 buffer (read out for chunk n-1)
         ok = wait_or_abort(bar(kFull0 + (n + 1) % kStages), ((n + 1) / kStages) & 1, abort_flag);
         if (ok && n >= 1)
@@ -269,21 +298,21 @@ __global__ void __launch_bounds__(kThreads, 1)
       // the chain is done with chunk n's stage (its MMAs completed with D_S)
       if (tid == 0) tc::mbar_arrive(bar(kEmpty0 + s));
     }
-    if (fail < 0 && a.hT && owner) {
-      const size_t base = ((size_t(bb) * H + h) * DK + srow) * DV + col0 + cb;
+    if (fail < 0 && hT && owner) {
+      const size_t base = (hT_idx * DK + srow) * SW + col0 + cb;
 #pragma unroll
       for (int j = 0; j < kHalf; j += 4)
-        *reinterpret_cast<float4*>(a.hT + base + j) = make_float4(S[j], S[j + 1], S[j + 2], S[j + 3]);
+        *reinterpret_cast<float4*>(hT + base + j) = make_float4(S[j], S[j + 1], S[j + 2], S[j + 3]);
     }
   } else {
     // ------------------------------------------------------------ output
     const int orow = tid - kOut;                // lanes 0..63 of D1 = rows of O_n
     int issued = 0;
     if (tid == kOut) {
-      for (int n = 0; n < min(kStages, n_chunks); ++n) load_chunk(n);
-      issued = min(kStages, n_chunks);
+      for (int n = 0; n < min(kStages, cnt); ++n) load_chunk(n);
+      issued = min(kStages, cnt);
     }
-    for (int n = 0; n < n_chunks; ++n) {
+    for (int n = 0; n < cnt; ++n) {
       const int s = n % kStages;
       const uint32_t st = sb + L::oStage + s * L::kStage;
       bool ok = true;
@@ -308,13 +337,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       ok = wait_or_abort(bar(kBO0 + (n & 1)), (n >> 1) & 1, abort_flag);
       if (tc::named_any(kOutBar, 64, !ok)) { fail = 4 * n + 3; break; }
       tc::fence_after_sync();
-      const int t0 = n * kChunk;
+      const int t0 = (c_begin + n) * kChunk;
       const int Lr = min(kChunk, T - t0);
       {
         float x[kNV];
         tc::tmem_ld64(tlane + D10 + (n & 1) * 64, x);
-        if (orow < Lr) {
-          __nv_bfloat16* op = static_cast<__nv_bfloat16*>(a.o) +
+        if (out && orow < Lr) {
+          __nv_bfloat16* op = static_cast<__nv_bfloat16*>(out) +
                               ((size_t(bb) * T + t0 + orow) * H + h) * DV + col0;
 #pragma unroll
           for (int j = 0; j < kNV; j += 8) *reinterpret_cast<uint4*>(op + j) = pack8(x + j);
@@ -326,7 +355,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc::mbar_arrive(bar(kOFree0 + (n & 1)));
         tc::mbar_arrive(bar(kEmpty0 + s));
         // refill the stage once the chain has released it too
-        if (n + kStages < n_chunks) {
+        if (n + kStages < cnt) {
           ok = wait_or_abort(bar(kEmpty0 + s), (n / kStages) & 1, abort_flag);
           if (ok) {
             load_chunk(n + kStages);
@@ -356,26 +385,29 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 template <int DK, int DV>
 cudaError_t launch_scan(const ChunkArgs& a, const unsigned char* packets, int* status,
-                        cudaStream_t stream) {
+                        cudaStream_t stream, ScanSegments sg) {
   using L = ScanLayout<DK>;
   static_assert(L::launch_bytes <= 232448, "shared memory budget of one CTA");
   auto kern = chunk_scan_kernel<DK, DV>;
   cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(L::launch_bytes));
   if (err != cudaSuccess) return err;
-  dim3 grid(DV / kNV, a.H, a.B);
-  kern<<<grid, kThreads, L::launch_bytes, stream>>>(a, packets, status);
+  if (sg.segments < 1) return cudaErrorInvalidValue;
+  if (sg.seg_chunks < 1) sg.seg_chunks = (a.T + kChunk - 1) / kChunk;
+  dim3 grid(DV / kNV + (sg.hT_hom ? DK / kNV : 0), a.H,
+            static_cast<unsigned>(a.B) * static_cast<unsigned>(sg.segments));
+  kern<<<grid, kThreads, L::launch_bytes, stream>>>(a, packets, status, sg);
   return cudaGetLastError();
 }
 
 }  // namespace
 
 cudaError_t launch_chunk_scan(const ChunkArgs& a, int dk, const unsigned char* packets,
-                              int* status, cudaStream_t stream) {
-  if (dk == 64 && a.dv == 64) return launch_scan<64, 64>(a, packets, status, stream);
-  if (dk == 64 && a.dv == 128) return launch_scan<64, 128>(a, packets, status, stream);
-  if (dk == 128 && a.dv == 64) return launch_scan<128, 64>(a, packets, status, stream);
-  if (dk == 128 && a.dv == 128) return launch_scan<128, 128>(a, packets, status, stream);
+                              int* status, cudaStream_t stream, const ScanSegments& sg) {
+  if (dk == 64 && a.dv == 64) return launch_scan<64, 64>(a, packets, status, stream, sg);
+  if (dk == 64 && a.dv == 128) return launch_scan<64, 128>(a, packets, status, stream, sg);
+  if (dk == 128 && a.dv == 64) return launch_scan<128, 64>(a, packets, status, stream, sg);
+  if (dk == 128 && a.dv == 128) return launch_scan<128, 128>(a, packets, status, stream, sg);
   return cudaErrorInvalidValue;
 }
 

@@ -61,6 +61,69 @@ gdr_status check_gates(const gdr_shape* s, const void* q, const void* k, const v
   return GDR_OK;
 }
 
+// Sequence split of the two-kernel path (bf16, every flag but BETA_CHANNEL).
+constexpr int kSplitTargetCtas = 152;   // one wave of scan CTAs on a GB300
+constexpr int kSplitMinChunks = 8;      // chunks per run, at least
+
+size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+int n_chunks_of(const gdr_shape* s) { return (s->T + gdr::kChunkLen - 1) / gdr::kChunkLen; }
+
+bool split_allowed(const gdr_shape* s) {
+  return s->dtype == GDR_BF16 && !(s->flags & GDR_BETA_CHANNEL);
+}
+
+// Runs per (batch, head) that the default path uses. The scan walks the chunks
+// of each (batch, head) in order, so when B * H leaves SMs idle the sequence is
+// cut into P runs. Cost in chunk steps of one scan CTA (about 1.3 us at 2 GHz):
+// unsplit, waves of the value CTAs times the chunks; split, the first pass
+// (value and identity slices) and the last pass each over one run, plus about
+// 4 steps per run for chaining the start states and 10 for the extra launches.
+// P is the power of two with the least cost among those whose first pass fits
+// one wave (a second wave measured slower per step than the model says) and
+// whose runs hold at least kSplitMinChunks chunks.
+int default_segments(const gdr_shape* s) {
+  if (!split_allowed(s)) return 1;
+  const long long bh = static_cast<long long>(s->B) * s->H;
+  const long long val = bh * (s->dv / 64), both = bh * ((s->dv + s->dk) / 64);
+  const long long nc = n_chunks_of(s);
+  const double unsplit =
+      static_cast<double>((val + kSplitTargetCtas - 1) / kSplitTargetCtas * nc);
+  double best = unsplit;
+  int best_p = 1;
+  for (int P = 2; P * both <= kSplitTargetCtas && static_cast<long long>(P) * kSplitMinChunks <= nc;
+       P *= 2) {
+    const long long per = (nc + P - 1) / P;
+    const double cost = 2.0 * per + 4.0 * P + 10.0;
+    if (cost < best) {
+      best = cost;
+      best_p = P;
+    }
+  }
+  return best_p;
+}
+
+// runs actually used for a request of P: every run non-empty
+void split_geometry(const gdr_shape* s, int P, int* runs, int* seg_chunks) {
+  const int nc = n_chunks_of(s);
+  const int per = (nc + P - 1) / P;
+  *seg_chunks = per;
+  *runs = (nc + per - 1) / per;
+}
+
+size_t two_kernel_bytes(const gdr_shape* s) {
+  const size_t chunks = static_cast<size_t>(s->B) * s->H * static_cast<size_t>(n_chunks_of(s));
+  return gdr::kChunkWorkspaceBytes + chunks * gdr::packet_bytes(s->dk, s->dv);
+}
+
+// status words, packets, then per-run local end states, transitions and start states
+size_t split_bytes(const gdr_shape* s, int P) {
+  if (P <= 1) return two_kernel_bytes(s);
+  const size_t runs = static_cast<size_t>(s->B) * s->H * P;
+  const size_t st = runs * s->dk * s->dv * sizeof(float), tr = runs * s->dk * s->dk * sizeof(float);
+  return align256(two_kernel_bytes(s)) + align256(st) + align256(tr) + align256(st);
+}
+
 gdr::ValueBetaArgs value_beta_args(const gdr_shape* s, const void* q, const void* k,
                                    const void* v, const float* g, const float* beta,
                                    const float* h0, void* o, float* hT) {
@@ -93,14 +156,13 @@ gdr_status gdr_chunk_fwd_workspace(const gdr_shape* shape, size_t* bytes) {
   const gdr_status st = check_shape(shape, false);
   if (st != GDR_OK) return st;
   // bf16: the status words, then one packet per chunk of every (batch, head)
-  // for the two-kernel path; fp32 and the value-channel scan need nothing
-  if (shape->dtype != GDR_BF16 || (shape->flags & GDR_BETA_CHANNEL)) {
+  // for the two-kernel path, and the run states when the sequence is split;
+  // fp32 and the value-channel scan need nothing
+  if (!split_allowed(shape)) {
     *bytes = 0;
     return GDR_OK;
   }
-  const size_t chunks = static_cast<size_t>(shape->B) * shape->H *
-                        static_cast<size_t>((shape->T + gdr::kChunkLen - 1) / gdr::kChunkLen);
-  *bytes = gdr::kChunkWorkspaceBytes + chunks * gdr::packet_bytes(shape->dk, shape->dv);
+  *bytes = split_bytes(shape, default_segments(shape));
   return GDR_OK;
 }
 
@@ -114,20 +176,45 @@ gdr_status gdr_chunk_fwd_workspace_min(const gdr_shape* shape, size_t* bytes) {
   return GDR_OK;
 }
 
-gdr_status gdr_chunk_fwd(const gdr_shape* shape, const void* q, const void* k, const void* v,
-                         const float* g, const float* beta, const float* lam, const void* b,
-                         const void* w, const float* h0, void* o, float* hT, void* workspace,
-                         size_t ws_bytes, gdr_stream_t stream) {
+gdr_status gdr_chunk_fwd_workspace_split(const gdr_shape* shape, int segments, size_t* bytes) {
+  if (!bytes || segments < 1) return GDR_ERR_INVALID_ARG;
+  const gdr_status st = check_shape(shape, false);
+  if (st != GDR_OK) return st;
+  if (!split_allowed(shape)) {
+    if (segments > 1) return GDR_ERR_UNSUPPORTED;
+    *bytes = 0;
+    return GDR_OK;
+  }
+  *bytes = split_bytes(shape, segments);
+  return GDR_OK;
+}
+
+}  // extern "C"
+
+namespace {
+
+// The chunked forward with `segments` runs per (batch, head) for the two-kernel
+// path (0: the default policy).
+gdr_status chunk_fwd_impl(const gdr_shape* shape, int segments, const void* q, const void* k,
+                          const void* v, const float* g, const float* beta, const float* lam,
+                          const void* b, const void* w, const float* h0, void* o, float* hT,
+                          void* workspace, size_t ws_bytes, gdr_stream_t stream) {
   gdr_status st = check_shape(shape, false);
   if (st != GDR_OK) return st;
   st = check_gates(shape, q, k, v, g, beta, lam, b, w, o);
   if (st != GDR_OK) return st;
   if ((h0 && !aligned(h0, 16)) || (hT && !aligned(hT, 16))) return GDR_ERR_INVALID_ARG;
+  const bool forced = segments > 0;
+  if (forced && segments > 1 && !split_allowed(shape)) return GDR_ERR_UNSUPPORTED;
+  if (forced && static_cast<long long>(shape->B) * segments > 65535)
+    return GDR_ERR_UNSUPPORTED;   // grid z extent of the split scan
+  const int P = forced ? segments : default_segments(shape);
   size_t need_min = 0, need_full = 0;
   gdr_chunk_fwd_workspace_min(shape, &need_min);
-  gdr_chunk_fwd_workspace(shape, &need_full);
+  need_full = split_allowed(shape) ? split_bytes(shape, P) : 0;
   if (need_min > 0 && (!workspace || ws_bytes < need_min || !aligned(workspace, 16)))
     return GDR_ERR_WORKSPACE;
+  if (forced && need_full > 0 && ws_bytes < need_full) return GDR_ERR_WORKSPACE;
 
   const bool f32 = shape->dtype == GDR_F32;
   if (shape->flags & GDR_BETA_CHANNEL) {
@@ -149,11 +236,50 @@ gdr_status gdr_chunk_fwd(const gdr_shape* shape, const void* q, const void* k, c
     int* status = static_cast<int*>(workspace);
     err = cudaMemsetAsync(status, 0, gdr::kStatusWords * sizeof(int), st_);
     if (err == cudaSuccess) {
-      if (ws_bytes >= need_full) {
+      // the two-kernel path without the split when the workspace holds the
+      // packets but not the run states
+      const int runs_req = ws_bytes >= need_full ? P : 1;
+      if (ws_bytes >= two_kernel_bytes(shape)) {
         // two kernels: every chunk's intra-chunk work in parallel, then the state pass
-        unsigned char* packets = static_cast<unsigned char*>(workspace) + gdr::kChunkWorkspaceBytes;
+        unsigned char* base = static_cast<unsigned char*>(workspace);
+        unsigned char* packets = base + gdr::kChunkWorkspaceBytes;
         err = gdr::launch_chunk_prep(a, shape->dk, packets, status, st_);
-        if (err == cudaSuccess) err = gdr::launch_chunk_scan(a, shape->dk, packets, status, st_);
+        if (err == cudaSuccess && runs_req <= 1) {
+          err = gdr::launch_chunk_scan(a, shape->dk, packets, status, st_);
+        } else if (err == cudaSuccess) {
+          // split: each run's local end state H_p (from zero) and transition M_p,
+          // then the start states S_p, then every run from its start state
+          int runs = 1, seg_chunks = 1;
+          split_geometry(shape, runs_req, &runs, &seg_chunks);
+          const size_t nrun = static_cast<size_t>(shape->B) * shape->H * runs_req;
+          const size_t st_b = nrun * shape->dk * shape->dv * sizeof(float);
+          const size_t tr_b = nrun * shape->dk * shape->dk * sizeof(float);
+          float* Hl = reinterpret_cast<float*>(base + align256(two_kernel_bytes(shape)));
+          float* M = reinterpret_cast<float*>(reinterpret_cast<unsigned char*>(Hl) + align256(st_b));
+          float* S0 = reinterpret_cast<float*>(reinterpret_cast<unsigned char*>(M) + align256(tr_b));
+          gdr::ChunkArgs a1 = a;
+          a1.h0 = nullptr;
+          a1.o = nullptr;
+          a1.hT = Hl;
+          gdr::ScanSegments s1;
+          s1.segments = runs;
+          s1.seg_chunks = seg_chunks;
+          s1.hT_per_seg = true;
+          s1.hT_hom = M;
+          err = gdr::launch_chunk_scan(a1, shape->dk, packets, status, st_, s1);
+          if (err == cudaSuccess)
+            err = gdr::launch_segment_combine(M, Hl, h0, S0, shape->B, shape->H, runs, shape->dk,
+                                              shape->dv, st_);
+          if (err == cudaSuccess) {
+            gdr::ChunkArgs a3 = a;
+            a3.h0 = S0;
+            gdr::ScanSegments s3;
+            s3.segments = runs;
+            s3.seg_chunks = seg_chunks;
+            s3.h0_per_seg = true;
+            err = gdr::launch_chunk_scan(a3, shape->dk, packets, status, st_, s3);
+          }
+        }
       } else if (gdr::chunk_fwd_pipe_supports(shape->flags)) {
         CUtensorMap tq, tk, tv;
         if (!gdr::make_bthd_tmap(&tq, q, shape->B, shape->T, shape->H, shape->dk) ||
@@ -167,6 +293,28 @@ gdr_status gdr_chunk_fwd(const gdr_shape* shape, const void* q, const void* k, c
     }
   }
   return err == cudaSuccess ? GDR_OK : GDR_ERR_CUDA;
+}
+
+}  // namespace
+
+extern "C" {
+
+gdr_status gdr_chunk_fwd(const gdr_shape* shape, const void* q, const void* k, const void* v,
+                         const float* g, const float* beta, const float* lam, const void* b,
+                         const void* w, const float* h0, void* o, float* hT, void* workspace,
+                         size_t ws_bytes, gdr_stream_t stream) {
+  return chunk_fwd_impl(shape, 0, q, k, v, g, beta, lam, b, w, h0, o, hT, workspace, ws_bytes,
+                        stream);
+}
+
+gdr_status gdr_chunk_fwd_split(const gdr_shape* shape, int segments, const void* q,
+                               const void* k, const void* v, const float* g, const float* beta,
+                               const float* lam, const void* b, const void* w, const float* h0,
+                               void* o, float* hT, void* workspace, size_t ws_bytes,
+                               gdr_stream_t stream) {
+  if (segments < 1) return GDR_ERR_INVALID_ARG;
+  return chunk_fwd_impl(shape, segments, q, k, v, g, beta, lam, b, w, h0, o, hT, workspace,
+                        ws_bytes, stream);
 }
 
 gdr_status gdr_chunk_fwd_check(const void* workspace, gdr_stream_t stream, int* detail) {

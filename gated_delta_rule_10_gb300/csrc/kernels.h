@@ -79,8 +79,28 @@ cudaError_t launch_chunk_fwd_pipe(const ChunkArgs& a, int dk, const CUtensorMap&
 // state pass over them. `packets` holds B * H * ceil(T / 64) packets.
 cudaError_t launch_chunk_prep(const ChunkArgs& a, int dk, unsigned char* packets, int* status,
                               cudaStream_t stream);
+// Sequence split of the scan: `segments` runs of `seg_chunks` chunks per
+// (batch, head) (seg_chunks 0: one run of every chunk). States per run are
+// [B, H, segments, d_k, width] fp32. h0_per_seg: a.h0 holds one start state
+// per run (else a.h0, [B, H, d_k, d_v], starts run 0 and the others start at
+// zero). hT_per_seg: every run writes its end state to a.hT (else only the
+// last run writes a.hT, [B, H, d_k, d_v]). hT_hom non-null adds d_k / 64
+// identity slices per run whose end states (each run's transition, d_k x d_k)
+// go there.
+struct ScanSegments {
+  int segments = 1;
+  int seg_chunks = 0;
+  bool h0_per_seg = false;
+  bool hT_per_seg = false;
+  float* hT_hom = nullptr;
+};
 cudaError_t launch_chunk_scan(const ChunkArgs& a, int dk, const unsigned char* packets,
-                              int* status, cudaStream_t stream);
+                              int* status, cudaStream_t stream,
+                              const ScanSegments& sg = ScanSegments());
+// S_start[p] = M[p-1] S_start[p-1] + H[p-1] over the runs of each (batch,
+// head), S_start[0] = h0 (or zero): M [B,H,P,d_k,d_k], Hl and S [B,H,P,d_k,d_v].
+cudaError_t launch_segment_combine(const float* M, const float* Hl, const float* h0, float* S,
+                                   int B, int H, int P, int dk, int dv, cudaStream_t stream);
 cudaError_t launch_recurrent_step(const StepArgs& a, int dk, int dv, bool f32,
                                   cudaStream_t stream);
 // Output epilogue over `rows` rows of d_v channels (dv 64, 128 or 256):

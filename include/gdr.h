@@ -118,6 +118,13 @@ typedef struct {
  * runs the state pass over the packets. Total: 256 + B * H * ceil(T / 64) *
  * packet bytes.
  *
+ * When B * H is small the state pass, which walks the chunks of each (batch,
+ * head) in order, leaves most SMs idle; the full size then also holds the
+ * states of a sequence split (see gdr_chunk_fwd_split) and gdr_chunk_fwd uses
+ * it when a cost model of the scan passes (waves of 152 CTAs times chunks per
+ * run) says it is faster, i.e. when B * H is small against the SM count and
+ * the sequences are long; runs hold at least 8 chunks.
+ *
  * gdr_chunk_fwd_workspace_min gives the least a call accepts (256 bytes for
  * bf16: the status words). A bf16 call whose workspace is at least that but
  * smaller than the full size runs the single-kernel path, which keeps every
@@ -167,6 +174,37 @@ gdr_status gdr_chunk_fwd(const gdr_shape* shape, const void* q, const void* k,
                          const float* lam, const void* b, const void* w,
                          const float* h0, void* o, float* hT, void* workspace,
                          size_t ws_bytes, gdr_stream_t stream);
+
+/*
+ * gdr_chunk_fwd with the sequence of every (batch, head) cut into `segments`
+ * runs of equal whole chunks (the last may be shorter; fewer runs when there
+ * are fewer chunks), bf16 two-kernel path only. The state update is affine in
+ * the state, so run p maps its start state by S_end = M_p S_start + H_p, and
+ * the maps of consecutive runs compose in order (LLMs from scratch ch. 11,
+ * section 11.4). The call runs the chunk preparation once, then one scan pass
+ * that gives every run's H_p (from a zero state) and M_p (from the identity,
+ * d_k x d_k), a pass that chains the start states S_p = M_{p-1} S_{p-1} +
+ * H_{p-1} from h0, and a scan pass of every run from its start state that
+ * writes o and, from the last run, hT. The result equals gdr_chunk_fwd up to
+ * rounding. segments = 1 is the plain two-kernel path.
+ *
+ * workspace: at least gdr_chunk_fwd_workspace_split(shape, segments) bytes,
+ * else GDR_ERR_WORKSPACE. segments < 1 is GDR_ERR_INVALID_ARG; segments > 1
+ * with fp32 or GDR_BETA_CHANNEL is GDR_ERR_UNSUPPORTED. Other arguments as
+ * gdr_chunk_fwd.
+ */
+gdr_status gdr_chunk_fwd_split(const gdr_shape* shape, int segments, const void* q,
+                               const void* k, const void* v, const float* g,
+                               const float* beta, const float* lam, const void* b,
+                               const void* w, const float* h0, void* o, float* hT,
+                               void* workspace, size_t ws_bytes, gdr_stream_t stream);
+
+/* Workspace bytes of gdr_chunk_fwd_split: the two-kernel workspace, then
+ * 256-byte aligned per-run buffers (local end states and start states,
+ * B * H * segments * d_k * d_v fp32 each; transitions, B * H * segments * d_k *
+ * d_k fp32) when segments > 1. */
+gdr_status gdr_chunk_fwd_workspace_split(const gdr_shape* shape, int segments,
+                                         size_t* bytes);
 
 /*
  * Reads the status a gdr_chunk_fwd call left in `workspace` once the work

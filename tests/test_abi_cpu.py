@@ -226,3 +226,39 @@ def test_value_beta_flag_rules(L):
     assert _call_chunk(L, _shape(flags=BC), beta=None) == 1
     big = _shape(B=1024, H=128, T=1, flags=BC)                       # grid y extent
     assert _call_chunk(L, big) == 2
+
+
+def test_sequence_split_workspace_and_policy(L):
+    n = ctypes.c_size_t(0)
+    s = _shape(B=2, T=64 * 9 + 17, H=3, dk=128, dv=128)
+    assert L.gdr_chunk_fwd_workspace_split(ctypes.byref(s), 1, ctypes.byref(n)) == 0
+    two = 256 + 2 * 3 * 10 * 74752
+    assert n.value == two
+    assert L.gdr_chunk_fwd_workspace_split(ctypes.byref(s), 4, ctypes.byref(n)) == 0
+    runs = 2 * 3 * 4
+    al = lambda x: (x + 255) // 256 * 256
+    assert n.value == al(two) + 2 * al(runs * 128 * 128 * 4) + al(runs * 128 * 128 * 4)
+    assert L.gdr_chunk_fwd_workspace_split(ctypes.byref(s), 0, ctypes.byref(n)) == 1
+    assert L.gdr_chunk_fwd_workspace_split(ctypes.byref(_shape(dtype=_binding.GDR_F32)), 2,
+                                           ctypes.byref(n)) == 2
+    assert L.gdr_chunk_fwd_workspace_split(ctypes.byref(_shape(flags=gdr.BETA_CHANNEL)), 2,
+                                           ctypes.byref(n)) == 2
+    # default policy: a long sequence with few heads is split, the benchmark shapes are not
+    long_few = _shape(B=1, T=65536, H=4, dk=128, dv=128)
+    assert L.gdr_chunk_fwd_workspace(ctypes.byref(long_few), ctypes.byref(n)) == 0
+    plain = ctypes.c_size_t(0)
+    L.gdr_chunk_fwd_workspace_split(ctypes.byref(long_few), 1, ctypes.byref(plain))
+    assert n.value > plain.value
+    L.gdr_chunk_fwd_workspace_split(ctypes.byref(long_few), 8, ctypes.byref(plain))
+    assert n.value == plain.value                        # 8 x 4 x 4 = 128 CTAs, one wave
+    for B, T, H in ((4, 4096, 16), (4, 8192, 16), (2, 16384, 32), (1, 65536, 32)):
+        shp = _shape(B=B, T=T, H=H, dk=128, dv=128)
+        L.gdr_chunk_fwd_workspace(ctypes.byref(shp), ctypes.byref(n))
+        L.gdr_chunk_fwd_workspace_split(ctypes.byref(shp), 1, ctypes.byref(plain))
+        assert n.value == plain.value
+    # a forced split needs its workspace
+    vp = ctypes.c_void_p
+    assert L.gdr_chunk_fwd_split(ctypes.byref(s), 4, *(vp(FAKE),) * 5, None, None, None, None,
+                                 vp(FAKE), None, vp(FAKE), ctypes.c_size_t(two), None) == 4
+    assert L.gdr_chunk_fwd_split(ctypes.byref(s), 0, *(vp(FAKE),) * 5, None, None, None, None,
+                                 vp(FAKE), None, vp(FAKE), ctypes.c_size_t(two), None) == 1
