@@ -150,7 +150,9 @@ def chunk_fwd(q, k, v, g, beta=None, lam=None, b=None, w=None, h0=None, *, scale
     (beta [B, T, H, d_v] selects the write strength per value channel);
     b: [B, T, H, d_k]; w: [B, T, H, d_v]; h0: [B, H, d_k, d_v] fp32 or None.
     ``flags`` defaults to what the given gates imply (channel g, b, w, lam);
-    ``scale`` to d_k^-1/2. ``segments`` cuts every sequence into that many runs
+    ``scale`` to d_k^-1/2. ``workspace`` defaults to the size of the fastest path
+    (pass a smaller tensor, even an empty one, to select another path).
+    ``segments`` cuts every sequence into that many runs
     (``gdr_chunk_fwd_split``); by default the library decides. Returns (o, hT)
     with hT None unless requested.
     """
@@ -202,7 +204,7 @@ def chunk_fwd_check(workspace, stream=None):
     Returns None when the call completed; raises GdrError(GDR_ERR_TIMEOUT) when a
     bounded device-side wait gave up.
     """
-    if workspace is None:
+    if workspace is None or workspace.numel() < 256:   # no status words: nothing to check
         return None
     detail = (ctypes.c_int * 2)()
     with torch.cuda.device(workspace.device):

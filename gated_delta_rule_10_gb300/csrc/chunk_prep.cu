@@ -33,6 +33,8 @@
 #include "tma.h"
 #include "tri_inverse.cuh"
 
+#include <type_traits>
+
 namespace gdr {
 namespace {
 
@@ -243,6 +245,62 @@ __device__ __forceinline__ void prep_keys_scalar(unsigned char* smem, unsigned c
   }
 }
 
+// Write strength per value channel (PacketVB): Q_gamma = s gamma (.) q and
+// K_gamma = gamma (.) k (rows 64..127 of the same packet tile), K_tail =
+// gamma_C / gamma (.) k; q and k stay as loaded for M1 (k in the E slot).
+template <int DK, int DV>
+__device__ __forceinline__ void prep_keys_vb(const unsigned char* smem, unsigned char* pkt,
+                                             const ChunkArgs& a, const float* sEG,
+                                             const float* sEGL) {
+  using L = PrepLayout<DK, DV>;
+  using P = PacketVB<DK, DV>;
+  constexpr int VK = DK / 8, RB = kThreads / VK, RPB = 64 / RB;
+  const int tid = threadIdx.x, rb = tid / VK, c0 = (tid % VK) * 8, r0 = rb * RPB;
+#pragma unroll
+  for (int i = 0; i < RPB; ++i) {
+    const int r = r0 + i;
+    float qv[8], kv[8];
+    unpack8(ld16(smem, L::oEQ + tc::tile_off(128, 64 + r, c0)), qv);
+    unpack8(ld16(smem, L::oEQ + tc::tile_off(128, r, c0)), kv);
+    const float eg = sEG[r], egl = sEGL[r], sq = a.scale * eg;
+    float Kg[8], Qg[8], Kt[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      Kg[j] = eg * kv[j];
+      Qg[j] = sq * qv[j];
+      Kt[j] = egl * kv[j];
+    }
+    st16(pkt, P::oQY + tc::tile_off(128, r, c0), pack8(Qg));
+    st16(pkt, P::oQY + tc::tile_off(128, 64 + r, c0), pack8(Kg));
+    st16(pkt, P::oKt + tc::tile_off(64, r, c0), pack8(Kt));
+  }
+}
+
+// Write strength per value channel: V (as loaded, the packet's tile layout) and
+// beta (fp32 from memory, bf16 in the tile layout) into the packet.
+template <int DK, int DV>
+__device__ __forceinline__ void prep_values_vb(const unsigned char* smem, unsigned char* pkt,
+                                               const ChunkArgs& a, size_t row0, int h, int Lr) {
+  using L = PrepLayout<DK, DV>;
+  using P = PacketVB<DK, DV>;
+  constexpr int VV = DV / 8, kIter = 64 * VV / kThreads;
+  const int tid = threadIdx.x;
+#pragma unroll
+  for (int u = 0; u < kIter; ++u) {
+    const int it = tid + u * kThreads, r = it / VV, c0 = (it % VV) * 8;
+    const uint32_t off = tc::tile_off(64, r, c0);
+    st16(pkt, P::oU + off, ld16(smem, L::oV + off));
+    float bv[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    if (r < Lr) {
+      const float4* src = reinterpret_cast<const float4*>(a.beta + ((row0 + r) * a.H + h) * DV + c0);
+      const float4 x0 = __ldg(src), x1 = __ldg(src + 1);
+      bv[0] = x0.x; bv[1] = x0.y; bv[2] = x0.z; bv[3] = x0.w;
+      bv[4] = x1.x; bv[5] = x1.y; bv[6] = x1.z; bv[7] = x1.w;
+    }
+    st16(pkt, P::oB + off, pack8(bv));
+  }
+}
+
 // Z = beta v (or w (.) v with the write gate), in place over v.
 template <int DK, int DV, bool WR>
 __device__ __forceinline__ void prep_z(unsigned char* smem, const float* sBeta) {
@@ -269,7 +327,7 @@ __device__ __forceinline__ void prep_z(unsigned char* smem, const float* sBeta) 
   }
 }
 
-template <int DK, int DV, bool SC>
+template <int DK, int DV, bool SC, bool VB>
 __global__ void __launch_bounds__(kThreads, 2)
     chunk_prep_kernel(const ChunkArgs a, const __grid_constant__ CUtensorMap tm_q,
                       const __grid_constant__ CUtensorMap tm_k,
@@ -278,7 +336,8 @@ __global__ void __launch_bounds__(kThreads, 2)
                       const __grid_constant__ CUtensorMap tm_w, unsigned char* packets,
                       int* status) {
   using L = PrepLayout<DK, DV>;
-  using P = Packet<DK, DV>;
+  using P = std::conditional_t<VB, PacketVB<DK, DV>, Packet<DK, DV>>;
+  static_assert(!VB || SC, "the value-channel packets take the scalar-gate tiles");
   extern __shared__ unsigned char smem_raw[];
   unsigned char* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   const uint32_t sbase = smem_u32(smem);
@@ -396,7 +455,10 @@ __global__ void __launch_bounds__(kThreads, 2)
           tc::bulk_prefetch(a.g + ti * DK, DK * 4);
         else
           tc::prefetch_l2(a.g + ti);
-        if (a.beta) tc::prefetch_l2(a.beta + ti);
+        if (VB)
+          tc::bulk_prefetch(a.beta + ti * DV, DV * 4);
+        else if (a.beta)
+          tc::prefetch_l2(a.beta + ti);
         if (QM) tc::prefetch_l2(a.lam + ti);
       }
     }
@@ -404,7 +466,7 @@ __global__ void __launch_bounds__(kThreads, 2)
     // per-row gates while the tiles are in flight: beta, lam; scalar decay cumsum
     if (tid < kChunk) {
       const size_t ti = (row0 + tid) * H + h;
-      sBeta[tid] = (tid < Lr && a.beta) ? __ldg(a.beta + ti) : 0.f;
+      sBeta[tid] = (!VB && tid < Lr && a.beta) ? __ldg(a.beta + ti) : 0.f;
       sLam[tid] = (tid < Lr && QM) ? __ldg(a.lam + ti) : 0.f;
     }
     if (!CH && warp == 3) {
@@ -438,6 +500,14 @@ __global__ void __launch_bounds__(kThreads, 2)
 
     if (__syncthreads_or(!tc::mbar_wait(bar(kBarV), par))) { fail_at = 4 * n; break; }
     v_done = v_issued;
+    if (VB) {
+      prep_values_vb<DK, DV>(smem, pkt, a, row0, h, Lr);
+      __syncthreads();   // v has been copied out: the next chunk's value tiles may land
+      if (wn < total) {
+        if (tid == 64) load_values(wn);
+        ++v_issued;
+      }
+    }
     if (!SC) {
       if (WR)
         prep_z<DK, DV, true>(smem, sBeta);
@@ -447,7 +517,9 @@ __global__ void __launch_bounds__(kThreads, 2)
     }
     if (__syncthreads_or(!tc::mbar_wait(bar(kBarK), par))) { fail_at = 4 * n; break; }
     k_done = k_issued;
-    if (SC) {
+    if (VB) {
+      prep_keys_vb<DK, DV>(smem, pkt, a, sEG, sEGL);
+    } else if (SC) {
       if (QM)
         prep_keys_scalar<DK, DV, true>(smem, pkt, a, sLam, sEG, sEGL);
       else
@@ -496,7 +568,7 @@ __global__ void __launch_bounds__(kThreads, 2)
       float x[32];
       tc::tmem_ld32(tmem + (static_cast<uint32_t>(32 * q) << 16) + c, x);
       if (SC) {   // the row factors the scalar-gate tiles left out: beta_r (T), s (A_qk)
-        const float f = isT ? sBeta[r] : a.scale;
+        const float f = isT ? (VB ? 1.f : sBeta[r]) : a.scale;
 #pragma unroll
         for (int j = 0; j < 32; ++j) x[j] *= f;
       }
@@ -513,7 +585,11 @@ __global__ void __launch_bounds__(kThreads, 2)
         for (int j = 0; j < 32; ++j)
           x[j] = select_f32(c + j < lim, __expf(fminf(Gr - sGs[c + j], 0.f)) * x[j], 0.f);
       }
-      if (isT) {
+      if (isT && VB) {   // L to the packet, fp32 row-major
+        float4* dst = reinterpret_cast<float4*>(pkt + PacketVB<DK, DV>::oL + (r * 64 + c) * 4);
+#pragma unroll
+        for (int j = 0; j < 32; j += 4) dst[j / 4] = make_float4(x[j], x[j + 1], x[j + 2], x[j + 3]);
+      } else if (isT) {
 #pragma unroll
         for (int j = 0; j < 32; ++j) sT[r * 65 + c + j] = x[j];
       } else {
@@ -523,6 +599,15 @@ __global__ void __launch_bounds__(kThreads, 2)
     }
     tc::fence_before_sync();
     __syncthreads();
+    if (VB) {
+      // no inverse and no M2: the key-side tiles are consumed, the chunk is done
+      if (wn < total) {
+        if (tid == 64) load_keys(wn);
+        ++k_issued;
+      }
+      tc::fence_after_sync();
+      continue;
+    }
 
     // ---- A = (I + T)^{-1} (all 8 warps), then the bf16 operand tile ----
     invert_unit_lower_64_w8(sT, sAf, sP, reinterpret_cast<float*>(smem + L::oX), warp, lane,
@@ -616,7 +701,7 @@ __global__ void __launch_bounds__(kThreads, 2)
   if (warp == 0) tc::tmem_dealloc(tmem, L::kTmemCols);
 }
 
-template <int DK, int DV, bool SC>
+template <int DK, int DV, bool SC, bool VB>
 cudaError_t launch_prep_kernel(const ChunkArgs& a, unsigned char* packets, int* status,
                                cudaStream_t stream) {
   using L = PrepLayout<DK, DV>;
@@ -629,7 +714,7 @@ cudaError_t launch_prep_kernel(const ChunkArgs& a, unsigned char* packets, int* 
   tw = tq;
   if ((a.flags & 2u) && !make_bthd_tmap(&tb, a.b, a.B, a.T, a.H, DK)) return cudaErrorInvalidValue;
   if ((a.flags & 4u) && !make_bthd_tmap(&tw, a.w, a.B, a.T, a.H, DV)) return cudaErrorInvalidValue;
-  auto kern = chunk_prep_kernel<DK, DV, SC>;
+  auto kern = chunk_prep_kernel<DK, DV, SC, VB>;
   cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(L::launch_bytes));
   if (err != cudaSuccess) return err;
@@ -647,8 +732,9 @@ cudaError_t launch_prep_kernel(const ChunkArgs& a, unsigned char* packets, int* 
 template <int DK, int DV>
 cudaError_t launch_prep(const ChunkArgs& a, unsigned char* packets, int* status,
                         cudaStream_t stream) {
-  if ((a.flags & 7u) == 0) return launch_prep_kernel<DK, DV, true>(a, packets, status, stream);
-  return launch_prep_kernel<DK, DV, false>(a, packets, status, stream);
+  if (a.flags & 16u) return launch_prep_kernel<DK, DV, true, true>(a, packets, status, stream);
+  if ((a.flags & 7u) == 0) return launch_prep_kernel<DK, DV, true, false>(a, packets, status, stream);
+  return launch_prep_kernel<DK, DV, false, false>(a, packets, status, stream);
 }
 
 }  // namespace

@@ -41,6 +41,8 @@
 #include "packet.h"
 #include "tc.cuh"
 
+#include <type_traits>
+
 namespace gdr {
 namespace {
 
@@ -49,7 +51,7 @@ constexpr int kOut = 256;       // first thread of the output role
 constexpr int kNV = 64;
 constexpr int kStages = 3;
 constexpr uint32_t kTmemCols = 256;
-constexpr uint32_t kChainBar = 1, kOutBar = 2;
+constexpr uint32_t kChainBar = 1, kOutBar = 2, kSubBar = 3;
 constexpr uint32_t kChainThreads = 256;
 constexpr int kHalf = 32;        // value columns per chain thread
 
@@ -60,14 +62,20 @@ enum : uint32_t {
   kFull0 = 0, kEmpty0 = 3, kBW = 6, kBS = 7, kBO0 = 8, kOFree0 = 10, kBars = 12
 };
 
-template <int DK>
+template <int DK, bool VB>
 struct ScanLayout {
-  using P = Packet<DK, 128>;
-  static constexpr uint32_t kStage = P::kCommon + P::kUSlice;   // common part + U slice
+  using P = std::conditional_t<VB, PacketVB<DK, 128>, Packet<DK, 128>>;
+  static constexpr int kNS = VB ? 2 : kStages;                 // stages of the packet ring
+  // common part + U slice (VB: + L + beta slice)
+  static constexpr uint32_t kStage =
+      P::kCommon + P::kUSlice + (VB ? PacketVB<DK, 128>::kL + PacketVB<DK, 128>::kBSlice : 0);
+  static constexpr uint32_t oSL = P::kCommon + P::kUSlice;      // L within a stage (VB)
+  static constexpr uint32_t oSB = oSL + 64 * 64 * 4;            // beta slice within a stage (VB)
   static constexpr uint32_t oStage = 0;
-  static constexpr uint32_t oS = kStages * kStage;              // S_n, K=DK x 64 (B, MN-major)
+  static constexpr uint32_t oS = kNS * kStage;                  // S_n, K=DK x 64 (B, MN-major)
   static constexpr uint32_t oW = oS + DK * 128;                 // W,   K=64 x 64 (B, MN-major)
-  static constexpr uint32_t oBar = oW + 8192;
+  static constexpr uint32_t oR = oW + 8192;                     // VB: R, fp32 [64][65]
+  static constexpr uint32_t oBar = oR + (VB ? 64 * 65 * 4 : 0);
   static constexpr uint32_t oSlot = oBar + kBars * 8;
   static constexpr uint32_t oAbort = oSlot + 4;
   static constexpr uint32_t bytes = oAbort + 12;
@@ -105,12 +113,13 @@ __device__ __forceinline__ bool wait_or_abort(uint32_t mbar, uint32_t parity,
   return false;
 }
 
-template <int DK, int DV>
+template <int DK, int DV, bool VB>
 __global__ void __launch_bounds__(kThreads, 1)
     chunk_scan_kernel(const ChunkArgs a, const unsigned char* packets, int* status,
                       const ScanSegments sg) {
-  using L = ScanLayout<DK>;
-  using P = Packet<DK, DV>;
+  using L = ScanLayout<DK, VB>;
+  using P = std::conditional_t<VB, PacketVB<DK, DV>, Packet<DK, DV>>;
+  constexpr int kStages = L::kNS;
   extern __shared__ unsigned char smem_raw[];
   unsigned char* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   const uint32_t sb = smem_u32(smem);
@@ -164,10 +173,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int s = n % kStages;
     const uint32_t st = sb + L::oStage + s * L::kStage;
     const unsigned char* pk = pk0 + size_t(n) * P::bytes;
-    tc::mbar_arrive_expect_tx(bar(kFull0 + s), P::kCommon + P::kUSlice);
+    tc::mbar_arrive_expect_tx(bar(kFull0 + s), L::kStage);
     tc::bulk_load(st, pk, P::kCommon, bar(kFull0 + s));
     tc::bulk_load(st + P::kCommon, pk + P::oU + (hom ? 0 : slice) * P::kUSlice, P::kUSlice,
                   bar(kFull0 + s));
+    if constexpr (VB) {
+      tc::bulk_load(st + L::oSL, pk + P::oL, P::kL, bar(kFull0 + s));
+      tc::bulk_load(st + L::oSB, pk + P::oB + (hom ? 0 : slice) * P::kBSlice, P::kBSlice,
+                    bar(kFull0 + s));
+    }
   };
 
   if (warp < 8) {
@@ -231,7 +245,56 @@ __global__ void __launch_bounds__(kThreads, 1)
       // W = U + (-Y S_n) -> bf16 operand (warps 2-3), once MMA1 has completed
       // and MMA3 of chunk n-1 (which reads the previous W) is done.
       float gc = 0.f;
-      if (wrole) {
+      if (VB && wrole) {
+        // R = V - K_gamma S_n (lanes 64..127 of D1) into shared memory, then per
+        // value column the substitution (I + diag(beta_c) L) W_c = diag(beta_c) R_c
+        // by warps 2 and 6 (one column per lane), W to the bf16 operand tile
+        ok = wait_or_abort(bar(kBW), n & 1, abort_flag);
+        if (ok && n >= 1) ok = wait_or_abort(bar(kBO0 + ((n - 1) & 1)), ((n - 1) >> 1) & 1, abort_flag);
+        float* sR = reinterpret_cast<float*>(smem + L::oR);
+        if (ok) {
+          tc::fence_after_sync();
+          gc = reinterpret_cast<const float*>(sst + P::oGc)[srow];
+          float x[kHalf];
+          tc::tmem_ld32(tlane + D10 + (n & 1) * 64 + cb, x);
+#pragma unroll
+          for (int j = 0; j < kHalf / 8; ++j) {
+            float u[8];
+            unpack8(*reinterpret_cast<const uint4*>(sst + P::kCommon +
+                                                    tc::tile_off(64, wrow, cb + 8 * j)), u);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) sR[wrow * 65 + cb + 8 * j + i] = u[i] - x[8 * j + i];
+          }
+        }
+        ok = !tc::named_any(kSubBar, 128, !ok);
+        if (ok && q == 2) {
+          const int c = cb + lane;
+          const float* sLm = reinterpret_cast<const float*>(sst + L::oSL);
+          float wv[64];
+#pragma unroll
+          for (int r = 0; r < 64; ++r) {
+            float acc[4] = {sR[r * 65 + c], 0.f, 0.f, 0.f};
+#pragma unroll
+            for (int i = 0; i < (r & ~3); i += 4) {
+              const float4 l = *reinterpret_cast<const float4*>(sLm + r * 64 + i);
+              acc[0] = fmaf(-l.x, wv[i], acc[0]);
+              acc[1] = fmaf(-l.y, wv[i + 1], acc[1]);
+              acc[2] = fmaf(-l.z, wv[i + 2], acc[2]);
+              acc[3] = fmaf(-l.w, wv[i + 3], acc[3]);
+            }
+#pragma unroll
+            for (int i = r & ~3; i < r; ++i) acc[i & 3] = fmaf(-sLm[r * 64 + i], wv[i], acc[i & 3]);
+            const float bta = __bfloat162float(*reinterpret_cast<const __nv_bfloat16*>(
+                sst + L::oSB + tc::tile_off(64, r, c)));
+            wv[r] = bta * ((acc[0] + acc[1]) + (acc[2] + acc[3]));
+          }
+#pragma unroll
+          for (int r = 0; r < 64; ++r)
+            *reinterpret_cast<__nv_bfloat16*>(smem + L::oW + tc::tile_off(64, r, c)) =
+                __float2bfloat16_rn(wv[r]);
+          tc::fence_proxy_async();
+        }
+      } else if (wrole) {
         ok = wait_or_abort(bar(kBW), n & 1, abort_flag);
         if (ok && n >= 1) ok = wait_or_abort(bar(kBO0 + ((n - 1) & 1)), ((n - 1) >> 1) & 1, abort_flag);
         if (ok) {
@@ -383,12 +446,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 0) tc::tmem_dealloc(tmem, kTmemCols);
 }
 
-template <int DK, int DV>
+template <int DK, int DV, bool VB>
 cudaError_t launch_scan(const ChunkArgs& a, const unsigned char* packets, int* status,
                         cudaStream_t stream, ScanSegments sg) {
-  using L = ScanLayout<DK>;
+  using L = ScanLayout<DK, VB>;
   static_assert(L::launch_bytes <= 232448, "shared memory budget of one CTA");
-  auto kern = chunk_scan_kernel<DK, DV>;
+  auto kern = chunk_scan_kernel<DK, DV, VB>;
   cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(L::launch_bytes));
   if (err != cudaSuccess) return err;
@@ -400,15 +463,23 @@ cudaError_t launch_scan(const ChunkArgs& a, const unsigned char* packets, int* s
   return cudaGetLastError();
 }
 
+template <bool VB>
+cudaError_t launch_scan_dims(const ChunkArgs& a, int dk, const unsigned char* packets,
+                             int* status, cudaStream_t stream, const ScanSegments& sg) {
+  if (dk == 64 && a.dv == 64) return launch_scan<64, 64, VB>(a, packets, status, stream, sg);
+  if (dk == 64 && a.dv == 128) return launch_scan<64, 128, VB>(a, packets, status, stream, sg);
+  if (dk == 128 && a.dv == 64) return launch_scan<128, 64, VB>(a, packets, status, stream, sg);
+  if (dk == 128 && a.dv == 128) return launch_scan<128, 128, VB>(a, packets, status, stream, sg);
+  return cudaErrorInvalidValue;
+}
+
 }  // namespace
 
 cudaError_t launch_chunk_scan(const ChunkArgs& a, int dk, const unsigned char* packets,
                               int* status, cudaStream_t stream, const ScanSegments& sg) {
-  if (dk == 64 && a.dv == 64) return launch_scan<64, 64>(a, packets, status, stream, sg);
-  if (dk == 64 && a.dv == 128) return launch_scan<64, 128>(a, packets, status, stream, sg);
-  if (dk == 128 && a.dv == 64) return launch_scan<128, 64>(a, packets, status, stream, sg);
-  if (dk == 128 && a.dv == 128) return launch_scan<128, 128>(a, packets, status, stream, sg);
-  return cudaErrorInvalidValue;
+  // the write strength per value channel (flag 16) takes the substitution variant
+  if (a.flags & 16u) return launch_scan_dims<true>(a, dk, packets, status, stream, sg);
+  return launch_scan_dims<false>(a, dk, packets, status, stream, sg);
 }
 
 }  // namespace gdr

@@ -113,7 +113,9 @@ void split_geometry(const gdr_shape* s, int P, int* runs, int* seg_chunks) {
 
 size_t two_kernel_bytes(const gdr_shape* s) {
   const size_t chunks = static_cast<size_t>(s->B) * s->H * static_cast<size_t>(n_chunks_of(s));
-  return gdr::kChunkWorkspaceBytes + chunks * gdr::packet_bytes(s->dk, s->dv);
+  const size_t per = (s->flags & GDR_BETA_CHANNEL) ? gdr::packet_vb_bytes(s->dk, s->dv)
+                                                   : gdr::packet_bytes(s->dk, s->dv);
+  return gdr::kChunkWorkspaceBytes + chunks * per;
 }
 
 // status words, packets, then per-run local end states, transitions and start states
@@ -157,12 +159,13 @@ gdr_status gdr_chunk_fwd_workspace(const gdr_shape* shape, size_t* bytes) {
   if (st != GDR_OK) return st;
   // bf16: the status words, then one packet per chunk of every (batch, head)
   // for the two-kernel path, and the run states when the sequence is split;
-  // fp32 and the value-channel scan need nothing
-  if (!split_allowed(shape)) {
+  // fp32 needs nothing
+  if (shape->dtype != GDR_BF16) {
     *bytes = 0;
     return GDR_OK;
   }
-  *bytes = split_bytes(shape, default_segments(shape));
+  *bytes = split_allowed(shape) ? split_bytes(shape, default_segments(shape))
+                                : two_kernel_bytes(shape);
   return GDR_OK;
 }
 
@@ -182,7 +185,7 @@ gdr_status gdr_chunk_fwd_workspace_split(const gdr_shape* shape, int segments, s
   if (st != GDR_OK) return st;
   if (!split_allowed(shape)) {
     if (segments > 1) return GDR_ERR_UNSUPPORTED;
-    *bytes = 0;
+    *bytes = shape->dtype == GDR_BF16 ? two_kernel_bytes(shape) : 0;
     return GDR_OK;
   }
   *bytes = split_bytes(shape, segments);
@@ -211,13 +214,17 @@ gdr_status chunk_fwd_impl(const gdr_shape* shape, int segments, const void* q, c
   const int P = forced ? segments : default_segments(shape);
   size_t need_min = 0, need_full = 0;
   gdr_chunk_fwd_workspace_min(shape, &need_min);
-  need_full = split_allowed(shape) ? split_bytes(shape, P) : 0;
+  need_full = split_allowed(shape) ? split_bytes(shape, P)
+                                   : (shape->dtype == GDR_BF16 ? two_kernel_bytes(shape) : 0);
   if (need_min > 0 && (!workspace || ws_bytes < need_min || !aligned(workspace, 16)))
     return GDR_ERR_WORKSPACE;
   if (forced && need_full > 0 && ws_bytes < need_full) return GDR_ERR_WORKSPACE;
 
   const bool f32 = shape->dtype == GDR_F32;
-  if (shape->flags & GDR_BETA_CHANNEL) {
+  // the write strength per value channel: the two-kernel path (bf16, full
+  // workspace) or the token-order scan
+  if ((shape->flags & GDR_BETA_CHANNEL) &&
+      (f32 || !workspace || ws_bytes < two_kernel_bytes(shape) || !aligned(workspace, 16))) {
     const cudaError_t err = gdr::launch_value_beta_scan(
         value_beta_args(shape, q, k, v, g, beta, h0, o, hT), shape->dk, shape->dv, f32,
         reinterpret_cast<cudaStream_t>(stream));

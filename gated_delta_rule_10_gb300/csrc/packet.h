@@ -44,4 +44,36 @@ inline size_t packet_bytes(int dk, int dv) {
   return static_cast<size_t>(3 * 128 * dk + 8192 + 1024 + 128 * dv);
 }
 
+// Packet of the write strength per value channel (one scalar decay per head,
+// beta per value channel; LLMs from scratch ch. 11, section 11.3). Each value
+// column c has its own transition, so there is no shared (I + T)^{-1}; the
+// packet carries what the scan needs to solve per column
+//   (I + diag(beta_c) L) W_c = diag(beta_c) (V_c - K_gamma S_n)_c
+// by substitution, with L = tril(decay (.) K K^T, -1) shared by the columns:
+//   [Q_gamma; K_gamma] 128 x d_k bf16: rows 64..127 hold +gamma_r k_r
+//   K_tail, gamma_C, A_qk              as in Packet
+//   V        64 x d_v bf16 in U's place (64-column blocks, right after A_qk)
+//   L        64 x 64 fp32, row-major, zero on and above the diagonal
+//   beta     64 x d_v bf16, 64-column blocks in the tile layout
+template <int DK, int DV>
+struct PacketVB {
+  static constexpr uint32_t oQY = 0;
+  static constexpr uint32_t oKt = oQY + 256 * DK;
+  static constexpr uint32_t oGc = oKt + 128 * DK;
+  static constexpr uint32_t oAqk = oGc + 1024;
+  static constexpr uint32_t kCommon = oAqk + 8192;
+  static constexpr uint32_t oU = kCommon;           // V
+  static constexpr uint32_t kUSlice = 8192;
+  static constexpr uint32_t oL = oU + 128 * DV;
+  static constexpr uint32_t kL = 64 * 64 * 4;
+  static constexpr uint32_t oB = oL + kL;            // beta
+  static constexpr uint32_t kBSlice = 8192;
+  static constexpr uint32_t bytes = oB + 128 * DV;
+  static_assert(bytes % 1024 == 0, "packets stay 1024-byte multiples");
+};
+
+inline size_t packet_vb_bytes(int dk, int dv) {
+  return static_cast<size_t>(3 * 128 * dk + 8192 + 1024 + 256 * dv + 64 * 64 * 4);
+}
+
 }  // namespace gdr

@@ -60,7 +60,7 @@ def gpu_forward(x, single_kernel=False, **kw):
     d = to_dev(x)
     shape = gdr.make_shape(*d["q"].shape, d["v"].shape[-1], d["q"].dtype, x["flags"], x["scale"])
     n = gdr.chunk_fwd_workspace_bytes(shape, minimum=single_kernel)
-    ws = torch.empty(n, dtype=torch.uint8, device="cuda") if n else None
+    ws = torch.empty(n, dtype=torch.uint8, device="cuda") if (n or single_kernel) else None
     out = gdr.chunk_fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], d["lam"], d["b"], d["w"],
                         d["h0"], scale=x["scale"], flags=x["flags"], workspace=ws, **kw)
     gdr.chunk_fwd_check(ws)

@@ -216,7 +216,12 @@ def test_value_beta_flag_rules(L):
     n = ctypes.c_size_t(7)
     BC = gdr.BETA_CHANNEL
     assert L.gdr_chunk_fwd_workspace(ctypes.byref(_shape(flags=BC)), ctypes.byref(n)) == 0
-    assert n.value == 0                                   # no workspace
+    # bf16: status words + one packet per chunk ([Q_gamma; K_gamma], K_tail, A_qk,
+    # gamma_C, V, L fp32, beta bf16); fp32 needs none
+    assert n.value == 256 + 3 * 64 * 64 * 2 + 8192 + 1024 + 2 * 64 * 64 * 2 + 64 * 64 * 4
+    assert L.gdr_chunk_fwd_workspace(ctypes.byref(_shape(flags=BC, dtype=_binding.GDR_F32)),
+                                     ctypes.byref(n)) == 0
+    assert n.value == 0
     assert L.gdr_chunk_fwd_workspace_min(ctypes.byref(_shape(flags=BC)), ctypes.byref(n)) == 0
     assert n.value == 0
     for other in (gdr.DECAY_CHANNEL, gdr.ERASE_CHANNEL, gdr.WRITE_CHANNEL, gdr.QMIX):

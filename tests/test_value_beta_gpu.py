@@ -2,10 +2,14 @@
 README variant of the LLMs-from-scratch Gated DeltaNet chapter, section 11.3)
 through the C ABI against the float64 oracle.
 
+Two paths: bf16 inputs with the full workspace take the two-kernel chunked
+path (per-column substitution); fp32 inputs, the minimum workspace and the
+decode step take the token-order scan.
+
 Bar, element by element on the same seeded inputs: max|d| / max|ref| <= 2e-2
-for bf16 inputs and 1e-4 for fp32 inputs, for o and the final state. The scan
-keeps the state in fp32 and rounds only o, so the final state is also held to
-1e-4 with bf16 inputs, and fp32 o to 1e-5.
+for bf16 inputs and 1e-4 for fp32 inputs, for o and the final state. The
+token-order scan keeps the state in fp32 and rounds only o, so there the final
+state is also held to 1e-4 with bf16 inputs, and fp32 o to 1e-5.
 """
 import numpy as np
 import pytest
@@ -20,23 +24,44 @@ pytestmark = pytest.mark.gpu
 DTYPES = [torch.float32, torch.bfloat16]
 
 
-def check(x):
-    o, hT = gpu_forward(x)
+def check(x, token):
+    """token: the token-order scan (minimum workspace), else the default path."""
+    o, hT = gpu_forward(x, single_kernel=token)
     torch.cuda.synchronize()
     ro, rh = oracle_forward(x)
     eo, eh = rel_err(o.float().cpu(), ro), rel_err(hT.cpu(), rh)
     f32 = x["q"].dtype == torch.float32
-    assert eo <= (1e-5 if f32 else TOL[torch.bfloat16]), eo
-    assert eh <= 1e-4, eh
+    if token or f32:
+        assert eo <= (1e-5 if f32 else TOL[torch.bfloat16]), eo
+        assert eh <= 1e-4, eh
+    else:
+        assert eo <= TOL[torch.bfloat16] and eh <= TOL[torch.bfloat16], (eo, eh)
     return eo, eh
 
 
 @pytest.mark.parametrize("dtype", DTYPES, ids=["f32", "bf16"])
 @pytest.mark.parametrize("dk,dv", [(64, 64), (128, 128), (64, 128), (128, 64)])
 @pytest.mark.parametrize("T", [1, 31, 32, 33, 100])
-def test_value_beta_small_shapes(T, dk, dv, dtype):
+def test_value_beta_small_shapes_token_scan(T, dk, dv, dtype):
     x = wl.make_inputs("vbeta", 2, T, 3, dk, dv, dtype, seed=T + dk + 3 * dv, h0_std=0.05)
-    check(x)
+    check(x, token=True)
+
+
+@pytest.mark.parametrize("dk,dv", [(64, 64), (128, 128), (64, 128), (128, 64)])
+@pytest.mark.parametrize("T", [1, 63, 64, 65, 130, 64 * 9 + 7])
+def test_value_beta_small_shapes_chunked(T, dk, dv):
+    x = wl.make_inputs("vbeta", 2, T, 3, dk, dv, torch.bfloat16, seed=T + dk + 5 * dv,
+                       h0_std=0.05)
+    check(x, token=False)
+
+
+def test_value_beta_paths_agree():
+    x = wl.make_inputs("vbeta", 2, 333, 4, 128, 128, torch.bfloat16, seed=71, h0_std=0.02)
+    o1, h1 = gpu_forward(x)
+    o2, h2 = gpu_forward(x, single_kernel=True)
+    torch.cuda.synchronize()
+    assert rel_err(o1.float().cpu(), o2.float().cpu().double().numpy()) <= TOL[torch.bfloat16]
+    assert rel_err(h1.cpu(), h2.cpu().double().numpy()) <= TOL[torch.bfloat16]
 
 
 def test_value_beta_zero_state_no_final_state():
@@ -105,5 +130,5 @@ def test_value_beta_workload_full_size_sampled():
         xs = select(x, batches=[b], heads=[h])
         ro, rh = oracle_forward(xs)
         assert rel_err(o[b:b + 1, :, h:h + 1].float().cpu(), ro) <= TOL[torch.bfloat16]
-        assert rel_err(hT[b:b + 1, h:h + 1].cpu(), rh) <= 1e-4
+        assert rel_err(hT[b:b + 1, h:h + 1].cpu(), rh) <= TOL[torch.bfloat16]
     assert torch.isfinite(o).all() and torch.isfinite(hT).all()
