@@ -40,6 +40,7 @@
 #include "kernels.h"
 #include "packet.h"
 #include "tc.cuh"
+#include "tri_inverse.cuh"
 
 #include <type_traits>
 
@@ -248,7 +249,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (VB && wrole) {
         // R = V - K_gamma S_n (lanes 64..127 of D1) into shared memory, then per
         // value column the substitution (I + diag(beta_c) L) W_c = diag(beta_c) R_c
-        // by warps 2 and 6 (one column per lane), W to the bf16 operand tile
+        // (blocked, below), W to the bf16 operand tile
         ok = wait_or_abort(bar(kBW), n & 1, abort_flag);
         if (ok && n >= 1) ok = wait_or_abort(bar(kBO0 + ((n - 1) & 1)), ((n - 1) >> 1) & 1, abort_flag);
         float* sR = reinterpret_cast<float*>(smem + L::oR);
@@ -266,32 +267,59 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int i = 0; i < 8; ++i) sR[wrow * 65 + cb + 8 * j + i] = u[i] - x[8 * j + i];
           }
         }
+        // blocked by 16 rows: R_J -= sum_{I<J} L_JI W_I for all columns on warp MMAs
+        // (fp32 operands split into bf16 hi + lo), then the 16-row diagonal
+        // solve per column on warps 2 and 3 (one column per lane); W overwrites R
         ok = !tc::named_any(kSubBar, 128, !ok);
-        if (ok && q == 2) {
-          const int c = cb + lane;
+        if (ok) {
           const float* sLm = reinterpret_cast<const float*>(sst + L::oSL);
-          float wv[64];
+          const int wi = (warp & 1) | ((warp >> 2) << 1);   // 0..3 over warps 2, 3, 6, 7
+          for (int J = 0; J < 4; ++J) {
+            if (J > 0) {
 #pragma unroll
-          for (int r = 0; r < 64; ++r) {
-            float acc[4] = {sR[r * 65 + c], 0.f, 0.f, 0.f};
-#pragma unroll
-            for (int i = 0; i < (r & ~3); i += 4) {
-              const float4 l = *reinterpret_cast<const float4*>(sLm + r * 64 + i);
-              acc[0] = fmaf(-l.x, wv[i], acc[0]);
-              acc[1] = fmaf(-l.y, wv[i + 1], acc[1]);
-              acc[2] = fmaf(-l.z, wv[i + 2], acc[2]);
-              acc[3] = fmaf(-l.w, wv[i + 3], acc[3]);
+              for (int t = 0; t < 2; ++t) {
+                const int n0 = 8 * (wi + 4 * t);
+                float c4[4] = {0.f, 0.f, 0.f, 0.f};
+                for (int I = 0; I < J; ++I)
+                  mma16x8x16_f32(c4, sLm, 64, 16 * J, 16 * I, sR, 65, 16 * I, n0);
+                const int r = 16 * J + (lane >> 2), nn = n0 + 2 * (lane & 3);
+                sR[r * 65 + nn] -= c4[0];
+                sR[r * 65 + nn + 1] -= c4[1];
+                sR[(r + 8) * 65 + nn] -= c4[2];
+                sR[(r + 8) * 65 + nn + 1] -= c4[3];
+              }
+              tc::named_sync(kSubBar, 128);
             }
+            if (wi < 2) {
+              const int c = 32 * wi + lane;
+              float w16[16];
 #pragma unroll
-            for (int i = r & ~3; i < r; ++i) acc[i & 3] = fmaf(-sLm[r * 64 + i], wv[i], acc[i & 3]);
-            const float bta = __bfloat162float(*reinterpret_cast<const __nv_bfloat16*>(
-                sst + L::oSB + tc::tile_off(64, r, c)));
-            wv[r] = bta * ((acc[0] + acc[1]) + (acc[2] + acc[3]));
+              for (int rr = 0; rr < 16; ++rr) {
+                const int r = 16 * J + rr;
+                float a0 = sR[r * 65 + c], a1 = 0.f;
+#pragma unroll
+                for (int ii = 0; ii < rr; ++ii) {
+                  const float l = sLm[r * 64 + 16 * J + ii];
+                  if (ii & 1)
+                    a1 = fmaf(-l, w16[ii], a1);
+                  else
+                    a0 = fmaf(-l, w16[ii], a0);
+                }
+                const float bta = __bfloat162float(*reinterpret_cast<const __nv_bfloat16*>(
+                    sst + L::oSB + tc::tile_off(64, r, c)));
+                w16[rr] = bta * (a0 + a1);
+              }
+#pragma unroll
+              for (int rr = 0; rr < 16; ++rr) sR[(16 * J + rr) * 65 + c] = w16[rr];
+            }
+            tc::named_sync(kSubBar, 128);
           }
+          // W (fp32 in sR) to the bf16 operand tile: thread -> row, 32 columns
+          const int t = 32 * wi + lane, r = t >> 1, c0 = 32 * (t & 1);
 #pragma unroll
-          for (int r = 0; r < 64; ++r)
-            *reinterpret_cast<__nv_bfloat16*>(smem + L::oW + tc::tile_off(64, r, c)) =
-                __float2bfloat16_rn(wv[r]);
+          for (int j = 0; j < 32; j += 8)
+            *reinterpret_cast<uint4*>(smem + L::oW + tc::tile_off(64, r, c0 + j)) =
+                pack8(sR + r * 65 + c0 + j);
           tc::fence_proxy_async();
         }
       } else if (wrole) {
