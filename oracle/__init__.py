@@ -11,6 +11,8 @@ plain, slow and written to be checked by eye against the pages it cites:
   chunk the algorithm itself defines).
 * ``expansion``   -- the closed-form product expansion of the affine
   recurrence (LLMs-from-scratch ch. 11, section 11.4).
+* ``backward``    -- gradients: float64 autograd through the token recurrence,
+  and the chunkwise backward of the Gated DeltaNet-2 notes (key design 3).
 * ``epilogue``    -- the output epilogue after the read-out: RMSNorm over
   the value channels times a gain, then the SiLU output gate (numpy, fp64).
 * ``native``      -- a ctypes wrapper around ``gdr_oracle.c``: the same
