@@ -7,31 +7,36 @@
 // kernel gives M_p (its identity slices) and H_p (the run from a zero state);
 // this kernel walks the runs in order,
 //   S_start[0] = h0 (or zero),  S_start[p] = M_{p-1} S_start[p-1] + H_{p-1},
-// one CTA per (batch, head, 32 value columns), 2 d_k threads, each owning a
-// 4 x 4 block of the d_k x 32 product. M_{p-1} is staged in shared memory with
-// its rows padded by one float, so the four row groups a warp reads fall in
+// one CTA per (batch, head, 8 value columns) so that even B * H = 1 spreads
+// over d_v / 8 SMs, 256 threads, each owning 4 rows of one column of the
+// d_k x 8 product. M_{p-1} is staged in shared memory with 16-byte loads, its
+// rows padded by four floats so that the row groups a warp reads fall in
 // different banks.
 #include "kernels.h"
 
 namespace gdr {
 namespace {
 
-constexpr int kCombCols = 32;
+constexpr int kCombCols = 8;
+constexpr int kCombThreads = 256;
+constexpr int kCombPad = 4;
 
 template <int DK>
-__global__ void __launch_bounds__(2 * DK)
+__global__ void __launch_bounds__(kCombThreads)
     segment_combine_kernel(const float* __restrict__ M, const float* __restrict__ Hl,
                            const float* __restrict__ h0, float* __restrict__ S, int P, int dv) {
+  constexpr int RPT = DK * kCombCols / kCombThreads;   // rows per thread (4 or 2)
+  constexpr int LD = DK + kCombPad;
   extern __shared__ float smc[];
-  float* sM = smc;                           // [DK][DK + 1]
-  float* sS = sM + DK * (DK + 1);            // [DK][kCombCols]
+  float* sM = smc;                           // [DK][LD]
+  float* sS = sM + DK * LD;                  // [DK][kCombCols]
   const int tid = threadIdx.x;
   const size_t bh = blockIdx.y;
   const int c0 = blockIdx.x * kCombCols;
-  const int r0 = (tid / 8) * 4, cc = (tid % 8) * 4;   // this thread's 4 x 4 block
+  const int cc = tid % kCombCols, r0 = (tid / kCombCols) * RPT;   // column, first row
 
   // S_start[0]
-  for (int e = tid; e < DK * kCombCols; e += 2 * DK) {
+  for (int e = tid; e < DK * kCombCols; e += kCombThreads) {
     const int i = e / kCombCols, c = e % kCombCols;
     const float x = h0 ? h0[(bh * DK + i) * dv + c0 + c] : 0.f;
     sS[e] = x;
@@ -39,34 +44,31 @@ __global__ void __launch_bounds__(2 * DK)
   }
   for (int p = 1; p < P; ++p) {
     const size_t run = bh * P + (p - 1);
-    for (int e = tid; e < DK * DK; e += 2 * DK) {
-      const int i = e / DK, j = e % DK;
-      sM[i * (DK + 1) + j] = M[(run * DK + i) * DK + j];
+    const float4* src = reinterpret_cast<const float4*>(M + run * DK * DK);
+    for (int e = tid; e < DK * DK / 4; e += kCombThreads) {
+      const int i = e / (DK / 4), j = (e % (DK / 4)) * 4;
+      *reinterpret_cast<float4*>(sM + i * LD + j) = __ldg(src + e);
     }
+    float acc[RPT];
+#pragma unroll
+    for (int a = 0; a < RPT; ++a) acc[a] = Hl[(run * DK + r0 + a) * dv + c0 + cc];
     __syncthreads();
-    float acc[4][4];
+#pragma unroll 4
+    for (int j = 0; j < DK; j += 4) {
+      float s4[4];
 #pragma unroll
-    for (int a = 0; a < 4; ++a)
+      for (int u = 0; u < 4; ++u) s4[u] = sS[(j + u) * kCombCols + cc];
 #pragma unroll
-      for (int b = 0; b < 4; ++b) acc[a][b] = Hl[(run * DK + r0 + a) * dv + c0 + cc + b];
-    for (int j = 0; j < DK; ++j) {
-      const float4 s = *reinterpret_cast<const float4*>(sS + j * kCombCols + cc);
-#pragma unroll
-      for (int a = 0; a < 4; ++a) {
-        const float m = sM[(r0 + a) * (DK + 1) + j];
-        acc[a][0] = fmaf(m, s.x, acc[a][0]);
-        acc[a][1] = fmaf(m, s.y, acc[a][1]);
-        acc[a][2] = fmaf(m, s.z, acc[a][2]);
-        acc[a][3] = fmaf(m, s.w, acc[a][3]);
+      for (int a = 0; a < RPT; ++a) {
+        const float4 m = *reinterpret_cast<const float4*>(sM + (r0 + a) * LD + j);
+        acc[a] = fmaf(m.x, s4[0], fmaf(m.y, s4[1], fmaf(m.z, s4[2], fmaf(m.w, s4[3], acc[a]))));
       }
     }
     __syncthreads();   // every thread has read sS and sM of this step
 #pragma unroll
-    for (int a = 0; a < 4; ++a) {
-      *reinterpret_cast<float4*>(sS + (r0 + a) * kCombCols + cc) =
-          make_float4(acc[a][0], acc[a][1], acc[a][2], acc[a][3]);
-      *reinterpret_cast<float4*>(S + ((bh * P + p) * DK + r0 + a) * dv + c0 + cc) =
-          make_float4(acc[a][0], acc[a][1], acc[a][2], acc[a][3]);
+    for (int a = 0; a < RPT; ++a) {
+      sS[(r0 + a) * kCombCols + cc] = acc[a];
+      S[((bh * P + p) * DK + r0 + a) * dv + c0 + cc] = acc[a];
     }
     __syncthreads();
   }
@@ -75,13 +77,13 @@ __global__ void __launch_bounds__(2 * DK)
 template <int DK>
 cudaError_t launch_combine(const float* M, const float* Hl, const float* h0, float* S, int B,
                            int H, int P, int dv, cudaStream_t stream) {
-  const size_t bytes = (static_cast<size_t>(DK) * (DK + 1) + DK * kCombCols) * sizeof(float);
+  const size_t bytes = (static_cast<size_t>(DK) * (DK + kCombPad) + DK * kCombCols) * sizeof(float);
   auto kern = segment_combine_kernel<DK>;
   cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(bytes));
   if (err != cudaSuccess) return err;
   const dim3 grid(dv / kCombCols, static_cast<unsigned>(B) * H);
-  kern<<<grid, 2 * DK, bytes, stream>>>(M, Hl, h0, S, P, dv);
+  kern<<<grid, kCombThreads, bytes, stream>>>(M, Hl, h0, S, P, dv);
   return cudaGetLastError();
 }
 
