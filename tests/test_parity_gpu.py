@@ -299,3 +299,42 @@ def test_binding_errors_on_gpu():
     with pytest.raises(gdr.GdrError) as e:
         gdr.chunk_fwd(q, q, q, x["g"], x["beta"])
     assert e.value.code == 2
+
+
+def test_many_sequences_few_chunks():
+    """B * H = 768 sequences of three chunks: the persistent preparation grid walks
+    2304 chunks in several passes and the scan runs 1536 CTAs; sampled sequences."""
+    B, H, T = 24, 32, 64 * 2 + 9
+    x = wl.make_inputs("kda", B, T, H, 64, 128, torch.bfloat16, seed=91, h0_std=0.02)
+    o, hT = gpu_forward(x)
+    torch.cuda.synchronize()
+    for b, h in [(0, 0), (23, 31), (11, 17)]:
+        xs = select(x, batches=[b], heads=[h])
+        ro, rh = oracle_forward(xs)
+        eo = rel_err(o[b:b + 1, :, h:h + 1].float().cpu(), ro)
+        eh = rel_err(hT[b:b + 1, h:h + 1].cpu(), rh)
+        assert eo <= TOL[torch.bfloat16] and eh <= TOL[torch.bfloat16], (b, h, eo, eh)
+
+
+def test_calls_on_two_streams():
+    """Two forwards with their own workspaces on two streams at once agree with the
+    oracle (nothing in the library is shared between calls)."""
+    xs = [wl.make_inputs(v, 2, 300, 4, 128, 128, torch.bfloat16, seed=s, h0_std=0.02)
+          for v, s in (("gdn", 1), ("gdn2", 2))]
+    streams = [torch.cuda.Stream(), torch.cuda.Stream()]
+    outs = []
+    for x, st in zip(xs, streams):
+        d = to_dev(x)
+        shape = gdr.make_shape(2, 300, 4, 128, 128, torch.bfloat16, x["flags"], x["scale"])
+        ws = torch.empty(gdr.chunk_fwd_workspace_bytes(shape), dtype=torch.uint8, device="cuda")
+        torch.cuda.synchronize()
+        with torch.cuda.stream(st):
+            outs.append(gdr.chunk_fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], d["lam"],
+                                      d["b"], d["w"], d["h0"], scale=x["scale"],
+                                      flags=x["flags"], workspace=ws, stream=st) + (ws, st))
+    torch.cuda.synchronize()
+    for x, (o, hT, ws, st) in zip(xs, outs):
+        gdr.chunk_fwd_check(ws, stream=st)
+        ro, rh = oracle_forward(x)
+        assert rel_err(o.float().cpu(), ro) <= TOL[torch.bfloat16]
+        assert rel_err(hT.cpu(), rh) <= TOL[torch.bfloat16]
