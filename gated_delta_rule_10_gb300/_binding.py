@@ -63,6 +63,8 @@ def lib():
         L.gdr_recurrent_step.argtypes = [sp] + [_vp] * 10 + [_vp]
         L.gdr_gate_cumsum.argtypes = [ctypes.c_int] * 4 + [_vp, _vp, _vp]
         L.gdr_chunk_fwd_check.argtypes = [_vp, _vp, ctypes.POINTER(ctypes.c_int)]
+        L.gdr_chunk_bwd_workspace.argtypes = [sp, ctypes.POINTER(ctypes.c_size_t)]
+        L.gdr_chunk_bwd.argtypes = [sp] + [_vp] * 20 + [_vp, ctypes.c_size_t, _vp]
         L.gdr_rmsnorm_gate.argtypes = [ctypes.c_longlong, ctypes.c_int, ctypes.c_int, _vp, _vp,
                                        _vp, ctypes.c_float, _vp, _vp]
         L.gdr_status_string.argtypes = [ctypes.c_int]
@@ -71,7 +73,8 @@ def lib():
         for name in ("gdr_chunk_fwd_workspace", "gdr_chunk_fwd_workspace_min", "gdr_chunk_fwd",
                      "gdr_chunk_fwd_split", "gdr_chunk_fwd_workspace_split",
                      "gdr_recurrent_step",
-                     "gdr_gate_cumsum", "gdr_chunk_fwd_check", "gdr_rmsnorm_gate"):
+                     "gdr_gate_cumsum", "gdr_chunk_fwd_check", "gdr_rmsnorm_gate",
+                     "gdr_chunk_bwd_workspace", "gdr_chunk_bwd"):
             getattr(L, name).restype = ctypes.c_int
         _lib = L
     return _lib
@@ -292,4 +295,50 @@ def rmsnorm_gate(o, z, weight, eps=1e-6, *, out=None, stream=None):
                                     _ptr(out), _stream(stream, dev))
     if st:
         raise GdrError(st, "gdr_rmsnorm_gate")
+    return out
+
+
+def chunk_bwd_workspace_bytes(shape):
+    n = ctypes.c_size_t(0)
+    st = lib().gdr_chunk_bwd_workspace(ctypes.byref(shape), ctypes.byref(n))
+    if st:
+        raise GdrError(st, "gdr_chunk_bwd_workspace")
+    return n.value
+
+
+def chunk_bwd(q, k, v, g, dO, beta=None, lam=None, b=None, w=None, h0=None, dhT=None, *,
+              scale=None, flags=None, workspace=None, stream=None):
+    """Gradients of <dO, o> + <dhT, hT> for ``chunk_fwd`` on the same inputs
+    (``gdr_chunk_bwd``). Returns a dict of fp32 tensors: q, k, v, g, and beta,
+    lam, b, w, h0 where they apply (None otherwise)."""
+    B, T, H, dk = q.shape
+    dv = v.shape[-1]
+    dev, dt = q.device, q.dtype
+    if flags is None:
+        flags = _infer_flags(g.dim() == 4, b, w, lam)
+    if scale is None:
+        scale = dk ** -0.5
+    _check(dO, "dO", dt, dev, (B, T, H, dv))
+    _check(dhT, "dhT", torch.float32, dev, (B, H, dk, dv))
+    f32 = dict(dtype=torch.float32, device=dev)
+    out = {"q": torch.empty(B, T, H, dk, **f32), "k": torch.empty(B, T, H, dk, **f32),
+           "v": torch.empty(B, T, H, dv, **f32), "g": torch.empty(tuple(g.shape), **f32),
+           "beta": None if beta is None else torch.empty(B, T, H, **f32),
+           "lam": None if lam is None else torch.empty(B, T, H, **f32),
+           "b": None if b is None else torch.empty(B, T, H, dk, **f32),
+           "w": None if w is None else torch.empty(B, T, H, dv, **f32),
+           "h0": torch.empty(B, H, dk, dv, **f32)}
+    shape = make_shape(B, T, H, dk, dv, dt, flags, scale)
+    if workspace is None:
+        workspace = torch.empty(chunk_bwd_workspace_bytes(shape), dtype=torch.uint8, device=dev)
+    with torch.cuda.device(dev):
+        st = lib().gdr_chunk_bwd(ctypes.byref(shape), _ptr(q), _ptr(k), _ptr(v), _ptr(g),
+                                 _ptr(beta), _ptr(lam), _ptr(b), _ptr(w), _ptr(h0), _ptr(dO),
+                                 _ptr(dhT), *(_ptr(out[n]) for n in
+                                              ("q", "k", "v", "g", "beta", "lam", "b", "w",
+                                               "h0")),
+                                 _ptr(workspace), ctypes.c_size_t(workspace.numel()),
+                                 _stream(stream, dev))
+    if st:
+        raise GdrError(st, "gdr_chunk_bwd")
     return out

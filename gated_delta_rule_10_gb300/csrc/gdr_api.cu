@@ -324,6 +324,53 @@ gdr_status gdr_chunk_fwd_split(const gdr_shape* shape, int segments, const void*
                         ws_bytes, stream);
 }
 
+gdr_status gdr_chunk_bwd_workspace(const gdr_shape* shape, size_t* bytes) {
+  if (!bytes) return GDR_ERR_INVALID_ARG;
+  const gdr_status st = check_shape(shape, false);
+  if (st != GDR_OK) return st;
+  if (shape->flags & GDR_BETA_CHANNEL) return GDR_ERR_UNSUPPORTED;
+  *bytes = gdr::chunk_bwd_workspace_bytes(shape->B, shape->T, shape->H, shape->dk, shape->dv);
+  return GDR_OK;
+}
+
+gdr_status gdr_chunk_bwd(const gdr_shape* shape, const void* q, const void* k, const void* v,
+                         const float* g, const float* beta, const float* lam, const void* b,
+                         const void* w, const float* h0, const void* dO, const float* dhT,
+                         float* dq, float* dk, float* dv, float* dg, float* dbeta, float* dlam,
+                         float* db, float* dw, float* dh0, void* workspace, size_t ws_bytes,
+                         gdr_stream_t stream) {
+  gdr_status st = check_shape(shape, false);
+  if (st != GDR_OK) return st;
+  if (shape->flags & GDR_BETA_CHANNEL) return GDR_ERR_UNSUPPORTED;
+  st = check_gates(shape, q, k, v, g, beta, lam, b, w, dO);   // dO takes o's rules
+  if (st != GDR_OK) return st;
+  const unsigned f = shape->flags;
+  const bool need_beta = !((f & GDR_ERASE_CHANNEL) && (f & GDR_WRITE_CHANNEL));
+  if (!dq || !dk || !dv || !dg || (need_beta && !dbeta) || ((f & GDR_QMIX) && !dlam) ||
+      ((f & GDR_ERASE_CHANNEL) && !db) || ((f & GDR_WRITE_CHANNEL) && !dw))
+    return GDR_ERR_INVALID_ARG;
+  for (const void* ptr : {static_cast<const void*>(h0), static_cast<const void*>(dhT),
+                          static_cast<const void*>(dq), static_cast<const void*>(dk),
+                          static_cast<const void*>(dv), static_cast<const void*>(dg),
+                          static_cast<const void*>(dbeta), static_cast<const void*>(dlam),
+                          static_cast<const void*>(db), static_cast<const void*>(dw),
+                          static_cast<const void*>(dh0)})
+    if (ptr && !aligned(ptr, 4)) return GDR_ERR_INVALID_ARG;
+  size_t need = 0;
+  gdr_chunk_bwd_workspace(shape, &need);
+  if (!workspace || ws_bytes < need || !aligned(workspace, 16)) return GDR_ERR_WORKSPACE;
+  gdr::ChunkBwdArgs a;
+  a.q = q; a.k = k; a.v = v; a.dO = dO; a.g = g; a.beta = beta; a.lam = lam; a.b = b; a.w = w;
+  a.h0 = h0; a.dhT = dhT;
+  a.dq = dq; a.dk = dk; a.dv = dv; a.dg = dg; a.dbeta = need_beta ? dbeta : nullptr;
+  a.dlam = dlam; a.db = db; a.dw = dw; a.dh0 = dh0; a.workspace = workspace;
+  a.B = shape->B; a.T = shape->T; a.H = shape->H; a.dk_dim = shape->dk; a.dv_dim = shape->dv;
+  a.flags = f; a.scale = shape->scale;
+  const cudaError_t err = gdr::launch_chunk_bwd(a, shape->dtype == GDR_F32,
+                                                reinterpret_cast<cudaStream_t>(stream));
+  return err == cudaSuccess ? GDR_OK : GDR_ERR_CUDA;
+}
+
 gdr_status gdr_chunk_fwd_check(const void* workspace, gdr_stream_t stream, int* detail) {
   if (!workspace || !aligned(workspace, 16)) return GDR_ERR_INVALID_ARG;
   int words[gdr::kStatusWords] = {0, 0, 0, 0};

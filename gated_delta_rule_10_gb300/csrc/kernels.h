@@ -108,6 +108,22 @@ cudaError_t launch_recurrent_step(const StepArgs& a, int dk, int dv, bool f32,
 cudaError_t launch_rmsnorm_gate(const void* o, const void* z, const float* weight, float eps,
                                 void* y, long long rows, int dv, bool f32,
                                 cudaStream_t stream);
+// Chunkwise backward (every flag but 16): fp32 records in the workspace,
+// chunk_bwd_workspace_bytes of it; gradients are fp32 in the inputs' layouts.
+struct ChunkBwdArgs {
+  const void *q, *k, *v, *dO;
+  const float *g, *beta, *lam;
+  const void *b, *w;
+  const float *h0, *dhT;
+  float *dq, *dk, *dv, *dg, *dbeta, *dlam, *db, *dw, *dh0;
+  void* workspace;
+  int B, T, H, dk_dim, dv_dim;
+  unsigned flags;
+  float scale;
+};
+size_t chunk_bwd_workspace_bytes(int B, int T, int H, int dk, int dv);
+cudaError_t launch_chunk_bwd(const ChunkBwdArgs& a, bool f32, cudaStream_t stream);
+
 // Write strength per value channel (flag 16): token-order scan, fp32 state.
 cudaError_t launch_value_beta_scan(const ValueBetaArgs& a, int dk, int dv, bool f32,
                                    cudaStream_t stream);

@@ -207,6 +207,37 @@ gdr_status gdr_chunk_fwd_workspace_split(const gdr_shape* shape, int segments,
                                          size_t* bytes);
 
 /*
+ * Gradients of the chunked forward (Gated DeltaNet-2 notes, key design 3: the
+ * reverse state pass over chunks, the gate-aware dA = dU Z^T + dY E_bar^T and
+ * the adjoint of the triangular inverse dT = -tril(A^T dA A^T, -1), then the
+ * chain through the decay factors to g, b, w, beta and lam). For the loss
+ * L = <dO, o> + <dhT, hT> of gdr_chunk_fwd on the same inputs it writes
+ *
+ *   dq, dk [B,T,H,d_k] fp32     dv [B,T,H,d_v] fp32
+ *   dg     [B,T,H] fp32, or [B,T,H,d_k] under GDR_DECAY_CHANNEL
+ *   dbeta  [B,T,H] fp32 (required unless both ERASE and WRITE are set)
+ *   dlam   [B,T,H] fp32 (GDR_QMIX)   db [B,T,H,d_k] fp32 (GDR_ERASE_CHANNEL)
+ *   dw     [B,T,H,d_v] fp32 (GDR_WRITE_CHANNEL)
+ *   dh0    [B,H,d_k,d_v] fp32, or NULL
+ *
+ * dO is [B,T,H,d_v] in the call's dtype (16-byte aligned); dhT [B,H,d_k,d_v]
+ * fp32 or NULL (zero). Inputs as gdr_chunk_fwd. The arithmetic is fp32 on the
+ * CUDA cores, through per-chunk records in `workspace` (at least
+ * gdr_chunk_bwd_workspace() bytes, 16-byte aligned; about 0.9 MB per chunk at
+ * d_k = d_v = 128): the chunk's forward quantities, the state entering and
+ * the gradient leaving every chunk. It assumes each in-chunk log-decay sum
+ * stays above -80 (1 / gamma within fp32). GDR_BETA_CHANNEL returns
+ * GDR_ERR_UNSUPPORTED.
+ */
+gdr_status gdr_chunk_bwd_workspace(const gdr_shape* shape, size_t* bytes);
+gdr_status gdr_chunk_bwd(const gdr_shape* shape, const void* q, const void* k, const void* v,
+                         const float* g, const float* beta, const float* lam, const void* b,
+                         const void* w, const float* h0, const void* dO, const float* dhT,
+                         float* dq, float* dk, float* dv, float* dg, float* dbeta, float* dlam,
+                         float* db, float* dw, float* dh0, void* workspace, size_t ws_bytes,
+                         gdr_stream_t stream);
+
+/*
  * Reads the status a gdr_chunk_fwd call left in `workspace` once the work
  * enqueued on `stream` has finished (this call synchronises the stream). It
  * returns GDR_OK, or GDR_ERR_TIMEOUT when a bounded device-side wait of that

@@ -1,0 +1,92 @@
+"""GPU parity of the chunkwise backward (gdr_chunk_bwd) against the float64
+oracle's chunk backward (oracle/backward.py, itself pinned to autograd and to
+finite differences).
+
+Bar, per gradient tensor on the same seeded inputs (the oracle sees the
+dtype-rounded inputs and dO): max|d| / max|ref| <= 1e-4 for fp32 inputs and
+2e-2 for bf16 inputs, as for the forward; the arithmetic is fp32 throughout.
+"""
+import numpy as np
+import pytest
+import torch
+
+import gated_delta_rule_10_gb300 as gdr
+from gated_delta_rule_10_gb300 import workloads as wl
+from oracle import backward as obw
+from tests.gdr_testutil import TOL, f64, rel_err, to_dev
+
+pytestmark = pytest.mark.gpu
+
+NAMES = ("q", "k", "v", "g", "beta", "lam", "b", "w")
+
+
+def _cotangents(x, seed):
+    B, T, H, dk = x["q"].shape
+    dv = x["v"].shape[-1]
+    gen = torch.Generator().manual_seed(seed)
+    dO = torch.randn(B, T, H, dv, generator=gen).to(x["q"].dtype)
+    dhT = torch.randn(B, H, dk, dv, generator=gen) * 0.1
+    return dO, dhT
+
+
+def _oracle(x, dO, dhT, b, h):
+    sel = lambda t: None if t is None else f64(t[b, :, h])
+    S0 = None if x["h0"] is None else f64(x["h0"][b, h])
+    return obw.chunked_backward(*(sel(x[n]) for n in NAMES), S0=S0, scale=x["scale"],
+                                flags=x["flags"], dO=sel(dO), dST=f64(dhT[b, h]), C=64)
+
+
+def check(x, seed=0, seqs=None, tol=None):
+    dO, dhT = _cotangents(x, seed)
+    d = to_dev(x)
+    grads = gdr.chunk_bwd(d["q"], d["k"], d["v"], d["g"], dO.cuda(), d["beta"], d["lam"], d["b"],
+                          d["w"], d["h0"], dhT.cuda(), scale=x["scale"], flags=x["flags"])
+    torch.cuda.synchronize()
+    B, H = x["q"].shape[0], x["q"].shape[2]
+    tol = tol or TOL[x["q"].dtype]
+    worst = 0.0
+    for b, h in (seqs or [(bb, hh) for bb in range(B) for hh in range(H)]):
+        ref = _oracle(x, dO, dhT, b, h)
+        for n in NAMES:
+            if x[n] is None:
+                continue
+            got = grads[n][b, :, h].cpu()
+            e = rel_err(got, ref[n])
+            worst = max(worst, e)
+            assert e <= tol, (n, b, h, e)
+        e = rel_err(grads["h0"][b, h].cpu(), ref["S0"])
+        assert e <= tol, ("h0", b, h, e)
+    return worst
+
+
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16], ids=["f32", "bf16"])
+@pytest.mark.parametrize("flags", range(16))
+def test_backward_every_flag(flags, dtype):
+    x = wl.make_inputs(flags, 2, 64 * 2 + 13, 2, 64, 64, dtype, seed=200 + flags, h0_std=0.05)
+    check(x, seed=flags)
+
+
+@pytest.mark.parametrize("dk,dv", [(128, 128), (64, 128), (128, 64)])
+@pytest.mark.parametrize("variant", ["gdn", "qdelta", "kda", "gdn2"])
+def test_backward_widths(variant, dk, dv):
+    x = wl.make_inputs(variant, 1, 64 * 3 + 1, 2, dk, dv, torch.bfloat16, seed=dk + dv,
+                       h0_std=0.05)
+    check(x, seed=dk)
+
+
+@pytest.mark.parametrize("T", [1, 63, 64, 65])
+def test_backward_short_sequences(T):
+    x = wl.make_inputs("gdn2", 2, T, 3, 64, 64, torch.float32, seed=T, h0_std=0.05)
+    check(x, seed=T)
+
+
+def test_backward_no_initial_state():
+    x = wl.make_inputs("kda", 2, 100, 2, 64, 64, torch.float32, seed=4)
+    assert x["h0"] is None
+    check(x, seed=4)
+
+
+def test_backward_gated_deltanet_workload_sampled():
+    """The 4 x 4096 x 16 x 128 bf16 workload; two sequences against the oracle."""
+    x = wl.config_inputs(2)
+    check(x, seed=5, seqs=[(0, 0), (3, 15)])
