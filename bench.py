@@ -52,6 +52,8 @@ def parse():
                    help="skip the per-value-channel write strength measurement")
     p.add_argument("--no-split", action="store_true",
                    help="skip the sequence-split measurement")
+    p.add_argument("--no-backward", action="store_true",
+                   help="skip the backward measurement")
     return p.parse_args()
 
 
@@ -283,6 +285,8 @@ def run_ours(args):
     value_beta_info = None if args.no_value_beta else measure_value_beta(gdr, dev, stream, flush,
                                                                          K, pk, clk)
     split_info = None if args.no_split else measure_split(gdr, dev, stream, flush, K, pk)
+    backward_info = None if args.no_backward else measure_backward(gdr, xd, c, dev, stream, flush,
+                                                                   min(K, 10), pk, clk)
 
     e2e = None if args.no_e2e else measure_e2e(gdr, x, y, c, dev, args, B, T, H, dk, dv, N)
 
@@ -302,6 +306,7 @@ def run_ours(args):
         "epilogue": epilogue_info,
         "value_beta": value_beta_info,
         "sequence_split": split_info,
+        "backward": backward_info,
         # this library's kernels per timed step: the two-kernel chunked forward
         # (bf16 with the full workspace) or one fused kernel (fp32), then the
         # decode steps
@@ -452,6 +457,60 @@ def measure_split(gdr, dev, stream, flush, K, pk, H=4):
     out["launches_per_call"] = {"split": 4, "one_run": 2}
     out["l2"] = "flushed before every call"
     return out
+
+
+def bwd_flops_per_th(dk, dv, C=64):
+    """Multiply-adds x 2 per token-head of the chunk backward as built: the chunk's
+    forward quantities (T, A, Y, U, A_qk), the forward and reverse state passes
+    (W, S', dW, dS: 6 dk dv), and the per-chunk gradient products (dA_qk, dQ_gamma,
+    dK_bar, dK_tail, dY, dA, dZ, dE_bar, dT)."""
+    d = max(dk, dv)
+    return 2.0 * (8 * dk * dv + 12 * C * d + C * C)
+
+
+def measure_backward(gdr, xd, c, dev, stream, flush, K, pk, clk):
+    """gdr_chunk_bwd on the step's workload (gradients of <dO, o> + <dhT, hT>), timed
+    alone: K calls, L2 flushed before each, CUDA events on the launching stream.
+    Not part of the step or its metric; fp32 arithmetic on the FP32 pipe."""
+    B, T, H, dk, dv = c["B"], c["T"], c["H"], c["dk"], c["dv"]
+    gen = torch.Generator().manual_seed(7)
+    dO = torch.randn(B, T, H, dv, generator=gen).to(c["dtype"]).to(dev)
+    dhT = (torch.randn(B, H, dk, dv, generator=gen) * 0.1).to(dev)
+    shape = gdr.make_shape(B, T, H, dk, dv, c["dtype"], xd["flags"], xd["scale"])
+    ws = torch.empty(gdr.chunk_bwd_workspace_bytes(shape), dtype=torch.uint8, device=dev)
+
+    def call():
+        return gdr.chunk_bwd(xd["q"], xd["k"], xd["v"], xd["g"], dO, xd["beta"], xd["lam"],
+                             xd["b"], xd["w"], xd["h0"], dhT, scale=xd["scale"],
+                             flags=xd["flags"], workspace=ws)
+
+    for _ in range(2):
+        grads = call()
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(K)]
+    torch.cuda.synchronize()
+    for i in range(K):
+        flush.fill_(float(i))
+        ev[i][0].record(stream)
+        call()
+        ev[i][1].record(stream)
+    torch.cuda.synchronize()
+    ms = statistics.mean(ev[i][0].elapsed_time(ev[i][1]) for i in range(K))
+    th = B * T * H
+    flops = bwd_flops_per_th(dk, dv) * th
+    tf = flops / (ms / 1e3) / 1e12
+    peak = fp32_alu_peak_tflops((clk or {}).get("sm_mhz") or 2070.0)
+    nbytes = tensor_bytes(xd["q"], xd["k"], xd["v"], xd["g"], xd["beta"], xd["lam"], xd["b"],
+                          xd["w"], xd["h0"], dO, dhT, *[t for t in grads.values() if t is not None])
+    gbs = nbytes / (ms / 1e3) / 1e9
+    return {"kernels": "bwd_chunk_prep, bwd_state_pass, bwd_dstate_pass, bwd_chunk_grad",
+            "workload": c["name"], "launches": K, "ms_mean": round(ms, 4),
+            "token_heads_per_s": round(th / (ms / 1e3), 1),
+            "roofline": {"bound": "alu", "achieved": round(tf, 2), "peak": round(peak, 2),
+                         "unit": "TFLOP/s", "frac": round(tf / peak, 4),
+                         "peak_source": "derived: 152 SMs x 128 FP32 lanes x 2 x SM clock"},
+            "algorithmic_flops_per_call": flops, "algorithmic_bytes_per_call": nbytes,
+            "achieved_gbs": round(gbs, 1), "frac_hbm": round(gbs / pk["hbm_gbs"], 4),
+            "workspace_bytes": ws.numel(), "l2": "flushed before every call"}
 
 
 def measure_e2e(gdr, x, y, c, dev, args, B, T, H, dk, dv, N, steps=8, n_up=1):

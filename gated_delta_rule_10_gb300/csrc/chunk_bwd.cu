@@ -4,12 +4,12 @@
 // For loss gradients dO (and dS_T) it returns dq, dk, dv, dg, dbeta, dlam, db,
 // dw and dh0 through four kernels over fp32 records in the workspace:
 //   1. bwd_chunk_prep  (one CTA per chunk): the chunk's forward quantities as
-//      the chunk algebra defines them -- G (in-chunk cumsum of g), gamma, the
+//      the chunk algebra defines them -- gamma = exp(in-chunk cumsum of g), the
 //      erase / write vectors E, Z, K_bar = k / gamma, E_bar = gamma E,
 //      T = tril(E_bar K_bar^T, -1), A = (I + T)^{-1} (forward substitution),
 //      Y = A E_bar, U = A Z, Q_gamma = s gamma q, K_tail = gamma_C / gamma k,
 //      A_qk = tril(Q_gamma K_bar^T, 0);
-//   2. bwd_state_pass  (one CTA per (batch, head, 32 value columns)): S_n and
+//   2. bwd_state_pass  (one CTA per (batch, head, 64 value columns)): S_n and
 //      W_n = U - Y S_n of every chunk, S_{n+1} = Diag(gamma_C) S_n + K_tail^T W_n;
 //   3. bwd_dstate_pass (same grid, chunks in reverse): dW_n = A_qk^T dO_n +
 //      K_tail dS_{n+1}, dS_n = Diag(gamma_C) dS_{n+1} + Q_gamma^T dO_n - Y^T dW_n,
@@ -19,9 +19,12 @@
 //      notes' adjoint of the triangular inverse dT = -tril(A^T dA A^T, -1), then
 //      the chain through the decay factors, the cumulative sum and the erase /
 //      write vectors to the inputs.
-// The products run on the FP32 pipe from the records (each CTA's operands stay
-// in L2 while it works); chunks past the end are zero-filled, which leaves every
-// product and the reverse cumulative sum exact for the valid rows.
+// The per-chunk kernels run their products on the tensor cores (warp-level MMA
+// with every fp32 operand split into tf32 hi + lo, about fp32 accuracy), their
+// operands staged through shared memory a 32-wide K slice at a time; the state
+// passes stage each chunk's operands whole and multiply on the FP32 pipe. Chunks
+// past the end are zero-filled, which leaves every product and the reverse
+// cumulative sum exact for the valid rows.
 #include <cuda_bf16.h>
 #include <stdint.h>
 
@@ -33,26 +36,193 @@ namespace {
 constexpr int kC = 64;            // chunk length
 constexpr int kBwdThreads = 256;
 
-// C (m, n) = alpha sum_k A(m, k) B(k, n) + beta C (m, n), every thread of the
-// CTA; operands by strides (a transpose is a stride swap). mask: 0 none,
-// 1 keep n <= m, 2 keep n < m (others written as zero).
-__device__ void block_gemm(float* C, int ldc, const float* A, int sam, int sak, const float* B,
-                           int sbk, int sbn, int M, int N, int K, float alpha, float beta,
-                           int mask = 0) {
-  for (int idx = threadIdx.x; idx < M * N; idx += blockDim.x) {
-    const int m = idx / N, n = idx % N;
-    float acc = 0.f;
-    if (!(mask == 1 && n > m) && !(mask == 2 && n >= m)) {
-      const float* a = A + static_cast<size_t>(m) * sam;
-      const float* b = B + static_cast<size_t>(n) * sbn;
-#pragma unroll 4
-      for (int k = 0; k < K; ++k) acc = fmaf(a[static_cast<size_t>(k) * sak], b[static_cast<size_t>(k) * sbk], acc);
+constexpr int kKT = 32;           // K slice of the staged products
+constexpr int kU = 4;             // elements per thread whose loads are issued together
+
+__device__ __forceinline__ uint32_t sa32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+// 16-byte asynchronous copy global -> shared (both 16-byte aligned)
+__device__ __forceinline__ void cp16(void* smem, const void* gmem) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(sa32(smem)), "l"(gmem)
+               : "memory");
+}
+__device__ __forceinline__ void cp_commit() { asm volatile("cp.async.commit_group;\n" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_wait() {
+  asm volatile("cp.async.wait_group %0;\n" ::"n"(N) : "memory");
+}
+__device__ __forceinline__ float warp_sum(float x) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
+  return x;
+}
+
+// fp32 -> tf32 hi + lo with x ~= hi + lo to ~2^-22 relative (round to nearest each)
+__device__ __forceinline__ uint32_t tf32_rna(float x) {
+  uint32_t r;
+  asm("cvt.rna.tf32.f32 %0, %1;\n" : "=r"(r) : "f"(x));
+  return r;
+}
+__device__ __forceinline__ void split_tf32(float x, uint32_t& hi, uint32_t& lo) {
+  hi = tf32_rna(x);
+  lo = tf32_rna(x - __uint_as_float(hi));
+}
+// warp-level MMA, D = A (16 x 8, row) B (8 x 8, col) + D, tf32 operands, fp32 accumulation
+__device__ __forceinline__ void mma_tf32(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
+                                         uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, "
+      "{%8, %9}, {%0, %1, %2, %3};\n"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+// C (m, n) = alpha sum_k A(m, k) B(k, n) + beta C (m, n) for M = 64 rows and
+// N = 16 TN columns (64 or 128), by the whole CTA (256 threads = 8 warps, each a
+// 16 WM x 32 tile of C in MMA accumulators). A and B are staged through shared
+// memory one 32-wide K slice at a time with asynchronous 16-byte copies, the
+// next slice in flight while the current one is used. Each operand keeps its
+// global layout in shared memory: AK / BK say that A / B is contiguous along k
+// (else along m / n); every base, stride and offset is a multiple of 4 floats.
+// The products run on the tensor cores with each fp32 operand split into tf32
+// hi + lo and the three products lo*hi + hi*lo + hi*hi accumulated in fp32,
+// which keeps about fp32 accuracy (the dropped lo*lo term is ~2^-22 relative).
+// mask: 0 none, 1 keep n <= m, 2 keep n < m (others written as 0).
+template <int TN, bool AK, bool BK>
+__device__ void gemm64_t(float* C, int ldc, const float* A, int sam, int sak, const float* B,
+                         int sbk, int sbn, int K, float alpha, float beta, int mask,
+                         float* sbuf) {
+  constexpr int M = 64, N = 16 * TN;
+  constexpr int WM = N == 128 ? 2 : 1, WN = 4;     // 16-row and 8-column tiles per warp
+  constexpr int WARPS_N = N / (8 * WN);
+  static_assert((M / (16 * WM)) * WARPS_N == kBwdThreads / 32, "one tile per warp");
+  // A slice: AK ? [M][kKT + 4] : [kKT][M + 8];  B slice: BK ? [N][kKT + 4] : [kKT][N + 8]
+  // (the paddings put the 32 lanes of every fragment load in 32 different banks)
+  constexpr int LA = AK ? kKT + 4 : M + 8, LB = BK ? kKT + 4 : N + 8;
+  constexpr int SA = AK ? M * LA : kKT * LA, SB = BK ? N * LB : kKT * LB;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, g = lane >> 2, t = lane & 3;
+  const int m0 = (warp / WARPS_N) * 16 * WM, n0 = (warp % WARPS_N) * 8 * WN;
+  auto stage = [&](int buf, int k0) {
+    float* As = sbuf + buf * (SA + SB);
+    float* Bs = As + SA;
+    for (int idx = tid; idx < M * kKT / 4; idx += blockDim.x) {
+      if (AK) {
+        const int m = idx / (kKT / 4), kk = (idx % (kKT / 4)) * 4;
+        cp16(As + m * LA + kk, A + static_cast<size_t>(m) * sam + k0 + kk);
+      } else {
+        const int m = (idx % (M / 4)) * 4, kk = idx / (M / 4);
+        cp16(As + kk * LA + m, A + static_cast<size_t>(k0 + kk) * sak + m);
+      }
     }
-    float* c = C + static_cast<size_t>(m) * ldc + n;
-    *c = alpha * acc + (beta != 0.f ? beta * *c : 0.f);
+    for (int idx = tid; idx < N * kKT / 4; idx += blockDim.x) {
+      if (BK) {
+        const int n = idx / (kKT / 4), kk = (idx % (kKT / 4)) * 4;
+        cp16(Bs + n * LB + kk, B + static_cast<size_t>(n) * sbn + k0 + kk);
+      } else {
+        const int n = (idx % (N / 4)) * 4, kk = idx / (N / 4);
+        cp16(Bs + kk * LB + n, B + static_cast<size_t>(k0 + kk) * sbk + n);
+      }
+    }
+    cp_commit();
+  };
+  float acc[WM][WN][4];
+#pragma unroll
+  for (int i = 0; i < WM; ++i)
+#pragma unroll
+    for (int j = 0; j < WN; ++j)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) acc[i][j][e] = 0.f;
+  const int slices = K / kKT;
+  stage(0, 0);
+  for (int sl = 0; sl < slices; ++sl) {
+    if (sl + 1 < slices) {
+      stage((sl + 1) & 1, (sl + 1) * kKT);
+      cp_wait<1>();
+    } else {
+      cp_wait<0>();
+    }
+    __syncthreads();
+    const float* As = sbuf + (sl & 1) * (SA + SB);
+    const float* Bs = As + SA;
+    auto a_at = [&](int m, int k) { return AK ? As[m * LA + k] : As[k * LA + m]; };
+    auto b_at = [&](int k, int n) { return BK ? Bs[n * LB + k] : Bs[k * LB + n]; };
+#pragma unroll
+    for (int k8 = 0; k8 < kKT; k8 += 8) {
+      // fragments: A rows g, g + 8 and columns t, t + 4; B rows t, t + 4 and column g
+      uint32_t ah[WM][4], al[WM][4], bh[WN][2], bl[WN][2];
+#pragma unroll
+      for (int i = 0; i < WM; ++i) {
+        const int r = m0 + 16 * i + g, k = k8 + t;
+        split_tf32(a_at(r, k), ah[i][0], al[i][0]);
+        split_tf32(a_at(r + 8, k), ah[i][1], al[i][1]);
+        split_tf32(a_at(r, k + 4), ah[i][2], al[i][2]);
+        split_tf32(a_at(r + 8, k + 4), ah[i][3], al[i][3]);
+      }
+#pragma unroll
+      for (int j = 0; j < WN; ++j) {
+        const int n = n0 + 8 * j + g, k = k8 + t;
+        split_tf32(b_at(k, n), bh[j][0], bl[j][0]);
+        split_tf32(b_at(k + 4, n), bh[j][1], bl[j][1]);
+      }
+#pragma unroll
+      for (int i = 0; i < WM; ++i)
+#pragma unroll
+        for (int j = 0; j < WN; ++j) {
+          mma_tf32(acc[i][j], al[i], bh[j][0], bh[j][1]);
+          mma_tf32(acc[i][j], ah[i], bl[j][0], bl[j][1]);
+          mma_tf32(acc[i][j], ah[i], bh[j][0], bh[j][1]);
+        }
+    }
+    __syncthreads();   // the buffer is restaged two slices on
   }
+  // accumulator e of a tile: row g (+ 8 for e >= 2), column 2 t (+ 1 for odd e)
+#pragma unroll
+  for (int i = 0; i < WM; ++i)
+#pragma unroll
+    for (int j = 0; j < WN; ++j)
+#pragma unroll
+      for (int hf = 0; hf < 2; ++hf) {
+        const int m = m0 + 16 * i + g + 8 * hf, n = n0 + 8 * j + 2 * t;
+        float2* c = reinterpret_cast<float2*>(C + static_cast<size_t>(m) * ldc + n);
+        float2 v = make_float2(alpha * acc[i][j][2 * hf], alpha * acc[i][j][2 * hf + 1]);
+        if (beta != 0.f) {
+          const float2 o = *c;
+          v.x = fmaf(beta, o.x, v.x);
+          v.y = fmaf(beta, o.y, v.y);
+        }
+        if ((mask == 1 && n > m) || (mask == 2 && n >= m)) v.x = 0.f;
+        if ((mask == 1 && n + 1 > m) || (mask == 2 && n + 1 >= m)) v.y = 0.f;
+        *c = v;
+      }
   __syncthreads();
 }
+
+template <int TN>
+__device__ void gemm64_n(float* C, int ldc, const float* A, int sam, int sak, const float* B,
+                         int sbk, int sbn, int K, float alpha, float beta, int mask, float* sbuf) {
+  if (sak == 1) {
+    if (sbk == 1) gemm64_t<TN, true, true>(C, ldc, A, sam, sak, B, sbk, sbn, K, alpha, beta, mask, sbuf);
+    else gemm64_t<TN, true, false>(C, ldc, A, sam, sak, B, sbk, sbn, K, alpha, beta, mask, sbuf);
+  } else {
+    if (sbk == 1) gemm64_t<TN, false, true>(C, ldc, A, sam, sak, B, sbk, sbn, K, alpha, beta, mask, sbuf);
+    else gemm64_t<TN, false, false>(C, ldc, A, sam, sak, B, sbk, sbn, K, alpha, beta, mask, sbuf);
+  }
+}
+
+// M = 64 products with N = 64 or 128 (the only shapes of the chunk algebra).
+__device__ void gemm64(float* C, int ldc, const float* A, int sam, int sak, const float* B,
+                       int sbk, int sbn, int N, int K, float alpha, float beta, float* sbuf,
+                       int mask = 0) {
+  if (N == 128)
+    gemm64_n<8>(C, ldc, A, sam, sak, B, sbk, sbn, K, alpha, beta, mask, sbuf);
+  else
+    gemm64_n<4>(C, ldc, A, sam, sak, B, sbk, sbn, K, alpha, beta, mask, sbuf);
+}
+
+// two stages of the largest slices: A [64][36] (or [kKT][72]), B [128][36] (or [kKT][136])
+constexpr size_t kGemmSmem = static_cast<size_t>(2) * (64 * 36 + 128 * 36) * sizeof(float);
+static_assert(64 * 36 >= kKT * 72 && 128 * 36 >= kKT * 136, "stage sizes cover every layout");
 
 template <typename T>
 __device__ __forceinline__ float ldx(const T* p, size_t i);
@@ -68,8 +238,7 @@ struct Rec {
   int dk, dv;
   __host__ __device__ size_t mk() const { return static_cast<size_t>(kC) * dk; }
   __host__ __device__ size_t mv() const { return static_cast<size_t>(kC) * dv; }
-  __host__ __device__ size_t oG() const { return 0; }
-  __host__ __device__ size_t oGam() const { return oG() + mk(); }
+  __host__ __device__ size_t oGam() const { return 0; }
   __host__ __device__ size_t oE() const { return oGam() + mk(); }
   __host__ __device__ size_t oKb() const { return oE() + mk(); }
   __host__ __device__ size_t oEb() const { return oKb() + mk(); }
@@ -116,115 +285,227 @@ __global__ void __launch_bounds__(kBwdThreads) bwd_chunk_prep(const BwdPtrs p) {
   const int dk = p.dk, dv = p.dv, tid = threadIdx.x;
   float* r = p.rec + static_cast<size_t>(cid) * R.size();
   const bool CH = p.flags & 1u, ER = p.flags & 2u, WR = p.flags & 4u, QM = p.flags & 8u;
+  extern __shared__ float sg[];
   const T* q = static_cast<const T*>(p.q);
   const T* k = static_cast<const T*>(p.k);
   const T* v = static_cast<const T*>(p.v);
   const T* bg = static_cast<const T*>(p.b);
   const T* wg = static_cast<const T*>(p.w);
   auto tok = [&](int i) { return (static_cast<size_t>(bb) * p.T + t0 + i) * p.H + h; };
-  // G: in-chunk inclusive cumsum per key channel (scalar gates broadcast)
-  for (int c = tid; c < dk; c += blockDim.x) {
+  const int bd = blockDim.x;
+  // G: in-chunk inclusive cumsum of the log-decay (per key channel, or one per row
+  // broadcast over the channels), in shared memory; rows past the end add nothing
+  float* sG = sg;                  // [64][dk] (per channel) or [64]
+  float* sGC = sg + kC * dk;       // [dk] gamma_C
+  if (CH) {
+    for (int e0 = tid; e0 < kC * dk; e0 += kU * bd) {
+      float x[kU];
+#pragma unroll
+      for (int u = 0; u < kU; ++u) {
+        const int e = e0 + u * bd, i = e / dk;
+        x[u] = (e < kC * dk && i < Lr) ? p.g[tok(i) * dk + e % dk] : 0.f;
+      }
+#pragma unroll
+      for (int u = 0; u < kU; ++u)
+        if (e0 + u * bd < kC * dk) sG[e0 + u * bd] = x[u];
+    }
+  } else if (tid < kC) {
+    sG[tid] = tid < Lr ? p.g[tok(tid)] : 0.f;
+  }
+  __syncthreads();
+  if (CH) {
+    for (int c = tid; c < dk; c += bd) {
+      float acc = 0.f;
+      for (int i = 0; i < kC; ++i) {
+        acc += sG[i * dk + c];
+        sG[i * dk + c] = acc;
+      }
+      sGC[c] = expf(acc);
+    }
+  } else if (tid == 0) {
     float acc = 0.f;
     for (int i = 0; i < kC; ++i) {
-      if (i < Lr) acc += CH ? p.g[tok(i) * dk + c] : p.g[tok(i)];
-      r[R.oG() + i * dk + c] = acc;
-      r[R.oGam() + i * dk + c] = expf(acc);
+      acc += sG[i];
+      sG[i] = acc;
     }
   }
   __syncthreads();
-  // E, x (erase input), K_bar, E_bar, Q_gamma, K_tail
-  for (int e = tid; e < kC * dk; e += blockDim.x) {
-    const int i = e / dk, c = e % dk;
-    float qv = 0.f, kv = 0.f, x = 0.f, E = 0.f;
-    if (i < Lr) {
-      qv = ldx(q, tok(i) * dk + c);
-      kv = ldx(k, tok(i) * dk + c);
-      x = QM ? kv + p.lam[tok(i)] * qv : kv;
-      E = ER ? ldx(bg, tok(i) * dk + c) * x : p.beta[tok(i)] * x;
+  if (!CH)
+    for (int c = tid; c < dk; c += bd) sGC[c] = expf(sG[kC - 1]);
+  __syncthreads();
+  // gamma, x (erase input), E, K_bar, E_bar, Q_gamma, K_tail; loads batched ahead
+  // of the stores so that they overlap
+  for (int e0 = tid; e0 < kC * dk; e0 += kU * bd) {
+    float qv[kU], kv[kU], bv[kU], rb[kU], rl[kU];
+#pragma unroll
+    for (int u = 0; u < kU; ++u) {
+      const int e = e0 + u * bd, i = e / dk, c = e % dk;
+      const bool ok = e < kC * dk && i < Lr;
+      qv[u] = ok ? ldx(q, tok(i) * dk + c) : 0.f;
+      kv[u] = ok ? ldx(k, tok(i) * dk + c) : 0.f;
+      bv[u] = ok && ER ? ldx(bg, tok(i) * dk + c) : 0.f;
+      rb[u] = ok && !ER ? p.beta[tok(i)] : 0.f;
+      rl[u] = ok && QM ? p.lam[tok(i)] : 0.f;
     }
-    const float gam = r[R.oGam() + e], gC = r[R.oGam() + (kC - 1) * dk + c];
-    r[R.oX() + e] = x;
-    r[R.oE() + e] = E;
-    r[R.oKb() + e] = kv / gam;
-    r[R.oEb() + e] = gam * E;
-    r[R.oQg() + e] = p.scale * gam * qv;
-    r[R.oKt() + e] = gC / gam * kv;
+#pragma unroll
+    for (int u = 0; u < kU; ++u) {
+      const int e = e0 + u * bd, i = e / dk, c = e % dk;
+      if (e >= kC * dk) continue;
+      const float gam = expf(CH ? sG[e] : sG[i]), gC = sGC[c];
+      const float x = QM ? kv[u] + rl[u] * qv[u] : kv[u];
+      const float E = ER ? bv[u] * x : rb[u] * x;
+      r[R.oGam() + e] = gam;
+      r[R.oX() + e] = x;
+      r[R.oE() + e] = E;
+      r[R.oKb() + e] = kv[u] / gam;
+      r[R.oEb() + e] = gam * E;
+      r[R.oQg() + e] = p.scale * gam * qv[u];
+      r[R.oKt() + e] = gC / gam * kv[u];
+    }
   }
-  for (int e = tid; e < kC * dv; e += blockDim.x) {
-    const int i = e / dv, c = e % dv;
-    float z = 0.f;
-    if (i < Lr) {
-      const float vv = ldx(v, tok(i) * dv + c);
-      z = WR ? ldx(wg, tok(i) * dv + c) * vv : p.beta[tok(i)] * vv;
+  for (int e0 = tid; e0 < kC * dv; e0 += kU * bd) {
+    float vv[kU], sc[kU];
+#pragma unroll
+    for (int u = 0; u < kU; ++u) {
+      const int e = e0 + u * bd, i = e / dv;
+      const bool ok = e < kC * dv && i < Lr;
+      vv[u] = ok ? ldx(v, tok(i) * dv + e % dv) : 0.f;
+      sc[u] = !ok ? 0.f : WR ? ldx(wg, tok(i) * dv + e % dv) : p.beta[tok(i)];
     }
-    r[R.oZ() + e] = z;
+#pragma unroll
+    for (int u = 0; u < kU; ++u)
+      if (e0 + u * bd < kC * dv) r[R.oZ() + e0 + u * bd] = sc[u] * vv[u];
   }
   __syncthreads();
   // T = tril(E_bar K_bar^T, -1), A_qk = tril(Q_gamma K_bar^T, 0)
-  block_gemm(r + R.oT(), kC, r + R.oEb(), dk, 1, r + R.oKb(), 1, dk, kC, kC, dk, 1.f, 0.f, 2);
-  block_gemm(r + R.oAqk(), kC, r + R.oQg(), dk, 1, r + R.oKb(), 1, dk, kC, kC, dk, 1.f, 0.f, 1);
-  // A = (I + T)^{-1}: row r of (I + T) A = I gives A_r = e_r - sum_{i<r} T_ri A_i;
-  // thread c owns column c
-  if (tid < kC) {
-    float* A = r + R.oA();
-    const float* Tm = r + R.oT();
-    for (int i = 0; i < kC; ++i) {
-      float acc = (i == tid) ? 1.f : 0.f;
-      for (int j = 0; j < i; ++j) acc = fmaf(-Tm[i * kC + j], A[j * kC + tid], acc);
-      A[i * kC + tid] = acc;
+  gemm64(r + R.oT(), kC, r + R.oEb(), dk, 1, r + R.oKb(), 1, dk, kC, dk, 1.f, 0.f, sg, 2);
+  gemm64(r + R.oAqk(), kC, r + R.oQg(), dk, 1, r + R.oKb(), 1, dk, kC, dk, 1.f, 0.f, sg, 1);
+  // A = (I + T)^{-1}: row i of (I + T) A = I gives A_i = e_i - sum_{j<i} T_ij A_j.
+  // T and A sit in shared memory; thread c owns column c (two accumulators).
+  {
+    float* sT = sg;              // [64][64]
+    float* sA = sg + kC * kC;    // [64][65]
+    for (int e = tid * 4; e < kC * kC; e += blockDim.x * 4) cp16(sT + e, r + R.oT() + e);
+    cp_commit();
+    cp_wait<0>();
+    __syncthreads();
+    if (tid < kC) {
+      for (int i = 0; i < kC; ++i) {
+        float a0 = (i == tid) ? 1.f : 0.f, a1 = 0.f;
+        const float* Ti = sT + i * kC;
+        int j = 0;
+        for (; j + 4 <= i; j += 4) {
+          const float4 t4 = *reinterpret_cast<const float4*>(Ti + j);
+          a0 = fmaf(-t4.x, sA[j * 65 + tid], a0);
+          a1 = fmaf(-t4.y, sA[(j + 1) * 65 + tid], a1);
+          a0 = fmaf(-t4.z, sA[(j + 2) * 65 + tid], a0);
+          a1 = fmaf(-t4.w, sA[(j + 3) * 65 + tid], a1);
+        }
+        for (; j < i; ++j) a0 = fmaf(-Ti[j], sA[j * 65 + tid], a0);
+        sA[i * 65 + tid] = a0 + a1;
+      }
     }
+    __syncthreads();
+    for (int e = tid; e < kC * kC; e += blockDim.x) r[R.oA() + e] = sA[(e / kC) * 65 + e % kC];
+    __syncthreads();
   }
-  __syncthreads();
   // Y = A E_bar, U = A Z
-  block_gemm(r + R.oY(), dk, r + R.oA(), kC, 1, r + R.oEb(), dk, 1, kC, dk, kC, 1.f, 0.f);
-  block_gemm(r + R.oU(), dv, r + R.oA(), kC, 1, r + R.oZ(), dv, 1, kC, dv, kC, 1.f, 0.f);
+  gemm64(r + R.oY(), dk, r + R.oA(), kC, 1, r + R.oEb(), dk, 1, dk, kC, 1.f, 0.f, sg);
+  gemm64(r + R.oU(), dv, r + R.oA(), kC, 1, r + R.oZ(), dv, 1, dv, kC, 1.f, 0.f, sg);
 }
 
 // ------------------------------------------------------- 2. forward states
-constexpr int kSlice = 32;
+constexpr int kSlice = 64;          // value columns per state-pass CTA
+constexpr int kPassThreads = 512;
 
-__global__ void __launch_bounds__(kBwdThreads) bwd_state_pass(const BwdPtrs p) {
+// Each chunk's operands are staged in shared memory (coalesced copies from the
+// records), then every product reads shared memory only.
+__host__ __device__ constexpr size_t state_pass_floats(int dk) {
+  return static_cast<size_t>(dk) * kSlice + kC * kSlice + kC * (dk + 4) + kC * dk +
+         kC * kSlice + dk;
+}
+
+__global__ void __launch_bounds__(kPassThreads) bwd_state_pass(const BwdPtrs p) {
   const Rec R{p.dk, p.dv};
   const int col0 = blockIdx.x * kSlice, h = blockIdx.y, bb = blockIdx.z;
   const int dk = p.dk, dv = p.dv, tid = threadIdx.x;
   extern __shared__ float sm[];
   float* S = sm;                       // [dk][kSlice]
   float* Wl = S + dk * kSlice;         // [64][kSlice]
+  float* Ys = Wl + kC * kSlice;        // [64][dk + 4]
+  float* Kts = Ys + kC * (dk + 4);     // [64][dk]
+  float* Us = Kts + kC * dk;           // [64][kSlice]
+  float* gC = Us + kC * kSlice;        // [dk]
   for (int e = tid; e < dk * kSlice; e += blockDim.x) {
     const int i = e / kSlice, c = e % kSlice;
     S[e] = p.h0 ? p.h0[((static_cast<size_t>(bb) * p.H + h) * dk + i) * dv + col0 + c] : 0.f;
   }
-  __syncthreads();
   for (int n = 0; n < p.Nc; ++n) {
     const size_t cid = chunk_id(p, bb, h, n);
     const float* r = p.rec + cid * R.size();
     float* Sg = p.S + cid * dk * dv;
     float* Wg = p.W + cid * kC * dv;
+    __syncthreads();   // S of the previous chunk is complete
     for (int e = tid; e < dk * kSlice; e += blockDim.x)
       Sg[(e / kSlice) * dv + col0 + e % kSlice] = S[e];
-    // W = U - Y S
-    for (int e = tid; e < kC * kSlice; e += blockDim.x) {
-      const int i = e / kSlice, c = e % kSlice;
-      float acc = r[R.oU() + i * dv + col0 + c];
-      for (int j = 0; j < dk; ++j) acc = fmaf(-r[R.oY() + i * dk + j], S[j * kSlice + c], acc);
-      Wl[e] = acc;
-      Wg[i * dv + col0 + c] = acc;
+    for (int e = tid * 4; e < kC * dk; e += blockDim.x * 4) {
+      cp16(Ys + (e / dk) * (dk + 4) + e % dk, r + R.oY() + e);
+      cp16(Kts + e, r + R.oKt() + e);
+    }
+    for (int e = tid * 4; e < kC * kSlice; e += blockDim.x * 4)
+      cp16(Us + e, r + R.oU() + (e / kSlice) * dv + col0 + e % kSlice);
+    for (int i = tid * 4; i < dk; i += blockDim.x * 4) cp16(gC + i, r + R.oGam() + (kC - 1) * dk + i);
+    cp_commit();
+    cp_wait<0>();
+    __syncthreads();
+    // W = U - Y S: thread -> (row i, 8 columns)
+    {
+      const int i = tid / (kSlice / 8), c0 = (tid % (kSlice / 8)) * 8;
+      float acc[8];
+#pragma unroll
+      for (int c = 0; c < 8; ++c) acc[c] = Us[i * kSlice + c0 + c];
+      for (int j = 0; j < dk; ++j) {
+        const float y = Ys[i * (dk + 4) + j];
+#pragma unroll
+        for (int c = 0; c < 8; ++c) acc[c] = fmaf(-y, S[j * kSlice + c0 + c], acc[c]);
+      }
+#pragma unroll
+      for (int c = 0; c < 8; ++c) {
+        Wl[i * kSlice + c0 + c] = acc[c];
+        Wg[i * dv + col0 + c0 + c] = acc[c];
+      }
     }
     __syncthreads();
-    // S' = Diag(gamma_C) S + K_tail^T W
-    for (int e = tid; e < dk * kSlice; e += blockDim.x) {
-      const int i = e / kSlice, c = e % kSlice;
-      float acc = r[R.oGam() + (kC - 1) * dk + i] * S[e];
-      for (int j = 0; j < kC; ++j) acc = fmaf(r[R.oKt() + j * dk + i], Wl[j * kSlice + c], acc);
-      S[e] = acc;   // each thread owns its elements; W is read from Wl only
+    // S' = Diag(gamma_C) S + K_tail^T W: thread -> (channel i, kSlice * dk / 512 columns)
+    {
+      constexpr int kMaxCols = 16;
+      const int per = dk * kSlice / kPassThreads;         // 16 (dk = 128) or 8 (dk = 64)
+      const int groups = kSlice / per;
+      const int i = tid / groups, c0 = (tid % groups) * per;
+      float acc[kMaxCols];
+#pragma unroll
+      for (int c = 0; c < kMaxCols; ++c) acc[c] = c < per ? gC[i] * S[i * kSlice + c0 + c] : 0.f;
+      for (int j = 0; j < kC; ++j) {
+        const float kt = Kts[j * dk + i];
+#pragma unroll
+        for (int c = 0; c < kMaxCols; ++c)
+          if (c < per) acc[c] = fmaf(kt, Wl[j * kSlice + c0 + c], acc[c]);
+      }
+#pragma unroll
+      for (int c = 0; c < kMaxCols; ++c)
+        if (c < per) S[i * kSlice + c0 + c] = acc[c];   // this thread's own elements
     }
-    __syncthreads();
   }
 }
 
 // ------------------------------------------------------- 3. reverse states
+__host__ __device__ constexpr size_t dstate_pass_floats(int dk) {
+  return static_cast<size_t>(dk) * kSlice + 2 * kC * kSlice + kC * kC + kC * (dk + 4) +
+         2 * kC * dk + dk;
+}
+
 template <typename T>
-__global__ void __launch_bounds__(kBwdThreads) bwd_dstate_pass(const BwdPtrs p) {
+__global__ void __launch_bounds__(kPassThreads) bwd_dstate_pass(const BwdPtrs p) {
   const Rec R{p.dk, p.dv};
   const int col0 = blockIdx.x * kSlice, h = blockIdx.y, bb = blockIdx.z;
   const int dk = p.dk, dv = p.dv, tid = threadIdx.x;
@@ -233,17 +514,22 @@ __global__ void __launch_bounds__(kBwdThreads) bwd_dstate_pass(const BwdPtrs p) 
   float* dS = sm;                      // [dk][kSlice]
   float* dWl = dS + dk * kSlice;       // [64][kSlice]
   float* dOl = dWl + kC * kSlice;      // [64][kSlice]
+  float* Aq = dOl + kC * kSlice;       // [64][64]
+  float* Kts = Aq + kC * kC;           // [64][dk + 4]
+  float* Qg = Kts + kC * (dk + 4);     // [64][dk]
+  float* Ys = Qg + kC * dk;            // [64][dk]
+  float* gC = Ys + kC * dk;            // [dk]
   for (int e = tid; e < dk * kSlice; e += blockDim.x) {
     const int i = e / kSlice, c = e % kSlice;
     dS[e] = p.dhT ? p.dhT[((static_cast<size_t>(bb) * p.H + h) * dk + i) * dv + col0 + c] : 0.f;
   }
-  __syncthreads();
   for (int n = p.Nc - 1; n >= 0; --n) {
     const size_t cid = chunk_id(p, bb, h, n);
     const float* r = p.rec + cid * R.size();
     const int t0 = n * kC, Lr = min(kC, p.T - t0);
     float* dSg = p.dS + cid * dk * dv;
     float* dWg = p.dW + cid * kC * dv;
+    __syncthreads();   // dS of the later chunk is complete
     for (int e = tid; e < dk * kSlice; e += blockDim.x)
       dSg[(e / kSlice) * dv + col0 + e % kSlice] = dS[e];
     for (int e = tid; e < kC * kSlice; e += blockDim.x) {
@@ -251,29 +537,59 @@ __global__ void __launch_bounds__(kBwdThreads) bwd_dstate_pass(const BwdPtrs p) 
       dOl[e] = i < Lr ? ldx(dO, ((static_cast<size_t>(bb) * p.T + t0 + i) * p.H + h) * dv + col0 + c)
                       : 0.f;
     }
-    __syncthreads();
-    // dW = A_qk^T dO + K_tail dS'
-    for (int e = tid; e < kC * kSlice; e += blockDim.x) {
-      const int i = e / kSlice, c = e % kSlice;
-      float acc = 0.f;
-      for (int j = 0; j < kC; ++j) acc = fmaf(r[R.oAqk() + j * kC + i], dOl[j * kSlice + c], acc);
-      for (int j = 0; j < dk; ++j) acc = fmaf(r[R.oKt() + i * dk + j], dS[j * kSlice + c], acc);
-      dWl[e] = acc;
-      dWg[i * dv + col0 + c] = acc;
+    for (int e = tid * 4; e < kC * kC; e += blockDim.x * 4) cp16(Aq + e, r + R.oAqk() + e);
+    for (int e = tid * 4; e < kC * dk; e += blockDim.x * 4) {
+      cp16(Kts + (e / dk) * (dk + 4) + e % dk, r + R.oKt() + e);
+      cp16(Qg + e, r + R.oQg() + e);
+      cp16(Ys + e, r + R.oY() + e);
     }
+    for (int i = tid * 4; i < dk; i += blockDim.x * 4) cp16(gC + i, r + R.oGam() + (kC - 1) * dk + i);
+    cp_commit();
+    cp_wait<0>();
     __syncthreads();
-    // dS = Diag(gamma_C) dS' + Q_gamma^T dO - Y^T dW
-    for (int e = tid; e < dk * kSlice; e += blockDim.x) {
-      const int i = e / kSlice, c = e % kSlice;
-      float acc = r[R.oGam() + (kC - 1) * dk + i] * dS[e];
+    // dW = A_qk^T dO + K_tail dS': thread -> (row i, 8 columns)
+    {
+      const int i = tid / (kSlice / 8), c0 = (tid % (kSlice / 8)) * 8;
+      float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
       for (int j = 0; j < kC; ++j) {
-        acc = fmaf(r[R.oQg() + j * dk + i], dOl[j * kSlice + c], acc);
-        acc = fmaf(-r[R.oY() + j * dk + i], dWl[j * kSlice + c], acc);
+        const float a = Aq[j * kC + i];
+#pragma unroll
+        for (int c = 0; c < 8; ++c) acc[c] = fmaf(a, dOl[j * kSlice + c0 + c], acc[c]);
       }
-      dS[e] = acc;
+      for (int j = 0; j < dk; ++j) {
+        const float kt = Kts[i * (dk + 4) + j];
+#pragma unroll
+        for (int c = 0; c < 8; ++c) acc[c] = fmaf(kt, dS[j * kSlice + c0 + c], acc[c]);
+      }
+#pragma unroll
+      for (int c = 0; c < 8; ++c) {
+        dWl[i * kSlice + c0 + c] = acc[c];
+        dWg[i * dv + col0 + c0 + c] = acc[c];
+      }
     }
     __syncthreads();
+    // dS = Diag(gamma_C) dS' + Q_gamma^T dO - Y^T dW: thread -> (channel i, columns)
+    {
+      constexpr int kMaxCols = 16;
+      const int per = dk * kSlice / kPassThreads;
+      const int groups = kSlice / per;
+      const int i = tid / groups, c0 = (tid % groups) * per;
+      float acc[kMaxCols];
+#pragma unroll
+      for (int c = 0; c < kMaxCols; ++c) acc[c] = c < per ? gC[i] * dS[i * kSlice + c0 + c] : 0.f;
+      for (int j = 0; j < kC; ++j) {
+        const float qg = Qg[j * dk + i], y = Ys[j * dk + i];
+#pragma unroll
+        for (int c = 0; c < kMaxCols; ++c)
+          if (c < per)
+            acc[c] = fmaf(qg, dOl[j * kSlice + c0 + c], fmaf(-y, dWl[j * kSlice + c0 + c], acc[c]));
+      }
+#pragma unroll
+      for (int c = 0; c < kMaxCols; ++c)
+        if (c < per) dS[i * kSlice + c0 + c] = acc[c];
+    }
   }
+  __syncthreads();
   if (p.d_h0)
     for (int e = tid; e < dk * kSlice; e += blockDim.x)
       p.d_h0[((static_cast<size_t>(bb) * p.H + h) * dk + e / kSlice) * dv + col0 + e % kSlice] = dS[e];
@@ -311,6 +627,7 @@ __global__ void __launch_bounds__(kBwdThreads) bwd_chunk_grad(const BwdPtrs p) {
   const bool CH = p.flags & 1u, ER = p.flags & 2u, WR = p.flags & 4u, QM = p.flags & 8u;
   const float* r = p.rec + static_cast<size_t>(cid) * R.size();
   float* s = p.scr + static_cast<size_t>(cid) * Q.size();
+  extern __shared__ float sg[];
   const float* S = p.S + static_cast<size_t>(cid) * dk * dv;
   const float* dSn = p.dS + static_cast<size_t>(cid) * dk * dv;
   const float* W = p.W + static_cast<size_t>(cid) * kC * dv;
@@ -318,129 +635,201 @@ __global__ void __launch_bounds__(kBwdThreads) bwd_chunk_grad(const BwdPtrs p) {
   const T* dOg = static_cast<const T*>(p.dO);
   auto tok = [&](int i) { return (static_cast<size_t>(bb) * p.T + t0 + i) * p.H + h; };
   float* dO = s + Q.oDO();
-  for (int e = tid; e < kC * dv; e += blockDim.x) {
-    const int i = e / dv, c = e % dv;
-    dO[e] = i < Lr ? ldx(dOg, tok(i) * dv + c) : 0.f;
+  const int bd = blockDim.x, warp = tid >> 5, lane = tid & 31, nw = bd >> 5;
+  for (int e0 = tid; e0 < kC * dv; e0 += kU * bd) {
+    float x[kU];
+#pragma unroll
+    for (int u = 0; u < kU; ++u) {
+      const int e = e0 + u * bd, i = e / dv;
+      x[u] = (e < kC * dv && i < Lr) ? ldx(dOg, tok(i) * dv + e % dv) : 0.f;
+    }
+#pragma unroll
+    for (int u = 0; u < kU; ++u)
+      if (e0 + u * bd < kC * dv) dO[e0 + u * bd] = x[u];
   }
-  // dgamma_C = rowsum(dS' (.) S)
-  for (int c = tid; c < dk; c += blockDim.x) {
-    float acc = 0.f;
-    for (int j = 0; j < dv; ++j) acc = fmaf(dSn[c * dv + j], S[c * dv + j], acc);
-    s[Q.oDgC() + c] = acc;
+  // dgamma_C = rowsum(dS' (.) S): one warp per row, 16-byte loads; lane l keeps
+  // the sum of the warp's l-th row and stores it after the loop
+  {
+    float keep = 0.f;
+    for (int l = 0; warp + nw * l < dk; ++l) {
+      const int c = warp + nw * l;
+      float acc = 0.f;
+      for (int j = lane * 4; j < dv; j += 128) {
+        const float4 x = *reinterpret_cast<const float4*>(dSn + static_cast<size_t>(c) * dv + j);
+        const float4 y = *reinterpret_cast<const float4*>(S + static_cast<size_t>(c) * dv + j);
+        acc = fmaf(x.x, y.x, fmaf(x.y, y.y, fmaf(x.z, y.z, fmaf(x.w, y.w, acc))));
+      }
+      acc = warp_sum(acc);
+      if (lane == l) keep = acc;
+    }
+    if (warp + nw * lane < dk) s[Q.oDgC() + warp + nw * lane] = keep;
   }
   __syncthreads();
   // dA_qk = tril(dO W^T, 0); dQ_gamma = dO S^T + dA_qk K_bar; dK_bar = dA_qk^T Q_gamma
-  block_gemm(s + Q.oDAqk(), kC, dO, dv, 1, W, 1, dv, kC, kC, dv, 1.f, 0.f, 1);
-  block_gemm(s + Q.oDQg(), dk, dO, dv, 1, S, 1, dv, kC, dk, dv, 1.f, 0.f);
-  block_gemm(s + Q.oDQg(), dk, s + Q.oDAqk(), kC, 1, r + R.oKb(), dk, 1, kC, dk, kC, 1.f, 1.f);
-  block_gemm(s + Q.oDKb(), dk, s + Q.oDAqk(), 1, kC, r + R.oQg(), dk, 1, kC, dk, kC, 1.f, 0.f);
+  gemm64(s + Q.oDAqk(), kC, dO, dv, 1, W, 1, dv, kC, dv, 1.f, 0.f, sg, 1);
+  gemm64(s + Q.oDQg(), dk, dO, dv, 1, S, 1, dv, dk, dv, 1.f, 0.f, sg);
+  gemm64(s + Q.oDQg(), dk, s + Q.oDAqk(), kC, 1, r + R.oKb(), dk, 1, dk, kC, 1.f, 1.f, sg);
+  gemm64(s + Q.oDKb(), dk, s + Q.oDAqk(), 1, kC, r + R.oQg(), dk, 1, dk, kC, 1.f, 0.f, sg);
   // dK_tail = W dS'^T; dY = -dW S^T
-  block_gemm(s + Q.oDKt(), dk, W, dv, 1, dSn, 1, dv, kC, dk, dv, 1.f, 0.f);
-  block_gemm(s + Q.oDY(), dk, dW, dv, 1, S, 1, dv, kC, dk, dv, -1.f, 0.f);
+  gemm64(s + Q.oDKt(), dk, W, dv, 1, dSn, 1, dv, dk, dv, 1.f, 0.f, sg);
+  gemm64(s + Q.oDY(), dk, dW, dv, 1, S, 1, dv, dk, dv, -1.f, 0.f, sg);
   // the notes' gate-aware dA = dU Z^T + dY E_bar^T (dU = dW)
-  block_gemm(s + Q.oDA(), kC, dW, dv, 1, r + R.oZ(), 1, dv, kC, kC, dv, 1.f, 0.f);
-  block_gemm(s + Q.oDA(), kC, s + Q.oDY(), dk, 1, r + R.oEb(), 1, dk, kC, kC, dk, 1.f, 1.f);
+  gemm64(s + Q.oDA(), kC, dW, dv, 1, r + R.oZ(), 1, dv, kC, dv, 1.f, 0.f, sg);
+  gemm64(s + Q.oDA(), kC, s + Q.oDY(), dk, 1, r + R.oEb(), 1, dk, kC, dk, 1.f, 1.f, sg);
   // dZ = A^T dU; dE_bar = A^T dY
-  block_gemm(s + Q.oDZ(), dv, r + R.oA(), 1, kC, dW, dv, 1, kC, dv, kC, 1.f, 0.f);
-  block_gemm(s + Q.oDEb(), dk, r + R.oA(), 1, kC, s + Q.oDY(), dk, 1, kC, dk, kC, 1.f, 0.f);
+  gemm64(s + Q.oDZ(), dv, r + R.oA(), 1, kC, dW, dv, 1, dv, kC, 1.f, 0.f, sg);
+  gemm64(s + Q.oDEb(), dk, r + R.oA(), 1, kC, s + Q.oDY(), dk, 1, dk, kC, 1.f, 0.f, sg);
   // the notes' adjoint of the inverse: dT = -tril(A^T dA A^T, -1)
-  block_gemm(s + Q.oX(), kC, r + R.oA(), 1, kC, s + Q.oDA(), kC, 1, kC, kC, kC, 1.f, 0.f);
-  block_gemm(s + Q.oDT(), kC, s + Q.oX(), kC, 1, r + R.oA(), 1, kC, kC, kC, kC, -1.f, 0.f, 2);
+  gemm64(s + Q.oX(), kC, r + R.oA(), 1, kC, s + Q.oDA(), kC, 1, kC, kC, 1.f, 0.f, sg);
+  gemm64(s + Q.oDT(), kC, s + Q.oX(), kC, 1, r + R.oA(), 1, kC, kC, kC, -1.f, 0.f, sg, 2);
   // dE_bar += dT K_bar; dK_bar += dT^T E_bar
-  block_gemm(s + Q.oDEb(), dk, s + Q.oDT(), kC, 1, r + R.oKb(), dk, 1, kC, dk, kC, 1.f, 1.f);
-  block_gemm(s + Q.oDKb(), dk, s + Q.oDT(), 1, kC, r + R.oEb(), dk, 1, kC, dk, kC, 1.f, 1.f);
-  // the decay factors: dG = gamma dgamma (+ gamma_C dgamma_C on the last row), with
-  // dgamma = dE_bar E - dK_bar K_bar / gamma - dK_tail K_tail / gamma + dQ_gamma Q_gamma / gamma
-  // and dgamma_C += sum_r dK_tail k / gamma; dq, dk, dE per element
-  for (int c = tid; c < dk; c += blockDim.x) {
-    float dgc = s[Q.oDgC() + c];
-    const float gC = r[R.oGam() + (kC - 1) * dk + c];
-    for (int i = 0; i < kC; ++i) {
-      const size_t e = static_cast<size_t>(i) * dk + c;
-      const float gam = r[R.oGam() + e];
-      const float kv = r[R.oKb() + e] * gam;     // k = K_bar gamma
-      dgc = fmaf(s[Q.oDKt() + e], kv / gam, dgc);
-      const float dgam = s[Q.oDEb() + e] * r[R.oE() + e] - s[Q.oDKb() + e] * r[R.oKb() + e] / gam -
-                         s[Q.oDKt() + e] * r[R.oKt() + e] / gam + s[Q.oDQg() + e] * r[R.oQg() + e] / gam;
-      s[Q.oDG() + e] = gam * dgam;
+  gemm64(s + Q.oDEb(), dk, s + Q.oDT(), kC, 1, r + R.oKb(), dk, 1, dk, kC, 1.f, 1.f, sg);
+  gemm64(s + Q.oDKb(), dk, s + Q.oDT(), 1, kC, r + R.oEb(), dk, 1, dk, kC, 1.f, 1.f, sg);
+  // the decay factors: dG = gamma dgamma with
+  //   dgamma = dE_bar E - dK_bar K_bar / gamma - dK_tail K_tail / gamma + dQ_gamma Q_gamma / gamma,
+  // dgamma_C += sum_r dK_tail k / gamma (= dK_tail K_bar), and dG of the last row
+  // gains gamma_C dgamma_C; dg is the reverse cumulative sum of dG within the
+  // chunk. Thread (channel c, part) owns rows [part RPT, part RPT + RPT) of
+  // channel c: pass A forms dG in shared memory with per-part column sums and
+  // writes dq, dk, db; pass B adds the later parts and gamma_C dgamma_C and runs
+  // the cumulative sum up its rows.
+  float* sDG = sg;                 // [64][dk]
+  float* sP = sDG + kC * dk;       // [parts][dk] column sums of dG
+  float* sQ = sP + 4 * dk;         // [parts][dk] column sums of dK_tail K_bar
+  const int parts = bd / dk, RPT = kC / parts;
+  const int c = tid % dk, part = tid / dk, i0 = part * RPT;
+  const float gC = r[R.oGam() + (kC - 1) * dk + c];
+  {
+    float psum = 0.f, pdgc = 0.f;
+    for (int ii = 0; ii < RPT; ii += kU) {
+      float gam[kU], kb[kU], E[kU], kt[kU], qg[kU], x[kU], deb[kU], dkb[kU], dkt[kU], dqg[kU];
+      float bv[kU], rb[kU], rl[kU];
+#pragma unroll
+      for (int u = 0; u < kU; ++u) {
+        const int i = i0 + ii + u;
+        const size_t e = static_cast<size_t>(i) * dk + c;
+        gam[u] = r[R.oGam() + e];
+        kb[u] = r[R.oKb() + e];
+        E[u] = r[R.oE() + e];
+        kt[u] = r[R.oKt() + e];
+        qg[u] = r[R.oQg() + e];
+        x[u] = r[R.oX() + e];
+        deb[u] = s[Q.oDEb() + e];
+        dkb[u] = s[Q.oDKb() + e];
+        dkt[u] = s[Q.oDKt() + e];
+        dqg[u] = s[Q.oDQg() + e];
+        const bool ok = i < Lr;
+        bv[u] = ok && ER ? ldx(static_cast<const T*>(p.b), tok(i) * dk + c) : 0.f;
+        rb[u] = ok && !ER ? p.beta[tok(i)] : 0.f;
+        rl[u] = ok && QM ? p.lam[tok(i)] : 0.f;
+      }
+#pragma unroll
+      for (int u = 0; u < kU; ++u) {
+        const int i = i0 + ii + u;
+        const float dgam = deb[u] * E[u] - dkb[u] * kb[u] / gam[u] - dkt[u] * kt[u] / gam[u] +
+                           dqg[u] * qg[u] / gam[u];
+        const float dG = gam[u] * dgam;
+        sDG[i * dk + c] = dG;
+        psum += dG;
+        pdgc = fmaf(dkt[u], kb[u], pdgc);
+        if (i < Lr) {
+          const float dE = gam[u] * deb[u];
+          const float dx = ER ? bv[u] * dE : rb[u] * dE;
+          p.d_k[tok(i) * dk + c] = dkb[u] / gam[u] + gC / gam[u] * dkt[u] + dx;
+          p.d_q[tok(i) * dk + c] = p.scale * gam[u] * dqg[u] + (QM ? rl[u] * dx : 0.f);
+          if (ER) p.d_b[tok(i) * dk + c] = x[u] * dE;
+        }
+      }
     }
-    s[Q.oDG() + (kC - 1) * dk + c] += gC * dgc;
-    // reverse cumulative sum within the chunk: dg_i = sum_{r >= i} dG_r
-    float acc = 0.f;
-    for (int i = kC - 1; i >= 0; --i) {
-      acc += s[Q.oDG() + static_cast<size_t>(i) * dk + c];
-      s[Q.oDG() + static_cast<size_t>(i) * dk + c] = acc;
+    sP[part * dk + c] = psum;
+    sQ[part * dk + c] = pdgc;
+  }
+  __syncthreads();
+  {
+    float dgc = s[Q.oDgC() + c];
+    for (int q2 = 0; q2 < parts; ++q2) dgc += sQ[q2 * dk + c];
+    float acc = gC * dgc;
+    for (int q2 = part + 1; q2 < parts; ++q2) acc += sP[q2 * dk + c];
+    for (int i = i0 + RPT - 1; i >= i0; --i) {
+      acc += sDG[i * dk + c];
+      sDG[i * dk + c] = acc;
+      if (CH && i < Lr) p.d_g[tok(i) * dk + c] = acc;
+    }
+  }
+  // value-side outputs per (row, channel)
+  for (int e0 = tid; e0 < kC * dv; e0 += kU * bd) {
+    float dZ[kU], vv[kU], sc[kU];
+#pragma unroll
+    for (int u = 0; u < kU; ++u) {
+      const int e = e0 + u * bd, i = e / dv;
+      const bool ok = e < kC * dv && i < Lr;
+      dZ[u] = ok ? s[Q.oDZ() + e] : 0.f;
+      vv[u] = ok ? ldx(static_cast<const T*>(p.v), tok(i) * dv + e % dv) : 0.f;
+      sc[u] = !ok ? 0.f : WR ? ldx(static_cast<const T*>(p.w), tok(i) * dv + e % dv) : p.beta[tok(i)];
+    }
+#pragma unroll
+    for (int u = 0; u < kU; ++u) {
+      const int e = e0 + u * bd, i = e / dv;
+      if (e >= kC * dv || i >= Lr) continue;
+      p.d_v[tok(i) * dv + e % dv] = sc[u] * dZ[u];
+      if (WR) p.d_w[tok(i) * dv + e % dv] = vv[u] * dZ[u];
     }
   }
   __syncthreads();
-  // key-side outputs per (row, channel)
-  for (int e = tid; e < kC * dk; e += blockDim.x) {
-    const int i = e / dk, c = e % dk;
-    if (i >= Lr) continue;
-    const float gam = r[R.oGam() + e], gC = r[R.oGam() + (kC - 1) * dk + c];
-    const float dE = gam * s[Q.oDEb() + e];
-    const float x = r[R.oX() + e];
-    const float bta = p.beta ? p.beta[tok(i)] : 0.f;
-    const float dx = ER ? ldx(static_cast<const T*>(p.b), tok(i) * dk + c) * dE : bta * dE;
-    float dkv = s[Q.oDKb() + e] / gam + gC / gam * s[Q.oDKt() + e] + dx;
-    float dqv = p.scale * gam * s[Q.oDQg() + e];
-    if (QM) dqv += p.lam[tok(i)] * dx;
-    p.d_k[tok(i) * dk + c] = dkv;
-    p.d_q[tok(i) * dk + c] = dqv;
-    if (ER) p.d_b[tok(i) * dk + c] = x * dE;
-    if (CH) p.d_g[tok(i) * dk + c] = s[Q.oDG() + e];
-  }
-  // value-side outputs
-  for (int e = tid; e < kC * dv; e += blockDim.x) {
-    const int i = e / dv, c = e % dv;
-    if (i >= Lr) continue;
-    const float dZ = s[Q.oDZ() + e];
-    const float vv = ldx(static_cast<const T*>(p.v), tok(i) * dv + c);
-    if (WR) {
-      p.d_v[tok(i) * dv + c] = ldx(static_cast<const T*>(p.w), tok(i) * dv + c) * dZ;
-      p.d_w[tok(i) * dv + c] = vv * dZ;
-    } else {
-      p.d_v[tok(i) * dv + c] = p.beta[tok(i)] * dZ;
-    }
-  }
-  // per-row outputs: scalar dg, dbeta, dlam
-  if (tid < kC && tid < Lr) {
-    const int i = tid;
+  // per-row outputs: scalar dg (sum of dg over the channels), dbeta, dlam; one
+  // warp per row, the channels over the lanes
+  for (int i = warp; i < Lr; i += nw) {
     float dgs = 0.f, dbe = 0.f, dla = 0.f;
-    for (int c = 0; c < dk; ++c) {
-      const size_t e = static_cast<size_t>(i) * dk + c;
-      dgs += s[Q.oDG() + e];
+    const float bt = p.beta ? p.beta[tok(i)] : 0.f;
+    for (int c2 = lane; c2 < dk; c2 += 32) {
+      const size_t e = static_cast<size_t>(i) * dk + c2;
+      dgs += sDG[e];
       const float dE = r[R.oGam() + e] * s[Q.oDEb() + e];
       if (!ER) dbe = fmaf(r[R.oX() + e], dE, dbe);
       if (QM) {
-        const float dx = ER ? ldx(static_cast<const T*>(p.b), tok(i) * dk + c) * dE
-                            : p.beta[tok(i)] * dE;
-        dla = fmaf(ldx(static_cast<const T*>(p.q), tok(i) * dk + c), dx, dla);
+        const float dx = ER ? ldx(static_cast<const T*>(p.b), tok(i) * dk + c2) * dE : bt * dE;
+        dla = fmaf(ldx(static_cast<const T*>(p.q), tok(i) * dk + c2), dx, dla);
       }
     }
     if (!WR)
-      for (int c = 0; c < dv; ++c)
-        dbe = fmaf(ldx(static_cast<const T*>(p.v), tok(i) * dv + c), s[Q.oDZ() + static_cast<size_t>(i) * dv + c], dbe);
-    if (!CH) p.d_g[tok(i)] = dgs;
-    if (p.d_beta) p.d_beta[tok(i)] = dbe;
-    if (QM) p.d_lam[tok(i)] = dla;
+      for (int c2 = lane; c2 < dv; c2 += 32)
+        dbe = fmaf(ldx(static_cast<const T*>(p.v), tok(i) * dv + c2),
+                   s[Q.oDZ() + static_cast<size_t>(i) * dv + c2], dbe);
+    dgs = warp_sum(dgs);
+    dbe = warp_sum(dbe);
+    dla = warp_sum(dla);
+    if (lane == 0) {
+      if (!CH) p.d_g[tok(i)] = dgs;
+      if (p.d_beta) p.d_beta[tok(i)] = dbe;
+      if (QM) p.d_lam[tok(i)] = dla;
+    }
   }
 }
 
 template <typename T>
 cudaError_t launch_all(const BwdPtrs& p, cudaStream_t stream) {
   const int chunks = p.B * p.H * p.Nc;
-  bwd_chunk_prep<T><<<chunks, kBwdThreads, 0, stream>>>(p);
-  cudaError_t err = cudaGetLastError();
-  if (err != cudaSuccess) return err;
+  cudaError_t err;
+  if ((err = cudaFuncSetAttribute(bwd_chunk_prep<T>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                  static_cast<int>(kGemmSmem))) != cudaSuccess ||
+      (err = cudaFuncSetAttribute(bwd_chunk_grad<T>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                  static_cast<int>(kGemmSmem))) != cudaSuccess)
+    return err;
+  bwd_chunk_prep<T><<<chunks, kBwdThreads, kGemmSmem, stream>>>(p);
+  if ((err = cudaGetLastError()) != cudaSuccess) return err;
   const dim3 sgrid(p.dv / kSlice, p.H, p.B);
-  const size_t sm2 = (static_cast<size_t>(p.dk) + kC) * kSlice * sizeof(float);
-  bwd_state_pass<<<sgrid, kBwdThreads, sm2, stream>>>(p);
+  const size_t sm2 = state_pass_floats(p.dk) * sizeof(float);
+  const size_t sm3 = dstate_pass_floats(p.dk) * sizeof(float);
+  if ((err = cudaFuncSetAttribute(bwd_state_pass, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                  static_cast<int>(sm2))) != cudaSuccess ||
+      (err = cudaFuncSetAttribute(bwd_dstate_pass<T>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                  static_cast<int>(sm3))) != cudaSuccess)
+    return err;
+  bwd_state_pass<<<sgrid, kPassThreads, sm2, stream>>>(p);
   if ((err = cudaGetLastError()) != cudaSuccess) return err;
-  const size_t sm3 = (static_cast<size_t>(p.dk) + 2 * kC) * kSlice * sizeof(float);
-  bwd_dstate_pass<T><<<sgrid, kBwdThreads, sm3, stream>>>(p);
+  bwd_dstate_pass<T><<<sgrid, kPassThreads, sm3, stream>>>(p);
   if ((err = cudaGetLastError()) != cudaSuccess) return err;
-  bwd_chunk_grad<T><<<chunks, kBwdThreads, 0, stream>>>(p);
+  bwd_chunk_grad<T><<<chunks, kBwdThreads, kGemmSmem, stream>>>(p);
   return cudaGetLastError();
 }
 
