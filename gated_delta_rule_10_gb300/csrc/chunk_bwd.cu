@@ -415,184 +415,446 @@ __global__ void __launch_bounds__(kBwdThreads) bwd_chunk_prep(const BwdPtrs p) {
 }
 
 // ------------------------------------------------------- 2. forward states
-constexpr int kSlice = 64;          // value columns per state-pass CTA
-constexpr int kPassThreads = 512;
+// Warp-level MMA on bf16 operands (m16n8k16, fp32 accumulation). An fp32
+// operand x is split into bf16 hi = rn(x) and lo = rn(x - hi); with NP = 3 the
+// three products lo*hi + hi*lo + hi*hi are accumulated, which leaves a relative
+// error of about 2^-17 per term (the dropped lo*lo is below it); NP = 1 keeps
+// hi*hi only. Operands are fp32 (or the input type) in shared memory, split as
+// the fragments are loaded.
+__device__ __forceinline__ uint32_t pack_bf16(float lo_idx, float hi_idx) {
+  uint32_t r;
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;\n" : "=r"(r) : "f"(hi_idx), "f"(lo_idx));
+  return r;
+}
+template <int NP>
+__device__ __forceinline__ void split_pair(float x0, float x1, uint32_t& hi, uint32_t& lo) {
+  hi = pack_bf16(x0, x1);
+  if (NP == 3)
+    lo = pack_bf16(x0 - __uint_as_float(hi << 16), x1 - __uint_as_float(hi & 0xffff0000u));
+}
+__device__ __forceinline__ void mma_bf16(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
+                                         uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, "
+      "{%8, %9}, {%0, %1, %2, %3};\n"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+template <int NP>
+struct FragA {
+  uint32_t h[4], l[4];
+  __device__ __forceinline__ void negate() {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      h[i] ^= 0x80008000u;
+      if (NP == 3) l[i] ^= 0x80008000u;
+    }
+  }
+};
+template <int NP>
+struct FragB {
+  uint32_t h[2], l[2];
+};
+__device__ __forceinline__ float ldf(const float* p) { return *p; }
+__device__ __forceinline__ float ldf(const __nv_bfloat16* p) { return __bfloat162float(*p); }
 
-// Each chunk's operands are staged in shared memory (coalesced copies from the
-// records), then every product reads shared memory only.
-__host__ __device__ constexpr size_t state_pass_floats(int dk) {
-  return static_cast<size_t>(dk) * kSlice + kC * kSlice + kC * (dk + 4) + kC * dk +
-         kC * kSlice + dk;
+// A fragment (16 x 16 at rows m0, columns k0) of a(m, k) = X[m ld + k] (KC) or
+// X[k ld + m] (!KC). Conflict-free shared-memory reads need ld = 8 (mod 32)
+// for KC and ld = 4 (mod 32) otherwise.
+template <bool KC, int NP>
+__device__ __forceinline__ void load_a(FragA<NP>& f, const float* X, int ld, int m0, int k0) {
+  const int lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
+  const int r0 = m0 + g, c0 = k0 + 2 * t;
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    const int r = r0 + (q & 1) * 8, c = c0 + (q >> 1) * 8;
+    float x0, x1;
+    if (KC) {
+      const float2 v = *reinterpret_cast<const float2*>(X + r * ld + c);
+      x0 = v.x;
+      x1 = v.y;
+    } else {
+      x0 = X[c * ld + r];
+      x1 = X[(c + 1) * ld + r];
+    }
+    split_pair<NP>(x0, x1, f.h[q], f.l[q]);
+  }
+}
+// B fragment (16 x 8 at rows k0, columns n0) of b(k, n) = X[n ld + k] (KC) or
+// X[k ld + n] (!KC); same padding rule as load_a.
+template <bool KC, int NP, typename T>
+__device__ __forceinline__ void load_b(FragB<NP>& f, const T* X, int ld, int k0, int n0) {
+  const int lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
+  const int n = n0 + g, k = k0 + 2 * t;
+#pragma unroll
+  for (int q = 0; q < 2; ++q) {
+    const int kk = k + q * 8;
+    float x0, x1;
+    if (KC) {
+      x0 = ldf(X + n * ld + kk);
+      x1 = ldf(X + n * ld + kk + 1);
+    } else {
+      x0 = ldf(X + kk * ld + n);
+      x1 = ldf(X + (kk + 1) * ld + n);
+    }
+    split_pair<NP>(x0, x1, f.h[q], f.l[q]);
+  }
+}
+template <int NP>
+__device__ __forceinline__ void mma_split(float (&d)[4], const FragA<NP>& a, const FragB<NP>& b) {
+  if (NP == 3) {
+    mma_bf16(d, a.l, b.h[0], b.h[1]);
+    mma_bf16(d, a.h, b.l[0], b.l[1]);
+  }
+  mma_bf16(d, a.h, b.h[0], b.h[1]);
 }
 
-__global__ void __launch_bounds__(kPassThreads) bwd_state_pass(const BwdPtrs p) {
-  const Rec R{p.dk, p.dv};
+// 16-byte asynchronous copy that reads src_bytes (0 or 16) and zero-fills the rest
+__device__ __forceinline__ void cp16z(void* smem, const void* gmem, int src_bytes) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(sa32(smem)), "l"(gmem),
+               "r"(src_bytes)
+               : "memory");
+}
+
+constexpr int kSlice = 64;          // value columns per state-pass CTA
+constexpr int kPassThreads = 256;   // 8 warps
+constexpr int kLS = kSlice + 4;     // row pitch of the state / W tiles (floats)
+
+// The accumulator tile of a warp in a [rows x 64] product with 8 warps:
+// rows 16 mt.., n-tiles nt0 .. nt0 + NT - 1 (NT = rows / 16 of 8-column tiles).
+template <int ROWS>
+struct WarpTile {
+  static constexpr int NT = ROWS / 16;            // n-tiles per warp
+  static constexpr int WPM = 8 / (ROWS / 16);     // warps per 16-row tile
+  int mt, nt0;
+  __device__ WarpTile(int warp) : mt(warp / WPM), nt0((warp % WPM) * NT) {}
+};
+
+// Forward state pass. One CTA per (batch, head, 64 value columns), chunks in
+// order: W_n = U_n - Y_n S_n, S_{n+1} = Diag(gamma_C) S_n + K_tail^T W_n, S_n
+// and W_n written out for the gradient kernel. S_n lives in the warps'
+// accumulators (and as the MMA operand in shared memory); the next chunk's
+// Y, U, K_tail and gamma_C are copied in while the current one is used.
+template <int DK>
+struct StatePassSmem {
+  static constexpr int LY = DK + 8, LU = kSlice, LKT = DK + 4;
+  static constexpr int STAGE = kC * LY + kC * LU + kC * LKT + DK;
+  static constexpr size_t floats = 2 * STAGE + DK * kLS + kC * kLS;
+};
+
+template <int DK, int NP>
+__global__ void __launch_bounds__(kPassThreads, 1) bwd_state_pass(const BwdPtrs p) {
+  using L = StatePassSmem<DK>;
+  const Rec R{DK, p.dv};
   const int col0 = blockIdx.x * kSlice, h = blockIdx.y, bb = blockIdx.z;
-  const int dk = p.dk, dv = p.dv, tid = threadIdx.x;
-  extern __shared__ float sm[];
-  float* S = sm;                       // [dk][kSlice]
-  float* Wl = S + dk * kSlice;         // [64][kSlice]
-  float* Ys = Wl + kC * kSlice;        // [64][dk + 4]
-  float* Kts = Ys + kC * (dk + 4);     // [64][dk]
-  float* Us = Kts + kC * dk;           // [64][kSlice]
-  float* gC = Us + kC * kSlice;        // [dk]
-  for (int e = tid; e < dk * kSlice; e += blockDim.x) {
-    const int i = e / kSlice, c = e % kSlice;
-    S[e] = p.h0 ? p.h0[((static_cast<size_t>(bb) * p.H + h) * dk + i) * dv + col0 + c] : 0.f;
-  }
+  const int dv = p.dv, tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int g = lane >> 2, t = lane & 3;
+  extern __shared__ __align__(16) float sm[];
+  float* S = sm + 2 * L::STAGE;        // [DK][kLS]
+  float* Wl = S + DK * kLS;            // [64][kLS]
+  auto stage = [&](int n) {
+    float* st = sm + (n & 1) * L::STAGE;
+    float* Ys = st;
+    float* Us = Ys + kC * L::LY;
+    float* Kts = Us + kC * L::LU;
+    float* gC = Kts + kC * L::LKT;
+    const float* r = p.rec + chunk_id(p, bb, h, n) * R.size();
+    for (int e = tid * 4; e < kC * DK; e += kPassThreads * 4) {
+      const int i = e / DK, c = e % DK;
+      cp16(Ys + i * L::LY + c, r + R.oY() + e);
+      cp16(Kts + i * L::LKT + c, r + R.oKt() + e);
+    }
+    for (int e = tid * 4; e < kC * kSlice; e += kPassThreads * 4) {
+      const int i = e / kSlice, c = e % kSlice;
+      cp16(Us + i * L::LU + c, r + R.oU() + static_cast<size_t>(i) * dv + col0 + c);
+    }
+    for (int e = tid * 4; e < DK; e += kPassThreads * 4) cp16(gC + e, r + R.oGam() + (kC - 1) * DK + e);
+    cp_commit();
+  };
+  // S accumulators: rows 16 ts.mt + g (+ 8), columns 8 (ts.nt0 + j) + 2 t (+ 1)
+  const WarpTile<DK> ts(warp);
+  float acc[WarpTile<DK>::NT][4];
+  const size_t bh = static_cast<size_t>(bb) * p.H + h;
+#pragma unroll
+  for (int j = 0; j < WarpTile<DK>::NT; ++j)
+#pragma unroll
+    for (int hf = 0; hf < 2; ++hf) {
+      const int r = 16 * ts.mt + g + 8 * hf, c = 8 * (ts.nt0 + j) + 2 * t;
+      float2 v = make_float2(0.f, 0.f);
+      if (p.h0) v = *reinterpret_cast<const float2*>(p.h0 + (bh * DK + r) * dv + col0 + c);
+      acc[j][2 * hf] = v.x;
+      acc[j][2 * hf + 1] = v.y;
+      *reinterpret_cast<float2*>(S + r * kLS + c) = v;
+    }
+  stage(0);
   for (int n = 0; n < p.Nc; ++n) {
     const size_t cid = chunk_id(p, bb, h, n);
-    const float* r = p.rec + cid * R.size();
-    float* Sg = p.S + cid * dk * dv;
-    float* Wg = p.W + cid * kC * dv;
-    __syncthreads();   // S of the previous chunk is complete
-    for (int e = tid; e < dk * kSlice; e += blockDim.x)
-      Sg[(e / kSlice) * dv + col0 + e % kSlice] = S[e];
-    for (int e = tid * 4; e < kC * dk; e += blockDim.x * 4) {
-      cp16(Ys + (e / dk) * (dk + 4) + e % dk, r + R.oY() + e);
-      cp16(Kts + e, r + R.oKt() + e);
-    }
-    for (int e = tid * 4; e < kC * kSlice; e += blockDim.x * 4)
-      cp16(Us + e, r + R.oU() + (e / kSlice) * dv + col0 + e % kSlice);
-    for (int i = tid * 4; i < dk; i += blockDim.x * 4) cp16(gC + i, r + R.oGam() + (kC - 1) * dk + i);
-    cp_commit();
-    cp_wait<0>();
-    __syncthreads();
-    // W = U - Y S: thread -> (row i, 8 columns)
+    float* Sg = p.S + cid * DK * dv;
+#pragma unroll
+    for (int j = 0; j < WarpTile<DK>::NT; ++j)
+#pragma unroll
+      for (int hf = 0; hf < 2; ++hf) {
+        const int r = 16 * ts.mt + g + 8 * hf, c = 8 * (ts.nt0 + j) + 2 * t;
+        *reinterpret_cast<float2*>(Sg + static_cast<size_t>(r) * dv + col0 + c) =
+            make_float2(acc[j][2 * hf], acc[j][2 * hf + 1]);
+      }
+    if (n + 1 < p.Nc) stage(n + 1);
+    else cp_commit();
+    cp_wait<1>();
+    __syncthreads();   // chunk n's operands landed; S_n complete in shared memory
+    const float* st = sm + (n & 1) * L::STAGE;
+    const float* Ys = st;
+    const float* Us = Ys + kC * L::LY;
+    const float* Kts = Us + kC * L::LU;
+    const float* gC = Kts + kC * L::LKT;
+    // W = U - Y S: warp -> rows 16 (warp & 3), n-tiles 4 (warp >> 2) .. + 3
     {
-      const int i = tid / (kSlice / 8), c0 = (tid % (kSlice / 8)) * 8;
-      float acc[8];
+      const int mt = warp & 3, nt0 = (warp >> 2) * 4;
+      float w[4][4];
 #pragma unroll
-      for (int c = 0; c < 8; ++c) acc[c] = Us[i * kSlice + c0 + c];
-      for (int j = 0; j < dk; ++j) {
-        const float y = Ys[i * (dk + 4) + j];
+      for (int j = 0; j < 4; ++j)
 #pragma unroll
-        for (int c = 0; c < 8; ++c) acc[c] = fmaf(-y, S[j * kSlice + c0 + c], acc[c]);
+        for (int e = 0; e < 4; ++e)
+          w[j][e] = Us[(16 * mt + g + 8 * (e >> 1)) * L::LU + 8 * (nt0 + j) + 2 * t + (e & 1)];
+#pragma unroll 2
+      for (int ks = 0; ks < DK / 16; ++ks) {
+        FragA<NP> a;
+        load_a<true, NP>(a, Ys, L::LY, 16 * mt, 16 * ks);
+        a.negate();
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          FragB<NP> b;
+          load_b<false, NP>(b, S, kLS, 16 * ks, 8 * (nt0 + j));
+          mma_split<NP>(w[j], a, b);
+        }
       }
+      float* Wg = p.W + cid * kC * dv;
 #pragma unroll
-      for (int c = 0; c < 8; ++c) {
-        Wl[i * kSlice + c0 + c] = acc[c];
-        Wg[i * dv + col0 + c0 + c] = acc[c];
-      }
+      for (int j = 0; j < 4; ++j)
+#pragma unroll
+        for (int hf = 0; hf < 2; ++hf) {
+          const int r = 16 * mt + g + 8 * hf, c = 8 * (nt0 + j) + 2 * t;
+          const float2 v = make_float2(w[j][2 * hf], w[j][2 * hf + 1]);
+          *reinterpret_cast<float2*>(Wl + r * kLS + c) = v;
+          *reinterpret_cast<float2*>(Wg + static_cast<size_t>(r) * dv + col0 + c) = v;
+        }
     }
-    __syncthreads();
-    // S' = Diag(gamma_C) S + K_tail^T W: thread -> (channel i, kSlice * dk / 512 columns)
+    __syncthreads();   // W complete; S no longer read
+    // S' = Diag(gamma_C) S + K_tail^T W
     {
-      constexpr int kMaxCols = 16;
-      const int per = dk * kSlice / kPassThreads;         // 16 (dk = 128) or 8 (dk = 64)
-      const int groups = kSlice / per;
-      const int i = tid / groups, c0 = (tid % groups) * per;
-      float acc[kMaxCols];
+      const float g0 = gC[16 * ts.mt + g], g1 = gC[16 * ts.mt + g + 8];
 #pragma unroll
-      for (int c = 0; c < kMaxCols; ++c) acc[c] = c < per ? gC[i] * S[i * kSlice + c0 + c] : 0.f;
-      for (int j = 0; j < kC; ++j) {
-        const float kt = Kts[j * dk + i];
-#pragma unroll
-        for (int c = 0; c < kMaxCols; ++c)
-          if (c < per) acc[c] = fmaf(kt, Wl[j * kSlice + c0 + c], acc[c]);
+      for (int j = 0; j < WarpTile<DK>::NT; ++j) {
+        acc[j][0] *= g0;
+        acc[j][1] *= g0;
+        acc[j][2] *= g1;
+        acc[j][3] *= g1;
       }
 #pragma unroll
-      for (int c = 0; c < kMaxCols; ++c)
-        if (c < per) S[i * kSlice + c0 + c] = acc[c];   // this thread's own elements
+      for (int ks = 0; ks < kC / 16; ++ks) {
+        FragA<NP> a;
+        load_a<false, NP>(a, Kts, L::LKT, 16 * ts.mt, 16 * ks);
+#pragma unroll
+        for (int j = 0; j < WarpTile<DK>::NT; ++j) {
+          FragB<NP> b;
+          load_b<false, NP>(b, Wl, kLS, 16 * ks, 8 * (ts.nt0 + j));
+          mma_split<NP>(acc[j], a, b);
+        }
+      }
+#pragma unroll
+      for (int j = 0; j < WarpTile<DK>::NT; ++j)
+#pragma unroll
+        for (int hf = 0; hf < 2; ++hf) {
+          const int r = 16 * ts.mt + g + 8 * hf, c = 8 * (ts.nt0 + j) + 2 * t;
+          *reinterpret_cast<float2*>(S + r * kLS + c) = make_float2(acc[j][2 * hf], acc[j][2 * hf + 1]);
+        }
     }
+    __syncthreads();   // S_{n+1} complete; this stage's buffers free
   }
+  cp_wait<0>();
 }
 
 // ------------------------------------------------------- 3. reverse states
-__host__ __device__ constexpr size_t dstate_pass_floats(int dk) {
-  return static_cast<size_t>(dk) * kSlice + 2 * kC * kSlice + kC * kC + kC * (dk + 4) +
-         2 * kC * dk + dk;
-}
+// Reverse state pass, chunks in reverse order: dW_n = A_qk^T dO_n + K_tail
+// dS_{n+1}, dS_n = Diag(gamma_C) dS_{n+1} + Q_gamma^T dO_n - Y^T dW_n, with
+// dS_{n+1} and dW_n written out. dS lives in the accumulators. The operands of
+// the dW product (A_qk, K_tail, dO) and of the dS product (Q_gamma, Y,
+// gamma_C) are two copy groups: each is refilled for the previous chunk as
+// soon as its product is done, so it lands while the other product runs (dO,
+// read by both, is double-buffered).
+template <int DK, typename T>
+struct DStateSmem {
+  static constexpr int LAQ = kC + 4, LKT = DK + 8, LQ = DK + 4;
+  // dO rows: 68 floats or 72 bf16 (a row pitch of 4 banks mod 32 either way)
+  static constexpr int LO = sizeof(T) == 4 ? kSlice + 4 : kSlice + 8;
+  static constexpr size_t f_aq = 0, f_kt = f_aq + kC * LAQ, f_do = f_kt + kC * LKT;
+  static constexpr size_t do_floats = (static_cast<size_t>(kC) * LO * sizeof(T) + 15) / 16 * 4;
+  static constexpr size_t f_qg = f_do + 2 * do_floats, f_y = f_qg + kC * LQ, f_gc = f_y + kC * LQ;
+  static constexpr size_t f_ds = f_gc + DK, f_dw = f_ds + DK * kLS;
+  static constexpr size_t floats = f_dw + kC * kLS;
+};
 
-template <typename T>
-__global__ void __launch_bounds__(kPassThreads) bwd_dstate_pass(const BwdPtrs p) {
-  const Rec R{p.dk, p.dv};
+template <int DK, int NP, typename T>
+__global__ void __launch_bounds__(kPassThreads, 1) bwd_dstate_pass(const BwdPtrs p) {
+  using L = DStateSmem<DK, T>;
+  const Rec R{DK, p.dv};
   const int col0 = blockIdx.x * kSlice, h = blockIdx.y, bb = blockIdx.z;
-  const int dk = p.dk, dv = p.dv, tid = threadIdx.x;
+  const int dv = p.dv, tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int g = lane >> 2, t = lane & 3;
   const T* dO = static_cast<const T*>(p.dO);
-  extern __shared__ float sm[];
-  float* dS = sm;                      // [dk][kSlice]
-  float* dWl = dS + dk * kSlice;       // [64][kSlice]
-  float* dOl = dWl + kC * kSlice;      // [64][kSlice]
-  float* Aq = dOl + kC * kSlice;       // [64][64]
-  float* Kts = Aq + kC * kC;           // [64][dk + 4]
-  float* Qg = Kts + kC * (dk + 4);     // [64][dk]
-  float* Ys = Qg + kC * dk;            // [64][dk]
-  float* gC = Ys + kC * dk;            // [dk]
-  for (int e = tid; e < dk * kSlice; e += blockDim.x) {
-    const int i = e / kSlice, c = e % kSlice;
-    dS[e] = p.dhT ? p.dhT[((static_cast<size_t>(bb) * p.H + h) * dk + i) * dv + col0 + c] : 0.f;
-  }
+  extern __shared__ __align__(16) float sm[];
+  float* Aq = sm + L::f_aq;
+  float* Kt = sm + L::f_kt;
+  float* Qg = sm + L::f_qg;
+  float* Ys = sm + L::f_y;
+  float* gC = sm + L::f_gc;
+  float* dS = sm + L::f_ds;
+  float* dWl = sm + L::f_dw;
+  auto dO_buf = [&](int n) { return reinterpret_cast<T*>(sm + L::f_do + (n & 1) * L::do_floats); };
+  auto stage_a = [&](int n) {
+    const float* r = p.rec + chunk_id(p, bb, h, n) * R.size();
+    for (int e = tid * 4; e < kC * kC; e += kPassThreads * 4) cp16(Aq + (e / kC) * L::LAQ + e % kC, r + R.oAqk() + e);
+    for (int e = tid * 4; e < kC * DK; e += kPassThreads * 4) cp16(Kt + (e / DK) * L::LKT + e % DK, r + R.oKt() + e);
+    constexpr int V = 16 / sizeof(T);   // elements per 16-byte copy
+    T* ob = dO_buf(n);
+    const int t0 = n * kC, Lr = min(kC, p.T - t0);
+    for (int e = tid * V; e < kC * kSlice; e += kPassThreads * V) {
+      const int i = e / kSlice, c = e % kSlice;
+      const bool ok = i < Lr;
+      const size_t src = ((static_cast<size_t>(bb) * p.T + t0 + (ok ? i : 0)) * p.H + h) * dv + col0 + c;
+      cp16z(ob + i * L::LO + c, dO + src, ok ? 16 : 0);
+    }
+    cp_commit();
+  };
+  auto stage_b = [&](int n) {
+    const float* r = p.rec + chunk_id(p, bb, h, n) * R.size();
+    for (int e = tid * 4; e < kC * DK; e += kPassThreads * 4) {
+      const int i = e / DK, c = e % DK;
+      cp16(Qg + i * L::LQ + c, r + R.oQg() + e);
+      cp16(Ys + i * L::LQ + c, r + R.oY() + e);
+    }
+    for (int e = tid * 4; e < DK; e += kPassThreads * 4) cp16(gC + e, r + R.oGam() + (kC - 1) * DK + e);
+    cp_commit();
+  };
+  const WarpTile<DK> ts(warp);
+  float acc[WarpTile<DK>::NT][4];
+  const size_t bh = static_cast<size_t>(bb) * p.H + h;
+#pragma unroll
+  for (int j = 0; j < WarpTile<DK>::NT; ++j)
+#pragma unroll
+    for (int hf = 0; hf < 2; ++hf) {
+      const int r = 16 * ts.mt + g + 8 * hf, c = 8 * (ts.nt0 + j) + 2 * t;
+      float2 v = make_float2(0.f, 0.f);
+      if (p.dhT) v = *reinterpret_cast<const float2*>(p.dhT + (bh * DK + r) * dv + col0 + c);
+      acc[j][2 * hf] = v.x;
+      acc[j][2 * hf + 1] = v.y;
+      *reinterpret_cast<float2*>(dS + r * kLS + c) = v;
+    }
+  stage_a(p.Nc - 1);
+  stage_b(p.Nc - 1);
   for (int n = p.Nc - 1; n >= 0; --n) {
     const size_t cid = chunk_id(p, bb, h, n);
-    const float* r = p.rec + cid * R.size();
-    const int t0 = n * kC, Lr = min(kC, p.T - t0);
-    float* dSg = p.dS + cid * dk * dv;
-    float* dWg = p.dW + cid * kC * dv;
-    __syncthreads();   // dS of the later chunk is complete
-    for (int e = tid; e < dk * kSlice; e += blockDim.x)
-      dSg[(e / kSlice) * dv + col0 + e % kSlice] = dS[e];
-    for (int e = tid; e < kC * kSlice; e += blockDim.x) {
-      const int i = e / kSlice, c = e % kSlice;
-      dOl[e] = i < Lr ? ldx(dO, ((static_cast<size_t>(bb) * p.T + t0 + i) * p.H + h) * dv + col0 + c)
-                      : 0.f;
-    }
-    for (int e = tid * 4; e < kC * kC; e += blockDim.x * 4) cp16(Aq + e, r + R.oAqk() + e);
-    for (int e = tid * 4; e < kC * dk; e += blockDim.x * 4) {
-      cp16(Kts + (e / dk) * (dk + 4) + e % dk, r + R.oKt() + e);
-      cp16(Qg + e, r + R.oQg() + e);
-      cp16(Ys + e, r + R.oY() + e);
-    }
-    for (int i = tid * 4; i < dk; i += blockDim.x * 4) cp16(gC + i, r + R.oGam() + (kC - 1) * dk + i);
-    cp_commit();
-    cp_wait<0>();
-    __syncthreads();
-    // dW = A_qk^T dO + K_tail dS': thread -> (row i, 8 columns)
+    float* dSg = p.dS + cid * DK * dv;
+#pragma unroll
+    for (int j = 0; j < WarpTile<DK>::NT; ++j)
+#pragma unroll
+      for (int hf = 0; hf < 2; ++hf) {
+        const int r = 16 * ts.mt + g + 8 * hf, c = 8 * (ts.nt0 + j) + 2 * t;
+        *reinterpret_cast<float2*>(dSg + static_cast<size_t>(r) * dv + col0 + c) =
+            make_float2(acc[j][2 * hf], acc[j][2 * hf + 1]);
+      }
+    cp_wait<1>();
+    __syncthreads();   // A_qk, K_tail, dO of chunk n landed; dS_{n+1} complete
+    const T* ob = dO_buf(n);
+    // dW = A_qk^T dO + K_tail dS': warp -> rows 16 (warp & 3), n-tiles 4 (warp >> 2) .. + 3
     {
-      const int i = tid / (kSlice / 8), c0 = (tid % (kSlice / 8)) * 8;
-      float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-      for (int j = 0; j < kC; ++j) {
-        const float a = Aq[j * kC + i];
+      const int mt = warp & 3, nt0 = (warp >> 2) * 4;
+      float w[4][4] = {};
 #pragma unroll
-        for (int c = 0; c < 8; ++c) acc[c] = fmaf(a, dOl[j * kSlice + c0 + c], acc[c]);
-      }
-      for (int j = 0; j < dk; ++j) {
-        const float kt = Kts[i * (dk + 4) + j];
+      for (int ks = 0; ks < kC / 16; ++ks) {
+        FragA<NP> a;
+        load_a<false, NP>(a, Aq, L::LAQ, 16 * mt, 16 * ks);
 #pragma unroll
-        for (int c = 0; c < 8; ++c) acc[c] = fmaf(kt, dS[j * kSlice + c0 + c], acc[c]);
+        for (int j = 0; j < 4; ++j) {
+          FragB<NP> b;
+          load_b<false, NP>(b, ob, L::LO, 16 * ks, 8 * (nt0 + j));
+          mma_split<NP>(w[j], a, b);
+        }
       }
+#pragma unroll 2
+      for (int ks = 0; ks < DK / 16; ++ks) {
+        FragA<NP> a;
+        load_a<true, NP>(a, Kt, L::LKT, 16 * mt, 16 * ks);
 #pragma unroll
-      for (int c = 0; c < 8; ++c) {
-        dWl[i * kSlice + c0 + c] = acc[c];
-        dWg[i * dv + col0 + c0 + c] = acc[c];
+        for (int j = 0; j < 4; ++j) {
+          FragB<NP> b;
+          load_b<false, NP>(b, dS, kLS, 16 * ks, 8 * (nt0 + j));
+          mma_split<NP>(w[j], a, b);
+        }
       }
+      float* dWg = p.dW + cid * kC * dv;
+#pragma unroll
+      for (int j = 0; j < 4; ++j)
+#pragma unroll
+        for (int hf = 0; hf < 2; ++hf) {
+          const int r = 16 * mt + g + 8 * hf, c = 8 * (nt0 + j) + 2 * t;
+          const float2 v = make_float2(w[j][2 * hf], w[j][2 * hf + 1]);
+          *reinterpret_cast<float2*>(dWl + r * kLS + c) = v;
+          *reinterpret_cast<float2*>(dWg + static_cast<size_t>(r) * dv + col0 + c) = v;
+        }
     }
-    __syncthreads();
-    // dS = Diag(gamma_C) dS' + Q_gamma^T dO - Y^T dW: thread -> (channel i, columns)
+    __syncthreads();   // dW complete; A_qk, K_tail and dS' no longer read
+    if (n > 0) stage_a(n - 1);
+    else cp_commit();
+    cp_wait<1>();
+    __syncthreads();   // Q_gamma, Y, gamma_C of chunk n landed
+    // dS = Diag(gamma_C) dS' + Q_gamma^T dO - Y^T dW
     {
-      constexpr int kMaxCols = 16;
-      const int per = dk * kSlice / kPassThreads;
-      const int groups = kSlice / per;
-      const int i = tid / groups, c0 = (tid % groups) * per;
-      float acc[kMaxCols];
+      const float g0 = gC[16 * ts.mt + g], g1 = gC[16 * ts.mt + g + 8];
 #pragma unroll
-      for (int c = 0; c < kMaxCols; ++c) acc[c] = c < per ? gC[i] * dS[i * kSlice + c0 + c] : 0.f;
-      for (int j = 0; j < kC; ++j) {
-        const float qg = Qg[j * dk + i], y = Ys[j * dk + i];
-#pragma unroll
-        for (int c = 0; c < kMaxCols; ++c)
-          if (c < per)
-            acc[c] = fmaf(qg, dOl[j * kSlice + c0 + c], fmaf(-y, dWl[j * kSlice + c0 + c], acc[c]));
+      for (int j = 0; j < WarpTile<DK>::NT; ++j) {
+        acc[j][0] *= g0;
+        acc[j][1] *= g0;
+        acc[j][2] *= g1;
+        acc[j][3] *= g1;
       }
 #pragma unroll
-      for (int c = 0; c < kMaxCols; ++c)
-        if (c < per) dS[i * kSlice + c0 + c] = acc[c];
+      for (int ks = 0; ks < kC / 16; ++ks) {
+        FragA<NP> aq, ay;
+        load_a<false, NP>(aq, Qg, L::LQ, 16 * ts.mt, 16 * ks);
+        load_a<false, NP>(ay, Ys, L::LQ, 16 * ts.mt, 16 * ks);
+        ay.negate();
+#pragma unroll
+        for (int j = 0; j < WarpTile<DK>::NT; ++j) {
+          FragB<NP> b;
+          load_b<false, NP>(b, ob, L::LO, 16 * ks, 8 * (ts.nt0 + j));
+          mma_split<NP>(acc[j], aq, b);
+          load_b<false, NP>(b, dWl, kLS, 16 * ks, 8 * (ts.nt0 + j));
+          mma_split<NP>(acc[j], ay, b);
+        }
+      }
+#pragma unroll
+      for (int j = 0; j < WarpTile<DK>::NT; ++j)
+#pragma unroll
+        for (int hf = 0; hf < 2; ++hf) {
+          const int r = 16 * ts.mt + g + 8 * hf, c = 8 * (ts.nt0 + j) + 2 * t;
+          *reinterpret_cast<float2*>(dS + r * kLS + c) = make_float2(acc[j][2 * hf], acc[j][2 * hf + 1]);
+        }
     }
+    __syncthreads();   // dS_n complete; Q_gamma, Y, gamma_C and dW no longer read
+    if (n > 0) stage_b(n - 1);
+    else cp_commit();
   }
-  __syncthreads();
+  cp_wait<0>();
   if (p.d_h0)
-    for (int e = tid; e < dk * kSlice; e += blockDim.x)
-      p.d_h0[((static_cast<size_t>(bb) * p.H + h) * dk + e / kSlice) * dv + col0 + e % kSlice] = dS[e];
+#pragma unroll
+    for (int j = 0; j < WarpTile<DK>::NT; ++j)
+#pragma unroll
+      for (int hf = 0; hf < 2; ++hf) {
+        const int r = 16 * ts.mt + g + 8 * hf, c = 8 * (ts.nt0 + j) + 2 * t;
+        *reinterpret_cast<float2*>(p.d_h0 + (bh * DK + r) * dv + col0 + c) =
+            make_float2(acc[j][2 * hf], acc[j][2 * hf + 1]);
+      }
 }
 
 // ------------------------------------------------------- 4. gradients
@@ -806,6 +1068,26 @@ __global__ void __launch_bounds__(kBwdThreads) bwd_chunk_grad(const BwdPtrs p) {
   }
 }
 
+// the forward and reverse state passes: one CTA per (batch, head, 64 value columns)
+template <int DK, typename T>
+cudaError_t launch_passes(const BwdPtrs& p, cudaStream_t stream) {
+  constexpr int NP = 3;
+  const dim3 grid(p.dv / kSlice, p.H, p.B);
+  const size_t sm2 = StatePassSmem<DK>::floats * sizeof(float);
+  const size_t sm3 = DStateSmem<DK, T>::floats * sizeof(float);
+  cudaError_t err;
+  if ((err = cudaFuncSetAttribute(bwd_state_pass<DK, NP>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                  static_cast<int>(sm2))) != cudaSuccess ||
+      (err = cudaFuncSetAttribute(bwd_dstate_pass<DK, NP, T>,
+                                  cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                  static_cast<int>(sm3))) != cudaSuccess)
+    return err;
+  bwd_state_pass<DK, NP><<<grid, kPassThreads, sm2, stream>>>(p);
+  if ((err = cudaGetLastError()) != cudaSuccess) return err;
+  bwd_dstate_pass<DK, NP, T><<<grid, kPassThreads, sm3, stream>>>(p);
+  return cudaGetLastError();
+}
+
 template <typename T>
 cudaError_t launch_all(const BwdPtrs& p, cudaStream_t stream) {
   const int chunks = p.B * p.H * p.Nc;
@@ -817,18 +1099,9 @@ cudaError_t launch_all(const BwdPtrs& p, cudaStream_t stream) {
     return err;
   bwd_chunk_prep<T><<<chunks, kBwdThreads, kGemmSmem, stream>>>(p);
   if ((err = cudaGetLastError()) != cudaSuccess) return err;
-  const dim3 sgrid(p.dv / kSlice, p.H, p.B);
-  const size_t sm2 = state_pass_floats(p.dk) * sizeof(float);
-  const size_t sm3 = dstate_pass_floats(p.dk) * sizeof(float);
-  if ((err = cudaFuncSetAttribute(bwd_state_pass, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                  static_cast<int>(sm2))) != cudaSuccess ||
-      (err = cudaFuncSetAttribute(bwd_dstate_pass<T>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                  static_cast<int>(sm3))) != cudaSuccess)
+  if ((err = (p.dk == 128 ? launch_passes<128, T>(p, stream) : launch_passes<64, T>(p, stream))) !=
+      cudaSuccess)
     return err;
-  bwd_state_pass<<<sgrid, kPassThreads, sm2, stream>>>(p);
-  if ((err = cudaGetLastError()) != cudaSuccess) return err;
-  bwd_dstate_pass<T><<<sgrid, kPassThreads, sm3, stream>>>(p);
-  if ((err = cudaGetLastError()) != cudaSuccess) return err;
   bwd_chunk_grad<T><<<chunks, kBwdThreads, kGemmSmem, stream>>>(p);
   return cudaGetLastError();
 }
