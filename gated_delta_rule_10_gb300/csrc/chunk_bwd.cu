@@ -22,7 +22,9 @@
 // The per-chunk kernels run their products on the tensor cores (warp-level MMA
 // with every fp32 operand split into tf32 hi + lo, about fp32 accuracy), their
 // operands staged through shared memory a 32-wide K slice at a time; the state
-// passes stage each chunk's operands whole and multiply on the FP32 pipe. Chunks
+// passes keep the state in MMA accumulators and multiply on warp-level MMAs
+// with bf16 hi + lo split operands, the next chunk's operands copied in while
+// the current one is used. Chunks
 // past the end are zero-filled, which leaves every product and the reverse
 // cumulative sum exact for the valid rows.
 #include <cuda_bf16.h>
