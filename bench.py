@@ -54,6 +54,9 @@ def parse():
                    help="skip the sequence-split measurement")
     p.add_argument("--no-backward", action="store_true",
                    help="skip the backward measurement")
+    p.add_argument("--pipeline", type=int, default=None,
+                   help="time segments of the pipelined forward (default: the library's "
+                        "recommendation for the workload; 1: the plain call)")
     return p.parse_args()
 
 
@@ -78,7 +81,7 @@ def peaks():
 # and chunk_scan_kernel), per workload, with the hash of the kernel sources they
 # were taken on: a changed kernel reports null traffic until it is profiled
 # again. Source: profiles/chunk_fwd_two_kernel_gdn_b4_t4096_h16_d128.md.
-TRAFFIC = {2: {"bytes": 818.4e6, "sources": "8b710db025653a93"}}
+TRAFFIC = {2: {"bytes": 813.7e6, "sources": "e71442f92e0cf5a2"}}
 KERNEL_SOURCES = ("chunk_prep.cu", "chunk_scan.cu", "packet.h", "tc.cuh", "tri_inverse.cuh",
                   "common.cuh")
 
@@ -197,13 +200,17 @@ def run_ours(args):
     stream = torch.cuda.current_stream(dev)
     flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
     shape = gdr.make_shape(B, T, H, dk, dv, c["dtype"], x["flags"], x["scale"])
-    ws_bytes = gdr.chunk_fwd_workspace_bytes(shape)
+    # long sequences with few (batch, head) pairs: the pipelined call overlaps the
+    # preparation of one time segment with the state pass of the previous one
+    pipe = args.pipeline if args.pipeline is not None else gdr.pipeline_segments(shape)
+    ws_bytes = (gdr.chunk_fwd_pipelined_workspace_bytes(shape, pipe) if pipe > 1
+                else gdr.chunk_fwd_workspace_bytes(shape))
     ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev) if ws_bytes else None
 
     def step():
         gdr.chunk_fwd(xd["q"], xd["k"], xd["v"], xd["g"], xd["beta"], xd["lam"], xd["b"],
                       xd["w"], xd["h0"], scale=x["scale"], flags=x["flags"], o=o, hT=hT,
-                      workspace=ws)
+                      workspace=ws, pipeline=pipe)
         for _ in range(args.decode_steps if has_decode else 0):
             gdr.recurrent_step(yd["q"], yd["k"], yd["v"], yd["g"], state, yd["beta"], yd["lam"],
                                yd["b"], yd["w"], scale=y["scale"], flags=y["flags"], o=o_dec)
@@ -224,7 +231,7 @@ def run_ours(args):
         ev[i][0].record(stream)
         gdr.chunk_fwd(xd["q"], xd["k"], xd["v"], xd["g"], xd["beta"], xd["lam"], xd["b"],
                       xd["w"], xd["h0"], scale=x["scale"], flags=x["flags"], o=o, hT=hT,
-                      workspace=ws)
+                      workspace=ws, pipeline=pipe)
         ev[i][1].record(stream)
         for _ in range(args.decode_steps if has_decode else 0):
             gdr.recurrent_step(yd["q"], yd["k"], yd["v"], yd["g"], state, yd["beta"], yd["lam"],
@@ -265,7 +272,11 @@ def run_ours(args):
         roof = {"bound": "tensor", "achieved": round(tflops, 2), "peak": pk["bf16_tflops"],
                 "unit": "TFLOP/s", "frac": round(tflops / pk["bf16_tflops"], 4)}
     roof.update({"traffic": measured_traffic(args.workload),
-                 "kernel": "gdr_chunk_fwd: chunk_prep_kernel + chunk_scan_kernel (one call)",
+                 "kernel": ("gdr_chunk_fwd: chunk_prep_kernel + chunk_scan_kernel (one call)"
+                            if pipe <= 1 else
+                            "gdr_chunk_fwd_pipelined: %d x (chunk_prep_kernel + chunk_scan_kernel)"
+                            ", one call" % pipe),
+                 "pipeline_segments": pipe,
                  "peak_source": pk_kind,
                  "algorithmic_bytes_per_launch": chunk_bytes,
                  "algorithmic_flops_per_launch": flops,
@@ -310,7 +321,8 @@ def run_ours(args):
         # this library's kernels per timed step: the two-kernel chunked forward
         # (bf16 with the full workspace) or one fused kernel (fp32), then the
         # decode steps
-        "gpu_launches": K * ((2 if ws is not None else 1) + (args.decode_steps if has_decode else 0)),
+        "gpu_launches": K * ((2 * max(pipe, 1) if ws is not None else 1) +
+                             (args.decode_steps if has_decode else 0)),
         "clocks": clk,
         "e2e": e2e,
     }

@@ -60,6 +60,11 @@ def lib():
                                           [_vp, ctypes.c_size_t, _vp])
         L.gdr_chunk_fwd_workspace_split.argtypes = [sp, ctypes.c_int,
                                                     ctypes.POINTER(ctypes.c_size_t)]
+        L.gdr_chunk_fwd_pipelined.argtypes = ([sp, ctypes.c_int] + [_vp] * 11 +
+                                              [_vp, ctypes.c_size_t, _vp, _vp])
+        L.gdr_chunk_fwd_workspace_pipelined.argtypes = [sp, ctypes.c_int,
+                                                        ctypes.POINTER(ctypes.c_size_t)]
+        L.gdr_chunk_fwd_pipeline_segments.argtypes = [sp, ctypes.POINTER(ctypes.c_int)]
         L.gdr_recurrent_step.argtypes = [sp] + [_vp] * 10 + [_vp]
         L.gdr_gate_cumsum.argtypes = [ctypes.c_int] * 4 + [_vp, _vp, _vp]
         L.gdr_chunk_fwd_check.argtypes = [_vp, _vp, ctypes.POINTER(ctypes.c_int)]
@@ -72,7 +77,8 @@ def lib():
         L.gdr_abi_version.restype = ctypes.c_int
         for name in ("gdr_chunk_fwd_workspace", "gdr_chunk_fwd_workspace_min", "gdr_chunk_fwd",
                      "gdr_chunk_fwd_split", "gdr_chunk_fwd_workspace_split",
-                     "gdr_recurrent_step",
+                     "gdr_chunk_fwd_pipelined", "gdr_chunk_fwd_workspace_pipelined",
+                     "gdr_chunk_fwd_pipeline_segments", "gdr_recurrent_step",
                      "gdr_gate_cumsum", "gdr_chunk_fwd_check", "gdr_rmsnorm_gate",
                      "gdr_chunk_bwd_workspace", "gdr_chunk_bwd"):
             getattr(L, name).restype = ctypes.c_int
@@ -143,9 +149,41 @@ def chunk_fwd_workspace_bytes(shape, minimum=False, segments=None):
     return n.value
 
 
+def pipeline_segments(shape):
+    """Time segments ``gdr_chunk_fwd_pipelined`` should use on `shape` (1: none)."""
+    n = ctypes.c_int(1)
+    st = lib().gdr_chunk_fwd_pipeline_segments(ctypes.byref(shape), ctypes.byref(n))
+    if st:
+        raise GdrError(st, "gdr_chunk_fwd_pipeline_segments")
+    return n.value
+
+
+def chunk_fwd_pipelined_workspace_bytes(shape, segments):
+    n = ctypes.c_size_t(0)
+    st = lib().gdr_chunk_fwd_workspace_pipelined(ctypes.byref(shape), int(segments),
+                                                 ctypes.byref(n))
+    if st:
+        raise GdrError(st, "gdr_chunk_fwd_workspace_pipelined")
+    return n.value
+
+
+_aux_streams = {}
+
+
+def aux_stream(device):
+    """The high-priority stream of `device` that pipelined forwards run their
+    state passes on (created once per device)."""
+    idx = torch.device(device).index
+    if idx is None:
+        idx = torch.cuda.current_device()
+    if idx not in _aux_streams:
+        _aux_streams[idx] = torch.cuda.Stream(device=idx, priority=-1)
+    return _aux_streams[idx]
+
+
 def chunk_fwd(q, k, v, g, beta=None, lam=None, b=None, w=None, h0=None, *, scale=None,
               flags=None, output_final_state=True, o=None, hT=None, workspace=None,
-              segments=None, stream=None):
+              segments=None, pipeline=None, aux=None, stream=None):
     """Chunkwise forward (``gdr_chunk_fwd``).
 
     q, k: [B, T, H, d_k]; v: [B, T, H, d_v] (bf16 or fp32, one dtype);
@@ -156,8 +194,12 @@ def chunk_fwd(q, k, v, g, beta=None, lam=None, b=None, w=None, h0=None, *, scale
     ``scale`` to d_k^-1/2. ``workspace`` defaults to the size of the fastest path
     (pass a smaller tensor, even an empty one, to select another path).
     ``segments`` cuts every sequence into that many runs
-    (``gdr_chunk_fwd_split``); by default the library decides. Returns (o, hT)
-    with hT None unless requested.
+    (``gdr_chunk_fwd_split``); by default the library decides. ``pipeline``
+    runs ``gdr_chunk_fwd_pipelined`` with that many time segments, the state
+    passes on ``aux`` (default: this module's high-priority auxiliary stream of
+    the device; 1: off); by default (no ``workspace`` or ``segments`` given) the
+    library's recommendation is taken. Returns (o, hT) with hT None unless
+    requested.
     """
     B, T, H, dk = q.shape
     dv = v.shape[-1]
@@ -185,19 +227,33 @@ def chunk_fwd(q, k, v, g, beta=None, lam=None, b=None, w=None, h0=None, *, scale
         hT = torch.empty(B, H, dk, dv, dtype=torch.float32, device=dev)
     _check(hT, "hT", torch.float32, dev, (B, H, dk, dv))
     shape = make_shape(B, T, H, dk, dv, dt, flags, scale)
-    ws_bytes = chunk_fwd_workspace_bytes(shape, segments=segments)
+    if pipeline is None:
+        pipeline = (pipeline_segments(shape) if workspace is None and segments is None else 1)
+    if pipeline > 1:
+        if segments is not None:
+            raise ValueError("pipeline and segments select different paths")
+        ws_bytes = chunk_fwd_pipelined_workspace_bytes(shape, pipeline)
+    else:
+        ws_bytes = chunk_fwd_workspace_bytes(shape, segments=segments)
     if ws_bytes and workspace is None:
         workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
     args = (_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(lam), _ptr(b), _ptr(w),
             _ptr(h0), _ptr(o), _ptr(hT), _ptr(workspace),
             ctypes.c_size_t(0 if workspace is None else workspace.numel()), _stream(stream, dev))
     with torch.cuda.device(dev):
-        if segments is None:
+        if pipeline > 1:
+            name = "gdr_chunk_fwd_pipelined"
+            st = lib().gdr_chunk_fwd_pipelined(ctypes.byref(shape), int(pipeline), *args,
+                                               _stream(aux if aux is not None else aux_stream(dev),
+                                                       dev))
+        elif segments is None:
+            name = "gdr_chunk_fwd"
             st = lib().gdr_chunk_fwd(ctypes.byref(shape), *args)
         else:
+            name = "gdr_chunk_fwd_split"
             st = lib().gdr_chunk_fwd_split(ctypes.byref(shape), int(segments), *args)
     if st:
-        raise GdrError(st, "gdr_chunk_fwd" if segments is None else "gdr_chunk_fwd_split")
+        raise GdrError(st, name)
     return o, hT
 
 

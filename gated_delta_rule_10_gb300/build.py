@@ -37,6 +37,15 @@ def _headers():
                   glob.glob(os.path.join(ROOT, "include", "*.h")))
 
 
+def _included_sources(src):
+    """Other .cu files that `src` includes (a translation unit that compiles the
+    same kernels with other settings depends on them)."""
+    import re
+    with open(src) as f:
+        names = re.findall(r'^\s*#\s*include\s+"([^"]+\.cu)"', f.read(), flags=re.M)
+    return [os.path.join(CSRC, n) for n in names]
+
+
 def _stale(target, deps):
     if not os.path.exists(target):
         return True
@@ -54,7 +63,7 @@ def build(force=False, verbose=False, extra_flags=()):
     for src in srcs:
         obj = os.path.join(BUILD, os.path.basename(src)[:-3] + ".o")
         objs.append(obj)
-        if force or _stale(obj, [src] + headers):
+        if force or _stale(obj, [src] + headers + _included_sources(src)):
             cmd = [nvcc()] + NVCC_FLAGS + list(extra_flags) + ["-c", src, "-o", obj]
             jobs.append(cmd)
     if jobs:

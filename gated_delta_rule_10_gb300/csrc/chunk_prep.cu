@@ -64,7 +64,7 @@ struct PrepLayout {
   static constexpr uint32_t oVec = oPart + 8192;            // beta, lam, G, e^G, e^{G_C-G}, e^-G [64]
   static constexpr uint32_t oBar = oVec + 6 * 64 * 4 + 16;  // 4 mbarriers (after a flag word)
   static constexpr uint32_t oSlot = oBar + 32;
-  static constexpr uint32_t bytes = oSlot + 16;
+  static constexpr uint32_t bytes = oSlot + 16;   // TMEM address, two claimed work items
   static constexpr uint32_t launch_bytes = bytes + 1024;
   static constexpr uint32_t kTmemCols = (DK + DV) > 128 ? 256 : 128;
 };
@@ -327,14 +327,14 @@ __device__ __forceinline__ void prep_z(unsigned char* smem, const float* sBeta) 
   }
 }
 
-template <int DK, int DV, bool SC, bool VB>
+template <int DK, int DV, bool SC, bool VB, bool DYN>
 __global__ void __launch_bounds__(kThreads, 2)
     chunk_prep_kernel(const ChunkArgs a, const __grid_constant__ CUtensorMap tm_q,
                       const __grid_constant__ CUtensorMap tm_k,
                       const __grid_constant__ CUtensorMap tm_v,
                       const __grid_constant__ CUtensorMap tm_b,
                       const __grid_constant__ CUtensorMap tm_w, unsigned char* packets,
-                      int* status) {
+                      int* status, const PrepRange rg) {
   using L = PrepLayout<DK, DV>;
   using P = std::conditional_t<VB, PacketVB<DK, DV>, Packet<DK, DV>>;
   static_assert(!VB || SC, "the value-channel packets take the scalar-gate tiles");
@@ -344,7 +344,9 @@ __global__ void __launch_bounds__(kThreads, 2)
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int T = a.T, H = a.H, B = a.B;
   const int n_chunks = (T + kChunk - 1) / kChunk;
-  const int total = n_chunks * B * H;
+  // chunks rg.chunk0 .. rg.chunk0 + rc - 1 of every (batch, head)
+  const int rc = rg.chunks > 0 ? rg.chunks : n_chunks - rg.chunk0;
+  const int total = rc * B * H;
   const bool CH = a.flags & 1u, ER = a.flags & 2u, WR = a.flags & 4u, QM = a.flags & 8u;
 
   float* sT = reinterpret_cast<float*>(smem + L::oT);
@@ -377,12 +379,23 @@ __global__ void __launch_bounds__(kThreads, 2)
     h = w % H;
     const int rest = w / H;
     bb = rest % B;
-    n = rest / B;
+    n = rg.chunk0 + rest / B;
+  };
+  // Work items: a fixed stride over the grid (persistent CTAs), or, with a
+  // counter, claimed one at a time by thread 64, at most rg.per_cta per CTA so
+  // that CTAs come and go and a concurrent kernel of higher priority gets SMs.
+  // A CTA knows its current item, the next, and (from the top of an
+  // iteration) the one after, which it publishes in slot iter % 2.
+  int* sClaim = reinterpret_cast<int*>(smem + L::oSlot + 4);   // [2]
+  auto claim = [&](int k) {   // the CTA's k-th item (thread 64, dynamic mode)
+    if (k >= rg.per_cta) return total;
+    const int x = atomicAdd(rg.counter, 1);
+    return x < total ? x : total;
   };
   // TMA loads of one chunk's input tiles (thread 64): the value side (v, w) and
   // the key side (q, k, b) each complete one phase of their barrier; the
   // CTA's chunk after that one is prefetched into L2 along with them
-  auto load_values = [&](int w) {
+  auto load_values = [&](int w, int w_after) {
     int n, bb, h;
     decode(w, n, bb, h);
     tc::fence_proxy_async();
@@ -393,8 +406,8 @@ __global__ void __launch_bounds__(kThreads, 2)
       if (WR)
         tc::tma_load_4d(sbase + L::oEa + blk * 8192, &tm_w, blk * 64, h, n * kChunk, bb, bar(kBarV));
     }
-    if (w + gridDim.x < total) {
-      decode(w + gridDim.x, n, bb, h);
+    if (w_after < total) {
+      decode(w_after, n, bb, h);
 #pragma unroll
       for (int blk = 0; blk < DV / 64; ++blk) {
         tc::tma_prefetch_4d(&tm_v, blk * 64, h, n * kChunk, bb);
@@ -402,7 +415,7 @@ __global__ void __launch_bounds__(kThreads, 2)
       }
     }
   };
-  auto load_keys = [&](int w) {
+  auto load_keys = [&](int w, int w_after) {
     int n, bb, h;
     decode(w, n, bb, h);
     tc::fence_proxy_async();
@@ -416,8 +429,8 @@ __global__ void __launch_bounds__(kThreads, 2)
         tc::tma_load_4d(sbase + L::oK + blk * 8192, &tm_k, blk * 64, h, n * kChunk, bb, bar(kBarK));
       if (ER) tc::tma_load_4d(sbase + L::oEQ + blk * 16384, &tm_b, blk * 64, h, n * kChunk, bb, bar(kBarK));
     }
-    if (w + gridDim.x < total) {
-      decode(w + gridDim.x, n, bb, h);
+    if (w_after < total) {
+      decode(w_after, n, bb, h);
 #pragma unroll
       for (int blk = 0; blk < DK / 64; ++blk) {
         tc::tma_prefetch_4d(&tm_q, blk * 64, h, n * kChunk, bb);
@@ -428,22 +441,47 @@ __global__ void __launch_bounds__(kThreads, 2)
   };
   // loads issued and waited for, to drain what is in flight on the way out
   int v_issued = 0, k_issued = 0, v_done = 0, k_done = 0;
-  if (tid == 64 && blockIdx.x < total) {
-    load_values(blockIdx.x);
-    load_keys(blockIdx.x);
+  constexpr bool dyn = DYN;   // work claimed from rg.counter
+  const int stride = static_cast<int>(gridDim.x);
+  int w = static_cast<int>(blockIdx.x), wn = w + stride, wa = wn + stride;   // this, next, after
+  if (dyn) {
+    if (tid == 64) {
+      sClaim[0] = claim(0);
+      sClaim[1] = sClaim[0] < total ? claim(1) : total;
+    }
+    __syncthreads();
+    w = sClaim[0];
+    wn = sClaim[1];
+    wa = total;
+    __syncthreads();   // both read before thread 64 writes a slot again
   }
-  if (blockIdx.x < total) { v_issued = 1; k_issued = 1; }
+  if (w < total) {
+    if (tid == 64) {
+      load_values(w, wn);
+      load_keys(w, wn);
+    }
+    v_issued = 1;
+    k_issued = 1;
+  }
 
   int fail_at = -1, iter = 0;
-  for (int w = blockIdx.x; w < total; w += gridDim.x, ++iter) {
+  for (; w < total; w = wn, wn = wa, ++iter) {
+    // the item after the next one: claimed now (published for the loop step)
+    if (dyn) {
+      if (tid == 64) {
+        wa = wn < total ? claim(iter + 2) : total;
+        sClaim[iter & 1] = wa;
+      }
+    } else {
+      wa = wn + stride;
+    }
     const uint32_t par = static_cast<uint32_t>(iter & 1);
     int n, bb, h;
     decode(w, n, bb, h);
     const int t0 = n * kChunk, Lr = min(kChunk, T - t0);
     const size_t row0 = size_t(bb) * T + t0;
     unsigned char* pkt = packets + ((size_t(bb) * H + h) * n_chunks + n) * P::bytes;
-    const int wn = w + gridDim.x;   // this CTA's next chunk
-    int nn = 0, nb = 0, nh = 0;
+    int nn = 0, nb = 0, nh = 0;   // this CTA's next chunk
     if (wn < total) decode(wn, nn, nb, nh);
 
     // gates of the next chunk into L2 (one row each for threads 128..191)
@@ -504,7 +542,7 @@ __global__ void __launch_bounds__(kThreads, 2)
       prep_values_vb<DK, DV>(smem, pkt, a, row0, h, Lr);
       __syncthreads();   // v has been copied out: the next chunk's value tiles may land
       if (wn < total) {
-        if (tid == 64) load_values(wn);
+        if (tid == 64) load_values(wn, wa);
         ++v_issued;
       }
     }
@@ -602,10 +640,11 @@ __global__ void __launch_bounds__(kThreads, 2)
     if (VB) {
       // no inverse and no M2: the key-side tiles are consumed, the chunk is done
       if (wn < total) {
-        if (tid == 64) load_keys(wn);
+        if (tid == 64) load_keys(wn, wa);
         ++k_issued;
       }
       tc::fence_after_sync();
+      if (dyn) wa = sClaim[iter & 1];
       continue;
     }
 
@@ -628,7 +667,7 @@ __global__ void __launch_bounds__(kThreads, 2)
     __syncthreads();
     // T and A are consumed: the key-side tiles of the next chunk may land now
     if (wn < total) {
-      if (tid == 64) load_keys(wn);
+      if (tid == 64) load_keys(wn, wa);
       ++k_issued;
     }
 
@@ -648,7 +687,7 @@ __global__ void __launch_bounds__(kThreads, 2)
     tc::fence_after_sync();
     // Z and E_abs are consumed: the value-side tiles of the next chunk may land now
     if (wn < total) {
-      if (tid == 64) load_values(wn);
+      if (tid == 64) load_values(wn, wa);
       ++v_issued;
     }
     {
@@ -683,6 +722,7 @@ __global__ void __launch_bounds__(kThreads, 2)
     tc::fence_before_sync();
     __syncthreads();
     tc::fence_after_sync();
+    if (dyn) wa = sClaim[iter & 1];
   }
 
   if (fail_at >= 0) {
@@ -701,9 +741,9 @@ __global__ void __launch_bounds__(kThreads, 2)
   if (warp == 0) tc::tmem_dealloc(tmem, L::kTmemCols);
 }
 
-template <int DK, int DV, bool SC, bool VB>
+template <int DK, int DV, bool SC, bool VB, bool DYN>
 cudaError_t launch_prep_kernel(const ChunkArgs& a, unsigned char* packets, int* status,
-                               cudaStream_t stream) {
+                               const PrepRange& rg, cudaStream_t stream) {
   using L = PrepLayout<DK, DV>;
   static_assert(2 * (L::launch_bytes + 1024) <= 233472, "two CTAs per SM");
   CUtensorMap tq, tk, tv, tb, tw;
@@ -714,7 +754,7 @@ cudaError_t launch_prep_kernel(const ChunkArgs& a, unsigned char* packets, int* 
   tw = tq;
   if ((a.flags & 2u) && !make_bthd_tmap(&tb, a.b, a.B, a.T, a.H, DK)) return cudaErrorInvalidValue;
   if ((a.flags & 4u) && !make_bthd_tmap(&tw, a.w, a.B, a.T, a.H, DV)) return cudaErrorInvalidValue;
-  auto kern = chunk_prep_kernel<DK, DV, SC, VB>;
+  auto kern = chunk_prep_kernel<DK, DV, SC, VB, DYN>;
   cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(L::launch_bytes));
   if (err != cudaSuccess) return err;
@@ -723,29 +763,59 @@ cudaError_t launch_prep_kernel(const ChunkArgs& a, unsigned char* packets, int* 
   if ((err = cudaGetDevice(&dev)) != cudaSuccess) return err;
   if ((err = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
     return err;
-  const long long total = static_cast<long long>((a.T + kChunk - 1) / kChunk) * a.B * a.H;
-  const int grid = static_cast<int>(total < 2LL * sms ? total : 2LL * sms);
-  kern<<<grid, kThreads, L::launch_bytes, stream>>>(a, tq, tk, tv, tb, tw, packets, status);
+  const int n_chunks = (a.T + kChunk - 1) / kChunk;
+  const int rc = rg.chunks > 0 ? rg.chunks : n_chunks - rg.chunk0;
+  if (rg.chunk0 < 0 || rc < 1 || rg.chunk0 + rc > n_chunks) return cudaErrorInvalidValue;
+  const long long total = static_cast<long long>(rc) * a.B * a.H;
+  long long grid = total < 2LL * sms ? total : 2LL * sms;
+  if (DYN != (rg.counter != nullptr)) return cudaErrorInvalidValue;
+  if (DYN) {   // claimed work: enough CTAs of at most per_cta items each
+    if (rg.per_cta < 1) return cudaErrorInvalidValue;
+    grid = (total + rg.per_cta - 1) / rg.per_cta;
+  }
+  kern<<<static_cast<unsigned>(grid), kThreads, L::launch_bytes, stream>>>(a, tq, tk, tv, tb, tw,
+                                                                          packets, status, rg);
   return cudaGetLastError();
 }
 
-template <int DK, int DV>
+template <int DK, int DV, bool DYN>
 cudaError_t launch_prep(const ChunkArgs& a, unsigned char* packets, int* status,
-                        cudaStream_t stream) {
-  if (a.flags & 16u) return launch_prep_kernel<DK, DV, true, true>(a, packets, status, stream);
-  if ((a.flags & 7u) == 0) return launch_prep_kernel<DK, DV, true, false>(a, packets, status, stream);
-  return launch_prep_kernel<DK, DV, false, false>(a, packets, status, stream);
+                        const PrepRange& rg, cudaStream_t stream) {
+  if (a.flags & 16u)
+    return launch_prep_kernel<DK, DV, true, true, DYN>(a, packets, status, rg, stream);
+  if ((a.flags & 7u) == 0)
+    return launch_prep_kernel<DK, DV, true, false, DYN>(a, packets, status, rg, stream);
+  return launch_prep_kernel<DK, DV, false, false, DYN>(a, packets, status, rg, stream);
+}
+
+template <bool DYN>
+cudaError_t launch_prep_dims(const ChunkArgs& a, int dk, unsigned char* packets, int* status,
+                             cudaStream_t stream, const PrepRange& rg) {
+  if (dk == 64 && a.dv == 64) return launch_prep<64, 64, DYN>(a, packets, status, rg, stream);
+  if (dk == 64 && a.dv == 128) return launch_prep<64, 128, DYN>(a, packets, status, rg, stream);
+  if (dk == 128 && a.dv == 64) return launch_prep<128, 64, DYN>(a, packets, status, rg, stream);
+  if (dk == 128 && a.dv == 128) return launch_prep<128, 128, DYN>(a, packets, status, rg, stream);
+  return cudaErrorInvalidValue;
 }
 
 }  // namespace
 
+// The kernel is compiled twice: with a fixed persistent stride here, and with
+// claimed work items in chunk_prep_claimed.cu (which defines
+// GDR_PREP_CLAIMED and includes this file), so that the stride variant carries
+// no code of the other and the two build in parallel.
+#ifndef GDR_PREP_CLAIMED
 cudaError_t launch_chunk_prep(const ChunkArgs& a, int dk, unsigned char* packets, int* status,
-                              cudaStream_t stream) {
-  if (dk == 64 && a.dv == 64) return launch_prep<64, 64>(a, packets, status, stream);
-  if (dk == 64 && a.dv == 128) return launch_prep<64, 128>(a, packets, status, stream);
-  if (dk == 128 && a.dv == 64) return launch_prep<128, 64>(a, packets, status, stream);
-  if (dk == 128 && a.dv == 128) return launch_prep<128, 128>(a, packets, status, stream);
-  return cudaErrorInvalidValue;
+                              cudaStream_t stream, const PrepRange& rg) {
+  if (rg.counter) return launch_chunk_prep_claimed(a, dk, packets, status, stream, rg);
+  return launch_prep_dims<false>(a, dk, packets, status, stream, rg);
 }
+#else
+cudaError_t launch_chunk_prep_claimed(const ChunkArgs& a, int dk, unsigned char* packets,
+                                      int* status, cudaStream_t stream, const PrepRange& rg) {
+  if (!rg.counter) return cudaErrorInvalidValue;
+  return launch_prep_dims<true>(a, dk, packets, status, stream, rg);
+}
+#endif
 
 }  // namespace gdr

@@ -133,7 +133,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int SW = hom ? DK : DV;               // width of this CTA's state
   const int col0 = slice * kNV;
   const int n_chunks = (T + kChunk - 1) / kChunk;
-  const int c_begin = seg * sg.seg_chunks;
+  const int c_begin = sg.chunk0 + seg * sg.seg_chunks;
   const int cnt = max(0, min(n_chunks, c_begin + sg.seg_chunks) - c_begin);   // chunks of this run
   const unsigned char* pk0 = packets + ((size_t(bb) * H + h) * n_chunks + c_begin) * P::bytes;
   const size_t run = (size_t(bb) * H + h) * sg.segments + seg;   // per-run state index
@@ -484,7 +484,8 @@ cudaError_t launch_scan(const ChunkArgs& a, const unsigned char* packets, int* s
                                          static_cast<int>(L::launch_bytes));
   if (err != cudaSuccess) return err;
   if (sg.segments < 1) return cudaErrorInvalidValue;
-  if (sg.seg_chunks < 1) sg.seg_chunks = (a.T + kChunk - 1) / kChunk;
+  if (sg.chunk0 < 0) return cudaErrorInvalidValue;
+  if (sg.seg_chunks < 1) sg.seg_chunks = (a.T + kChunk - 1) / kChunk - sg.chunk0;
   dim3 grid(DV / kNV + (sg.hT_hom ? DK / kNV : 0), a.H,
             static_cast<unsigned>(a.B) * static_cast<unsigned>(sg.segments));
   kern<<<grid, kThreads, L::launch_bytes, stream>>>(a, packets, status, sg);

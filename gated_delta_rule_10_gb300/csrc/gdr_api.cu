@@ -3,6 +3,7 @@
 // synchronises the stream.
 #include <stdint.h>
 
+#include <algorithm>
 #include <cmath>
 #include <limits>
 
@@ -302,6 +303,103 @@ gdr_status chunk_fwd_impl(const gdr_shape* shape, int segments, const void* q, c
   return err == cudaSuccess ? GDR_OK : GDR_ERR_CUDA;
 }
 
+// ---- pipelined two-kernel path: time segments, preparation of segment s + 1
+// on `stream` while the scan of segment s runs on `aux` ----
+constexpr int kPipePerCta = 1;          // chunks a preparation CTA claims at most
+constexpr int kPipeMaxSegments = 64;
+constexpr int kPipeTargetSegments = 8;  // segments the default policy aims for
+constexpr int kPipeMinChunks = 32;      // chunks per segment, at least
+
+// segments actually used for a request of S: every segment non-empty
+void pipe_geometry(const gdr_shape* s, int S, int* segs, int* seg_chunks) {
+  const int nc = n_chunks_of(s);
+  if (S > nc) S = nc;
+  const int per = (nc + S - 1) / S;
+  *seg_chunks = per;
+  *segs = (nc + per - 1) / per;
+}
+
+// status words and packets, then the state handed between segments
+// ([B, H, d_k, d_v] fp32) and one work counter per segment
+size_t pipelined_bytes(const gdr_shape* s, int S) {
+  const size_t st = static_cast<size_t>(s->B) * s->H * s->dk * s->dv * sizeof(float);
+  return align256(two_kernel_bytes(s)) + align256(st) + align256(static_cast<size_t>(S) * sizeof(int));
+}
+
+gdr_status chunk_fwd_pipelined_impl(const gdr_shape* shape, int segments, const void* q,
+                                    const void* k, const void* v, const float* g,
+                                    const float* beta, const float* lam, const void* b,
+                                    const void* w, const float* h0, void* o, float* hT,
+                                    void* workspace, size_t ws_bytes, gdr_stream_t stream,
+                                    gdr_stream_t aux_stream) {
+  if (segments < 1 || segments > kPipeMaxSegments) return GDR_ERR_INVALID_ARG;
+  gdr_status st = check_shape(shape, false);
+  if (st != GDR_OK) return st;
+  st = check_gates(shape, q, k, v, g, beta, lam, b, w, o);
+  if (st != GDR_OK) return st;
+  if ((h0 && !aligned(h0, 16)) || (hT && !aligned(hT, 16))) return GDR_ERR_INVALID_ARG;
+  if (shape->dtype != GDR_BF16) return GDR_ERR_UNSUPPORTED;
+  if (!workspace || !aligned(workspace, 16) || ws_bytes < pipelined_bytes(shape, segments))
+    return GDR_ERR_WORKSPACE;
+  int S = 1, per = 1;
+  pipe_geometry(shape, segments, &S, &per);
+
+  gdr::ChunkArgs a;
+  a.q = q; a.k = k; a.v = v; a.g = g; a.beta = beta; a.lam = lam; a.b = b; a.w = w;
+  a.h0 = h0; a.o = o; a.hT = hT;
+  a.B = shape->B; a.T = shape->T; a.H = shape->H; a.dv = shape->dv;
+  a.flags = shape->flags; a.scale = shape->scale;
+  const cudaStream_t main_ = reinterpret_cast<cudaStream_t>(stream);
+  const cudaStream_t aux_ = reinterpret_cast<cudaStream_t>(aux_stream);
+  unsigned char* base = static_cast<unsigned char*>(workspace);
+  int* status = reinterpret_cast<int*>(base);
+  unsigned char* packets = base + gdr::kChunkWorkspaceBytes;
+  float* hbuf = reinterpret_cast<float*>(base + align256(two_kernel_bytes(shape)));
+  int* counters = reinterpret_cast<int*>(
+      reinterpret_cast<unsigned char*>(hbuf) +
+      align256(static_cast<size_t>(shape->B) * shape->H * shape->dk * shape->dv * sizeof(float)));
+
+  cudaError_t err = cudaMemsetAsync(status, 0, gdr::kStatusWords * sizeof(int), main_);
+  if (err == cudaSuccess) err = cudaMemsetAsync(counters, 0, S * sizeof(int), main_);
+  if (err != cudaSuccess) return GDR_ERR_CUDA;
+  if (S == 1) {
+    err = gdr::launch_chunk_prep(a, shape->dk, packets, status, main_);
+    if (err == cudaSuccess) err = gdr::launch_chunk_scan(a, shape->dk, packets, status, main_);
+    return err == cudaSuccess ? GDR_OK : GDR_ERR_CUDA;
+  }
+  // one event per segment (its packets are written) and one for the last scan
+  cudaEvent_t ev[kPipeMaxSegments + 1];
+  int made = 0;
+  for (; made <= S; ++made)
+    if ((err = cudaEventCreateWithFlags(&ev[made], cudaEventDisableTiming)) != cudaSuccess) break;
+  for (int s = 0; err == cudaSuccess && s < S; ++s) {
+    gdr::PrepRange rg;
+    rg.chunk0 = s * per;
+    rg.chunks = std::min(per, n_chunks_of(shape) - rg.chunk0);
+    rg.counter = counters + s;
+    rg.per_cta = kPipePerCta;
+    err = gdr::launch_chunk_prep(a, shape->dk, packets, status, main_, rg);
+    if (err == cudaSuccess) err = cudaEventRecord(ev[s], main_);
+    if (err == cudaSuccess) err = cudaStreamWaitEvent(aux_, ev[s], 0);
+    if (err == cudaSuccess) {
+      // segment s starts from h0 or the state segment s - 1 left in hbuf and
+      // leaves its end state in hbuf, the last one in hT
+      gdr::ChunkArgs as = a;
+      as.h0 = s == 0 ? h0 : hbuf;
+      as.hT = s == S - 1 ? hT : hbuf;
+      gdr::ScanSegments sg;
+      sg.chunk0 = rg.chunk0;
+      sg.seg_chunks = rg.chunks;
+      err = gdr::launch_chunk_scan(as, shape->dk, packets, status, aux_, sg);
+    }
+  }
+  // `stream` resumes after the last scan
+  if (err == cudaSuccess) err = cudaEventRecord(ev[S], aux_);
+  if (err == cudaSuccess) err = cudaStreamWaitEvent(main_, ev[S], 0);
+  for (int i = 0; i < made; ++i) cudaEventDestroy(ev[i]);   // released once completed
+  return err == cudaSuccess ? GDR_OK : GDR_ERR_CUDA;
+}
+
 }  // namespace
 
 extern "C" {
@@ -322,6 +420,43 @@ gdr_status gdr_chunk_fwd_split(const gdr_shape* shape, int segments, const void*
   if (segments < 1) return GDR_ERR_INVALID_ARG;
   return chunk_fwd_impl(shape, segments, q, k, v, g, beta, lam, b, w, h0, o, hT, workspace,
                         ws_bytes, stream);
+}
+
+gdr_status gdr_chunk_fwd_workspace_pipelined(const gdr_shape* shape, int segments,
+                                             size_t* bytes) {
+  if (!bytes || segments < 1 || segments > kPipeMaxSegments) return GDR_ERR_INVALID_ARG;
+  const gdr_status st = check_shape(shape, false);
+  if (st != GDR_OK) return st;
+  if (shape->dtype != GDR_BF16) return GDR_ERR_UNSUPPORTED;
+  *bytes = pipelined_bytes(shape, segments);
+  return GDR_OK;
+}
+
+gdr_status gdr_chunk_fwd_pipeline_segments(const gdr_shape* shape, int* segments) {
+  if (!segments) return GDR_ERR_INVALID_ARG;
+  const gdr_status st = check_shape(shape, false);
+  if (st != GDR_OK) return st;
+  *segments = 1;
+  if (shape->dtype != GDR_BF16 || default_segments(shape) > 1) return GDR_OK;
+  // the scan CTAs (one per (batch, head, 64 value columns)) leave at least
+  // half of the SMs to the preparation, and every segment keeps 32 chunks
+  const long long scan_ctas = static_cast<long long>(shape->B) * shape->H * (shape->dv / 64);
+  const int nc = n_chunks_of(shape);
+  if (2 * scan_ctas > kSplitTargetCtas) return GDR_OK;
+  int S = 1;
+  while (S < kPipeTargetSegments && 2 * S * kPipeMinChunks <= nc) S *= 2;
+  *segments = S;
+  return GDR_OK;
+}
+
+gdr_status gdr_chunk_fwd_pipelined(const gdr_shape* shape, int segments, const void* q,
+                                   const void* k, const void* v, const float* g,
+                                   const float* beta, const float* lam, const void* b,
+                                   const void* w, const float* h0, void* o, float* hT,
+                                   void* workspace, size_t ws_bytes, gdr_stream_t stream,
+                                   gdr_stream_t aux_stream) {
+  return chunk_fwd_pipelined_impl(shape, segments, q, k, v, g, beta, lam, b, w, h0, o, hT,
+                                  workspace, ws_bytes, stream, aux_stream);
 }
 
 gdr_status gdr_chunk_bwd_workspace(const gdr_shape* shape, size_t* bytes) {

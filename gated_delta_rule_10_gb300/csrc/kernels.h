@@ -77,10 +77,24 @@ cudaError_t launch_chunk_fwd_pipe(const ChunkArgs& a, int dk, const CUtensorMap&
 // bf16 inputs, two-kernel path: the chunk preparation kernel writes one packet
 // per chunk (packet.h) into `packets`, then the chunk scan kernel runs the
 // state pass over them. `packets` holds B * H * ceil(T / 64) packets.
+// PrepRange limits the preparation to chunks chunk0 .. chunk0 + chunks - 1 of
+// every (batch, head) (chunks 0: to the end). With a counter (an int that
+// reads 0 when the launch starts), CTAs claim the chunks one at a time, at
+// most per_cta each, instead of a fixed persistent stride.
+struct PrepRange {
+  int chunk0 = 0;
+  int chunks = 0;
+  int* counter = nullptr;
+  int per_cta = 0;
+};
 cudaError_t launch_chunk_prep(const ChunkArgs& a, int dk, unsigned char* packets, int* status,
-                              cudaStream_t stream);
+                              cudaStream_t stream, const PrepRange& rg = PrepRange());
+// the claimed-work variant (rg.counter non-null), which launch_chunk_prep calls
+cudaError_t launch_chunk_prep_claimed(const ChunkArgs& a, int dk, unsigned char* packets,
+                                      int* status, cudaStream_t stream, const PrepRange& rg);
 // Sequence split of the scan: `segments` runs of `seg_chunks` chunks per
-// (batch, head) (seg_chunks 0: one run of every chunk). States per run are
+// (batch, head) from chunk `chunk0` on (seg_chunks 0: one run of every chunk
+// from chunk0). States per run are
 // [B, H, segments, d_k, width] fp32. h0_per_seg: a.h0 holds one start state
 // per run (else a.h0, [B, H, d_k, d_v], starts run 0 and the others start at
 // zero). hT_per_seg: every run writes its end state to a.hT (else only the
@@ -90,6 +104,7 @@ cudaError_t launch_chunk_prep(const ChunkArgs& a, int dk, unsigned char* packets
 struct ScanSegments {
   int segments = 1;
   int seg_chunks = 0;
+  int chunk0 = 0;          // the first run starts at this chunk
   bool h0_per_seg = false;
   bool hT_per_seg = false;
   float* hT_hom = nullptr;

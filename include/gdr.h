@@ -207,6 +207,54 @@ gdr_status gdr_chunk_fwd_workspace_split(const gdr_shape* shape, int segments,
                                          size_t* bytes);
 
 /*
+ * gdr_chunk_fwd for long sequences with few (batch, head) pairs, bf16 only,
+ * overlapping the two kernels of the two-kernel path in time. The chunks of
+ * every sequence are cut into `segments` time segments of equal whole chunks
+ * (fewer when there are fewer chunks). The chunk preparation of segment s runs
+ * on `stream`; the state pass of segment s runs on `aux_stream` once those
+ * packets exist, continuing from the state segment s - 1 left in the
+ * workspace, while the preparation of segment s + 1 runs on the SMs the state
+ * pass leaves free (it walks the chunks of each (batch, head) in order and
+ * takes one SM per (batch, head, 64 value columns)). The state update and the
+ * read-out are those of gdr_chunk_fwd (Gated DeltaNet-2 notes, key design 2);
+ * only the order of the launches differs, so the result is the same up to
+ * rounding. Each preparation CTA claims one chunk from a counter and exits,
+ * so that CTAs come and go and the state pass, which needs a whole SM per CTA,
+ * gets its SMs as soon as it may start; give `aux_stream` a higher priority
+ * than `stream` (cudaStreamCreateWithPriority) so that its CTAs are scheduled
+ * first. `stream` waits for the last state pass before it
+ * runs anything enqueued after the call, so results are ordered on `stream`
+ * as for gdr_chunk_fwd. `aux_stream` may equal `stream` (no overlap). The call
+ * creates and destroys segments + 1 CUDA events (no device memory).
+ *
+ * workspace: at least gdr_chunk_fwd_workspace_pipelined(shape, segments)
+ * bytes, 16-byte aligned (status words, packets, the state between segments,
+ * one counter per segment), else GDR_ERR_WORKSPACE; calls sharing one
+ * workspace must be ordered. segments outside 1..64 is GDR_ERR_INVALID_ARG;
+ * fp32 inputs are GDR_ERR_UNSUPPORTED. Other arguments as gdr_chunk_fwd;
+ * gdr_chunk_fwd_check reads its status words.
+ */
+gdr_status gdr_chunk_fwd_pipelined(const gdr_shape* shape, int segments, const void* q,
+                                   const void* k, const void* v, const float* g,
+                                   const float* beta, const float* lam, const void* b,
+                                   const void* w, const float* h0, void* o, float* hT,
+                                   void* workspace, size_t ws_bytes, gdr_stream_t stream,
+                                   gdr_stream_t aux_stream);
+
+/* Workspace bytes of gdr_chunk_fwd_pipelined: the two-kernel workspace, then
+ * 256-byte aligned the state between segments (B * H * d_k * d_v fp32) and
+ * `segments` ints. */
+gdr_status gdr_chunk_fwd_workspace_pipelined(const gdr_shape* shape, int segments,
+                                             size_t* bytes);
+
+/* The number of time segments gdr_chunk_fwd_pipelined should use on `shape`;
+ * 1 means that the overlap is not expected to pay and gdr_chunk_fwd is the
+ * call to make. It is above 1 for bf16 when the state pass takes at most half
+ * of 152 SMs (B * H * d_v / 64 <= 76), gdr_chunk_fwd would not split the
+ * sequences, and every segment keeps at least 32 chunks (up to 8 segments). */
+gdr_status gdr_chunk_fwd_pipeline_segments(const gdr_shape* shape, int* segments);
+
+/*
  * Gradients of the chunked forward (Gated DeltaNet-2 notes, key design 3: the
  * reverse state pass over chunks, the gate-aware dA = dU Z^T + dY E_bar^T and
  * the adjoint of the triangular inverse dT = -tril(A^T dA A^T, -1), then the
@@ -221,8 +269,9 @@ gdr_status gdr_chunk_fwd_workspace_split(const gdr_shape* shape, int segments,
  *   dh0    [B,H,d_k,d_v] fp32, or NULL
  *
  * dO is [B,T,H,d_v] in the call's dtype (16-byte aligned); dhT [B,H,d_k,d_v]
- * fp32 or NULL (zero). Inputs as gdr_chunk_fwd. The arithmetic is fp32 on the
- * CUDA cores, through per-chunk records in `workspace` (at least
+ * fp32 or NULL (zero). Inputs as gdr_chunk_fwd. The arithmetic is fp32 (products
+ * on warp-level tensor-core MMAs with split operands), through per-chunk records
+ * in `workspace` (at least
  * gdr_chunk_bwd_workspace() bytes, 16-byte aligned; about 0.9 MB per chunk at
  * d_k = d_v = 128): the chunk's forward quantities, the state entering and
  * the gradient leaving every chunk. It assumes each in-chunk log-decay sum

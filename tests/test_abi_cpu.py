@@ -267,3 +267,51 @@ def test_sequence_split_workspace_and_policy(L):
                                  vp(FAKE), None, vp(FAKE), ctypes.c_size_t(two), None) == 4
     assert L.gdr_chunk_fwd_split(ctypes.byref(s), 0, *(vp(FAKE),) * 5, None, None, None, None,
                                  vp(FAKE), None, vp(FAKE), ctypes.c_size_t(two), None) == 1
+
+
+def test_pipelined_forward_workspace_policy_and_argument_rules(L):
+    n = ctypes.c_size_t(0)
+    seg = ctypes.c_int(0)
+    al = lambda x: (x + 255) // 256 * 256
+    s = _shape(B=1, T=64 * 100 + 5, H=4, dk=128, dv=128)
+    two = 256 + 4 * 101 * 74752
+    assert L.gdr_chunk_fwd_workspace_pipelined(ctypes.byref(s), 4, ctypes.byref(n)) == 0
+    assert n.value == al(two) + al(4 * 128 * 128 * 4) + al(4 * 4)
+    assert L.gdr_chunk_fwd_workspace_pipelined(ctypes.byref(s), 0, ctypes.byref(n)) == 1
+    assert L.gdr_chunk_fwd_workspace_pipelined(ctypes.byref(s), 65, ctypes.byref(n)) == 1
+    assert L.gdr_chunk_fwd_workspace_pipelined(ctypes.byref(_shape(dtype=_binding.GDR_F32)), 2,
+                                               ctypes.byref(n)) == 2
+    assert L.gdr_chunk_fwd_workspace_pipelined(ctypes.byref(s), 2, None) == 1
+    # policy: the Gated DeltaNet-2 prefill (B*H = 32, 1024 chunks) is pipelined in 8
+    # segments; workloads whose state pass fills most SMs, that the sequence split
+    # takes, that are short or fp32 are not
+    for (B, T, H, dt), want in (((1, 65536, 32, _binding.GDR_BF16), 8),
+                                ((4, 4096, 16, _binding.GDR_BF16), 1),
+                                ((2, 16384, 32, _binding.GDR_BF16), 1),
+                                ((1, 65536, 4, _binding.GDR_BF16), 1),
+                                ((1, 2048, 8, _binding.GDR_BF16), 1),
+                                ((2, 8192, 16, _binding.GDR_BF16), 4),
+                                ((1, 65536, 32, _binding.GDR_F32), 1)):
+        shp = _shape(B=B, T=T, H=H, dk=128, dv=128, dtype=dt)
+        assert L.gdr_chunk_fwd_pipeline_segments(ctypes.byref(shp), ctypes.byref(seg)) == 0
+        assert seg.value == want, (B, T, H, dt)
+    assert L.gdr_chunk_fwd_pipeline_segments(ctypes.byref(s), None) == 1
+    assert L.gdr_chunk_fwd_pipeline_segments(ctypes.byref(_shape(dk=96)), ctypes.byref(seg)) == 2
+    # argument errors return before anything is enqueued
+    vp = ctypes.c_void_p
+
+    def call(shape, segments, ws, ws_bytes, q=FAKE, hT=None):
+        return L.gdr_chunk_fwd_pipelined(ctypes.byref(shape), segments, vp(q), *(vp(FAKE),) * 4,
+                                         None, None, None, None, vp(FAKE),
+                                         None if hT is None else vp(hT),
+                                         None if ws is None else vp(ws), ctypes.c_size_t(ws_bytes),
+                                         None, None)
+    L.gdr_chunk_fwd_workspace_pipelined(ctypes.byref(s), 4, ctypes.byref(n))
+    full = n.value
+    assert call(s, 4, FAKE, full - 1) == 4
+    assert call(s, 4, None, full) == 4
+    assert call(s, 4, FAKE + 8, full) == 4
+    assert call(s, 0, FAKE, full) == 1
+    assert call(s, 4, FAKE, full, q=None) == 1
+    assert call(s, 4, FAKE, full, hT=FAKE + 4) == 1
+    assert call(_shape(dtype=_binding.GDR_F32), 2, FAKE, full) == 2

@@ -1,0 +1,118 @@
+"""GPU parity of the pipelined forward (gdr_chunk_fwd_pipelined): time
+segments whose chunk preparation runs on the caller's stream while the state
+pass of the previous segment runs on a second stream.
+
+Bar: max|d| / max|ref| <= 2e-2 (bf16) against the float64 oracle for o and the
+final state, as for every bf16 path. The pipelined call runs the same kernels
+on the same chunks and hands the fp32 state from one segment to the next, so
+it must also equal the plain two-kernel call bit for bit.
+"""
+import pytest
+import torch
+
+import gated_delta_rule_10_gb300 as gdr
+from gated_delta_rule_10_gb300 import workloads as wl
+from tests.gdr_testutil import TOL, gpu_forward, oracle_forward, rel_err, select, to_dev
+
+pytestmark = pytest.mark.gpu
+
+BAR = TOL[torch.bfloat16]
+
+
+def pipe_forward(x, segments, output_final_state=True, aux=None):
+    d = to_dev(x)
+    shape = gdr.make_shape(*d["q"].shape, d["v"].shape[-1], d["q"].dtype, x["flags"], x["scale"])
+    ws = torch.empty(gdr.chunk_fwd_pipelined_workspace_bytes(shape, segments), dtype=torch.uint8,
+                     device="cuda")
+    o, hT = gdr.chunk_fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], d["lam"], d["b"], d["w"],
+                          d["h0"], scale=x["scale"], flags=x["flags"], workspace=ws,
+                          pipeline=segments, aux=aux, output_final_state=output_final_state)
+    gdr.chunk_fwd_check(ws)
+    return o, hT
+
+
+def check(x, segments, **kw):
+    o, hT = pipe_forward(x, segments, **kw)
+    torch.cuda.synchronize()
+    ro, rh = oracle_forward(x)
+    eo = rel_err(o.float().cpu(), ro)
+    assert eo <= BAR, eo
+    if hT is not None:
+        eh = rel_err(hT.cpu(), rh)
+        assert eh <= BAR, eh
+    # the plain two-kernel path on the same inputs, bit for bit
+    o2, h2 = gpu_forward(x)
+    torch.cuda.synchronize()
+    assert torch.equal(o, o2)
+    if hT is not None:
+        assert torch.equal(hT, h2)
+
+
+@pytest.mark.parametrize("segments", [2, 3, 7])
+@pytest.mark.parametrize("variant", ["gdn", "qdelta", "kda", "gdn2", "vbeta"])
+def test_pipelined_every_variant(variant, segments):
+    x = wl.make_inputs(variant, 1, 64 * 20 + 17, 2, 128, 128, torch.bfloat16, seed=segments,
+                       h0_std=0.02)
+    check(x, segments)
+
+
+@pytest.mark.parametrize("flags", range(16))
+def test_pipelined_every_flag_combination(flags):
+    x = wl.make_inputs(flags, 2, 64 * 6 + 5, 2, 128, 64, torch.bfloat16, seed=400 + flags,
+                       h0_std=0.05)
+    check(x, 3)
+
+
+@pytest.mark.parametrize("dk,dv", [(64, 64), (64, 128), (128, 64)])
+def test_pipelined_widths(dk, dv):
+    x = wl.make_inputs("gdn2", 2, 64 * 9 + 1, 3, dk, dv, torch.bfloat16, seed=dk + dv,
+                       h0_std=0.05)
+    check(x, 4)
+
+
+def test_pipelined_more_segments_than_chunks_and_no_states():
+    x = wl.make_inputs("kda", 1, 130, 2, 128, 128, torch.bfloat16, seed=9)
+    assert x["h0"] is None
+    check(x, 8)                                    # 3 chunks: 3 segments
+    o, hT = pipe_forward(x, 8, output_final_state=False)
+    assert hT is None
+
+
+def test_pipelined_on_one_stream():
+    """aux = the caller's stream: the launches run in order, same result."""
+    x = wl.make_inputs("gdn", 1, 64 * 12, 4, 128, 128, torch.bfloat16, seed=12, h0_std=0.02)
+    check(x, 4, aux=torch.cuda.current_stream())
+
+
+def test_pipelined_many_claims_per_segment():
+    """Segments of 75 chunks over 8 sequences: 600 work items per preparation
+    launch, claimed eight at a time; sampled sequences against the oracle and
+    the whole output against the plain path."""
+    B, H, T = 2, 4, 64 * 300
+    x = wl.make_inputs("gdn2", B, T, H, 128, 128, torch.bfloat16, seed=31, h0_std=0.02)
+    o, hT = pipe_forward(x, 4)
+    o2, h2 = gpu_forward(x)
+    torch.cuda.synchronize()
+    assert torch.equal(o, o2) and torch.equal(hT, h2)
+    for b, h in [(0, 0), (1, 3)]:
+        xs = select(x, batches=[b], heads=[h])
+        ro, rh = oracle_forward(xs)
+        eo = rel_err(o[b:b + 1, :, h:h + 1].float().cpu(), ro)
+        eh = rel_err(hT[b:b + 1, h:h + 1].cpu(), rh)
+        assert eo <= BAR and eh <= BAR, (b, h, eo, eh)
+
+
+def test_default_policy_pipelines_the_gdn2_prefill():
+    """The Gated DeltaNet-2 prefill (1 x 65536 x 32 x 128) at full size goes
+    through the pipelined path by default (no workspace given) and equals the
+    plain two-kernel path, which the full-size parity test checks against the
+    oracle."""
+    x = wl.config_inputs(5)
+    d = to_dev(x)
+    shape = gdr.make_shape(*d["q"].shape, d["v"].shape[-1], d["q"].dtype, x["flags"], x["scale"])
+    assert gdr.pipeline_segments(shape) == 8
+    o, hT = gdr.chunk_fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], d["lam"], d["b"], d["w"],
+                          d["h0"], scale=x["scale"], flags=x["flags"])
+    o2, h2 = gpu_forward(x)
+    torch.cuda.synchronize()
+    assert torch.equal(o, o2) and torch.equal(hT, h2)
