@@ -67,6 +67,23 @@ def dist_env():
     return rank, world, local
 
 
+def max_over_ranks(x, device=None):
+    """The largest of a per-rank value over all ranks of the process group (the
+    slowest rank's time); x itself without a group or with one rank."""
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return float(x)
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_value(units_per_rank_step, steps, world, total_ms):
+    """Units per second of the whole job: each of `world` ranks ran `steps` steps
+    of `units_per_rank_step` units, the slowest in `total_ms` milliseconds."""
+    return units_per_rank_step * steps * world / (total_ms / 1e3)
+
+
 def peaks():
     try:
         with open(PEAKS_FILE) as f:
@@ -244,16 +261,12 @@ def run_ours(args):
     chunk_ms = [ev[i][0].elapsed_time(ev[i][1]) for i in range(K)]
     dec_ms = [ev[i][1].elapsed_time(ev[i][2]) for i in range(K)]
     step_ms = [a + b for a, b in zip(chunk_ms, dec_ms)]
-    total_ms = sum(step_ms)
-    if world > 1:
-        t = torch.tensor([total_ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = max_over_ranks(sum(step_ms), device=dev)
 
     th_prefill = B * T * H
     th_decode = N * H * (args.decode_steps if has_decode else 0)
     th_step = th_prefill + th_decode
-    value = th_step * K * world / (total_ms / 1e3)
+    value = whole_job_value(th_step, K, world, total_ms)
 
     # roofline of the dominant kernel (the chunked forward), algorithmic bytes
     pk, pk_kind = peaks()
