@@ -55,6 +55,26 @@ __device__ __forceinline__ void store_tile(float* D, int ld, int r0, int n0, con
   D[(r + 8) * ld + n + 1] = sign * c[3];
 }
 
+// Column `lane` (< 16) of the inverse of the unit lower-triangular diagonal
+// block I + T[base.., base..] (16 x 16, T strictly lower in a [..][65] fp32
+// array) by forward substitution, right-looking: once col[j] is known it is
+// folded into the running sums of every later row, so each row's sum takes its
+// terms in the same order (j = 0, 1, ...) as a row-by-row dot product, and the
+// result is the same to the bit, but a row waits only for the one update that
+// its predecessor adds, not for a whole dot product.
+__device__ __forceinline__ void diag_block_column(const float* sT, int base, int lane,
+                                                  float (&col)[16]) {
+  float acc[16];
+#pragma unroll
+  for (int r = 0; r < 16; ++r) acc[r] = 0.f;
+#pragma unroll
+  for (int j = 0; j < 16; ++j) {
+    col[j] = (j == lane ? 1.f : 0.f) - acc[j];
+#pragma unroll
+    for (int r = j + 1; r < 16; ++r) acc[r] = fmaf(sT[(base + r) * 65 + base + j], col[j], acc[r]);
+  }
+}
+
 // T: [64][65] fp32 (zeros on and above the diagonal); A: [64][65] fp32 out
 // (blocks above the diagonal are left undefined); scratch: 4 x 256 floats.
 // `w` is the warp index within the warpgroup, `sync` a barrier over it.
@@ -64,13 +84,7 @@ __device__ __forceinline__ void invert_unit_lower_64(const float* sT, float* sAf
   if (lane < 16) {
     const int base = w * 16;
     float col[16];
-#pragma unroll
-    for (int r = 0; r < 16; ++r) {
-      float acc = 0.f;
-#pragma unroll
-      for (int i = 0; i < r; ++i) acc += sT[(base + r) * 65 + base + i] * col[i];
-      col[r] = (r == lane ? 1.f : 0.f) - acc;
-    }
+    diag_block_column(sT, base, lane, col);
 #pragma unroll
     for (int r = 0; r < 16; ++r) sAf[(base + r) * 65 + base + lane] = col[r];
   }
@@ -129,13 +143,7 @@ __device__ __forceinline__ void invert_unit_lower_64_w8(const float* sT, float* 
     if (lane < 16) {
       const int base = w * 16;
       float col[16];
-#pragma unroll
-      for (int r = 0; r < 16; ++r) {
-        float acc = 0.f;
-#pragma unroll
-        for (int i = 0; i < r; ++i) acc += sT[(base + r) * 65 + base + i] * col[i];
-        col[r] = (r == lane ? 1.f : 0.f) - acc;
-      }
+      diag_block_column(sT, base, lane, col);
 #pragma unroll
       for (int r = 0; r < 16; ++r) sAf[(base + r) * 65 + base + lane] = col[r];
     }
