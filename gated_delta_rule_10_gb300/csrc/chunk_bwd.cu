@@ -279,7 +279,7 @@ __device__ __forceinline__ size_t chunk_id(const BwdPtrs& p, int bb, int h, int 
 
 // ---------------------------------------------------------------- 1. records
 template <typename T>
-__global__ void __launch_bounds__(kBwdThreads) bwd_chunk_prep(const BwdPtrs p) {
+__global__ void __launch_bounds__(kBwdThreads, 3) bwd_chunk_prep(const BwdPtrs p) {
   const Rec R{p.dk, p.dv};
   const int cid = blockIdx.x;
   const int n = cid % p.Nc, bh = cid / p.Nc, h = bh % p.H, bb = bh / p.H;
@@ -881,7 +881,7 @@ struct Scr {
 };
 
 template <typename T>
-__global__ void __launch_bounds__(kBwdThreads) bwd_chunk_grad(const BwdPtrs p) {
+__global__ void __launch_bounds__(kBwdThreads, 3) bwd_chunk_grad(const BwdPtrs p) {
   const Rec R{p.dk, p.dv};
   const Scr Q{p.dk, p.dv};
   const int cid = blockIdx.x;
