@@ -54,6 +54,8 @@ def parse():
                    help="skip the sequence-split measurement")
     p.add_argument("--no-backward", action="store_true",
                    help="skip the backward measurement")
+    p.add_argument("--no-pipelined", action="store_true",
+                   help="skip the long-sequence (pipelined call) measurement")
     p.add_argument("--pipeline", type=int, default=None,
                    help="time segments of the pipelined forward (default: the library's "
                         "recommendation for the workload; 1: the plain call)")
@@ -98,7 +100,7 @@ def peaks():
 # and chunk_scan_kernel), per workload, with the hash of the kernel sources they
 # were taken on: a changed kernel reports null traffic until it is profiled
 # again. Source: profiles/chunk_fwd_two_kernel_gdn_b4_t4096_h16_d128.md.
-TRAFFIC = {2: {"bytes": 813.7e6, "sources": "e71442f92e0cf5a2"}}
+TRAFFIC = {2: {"bytes": 813.7e6, "sources": "0c586e4b8c24e85b"}}
 KERNEL_SOURCES = ("chunk_prep.cu", "chunk_scan.cu", "packet.h", "tc.cuh", "tri_inverse.cuh",
                   "common.cuh")
 
@@ -309,6 +311,8 @@ def run_ours(args):
     value_beta_info = None if args.no_value_beta else measure_value_beta(gdr, dev, stream, flush,
                                                                          K, pk, clk)
     split_info = None if args.no_split else measure_split(gdr, dev, stream, flush, K, pk)
+    pipe_info = None if args.no_pipelined else measure_pipelined(gdr, dev, stream, flush,
+                                                                 min(K, 10), pk)
     backward_info = None if args.no_backward else measure_backward(gdr, xd, c, dev, stream, flush,
                                                                    min(K, 10), pk, clk)
 
@@ -330,6 +334,7 @@ def run_ours(args):
         "epilogue": epilogue_info,
         "value_beta": value_beta_info,
         "sequence_split": split_info,
+        "pipelined": pipe_info,
         "backward": backward_info,
         # this library's kernels per timed step: the two-kernel chunked forward
         # (bf16 with the full workspace) or one fused kernel (fp32), then the
@@ -481,6 +486,49 @@ def measure_split(gdr, dev, stream, flush, K, pk, H=4):
                                     ) if ws.numel() > plain else 1
     out["launches_per_call"] = {"split": 4, "one_run": 2}
     out["l2"] = "flushed before every call"
+    return out
+
+
+def measure_pipelined(gdr, dev, stream, flush, K, pk):
+    """The Gated DeltaNet-2 prefill (1 x 65536 x 32 x 128 bf16: B * H = 32, the
+    state pass on 64 SMs) through the plain call and through the pipelined call
+    with the library's recommended time segments, K calls each, L2 flushed
+    before every call, CUDA events on the launching stream."""
+    x = wl.config_inputs(5)
+    x = {k: (v.to(dev) if torch.is_tensor(v) else v) for k, v in x.items()}
+    B, T, H, dk = x["q"].shape
+    dv = x["v"].shape[-1]
+    shape = gdr.make_shape(B, T, H, dk, dv, x["q"].dtype, x["flags"], x["scale"])
+    o = torch.empty(B, T, H, dv, dtype=x["q"].dtype, device=dev)
+    hT = torch.empty(B, H, dk, dv, dtype=torch.float32, device=dev)
+    seg = gdr.pipeline_segments(shape)
+    nbytes = tensor_bytes(x["q"], x["k"], x["v"], x["g"], x["beta"], x["lam"], x["b"], x["w"],
+                          x["h0"], o, hT)
+    out = {"workload": "gdn2_bf16_b1_t65536_h32_d128", "segments": seg, "launches": K,
+           "algorithmic_bytes_per_call": nbytes, "l2": "flushed before every call"}
+    for name, pipe in (("plain", 1), ("pipelined", seg)):
+        ws = torch.empty(gdr.chunk_fwd_pipelined_workspace_bytes(shape, pipe) if pipe > 1
+                         else gdr.chunk_fwd_workspace_bytes(shape), dtype=torch.uint8, device=dev)
+
+        def call():
+            gdr.chunk_fwd(x["q"], x["k"], x["v"], x["g"], x["beta"], x["lam"], x["b"], x["w"],
+                          x["h0"], scale=x["scale"], flags=x["flags"], o=o, hT=hT, workspace=ws,
+                          pipeline=pipe)
+        for _ in range(2):
+            call()
+        ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(K)]
+        torch.cuda.synchronize()
+        for i in range(K):
+            flush.fill_(float(i))
+            ev[i][0].record(stream)
+            call()
+            ev[i][1].record(stream)
+        torch.cuda.synchronize()
+        ms = statistics.mean(ev[i][0].elapsed_time(ev[i][1]) for i in range(K))
+        gbs = nbytes / (ms / 1e3) / 1e9
+        out[name] = {"ms_mean": round(ms, 4), "token_heads_per_s": round(B * T * H / (ms / 1e3), 1),
+                     "achieved_gbs": round(gbs, 1), "frac_hbm": round(gbs / pk["hbm_gbs"], 4)}
+        del ws
     return out
 
 
