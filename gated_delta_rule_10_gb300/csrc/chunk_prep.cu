@@ -69,7 +69,35 @@ struct PrepLayout {
   static constexpr uint32_t kTmemCols = (DK + DV) > 128 ? 256 : 128;
 };
 
-enum : uint32_t { kBarV = 0, kBarK = 1, kBarM1 = 2, kBarM2 = 3 };
+// Scalar gates without QMIX (the lean variant, three CTAs per SM): the [K; Q]
+// tiles (256 d_k bytes) until M1 completes, then inside that region T inverted
+// in place into A (fp32 [64][65]), the inverse's scratch and the bf16 A tile;
+// v and E_abs after it. 128 TMEM columns: M1, then M2 as two groups, U = A v
+// and Y = A E_abs, each read out before the next.
+template <int DK, int DV>
+struct LeanLayout {
+  static constexpr uint32_t oEQ = 0;
+  static constexpr uint32_t oT = 0;                          // T, then A in place
+  static constexpr uint32_t oAf = oT;
+  static constexpr uint32_t oP = 64 * 65 * 4;                // [4][128] per-warp scratch
+  static constexpr uint32_t oX = oP + 4 * 128 * 4;           // [32][33] inverse scratch
+  static constexpr uint32_t oA = align1k(oX + 32 * 33 * 4);  // A 64 x 64 (A, K-major)
+  static constexpr uint32_t kR1 = align1k(cmax(256 * DK, oA + 8192));
+  static constexpr uint32_t oK = 256 * DK;                   // (not used: k sits in the E slot)
+  static constexpr uint32_t oV = kR1;                        // K=64 x DV (B, MN-major)
+  static constexpr uint32_t oEa = oV + 128 * DV;             // K=64 x DK (B, MN-major)
+  static constexpr uint32_t oPart = oP;                      // (channel gates only: not used)
+  static constexpr uint32_t oVec = oEa + 128 * DK;
+  static constexpr uint32_t oBar = oVec + 6 * 64 * 4 + 16;   // 5 mbarriers (after a flag word)
+  static constexpr uint32_t oSlot = oBar + 48;
+  static constexpr uint32_t bytes = oSlot + 16;
+  static constexpr uint32_t launch_bytes = bytes + 1024;
+  static constexpr uint32_t kTmemCols = 128;
+  static_assert(oX + 32 * 33 * 4 <= oA && oA + 8192 <= kR1 && 256 * DK <= kR1, "region 1");
+  static_assert(oEa + 128 * DK == oVec && oV % 1024 == 0 && oEa % 1024 == 0, "v and E_abs");
+};
+
+enum : uint32_t { kBarV = 0, kBarK = 1, kBarM1 = 2, kBarM2 = 3, kBarM2b = 4 };
 
 __device__ __forceinline__ uint4 pack8(const float* x) {
   uint4 u;
@@ -211,11 +239,11 @@ __device__ __forceinline__ void prep_keys(unsigned char* smem, unsigned char* pk
 // loaded and only three tiles are formed per element: E_abs' = e^{G_r} x_r
 // (x = k, or k + lam q), Q_gamma and K_tail (packet). k sits in the E slot;
 // under QMIX x replaces it there and k moves to the K slot.
-template <int DK, int DV, bool QM>
+template <int DK, int DV, bool QM, typename L = PrepLayout<DK, DV>>
 __device__ __forceinline__ void prep_keys_scalar(unsigned char* smem, unsigned char* pkt,
                                                  const ChunkArgs& a, const float* sLam,
                                                  const float* sEG, const float* sEGL) {
-  using L = PrepLayout<DK, DV>;
+  static_assert(!QM || L::oK + 128 * DK <= L::oV, "the K slot exists");
   using P = Packet<DK, DV>;
   constexpr int VK = DK / 8, RB = kThreads / VK, RPB = 64 / RB;
   const int tid = threadIdx.x, rb = tid / VK, c0 = (tid % VK) * 8, r0 = rb * RPB;
@@ -327,17 +355,18 @@ __device__ __forceinline__ void prep_z(unsigned char* smem, const float* sBeta) 
   }
 }
 
-template <int DK, int DV, bool SC, bool VB, bool DYN>
-__global__ void __launch_bounds__(kThreads, 2)
+template <int DK, int DV, bool SC, bool VB, bool DYN, bool LEAN>
+__global__ void __launch_bounds__(kThreads, LEAN ? 3 : 2)
     chunk_prep_kernel(const ChunkArgs a, const __grid_constant__ CUtensorMap tm_q,
                       const __grid_constant__ CUtensorMap tm_k,
                       const __grid_constant__ CUtensorMap tm_v,
                       const __grid_constant__ CUtensorMap tm_b,
                       const __grid_constant__ CUtensorMap tm_w, unsigned char* packets,
                       int* status, const PrepRange rg) {
-  using L = PrepLayout<DK, DV>;
+  using L = std::conditional_t<LEAN, LeanLayout<DK, DV>, PrepLayout<DK, DV>>;
   using P = std::conditional_t<VB, PacketVB<DK, DV>, Packet<DK, DV>>;
   static_assert(!VB || SC, "the value-channel packets take the scalar-gate tiles");
+  static_assert(!LEAN || (SC && !VB), "the lean variant is for scalar gates");
   extern __shared__ unsigned char smem_raw[];
   unsigned char* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   const uint32_t sbase = smem_u32(smem);
@@ -365,7 +394,7 @@ __global__ void __launch_bounds__(kThreads, 2)
 
   if (warp == 0) tc::tmem_alloc(smem_u32(tslot), L::kTmemCols);
   if (tid == 32) {
-    for (uint32_t i = 0; i < 4; ++i) tc::mbar_init(bar(i), 1);
+    for (uint32_t i = 0; i < (LEAN ? 5u : 4u); ++i) tc::mbar_init(bar(i), 1);
     tc::fence_mbar_init();
   }
   tc::fence_before_sync();
@@ -558,10 +587,14 @@ __global__ void __launch_bounds__(kThreads, 2)
     if (VB) {
       prep_keys_vb<DK, DV>(smem, pkt, a, sEG, sEGL);
     } else if (SC) {
-      if (QM)
-        prep_keys_scalar<DK, DV, true>(smem, pkt, a, sLam, sEG, sEGL);
-      else
-        prep_keys_scalar<DK, DV, false>(smem, pkt, a, sLam, sEG, sEGL);
+      if constexpr (LEAN) {   // no QMIX: the lean layout has no K slot
+        prep_keys_scalar<DK, DV, false, L>(smem, pkt, a, sLam, sEG, sEGL);
+      } else {
+        if (QM)
+          prep_keys_scalar<DK, DV, true, L>(smem, pkt, a, sLam, sEG, sEGL);
+        else
+          prep_keys_scalar<DK, DV, false, L>(smem, pkt, a, sLam, sEG, sEGL);
+      }
     } else switch (a.flags & 11u) {   // CH | ER | QM select the key-side tiles
 #define GDR_PREP(F)                                                                       \
   case F:                                                                                 \
@@ -649,8 +682,13 @@ __global__ void __launch_bounds__(kThreads, 2)
     }
 
     // ---- A = (I + T)^{-1} (all 8 warps), then the bf16 operand tile ----
-    invert_unit_lower_64_w8(sT, sAf, sP, reinterpret_cast<float*>(smem + L::oX), warp, lane,
-                            [] { tc::named_sync(kInvBar, 128); }, [] { __syncthreads(); });
+    if constexpr (LEAN)
+      invert_unit_lower_64_w8_inplace(sT, sP, reinterpret_cast<float*>(smem + L::oX), warp, lane,
+                                      [] { tc::named_sync(kInvBar, 128); },
+                                      [] { __syncthreads(); });
+    else
+      invert_unit_lower_64_w8(sT, sAf, sP, reinterpret_cast<float*>(smem + L::oX), warp, lane,
+                              [] { tc::named_sync(kInvBar, 128); }, [] { __syncthreads(); });
 #pragma unroll
     for (int u = 0; u < 2; ++u) {
       const int it = tid + u * kThreads, r = it >> 3, c0 = (it & 7) * 8;
@@ -666,11 +704,77 @@ __global__ void __launch_bounds__(kThreads, 2)
     tc::fence_proxy_async();
     __syncthreads();
     // T and A are consumed: the key-side tiles of the next chunk may land now
-    if (wn < total) {
+    // (lean variant: the A tile sits in their region, so after M2)
+    if (!LEAN && wn < total) {
       if (tid == 64) load_keys(wn, wa);
       ++k_issued;
     }
 
+    if constexpr (LEAN) {
+      // ---- M2 in two groups within 128 TMEM columns: U = A Z (N = DV), read
+      // out, then Y = A E_abs (N = DK), read out ----
+      const uint64_t dA = tc::smem_desc(sbase + L::oA, 16, 1024);
+      // M=64 accumulators: row 16 q + l in lane l < 16 of quadrant q; warp w
+      // takes quadrant w % 4 and half w / 4 of the columns
+      const int q = warp & 3, half = warp >> 2;
+      const int r = 16 * q + (lane & 15);
+      const uint32_t tl = tmem + (static_cast<uint32_t>(32 * q) << 16);
+      if (tid == 0) {
+        tc::fence_after_sync();
+        constexpr uint32_t idu = tc::idesc_bf16(64, DV, 0, 1);
+        const uint64_t dZ = tc::smem_desc(sbase + L::oV, 64 * 128, 1024);
+#pragma unroll
+        for (int k0 = 0; k0 < 64; k0 += 16)
+          tc::mma_bf16(tmem, dA + ((k0 * 2) >> 4), dZ + (((k0 / 8) * 1024) >> 4), idu, k0 > 0);
+        tc::commit(bar(kBarM2));
+      }
+      if (__syncthreads_or(!tc::mbar_wait(bar(kBarM2), par))) { fail_at = 4 * n + 2; break; }
+      tc::fence_after_sync();
+      // v is consumed: the value-side tiles of the next chunk may land now
+      if (wn < total) {
+        if (tid == 64) load_values(wn, wa);
+        ++v_issued;
+      }
+#pragma unroll
+      for (int c = half * (DV / 2); c < (half + 1) * (DV / 2); c += 32) {
+        float x[32];
+        tc::tmem_ld32(tl + c, x);
+        if (lane < 16) {
+#pragma unroll
+          for (int j = 0; j < 32; j += 8) st16(pkt, P::oU + tc::tile_off(64, r, c + j), pack8(x + j));
+        }
+      }
+      tc::fence_before_sync();
+      __syncthreads();   // U is read out: the columns take Y
+      if (tid == 0) {
+        tc::fence_after_sync();
+        constexpr uint32_t idy = tc::idesc_bf16(64, DK, 0, 1);
+        const uint64_t dE = tc::smem_desc(sbase + L::oEa, 64 * 128, 1024);
+#pragma unroll
+        for (int k0 = 0; k0 < 64; k0 += 16)
+          tc::mma_bf16(tmem, dA + ((k0 * 2) >> 4), dE + (((k0 / 8) * 1024) >> 4), idy, k0 > 0);
+        tc::commit(bar(kBarM2b));
+      }
+      if (__syncthreads_or(!tc::mbar_wait(bar(kBarM2b), par))) { fail_at = 4 * n + 3; break; }
+      tc::fence_after_sync();
+      // the A tile and E_abs are consumed: the key-side tiles of the next chunk may land now
+      if (wn < total) {
+        if (tid == 64) load_keys(wn, wa);
+        ++k_issued;
+      }
+#pragma unroll
+      for (int c = half * (DK / 2); c < (half + 1) * (DK / 2); c += 32) {
+        float x[32];
+        tc::tmem_ld32(tl + c, x);
+#pragma unroll
+        for (int j = 0; j < 32; ++j) x[j] = -x[j];
+        if (lane < 16) {
+#pragma unroll
+          for (int j = 0; j < 32; j += 8)
+            st16(pkt, P::oQY + tc::tile_off(128, 64 + r, c + j), pack8(x + j));
+        }
+      }
+    } else {
     // ---- M2: [U | Y] = A [Z | E_abs] (N = DV + DK): U in columns 0..DV-1,
     // Y in columns DV..DV+DK-1 ----
     if (tid == 0) {
@@ -718,6 +822,7 @@ __global__ void __launch_bounds__(kThreads, 2)
         }
       }
     }
+    }   // !LEAN
     // the next chunk reuses every shared tile and the tensor memory
     tc::fence_before_sync();
     __syncthreads();
@@ -741,11 +846,12 @@ __global__ void __launch_bounds__(kThreads, 2)
   if (warp == 0) tc::tmem_dealloc(tmem, L::kTmemCols);
 }
 
-template <int DK, int DV, bool SC, bool VB, bool DYN>
+template <int DK, int DV, bool SC, bool VB, bool DYN, bool LEAN = false>
 cudaError_t launch_prep_kernel(const ChunkArgs& a, unsigned char* packets, int* status,
                                const PrepRange& rg, cudaStream_t stream) {
-  using L = PrepLayout<DK, DV>;
-  static_assert(2 * (L::launch_bytes + 1024) <= 233472, "two CTAs per SM");
+  using L = std::conditional_t<LEAN, LeanLayout<DK, DV>, PrepLayout<DK, DV>>;
+  constexpr int kPerSm = LEAN ? 3 : 2;
+  static_assert(kPerSm * (L::launch_bytes + 1024) <= 233472, "CTAs per SM");
   CUtensorMap tq, tk, tv, tb, tw;
   if (!make_bthd_tmap(&tq, a.q, a.B, a.T, a.H, DK) || !make_bthd_tmap(&tk, a.k, a.B, a.T, a.H, DK) ||
       !make_bthd_tmap(&tv, a.v, a.B, a.T, a.H, DV))
@@ -754,10 +860,14 @@ cudaError_t launch_prep_kernel(const ChunkArgs& a, unsigned char* packets, int* 
   tw = tq;
   if ((a.flags & 2u) && !make_bthd_tmap(&tb, a.b, a.B, a.T, a.H, DK)) return cudaErrorInvalidValue;
   if ((a.flags & 4u) && !make_bthd_tmap(&tw, a.w, a.B, a.T, a.H, DV)) return cudaErrorInvalidValue;
-  auto kern = chunk_prep_kernel<DK, DV, SC, VB, DYN>;
+  auto kern = chunk_prep_kernel<DK, DV, SC, VB, DYN, LEAN>;
   cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(L::launch_bytes));
   if (err != cudaSuccess) return err;
+  if (LEAN &&   // three CTAs' shared memory needs the largest carve-out
+      (err = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                  static_cast<int>(cudaSharedmemCarveoutMaxShared))) != cudaSuccess)
+    return err;
   // persistent: two CTAs per SM walk the B * H * ceil(T / 64) chunks
   int dev = 0, sms = 0;
   if ((err = cudaGetDevice(&dev)) != cudaSuccess) return err;
@@ -767,7 +877,7 @@ cudaError_t launch_prep_kernel(const ChunkArgs& a, unsigned char* packets, int* 
   const int rc = rg.chunks > 0 ? rg.chunks : n_chunks - rg.chunk0;
   if (rg.chunk0 < 0 || rc < 1 || rg.chunk0 + rc > n_chunks) return cudaErrorInvalidValue;
   const long long total = static_cast<long long>(rc) * a.B * a.H;
-  long long grid = total < 2LL * sms ? total : 2LL * sms;
+  long long grid = total < 1LL * kPerSm * sms ? total : 1LL * kPerSm * sms;
   if (DYN != (rg.counter != nullptr)) return cudaErrorInvalidValue;
   if (DYN) {   // claimed work: enough CTAs of at most per_cta items each
     if (rg.per_cta < 1) return cudaErrorInvalidValue;
@@ -783,6 +893,8 @@ cudaError_t launch_prep(const ChunkArgs& a, unsigned char* packets, int* status,
                         const PrepRange& rg, cudaStream_t stream) {
   if (a.flags & 16u)
     return launch_prep_kernel<DK, DV, true, true, DYN>(a, packets, status, rg, stream);
+  if ((a.flags & 15u) == 0)   // scalar gates without QMIX: three CTAs per SM
+    return launch_prep_kernel<DK, DV, true, false, DYN, true>(a, packets, status, rg, stream);
   if ((a.flags & 7u) == 0)
     return launch_prep_kernel<DK, DV, true, false, DYN>(a, packets, status, rg, stream);
   return launch_prep_kernel<DK, DV, false, false, DYN>(a, packets, status, rg, stream);

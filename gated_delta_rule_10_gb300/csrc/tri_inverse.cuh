@@ -176,4 +176,53 @@ __device__ __forceinline__ void invert_unit_lower_64_w8(const float* sT, float* 
   sync8();
 }
 
+// invert_unit_lower_64_w8 in place: sA ([64][65] fp32, shared) holds T on
+// entry and A on exit. A block of A overwrites the block of T at its place only
+// once every read of that T block is done: within the warp for the diagonal
+// blocks, over warps 0-3 for the 16-row level; the 32-row level writes after the
+// barrier that ends its reads of T. sP: per-warp 16 x 8 scratch (4 x 128
+// floats); sX: [32][33] floats.
+template <typename Sync4, typename Sync8>
+__device__ __forceinline__ void invert_unit_lower_64_w8_inplace(float* sA, float* sP, float* sX,
+                                                                int w, int lane, Sync4 sync4,
+                                                                Sync8 sync8) {
+  if (w < 4) {
+    if (lane < 16) {
+      const int base = w * 16;
+      float col[16];
+      diag_block_column(sA, base, lane, col);
+      __syncwarp(0x0000ffffu);                     // every lane has read its rows of T_JJ
+#pragma unroll
+      for (int r = 0; r < 16; ++r) sA[(base + r) * 65 + base + lane] = col[r];
+    }
+    sync4();
+    float* sY = sP + w * 128;
+    const int I = w < 2 ? 1 : 3, J = I - 1, n0 = 16 * J + 8 * (w & 1);
+    float c[4] = {0.f, 0.f, 0.f, 0.f};
+    mma16x8x16_f32(c, sA, 65, 16 * I, 16 * J, sA, 65, 16 * J, n0);
+    store_tile(sY, 8, 0, 0, c, -1.f);              // -T_IJ Dinv_J
+    __syncwarp();
+    float d[4] = {0.f, 0.f, 0.f, 0.f};
+    mma16x8x16_f32(d, sA, 65, 16 * I, 16 * I, sY, 8, 0, 0);
+    sync4();                                       // both warps of block (I, J) have read T_IJ
+    store_tile(sA, 65, 16 * I, n0, d, 1.f);        // A_IJ
+  }
+  sync8();
+  const int r0 = 32 + 16 * (w >> 2), n0 = 8 * (w & 3);
+  {
+    float c[4] = {0.f, 0.f, 0.f, 0.f};
+    if (n0 < 16) mma16x8x16_f32(c, sA, 65, r0, 0, sA, 65, 0, n0);
+    mma16x8x16_f32(c, sA, 65, r0, 16, sA, 65, 16, n0);
+    store_tile(sX, 33, r0 - 32, n0, c, -1.f);
+  }
+  sync8();
+  {
+    float d[4] = {0.f, 0.f, 0.f, 0.f};
+    mma16x8x16_f32(d, sA, 65, r0, 32, sX, 33, 0, n0);
+    if (r0 == 48) mma16x8x16_f32(d, sA, 65, r0, 48, sX, 33, 16, n0);
+    store_tile(sA, 65, r0, n0, d, 1.f);
+  }
+  sync8();
+}
+
 }  // namespace gdr
