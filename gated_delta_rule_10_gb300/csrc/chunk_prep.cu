@@ -69,11 +69,12 @@ struct PrepLayout {
   static constexpr uint32_t kTmemCols = (DK + DV) > 128 ? 256 : 128;
 };
 
-// Scalar gates without QMIX (the lean variant, three CTAs per SM): the [K; Q]
-// tiles (256 d_k bytes) until M1 completes, then inside that region T inverted
-// in place into A (fp32 [64][65]), the inverse's scratch and the bf16 A tile;
-// v and E_abs after it. 128 TMEM columns: M1, then M2 as two groups, U = A v
-// and Y = A E_abs, each read out before the next.
+// Scalar gates (the lean variant, three CTAs per SM): the [E; Q] tiles (256 d_k
+// bytes) until M1 completes, then inside that region T inverted in place into A
+// (fp32 [64][65]), the inverse's scratch and the bf16 A tile; then one slot
+// that holds k until M1 completes under QMIX (x = k + lam q takes the E slot)
+// and v after it, and E_abs. 128 TMEM columns: M1, then M2 as two groups,
+// U = A v and Y = A E_abs, each read out before the next.
 template <int DK, int DV>
 struct LeanLayout {
   static constexpr uint32_t oEQ = 0;
@@ -83,9 +84,11 @@ struct LeanLayout {
   static constexpr uint32_t oX = oP + 4 * 128 * 4;           // [32][33] inverse scratch
   static constexpr uint32_t oA = align1k(oX + 32 * 33 * 4);  // A 64 x 64 (A, K-major)
   static constexpr uint32_t kR1 = align1k(cmax(256 * DK, oA + 8192));
-  static constexpr uint32_t oK = 256 * DK;                   // (not used: k sits in the E slot)
+  // one slot for k (QMIX: the B operand of M1, until M1 completes) and then v
   static constexpr uint32_t oV = kR1;                        // K=64 x DV (B, MN-major)
-  static constexpr uint32_t oEa = oV + 128 * DV;             // K=64 x DK (B, MN-major)
+  static constexpr uint32_t oK = oV;                         // 64 x DK (QMIX only)
+  static constexpr uint32_t kKV = 128 * cmax(DK, DV);
+  static constexpr uint32_t oEa = oV + kKV;                  // K=64 x DK (B, MN-major)
   static constexpr uint32_t oPart = oP;                      // (channel gates only: not used)
   static constexpr uint32_t oVec = oEa + 128 * DK;
   static constexpr uint32_t oBar = oVec + 6 * 64 * 4 + 16;   // 5 mbarriers (after a flag word)
@@ -95,6 +98,7 @@ struct LeanLayout {
   static constexpr uint32_t kTmemCols = 128;
   static_assert(oX + 32 * 33 * 4 <= oA && oA + 8192 <= kR1 && 256 * DK <= kR1, "region 1");
   static_assert(oEa + 128 * DK == oVec && oV % 1024 == 0 && oEa % 1024 == 0, "v and E_abs");
+  static_assert(oK + 128 * DK <= oEa && oV + 128 * DV <= oEa, "the k / v slot");
 };
 
 enum : uint32_t { kBarV = 0, kBarK = 1, kBarM1 = 2, kBarM2 = 3, kBarM2b = 4 };
@@ -239,11 +243,12 @@ __device__ __forceinline__ void prep_keys(unsigned char* smem, unsigned char* pk
 // loaded and only three tiles are formed per element: E_abs' = e^{G_r} x_r
 // (x = k, or k + lam q), Q_gamma and K_tail (packet). k sits in the E slot;
 // under QMIX x replaces it there and k moves to the K slot.
-template <int DK, int DV, bool QM, typename L = PrepLayout<DK, DV>>
+template <int DK, int DV, bool QM, typename L = PrepLayout<DK, DV>, bool KINK = false>
 __device__ __forceinline__ void prep_keys_scalar(unsigned char* smem, unsigned char* pkt,
                                                  const ChunkArgs& a, const float* sLam,
                                                  const float* sEG, const float* sEGL) {
-  static_assert(!QM || L::oK + 128 * DK <= L::oV, "the K slot exists");
+  // KINK: k was loaded into the K slot (lean layout) and stays there
+  static_assert(!QM || KINK || L::oK + 128 * DK <= L::oV, "the K slot exists");
   using P = Packet<DK, DV>;
   constexpr int VK = DK / 8, RB = kThreads / VK, RPB = 64 / RB;
   const int tid = threadIdx.x, rb = tid / VK, c0 = (tid % VK) * 8, r0 = rb * RPB;
@@ -252,7 +257,8 @@ __device__ __forceinline__ void prep_keys_scalar(unsigned char* smem, unsigned c
     const int r = r0 + i;
     float qv[8], kv[8];
     unpack8(ld16(smem, L::oEQ + tc::tile_off(128, 64 + r, c0)), qv);
-    const uint4 kraw = ld16(smem, L::oEQ + tc::tile_off(128, r, c0));
+    const uint4 kraw = ld16(smem, KINK ? L::oK + tc::tile_off(64, r, c0)
+                                       : L::oEQ + tc::tile_off(128, r, c0));
     unpack8(kraw, kv);
     const float lam = sLam[r], eg = sEG[r], egl = sEGL[r], sq = a.scale * eg;
     float x[8], Ea[8], Qg[8], Kt[8];
@@ -265,7 +271,7 @@ __device__ __forceinline__ void prep_keys_scalar(unsigned char* smem, unsigned c
     }
     if (QM) {
       st16(smem, L::oEQ + tc::tile_off(128, r, c0), pack8(x));
-      st16(smem, L::oK + tc::tile_off(64, r, c0), kraw);
+      if (!KINK) st16(smem, L::oK + tc::tile_off(64, r, c0), kraw);
     }
     st16(smem, L::oEa + tc::tile_off(64, r, c0), pack8(Ea));
     st16(pkt, P::oQY + tc::tile_off(128, r, c0), pack8(Qg));
@@ -377,6 +383,9 @@ __global__ void __launch_bounds__(kThreads, LEAN ? 3 : 2)
   const int rc = rg.chunks > 0 ? rg.chunks : n_chunks - rg.chunk0;
   const int total = rc * B * H;
   const bool CH = a.flags & 1u, ER = a.flags & 2u, WR = a.flags & 4u, QM = a.flags & 8u;
+  // lean layout under QMIX: k in the shared k / v slot, so a chunk's v is
+  // loaded once its M1 has completed and waited for before M2
+  const bool vlate = LEAN && QM;
 
   float* sT = reinterpret_cast<float*>(smem + L::oT);
   float* sAf = reinterpret_cast<float*>(smem + L::oAf);
@@ -452,7 +461,7 @@ __global__ void __launch_bounds__(kThreads, LEAN ? 3 : 2)
 #pragma unroll
     for (int blk = 0; blk < DK / 64; ++blk) {
       tc::tma_load_4d(sbase + L::oEQ + blk * 16384 + 8192, &tm_q, blk * 64, h, n * kChunk, bb, bar(kBarK));
-      if (SC)
+      if (SC && !vlate)
         tc::tma_load_4d(sbase + L::oEQ + blk * 16384, &tm_k, blk * 64, h, n * kChunk, bb, bar(kBarK));
       else
         tc::tma_load_4d(sbase + L::oK + blk * 8192, &tm_k, blk * 64, h, n * kChunk, bb, bar(kBarK));
@@ -486,10 +495,10 @@ __global__ void __launch_bounds__(kThreads, LEAN ? 3 : 2)
   }
   if (w < total) {
     if (tid == 64) {
-      load_values(w, wn);
+      if (!vlate) load_values(w, wn);
       load_keys(w, wn);
     }
-    v_issued = 1;
+    v_issued = vlate ? 0 : 1;
     k_issued = 1;
   }
 
@@ -565,8 +574,10 @@ __global__ void __launch_bounds__(kThreads, LEAN ? 3 : 2)
     if (CH) load_channel_gates<DK>(a, row0, h, Lr, sPart, gv);
     __syncthreads();
 
-    if (__syncthreads_or(!tc::mbar_wait(bar(kBarV), par))) { fail_at = 4 * n; break; }
-    v_done = v_issued;
+    if (!vlate) {
+      if (__syncthreads_or(!tc::mbar_wait(bar(kBarV), par))) { fail_at = 4 * n; break; }
+      v_done = v_issued;
+    }
     if (VB) {
       prep_values_vb<DK, DV>(smem, pkt, a, row0, h, Lr);
       __syncthreads();   // v has been copied out: the next chunk's value tiles may land
@@ -587,8 +598,11 @@ __global__ void __launch_bounds__(kThreads, LEAN ? 3 : 2)
     if (VB) {
       prep_keys_vb<DK, DV>(smem, pkt, a, sEG, sEGL);
     } else if (SC) {
-      if constexpr (LEAN) {   // no QMIX: the lean layout has no K slot
-        prep_keys_scalar<DK, DV, false, L>(smem, pkt, a, sLam, sEG, sEGL);
+      if constexpr (LEAN) {   // under QMIX k already sits in the K slot
+        if (QM)
+          prep_keys_scalar<DK, DV, true, L, true>(smem, pkt, a, sLam, sEG, sEGL);
+        else
+          prep_keys_scalar<DK, DV, false, L>(smem, pkt, a, sLam, sEG, sEGL);
       } else {
         if (QM)
           prep_keys_scalar<DK, DV, true, L>(smem, pkt, a, sLam, sEG, sEGL);
@@ -628,6 +642,10 @@ __global__ void __launch_bounds__(kThreads, LEAN ? 3 : 2)
     }
     if (__syncthreads_or(!tc::mbar_wait(bar(kBarM1), par))) { fail_at = 4 * n + 1; break; }
     tc::fence_after_sync();
+    if (vlate) {   // M1 has read k: this chunk's v may take the slot
+      if (tid == 64) load_values(w, wn);
+      ++v_issued;
+    }
     // ---- T (fp32, shared) and A_qk (bf16, packet): warp w reads lane quadrant
     // w % 4 (quadrants 0-1: E_bar K_bar^T rows, 2-3: Q' K_bar^T rows), columns
     // 32 (w / 4) .. +31 ----
@@ -719,6 +737,10 @@ __global__ void __launch_bounds__(kThreads, LEAN ? 3 : 2)
       const int q = warp & 3, half = warp >> 2;
       const int r = 16 * q + (lane & 15);
       const uint32_t tl = tmem + (static_cast<uint32_t>(32 * q) << 16);
+      if (vlate) {
+        if (__syncthreads_or(!tc::mbar_wait(bar(kBarV), par))) { fail_at = 4 * n + 2; break; }
+        v_done = v_issued;
+      }
       if (tid == 0) {
         tc::fence_after_sync();
         constexpr uint32_t idu = tc::idesc_bf16(64, DV, 0, 1);
@@ -731,7 +753,8 @@ __global__ void __launch_bounds__(kThreads, LEAN ? 3 : 2)
       if (__syncthreads_or(!tc::mbar_wait(bar(kBarM2), par))) { fail_at = 4 * n + 2; break; }
       tc::fence_after_sync();
       // v is consumed: the value-side tiles of the next chunk may land now
-      if (wn < total) {
+      // (under QMIX after the next chunk's M1)
+      if (!vlate && wn < total) {
         if (tid == 64) load_values(wn, wa);
         ++v_issued;
       }
@@ -893,10 +916,8 @@ cudaError_t launch_prep(const ChunkArgs& a, unsigned char* packets, int* status,
                         const PrepRange& rg, cudaStream_t stream) {
   if (a.flags & 16u)
     return launch_prep_kernel<DK, DV, true, true, DYN>(a, packets, status, rg, stream);
-  if ((a.flags & 15u) == 0)   // scalar gates without QMIX: three CTAs per SM
+  if ((a.flags & 7u) == 0)   // scalar gates: three CTAs per SM
     return launch_prep_kernel<DK, DV, true, false, DYN, true>(a, packets, status, rg, stream);
-  if ((a.flags & 7u) == 0)
-    return launch_prep_kernel<DK, DV, true, false, DYN>(a, packets, status, rg, stream);
   return launch_prep_kernel<DK, DV, false, false, DYN>(a, packets, status, rg, stream);
 }
 
