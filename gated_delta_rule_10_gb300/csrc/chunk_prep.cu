@@ -6,7 +6,8 @@
 // B * H * ceil(T / 64) independent CTAs and fills the GPU even when B * H is
 // small.
 //
-// Persistent CTAs (256 threads, two per SM) walk the chunks; per chunk:
+// Persistent CTAs (256 threads; two per SM, three for scalar gates, whose lean
+// layout is described at LeanLayout) walk the chunks; per chunk:
 //   load    TMA brings the chunk's q, k, v (and b, w) tiles in: the key side as
 //           soon as the previous chunk's inverse is done with their shared
 //           memory, the value side as soon as its M2 is; the chunk after is
@@ -891,7 +892,8 @@ cudaError_t launch_prep_kernel(const ChunkArgs& a, unsigned char* packets, int* 
       (err = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout,
                                   static_cast<int>(cudaSharedmemCarveoutMaxShared))) != cudaSuccess)
     return err;
-  // persistent: two CTAs per SM walk the B * H * ceil(T / 64) chunks
+  // persistent: two CTAs per SM (three for the lean layout) walk the B * H * ceil(T / 64)
+  // chunks
   int dev = 0, sms = 0;
   if ((err = cudaGetDevice(&dev)) != cudaSuccess) return err;
   if ((err = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
