@@ -1,20 +1,25 @@
-"""Throughput of the chunked gated-delta forward on one GB300 (JSON line out).
+"""Throughput of the gated-delta hot path on one GB300 (one JSON line out).
 
-One step = the whole hot path over one batch: the chunkwise forward of the
-Gated DeltaNet workload B=4, T=4096, H=16, d_k=d_v=128 (bf16 inputs, fp32
-state, random initial state, final state returned), then one decode step per
-(sequence, head) continuing from that final state. Unit: token-heads per
-second (prefill B*T*H plus decode B*H per step). Other workloads are selected
-with --workload (1..5; the decode phase applies where the workload has one).
+One step = the whole hot path over one batch of the Gated DeltaNet-2 workload:
+the chunkwise forward of B=1, T=65536, H=32, d_k=d_v=128 (bf16 inputs, fp32
+state, final state returned), then its decode phase, 256 single-token steps
+at batch N=256 (H=32) from random fp32 states, one gdr_recurrent_step call per
+token. Unit: token-heads per second (prefill B*T*H plus decode N*H per decode
+step). --workload 1..4 selects another workload as the step (then one decode
+step per (batch, head) from the prefill's final state); every run also times
+the other workloads' chunked forwards alone (`configs`).
 
 Timing: W untimed warm-up steps, then K steps, each bracketed by CUDA events
-on the launching stream with the L2 flushed (a 256 MiB write) before every
-step, outside the events. Per-kernel events give the roofline of the chunk
-kernel. Under torchrun each rank runs its own copy of the workload (weak
-scaling; no collective on the data path) and the time is the max over ranks.
+on the launching stream with the L2 flushed (a 256 MiB write) and the decode
+states reset before every step, outside the events. The `roofline` object is
+the chunked forward's (the metric's subject): algorithmic bytes over its
+event-timed duration against the measured HBM copy bandwidth; the decode
+phase, the standalone gate cumsum and every other workload carry their own.
+Under torchrun each rank runs its own copy of the workload (weak scaling; no
+collective on the data path) and the time is the max over ranks.
 
 --impl reference times the float64 CPU oracle on the host cores instead (a
-bounded sample of the same workload per step).
+bounded sample of the same workload's recipe per step).
 """
 import argparse
 import json
@@ -44,8 +49,11 @@ def parse():
     p.add_argument("--steps", type=int, default=300)
     p.add_argument("--warmup", type=int, default=5)
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    p.add_argument("--workload", type=int, default=2, choices=[1, 2, 3, 4, 5])
-    p.add_argument("--decode-steps", type=int, default=1)
+    p.add_argument("--workload", type=int, default=5, choices=[1, 2, 3, 4, 5])
+    p.add_argument("--decode-steps", type=int, default=None,
+                   help="decode steps per step (default: the workload's decode phase, else 1)")
+    p.add_argument("--no-configs", action="store_true",
+                   help="skip timing the other workloads")
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-value-beta", action="store_true",
@@ -54,8 +62,6 @@ def parse():
                    help="skip the sequence-split measurement")
     p.add_argument("--no-backward", action="store_true",
                    help="skip the backward measurement")
-    p.add_argument("--no-pipelined", action="store_true",
-                   help="skip the long-sequence (pipelined call) measurement")
     p.add_argument("--pipeline", type=int, default=None,
                    help="time segments of the pipelined forward (default: the library's "
                         "recommendation for the workload; 1: the plain call)")
@@ -97,9 +103,9 @@ def peaks():
 
 # DRAM bytes (read + write) of one gdr_chunk_fwd call as ncu counted them
 # (dram__bytes_read.sum + dram__bytes_write.sum summed over chunk_prep_kernel
-# and chunk_scan_kernel), per workload, with the hash of the kernel sources they
-# were taken on: a changed kernel reports null traffic until it is profiled
-# again. Source: profiles/chunk_fwd_two_kernel_gdn_b4_t4096_h16_d128.md.
+# and chunk_scan_kernel, from one capture of the plain two-kernel call), per
+# workload, with the hash of the kernel sources they were taken on: a changed
+# kernel reports null traffic until it is profiled again.
 TRAFFIC = {2: {"bytes": 835.4e6, "sources": "23b49c3cb85400d5"}}
 KERNEL_SOURCES = ("chunk_prep.cu", "chunk_scan.cu", "packet.h", "tc.cuh", "tri_inverse.cuh",
                   "common.cuh")
@@ -176,19 +182,70 @@ class ClockSampler:
                 "samples": len(rows)}
 
 
-def make_step_inputs(cfg_id, rank, dev):
+def decode_of(cfg_id, N_default):
+    """(steps, N) of the workload's decode phase: its own, else one decode step
+    per (batch, head) continuing from the prefill's final state."""
     c = wl.CONFIGS[cfg_id]
-    x = wl.config_inputs(cfg_id, seed=c["seed"] + 1000 * rank)
-    N, H = c["B"], c["H"]
     if "decode" in c:
-        N = c["decode"]["N"]
-    y = wl.make_inputs(c["variant"], N, 1, H, c["dk"], c["dv"], c["dtype"],
-                       seed=c["seed"] + 1000 * rank + 1, q_prescaled=c["q_prescaled"])
-    return c, x, y
+        return c["decode"]["steps"], c["decode"]["N"]
+    return 1, N_default
 
 
-def squeeze_t(t):
-    return None if t is None else t[:, 0].contiguous()
+def prefill_bytes(x, o, hT):
+    """Algorithmic bytes of one chunked forward: every input read once, o and the
+    final state written once."""
+    return tensor_bytes(x["q"], x["k"], x["v"], x["g"], x["beta"], x["lam"], x["b"], x["w"],
+                        x["h0"], o, hT)
+
+
+def roofline_obj(nbytes, flops, ms, pk, pk_kind):
+    """HBM or tensor roofline of one launch from its algorithmic bytes / flops and
+    its mean event-timed duration."""
+    s = ms / 1e3
+    gbs = nbytes / s / 1e9
+    tflops = flops / s / 1e12
+    ridge = pk["bf16_tflops"] * 1e12 / (pk["hbm_gbs"] * 1e9)
+    if flops / max(nbytes, 1) < ridge:
+        r = {"bound": "hbm", "achieved": round(gbs, 1), "peak": pk["hbm_gbs"], "unit": "GB/s",
+             "frac": round(gbs / pk["hbm_gbs"], 4)}
+    else:
+        r = {"bound": "tensor", "achieved": round(tflops, 2), "peak": pk["bf16_tflops"],
+             "unit": "TFLOP/s", "frac": round(tflops / pk["bf16_tflops"], 4)}
+    r.update({"peak_source": pk_kind, "algorithmic_bytes_per_launch": nbytes,
+              "algorithmic_flops_per_launch": flops,
+              "tensor_tflops_achieved": round(tflops, 2),
+              "tensor_frac_of_bf16_peak": round(tflops / pk["bf16_tflops"], 4),
+              "launch_ms_mean": round(ms, 4)})
+    return r
+
+
+def time_calls(call, K, stream, flush, warm=3, before=None):
+    """Mean milliseconds of `call` over K calls, each bracketed by CUDA events on
+    `stream`, the L2 flushed (and `before` run) ahead of each outside the events."""
+    for _ in range(warm):
+        if before is not None:
+            before()
+        call()
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(K)]
+    torch.cuda.synchronize()
+    for i in range(K):
+        flush.fill_(float(i))
+        if before is not None:
+            before()
+        ev[i][0].record(stream)
+        call()
+        ev[i][1].record(stream)
+    torch.cuda.synchronize()
+    return statistics.mean(ev[i][0].elapsed_time(ev[i][1]) for i in range(K))
+
+
+def fwd_launches(gdr, shape, pipe, ws):
+    """This library's kernel launches in one chunked forward call."""
+    if ws is None:
+        return 1                       # fp32: one fused kernel
+    if pipe > 1:
+        return 2 * pipe                # preparation + state pass per time segment
+    return 2                           # the five workloads never split (B * H >= 32)
 
 
 def run_ours(args):
@@ -200,22 +257,25 @@ def run_ours(args):
         dist.init_process_group("nccl")
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
-    c, x, y = make_step_inputs(args.workload, rank, dev)
-    xd = {k: (v.to(dev) if torch.is_tensor(v) else v) for k, v in x.items()}
-    yd = {k: (squeeze_t(v).to(dev) if torch.is_tensor(v) else v) for k, v in y.items()}
+    cfg = args.workload
+    c = wl.CONFIGS[cfg]
+    # inputs drawn on the device (seeded CUDA generator), resident in HBM
+    x = wl.config_inputs(cfg, gen_device=dev, seed=c["seed"] + 1000 * rank)
     B, T, H, dk, dv = c["B"], c["T"], c["H"], c["dk"], c["dv"]
-    N = y["q"].shape[0]
-    has_decode = args.decode_steps > 0
+    dec_steps, N = decode_of(cfg, B)
+    if args.decode_steps is not None:
+        dec_steps = args.decode_steps
+    if "decode" in c:
+        y = wl.decode_phase_inputs(cfg, seed=c["seed"] + 500 + 1000 * rank, gen_device=dev,
+                                   steps=max(dec_steps, 1))
+    else:   # one token per (batch, head) after the prefill, from its final state
+        y = wl.make_inputs(c["variant"], max(dec_steps, 1), B, H, dk, dv, c["dtype"],
+                           seed=c["seed"] + 1000 * rank + 1, gen_device=dev)
+        y["h0"] = None
     o = torch.empty(B, T, H, dv, dtype=c["dtype"], device=dev)
     hT = torch.empty(B, H, dk, dv, dtype=torch.float32, device=dev)
-    # decode state: the prefill's final state when the batch matches, else its own
-    if N == B:
-        state = hT
-    else:
-        gen = torch.Generator().manual_seed(99 + rank)
-        state = (torch.randn(N, H, dk, dv, generator=gen) * c.get("decode", {}).get("h_std", 0.02)
-                 ).to(dev)
-    o_dec = torch.empty(N, H, dv, dtype=c["dtype"], device=dev)
+    state = hT if y["h0"] is None else torch.empty_like(y["h0"])
+    o_dec = torch.empty(max(dec_steps, 1), N, H, dv, dtype=c["dtype"], device=dev)
     stream = torch.cuda.current_stream(dev)
     flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
     shape = gdr.make_shape(B, T, H, dk, dv, c["dtype"], x["flags"], x["scale"])
@@ -225,17 +285,28 @@ def run_ours(args):
     ws_bytes = (gdr.chunk_fwd_pipelined_workspace_bytes(shape, pipe) if pipe > 1
                 else gdr.chunk_fwd_workspace_bytes(shape))
     ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev) if ws_bytes else None
+    yg = lambda n, s: None if y[n] is None else y[n][s]
 
-    def step():
-        gdr.chunk_fwd(xd["q"], xd["k"], xd["v"], xd["g"], xd["beta"], xd["lam"], xd["b"],
-                      xd["w"], xd["h0"], scale=x["scale"], flags=x["flags"], o=o, hT=hT,
-                      workspace=ws, pipeline=pipe)
-        for _ in range(args.decode_steps if has_decode else 0):
-            gdr.recurrent_step(yd["q"], yd["k"], yd["v"], yd["g"], state, yd["beta"], yd["lam"],
-                               yd["b"], yd["w"], scale=y["scale"], flags=y["flags"], o=o_dec)
+    def prefill():
+        gdr.chunk_fwd(x["q"], x["k"], x["v"], x["g"], x["beta"], x["lam"], x["b"], x["w"],
+                      x["h0"], scale=x["scale"], flags=x["flags"], o=o, hT=hT, workspace=ws,
+                      pipeline=pipe)
+
+    def decode():
+        for s in range(dec_steps):
+            gdr.recurrent_step(yg("q", s), yg("k", s), yg("v", s), yg("g", s), state,
+                               yg("beta", s), yg("lam", s), yg("b", s), yg("w", s),
+                               scale=y["scale"], flags=y["flags"], o=o_dec[s])
+
+    def reset():
+        # the decode phase starts from its own random states (outside the events)
+        if y["h0"] is not None:
+            state.copy_(y["h0"])
 
     for _ in range(args.warmup):
-        step()
+        reset()
+        prefill()
+        decode()
     torch.cuda.synchronize()
 
     K = args.steps
@@ -247,14 +318,11 @@ def run_ours(args):
     time.sleep(0.1)
     for i in range(K):
         flush.fill_(float(i))
+        reset()
         ev[i][0].record(stream)
-        gdr.chunk_fwd(xd["q"], xd["k"], xd["v"], xd["g"], xd["beta"], xd["lam"], xd["b"],
-                      xd["w"], xd["h0"], scale=x["scale"], flags=x["flags"], o=o, hT=hT,
-                      workspace=ws, pipeline=pipe)
+        prefill()
         ev[i][1].record(stream)
-        for _ in range(args.decode_steps if has_decode else 0):
-            gdr.recurrent_step(yd["q"], yd["k"], yd["v"], yd["g"], state, yd["beta"], yd["lam"],
-                               yd["b"], yd["w"], scale=y["scale"], flags=y["flags"], o=o_dec)
+        decode()
         ev[i][2].record(stream)
     torch.cuda.synchronize()
     clk = clocks.stop()
@@ -266,90 +334,142 @@ def run_ours(args):
     total_ms = max_over_ranks(sum(step_ms), device=dev)
 
     th_prefill = B * T * H
-    th_decode = N * H * (args.decode_steps if has_decode else 0)
+    th_decode = N * H * dec_steps
     th_step = th_prefill + th_decode
     value = whole_job_value(th_step, K, world, total_ms)
 
-    # roofline of the dominant kernel (the chunked forward), algorithmic bytes
+    # roofline of the chunked forward (the metric's subject), algorithmic bytes
     pk, pk_kind = peaks()
-    chunk_bytes = tensor_bytes(xd["q"], xd["k"], xd["v"], xd["g"], xd["beta"], xd["lam"],
-                               xd["b"], xd["w"], xd["h0"], o, hT)
-    mean_chunk_s = statistics.mean(chunk_ms) / 1e3
-    gbs = chunk_bytes / mean_chunk_s / 1e9
-    flops = algorithmic_flops_per_th(dk, dv) * th_prefill
-    tflops = flops / mean_chunk_s / 1e12
-    ridge = pk["bf16_tflops"] * 1e12 / (pk["hbm_gbs"] * 1e9)
-    bound = "hbm" if flops / chunk_bytes < ridge else "tensor"
-    if bound == "hbm":
-        roof = {"bound": "hbm", "achieved": round(gbs, 1), "peak": pk["hbm_gbs"], "unit": "GB/s",
-                "frac": round(gbs / pk["hbm_gbs"], 4)}
-    else:
-        roof = {"bound": "tensor", "achieved": round(tflops, 2), "peak": pk["bf16_tflops"],
-                "unit": "TFLOP/s", "frac": round(tflops / pk["bf16_tflops"], 4)}
-    roof.update({"traffic": measured_traffic(args.workload),
+    mean_chunk = statistics.mean(chunk_ms)
+    roof = roofline_obj(prefill_bytes(x, o, hT), algorithmic_flops_per_th(dk, dv) * th_prefill,
+                        mean_chunk, pk, pk_kind)
+    roof.update({"traffic": measured_traffic(cfg),
                  "kernel": ("gdr_chunk_fwd: chunk_prep_kernel + chunk_scan_kernel (one call)"
                             if pipe <= 1 else
                             "gdr_chunk_fwd_pipelined: %d x (chunk_prep_kernel + chunk_scan_kernel)"
                             ", one call" % pipe),
                  "pipeline_segments": pipe,
-                 "peak_source": pk_kind,
-                 "algorithmic_bytes_per_launch": chunk_bytes,
-                 "algorithmic_flops_per_launch": flops,
-                 "tensor_tflops_achieved": round(tflops, 2),
-                 "tensor_frac_of_bf16_peak": round(tflops / pk["bf16_tflops"], 4),
-                 "launch_ms_mean": round(statistics.mean(chunk_ms), 4)})
-    dec_bytes = tensor_bytes(yd["q"], yd["k"], yd["v"], yd["g"], yd["beta"], yd["lam"],
-                             yd["b"], yd["w"], o_dec) + 2 * tensor_bytes(state)
+                 "token_heads_per_s": round(th_prefill / (mean_chunk / 1e3), 1)})
     decode_info = None
-    if has_decode and statistics.mean(dec_ms) > 0:
-        dgbs = dec_bytes * args.decode_steps / (statistics.mean(dec_ms) / 1e3) / 1e9
-        decode_info = {"kernel": "recurrent_step_kernel", "N": N, "H": H,
-                       "ms_mean": round(statistics.mean(dec_ms), 4),
-                       "achieved_gbs": round(dgbs, 1), "frac_hbm": round(dgbs / pk["hbm_gbs"], 4)}
+    if dec_steps > 0:
+        per = statistics.mean(dec_ms) / dec_steps
+        dbytes = (tensor_bytes(*(yg(n, 0) for n in ("q", "k", "v", "g", "beta", "lam", "b",
+                                                      "w")), o_dec[0]) + 2 * tensor_bytes(state))
+        droof = roofline_obj(dbytes, 5.0 * dk * dv * N * H, per, pk, pk_kind)
+        decode_info = {"kernel": "recurrent_step_kernel", "steps": dec_steps, "N": N, "H": H,
+                       "from": "random fp32 states" if y["h0"] is not None else
+                               "the prefill's final state",
+                       "ms_per_phase": round(statistics.mean(dec_ms), 4),
+                       "ms_per_decode_step": round(per, 5),
+                       "token_heads_per_s": round(th_decode / (statistics.mean(dec_ms) / 1e3), 1),
+                       "roofline": droof}
+    plain_ms = None
+    if pipe > 1:   # the same inputs through the plain two-kernel call, for comparison
+        ws1 = torch.empty(gdr.chunk_fwd_workspace_bytes(shape), dtype=torch.uint8, device=dev)
+        plain_ms = time_calls(lambda: gdr.chunk_fwd(
+            x["q"], x["k"], x["v"], x["g"], x["beta"], x["lam"], x["b"], x["w"], x["h0"],
+            scale=x["scale"], flags=x["flags"], o=o, hT=hT, workspace=ws1, pipeline=1),
+            min(K, 10), stream, flush)
+        del ws1
+        roof["plain_call_ms"] = round(plain_ms, 4)
 
-    epilogue_info = measure_epilogue(gdr, o, c, dev, stream, flush, K, pk)
+    cumsum_info = measure_gate_cumsum(gdr, x, c, dev, stream, flush, min(K, 20), pk, pk_kind)
+    epilogue_info = measure_epilogue(gdr, o, c, dev, stream, flush, min(K, 20), pk)
+    e2e = None if args.no_e2e else measure_e2e(gdr, x, y, c, dev, pipe, dec_steps, N)
+    # the other workloads, each timed alone in its default launch configuration
+    configs_info = None
+    if not args.no_configs:
+        configs_info = {}
+        del ws
+        for other in (1, 2, 3, 4, 5):
+            if other != cfg:
+                configs_info[str(other)] = measure_config(gdr, other, dev, stream, flush,
+                                                          min(K, 20), pk, pk_kind)
     value_beta_info = None if args.no_value_beta else measure_value_beta(gdr, dev, stream, flush,
-                                                                         K, pk, clk)
-    split_info = None if args.no_split else measure_split(gdr, dev, stream, flush, K, pk)
-    pipe_info = None if args.no_pipelined else measure_pipelined(gdr, dev, stream, flush,
-                                                                 min(K, 10), pk)
-    backward_info = None if args.no_backward else measure_backward(gdr, xd, c, dev, stream, flush,
+                                                                         min(K, 10), pk, clk)
+    split_info = None if args.no_split else measure_split(gdr, dev, stream, flush, min(K, 10), pk)
+    backward_info = None if args.no_backward else measure_backward(gdr, dev, stream, flush,
                                                                    min(K, 10), pk, clk)
-
-    e2e = None if args.no_e2e else measure_e2e(gdr, x, y, c, dev, args, B, T, H, dk, dv, N)
 
     result = {
         "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world, "steps": K,
         "warmup": args.warmup, "ms_per_step": round(total_ms / K, 5), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16" if c["dtype"] == torch.bfloat16
         else "f32", "data": "synthetic",
-        "config": {"workload": c["name"] + (" + %d decode step(s) at N=%d" %
-                                            (args.decode_steps, N) if has_decode else ""),
-                   "variant": c["variant"], "B": B, "T": T, "H": H, "dk": dk, "dv": dv,
-                   "chunk": 64, "token_heads_per_step": th_step,
-                   "l2": "flushed before every timed step (256 MiB write, outside the events)",
-                   "parallelism": "replica per GPU" if world > 1 else "single GPU"},
+        "config": dict(config_obj(c, dec_steps, N, world),
+                       l2="flushed before every timed step (256 MiB write, outside the events)",
+                       inputs="drawn on the device with a seeded CUDA generator, resident in HBM"),
         "roofline": roof,
         "decode": decode_info,
+        "gate_cumsum": cumsum_info,
+        "configs": configs_info,
         "epilogue": epilogue_info,
         "value_beta": value_beta_info,
         "sequence_split": split_info,
-        "pipelined": pipe_info,
         "backward": backward_info,
-        # this library's kernels per timed step: the two-kernel chunked forward
-        # (bf16 with the full workspace) or one fused kernel (fp32), then the
-        # decode steps
-        "gpu_launches": K * ((2 * max(pipe, 1) if ws is not None else 1) +
-                             (args.decode_steps if has_decode else 0)),
+        # this library's kernels per timed step: the chunked forward's launches,
+        # then one per decode step
+        "gpu_launches": K * (fwd_launches(gdr, shape, pipe, ws_bytes or None) + dec_steps),
         "clocks": clk,
         "e2e": e2e,
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        result["cpu_baseline"] = cpu_baseline(x, y if N == B else None, th_step)
+        result["cpu_baseline"] = cpu_baseline(x, y, dec_steps)
     if rank == 0:
         print(json.dumps(result), flush=True)
     if world > 1:
         torch.distributed.destroy_process_group()
+
+
+def measure_config(gdr, cfg, dev, stream, flush, K, pk, pk_kind):
+    """One workload's chunked forward timed alone in the launch configuration the
+    library picks for it (pipelined where it recommends time segments): K calls,
+    L2 flushed before each, CUDA events on the launching stream."""
+    c = wl.CONFIGS[cfg]
+    x = wl.config_inputs(cfg, gen_device=dev)
+    B, T, H, dk, dv = c["B"], c["T"], c["H"], c["dk"], c["dv"]
+    o = torch.empty(B, T, H, dv, dtype=c["dtype"], device=dev)
+    hT = torch.empty(B, H, dk, dv, dtype=torch.float32, device=dev)
+    shape = gdr.make_shape(B, T, H, dk, dv, c["dtype"], x["flags"], x["scale"])
+    pipe = gdr.pipeline_segments(shape)
+    nws = (gdr.chunk_fwd_pipelined_workspace_bytes(shape, pipe) if pipe > 1
+           else gdr.chunk_fwd_workspace_bytes(shape))
+    ws = torch.empty(nws, dtype=torch.uint8, device=dev) if nws else None
+
+    def call():
+        gdr.chunk_fwd(x["q"], x["k"], x["v"], x["g"], x["beta"], x["lam"], x["b"], x["w"],
+                      x["h0"], scale=x["scale"], flags=x["flags"], o=o, hT=hT, workspace=ws,
+                      pipeline=pipe)
+
+    ms = time_calls(call, K, stream, flush)
+    th = B * T * H
+    roof = roofline_obj(prefill_bytes(x, o, hT), algorithmic_flops_per_th(dk, dv) * th, ms, pk,
+                        pk_kind)
+    roof["traffic"] = measured_traffic(cfg)
+    out = {"workload": c["name"], "dtype": "bf16" if c["dtype"] == torch.bfloat16 else "f32",
+           "launches": K, "ms_mean": round(ms, 4), "token_heads_per_s": round(th / (ms / 1e3), 1),
+           "pipeline_segments": pipe, "roofline": roof, "l2": "flushed before every call",
+           "kernels": ("chunk_fwd_kernel (fp32)" if ws is None else
+                       "chunk_prep_kernel + chunk_scan_kernel" +
+                       (" x %d time segments" % pipe if pipe > 1 else ""))}
+    del x, o, hT, ws
+    torch.cuda.empty_cache()
+    return out
+
+
+def measure_gate_cumsum(gdr, x, c, dev, stream, flush, K, pk, pk_kind):
+    """The standalone chunk-local log-decay cumsum (gdr_gate_cumsum) on the
+    workload's gate tensor (per key channel for the channel-decay variants), timed
+    alone: K launches, L2 flushed before each. Bytes: g read once, G written once."""
+    g = x["g"]
+    G = torch.empty_like(g)
+    ms = time_calls(lambda: gdr.gate_cumsum(g, out=G), K, stream, flush)
+    nbytes = tensor_bytes(g, G)
+    roof = roofline_obj(nbytes, float(g.numel()), ms, pk, pk_kind)
+    del G
+    return {"kernel": "gate_cumsum_vec4" if g.dim() == 4 else "gate_cumsum_scalar",
+            "shape": list(g.shape), "launches": K, "ms_mean": round(ms, 4),
+            "roofline": roof, "l2": "flushed before every launch"}
 
 
 def measure_epilogue(gdr, o, c, dev, stream, flush, K, pk, eps=1e-6):
@@ -396,7 +516,7 @@ def measure_value_beta(gdr, dev, stream, flush, K, pk, clk):
     rank-1 write)."""
     from gated_delta_rule_10_gb300 import workloads as wl
     c = wl.CONFIGS["vbeta"]
-    x = wl.config_inputs("vbeta", device=dev)
+    x = wl.config_inputs("vbeta", gen_device=dev)
     B, T, H, dk, dv = c["B"], c["T"], c["H"], c["dk"], c["dv"]
     o = torch.empty(B, T, H, dv, dtype=c["dtype"], device=dev)
     hT = torch.empty(B, H, dk, dv, dtype=torch.float32, device=dev)
@@ -452,7 +572,7 @@ def measure_split(gdr, dev, stream, flush, K, pk, H=4):
     step or its metric."""
     from gated_delta_rule_10_gb300 import workloads as wl
     c = dict(wl.CONFIGS[5], H=H)
-    x = wl.config_inputs(5, device=dev, H=H)
+    x = wl.config_inputs(5, gen_device=dev, H=H)
     B, T, dk, dv = c["B"], c["T"], c["dk"], c["dv"]
     o = torch.empty(B, T, H, dv, dtype=c["dtype"], device=dev)
     hT = torch.empty(B, H, dk, dv, dtype=torch.float32, device=dev)
@@ -489,49 +609,6 @@ def measure_split(gdr, dev, stream, flush, K, pk, H=4):
     return out
 
 
-def measure_pipelined(gdr, dev, stream, flush, K, pk):
-    """The Gated DeltaNet-2 prefill (1 x 65536 x 32 x 128 bf16: B * H = 32, the
-    state pass on 64 SMs) through the plain call and through the pipelined call
-    with the library's recommended time segments, K calls each, L2 flushed
-    before every call, CUDA events on the launching stream."""
-    x = wl.config_inputs(5)
-    x = {k: (v.to(dev) if torch.is_tensor(v) else v) for k, v in x.items()}
-    B, T, H, dk = x["q"].shape
-    dv = x["v"].shape[-1]
-    shape = gdr.make_shape(B, T, H, dk, dv, x["q"].dtype, x["flags"], x["scale"])
-    o = torch.empty(B, T, H, dv, dtype=x["q"].dtype, device=dev)
-    hT = torch.empty(B, H, dk, dv, dtype=torch.float32, device=dev)
-    seg = gdr.pipeline_segments(shape)
-    nbytes = tensor_bytes(x["q"], x["k"], x["v"], x["g"], x["beta"], x["lam"], x["b"], x["w"],
-                          x["h0"], o, hT)
-    out = {"workload": "gdn2_bf16_b1_t65536_h32_d128", "segments": seg, "launches": K,
-           "algorithmic_bytes_per_call": nbytes, "l2": "flushed before every call"}
-    for name, pipe in (("plain", 1), ("pipelined", seg)):
-        ws = torch.empty(gdr.chunk_fwd_pipelined_workspace_bytes(shape, pipe) if pipe > 1
-                         else gdr.chunk_fwd_workspace_bytes(shape), dtype=torch.uint8, device=dev)
-
-        def call():
-            gdr.chunk_fwd(x["q"], x["k"], x["v"], x["g"], x["beta"], x["lam"], x["b"], x["w"],
-                          x["h0"], scale=x["scale"], flags=x["flags"], o=o, hT=hT, workspace=ws,
-                          pipeline=pipe)
-        for _ in range(2):
-            call()
-        ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(K)]
-        torch.cuda.synchronize()
-        for i in range(K):
-            flush.fill_(float(i))
-            ev[i][0].record(stream)
-            call()
-            ev[i][1].record(stream)
-        torch.cuda.synchronize()
-        ms = statistics.mean(ev[i][0].elapsed_time(ev[i][1]) for i in range(K))
-        gbs = nbytes / (ms / 1e3) / 1e9
-        out[name] = {"ms_mean": round(ms, 4), "token_heads_per_s": round(B * T * H / (ms / 1e3), 1),
-                     "achieved_gbs": round(gbs, 1), "frac_hbm": round(gbs / pk["hbm_gbs"], 4)}
-        del ws
-    return out
-
-
 def bwd_flops_per_th(dk, dv, C=64):
     """Multiply-adds x 2 per token-head of the chunk backward as built: the chunk's
     forward quantities (T, A, Y, U, A_qk), the forward and reverse state passes
@@ -541,10 +618,13 @@ def bwd_flops_per_th(dk, dv, C=64):
     return 2.0 * (8 * dk * dv + 12 * C * d + C * C)
 
 
-def measure_backward(gdr, xd, c, dev, stream, flush, K, pk, clk):
-    """gdr_chunk_bwd on the step's workload (gradients of <dO, o> + <dhT, hT>), timed
-    alone: K calls, L2 flushed before each, CUDA events on the launching stream.
-    Not part of the step or its metric; fp32 arithmetic on the FP32 pipe."""
+def measure_backward(gdr, dev, stream, flush, K, pk, clk, cfg=2):
+    """gdr_chunk_bwd on the Gated DeltaNet workload (4 x 4096 x 16 x 128 bf16;
+    gradients of <dO, o> + <dhT, hT>), timed alone: K calls, L2 flushed before
+    each, CUDA events on the launching stream. Not part of the step or its
+    metric; fp32 arithmetic."""
+    c = wl.CONFIGS[cfg]
+    xd = wl.config_inputs(cfg, gen_device=dev)
     B, T, H, dk, dv = c["B"], c["T"], c["H"], c["dk"], c["dv"]
     gen = torch.Generator().manual_seed(7)
     dO = torch.randn(B, T, H, dv, generator=gen).to(c["dtype"]).to(dev)
@@ -586,192 +666,224 @@ def measure_backward(gdr, xd, c, dev, stream, flush, K, pk, clk):
             "workspace_bytes": ws.numel(), "l2": "flushed before every call"}
 
 
-def measure_e2e(gdr, x, y, c, dev, args, B, T, H, dk, dv, N, steps=8, n_up=1):
+def measure_e2e(gdr, x, y, c, dev, pipe, dec_steps, N, steps=6):
     """Same metric through the public API with pinned host buffers: every step
-    copies its inputs host->device, runs the path, and copies o, the decode
-    output and the final state back. The steps are pipelined the way a server
-    would run them: inputs of step i+1 go up on a copy stream while step i
-    computes, and step i's results come down on another while step i+1
-    computes (device buffers double-buffered); every copy of every step is
-    inside the timed region. The upload bounds the step (~180 GB/s host to
-    device here); two to four upload streams measured no faster than one."""
+    copies its inputs host->device (the prefill's tensors, the decode phase's
+    per-token tensors and its starting states), runs the path, and copies o, the
+    prefill's final state, every decode output and the decode's final states
+    back. The steps are pipelined the way a server would run them: inputs of step
+    i+1 go up on a copy stream while step i computes, and step i's results come
+    down on another while step i+1 computes (device buffers double-buffered);
+    every copy of every step is inside the timed region."""
+    B, T, H, dk, dv = c["B"], c["T"], c["H"], c["dk"], c["dv"]
     names = ("q", "k", "v", "g", "beta", "lam", "b", "w", "h0")
-    hx = {n: x[n].pin_memory() for n in names if x[n] is not None}
-    hy = {n: squeeze_t(y[n]).pin_memory() for n in ("q", "k", "v", "g", "beta", "lam", "b", "w")
+    hx = {n: x[n].cpu().pin_memory() for n in names if x[n] is not None}
+    hy = {n: y[n][:max(dec_steps, 1)].cpu().pin_memory() for n in names[:-1]
           if y[n] is not None}
+    if y["h0"] is not None:
+        hy["h0"] = y["h0"].cpu().pin_memory()
     nb = 2
     dx = [{n: torch.empty_like(t, device=dev) for n, t in hx.items()} for _ in range(nb)]
     dy = [{n: torch.empty_like(t, device=dev) for n, t in hy.items()} for _ in range(nb)]
     o = [torch.empty(B, T, H, dv, dtype=c["dtype"], device=dev) for _ in range(nb)]
     hT = [torch.empty(B, H, dk, dv, dtype=torch.float32, device=dev) for _ in range(nb)]
-    state = [hT[i] if N == B else torch.zeros(N, H, dk, dv, device=dev) for i in range(nb)]
-    o_dec = [torch.empty(N, H, dv, dtype=c["dtype"], device=dev) for _ in range(nb)]
+    o_dec = [torch.empty(max(dec_steps, 1), N, H, dv, dtype=c["dtype"], device=dev)
+             for _ in range(nb)]
     ho = torch.empty_like(o[0], device="cpu").pin_memory()
-    hhT = torch.empty_like(state[0], device="cpu").pin_memory()
+    hhT = torch.empty_like(hT[0], device="cpu").pin_memory()
     ho_dec = torch.empty_like(o_dec[0], device="cpu").pin_memory()
+    hstate = (torch.empty_like(hy["h0"]).pin_memory() if "h0" in hy else None)
     shape = gdr.make_shape(B, T, H, dk, dv, c["dtype"], x["flags"], x["scale"])
-    nws = gdr.chunk_fwd_workspace_bytes(shape)
+    nws = (gdr.chunk_fwd_pipelined_workspace_bytes(shape, pipe) if pipe > 1
+           else gdr.chunk_fwd_workspace_bytes(shape))
     ws = [torch.empty(nws, dtype=torch.uint8, device=dev) if nws else None for _ in range(nb)]
     comp = torch.cuda.current_stream(dev)
-    ups = [torch.cuda.Stream(dev) for _ in range(n_up)]
+    up = torch.cuda.Stream(dev)
     down = torch.cuda.Stream(dev)
     g = lambda d, n: d.get(n)
-    # the input tensors dealt over the upload streams, largest first
-    order = sorted(list(hx.items()) + [("y." + n, t) for n, t in hy.items()],
-                   key=lambda kv: -kv[1].numel() * kv[1].element_size())
-    lanes = [[] for _ in range(n_up)]
-    load = [0] * n_up
-    for n, t in order:
-        j = load.index(min(load))
-        lanes[j].append(n)
-        load[j] += t.numel() * t.element_size()
+    gs = lambda d, n, s: None if d.get(n) is None else d[n][s]
 
     def run(steps_n):
-        up_done = [[torch.cuda.Event() for _ in range(n_up)] for _ in range(steps_n)]
+        up_done = [torch.cuda.Event() for _ in range(steps_n)]
         comp_done = [torch.cuda.Event() for _ in range(steps_n)]
         down_done = [torch.cuda.Event() for _ in range(steps_n)]
         for i in range(steps_n):
             s = i % nb
             # inputs of step i: after step i - nb has finished reading buffer s
-            for j, up in enumerate(ups):
-                with torch.cuda.stream(up):
-                    if i >= nb:
-                        up.wait_event(comp_done[i - nb])
-                    for n in lanes[j]:
-                        if n.startswith("y."):
-                            dy[s][n[2:]].copy_(hy[n[2:]], non_blocking=True)
-                        else:
-                            dx[s][n].copy_(hx[n], non_blocking=True)
-                    up_done[i][j].record(up)
-                comp.wait_event(up_done[i][j])
+            with torch.cuda.stream(up):
+                if i >= nb:
+                    up.wait_event(comp_done[i - nb])
+                for n, t in hx.items():
+                    dx[s][n].copy_(t, non_blocking=True)
+                for n, t in hy.items():
+                    dy[s][n].copy_(t, non_blocking=True)
+                up_done[i].record(up)
+            comp.wait_event(up_done[i])
             if i >= nb:
                 comp.wait_event(down_done[i - nb])   # results of step i - nb are down
             d, e = dx[s], dy[s]
             gdr.chunk_fwd(g(d, "q"), g(d, "k"), g(d, "v"), g(d, "g"), g(d, "beta"), g(d, "lam"),
                           g(d, "b"), g(d, "w"), g(d, "h0"), scale=x["scale"], flags=x["flags"],
-                          o=o[s], hT=hT[s], workspace=ws[s])
-            for _ in range(args.decode_steps):
-                gdr.recurrent_step(g(e, "q"), g(e, "k"), g(e, "v"), g(e, "g"), state[s],
-                                   g(e, "beta"), g(e, "lam"), g(e, "b"), g(e, "w"),
-                                   scale=y["scale"], flags=y["flags"], o=o_dec[s])
+                          o=o[s], hT=hT[s], workspace=ws[s], pipeline=pipe)
+            state = e["h0"] if "h0" in e else hT[s]
+            for t in range(dec_steps):
+                gdr.recurrent_step(gs(e, "q", t), gs(e, "k", t), gs(e, "v", t), gs(e, "g", t),
+                                   state, gs(e, "beta", t), gs(e, "lam", t), gs(e, "b", t),
+                                   gs(e, "w", t), scale=y["scale"], flags=y["flags"],
+                                   o=o_dec[s][t])
             comp_done[i].record(comp)
             with torch.cuda.stream(down):
                 down.wait_event(comp_done[i])
                 ho.copy_(o[s], non_blocking=True)
+                hhT.copy_(hT[s], non_blocking=True)
                 ho_dec.copy_(o_dec[s], non_blocking=True)
-                hhT.copy_(state[s], non_blocking=True)
+                if hstate is not None:
+                    hstate.copy_(e["h0"], non_blocking=True)
                 down_done[i].record(down)
         comp.wait_event(down_done[steps_n - 1])
-        for up in ups:
-            up.wait_stream(comp)
+        up.wait_stream(comp)
         down.wait_stream(comp)
 
     run(2)
     torch.cuda.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(comp)
-    for up in ups:
-        up.wait_event(e0)
+    up.wait_event(e0)
     run(steps)
     e1.record(comp)
     torch.cuda.synchronize()
     ms = e0.elapsed_time(e1) / steps
-    th = B * T * H + N * H * args.decode_steps
-    h2d = sum(t.numel() * t.element_size() for t in hx.values()) + \
-        sum(t.numel() * t.element_size() for t in hy.values()) * args.decode_steps
-    d2h = tensor_bytes(ho, ho_dec, hhT)
-    return {"value": round(th / (ms / 1e3), 1), "unit": UNIT, "h2d_bytes_per_step": h2d,
-            "d2h_bytes_per_step": d2h, "ms_per_step": round(ms, 4), "steps": steps,
-            "pipelined": "inputs of step i+1 up (%d copy streams) and results of step i-1 down "
-                         "while step i computes" % n_up}
+    th = B * T * H + N * H * dec_steps
+    h2d = tensor_bytes(*hx.values()) + tensor_bytes(*hy.values())
+    d2h = tensor_bytes(ho, hhT, ho_dec, hstate)
+    out = {"value": round(th / (ms / 1e3), 1), "unit": UNIT, "h2d_bytes_per_step": h2d,
+           "d2h_bytes_per_step": d2h, "ms_per_step": round(ms, 4), "steps": steps,
+           "pipelined": "inputs of step i+1 up and results of step i-1 down while step i "
+                        "computes (one copy stream each way)"}
+    del dx, dy, o, hT, o_dec, ws
+    torch.cuda.empty_cache()
+    return out
 
 
-def oracle_step(x, y, seqs, nthreads):
-    """The oracle on `seqs` (batch, head) sequences of the step's workload: the
-    prefill tokens followed by the decode token (same math as the GPU step)."""
-    import numpy as np
+def config_obj(c, dec_steps, N, world):
+    """The `config` object of the JSON line (shared by both arms)."""
+    B, T, H = c["B"], c["T"], c["H"]
+    return {"workload": c["name"] + (" + %d decode step(s) at N=%d" % (dec_steps, N)
+                                     if dec_steps else ""),
+            "variant": c["variant"], "B": B, "T": T, "H": H, "dk": c["dk"], "dv": c["dv"],
+            "chunk": 64, "token_heads_per_step": B * T * H + N * H * dec_steps,
+            "prefill_token_heads": B * T * H, "decode_token_heads": N * H * dec_steps,
+            "parallelism": "replica per GPU" if world > 1 else "single GPU"}
+
+
+def oracle_sample(xp, yd, nthreads):
+    """The float64 oracle (C token recurrence, OpenMP over (batch, head)) on a
+    sample of a workload: prefill sequences xp ([B, T, H, d] tensors, each from
+    its h0 or zero) and decode sequences yd ([steps, N, H, d] per-token tensors
+    from their starting states yd["h0"]), the latter run as N sequences of
+    `steps` tokens. Returns (token-heads, seconds)."""
     from oracle import native
 
-    f64 = lambda t: None if t is None else t.double().numpy()
-    out_th = 0
-    t_total = 0.0
-    for (b, h) in seqs:
-        def pick(n):
-            t = x[n]
-            if t is None:
-                return None
-            t = t[b:b + 1, :, h:h + 1]
-            if y is not None and y[n] is not None:
-                t = torch.cat([t, y[n][b:b + 1, :, h:h + 1]], dim=1)
-            return f64(t.contiguous())
-        args = [pick(n) for n in ("q", "k", "v", "g", "beta", "lam", "b", "w")]
-        h0 = None if x["h0"] is None else f64(x["h0"][b:b + 1, h:h + 1].contiguous())
-        t0 = time.perf_counter()
-        native.recurrence(*args[:4], beta=args[4], lam=args[5], b=args[6], w=args[7], h0=h0,
-                          scale=x["scale"], flags=x["flags"], nthreads=1)
-        t_total += time.perf_counter() - t0
-        out_th += args[0].shape[1]
-    return out_th, t_total
-
-
-def cpu_baseline(x, y, th_step, budget_s=20.0):
-    """The oracle as it stands, timed on the host cores: every (batch, head)
-    sequence of the workload (each the prefill plus the decode token), spread
-    over all cores with OpenMP, repeated until ~budget_s or one pass."""
-    import numpy as np
-    from oracle import native
-
-    f64 = lambda t: None if t is None else t.double().numpy()
-    cat = lambda n: (torch.cat([x[n], y[n]], dim=1) if (y is not None and x[n] is not None)
-                     else x[n])
-    arrs = {n: f64(cat(n)) for n in ("q", "k", "v", "g", "beta", "lam", "b", "w")}
-    h0 = f64(x["h0"])
-    cores = native.max_threads()
-    th = arrs["q"].shape[0] * arrs["q"].shape[1] * arrs["q"].shape[2]
-    reps, t_total = 0, 0.0
-    while reps == 0 or (t_total < budget_s and reps < 3):
+    f64 = lambda t: None if t is None else t.detach().double().cpu().numpy()
+    names = ("q", "k", "v", "g", "beta", "lam", "b", "w")
+    jobs = [(({n: f64(xp[n]) for n in names}), f64(xp["h0"]))]
+    if yd is not None:
+        jobs.append(({n: (None if yd[n] is None else f64(yd[n].transpose(0, 1)))
+                      for n in names}, f64(yd["h0"])))
+    th, secs = 0, 0.0
+    for arrs, h0 in jobs:
         t0 = time.perf_counter()
         native.recurrence(arrs["q"], arrs["k"], arrs["v"], arrs["g"], arrs["beta"], arrs["lam"],
-                          arrs["b"], arrs["w"], h0, x["scale"], x["flags"], nthreads=cores)
-        t_total += time.perf_counter() - t0
+                          arrs["b"], arrs["w"], h0, xp["scale"], xp["flags"], nthreads=nthreads)
+        secs += time.perf_counter() - t0
+        th += arrs["q"].shape[0] * arrs["q"].shape[1] * arrs["q"].shape[2]
+    return th, secs
+
+
+def cpu_baseline(x, y, dec_steps, budget_s=12.0):
+    """The oracle as it stands, timed on all host cores on a bounded sample of the
+    step's workload: the prefill of batch row 0 for up to 16 heads over every
+    token, and (where the decode phase starts from its own states) the decode
+    of every sequence for up to 4 heads over all its steps; repeated until
+    ~budget_s or three passes."""
+    from oracle import native
+
+    H = x["q"].shape[2]
+    hs = slice(0, min(H, 16))
+    sel = lambda t, hsl: None if t is None else t[0:1, :, hsl]
+    xp = {n: sel(x[n], hs) for n in ("q", "k", "v", "g", "beta", "lam", "b", "w")}
+    xp.update(h0=None if x["h0"] is None else x["h0"][0:1, hs], scale=x["scale"],
+              flags=x["flags"])
+    yd = None
+    if y.get("h0") is not None and dec_steps > 0:
+        hd = slice(0, min(H, 4))
+        yd = {n: (None if y[n] is None else y[n][:dec_steps, :, hd])
+              for n in ("q", "k", "v", "g", "beta", "lam", "b", "w")}
+        yd["h0"] = y["h0"][:, hd]
+    cores = native.max_threads()
+    reps, th_total, t_total = 0, 0, 0.0
+    while reps == 0 or (t_total < budget_s and reps < 3):
+        th, t = oracle_sample(xp, yd, cores)
+        th_total += th
+        t_total += t
         reps += 1
-    return {"value": round(th * reps / t_total, 1), "unit": UNIT, "cores": cores,
-            "kind": "oracle", "sample": "whole workload (%d token-heads incl. decode tokens), "
-            "%d pass(es), C fp64 token recurrence, OpenMP over (batch, head)" % (th, reps),
-            "seconds": round(t_total, 3)}
+    npre = xp["q"].shape[1] * xp["q"].shape[2]
+    what = "prefill of %d (batch, head) sequences x %d tokens" % (xp["q"].shape[2],
+                                                                xp["q"].shape[1])
+    if yd is not None:
+        what += " + decode of %d sequences x %d heads x %d steps from their states" % (
+            yd["q"].shape[1], yd["q"].shape[2], yd["q"].shape[0])
+    return {"value": round(th_total / t_total, 1), "unit": UNIT, "cores": cores,
+            "kind": "oracle", "sample": what + "; %d token-heads per pass (%d prefill), %d "
+            "pass(es); C fp64 token recurrence, OpenMP over (batch, head)" % (
+                th_total // reps, npre, reps), "seconds": round(t_total, 3)}
 
 
 def run_reference(args):
+    """The float64 oracle, as it stands, on the host cores, on the same workload's
+    recipe at a bounded sample size per step: the prefill of 16 heads over 8192
+    tokens and the decode of every sequence of 2 heads over 128 steps (where the
+    workload has a decode phase from its own states)."""
     rank, world, _ = dist_env()
     if rank != 0:
         return
     from oracle import native
-    c, x, y = make_step_inputs(args.workload, 0, "cpu")
-    N = y["q"].shape[0]
-    yy = y if N == c["B"] else None
-    B, H = c["B"], c["H"]
-    # bounded sample per step: 2 sequences (each ~0.5 GFLOP at T=4096)
-    seqs_all = [(b, h) for b in range(B) for h in range(H)]
-    per_step = 2
-    for i in range(args.warmup):
-        oracle_step(x, yy, seqs_all[:1], 1)
+    cfg = args.workload
+    c = wl.CONFIGS[cfg]
+    dec_steps, N = decode_of(cfg, c["B"])
+    if args.decode_steps is not None:
+        dec_steps = args.decode_steps
+    xp = wl.config_inputs(cfg, B=1, T=min(c["T"], 8192), H=min(c["H"], 16))
+    yd = None
+    if "decode" in c and dec_steps > 0:
+        yd = wl.decode_phase_inputs(cfg, steps=min(dec_steps, 128), H=min(c["H"], 2))
+    cores = native.max_threads()
+    for _ in range(args.warmup):
+        oracle_sample(dict(xp, q=xp["q"][:, :64], k=xp["k"][:, :64], v=xp["v"][:, :64],
+                           g=xp["g"][:, :64],
+                           **{n: (None if xp[n] is None else xp[n][:, :64])
+                              for n in ("beta", "lam", "b", "w")}), None, cores)
     th_total, t_total = 0, 0.0
-    steps = max(1, min(args.steps, 8))
-    for i in range(steps):
-        seqs = [seqs_all[(i * per_step + j) % len(seqs_all)] for j in range(per_step)]
-        th, t = oracle_step(x, yy, seqs, 1)
+    for _ in range(args.steps):
+        th, t = oracle_sample(xp, yd, cores)
         th_total += th
         t_total += t
     value = th_total / t_total
+    sample = "prefill of %d sequences x %d tokens" % (xp["q"].shape[2], xp["q"].shape[1])
+    if yd is not None:
+        sample += " + decode of %d sequences x %d heads x %d steps" % (
+            yd["q"].shape[1], yd["q"].shape[2], yd["q"].shape[0])
     res = {"metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world,
-           "steps": steps, "warmup": args.warmup, "ms_per_step": round(1e3 * t_total / steps, 3),
+           "steps": args.steps, "warmup": args.warmup,
+           "ms_per_step": round(1e3 * t_total / args.steps, 3),
            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
            "data": "synthetic", "impl": "reference",
-           "config": {"workload": c["name"], "variant": c["variant"], "B": c["B"], "T": c["T"],
-                      "H": c["H"], "dk": c["dk"], "dv": c["dv"]},
-           "cpu_baseline": {"value": round(value, 1), "unit": UNIT, "cores": 1, "kind": "oracle",
-                            "sample": "%d (batch, head) sequences per step (prefill plus "
-                                      "decode token), single thread" % per_step},
+           "config": config_obj(c, dec_steps, N, world),
+           "cpu_baseline": {"value": round(value, 1), "unit": UNIT, "cores": cores,
+                            "kind": "oracle",
+                            "sample": sample + " per step (same recipe as the workload, "
+                                      "%d token-heads), all host cores" % (th_total //
+                                                                          args.steps)},
            "e2e": {"value": round(value, 1), "unit": UNIT, "h2d_bytes_per_step": 0,
                    "d2h_bytes_per_step": 0}}
     print(json.dumps(res), flush=True)

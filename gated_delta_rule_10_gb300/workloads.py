@@ -78,12 +78,19 @@ def _l2norm(x):
 
 
 def make_inputs(variant, B, T, H, dk, dv, dtype=torch.bfloat16, seed=0,
-                q_prescaled=False, h0_std=None, device="cpu"):
+                q_prescaled=False, h0_std=None, device="cpu", gen_device=None):
     """Seeded inputs of one variant (a name or a flag bitmask), [B, T, H, d] layout.
 
     Returns a dict with q, k, v (dtype), g (fp32, [B,T,H] or [B,T,H,d_k]),
     beta / lam (fp32 [B,T,H] or None), b / w (dtype or None), h0 (fp32 or
     None), scale (float), flags (int) and variant.
+
+    gen_device: where the numbers are drawn (default the CPU). The CPU
+    generator is single-threaded, so the full-size workloads (a few hundred
+    million values per tensor) are drawn on the GPU with a seeded CUDA
+    generator instead: same recipe, different stream of numbers, and the
+    tensors stay on that device. Whoever compares two paths hands both the
+    same tensors.
     """
     if isinstance(variant, int):
         flags = variant                    # any flag combination, same recipe per gate
@@ -91,10 +98,11 @@ def make_inputs(variant, B, T, H, dk, dv, dtype=torch.bfloat16, seed=0,
         flags = VARIANT_FLAGS[variant]
     else:
         raise ValueError("unknown variant %r" % variant)
-    gen = torch.Generator().manual_seed(int(seed))
+    gdev = torch.device(gen_device) if gen_device is not None else torch.device("cpu")
+    gen = torch.Generator(device=gdev).manual_seed(int(seed))
 
     def normal(*shape, mean=0.0, std=1.0):
-        return torch.randn(*shape, generator=gen, dtype=torch.float32) * std + mean
+        return torch.randn(*shape, generator=gen, dtype=torch.float32, device=gdev) * std + mean
 
     q = _l2norm(normal(B, T, H, dk))
     k = _l2norm(normal(B, T, H, dk))
@@ -116,7 +124,7 @@ def make_inputs(variant, B, T, H, dk, dv, dtype=torch.bfloat16, seed=0,
     elif not (flags & ERASE_CHANNEL and flags & WRITE_CHANNEL):
         beta = torch.sigmoid(normal(B, T, H))
     if flags & QMIX:
-        lam_h = torch.rand(H, generator=gen, dtype=torch.float32)
+        lam_h = torch.rand(H, generator=gen, dtype=torch.float32, device=gdev)
         lam = lam_h.view(1, 1, H).expand(B, T, H).contiguous()
     if flags & QMIX and beta is not None:
         kf, qf = k.float(), q.float()
@@ -133,17 +141,38 @@ def make_inputs(variant, B, T, H, dk, dv, dtype=torch.bfloat16, seed=0,
         h0 = normal(B, H, dk, dv, std=h0_std)
     out = dict(q=q, k=k, v=v, g=g.contiguous(), beta=beta, lam=lam, b=b, w=w, h0=h0,
                scale=float(scale), flags=flags, variant=variant)
-    if device != "cpu":
+    if gen_device is None and torch.device(device) != gdev:
         out = {key: (val.to(device) if torch.is_tensor(val) else val) for key, val in out.items()}
     return out
 
 
-def config_inputs(cfg_id, device="cpu", **override):
-    """Inputs of one of the five named workloads (prefill part)."""
+def config_inputs(cfg_id, device="cpu", gen_device=None, **override):
+    """Inputs of one of the five named workloads (prefill part); drawn on
+    gen_device when given (and left there)."""
     c = dict(CONFIGS[cfg_id])
     c.update(override)
     return make_inputs(c["variant"], c["B"], c["T"], c["H"], c["dk"], c["dv"], c["dtype"],
-                       c["seed"], c["q_prescaled"], c["h0_std"], device=device)
+                       c["seed"], c["q_prescaled"], c["h0_std"], device=device,
+                       gen_device=gen_device)
+
+
+def decode_phase_inputs(cfg_id=5, seed=None, gen_device=None, steps=None, **override):
+    """The decode phase of a workload (the fifth has one): ``steps`` single-token
+    steps for N sequences of H heads, as [steps, N, H, d] tensors (entry s is
+    step s's contiguous [N, H, d] input, drawn with the prefill recipe), plus
+    the starting states h0 [N, H, d_k, d_v] ~ N(0, h_std^2) fp32."""
+    c = dict(CONFIGS[cfg_id])
+    c.update(override)
+    dec = c["decode"]
+    steps = steps or dec["steps"]
+    seed = c["seed"] + 500 if seed is None else seed
+    y = make_inputs(c["variant"], steps, dec["N"], c["H"], c["dk"], c["dv"], c["dtype"],
+                    seed=seed, gen_device=gen_device)
+    gdev = torch.device(gen_device) if gen_device is not None else torch.device("cpu")
+    gen = torch.Generator(device=gdev).manual_seed(int(seed) + 1)
+    y["h0"] = torch.randn(dec["N"], c["H"], c["dk"], c["dv"], generator=gen,
+                          device=gdev) * dec["h_std"]
+    return y
 
 
 def decode_inputs(variant, N, H, dk, dv, dtype=torch.bfloat16, seed=0, h_std=0.02,
@@ -154,12 +183,14 @@ def decode_inputs(variant, N, H, dk, dv, dtype=torch.bfloat16, seed=0, h_std=0.0
 
 
 def epilogue_inputs(rows, dv, dtype=torch.bfloat16, seed=0, device="cpu"):
-    """Inputs of the output epilogue: o, z [rows, d_v] and weight [d_v]."""
-    gen = torch.Generator().manual_seed(seed)
-    o = (0.05 * torch.randn(rows, dv, generator=gen)).to(dtype)
-    z = torch.randn(rows, dv, generator=gen).to(dtype)
-    weight = 1.0 + 0.1 * torch.randn(dv, generator=gen)
-    return {"o": o.to(device), "z": z.to(device), "weight": weight.to(device)}
+    """Inputs of the output epilogue: o, z [rows, d_v] and weight [d_v], drawn
+    on `device` with a generator seeded there."""
+    dev = torch.device(device)
+    gen = torch.Generator(device=dev).manual_seed(seed)
+    o = (0.05 * torch.randn(rows, dv, generator=gen, device=dev)).to(dtype)
+    z = torch.randn(rows, dv, generator=gen, device=dev).to(dtype)
+    weight = 1.0 + 0.1 * torch.randn(dv, generator=gen, device=dev)
+    return {"o": o, "z": z, "weight": weight}
 
 
 def token_heads(cfg_id):

@@ -37,9 +37,15 @@
  *
  * with one scalar decay per head (g is [B, T, H]). It combines with no other
  * flag (GDR_ERR_UNSUPPORTED) and needs B * H <= 65535. Every column of S then
- * follows its own affine map, so there is no shared (I + T)^{-1}: both
- * gdr_chunk_fwd and gdr_recurrent_step run it as a token-order scan with the
- * state in fp32 registers, and it needs no workspace.
+ * follows its own affine map, so there is no shared (I + T)^{-1}. With bf16
+ * inputs and the full workspace (gdr_chunk_fwd_workspace), gdr_chunk_fwd runs
+ * it chunkwise on the tensor cores: a preparation kernel writes one packet per
+ * chunk (the shared L = tril(decay (.) K K^T, -1), A_qk, the gated q and k, v
+ * and beta) into the workspace, and the state pass solves each value column's
+ * (I + diag(beta_c) L) W_c = diag(beta_c) R_c by substitution. With fp32
+ * inputs or a smaller workspace, gdr_chunk_fwd runs it as a token-order scan
+ * with the state in fp32 registers, which needs no workspace;
+ * gdr_recurrent_step always takes the token-order form.
  *
  * Conventions common to every call:
  *  - Layouts are dense and row-major. Per-token tensors are [B, T, H, d] with
@@ -311,15 +317,26 @@ gdr_status gdr_chunk_fwd_check(const void* workspace, gdr_stream_t stream,
  * scratch, which keeps what the last call left; each call clears the status
  * words it needs on `stream` first. Calls whose work overlaps on the GPU race
  * on the scratch, so order them on one stream. A device-side timeout is
- * recorded in the scratch but not returned; use gdr_chunk_fwd with
- * gdr_chunk_fwd_check when that report matters. The first call on each
- * device looks up the scratch address; make it before any stream capture.
+ * recorded in the scratch; gdr_chunk_fwd_static_check reads it back. The
+ * first call on each device looks up the scratch address; make it before any
+ * stream capture. `stream` must belong to the current device (else
+ * GDR_ERR_INVALID_ARG); a failed lookup or launch clears the cached address,
+ * so the first call after cudaDeviceReset looks it up again.
  */
 gdr_status gdr_chunk_fwd_static(const gdr_shape* shape, const void* q,
                                 const void* k, const void* v, const float* g,
                                 const float* beta, const float* lam,
                                 const void* b, const void* w, const float* h0,
                                 void* o, float* hT, gdr_stream_t stream);
+
+/*
+ * The status the last gdr_chunk_fwd_static call on the current device left in
+ * the library's scratch, read once the work enqueued on `stream` has finished
+ * (this call synchronises the stream), exactly as gdr_chunk_fwd_check reads a
+ * workspace: GDR_OK, or GDR_ERR_TIMEOUT with detail[0] the CTA and detail[1]
+ * 4 * chunk + the wait. No counterpart on the pages either.
+ */
+gdr_status gdr_chunk_fwd_static_check(gdr_stream_t stream, int* detail);
 
 /*
  * One recurrent step for decoding (LLMs from scratch ch. 11, section 11.2,

@@ -86,7 +86,33 @@ def test_backward_no_initial_state():
     check(x, seed=4)
 
 
-def test_backward_gated_deltanet_workload_sampled():
-    """The 4 x 4096 x 16 x 128 bf16 workload; two sequences against the oracle."""
-    x = wl.config_inputs(2)
-    check(x, seed=5, seqs=[(0, 0), (3, 15)])
+def test_backward_gated_deltanet_workload_every_sequence():
+    """The 4 x 4096 x 16 x 128 bf16 workload; every (batch, head) sequence's nine
+    gradients against the oracle."""
+    x = wl.config_inputs(2, gen_device="cuda")
+    check(x, seed=5)
+
+
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16], ids=["f32", "bf16"])
+@pytest.mark.parametrize("flags", [0, 1, 8, 7, 15])
+def test_backward_against_autograd(flags, dtype):
+    """The GPU gradients straight against float64 autograd through the token
+    recurrence (no chunk structure in the reference at all)."""
+    x = wl.make_inputs(flags, 1, 64 * 2 + 5, 2, 64, 128, dtype, seed=400 + flags, h0_std=0.05)
+    dO, dhT = _cotangents(x, 40 + flags)
+    d = to_dev(x)
+    grads = gdr.chunk_bwd(d["q"], d["k"], d["v"], d["g"], dO.cuda(), d["beta"], d["lam"], d["b"],
+                          d["w"], d["h0"], dhT.cuda(), scale=x["scale"], flags=x["flags"])
+    torch.cuda.synchronize()
+    tol = TOL[dtype]
+    for h in range(2):
+        sel = lambda t: None if t is None else f64(t[0, :, h])
+        ref = obw.grad_autograd(*(sel(x[n]) for n in NAMES), S0=f64(x["h0"][0, h]),
+                                scale=x["scale"], flags=x["flags"], dO=sel(dO),
+                                dST=f64(dhT[0, h]))
+        for n in NAMES:
+            if x[n] is None:
+                continue
+            e = rel_err(grads[n][0, :, h].cpu(), ref[n])
+            assert e <= tol, (n, h, e)
+        assert rel_err(grads["h0"][0, h].cpu(), ref["S0"]) <= tol

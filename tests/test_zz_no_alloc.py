@@ -29,10 +29,18 @@ def _static_entry():
     return fn
 
 
-@pytest.mark.parametrize("variant", ["gdn", "gdn2"])   # pipelined and general kernels
-def test_static_scratch_entry_matches_workspace_entry(variant):
+@pytest.mark.parametrize("variant,dtype", [("gdn", torch.bfloat16), ("gdn2", torch.bfloat16),
+                                           ("kda", torch.float32), ("vbeta", torch.bfloat16)],
+                         ids=["gdn-bf16", "gdn2-bf16", "kda-f32", "vbeta-bf16"])
+def test_static_scratch_entry_matches_workspace_entry(variant, dtype):
+    """bf16 scalar and channel gates take the single-kernel path with the status
+    words in the scratch; fp32 and the per-value-channel write strength need no
+    scratch at all (need = 0)."""
     fn = _static_entry()
-    x = wl.make_inputs(variant, 2, 200, 4, 128, 128, torch.bfloat16, seed=123, h0_std=0.02)
+    check = gdr.lib().gdr_chunk_fwd_static_check
+    check.argtypes = [ctypes.c_void_p, ctypes.POINTER(ctypes.c_int)]
+    check.restype = ctypes.c_int
+    x = wl.make_inputs(variant, 2, 200, 4, 128, 128, dtype, seed=123, h0_std=0.02)
     o_ref, h_ref = gpu_forward(x)
     torch.cuda.synchronize()
     d = to_dev(x)
@@ -47,9 +55,11 @@ def test_static_scratch_entry_matches_workspace_entry(variant):
                 ptr(d["beta"]), ptr(d["lam"]), ptr(d["b"]), ptr(d["w"]), ptr(d["h0"]), ptr(o),
                 ptr(hT), stream)
         assert st == 0, gdr.status_string(st)
+        detail = (ctypes.c_int * 2)()
+        assert check(stream, detail) == 0
         torch.cuda.synchronize()
-        assert rel_err(o.float().cpu(), o_ref.float().cpu().numpy()) <= TOL[torch.bfloat16]
-        assert rel_err(hT.cpu(), h_ref.cpu().numpy()) <= TOL[torch.bfloat16]
+        assert rel_err(o.float().cpu(), o_ref.float().cpu().numpy()) <= TOL[dtype]
+        assert rel_err(hT.cpu(), h_ref.cpu().numpy()) <= TOL[dtype]
 
 
 def test_static_scratch_entry_rejects_bad_shapes():
