@@ -54,6 +54,9 @@ def parse():
                    help="decode steps per step (default: the workload's decode phase, else 1)")
     p.add_argument("--no-configs", action="store_true",
                    help="skip timing the other workloads")
+    p.add_argument("--minimal", action="store_true",
+                   help="the step alone: no other workloads, epilogue, gate cumsum, e2e, CPU "
+                        "baseline or side measurements (for profiler runs)")
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-value-beta", action="store_true",
@@ -251,6 +254,10 @@ def fwd_launches(gdr, shape, pipe, ws):
 def run_ours(args):
     import gated_delta_rule_10_gb300 as gdr
 
+    if args.minimal:
+        args.no_configs = args.no_e2e = args.no_cpu_baseline = True
+        args.no_value_beta = args.no_split = args.no_backward = True
+
     rank, world, local = dist_env()
     if world > 1:
         import torch.distributed as dist
@@ -364,7 +371,7 @@ def run_ours(args):
                        "token_heads_per_s": round(th_decode / (statistics.mean(dec_ms) / 1e3), 1),
                        "roofline": droof}
     plain_ms = None
-    if pipe > 1:   # the same inputs through the plain two-kernel call, for comparison
+    if pipe > 1 and not args.minimal:   # the same inputs through the plain two-kernel call
         ws1 = torch.empty(gdr.chunk_fwd_workspace_bytes(shape), dtype=torch.uint8, device=dev)
         plain_ms = time_calls(lambda: gdr.chunk_fwd(
             x["q"], x["k"], x["v"], x["g"], x["beta"], x["lam"], x["b"], x["w"], x["h0"],
@@ -373,8 +380,14 @@ def run_ours(args):
         del ws1
         roof["plain_call_ms"] = round(plain_ms, 4)
 
-    cumsum_info = measure_gate_cumsum(gdr, x, c, dev, stream, flush, min(K, 20), pk, pk_kind)
-    epilogue_info = measure_epilogue(gdr, o, c, dev, stream, flush, min(K, 20), pk)
+    cumsum_info = epilogue_info = None
+    if not args.minimal:
+        cumsum_info = measure_gate_cumsum(gdr, x, c, dev, stream, flush, min(K, 20), pk,
+                                          pk_kind)
+        epilogue_info = measure_epilogue(gdr, o, c, dev, stream, flush, min(K, 20), pk)
+        if c["dtype"] == torch.bfloat16:
+            epilogue_info["fused"] = measure_fused_epilogue(gdr, x, c, dev, stream, flush,
+                                                            min(K, 10), pk, pk_kind, pipe)
     e2e = None if args.no_e2e else measure_e2e(gdr, x, y, c, dev, pipe, dec_steps, N)
     # the other workloads, each timed alone in its default launch configuration
     configs_info = None
@@ -498,6 +511,44 @@ def measure_epilogue(gdr, o, c, dev, stream, flush, K, pk, eps=1e-6):
             "ms_mean": round(ms, 4), "algorithmic_bytes_per_launch": nbytes,
             "achieved_gbs": round(gbs, 1), "frac_hbm": round(gbs / pk["hbm_gbs"], 4),
             "l2": "flushed before every launch"}
+
+
+def measure_fused_epilogue(gdr, x, c, dev, stream, flush, K, pk, pk_kind, pipe, eps=1e-6):
+    """The step's chunked forward with the output epilogue fused into its state
+    pass (gdr_chunk_fwd_gated[_pipelined]), against the same forward followed by
+    the standalone epilogue kernel: K calls each, L2 flushed before every call,
+    CUDA events on the launching stream. Bytes of the fused call: the forward's
+    inputs, z and the gain read, y and the final state written."""
+    B, T, H, dk, dv = c["B"], c["T"], c["H"], c["dk"], c["dv"]
+    e = wl.epilogue_inputs(B * T * H, dv, c["dtype"], seed=11, device=dev)
+    z, weight = e["z"].reshape(B, T, H, dv), e["weight"]
+    y = torch.empty(B, T, H, dv, dtype=c["dtype"], device=dev)
+    hT = torch.empty(B, H, dk, dv, dtype=torch.float32, device=dev)
+    shape = gdr.make_shape(B, T, H, dk, dv, c["dtype"], x["flags"], x["scale"])
+    ws = torch.empty(gdr.chunk_fwd_pipelined_workspace_bytes(shape, pipe) if pipe > 1
+                     else gdr.chunk_fwd_workspace_bytes(shape), dtype=torch.uint8, device=dev)
+    fwd = lambda gate: gdr.chunk_fwd(x["q"], x["k"], x["v"], x["g"], x["beta"], x["lam"], x["b"],
+                                     x["w"], x["h0"], scale=x["scale"], flags=x["flags"], o=y,
+                                     hT=hT, workspace=ws, pipeline=pipe, out_gate=gate)
+    fused_ms = time_calls(lambda: fwd((z, weight, eps)), K, stream, flush)
+    yy = y.reshape(-1, dv)
+
+    def separate():
+        fwd(None)
+        gdr.rmsnorm_gate(yy, z.reshape(-1, dv), weight, eps, out=yy)
+
+    sep_ms = time_calls(separate, K, stream, flush)
+    nbytes = prefill_bytes(x, y, hT) + tensor_bytes(z, weight)
+    th = B * T * H
+    roof = roofline_obj(nbytes, algorithmic_flops_per_th(dk, dv) * th, fused_ms, pk, pk_kind)
+    del ws, y, z, e
+    torch.cuda.empty_cache()
+    return {"workload": c["name"], "fused_ms_mean": round(fused_ms, 4),
+            "forward_then_epilogue_ms_mean": round(sep_ms, 4),
+            "fused_token_heads_per_s": round(th / (fused_ms / 1e3), 1),
+            "kernels": "chunk_prep_kernel + chunk_scan_t_kernel with the epilogue in its output "
+                       "role" + (" x %d time segments" % pipe if pipe > 1 else ""),
+            "launches": K, "roofline": roof, "l2": "flushed before every call"}
 
 
 def fp32_alu_peak_tflops(sm_mhz):

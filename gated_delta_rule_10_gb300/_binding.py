@@ -40,6 +40,11 @@ class Shape(ctypes.Structure):
                 ("flags", ctypes.c_uint), ("scale", ctypes.c_float)]
 
 
+class OutGate(ctypes.Structure):
+    """Mirror of ``gdr_out_gate``."""
+    _fields_ = [("z", ctypes.c_void_p), ("weight", ctypes.c_void_p), ("eps", ctypes.c_float)]
+
+
 _lib = None
 _vp = ctypes.c_void_p
 
@@ -72,6 +77,12 @@ def lib():
         L.gdr_chunk_bwd.argtypes = [sp] + [_vp] * 20 + [_vp, ctypes.c_size_t, _vp]
         L.gdr_rmsnorm_gate.argtypes = [ctypes.c_longlong, ctypes.c_int, ctypes.c_int, _vp, _vp,
                                        _vp, ctypes.c_float, _vp, _vp]
+        gp = ctypes.POINTER(OutGate)
+        L.gdr_chunk_fwd_gated.argtypes = ([sp] + [_vp] * 9 + [gp, _vp, _vp] +
+                                          [_vp, ctypes.c_size_t, _vp])
+        L.gdr_chunk_fwd_gated_pipelined.argtypes = ([sp, ctypes.c_int] + [_vp] * 9 +
+                                                    [gp, _vp, _vp] +
+                                                    [_vp, ctypes.c_size_t, _vp, _vp])
         L.gdr_status_string.argtypes = [ctypes.c_int]
         L.gdr_status_string.restype = ctypes.c_char_p
         L.gdr_abi_version.restype = ctypes.c_int
@@ -80,7 +91,8 @@ def lib():
                      "gdr_chunk_fwd_pipelined", "gdr_chunk_fwd_workspace_pipelined",
                      "gdr_chunk_fwd_pipeline_segments", "gdr_recurrent_step",
                      "gdr_gate_cumsum", "gdr_chunk_fwd_check", "gdr_rmsnorm_gate",
-                     "gdr_chunk_bwd_workspace", "gdr_chunk_bwd"):
+                     "gdr_chunk_bwd_workspace", "gdr_chunk_bwd", "gdr_chunk_fwd_gated",
+                     "gdr_chunk_fwd_gated_pipelined"):
             getattr(L, name).restype = ctypes.c_int
         _lib = L
     return _lib
@@ -183,7 +195,7 @@ def aux_stream(device):
 
 def chunk_fwd(q, k, v, g, beta=None, lam=None, b=None, w=None, h0=None, *, scale=None,
               flags=None, output_final_state=True, o=None, hT=None, workspace=None,
-              segments=None, pipeline=None, aux=None, stream=None):
+              segments=None, pipeline=None, aux=None, stream=None, out_gate=None):
     """Chunkwise forward (``gdr_chunk_fwd``).
 
     q, k: [B, T, H, d_k]; v: [B, T, H, d_v] (bf16 or fp32, one dtype);
@@ -198,8 +210,10 @@ def chunk_fwd(q, k, v, g, beta=None, lam=None, b=None, w=None, h0=None, *, scale
     runs ``gdr_chunk_fwd_pipelined`` with that many time segments, the state
     passes on ``aux`` (default: this module's high-priority auxiliary stream of
     the device; 1: off); by default (no ``workspace`` or ``segments`` given) the
-    library's recommendation is taken. Returns (o, hT) with hT None unless
-    requested.
+    library's recommendation is taken. ``out_gate=(z, weight, eps)`` applies the
+    output epilogue (``gdr_chunk_fwd_gated``): o then holds y = RMSNorm(o) *
+    weight * silu(z) per (token, head) row, z of o's shape and dtype, weight
+    [d_v] fp32. Returns (o, hT) with hT None unless requested.
     """
     B, T, H, dk = q.shape
     dv = v.shape[-1]
@@ -237,6 +251,31 @@ def chunk_fwd(q, k, v, g, beta=None, lam=None, b=None, w=None, h0=None, *, scale
         ws_bytes = chunk_fwd_workspace_bytes(shape, segments=segments)
     if ws_bytes and workspace is None:
         workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+    if out_gate is not None:
+        z, weight, eps = out_gate
+        _check(z, "z", dt, dev, (B, T, H, dv))
+        _check(weight, "weight", torch.float32, dev, (dv,))
+        if segments is not None and segments != 1:
+            raise ValueError("out_gate takes the default or the pipelined path")
+        gate = OutGate(_ptr(z), _ptr(weight), float(eps))
+        ins = (_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(lam), _ptr(b), _ptr(w),
+               _ptr(h0))
+        tail = (_ptr(o), _ptr(hT), _ptr(workspace),
+                ctypes.c_size_t(0 if workspace is None else workspace.numel()),
+                _stream(stream, dev))
+        with torch.cuda.device(dev):
+            if pipeline > 1:
+                name = "gdr_chunk_fwd_gated_pipelined"
+                st = lib().gdr_chunk_fwd_gated_pipelined(
+                    ctypes.byref(shape), int(pipeline), *ins, ctypes.byref(gate), *tail,
+                    _stream(aux if aux is not None else aux_stream(dev), dev))
+            else:
+                name = "gdr_chunk_fwd_gated"
+                st = lib().gdr_chunk_fwd_gated(ctypes.byref(shape), *ins, ctypes.byref(gate),
+                                               *tail)
+        if st:
+            raise GdrError(st, name)
+        return o, hT
     args = (_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(lam), _ptr(b), _ptr(w),
             _ptr(h0), _ptr(o), _ptr(hT), _ptr(workspace),
             ctypes.c_size_t(0 if workspace is None else workspace.numel()), _stream(stream, dev))
@@ -261,13 +300,16 @@ def chunk_fwd_check(workspace, stream=None):
     """Status a chunk_fwd call left in its workspace (synchronises the stream).
 
     Returns None when the call completed; raises GdrError(GDR_ERR_TIMEOUT) when a
-    bounded device-side wait gave up.
+    bounded device-side wait gave up, GdrError(GDR_ERR_RANGE) when a chunk's
+    summed channel log-decay was below the chunked path's limit.
     """
     if workspace is None or workspace.numel() < 256:   # no status words: nothing to check
         return None
     detail = (ctypes.c_int * 2)()
     with torch.cuda.device(workspace.device):
         st = lib().gdr_chunk_fwd_check(_ptr(workspace), _stream(stream, workspace.device), detail)
+    if st == 6:
+        raise GdrError(st, "gdr_chunk_fwd (sequence %d, chunk %d)" % (detail[0], detail[1]))
     if st:
         raise GdrError(st, "gdr_chunk_fwd (CTA %d, wait %d)" % (detail[0], detail[1]))
     return None

@@ -102,7 +102,35 @@ struct LeanLayout {
   static_assert(oK + 128 * DK <= oEa && oV + 128 * DV <= oEa, "the k / v slot");
 };
 
-enum : uint32_t { kBarV = 0, kBarK = 1, kBarM1 = 2, kBarM2 = 3, kBarM2b = 4 };
+// Channel decay with d_k = d_v = 128 (the rho-folded variant, see
+// prep_keys_rf): the [E_bar; Q'] tiles and K_bar until M1 completes, then T
+// inverted in place into A (fp32 [64][65]) with the inverse's scratch over the
+// second Q' block and K_bar, while the E_bar rows stay until M2 (Y_bar = A
+// E_bar); v (then Z in place) and w; the bf16 A tile; the gate sums.
+template <int DK, int DV>
+struct RfLayout {
+  static constexpr uint32_t oEQ = 0;
+  static constexpr uint32_t oK = 256 * DK;
+  static constexpr uint32_t kR1 = 384 * DK;
+  static constexpr uint32_t oT = 24576;                      // Q' rows of block 1, then K_bar
+  static constexpr uint32_t oAf = oT;
+  static constexpr uint32_t oX = oT + 64 * 65 * 4;           // [32][33] inverse scratch
+  static constexpr uint32_t oP = oX + 32 * 33 * 4;           // [4][128] per-warp scratch
+  static constexpr uint32_t oV = kR1;                        // K=64 x DV (B, MN-major)
+  static constexpr uint32_t oEa = oV + 128 * DV;             // w (write gate), until Z is formed
+  static constexpr uint32_t oA = oEa + 128 * DV;             // A 64 x 64 (K-major)
+  static constexpr uint32_t oPart = oA + 8192;               // per-row-block gate sums
+  static constexpr uint32_t oVec = oPart + 8192;
+  static constexpr uint32_t oBar = oVec + 6 * 64 * 4 + 16;   // 5 mbarriers (after a flag word)
+  static constexpr uint32_t oSlot = oBar + 48;
+  static constexpr uint32_t bytes = oSlot + 16;
+  static constexpr uint32_t launch_bytes = bytes + 1024;
+  static constexpr uint32_t kTmemCols = 256;
+  static_assert(DK == 128 && DV == 128, "the rho-folded packets are for d_k = d_v = 128");
+  static_assert(oP + 4 * 128 * 4 <= kR1, "inverse scratch inside the Q' / K_bar region");
+};
+
+enum : uint32_t { kBarV = 0, kBarK = 1, kBarM1 = 2, kBarM2 = 3, kBarM2b = 4, kBarB = 4 };
 
 __device__ __forceinline__ uint4 pack8(const float* x) {
   uint4 u;
@@ -128,6 +156,19 @@ __device__ __forceinline__ uint4 ld16(const unsigned char* base, uint32_t off) {
 }
 __device__ __forceinline__ void st16(unsigned char* base, uint32_t off, uint4 v) {
   *reinterpret_cast<uint4*>(base + off) = v;
+}
+
+// The summed log-decay of a chunk below which the factors e^{+-(G - rho)} of
+// the channel-gate tiles leave the fp32 range (|G - rho| <= -G_C / 2 < 88 with
+// margin); a chunk past it reports GDR_ERR_RANGE into the status words (the
+// first report wins): [1] = batch * H + head, [2] = chunk.
+constexpr float kDecayFloor = -140.f;
+
+__device__ __forceinline__ void report_range(int* status, int seq, int chunk) {
+  if (status && atomicCAS(status, 0, 6) == 0) {   // GDR_ERR_RANGE
+    status[1] = seq;
+    status[2] = chunk;
+  }
 }
 
 // Channel gates, first half of the in-chunk cumsum: thread t loads g for the
@@ -166,7 +207,8 @@ __device__ __forceinline__ void prep_keys(unsigned char* smem, unsigned char* pk
                                           const ChunkArgs& a, const float* sPart,
                                           const float* sBeta, const float* sLam,
                                           const float* sEG, const float* sEGL,
-                                          const float (&gv)[64 * DK / 8 / kThreads][8]) {
+                                          const float (&gv)[64 * DK / 8 / kThreads][8],
+                                          int* status, int seq, int chunk) {
   using L = PrepLayout<DK, DV>;
   using P = Packet<DK, DV>;
   constexpr int VK = DK / 8, RB = kThreads / VK, RPB = 64 / RB;
@@ -199,6 +241,10 @@ __device__ __forceinline__ void prep_keys(unsigned char* smem, unsigned char* pk
       float4* dst = reinterpret_cast<float4*>(pkt + P::oGc + c0 * 4);
       dst[0] = make_float4(gc[0], gc[1], gc[2], gc[3]);
       dst[1] = make_float4(gc[4], gc[5], gc[6], gc[7]);
+      bool low = false;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) low |= tot[j] < kDecayFloor;
+      if (low) report_range(status, seq, chunk);
     }
   }
 #pragma unroll
@@ -236,6 +282,88 @@ __device__ __forceinline__ void prep_keys(unsigned char* smem, unsigned char* pk
     st16(smem, L::oEa + tc::tile_off(64, r, c0), pack8(Ea));
     st16(pkt, P::oQY + tc::tile_off(128, r, c0), pack8(Qg));
     st16(pkt, P::oKt + tc::tile_off(64, r, c0), pack8(Kt));
+  }
+}
+
+// Channel decay, d_k = d_v = 128 (packets for the transposed scan): the decay
+// factors e^{+-(G - rho)} with rho = G_C / 2 per key channel form only the
+// tiles M1 needs, E_bar = f (.) e, Q' = s f (.) q and K_bar = f^-1 (.) k with
+// f = e^{G - rho}; the packet takes Q' (rows 0..63 of its [Q_gamma; -Y] tile),
+// K_bar (in K_tail's place), gamma_C and e^{rho}. The factor e^{rho} that
+// turns them into Q_gamma = e^{rho} (.) Q', K_tail = e^{rho} (.) K_bar and
+// E_abs = e^{rho} (.) E_bar (so Y = A E_bar diag(e^{rho})) is per key
+// channel, so the scan applies it to the rows of S instead:
+//   [Q_gamma; -Y] S_n = [Q'; -A E_bar] (diag(e^rho) S_n),
+//   K_tail^T W = diag(e^rho) K_bar^T W.
+template <int DK, int DV, bool ER, bool QM>
+__device__ __forceinline__ void prep_keys_rf(unsigned char* smem, unsigned char* pkt,
+                                             const ChunkArgs& a, const float* sPart,
+                                             const float* sBeta, const float* sLam,
+                                             const float (&gv)[64 * DK / 8 / kThreads][8],
+                                             int* status, int seq, int chunk) {
+  using L = RfLayout<DK, DV>;
+  using P = Packet<DK, DV>;
+  constexpr int VK = DK / 8, RB = kThreads / VK, RPB = 64 / RB;
+  const int tid = threadIdx.x, rb = tid / VK, c0 = (tid % VK) * 8, r0 = rb * RPB;
+  float G[8], rho[8], tot[8];
+#pragma unroll
+  for (int j = 0; j < 8; ++j) { G[j] = 0.f; tot[j] = 0.f; }
+#pragma unroll
+  for (int b = 0; b < RB; ++b) {
+    const float4* src = reinterpret_cast<const float4*>(sPart + b * DK + c0);
+    const float4 x0 = src[0], x1 = src[1];
+    const float x[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      tot[j] += x[j];
+      G[j] += select_f32(b < rb, x[j], 0.f);
+    }
+  }
+#pragma unroll
+  for (int j = 0; j < 8; ++j) rho[j] = 0.5f * tot[j];
+  if (rb == 0) {
+    bool low = false;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) low |= tot[j] < kDecayFloor;
+    if (low) report_range(status, seq, chunk);
+    float gc[8], er[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      gc[j] = __expf(tot[j]);
+      er[j] = __expf(rho[j]);
+    }
+    float4* dst = reinterpret_cast<float4*>(pkt + P::oGc + c0 * 4);
+    dst[0] = make_float4(gc[0], gc[1], gc[2], gc[3]);
+    dst[1] = make_float4(gc[4], gc[5], gc[6], gc[7]);
+    float4* dre = reinterpret_cast<float4*>(pkt + P::oGc + (DK + c0) * 4);
+    dre[0] = make_float4(er[0], er[1], er[2], er[3]);
+    dre[1] = make_float4(er[4], er[5], er[6], er[7]);
+  }
+#pragma unroll
+  for (int i = 0; i < RPB; ++i) {
+    const int r = r0 + i;
+    float qv[8], kv[8], bv[8];
+    unpack8(ld16(smem, L::oEQ + tc::tile_off(128, 64 + r, c0)), qv);
+    unpack8(ld16(smem, L::oK + tc::tile_off(64, r, c0)), kv);
+    if (ER) unpack8(ld16(smem, L::oEQ + tc::tile_off(128, r, c0)), bv);
+    const float lam = sLam[r], beta = sBeta[r];
+    float Eb[8], Qr[8], Kb[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const float x = QM ? kv[j] + lam * qv[j] : kv[j];
+      const float e = ER ? bv[j] * x : beta * x;
+      G[j] += gv[i][j];
+      const float f = __expf(G[j] - rho[j]), fi = __expf(rho[j] - G[j]);
+      Eb[j] = f * e;
+      Qr[j] = a.scale * f * qv[j];
+      Kb[j] = fi * kv[j];
+    }
+    const uint4 qr = pack8(Qr), kb = pack8(Kb);
+    st16(smem, L::oEQ + tc::tile_off(128, r, c0), pack8(Eb));
+    st16(smem, L::oEQ + tc::tile_off(128, 64 + r, c0), qr);
+    st16(smem, L::oK + tc::tile_off(64, r, c0), kb);
+    st16(pkt, P::oQY + tc::tile_off(128, r, c0), qr);
+    st16(pkt, P::oKt + tc::tile_off(64, r, c0), kb);
   }
 }
 
@@ -336,10 +464,23 @@ __device__ __forceinline__ void prep_values_vb(const unsigned char* smem, unsign
   }
 }
 
+// U^T (M=128 accumulator in tensor-memory columns 0..63: lane c = value column,
+// column r = token) into the packet's U region as a 128-row tile of 64 tokens:
+// warp w reads lane quadrant w % 4, tokens 32 (w / 4) .. +31, and each thread
+// writes four 16-byte pieces of its value column's row.
+__device__ __forceinline__ void store_ut(unsigned char* pkt, uint32_t tmem, int warp, int lane) {
+  using P = Packet<128, 128>;
+  const int q = warp & 3, half = warp >> 2, c = 32 * q + lane;
+  float x[32];
+  tc::tmem_ld32(tmem + (static_cast<uint32_t>(32 * q) << 16) + 32 * half, x);
+#pragma unroll
+  for (int j = 0; j < 32; j += 8)
+    st16(pkt, P::oU + tc::tile_off(128, c, 32 * half + j), pack8(x + j));
+}
+
 // Z = beta v (or w (.) v with the write gate), in place over v.
-template <int DK, int DV, bool WR>
+template <int DK, int DV, bool WR, typename L>
 __device__ __forceinline__ void prep_z(unsigned char* smem, const float* sBeta) {
-  using L = PrepLayout<DK, DV>;
   constexpr int VV = DV / 8, kIter = 64 * VV / kThreads;
   const int tid = threadIdx.x;
   uint4 vr[kIter], wr[WR ? kIter : 1];
@@ -362,7 +503,7 @@ __device__ __forceinline__ void prep_z(unsigned char* smem, const float* sBeta) 
   }
 }
 
-template <int DK, int DV, bool SC, bool VB, bool DYN, bool LEAN>
+template <int DK, int DV, bool SC, bool VB, bool DYN, bool LEAN, bool RF>
 __global__ void __launch_bounds__(kThreads, LEAN ? 3 : 2)
     chunk_prep_kernel(const ChunkArgs a, const __grid_constant__ CUtensorMap tm_q,
                       const __grid_constant__ CUtensorMap tm_k,
@@ -370,10 +511,16 @@ __global__ void __launch_bounds__(kThreads, LEAN ? 3 : 2)
                       const __grid_constant__ CUtensorMap tm_b,
                       const __grid_constant__ CUtensorMap tm_w, unsigned char* packets,
                       int* status, const PrepRange rg) {
-  using L = std::conditional_t<LEAN, LeanLayout<DK, DV>, PrepLayout<DK, DV>>;
+  // RF: channel decay with d_k = d_v = 128, rho-folded packets (prep_keys_rf)
+  using L = std::conditional_t<LEAN, LeanLayout<DK, DV>,
+                               std::conditional_t<RF, RfLayout<DK, DV>, PrepLayout<DK, DV>>>;
   using P = std::conditional_t<VB, PacketVB<DK, DV>, Packet<DK, DV>>;
   static_assert(!VB || SC, "the value-channel packets take the scalar-gate tiles");
+  static_assert(!RF || (!SC && !LEAN && !VB && DK == 128 && DV == 128), "rho-folded variant");
   static_assert(!LEAN || (SC && !VB), "the lean variant is for scalar gates");
+  // d_k = d_v = 128: the packet carries U^T (d_v rows of 64 tokens) for the
+  // transposed scan (chunk_scan_t.cu), produced directly as Z^T A^T
+  constexpr bool UT = DK == 128 && DV == 128 && !VB;
   extern __shared__ unsigned char smem_raw[];
   unsigned char* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   const uint32_t sbase = smem_u32(smem);
@@ -404,7 +551,7 @@ __global__ void __launch_bounds__(kThreads, LEAN ? 3 : 2)
 
   if (warp == 0) tc::tmem_alloc(smem_u32(tslot), L::kTmemCols);
   if (tid == 32) {
-    for (uint32_t i = 0; i < (LEAN ? 5u : 4u); ++i) tc::mbar_init(bar(i), 1);
+    for (uint32_t i = 0; i < ((LEAN || RF) ? 5u : 4u); ++i) tc::mbar_init(bar(i), 1);
     tc::fence_mbar_init();
   }
   tc::fence_before_sync();
@@ -454,11 +601,23 @@ __global__ void __launch_bounds__(kThreads, LEAN ? 3 : 2)
       }
     }
   };
+  // RF: the erase gate b (over the E_bar rows, which M2 reads) has a barrier
+  // of its own and is loaded after M2; q and k as soon as the inverse is done
+  auto load_b = [&](int w) {
+    int n, bb, h;
+    decode(w, n, bb, h);
+    tc::fence_proxy_async();
+    tc::mbar_arrive_expect_tx(bar(kBarB), 128u * DK);
+#pragma unroll
+    for (int blk = 0; blk < DK / 64; ++blk)
+      tc::tma_load_4d(sbase + L::oEQ + blk * 16384, &tm_b, blk * 64, h, n * kChunk, bb, bar(kBarB));
+  };
+  const bool bsep = RF && ER;
   auto load_keys = [&](int w, int w_after) {
     int n, bb, h;
     decode(w, n, bb, h);
     tc::fence_proxy_async();
-    tc::mbar_arrive_expect_tx(bar(kBarK), (ER ? 3u : 2u) * 128u * DK);
+    tc::mbar_arrive_expect_tx(bar(kBarK), ((ER && !bsep) ? 3u : 2u) * 128u * DK);
 #pragma unroll
     for (int blk = 0; blk < DK / 64; ++blk) {
       tc::tma_load_4d(sbase + L::oEQ + blk * 16384 + 8192, &tm_q, blk * 64, h, n * kChunk, bb, bar(kBarK));
@@ -466,7 +625,8 @@ __global__ void __launch_bounds__(kThreads, LEAN ? 3 : 2)
         tc::tma_load_4d(sbase + L::oEQ + blk * 16384, &tm_k, blk * 64, h, n * kChunk, bb, bar(kBarK));
       else
         tc::tma_load_4d(sbase + L::oK + blk * 8192, &tm_k, blk * 64, h, n * kChunk, bb, bar(kBarK));
-      if (ER) tc::tma_load_4d(sbase + L::oEQ + blk * 16384, &tm_b, blk * 64, h, n * kChunk, bb, bar(kBarK));
+      if (ER && !bsep)
+        tc::tma_load_4d(sbase + L::oEQ + blk * 16384, &tm_b, blk * 64, h, n * kChunk, bb, bar(kBarK));
     }
     if (w_after < total) {
       decode(w_after, n, bb, h);
@@ -479,7 +639,7 @@ __global__ void __launch_bounds__(kThreads, LEAN ? 3 : 2)
     }
   };
   // loads issued and waited for, to drain what is in flight on the way out
-  int v_issued = 0, k_issued = 0, v_done = 0, k_done = 0;
+  int v_issued = 0, k_issued = 0, v_done = 0, k_done = 0, b_issued = 0, b_done = 0;
   constexpr bool dyn = DYN;   // work claimed from rg.counter
   const int stride = static_cast<int>(gridDim.x);
   int w = static_cast<int>(blockIdx.x), wn = w + stride, wa = wn + stride;   // this, next, after
@@ -498,9 +658,11 @@ __global__ void __launch_bounds__(kThreads, LEAN ? 3 : 2)
     if (tid == 64) {
       if (!vlate) load_values(w, wn);
       load_keys(w, wn);
+      if (bsep) load_b(w);
     }
     v_issued = vlate ? 0 : 1;
     k_issued = 1;
+    b_issued = bsep ? 1 : 0;
   }
 
   int fail_at = -1, iter = 0;
@@ -575,7 +737,7 @@ __global__ void __launch_bounds__(kThreads, LEAN ? 3 : 2)
     if (CH) load_channel_gates<DK>(a, row0, h, Lr, sPart, gv);
     __syncthreads();
 
-    if (!vlate) {
+    if (!vlate && !RF) {   // (RF: the value side is waited for after the inverse)
       if (__syncthreads_or(!tc::mbar_wait(bar(kBarV), par))) { fail_at = 4 * n; break; }
       v_done = v_issued;
     }
@@ -587,15 +749,20 @@ __global__ void __launch_bounds__(kThreads, LEAN ? 3 : 2)
         ++v_issued;
       }
     }
-    if (!SC) {
+    if (!SC && !RF) {
       if (WR)
-        prep_z<DK, DV, true>(smem, sBeta);
+        prep_z<DK, DV, true, L>(smem, sBeta);
       else
-        prep_z<DK, DV, false>(smem, sBeta);
+        prep_z<DK, DV, false, L>(smem, sBeta);
       __syncthreads();   // w has been read: its slot takes E_abs below
     }
-    if (__syncthreads_or(!tc::mbar_wait(bar(kBarK), par))) { fail_at = 4 * n; break; }
+    if (__syncthreads_or(!tc::mbar_wait(bar(kBarK), par) ||
+                         (bsep && !tc::mbar_wait(bar(kBarB), par)))) {
+      fail_at = 4 * n;
+      break;
+    }
     k_done = k_issued;
+    b_done = b_issued;
     if (VB) {
       prep_keys_vb<DK, DV>(smem, pkt, a, sEG, sEGL);
     } else if (SC) {
@@ -610,11 +777,31 @@ __global__ void __launch_bounds__(kThreads, LEAN ? 3 : 2)
         else
           prep_keys_scalar<DK, DV, false, L>(smem, pkt, a, sLam, sEG, sEGL);
       }
+    } else if constexpr (RF) {   // channel decay (launched only with it)
+      switch (a.flags & 10u) {
+        case 0:
+          prep_keys_rf<DK, DV, false, false>(smem, pkt, a, sPart, sBeta, sLam, gv, status,
+                                             bb * H + h, n);
+          break;
+        case 2:
+          prep_keys_rf<DK, DV, true, false>(smem, pkt, a, sPart, sBeta, sLam, gv, status,
+                                            bb * H + h, n);
+          break;
+        case 8:
+          prep_keys_rf<DK, DV, false, true>(smem, pkt, a, sPart, sBeta, sLam, gv, status,
+                                            bb * H + h, n);
+          break;
+        default:
+          prep_keys_rf<DK, DV, true, true>(smem, pkt, a, sPart, sBeta, sLam, gv, status,
+                                           bb * H + h, n);
+          break;
+      }
     } else switch (a.flags & 11u) {   // CH | ER | QM select the key-side tiles
 #define GDR_PREP(F)                                                                       \
   case F:                                                                                 \
     prep_keys<DK, DV, (F & 1u) != 0, (F & 2u) != 0, (F & 8u) != 0>(smem, pkt, a, sPart, sBeta, \
-                                                                   sLam, sEG, sEGL, gv);  \
+                                                                   sLam, sEG, sEGL, gv,   \
+                                                                   status, bb * H + h, n); \
     break;
       GDR_PREP(0) GDR_PREP(1) GDR_PREP(2) GDR_PREP(3)
       GDR_PREP(8) GDR_PREP(9) GDR_PREP(10) GDR_PREP(11)
@@ -701,7 +888,7 @@ __global__ void __launch_bounds__(kThreads, LEAN ? 3 : 2)
     }
 
     // ---- A = (I + T)^{-1} (all 8 warps), then the bf16 operand tile ----
-    if constexpr (LEAN)
+    if constexpr (LEAN || RF)
       invert_unit_lower_64_w8_inplace(sT, sP, reinterpret_cast<float*>(smem + L::oX), warp, lane,
                                       [] { tc::named_sync(kInvBar, 128); },
                                       [] { __syncthreads(); });
@@ -744,11 +931,18 @@ __global__ void __launch_bounds__(kThreads, LEAN ? 3 : 2)
       }
       if (tid == 0) {
         tc::fence_after_sync();
-        constexpr uint32_t idu = tc::idesc_bf16(64, DV, 0, 1);
         const uint64_t dZ = tc::smem_desc(sbase + L::oV, 64 * 128, 1024);
+        if constexpr (UT) {   // U^T = Z^T A^T: Z as the MN-major A, the A tile as a K-major B
+          constexpr uint32_t idu = tc::idesc_bf16(128, 64, 1, 0);
 #pragma unroll
-        for (int k0 = 0; k0 < 64; k0 += 16)
-          tc::mma_bf16(tmem, dA + ((k0 * 2) >> 4), dZ + (((k0 / 8) * 1024) >> 4), idu, k0 > 0);
+          for (int k0 = 0; k0 < 64; k0 += 16)
+            tc::mma_bf16(tmem, dZ + (((k0 / 8) * 1024) >> 4), dA + ((k0 * 2) >> 4), idu, k0 > 0);
+        } else {
+          constexpr uint32_t idu = tc::idesc_bf16(64, DV, 0, 1);
+#pragma unroll
+          for (int k0 = 0; k0 < 64; k0 += 16)
+            tc::mma_bf16(tmem, dA + ((k0 * 2) >> 4), dZ + (((k0 / 8) * 1024) >> 4), idu, k0 > 0);
+        }
         tc::commit(bar(kBarM2));
       }
       if (__syncthreads_or(!tc::mbar_wait(bar(kBarM2), par))) { fail_at = 4 * n + 2; break; }
@@ -759,13 +953,17 @@ __global__ void __launch_bounds__(kThreads, LEAN ? 3 : 2)
         if (tid == 64) load_values(wn, wa);
         ++v_issued;
       }
+      if constexpr (UT) {
+        store_ut(pkt, tmem, warp, lane);
+      } else {
 #pragma unroll
-      for (int c = half * (DV / 2); c < (half + 1) * (DV / 2); c += 32) {
-        float x[32];
-        tc::tmem_ld32(tl + c, x);
-        if (lane < 16) {
+        for (int c = half * (DV / 2); c < (half + 1) * (DV / 2); c += 32) {
+          float x[32];
+          tc::tmem_ld32(tl + c, x);
+          if (lane < 16) {
 #pragma unroll
-          for (int j = 0; j < 32; j += 8) st16(pkt, P::oU + tc::tile_off(64, r, c + j), pack8(x + j));
+            for (int j = 0; j < 32; j += 8) st16(pkt, P::oU + tc::tile_off(64, r, c + j), pack8(x + j));
+          }
         }
       }
       tc::fence_before_sync();
@@ -773,7 +971,8 @@ __global__ void __launch_bounds__(kThreads, LEAN ? 3 : 2)
       if (tid == 0) {
         tc::fence_after_sync();
         constexpr uint32_t idy = tc::idesc_bf16(64, DK, 0, 1);
-        const uint64_t dE = tc::smem_desc(sbase + L::oEa, 64 * 128, 1024);
+        const uint64_t dE = RF ? tc::smem_desc(sbase + L::oEQ, 128 * 128, 1024)
+                               : tc::smem_desc(sbase + L::oEa, 64 * 128, 1024);
 #pragma unroll
         for (int k0 = 0; k0 < 64; k0 += 16)
           tc::mma_bf16(tmem, dA + ((k0 * 2) >> 4), dE + (((k0 / 8) * 1024) >> 4), idy, k0 > 0);
@@ -801,22 +1000,55 @@ __global__ void __launch_bounds__(kThreads, LEAN ? 3 : 2)
     } else {
     // ---- M2: [U | Y] = A [Z | E_abs] (N = DV + DK): U in columns 0..DV-1,
     // Y in columns DV..DV+DK-1 ----
+    if constexpr (RF) {
+      // the value side, loaded since the start of the chunk: Z = w (.) v or beta v
+      if (__syncthreads_or(!tc::mbar_wait(bar(kBarV), par))) { fail_at = 4 * n + 2; break; }
+      v_done = v_issued;
+      if (WR)
+        prep_z<DK, DV, true, L>(smem, sBeta);
+      else
+        prep_z<DK, DV, false, L>(smem, sBeta);
+      tc::fence_proxy_async();
+      __syncthreads();
+    }
+    // (U^T case: U^T = Z^T A^T in columns 0..63, Y in columns 64..64+DK-1;
+    // RF: Y_bar = A E_bar from the E_bar rows of the [E_bar; Q'] tile)
+    constexpr uint32_t kYcol = UT ? 64 : DV;
     if (tid == 0) {
       tc::fence_after_sync();
-      constexpr uint32_t id2 = tc::idesc_bf16(64, DV + DK, 0, 1);
       const uint64_t dA = tc::smem_desc(sbase + L::oA, 16, 1024);
       const uint64_t dZE = tc::smem_desc(sbase + L::oV, 64 * 128, 1024);
+      if constexpr (UT) {
+        constexpr uint32_t idu = tc::idesc_bf16(128, 64, 1, 0);
+        constexpr uint32_t idy = tc::idesc_bf16(64, DK, 0, 1);
+        const uint64_t dE = RF ? tc::smem_desc(sbase + L::oEQ, 128 * 128, 1024)
+                               : tc::smem_desc(sbase + L::oEa, 64 * 128, 1024);
 #pragma unroll
-      for (int k0 = 0; k0 < 64; k0 += 16)
-        tc::mma_bf16(tmem, dA + ((k0 * 2) >> 4), dZE + (((k0 / 8) * 1024) >> 4), id2, k0 > 0);
+        for (int k0 = 0; k0 < 64; k0 += 16)
+          tc::mma_bf16(tmem, dZE + (((k0 / 8) * 1024) >> 4), dA + ((k0 * 2) >> 4), idu, k0 > 0);
+#pragma unroll
+        for (int k0 = 0; k0 < 64; k0 += 16)
+          tc::mma_bf16(tmem + kYcol, dA + ((k0 * 2) >> 4), dE + (((k0 / 8) * 1024) >> 4), idy,
+                       k0 > 0);
+      } else {
+        constexpr uint32_t id2 = tc::idesc_bf16(64, DV + DK, 0, 1);
+#pragma unroll
+        for (int k0 = 0; k0 < 64; k0 += 16)
+          tc::mma_bf16(tmem, dA + ((k0 * 2) >> 4), dZE + (((k0 / 8) * 1024) >> 4), id2, k0 > 0);
+      }
       tc::commit(bar(kBarM2));
     }
     if (__syncthreads_or(!tc::mbar_wait(bar(kBarM2), par))) { fail_at = 4 * n + 2; break; }
     tc::fence_after_sync();
     // Z and E_abs are consumed: the value-side tiles of the next chunk may land now
+    // (RF: and the key side, E_bar being consumed too)
     if (wn < total) {
-      if (tid == 64) load_values(wn, wa);
+      if (tid == 64) {
+        load_values(wn, wa);
+        if (bsep) load_b(wn);
+      }
       ++v_issued;
+      if (bsep) ++b_issued;
     }
     {
       // M=64 accumulators: row 16 q + l in lane l < 16 of quadrant q; warp w
@@ -827,7 +1059,7 @@ __global__ void __launch_bounds__(kThreads, LEAN ? 3 : 2)
 #pragma unroll
       for (int c = half * (DK / 2); c < (half + 1) * (DK / 2); c += 32) {
         float x[32];
-        tc::tmem_ld32(tl + DV + c, x);
+        tc::tmem_ld32(tl + kYcol + c, x);
 #pragma unroll
         for (int j = 0; j < 32; ++j) x[j] = -x[j];
         if (lane < 16) {
@@ -836,13 +1068,17 @@ __global__ void __launch_bounds__(kThreads, LEAN ? 3 : 2)
             st16(pkt, P::oQY + tc::tile_off(128, 64 + r, c + j), pack8(x + j));
         }
       }
+      if constexpr (UT) {
+        store_ut(pkt, tmem, warp, lane);
+      } else {
 #pragma unroll
-      for (int c = half * (DV / 2); c < (half + 1) * (DV / 2); c += 32) {
-        float x[32];
-        tc::tmem_ld32(tl + c, x);
-        if (lane < 16) {
+        for (int c = half * (DV / 2); c < (half + 1) * (DV / 2); c += 32) {
+          float x[32];
+          tc::tmem_ld32(tl + c, x);
+          if (lane < 16) {
 #pragma unroll
-          for (int j = 0; j < 32; j += 8) st16(pkt, P::oU + tc::tile_off(64, r, c + j), pack8(x + j));
+            for (int j = 0; j < 32; j += 8) st16(pkt, P::oU + tc::tile_off(64, r, c + j), pack8(x + j));
+          }
         }
       }
     }
@@ -859,6 +1095,7 @@ __global__ void __launch_bounds__(kThreads, LEAN ? 3 : 2)
     if (tid == 64) {
       if (v_issued > v_done) tc::mbar_wait(bar(kBarV), static_cast<uint32_t>((v_issued - 1) & 1));
       if (k_issued > k_done) tc::mbar_wait(bar(kBarK), static_cast<uint32_t>((k_issued - 1) & 1));
+      if (b_issued > b_done) tc::mbar_wait(bar(kBarB), static_cast<uint32_t>((b_issued - 1) & 1));
     }
     if (tid == 0 && status && atomicCAS(status, 0, 5) == 0) {  // GDR_ERR_TIMEOUT
       status[1] = static_cast<int>(blockIdx.x);
@@ -870,10 +1107,11 @@ __global__ void __launch_bounds__(kThreads, LEAN ? 3 : 2)
   if (warp == 0) tc::tmem_dealloc(tmem, L::kTmemCols);
 }
 
-template <int DK, int DV, bool SC, bool VB, bool DYN, bool LEAN = false>
+template <int DK, int DV, bool SC, bool VB, bool DYN, bool LEAN = false, bool RF = false>
 cudaError_t launch_prep_kernel(const ChunkArgs& a, unsigned char* packets, int* status,
                                const PrepRange& rg, cudaStream_t stream) {
-  using L = std::conditional_t<LEAN, LeanLayout<DK, DV>, PrepLayout<DK, DV>>;
+  using L = std::conditional_t<LEAN, LeanLayout<DK, DV>,
+                               std::conditional_t<RF, RfLayout<DK, DV>, PrepLayout<DK, DV>>>;
   constexpr int kPerSm = LEAN ? 3 : 2;
   static_assert(kPerSm * (L::launch_bytes + 1024) <= 233472, "CTAs per SM");
   CUtensorMap tq, tk, tv, tb, tw;
@@ -884,7 +1122,7 @@ cudaError_t launch_prep_kernel(const ChunkArgs& a, unsigned char* packets, int* 
   tw = tq;
   if ((a.flags & 2u) && !make_bthd_tmap(&tb, a.b, a.B, a.T, a.H, DK)) return cudaErrorInvalidValue;
   if ((a.flags & 4u) && !make_bthd_tmap(&tw, a.w, a.B, a.T, a.H, DV)) return cudaErrorInvalidValue;
-  auto kern = chunk_prep_kernel<DK, DV, SC, VB, DYN, LEAN>;
+  auto kern = chunk_prep_kernel<DK, DV, SC, VB, DYN, LEAN, RF>;
   cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(L::launch_bytes));
   if (err != cudaSuccess) return err;
@@ -920,6 +1158,11 @@ cudaError_t launch_prep(const ChunkArgs& a, unsigned char* packets, int* status,
     return launch_prep_kernel<DK, DV, true, true, DYN>(a, packets, status, rg, stream);
   if ((a.flags & 7u) == 0)   // scalar gates: three CTAs per SM
     return launch_prep_kernel<DK, DV, true, false, DYN, true>(a, packets, status, rg, stream);
+  if constexpr (DK == 128 && DV == 128) {   // channel decay: rho-folded packets
+    if (a.flags & 1u)
+      return launch_prep_kernel<DK, DV, false, false, DYN, false, true>(a, packets, status, rg,
+                                                                        stream);
+  }
   return launch_prep_kernel<DK, DV, false, false, DYN>(a, packets, status, rg, stream);
 }
 

@@ -508,6 +508,9 @@ cudaError_t launch_chunk_scan(const ChunkArgs& a, int dk, const unsigned char* p
                               int* status, cudaStream_t stream, const ScanSegments& sg) {
   // the write strength per value channel (flag 16) takes the substitution variant
   if (a.flags & 16u) return launch_scan_dims<true>(a, dk, packets, status, stream, sg);
+  // d_k = d_v = 128: the transposed kernel (one CTA per (batch, head), U^T packets)
+  if (scan_transposed(dk, a.dv, a.flags))
+    return launch_chunk_scan_t(a, dk, packets, status, stream, sg);
   return launch_scan_dims<false>(a, dk, packets, status, stream, sg);
 }
 

@@ -150,6 +150,8 @@ const char* gdr_status_string(gdr_status status) {
     case GDR_ERR_CUDA: return "GDR_ERR_CUDA: the CUDA runtime reported an error";
     case GDR_ERR_WORKSPACE: return "GDR_ERR_WORKSPACE: workspace missing or too small";
     case GDR_ERR_TIMEOUT: return "GDR_ERR_TIMEOUT: a bounded device-side wait gave up";
+    case GDR_ERR_RANGE:
+      return "GDR_ERR_RANGE: a chunk's summed channel log-decay is below the chunked path's limit";
   }
   return "unknown gdr_status";
 }
@@ -199,14 +201,38 @@ namespace {
 
 // The chunked forward with `segments` runs per (batch, head) for the two-kernel
 // path (0: the default policy).
+// The output epilogue's arguments: valid, and y apart from z.
+gdr_status check_out_gate(const gdr_shape* s, const gdr_out_gate* gate, const void* y) {
+  if (!gate || !gate->z || !gate->weight) return GDR_ERR_INVALID_ARG;
+  if (!aligned(gate->z, 16) || !aligned(gate->weight, 16)) return GDR_ERR_INVALID_ARG;
+  if (!std::isfinite(gate->eps) || gate->eps < 0.f) return GDR_ERR_INVALID_ARG;
+  if (s->dv != 64 && s->dv != 128) return GDR_ERR_UNSUPPORTED;
+  const uintptr_t bytes = static_cast<uintptr_t>(s->B) * s->T * s->H * s->dv *
+                          (s->dtype == GDR_F32 ? 4 : 2);
+  const uintptr_t py = reinterpret_cast<uintptr_t>(y), pz = reinterpret_cast<uintptr_t>(gate->z);
+  if (pz < py + bytes && py < pz + bytes) return GDR_ERR_INVALID_ARG;
+  return GDR_OK;
+}
+
+// Applies the epilogue in place on the forward's output (the shapes whose state
+// pass does not fuse it).
+cudaError_t out_gate_after(const gdr_shape* s, const gdr_out_gate* gate, void* y,
+                           cudaStream_t st_) {
+  return gdr::launch_rmsnorm_gate(y, gate->z, gate->weight, gate->eps, y,
+                                  static_cast<long long>(s->B) * s->T * s->H, s->dv,
+                                  s->dtype == GDR_F32, st_);
+}
+
 gdr_status chunk_fwd_impl(const gdr_shape* shape, int segments, const void* q, const void* k,
                           const void* v, const float* g, const float* beta, const float* lam,
                           const void* b, const void* w, const float* h0, void* o, float* hT,
-                          void* workspace, size_t ws_bytes, gdr_stream_t stream) {
+                          void* workspace, size_t ws_bytes, gdr_stream_t stream,
+                          const gdr_out_gate* gate = nullptr) {
   gdr_status st = check_shape(shape, false);
   if (st != GDR_OK) return st;
   st = check_gates(shape, q, k, v, g, beta, lam, b, w, o);
   if (st != GDR_OK) return st;
+  if (gate && (st = check_out_gate(shape, gate, o)) != GDR_OK) return st;
   if ((h0 && !aligned(h0, 16)) || (hT && !aligned(hT, 16))) return GDR_ERR_INVALID_ARG;
   const bool forced = segments > 0;
   if (forced && segments > 1 && !split_allowed(shape)) return GDR_ERR_UNSUPPORTED;
@@ -226,9 +252,11 @@ gdr_status chunk_fwd_impl(const gdr_shape* shape, int segments, const void* q, c
   // workspace) or the token-order scan
   if ((shape->flags & GDR_BETA_CHANNEL) &&
       (f32 || !workspace || ws_bytes < two_kernel_bytes(shape) || !aligned(workspace, 16))) {
-    const cudaError_t err = gdr::launch_value_beta_scan(
+    cudaError_t err = gdr::launch_value_beta_scan(
         value_beta_args(shape, q, k, v, g, beta, h0, o, hT), shape->dk, shape->dv, f32,
         reinterpret_cast<cudaStream_t>(stream));
+    if (err == cudaSuccess && gate)
+      err = out_gate_after(shape, gate, o, reinterpret_cast<cudaStream_t>(stream));
     return err == cudaSuccess ? GDR_OK : GDR_ERR_CUDA;
   }
   gdr::ChunkArgs a;
@@ -237,6 +265,14 @@ gdr_status chunk_fwd_impl(const gdr_shape* shape, int segments, const void* q, c
   a.B = shape->B; a.T = shape->T; a.H = shape->H; a.dv = shape->dv;
   a.flags = shape->flags; a.scale = shape->scale;
   const cudaStream_t st_ = reinterpret_cast<cudaStream_t>(stream);
+  // the epilogue rides in the state pass where the transposed scan runs
+  const bool fused = gate && !f32 && ws_bytes >= two_kernel_bytes(shape) &&
+                     gdr::scan_transposed(shape->dk, shape->dv, shape->flags);
+  if (fused) {
+    a.gz = gate->z;
+    a.gw = gate->weight;
+    a.geps = gate->eps;
+  }
   cudaError_t err;
   if (f32) {
     err = gdr::launch_chunk_fwd_f32(a, shape->dk, st_);
@@ -300,6 +336,7 @@ gdr_status chunk_fwd_impl(const gdr_shape* shape, int segments, const void* q, c
       }
     }
   }
+  if (err == cudaSuccess && gate && !fused) err = out_gate_after(shape, gate, o, st_);
   return err == cudaSuccess ? GDR_OK : GDR_ERR_CUDA;
 }
 
@@ -331,12 +368,13 @@ gdr_status chunk_fwd_pipelined_impl(const gdr_shape* shape, int segments, const 
                                     const float* beta, const float* lam, const void* b,
                                     const void* w, const float* h0, void* o, float* hT,
                                     void* workspace, size_t ws_bytes, gdr_stream_t stream,
-                                    gdr_stream_t aux_stream) {
+                                    gdr_stream_t aux_stream, const gdr_out_gate* gate = nullptr) {
   if (segments < 1 || segments > kPipeMaxSegments) return GDR_ERR_INVALID_ARG;
   gdr_status st = check_shape(shape, false);
   if (st != GDR_OK) return st;
   st = check_gates(shape, q, k, v, g, beta, lam, b, w, o);
   if (st != GDR_OK) return st;
+  if (gate && (st = check_out_gate(shape, gate, o)) != GDR_OK) return st;
   if ((h0 && !aligned(h0, 16)) || (hT && !aligned(hT, 16))) return GDR_ERR_INVALID_ARG;
   if (shape->dtype != GDR_BF16) return GDR_ERR_UNSUPPORTED;
   if (!workspace || !aligned(workspace, 16) || ws_bytes < pipelined_bytes(shape, segments))
@@ -349,6 +387,12 @@ gdr_status chunk_fwd_pipelined_impl(const gdr_shape* shape, int segments, const 
   a.h0 = h0; a.o = o; a.hT = hT;
   a.B = shape->B; a.T = shape->T; a.H = shape->H; a.dv = shape->dv;
   a.flags = shape->flags; a.scale = shape->scale;
+  const bool fused = gate && gdr::scan_transposed(shape->dk, shape->dv, shape->flags);
+  if (fused) {
+    a.gz = gate->z;
+    a.gw = gate->weight;
+    a.geps = gate->eps;
+  }
   const cudaStream_t main_ = reinterpret_cast<cudaStream_t>(stream);
   const cudaStream_t aux_ = reinterpret_cast<cudaStream_t>(aux_stream);
   unsigned char* base = static_cast<unsigned char*>(workspace);
@@ -365,6 +409,7 @@ gdr_status chunk_fwd_pipelined_impl(const gdr_shape* shape, int segments, const 
   if (S == 1) {
     err = gdr::launch_chunk_prep(a, shape->dk, packets, status, main_);
     if (err == cudaSuccess) err = gdr::launch_chunk_scan(a, shape->dk, packets, status, main_);
+    if (err == cudaSuccess && gate && !fused) err = out_gate_after(shape, gate, o, main_);
     return err == cudaSuccess ? GDR_OK : GDR_ERR_CUDA;
   }
   // one event per segment (its packets are written) and one for the last scan
@@ -396,6 +441,7 @@ gdr_status chunk_fwd_pipelined_impl(const gdr_shape* shape, int segments, const 
   // `stream` resumes after the last scan
   if (err == cudaSuccess) err = cudaEventRecord(ev[S], aux_);
   if (err == cudaSuccess) err = cudaStreamWaitEvent(main_, ev[S], 0);
+  if (err == cudaSuccess && gate && !fused) err = out_gate_after(shape, gate, o, main_);
   for (int i = 0; i < made; ++i) cudaEventDestroy(ev[i]);   // released once completed
   return err == cudaSuccess ? GDR_OK : GDR_ERR_CUDA;
 }
@@ -438,13 +484,19 @@ gdr_status gdr_chunk_fwd_pipeline_segments(const gdr_shape* shape, int* segments
   if (st != GDR_OK) return st;
   *segments = 1;
   if (shape->dtype != GDR_BF16 || default_segments(shape) > 1) return GDR_OK;
-  // the scan CTAs (one per (batch, head, 64 value columns)) leave at least
-  // half of the SMs to the preparation, and every segment keeps 32 chunks
-  const long long scan_ctas = static_cast<long long>(shape->B) * shape->H * (shape->dv / 64);
+  // the scan CTAs (one per (batch, head), or per (batch, head, 64 value columns)
+  // outside the transposed scan) leave at least half of the SMs to the
+  // preparation, and every segment keeps 32 chunks; eight segments when the
+  // scan takes at most a quarter of the SMs, two otherwise (measured: at
+  // B * H = 64 two segments beat four and eight)
+  const bool tr = gdr::scan_transposed(shape->dk, shape->dv, shape->flags);
+  const long long scan_ctas =
+      static_cast<long long>(shape->B) * shape->H * (tr ? 1 : shape->dv / 64);
   const int nc = n_chunks_of(shape);
   if (2 * scan_ctas > kSplitTargetCtas) return GDR_OK;
+  const int target = 4 * scan_ctas <= kSplitTargetCtas ? kPipeTargetSegments : 2;
   int S = 1;
-  while (S < kPipeTargetSegments && 2 * S * kPipeMinChunks <= nc) S *= 2;
+  while (S < target && 2 * S * kPipeMinChunks <= nc) S *= 2;
   *segments = S;
   return GDR_OK;
 }
@@ -457,6 +509,28 @@ gdr_status gdr_chunk_fwd_pipelined(const gdr_shape* shape, int segments, const v
                                    gdr_stream_t aux_stream) {
   return chunk_fwd_pipelined_impl(shape, segments, q, k, v, g, beta, lam, b, w, h0, o, hT,
                                   workspace, ws_bytes, stream, aux_stream);
+}
+
+gdr_status gdr_chunk_fwd_gated(const gdr_shape* shape, const void* q, const void* k,
+                               const void* v, const float* g, const float* beta,
+                               const float* lam, const void* b, const void* w, const float* h0,
+                               const gdr_out_gate* gate, void* y, float* hT, void* workspace,
+                               size_t ws_bytes, gdr_stream_t stream) {
+  if (!gate) return GDR_ERR_INVALID_ARG;
+  return chunk_fwd_impl(shape, 0, q, k, v, g, beta, lam, b, w, h0, y, hT, workspace, ws_bytes,
+                        stream, gate);
+}
+
+gdr_status gdr_chunk_fwd_gated_pipelined(const gdr_shape* shape, int segments, const void* q,
+                                         const void* k, const void* v, const float* g,
+                                         const float* beta, const float* lam, const void* b,
+                                         const void* w, const float* h0,
+                                         const gdr_out_gate* gate, void* y, float* hT,
+                                         void* workspace, size_t ws_bytes, gdr_stream_t stream,
+                                         gdr_stream_t aux_stream) {
+  if (!gate) return GDR_ERR_INVALID_ARG;
+  return chunk_fwd_pipelined_impl(shape, segments, q, k, v, g, beta, lam, b, w, h0, y, hT,
+                                  workspace, ws_bytes, stream, aux_stream, gate);
 }
 
 gdr_status gdr_chunk_bwd_workspace(const gdr_shape* shape, size_t* bytes) {

@@ -24,6 +24,12 @@ struct ChunkArgs {
   int B, T, H, dv;
   unsigned flags;
   float scale;
+  // output epilogue fused into the state pass (transposed scan only): with gz
+  // non-null, o receives y = o rsqrt(mean(o^2) + geps) gw silu(gz) per
+  // (token, head) row instead of o
+  const void* gz = nullptr;
+  const float* gw = nullptr;
+  float geps = 0.f;
 };
 
 // Arguments of the single-token recurrent step.
@@ -112,6 +118,14 @@ struct ScanSegments {
 cudaError_t launch_chunk_scan(const ChunkArgs& a, int dk, const unsigned char* packets,
                               int* status, cudaStream_t stream,
                               const ScanSegments& sg = ScanSegments());
+// d_k = d_v = 128 without the per-value-channel write strength: the state pass
+// runs transposed (chunk_scan_t.cu), one CTA per (batch, head), and the packets
+// hold U^T instead of U.
+inline bool scan_transposed(int dk, int dv, unsigned flags) {
+  return dk == 128 && dv == 128 && !(flags & 16u);
+}
+cudaError_t launch_chunk_scan_t(const ChunkArgs& a, int dk, const unsigned char* packets,
+                                int* status, cudaStream_t stream, ScanSegments sg);
 // S_start[p] = M[p-1] S_start[p-1] + H[p-1] over the runs of each (batch,
 // head), S_start[0] = h0 (or zero): M [B,H,P,d_k,d_k], Hl and S [B,H,P,d_k,d_v].
 cudaError_t launch_segment_combine(const float* M, const float* Hl, const float* h0, float* S,

@@ -71,9 +71,14 @@
  *    state; 4-byte alignment for g, beta and lam.
  *  - Decay range of the chunked path with per-channel gates
  *    (GDR_DECAY_CHANNEL): within one 64-token chunk the summed log-decay of
- *    any key channel must stay above -140 (beyond that the decay factors of
- *    the chunk algebra approach the bottom of the fp32 normal range and lose
- *    precision). Scalar gates and the recurrent step have no such limit.
+ *    any key channel must stay above -140 (the chunk algebra factors the decay
+ *    of a row pair as e^{G_r - rho} e^{rho - G_i} with rho the half-chunk sum,
+ *    and past that the factors leave the fp32 range). The bf16 two-kernel
+ *    path checks every chunk: a chunk past the limit makes gdr_chunk_fwd_check
+ *    return GDR_ERR_RANGE (detail[0] = b * H + h of the first such sequence
+ *    seen, detail[1] = its chunk) and its outputs are not to be used. Scalar
+ *    gates, GDR_BETA_CHANNEL and the recurrent step have no such limit. The
+ *    chunk backward assumes every in-chunk sum above -80.
  */
 #ifndef GDR_H_
 #define GDR_H_
@@ -93,7 +98,8 @@ typedef enum {
   GDR_ERR_UNSUPPORTED = 2, /* valid request outside the supported set  */
   GDR_ERR_CUDA = 3,        /* the CUDA runtime reported an error        */
   GDR_ERR_WORKSPACE = 4,   /* workspace missing or smaller than needed  */
-  GDR_ERR_TIMEOUT = 5      /* a bounded device-side wait gave up        */
+  GDR_ERR_TIMEOUT = 5,     /* a bounded device-side wait gave up        */
+  GDR_ERR_RANGE = 6        /* channel decay past the chunked range       */
 } gdr_status;
 
 typedef enum { GDR_F32 = 0, GDR_BF16 = 1 } gdr_dtype;
@@ -295,10 +301,12 @@ gdr_status gdr_chunk_bwd(const gdr_shape* shape, const void* q, const void* k, c
 /*
  * Reads the status a gdr_chunk_fwd call left in `workspace` once the work
  * enqueued on `stream` has finished (this call synchronises the stream). It
- * returns GDR_OK, or GDR_ERR_TIMEOUT when a bounded device-side wait of that
- * call gave up (the affected outputs are then incomplete); with a non-NULL
+ * returns GDR_OK; GDR_ERR_TIMEOUT when a bounded device-side wait of that
+ * call gave up (the affected outputs are then incomplete; with a non-NULL
  * `detail`, detail[0] receives the index of the CTA that gave up and
- * detail[1] 4 * chunk + the wait. Workspaces of 0 bytes need no check.
+ * detail[1] 4 * chunk + the wait); or GDR_ERR_RANGE when a chunk's channel
+ * decay was past the limit above (detail as described there). The first
+ * report wins. Workspaces of 0 bytes need no check.
  */
 gdr_status gdr_chunk_fwd_check(const void* workspace, gdr_stream_t stream,
                                int* detail);
@@ -337,6 +345,57 @@ gdr_status gdr_chunk_fwd_static(const gdr_shape* shape, const void* q,
  * 4 * chunk + the wait. No counterpart on the pages either.
  */
 gdr_status gdr_chunk_fwd_static_check(gdr_stream_t stream, int* detail);
+
+/*
+ * The output epilogue fused into the chunked forward (Gated DeltaNet-2 notes,
+ * overall framework, the last stage of its flow chart: the read-out o goes
+ * through RMSNorm and the SiLU output gate before the heads merge; LLMs from
+ * scratch ch. 11, section 11.3). The result is gdr_rmsnorm_gate applied to the
+ * output of gdr_chunk_fwd,
+ *
+ *   y[b,t,h,c] = o[b,t,h,c] / sqrt(mean_c' o[b,t,h,c']^2 + eps) * weight[c]
+ *                * z[b,t,h,c] * sigmoid(z[b,t,h,c]),
+ *
+ * with o never written: the state pass computes y from its fp32 read-out. It
+ * is fused for bf16 inputs with d_k = d_v = 128 and the full workspace (the
+ * two-kernel path, whose state pass holds every value column of a row); for
+ * every other shape the call runs the forward into y and then the epilogue
+ * kernel in place, with the same result up to rounding.
+ *
+ *   gate->z       [B,T,H,d_v] in the call's dtype, device, 16-byte aligned, apart
+ *                 from y
+ *   gate->weight  [d_v] fp32 device, 16-byte aligned
+ *   gate->eps     finite, >= 0
+ *   y             [B,T,H,d_v] in the call's dtype (o's place in gdr_chunk_fwd)
+ *
+ * Every other argument, the workspace and the errors are those of
+ * gdr_chunk_fwd (gdr_chunk_fwd_pipelined for the second form); a null gate or
+ * a bad gate argument returns GDR_ERR_INVALID_ARG, d_v other than 64 or 128
+ * GDR_ERR_UNSUPPORTED.
+ */
+typedef struct {
+  const void* z;        /* output-gate input, [B,T,H,d_v] */
+  const float* weight;  /* RMSNorm gain, [d_v] fp32 */
+  float eps;            /* added to the mean square */
+} gdr_out_gate;
+
+gdr_status gdr_chunk_fwd_gated(const gdr_shape* shape, const void* q,
+                               const void* k, const void* v, const float* g,
+                               const float* beta, const float* lam,
+                               const void* b, const void* w, const float* h0,
+                               const gdr_out_gate* gate, void* y, float* hT,
+                               void* workspace, size_t ws_bytes,
+                               gdr_stream_t stream);
+gdr_status gdr_chunk_fwd_gated_pipelined(const gdr_shape* shape, int segments,
+                                         const void* q, const void* k,
+                                         const void* v, const float* g,
+                                         const float* beta, const float* lam,
+                                         const void* b, const void* w,
+                                         const float* h0,
+                                         const gdr_out_gate* gate, void* y,
+                                         float* hT, void* workspace,
+                                         size_t ws_bytes, gdr_stream_t stream,
+                                         gdr_stream_t aux_stream);
 
 /*
  * One recurrent step for decoding (LLMs from scratch ch. 11, section 11.2,

@@ -141,6 +141,20 @@ def test_channel_decay_near_documented_limit():
     check(x)
 
 
+@pytest.mark.parametrize("variant", ["kda", "gdn2"])
+def test_channel_decay_past_the_limit_is_reported(variant):
+    """A chunk whose summed channel log-decay is below -140 makes the call's
+    status GDR_ERR_RANGE (naming the sequence and chunk); chunks inside the
+    limit (-137.6, the test above) report nothing."""
+    B, T, H = 1, 200, 2
+    x = wl.make_inputs(variant, B, T, H, 128, 128, torch.bfloat16, seed=14, h0_std=0.02)
+    x["g"][0, 64:128, 1, 5] = -2.5          # chunk 1 of head 1: -160 on one channel
+    with pytest.raises(gdr.GdrError) as e:
+        gpu_forward(x)
+    assert e.value.code == 6
+    assert "sequence 1, chunk 1" in str(e.value)
+
+
 def test_unnormalised_keys_and_extended_erase_range():
     # b in [0, 2] (the extended erase range of the Gated DeltaNet-2 ablations)
     x = wl.make_inputs("gdn2", 1, 130, 2, 64, 64, torch.float32, seed=9, h0_std=0.1)

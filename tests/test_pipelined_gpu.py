@@ -5,7 +5,10 @@ pass of the previous segment runs on a second stream.
 Bar: max|d| / max|ref| <= 2e-2 (bf16) against the float64 oracle for o and the
 final state, as for every bf16 path. The pipelined call runs the same kernels
 on the same chunks and hands the fp32 state from one segment to the next, so
-it must also equal the plain two-kernel call bit for bit.
+with scalar decay it equals the plain two-kernel call bit for bit. With channel
+decay (d_k = d_v = 128) the state pass carries diag(e^{rho}) S within a
+segment and S itself across a segment boundary, so the two calls round
+differently there and agree within the bar.
 """
 import pytest
 import torch
@@ -40,12 +43,20 @@ def check(x, segments, **kw):
     if hT is not None:
         eh = rel_err(hT.cpu(), rh)
         assert eh <= BAR, eh
-    # the plain two-kernel path on the same inputs, bit for bit
+    # the plain two-kernel path on the same inputs: bit for bit, or within the
+    # bar where the state is carried scaled (channel decay at d = 128)
     o2, h2 = gpu_forward(x)
     torch.cuda.synchronize()
-    assert torch.equal(o, o2)
-    if hT is not None:
-        assert torch.equal(hT, h2)
+    scaled = (x["flags"] & 1) and x["q"].shape[-1] == 128 and x["v"].shape[-1] == 128 and \
+        not (x["flags"] & 16)
+    if scaled:
+        assert rel_err(o.float().cpu(), o2.float().cpu().double().numpy()) <= BAR
+        if hT is not None:
+            assert rel_err(hT.cpu(), h2.cpu().double().numpy()) <= BAR
+    else:
+        assert torch.equal(o, o2)
+        if hT is not None:
+            assert torch.equal(hT, h2)
 
 
 @pytest.mark.parametrize("segments", [2, 3, 7])
@@ -93,7 +104,9 @@ def test_pipelined_many_claims_per_segment():
     o, hT = pipe_forward(x, 4)
     o2, h2 = gpu_forward(x)
     torch.cuda.synchronize()
-    assert torch.equal(o, o2) and torch.equal(hT, h2)
+    # channel decay: the state crosses segment boundaries unscaled (see above)
+    assert rel_err(o.float().cpu(), o2.float().cpu().double().numpy()) <= BAR
+    assert rel_err(hT.cpu(), h2.cpu().double().numpy()) <= BAR
     for b, h in [(0, 0), (1, 3)]:
         xs = select(x, batches=[b], heads=[h])
         ro, rh = oracle_forward(xs)
@@ -104,10 +117,10 @@ def test_pipelined_many_claims_per_segment():
 
 def test_default_policy_pipelines_the_gdn2_prefill():
     """The Gated DeltaNet-2 prefill (1 x 65536 x 32 x 128) at full size goes
-    through the pipelined path by default (no workspace given) and equals the
-    plain two-kernel path, which the full-size parity test checks against the
-    oracle."""
-    x = wl.config_inputs(5)
+    through the pipelined path by default (no workspace given) and agrees with
+    the plain two-kernel path within the bar (the full-size parity test checks
+    the pipelined call against the oracle)."""
+    x = wl.config_inputs(5, gen_device="cuda")
     d = to_dev(x)
     shape = gdr.make_shape(*d["q"].shape, d["v"].shape[-1], d["q"].dtype, x["flags"], x["scale"])
     assert gdr.pipeline_segments(shape) == 8
@@ -115,4 +128,5 @@ def test_default_policy_pipelines_the_gdn2_prefill():
                           d["h0"], scale=x["scale"], flags=x["flags"])
     o2, h2 = gpu_forward(x)
     torch.cuda.synchronize()
-    assert torch.equal(o, o2) and torch.equal(hT, h2)
+    assert rel_err(o.float().cpu(), o2.float().cpu().double().numpy()) <= BAR
+    assert rel_err(hT.cpu(), h2.cpu().double().numpy()) <= BAR
