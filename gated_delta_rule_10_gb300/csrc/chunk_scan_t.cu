@@ -52,6 +52,7 @@
 #include "kernels.h"
 #include "packet.h"
 #include "tc.cuh"
+#include "tma.h"
 
 namespace gdr {
 namespace {
@@ -75,20 +76,27 @@ constexpr uint32_t SA = 384;       // S^T as bf16 pairs (d_k / 2 columns): A of 
 constexpr uint32_t WA = 448;       // W^T as bf16 pairs (32 columns): A of MMA2 and MMA3
 
 enum : uint32_t {
-  kFull0 = 0, kEmpty0 = 3, kBW = 6, kBS = 7, kBO0 = 8, kOFree0 = 10, kBars = 12
+  kFull0 = 0, kEmpty0 = 3, kBW = 6, kBS = 7, kBO0 = 8, kOFree0 = 10, kZFull0 = 12, kBars = 14
 };
 
-template <int DK>
+template <int DK, bool GATE>
 struct TLayout {
   using P = Packet<DK, 128>;
-  static constexpr uint32_t kStage = P::bytes;   // the whole packet, U^T included
-  static constexpr uint32_t oRed = kStages * kStage;   // epilogue: [2][4][64] row partial sums
-  static constexpr uint32_t oM = oRed + 2 * 4 * 64 * 4;  // RF: the update's factor per key channel
+  // the fused epilogue adds a two-slot ring of z tiles and a double-buffered y
+  // tile that a TMA store writes out (two packet stages then); the packet
+  // stages go back to the ring as soon as MMA3 is done with them
+  static constexpr int kNS = GATE ? 2 : kStages;
+  static constexpr uint32_t kStage = P::bytes;
+  static constexpr uint32_t oZ = kNS * kStage;                    // [2] z tiles
+  static constexpr uint32_t oY = oZ + (GATE ? 2 * 16384 : 0);     // [2] y tiles
+  static constexpr uint32_t oRed = oY + (GATE ? 2 * 16384 : 0);   // [2][4][64] row sums
+  static constexpr uint32_t oM = oRed + (GATE ? 2 * 4 * 64 * 4 : 0);   // RF: update factor
   static constexpr uint32_t oBar = oM + DK * 4;
   static constexpr uint32_t oSlot = oBar + kBars * 8;
   static constexpr uint32_t oAbort = oSlot + 4;
   static constexpr uint32_t bytes = oAbort + 12;
   static constexpr uint32_t launch_bytes = bytes + 1024;
+  static_assert(kStage % 1024 == 0 && oZ % 1024 == 0 && oY % 1024 == 0, "tile alignment");
 };
 
 __device__ __forceinline__ void unpack8(uint4 u, float* x) {
@@ -110,25 +118,14 @@ __device__ __forceinline__ bool spin_test(uint32_t mbar, uint32_t parity, int sp
   return false;
 }
 
-// 8 x 8 transpose across the 8-lane groups of a warp: afterwards v[j] of lane
-// 8g + i holds what v[i] of lane 8g + j held (three butterfly exchanges). The
-// output role holds one value column per lane and the token rows in registers;
-// transposed, a lane holds 8 adjacent columns of one row, a 16-byte access.
-__device__ __forceinline__ void transpose8(float (&v)[8], int lane) {
-#pragma unroll
-  for (int s = 4; s >= 1; s >>= 1) {
-    const bool up = (lane & s) != 0;
-#pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      if (j & s) continue;
-      const float send = up ? v[j] : v[j + s];
-      const float recv = __shfl_xor_sync(0xffffffffu, send, s);
-      if (up)
-        v[j] = recv;
-      else
-        v[j + s] = recv;
-    }
-  }
+// tanh by the special-function unit (one instruction, about 2^-11 relative
+// error); SiLU below takes sigmoid(z) = (1 + tanh(z / 2)) / 2, one
+// special-function operation per element instead of an exponential and a
+// reciprocal, which the output role's epilogue is bound by.
+__device__ __forceinline__ float tanh_fast(float x) {
+  float y;
+  asm("tanh.approx.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
 }
 
 // Bounded mbarrier wait that also gives up once another role has aborted.
@@ -146,13 +143,15 @@ __device__ __forceinline__ bool wait_or_abort(uint32_t mbar, uint32_t parity,
 template <int DK, int CW, bool RF, bool GATE>
 __global__ void __launch_bounds__(Roles<CW>::kThreads, 1)
     chunk_scan_t_kernel(const ChunkArgs a, const unsigned char* packets, int* status,
-                        const ScanSegments sg) {
+                        const ScanSegments sg, const __grid_constant__ CUtensorMap tm_z,
+                        const __grid_constant__ CUtensorMap tm_o) {
   constexpr int DV = 128;
   constexpr int KH = DK / CW;      // key channels per chain thread
   constexpr int TW = 64 / CW;      // tokens of W per chain thread
   constexpr int kChainThreads = Roles<CW>::kChainThreads, kOut = Roles<CW>::kOut;
-  using L = TLayout<DK>;
+  using L = TLayout<DK, GATE>;
   using P = Packet<DK, DV>;
+  constexpr int kStages = L::kNS;
   extern __shared__ unsigned char smem_raw[];
   unsigned char* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   const uint32_t sb = smem_u32(smem);
@@ -187,6 +186,7 @@ __global__ void __launch_bounds__(Roles<CW>::kThreads, 1)
     for (int i = 0; i < 2; ++i) {
       tc::mbar_init(bar(kBO0 + i), 1);
       tc::mbar_init(bar(kOFree0 + i), 1);
+      tc::mbar_init(bar(kZFull0 + i), 1);
     }
     *abort_flag = 0;
     tc::fence_mbar_init();
@@ -202,8 +202,17 @@ __global__ void __launch_bounds__(Roles<CW>::kThreads, 1)
   auto load_chunk = [&](int n) {   // thread kOut only
     const int s = n % kStages;
     tc::mbar_arrive_expect_tx(bar(kFull0 + s), L::kStage);
-    tc::bulk_load(sb + s * L::kStage, pk0 + size_t(n) * P::bytes, L::kStage, bar(kFull0 + s));
+    tc::bulk_load(sb + s * L::kStage, pk0 + size_t(n) * P::bytes, P::bytes, bar(kFull0 + s));
   };
+  auto load_z = [&](int n) {   // thread kOut only: the chunk's z rows (past T: zeros)
+    const int zs = n & 1;
+    tc::mbar_arrive_expect_tx(bar(kZFull0 + zs), 16384);
+#pragma unroll
+    for (int blk = 0; blk < DV / 64; ++blk)
+      tc::tma_load_4d(sb + L::oZ + zs * 16384 + blk * 8192, &tm_z, blk * 64, h,
+                      (c_begin + n) * kChunk, bb, bar(kZFull0 + zs));
+  };
+  const bool zring = GATE && out != nullptr;
 
   if (warp < 4 * CW) {
     // ------------------------------------------------------------ state chain
@@ -381,10 +390,14 @@ __global__ void __launch_bounds__(Roles<CW>::kThreads, 1)
     }
   } else {
     // ------------------------------------------------------------ output
-    int issued = 0;
+    int issued = 0, zissued = 0;
     if (tid == kOut) {
       for (int n = 0; n < min(kStages, cnt); ++n) load_chunk(n);
       issued = min(kStages, cnt);
+      if (zring) {
+        for (int n = 0; n < min(2, cnt); ++n) load_z(n);
+        zissued = min(2, cnt);
+      }
     }
     for (int n = 0; n < cnt; ++n) {
       const int s = n % kStages;
@@ -416,11 +429,10 @@ __global__ void __launch_bounds__(Roles<CW>::kThreads, 1)
       float x[64];
       tc::tmem_ld64(tl + D10 + (n & 1) * 128, x);
       tc::fence_before_sync();
-      tc::named_sync(kOutBar, kOutThreads);
-      if (tid == kOut) {
-        tc::mbar_arrive(bar(kOFree0 + (n & 1)));
+      // thread kOut: the stage goes back to the chain's ring once both roles are
+      // done with it, and is refilled with chunk n + kStages
+      auto release_and_refill = [&]() {
         tc::mbar_arrive(bar(kEmpty0 + s));
-        // refill the stage once the chain has released it too
         if (n + kStages < cnt) {
           ok = wait_or_abort(bar(kEmpty0 + s), (n / kStages) & 1, abort_flag);
           if (ok) {
@@ -428,84 +440,99 @@ __global__ void __launch_bounds__(Roles<CW>::kThreads, 1)
             issued = n + kStages + 1;
           }
         }
-      }
-      // o (or y) rows of this warp's 32 columns: lane 8g + i stores columns
-      // 32q + 8g .. +7 of rows 8b + i, 16 bytes at a time
-      const int g8 = lane >> 3, i8 = lane & 7;
-      const size_t row0 = (size_t(bb) * T + t0) * H + h;
-      auto store_block = [&](const float (&v)[8], int b) {
-        const int r = 8 * b + i8;
-        if (r < Lr) {
-          uint4 u;
-          u.x = pack_bf16x2(v[0], v[1]);
-          u.y = pack_bf16x2(v[2], v[3]);
-          u.z = pack_bf16x2(v[4], v[5]);
-          u.w = pack_bf16x2(v[6], v[7]);
-          *reinterpret_cast<uint4*>(out + (row0 + size_t(r) * H) * DV + 32 * q + 8 * g8) = u;
-        }
       };
-      if (GATE && out) {
-        // the output epilogue on the chunk's rows: y = o rsqrt(mean_c o^2 + eps)
-        // weight_c silu(z); each row's sum of squares over the d_v columns is a
-        // reduce-scatter over the warp's 32 lanes (lane l ends with token l of
-        // the half) and then over the four warps through shared memory. z comes
-        // in 16-byte rows and is transposed to a column per lane.
-        const __nv_bfloat16* zb = static_cast<const __nv_bfloat16*>(a.gz);
-        float* red = reinterpret_cast<float*>(smem + L::oRed) + (n & 1) * 256;
-        const float wc = a.gw[c];
+      if (tid == kOut) {
+        tc::mbar_arrive(bar(kOFree0 + (n & 1)));
+        release_and_refill();   // MMA3 is done with the packet
+        if (zring) {
+          tc::bulk_wait_read<1>();   // the y tile of chunk n-2 has been read out
+          if (ok && !wait_or_abort(bar(kZFull0 + (n & 1)), (n >> 1) & 1, abort_flag)) ok = false;
+        }
+      }
+      if (zring && tc::named_any(kOutBar, kOutThreads, !ok)) { fail = 4 * n + 3; break; }
+      if (!zring) tc::named_sync(kOutBar, kOutThreads);
+      if constexpr (GATE) {
+        if (out) {
+          // the output epilogue on the chunk's rows: y = o rsqrt(mean_c o^2 + eps)
+          // weight_c silu(z), z from the stage (TMA), y through a shared tile and
+          // a TMA store. Each row's sum of squares over the d_v columns is a
+          // reduce-scatter over the warp's 32 lanes (lane l ends with token l of
+          // the half) and then over the four warps through shared memory.
+          const unsigned char* zt = smem + L::oZ + (n & 1) * 16384;
+          unsigned char* yt = smem + L::oY + (n & 1) * 16384;
+          float* red = reinterpret_cast<float*>(smem + L::oRed) + (n & 1) * 256;
 #pragma unroll
-        for (int p = 0; p < 2; ++p) {
-          float z[32];
+          for (int p = 0; p < 2; ++p) {
+            float v[32];
 #pragma unroll
-          for (int b = 0; b < 4; ++b) {
-            const int r = 32 * p + 8 * b + i8;
-            float zv[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-            if (r < Lr) {
-              const uint4 u = *reinterpret_cast<const uint4*>(zb + (row0 + size_t(r) * H) * DV +
-                                                              32 * q + 8 * g8);
-              unpack8(u, zv);
+            for (int j = 0; j < 32; ++j) v[j] = x[32 * p + j] * x[32 * p + j];
+#pragma unroll
+            for (int off = 16, m = 16; off >= 1; off >>= 1, m >>= 1) {
+              const bool up = (lane & off) != 0;
+#pragma unroll
+              for (int i = 0; i < m; ++i) {
+                const float send = up ? v[i] : v[i + m];
+                const float keep = up ? v[i + m] : v[i];
+                v[i] = keep + __shfl_xor_sync(0xffffffffu, send, off);
+              }
             }
-            transpose8(zv, lane);
-#pragma unroll
-            for (int j = 0; j < 8; ++j) z[8 * b + j] = zv[j];
+            red[q * 64 + 32 * p + lane] = v[0];
           }
-          float v[32];
-#pragma unroll
-          for (int j = 0; j < 32; ++j) v[j] = x[32 * p + j] * x[32 * p + j];
-#pragma unroll
-          for (int off = 16, m = 16; off >= 1; off >>= 1, m >>= 1) {
-            const bool up = (lane & off) != 0;
-#pragma unroll
-            for (int i = 0; i < m; ++i) {
-              const float send = up ? v[i] : v[i + m];
-              const float keep = up ? v[i + m] : v[i];
-              v[i] = keep + __shfl_xor_sync(0xffffffffu, send, off);
-            }
-          }
-          red[q * 64 + 32 * p + lane] = v[0];
           tc::named_sync(kOutBar, kOutThreads);
-          const int t = 32 * p + lane;
-          const float tot = red[t] + red[64 + t] + red[128 + t] + red[192 + t];
-          const float rs = rsqrtf(tot * (1.f / DV) + a.geps);
+          // warp q finishes rows 16 q .. 16 q + 15: rsqrt(mean + eps) into the
+          // first 64 floats of this chunk's red buffer (after everyone read the sums)
+          float rsv = 0.f;
+          if (lane < 16) {
+            const int t = 16 * q + lane;
+            rsv = rsqrtf((red[t] + red[64 + t] + red[128 + t] + red[192 + t]) * (1.f / DV) +
+                         a.geps);
+          }
+          tc::named_sync(kOutBar, kOutThreads);
+          if (lane < 16) red[16 * q + lane] = rsv;
+          tc::named_sync(kOutBar, kOutThreads);
+          const float wc = a.gw[c];
+          const float4* rs4 = reinterpret_cast<const float4*>(red);
 #pragma unroll
-          for (int b = 0; b < 4; ++b) {
-            float yv[8];
+          for (int p = 0; p < 4; ++p) {
+            // all of the quarter's z first: the y stores below could alias the z
+            // tile for the compiler, which would otherwise serialise the rows
+            float zf[16];
 #pragma unroll
-            for (int j = 0; j < 8; ++j) {
-              const int jj = 8 * b + j;
-              const float r = __shfl_sync(0xffffffffu, rs, jj);
-              const float zj = z[jj];
-              yv[j] = x[32 * p + jj] * r * wc * __fdividef(zj, 1.f + __expf(-zj));
+            for (int j = 0; j < 16; ++j)
+              zf[j] = __bfloat162float(*reinterpret_cast<const __nv_bfloat16*>(
+                  zt + tc::tile_off(64, 16 * p + j, c)));
+#pragma unroll
+            for (int j = 0; j < 16; j += 4) {
+              const float4 r4 = rs4[(16 * p + j) / 4];
+              const float rr[4] = {r4.x, r4.y, r4.z, r4.w};
+#pragma unroll
+              for (int i = 0; i < 4; ++i) {
+                const float hz = 0.5f * zf[j + i];
+                const float silu = fmaf(hz, tanh_fast(hz), hz);   // z sigmoid(z)
+                const float y = (x[16 * p + j + i] * rr[i] * wc) * silu;
+                *reinterpret_cast<__nv_bfloat16*>(yt + tc::tile_off(64, 16 * p + j + i, c)) =
+                    __float2bfloat16_rn(y);
+              }
             }
-            transpose8(yv, lane);
-            store_block(yv, 4 * p + b);
+          }
+          tc::fence_proxy_async();
+          tc::named_sync(kOutBar, kOutThreads);
+          if (tid == kOut) {   // rows past T are clipped by the store
+#pragma unroll
+            for (int blk = 0; blk < DV / 64; ++blk)
+              tc::tma_store_4d(&tm_o, blk * 64, h, t0, bb, smem_u32(yt) + blk * 8192);
+            tc::bulk_commit();
+            if (n + 2 < cnt) {   // this z slot is free again
+              load_z(n + 2);
+              zissued = n + 3;
+            }
           }
         }
       } else if (out) {
         // one column per lane: each warp store covers 32 adjacent columns of a
         // row (64 bytes); fewer instructions than transposing to 16-byte rows,
         // which cost the chain warps more issue slots than they saved
-        __nv_bfloat16* op = out + row0 * DV + 32 * q + lane;
+        __nv_bfloat16* op = out + ((size_t(bb) * T + t0) * H + h) * DV + c;
 #pragma unroll
         for (int j = 0; j < 64; ++j)
           if (j < Lr) op[size_t(j) * H * DV] = __float2bfloat16_rn(x[j]);
@@ -513,10 +540,15 @@ __global__ void __launch_bounds__(Roles<CW>::kThreads, 1)
       if (tc::named_any(kOutBar, kOutThreads, !ok)) { fail = 4 * n + 3; break; }
     }
     // let the copies already issued land before the CTA can exit (a plain
-    // bounded wait: an abort elsewhere does not stop a copy in flight)
-    if (tid == kOut)
+    // bounded wait: an abort elsewhere does not stop a copy in flight), and
+    // the y stores finish
+    if (tid == kOut) {
       for (int n = max(0, issued - kStages); n < issued; ++n)
         tc::mbar_wait(bar(kFull0 + n % kStages), (n / kStages) & 1);
+      for (int n = max(0, zissued - 2); n < zissued; ++n)
+        tc::mbar_wait(bar(kZFull0 + (n & 1)), (n >> 1) & 1);
+      if constexpr (GATE) tc::bulk_wait_all<0>();
+    }
   }
 
   if (fail >= 0 && status && lane == 0) {
@@ -535,7 +567,7 @@ __global__ void __launch_bounds__(Roles<CW>::kThreads, 1)
 template <int CW, bool RF, bool GATE>
 cudaError_t launch_scan_t(const ChunkArgs& a, const unsigned char* packets, int* status,
                           cudaStream_t stream, ScanSegments sg) {
-  using L = TLayout<128>;
+  using L = TLayout<128, GATE>;
   static_assert(L::launch_bytes <= 232448, "shared memory budget of one CTA");
   auto kern = chunk_scan_t_kernel<128, CW, RF, GATE>;
   cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -543,8 +575,12 @@ cudaError_t launch_scan_t(const ChunkArgs& a, const unsigned char* packets, int*
   if (err != cudaSuccess) return err;
   if (sg.segments < 1 || sg.chunk0 < 0) return cudaErrorInvalidValue;
   if (sg.seg_chunks < 1) sg.seg_chunks = (a.T + kChunk - 1) / kChunk - sg.chunk0;
+  CUtensorMap tz{}, to{};   // (read only by the fused epilogue)
+  if (GATE && (!make_bthd_tmap(&tz, a.gz, a.B, a.T, a.H, 128) ||
+               !make_bthd_tmap(&to, a.o, a.B, a.T, a.H, 128)))
+    return cudaErrorInvalidValue;
   dim3 grid(sg.hT_hom ? 2 : 1, a.H, static_cast<unsigned>(a.B) * static_cast<unsigned>(sg.segments));
-  kern<<<grid, Roles<CW>::kThreads, L::launch_bytes, stream>>>(a, packets, status, sg);
+  kern<<<grid, Roles<CW>::kThreads, L::launch_bytes, stream>>>(a, packets, status, sg, tz, to);
   return cudaGetLastError();
 }
 
