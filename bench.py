@@ -54,6 +54,9 @@ def parse():
                    help="decode steps per step (default: the workload's decode phase, else 1)")
     p.add_argument("--no-configs", action="store_true",
                    help="skip timing the other workloads")
+    p.add_argument("--seq-len", type=int, default=None,
+                   help="override the workload's T (a shortened case for profiler runs; "
+                        "the line then does not describe the named workload)")
     p.add_argument("--minimal", action="store_true",
                    help="the step alone: no other workloads, epilogue, gate cumsum, e2e, CPU "
                         "baseline or side measurements (for profiler runs)")
@@ -109,9 +112,11 @@ def peaks():
 # and chunk_scan_kernel, from one capture of the plain two-kernel call), per
 # workload, with the hash of the kernel sources they were taken on: a changed
 # kernel reports null traffic until it is profiled again.
-TRAFFIC = {2: {"bytes": 835.4e6, "sources": "23b49c3cb85400d5"}}
-KERNEL_SOURCES = ("chunk_prep.cu", "chunk_scan.cu", "packet.h", "tc.cuh", "tri_inverse.cuh",
-                  "common.cuh")
+TRAFFIC = {2: {"bytes": 846.5e6, "sources": "9341e0d30b207844"},
+           3: {"bytes": 1767.3e6, "sources": "9341e0d30b207844"},
+           4: {"bytes": 4158.2e6, "sources": "9341e0d30b207844"}}
+KERNEL_SOURCES = ("chunk_prep.cu", "chunk_scan.cu", "chunk_scan_t.cu", "packet.h", "tc.cuh",
+                  "tri_inverse.cuh", "common.cuh")
 
 
 def kernel_sources_hash():
@@ -265,9 +270,12 @@ def run_ours(args):
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     cfg = args.workload
-    c = wl.CONFIGS[cfg]
+    c = dict(wl.CONFIGS[cfg])
+    if args.seq_len:
+        c["T"] = args.seq_len
+        c["name"] = c["name"] + "_T%d" % args.seq_len
     # inputs drawn on the device (seeded CUDA generator), resident in HBM
-    x = wl.config_inputs(cfg, gen_device=dev, seed=c["seed"] + 1000 * rank)
+    x = wl.config_inputs(cfg, gen_device=dev, seed=c["seed"] + 1000 * rank, T=c["T"])
     B, T, H, dk, dv = c["B"], c["T"], c["H"], c["dk"], c["dv"]
     dec_steps, N = decode_of(cfg, B)
     if args.decode_steps is not None:
@@ -350,7 +358,7 @@ def run_ours(args):
     mean_chunk = statistics.mean(chunk_ms)
     roof = roofline_obj(prefill_bytes(x, o, hT), algorithmic_flops_per_th(dk, dv) * th_prefill,
                         mean_chunk, pk, pk_kind)
-    roof.update({"traffic": measured_traffic(cfg),
+    roof.update({"traffic": None if args.seq_len else measured_traffic(cfg),
                  "kernel": ("gdr_chunk_fwd: chunk_prep_kernel + chunk_scan_kernel (one call)"
                             if pipe <= 1 else
                             "gdr_chunk_fwd_pipelined: %d x (chunk_prep_kernel + chunk_scan_kernel)"

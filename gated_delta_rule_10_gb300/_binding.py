@@ -77,6 +77,7 @@ def lib():
         L.gdr_chunk_bwd.argtypes = [sp] + [_vp] * 20 + [_vp, ctypes.c_size_t, _vp]
         L.gdr_rmsnorm_gate.argtypes = [ctypes.c_longlong, ctypes.c_int, ctypes.c_int, _vp, _vp,
                                        _vp, ctypes.c_float, _vp, _vp]
+        L.gdr_token_fwd.argtypes = [sp] + [_vp] * 11 + [_vp]
         gp = ctypes.POINTER(OutGate)
         L.gdr_chunk_fwd_gated.argtypes = ([sp] + [_vp] * 9 + [gp, _vp, _vp] +
                                           [_vp, ctypes.c_size_t, _vp])
@@ -92,7 +93,7 @@ def lib():
                      "gdr_chunk_fwd_pipeline_segments", "gdr_recurrent_step",
                      "gdr_gate_cumsum", "gdr_chunk_fwd_check", "gdr_rmsnorm_gate",
                      "gdr_chunk_bwd_workspace", "gdr_chunk_bwd", "gdr_chunk_fwd_gated",
-                     "gdr_chunk_fwd_gated_pipelined"):
+                     "gdr_chunk_fwd_gated_pipelined", "gdr_token_fwd"):
             getattr(L, name).restype = ctypes.c_int
         _lib = L
     return _lib
@@ -293,6 +294,41 @@ def chunk_fwd(q, k, v, g, beta=None, lam=None, b=None, w=None, h0=None, *, scale
             st = lib().gdr_chunk_fwd_split(ctypes.byref(shape), int(segments), *args)
     if st:
         raise GdrError(st, name)
+    return o, hT
+
+
+def token_fwd(q, k, v, g, beta=None, lam=None, b=None, w=None, h0=None, *, scale=None,
+              flags=None, output_final_state=True, o=None, hT=None, stream=None):
+    """The forward token by token (``gdr_token_fwd``): no decay factoring, so no
+    range limit on the log-decay; same arguments and results as chunk_fwd."""
+    B, T, H, dk = q.shape
+    dv = v.shape[-1]
+    dev, dt = q.device, q.dtype
+    if flags is None:
+        flags = _infer_flags(g.dim() == 4, b, w, lam, beta is not None and beta.dim() == 4)
+    if scale is None:
+        scale = dk ** -0.5
+    for name, t, want, shp in (("q", q, dt, (B, T, H, dk)), ("k", k, dt, (B, T, H, dk)),
+                               ("v", v, dt, (B, T, H, dv)), ("b", b, dt, (B, T, H, dk)),
+                               ("w", w, dt, (B, T, H, dv)), ("lam", lam, torch.float32, (B, T, H)),
+                               ("h0", h0, torch.float32, (B, H, dk, dv))):
+        _check(t, name, want, dev, shp)
+    _check(g, "g", torch.float32, dev, (B, T, H, dk) if flags & DECAY_CHANNEL else (B, T, H))
+    _check(beta, "beta", torch.float32, dev,
+           (B, T, H, dv) if flags & BETA_CHANNEL else (B, T, H))
+    if o is None:
+        o = torch.empty(B, T, H, dv, dtype=dt, device=dev)
+    _check(o, "o", dt, dev, (B, T, H, dv))
+    if hT is None and output_final_state:
+        hT = torch.empty(B, H, dk, dv, dtype=torch.float32, device=dev)
+    _check(hT, "hT", torch.float32, dev, (B, H, dk, dv))
+    shape = make_shape(B, T, H, dk, dv, dt, flags, scale)
+    with torch.cuda.device(dev):
+        st = lib().gdr_token_fwd(ctypes.byref(shape), _ptr(q), _ptr(k), _ptr(v), _ptr(g),
+                                 _ptr(beta), _ptr(lam), _ptr(b), _ptr(w), _ptr(h0), _ptr(o),
+                                 _ptr(hT), _stream(stream, dev))
+    if st:
+        raise GdrError(st, "gdr_token_fwd")
     return o, hT
 
 

@@ -511,6 +511,32 @@ gdr_status gdr_chunk_fwd_pipelined(const gdr_shape* shape, int segments, const v
                                   workspace, ws_bytes, stream, aux_stream);
 }
 
+gdr_status gdr_token_fwd(const gdr_shape* shape, const void* q, const void* k, const void* v,
+                         const float* g, const float* beta, const float* lam, const void* b,
+                         const void* w, const float* h0, void* o, float* hT,
+                         gdr_stream_t stream) {
+  gdr_status st = check_shape(shape, false);
+  if (st != GDR_OK) return st;
+  st = check_gates(shape, q, k, v, g, beta, lam, b, w, o);
+  if (st != GDR_OK) return st;
+  if ((h0 && !aligned(h0, 16)) || (hT && !aligned(hT, 16))) return GDR_ERR_INVALID_ARG;
+  const bool f32 = shape->dtype == GDR_F32;
+  const cudaStream_t st_ = reinterpret_cast<cudaStream_t>(stream);
+  if (shape->flags & GDR_BETA_CHANNEL) {   // its own token-order scan
+    const cudaError_t err = gdr::launch_value_beta_scan(
+        value_beta_args(shape, q, k, v, g, beta, h0, o, hT), shape->dk, shape->dv, f32, st_);
+    return err == cudaSuccess ? GDR_OK : GDR_ERR_CUDA;
+  }
+  if (shape->B > 65535 || shape->H > 65535) return GDR_ERR_UNSUPPORTED;
+  gdr::ChunkArgs a;
+  a.q = q; a.k = k; a.v = v; a.g = g; a.beta = beta; a.lam = lam; a.b = b; a.w = w;
+  a.h0 = h0; a.o = o; a.hT = hT;
+  a.B = shape->B; a.T = shape->T; a.H = shape->H; a.dv = shape->dv;
+  a.flags = shape->flags; a.scale = shape->scale;
+  const cudaError_t err = gdr::launch_token_scan(a, shape->dk, f32, st_);
+  return err == cudaSuccess ? GDR_OK : GDR_ERR_CUDA;
+}
+
 gdr_status gdr_chunk_fwd_gated(const gdr_shape* shape, const void* q, const void* k,
                                const void* v, const float* g, const float* beta,
                                const float* lam, const void* b, const void* w, const float* h0,

@@ -153,6 +153,9 @@ struct ChunkBwdArgs {
 size_t chunk_bwd_workspace_bytes(int B, int T, int H, int dk, int dv);
 cudaError_t launch_chunk_bwd(const ChunkBwdArgs& a, bool f32, cudaStream_t stream);
 
+// Token-order scan for every flag but 16 (no decay factoring: the path past the
+// chunked path's channel-decay range); o and hT as in the chunked forward.
+cudaError_t launch_token_scan(const ChunkArgs& a, int dk, bool f32, cudaStream_t stream);
 // Write strength per value channel (flag 16): token-order scan, fp32 state.
 cudaError_t launch_value_beta_scan(const ValueBetaArgs& a, int dk, int dv, bool f32,
                                    cudaStream_t stream);

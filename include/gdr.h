@@ -76,7 +76,8 @@
  *    and past that the factors leave the fp32 range). The bf16 two-kernel
  *    path checks every chunk: a chunk past the limit makes gdr_chunk_fwd_check
  *    return GDR_ERR_RANGE (detail[0] = b * H + h of the first such sequence
- *    seen, detail[1] = its chunk) and its outputs are not to be used. Scalar
+ *    seen, detail[1] = its chunk) and its outputs are not to be used;
+ *    gdr_token_fwd computes such inputs without the limit. Scalar
  *    gates, GDR_BETA_CHANNEL and the recurrent step have no such limit. The
  *    chunk backward assumes every in-chunk sum above -80.
  */
@@ -345,6 +346,24 @@ gdr_status gdr_chunk_fwd_static(const gdr_shape* shape, const void* q,
  * 4 * chunk + the wait. No counterpart on the pages either.
  */
 gdr_status gdr_chunk_fwd_static_check(gdr_stream_t stream, int* detail);
+
+/*
+ * The same forward (arguments, layouts and results of gdr_chunk_fwd, no
+ * workspace) by walking the tokens in order with the fp32 state in registers:
+ * S~ = Diag(alpha_t) S, S_t = S~ + k_t (z_t - S~^T e_t)^T, o_t = S_t^T (scale q_t)
+ * for each token (LLMs from scratch ch. 11, section 11.2, in the general form
+ * of the Gated DeltaNet-2 notes, key design 1). No decay is factored, so any
+ * finite log-decay is exact in fp32: this is the path for inputs past the
+ * chunked path's channel-decay range (gdr_chunk_fwd_check returning
+ * GDR_ERR_RANGE). It is sequential in the tokens, one CTA per (batch, head, 32
+ * value columns), and so far slower than the chunked path on long sequences.
+ * Every flag; GDR_BETA_CHANNEL takes its own token-order scan. h0 and hT may
+ * alias.
+ */
+gdr_status gdr_token_fwd(const gdr_shape* shape, const void* q, const void* k,
+                         const void* v, const float* g, const float* beta,
+                         const float* lam, const void* b, const void* w,
+                         const float* h0, void* o, float* hT, gdr_stream_t stream);
 
 /*
  * The output epilogue fused into the chunked forward (Gated DeltaNet-2 notes,

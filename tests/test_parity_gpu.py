@@ -155,6 +155,57 @@ def test_channel_decay_past_the_limit_is_reported(variant):
     assert "sequence 1, chunk 1" in str(e.value)
 
 
+def _token_forward(x):
+    d = to_dev(x)
+    return gdr.token_fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], d["lam"], d["b"], d["w"],
+                         d["h0"], scale=x["scale"], flags=x["flags"])
+
+
+@pytest.mark.parametrize("dtype", DTYPES, ids=["f32", "bf16"])
+@pytest.mark.parametrize("dk,dv", [(64, 64), (128, 128), (64, 128), (128, 64)])
+@pytest.mark.parametrize("flags", range(16))
+def test_token_forward_every_flag(flags, dk, dv, dtype):
+    """gdr_token_fwd (the recurrence token by token, fp32 state) against the oracle."""
+    x = wl.make_inputs(flags, 2, 77, 3, dk, dv, dtype, seed=600 + flags, h0_std=0.05)
+    o, hT = _token_forward(x)
+    torch.cuda.synchronize()
+    ro, rh = oracle_forward(x)
+    tol = TOL[dtype]
+    assert rel_err(o.float().cpu(), ro) <= tol and rel_err(hT.cpu(), rh) <= tol
+
+
+@pytest.mark.parametrize("dtype", DTYPES, ids=["f32", "bf16"])
+@pytest.mark.parametrize("variant", ["kda", "gdn2"])
+def test_channel_decay_minus_300_per_chunk(variant, dtype):
+    """Per-channel in-chunk log-decay sums of -300 (past the chunked path's
+    range, which reports GDR_ERR_RANGE for them): the token-order path matches
+    the oracle at the forward's bar, o and the final state."""
+    x = wl.make_inputs(variant, 2, 200, 3, 128, 128, dtype, seed=31, h0_std=0.1)
+    g = -300.0 / 64 * torch.ones_like(x["g"])
+    g[..., 1::3] = -0.02                      # some channels keep their memory
+    x["g"] = g.contiguous()
+    if dtype == torch.bfloat16:
+        with pytest.raises(gdr.GdrError) as e:
+            gpu_forward(x)
+        assert e.value.code == 6
+    o, hT = _token_forward(x)
+    torch.cuda.synchronize()
+    ro, rh = oracle_forward(x)
+    tol = TOL[dtype]
+    assert rel_err(o.float().cpu(), ro) <= tol and rel_err(hT.cpu(), rh) <= tol
+
+
+def test_token_forward_h0_and_hT_may_alias():
+    x = wl.make_inputs("gdn2", 2, 90, 2, 128, 64, torch.float32, seed=32, h0_std=0.05)
+    d = to_dev(x)
+    state = d["h0"].clone()
+    o, _ = gdr.token_fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], d["lam"], d["b"], d["w"],
+                         state, hT=state, scale=x["scale"], flags=x["flags"])
+    torch.cuda.synchronize()
+    ro, rh = oracle_forward(x)
+    assert rel_err(o.cpu(), ro) <= 1e-4 and rel_err(state.cpu(), rh) <= 1e-4
+
+
 def test_unnormalised_keys_and_extended_erase_range():
     # b in [0, 2] (the extended erase range of the Gated DeltaNet-2 ablations)
     x = wl.make_inputs("gdn2", 1, 130, 2, 64, 64, torch.float32, seed=9, h0_std=0.1)
