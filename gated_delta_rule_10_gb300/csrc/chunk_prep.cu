@@ -121,7 +121,7 @@ struct RfLayout {
   static constexpr uint32_t oA = oEa + 128 * DV;             // A 64 x 64 (K-major)
   static constexpr uint32_t oPart = oA + 8192;               // per-row-block gate sums
   static constexpr uint32_t oVec = oPart + 8192;
-  static constexpr uint32_t oBar = oVec + 6 * 64 * 4 + 16;   // 5 mbarriers (after a flag word)
+  static constexpr uint32_t oBar = oVec + 6 * 64 * 4 + 16;   // 6 mbarriers (after a flag word)
   static constexpr uint32_t oSlot = oBar + 48;
   static constexpr uint32_t bytes = oSlot + 16;
   static constexpr uint32_t launch_bytes = bytes + 1024;
@@ -130,7 +130,9 @@ struct RfLayout {
   static_assert(oP + 4 * 128 * 4 <= kR1, "inverse scratch inside the Q' / K_bar region");
 };
 
-enum : uint32_t { kBarV = 0, kBarK = 1, kBarM1 = 2, kBarM2 = 3, kBarM2b = 4, kBarB = 4 };
+// kBarB and kBarW (the erase and write gates loaded on their own) exist in the
+// rho-folded variant, which has no second M2 group
+enum : uint32_t { kBarV = 0, kBarK = 1, kBarM1 = 2, kBarM2 = 3, kBarM2b = 4, kBarB = 4, kBarW = 5 };
 
 __device__ __forceinline__ uint4 pack8(const float* x) {
   uint4 u;
@@ -298,26 +300,25 @@ __device__ __forceinline__ void prep_keys(unsigned char* smem, unsigned char* pk
 template <int DK, int DV, bool ER, bool QM>
 __device__ __forceinline__ void prep_keys_rf(unsigned char* smem, unsigned char* pkt,
                                              const ChunkArgs& a, const float* sPart,
-                                             const float* sBeta, const float* sLam,
+                                             const float* sTot, const float* sBeta,
+                                             const float* sLam,
                                              const float (&gv)[64 * DK / 8 / kThreads][8],
                                              int* status, int seq, int chunk) {
   using L = RfLayout<DK, DV>;
   using P = Packet<DK, DV>;
   constexpr int VK = DK / 8, RB = kThreads / VK, RPB = 64 / RB;
   const int tid = threadIdx.x, rb = tid / VK, c0 = (tid % VK) * 8, r0 = rb * RPB;
+  // sPart: the log-decay summed over the row blocks before this thread's
+  // (exclusive prefix per key channel); sTot: over the whole chunk
   float G[8], rho[8], tot[8];
-#pragma unroll
-  for (int j = 0; j < 8; ++j) { G[j] = 0.f; tot[j] = 0.f; }
-#pragma unroll
-  for (int b = 0; b < RB; ++b) {
-    const float4* src = reinterpret_cast<const float4*>(sPart + b * DK + c0);
-    const float4 x0 = src[0], x1 = src[1];
-    const float x[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
-#pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      tot[j] += x[j];
-      G[j] += select_f32(b < rb, x[j], 0.f);
-    }
+  {
+    const float4* pre = reinterpret_cast<const float4*>(sPart + rb * DK + c0);
+    const float4* all = reinterpret_cast<const float4*>(sTot + c0);
+    const float4 p0 = pre[0], p1 = pre[1], t0 = all[0], t1 = all[1];
+    G[0] = p0.x; G[1] = p0.y; G[2] = p0.z; G[3] = p0.w;
+    G[4] = p1.x; G[5] = p1.y; G[6] = p1.z; G[7] = p1.w;
+    tot[0] = t0.x; tot[1] = t0.y; tot[2] = t0.z; tot[3] = t0.w;
+    tot[4] = t1.x; tot[5] = t1.y; tot[6] = t1.z; tot[7] = t1.w;
   }
 #pragma unroll
   for (int j = 0; j < 8; ++j) rho[j] = 0.5f * tot[j];
@@ -345,7 +346,7 @@ __device__ __forceinline__ void prep_keys_rf(unsigned char* smem, unsigned char*
     float qv[8], kv[8], bv[8];
     unpack8(ld16(smem, L::oEQ + tc::tile_off(128, 64 + r, c0)), qv);
     unpack8(ld16(smem, L::oK + tc::tile_off(64, r, c0)), kv);
-    if (ER) unpack8(ld16(smem, L::oEQ + tc::tile_off(128, r, c0)), bv);
+    if (ER) unpack8(ld16(smem, L::oEa + tc::tile_off(64, r, c0)), bv);   // b: the w slot
     const float lam = sLam[r], beta = sBeta[r];
     float Eb[8], Qr[8], Kb[8];
 #pragma unroll
@@ -551,7 +552,7 @@ __global__ void __launch_bounds__(kThreads, LEAN ? 3 : 2)
 
   if (warp == 0) tc::tmem_alloc(smem_u32(tslot), L::kTmemCols);
   if (tid == 32) {
-    for (uint32_t i = 0; i < ((LEAN || RF) ? 5u : 4u); ++i) tc::mbar_init(bar(i), 1);
+    for (uint32_t i = 0; i < (RF ? 6u : LEAN ? 5u : 4u); ++i) tc::mbar_init(bar(i), 1);
     tc::fence_mbar_init();
   }
   tc::fence_before_sync();
@@ -578,18 +579,23 @@ __global__ void __launch_bounds__(kThreads, LEAN ? 3 : 2)
     const int x = atomicAdd(rg.counter, 1);
     return x < total ? x : total;
   };
+  // RF with the erase gate: b lands in the w slot (oEa) and has a barrier of
+  // its own, issued as soon as the previous chunk's w is consumed (Z formed),
+  // and w follows once this chunk's tile pass has read b
+  const bool bsep = RF && ER;
   // TMA loads of one chunk's input tiles (thread 64): the value side (v, w) and
   // the key side (q, k, b) each complete one phase of their barrier; the
   // CTA's chunk after that one is prefetched into L2 along with them
   auto load_values = [&](int w, int w_after) {
     int n, bb, h;
     decode(w, n, bb, h);
+    const bool lw = WR && !bsep;
     tc::fence_proxy_async();
-    tc::mbar_arrive_expect_tx(bar(kBarV), (WR ? 2u : 1u) * 128u * DV);
+    tc::mbar_arrive_expect_tx(bar(kBarV), (lw ? 2u : 1u) * 128u * DV);
 #pragma unroll
     for (int blk = 0; blk < DV / 64; ++blk) {
       tc::tma_load_4d(sbase + L::oV + blk * 8192, &tm_v, blk * 64, h, n * kChunk, bb, bar(kBarV));
-      if (WR)
+      if (lw)
         tc::tma_load_4d(sbase + L::oEa + blk * 8192, &tm_w, blk * 64, h, n * kChunk, bb, bar(kBarV));
     }
     if (w_after < total) {
@@ -601,18 +607,24 @@ __global__ void __launch_bounds__(kThreads, LEAN ? 3 : 2)
       }
     }
   };
-  // RF: the erase gate b (over the E_bar rows, which M2 reads) has a barrier
-  // of its own and is loaded after M2; q and k as soon as the inverse is done
-  auto load_b = [&](int w) {
+  auto load_b = [&](int w) {   // (bsep) b into the w slot
     int n, bb, h;
     decode(w, n, bb, h);
     tc::fence_proxy_async();
     tc::mbar_arrive_expect_tx(bar(kBarB), 128u * DK);
 #pragma unroll
     for (int blk = 0; blk < DK / 64; ++blk)
-      tc::tma_load_4d(sbase + L::oEQ + blk * 16384, &tm_b, blk * 64, h, n * kChunk, bb, bar(kBarB));
+      tc::tma_load_4d(sbase + L::oEa + blk * 8192, &tm_b, blk * 64, h, n * kChunk, bb, bar(kBarB));
   };
-  const bool bsep = RF && ER;
+  auto load_w = [&](int w) {   // (bsep and the write gate) w into the w slot
+    int n, bb, h;
+    decode(w, n, bb, h);
+    tc::fence_proxy_async();
+    tc::mbar_arrive_expect_tx(bar(kBarW), 128u * DV);
+#pragma unroll
+    for (int blk = 0; blk < DV / 64; ++blk)
+      tc::tma_load_4d(sbase + L::oEa + blk * 8192, &tm_w, blk * 64, h, n * kChunk, bb, bar(kBarW));
+  };
   auto load_keys = [&](int w, int w_after) {
     int n, bb, h;
     decode(w, n, bb, h);
@@ -640,6 +652,7 @@ __global__ void __launch_bounds__(kThreads, LEAN ? 3 : 2)
   };
   // loads issued and waited for, to drain what is in flight on the way out
   int v_issued = 0, k_issued = 0, v_done = 0, k_done = 0, b_issued = 0, b_done = 0;
+  int w_issued = 0, w_done = 0;
   constexpr bool dyn = DYN;   // work claimed from rg.counter
   const int stride = static_cast<int>(gridDim.x);
   int w = static_cast<int>(blockIdx.x), wn = w + stride, wa = wn + stride;   // this, next, after
@@ -736,6 +749,23 @@ __global__ void __launch_bounds__(kThreads, LEAN ? 3 : 2)
     float gv[64 * DK / 8 / kThreads][8];
     if (CH) load_channel_gates<DK>(a, row0, h, Lr, sPart, gv);
     __syncthreads();
+    if constexpr (RF) {
+      // per key channel: the row blocks' partial sums become exclusive prefix
+      // sums (the same additions, in the same order, as summing them per
+      // thread) and the chunk's total G_C goes to sGs (with sEG: the
+      // scalar-decay arrays, unused here); the key-side wait below orders
+      // these writes before the tile pass reads them
+      if (tid < DK) {
+        float run = 0.f;
+#pragma unroll
+        for (int b = 0; b < kThreads / (DK / 8); ++b) {
+          const float v = sPart[b * DK + tid];
+          sPart[b * DK + tid] = run;
+          run += v;
+        }
+        sGs[tid] = run;
+      }
+    }
 
     if (!vlate && !RF) {   // (RF: the value side is waited for after the inverse)
       if (__syncthreads_or(!tc::mbar_wait(bar(kBarV), par))) { fail_at = 4 * n; break; }
@@ -780,19 +810,19 @@ __global__ void __launch_bounds__(kThreads, LEAN ? 3 : 2)
     } else if constexpr (RF) {   // channel decay (launched only with it)
       switch (a.flags & 10u) {
         case 0:
-          prep_keys_rf<DK, DV, false, false>(smem, pkt, a, sPart, sBeta, sLam, gv, status,
+          prep_keys_rf<DK, DV, false, false>(smem, pkt, a, sPart, sGs, sBeta, sLam, gv, status,
                                              bb * H + h, n);
           break;
         case 2:
-          prep_keys_rf<DK, DV, true, false>(smem, pkt, a, sPart, sBeta, sLam, gv, status,
+          prep_keys_rf<DK, DV, true, false>(smem, pkt, a, sPart, sGs, sBeta, sLam, gv, status,
                                             bb * H + h, n);
           break;
         case 8:
-          prep_keys_rf<DK, DV, false, true>(smem, pkt, a, sPart, sBeta, sLam, gv, status,
+          prep_keys_rf<DK, DV, false, true>(smem, pkt, a, sPart, sGs, sBeta, sLam, gv, status,
                                             bb * H + h, n);
           break;
         default:
-          prep_keys_rf<DK, DV, true, true>(smem, pkt, a, sPart, sBeta, sLam, gv, status,
+          prep_keys_rf<DK, DV, true, true>(smem, pkt, a, sPart, sGs, sBeta, sLam, gv, status,
                                            bb * H + h, n);
           break;
       }
@@ -810,6 +840,15 @@ __global__ void __launch_bounds__(kThreads, LEAN ? 3 : 2)
     }
     tc::fence_proxy_async();
     __syncthreads();
+    if (bsep) {   // b is read: the w slot takes this chunk's w, or (no write gate) the next b
+      if (WR) {
+        if (tid == 64) load_w(w);
+        ++w_issued;
+      } else if (wn < total) {
+        if (tid == 64) load_b(wn);
+        ++b_issued;
+      }
+    }
 
     // ---- M1: [E_bar; Q'] K_bar^T into columns 0..63 ----
     if (tid == 0) {
@@ -1001,15 +1040,25 @@ __global__ void __launch_bounds__(kThreads, LEAN ? 3 : 2)
     // ---- M2: [U | Y] = A [Z | E_abs] (N = DV + DK): U in columns 0..DV-1,
     // Y in columns DV..DV+DK-1 ----
     if constexpr (RF) {
-      // the value side, loaded since the start of the chunk: Z = w (.) v or beta v
-      if (__syncthreads_or(!tc::mbar_wait(bar(kBarV), par))) { fail_at = 4 * n + 2; break; }
+      // the value side, loaded since the start of the chunk (w since the tile
+      // pass when b came first): Z = w (.) v or beta v
+      if (__syncthreads_or(!tc::mbar_wait(bar(kBarV), par) ||
+                           (bsep && WR && !tc::mbar_wait(bar(kBarW), par)))) {
+        fail_at = 4 * n + 2;
+        break;
+      }
       v_done = v_issued;
+      w_done = w_issued;
       if (WR)
         prep_z<DK, DV, true, L>(smem, sBeta);
       else
         prep_z<DK, DV, false, L>(smem, sBeta);
       tc::fence_proxy_async();
       __syncthreads();
+      if (bsep && WR && wn < total) {   // w is consumed: the next chunk's b
+        if (tid == 64) load_b(wn);
+        ++b_issued;
+      }
     }
     // (U^T case: U^T = Z^T A^T in columns 0..63, Y in columns 64..64+DK-1;
     // RF: Y_bar = A E_bar from the E_bar rows of the [E_bar; Q'] tile)
@@ -1043,12 +1092,8 @@ __global__ void __launch_bounds__(kThreads, LEAN ? 3 : 2)
     // Z and E_abs are consumed: the value-side tiles of the next chunk may land now
     // (RF: and the key side, E_bar being consumed too)
     if (wn < total) {
-      if (tid == 64) {
-        load_values(wn, wa);
-        if (bsep) load_b(wn);
-      }
+      if (tid == 64) load_values(wn, wa);
       ++v_issued;
-      if (bsep) ++b_issued;
     }
     {
       // M=64 accumulators: row 16 q + l in lane l < 16 of quadrant q; warp w
@@ -1096,6 +1141,7 @@ __global__ void __launch_bounds__(kThreads, LEAN ? 3 : 2)
       if (v_issued > v_done) tc::mbar_wait(bar(kBarV), static_cast<uint32_t>((v_issued - 1) & 1));
       if (k_issued > k_done) tc::mbar_wait(bar(kBarK), static_cast<uint32_t>((k_issued - 1) & 1));
       if (b_issued > b_done) tc::mbar_wait(bar(kBarB), static_cast<uint32_t>((b_issued - 1) & 1));
+      if (w_issued > w_done) tc::mbar_wait(bar(kBarW), static_cast<uint32_t>((w_issued - 1) & 1));
     }
     if (tid == 0 && status && atomicCAS(status, 0, 5) == 0) {  // GDR_ERR_TIMEOUT
       status[1] = static_cast<int>(blockIdx.x);
