@@ -174,16 +174,14 @@ __device__ __forceinline__ void report_range(int* status, int seq, int chunk) {
 }
 
 // Channel gates, first half of the in-chunk cumsum: thread t loads g for the
-// RPB consecutive rows from r0 = RPB (t / VK), channels c0 = 8 (t % VK) .. +7,
-// keeps them and writes their sums per row block.
+// RPB consecutive rows from r0 = RPB (t / VK), channels c0 = 8 (t % VK) .. +7
+// (rows past the sequence: zeros) and keeps them ...
 template <int DK>
-__device__ __forceinline__ void load_channel_gates(const ChunkArgs& a, size_t row0, int h, int Lr,
-                                                   float* sPart, float (&gv)[64 * DK / 8 / kThreads][8]) {
+__device__ __forceinline__ void load_channel_gate_values(const ChunkArgs& a, size_t row0, int h,
+                                                         int Lr,
+                                                         float (&gv)[64 * DK / 8 / kThreads][8]) {
   constexpr int VK = DK / 8, RPB = 64 * VK / kThreads;
   const int tid = threadIdx.x, rb = tid / VK, c0 = (tid % VK) * 8, r0 = rb * RPB;
-  float ps[8];
-#pragma unroll
-  for (int j = 0; j < 8; ++j) ps[j] = 0.f;
 #pragma unroll
   for (int i = 0; i < RPB; ++i) {
     const int r = r0 + i;
@@ -195,6 +193,19 @@ __device__ __forceinline__ void load_channel_gates(const ChunkArgs& a, size_t ro
     }
     gv[i][0] = x0.x; gv[i][1] = x0.y; gv[i][2] = x0.z; gv[i][3] = x0.w;
     gv[i][4] = x1.x; gv[i][5] = x1.y; gv[i][6] = x1.z; gv[i][7] = x1.w;
+  }
+}
+// ... and writes their sums per row block.
+template <int DK>
+__device__ __forceinline__ void channel_gate_sums(const float (&gv)[64 * DK / 8 / kThreads][8],
+                                                  float* sPart) {
+  constexpr int VK = DK / 8, RPB = 64 * VK / kThreads;
+  const int tid = threadIdx.x, rb = tid / VK, c0 = (tid % VK) * 8;
+  float ps[8];
+#pragma unroll
+  for (int j = 0; j < 8; ++j) ps[j] = 0.f;
+#pragma unroll
+  for (int i = 0; i < RPB; ++i) {
 #pragma unroll
     for (int j = 0; j < 8; ++j) ps[j] += gv[i][j];
   }
@@ -678,6 +689,9 @@ __global__ void __launch_bounds__(kThreads, LEAN ? 3 : 2)
     b_issued = bsep ? 1 : 0;
   }
 
+  // channel gates of the current chunk (RF: the next chunk's are loaded while
+  // this chunk's M2 runs, so they are in registers when its gates phase starts)
+  float gv[64 * DK / 8 / kThreads][8];
   int fail_at = -1, iter = 0;
   for (; w < total; w = wn, wn = wa, ++iter) {
     // the item after the next one: claimed now (published for the loop step)
@@ -746,8 +760,10 @@ __global__ void __launch_bounds__(kThreads, LEAN ? 3 : 2)
       sEGn[lane + 32] = __expf(-g1);
       if (lane == 0) *sFactor = tot >= -80.f ? 1 : 0;
     }
-    float gv[64 * DK / 8 / kThreads][8];
-    if (CH) load_channel_gates<DK>(a, row0, h, Lr, sPart, gv);
+    if (CH) {
+      if (!RF || iter == 0) load_channel_gate_values<DK>(a, row0, h, Lr, gv);
+      channel_gate_sums<DK>(gv, sPart);
+    }
     __syncthreads();
     if constexpr (RF) {
       // per key channel: the row blocks' partial sums become exclusive prefix
@@ -1086,6 +1102,10 @@ __global__ void __launch_bounds__(kThreads, LEAN ? 3 : 2)
           tc::mma_bf16(tmem, dA + ((k0 * 2) >> 4), dZE + (((k0 / 8) * 1024) >> 4), id2, k0 > 0);
       }
       tc::commit(bar(kBarM2));
+    }
+    if (RF && wn < total) {   // the next chunk's channel gates, in flight during M2
+      const int t0n = nn * kChunk;
+      load_channel_gate_values<DK>(a, size_t(nb) * T + t0n, nh, min(kChunk, T - t0n), gv);
     }
     if (__syncthreads_or(!tc::mbar_wait(bar(kBarM2), par))) { fail_at = 4 * n + 2; break; }
     tc::fence_after_sync();
