@@ -73,6 +73,7 @@ def lib():
         L.gdr_recurrent_step.argtypes = [sp] + [_vp] * 10 + [_vp]
         L.gdr_gate_cumsum.argtypes = [ctypes.c_int] * 4 + [_vp, _vp, _vp]
         L.gdr_chunk_fwd_check.argtypes = [_vp, _vp, ctypes.POINTER(ctypes.c_int)]
+        L.gdr_chunk_bwd_check.argtypes = [_vp, _vp, ctypes.POINTER(ctypes.c_int)]
         L.gdr_chunk_bwd_workspace.argtypes = [sp, ctypes.POINTER(ctypes.c_size_t)]
         L.gdr_chunk_bwd.argtypes = [sp] + [_vp] * 20 + [_vp, ctypes.c_size_t, _vp]
         L.gdr_rmsnorm_gate.argtypes = [ctypes.c_longlong, ctypes.c_int, ctypes.c_int, _vp, _vp,
@@ -91,7 +92,7 @@ def lib():
                      "gdr_chunk_fwd_split", "gdr_chunk_fwd_workspace_split",
                      "gdr_chunk_fwd_pipelined", "gdr_chunk_fwd_workspace_pipelined",
                      "gdr_chunk_fwd_pipeline_segments", "gdr_recurrent_step",
-                     "gdr_gate_cumsum", "gdr_chunk_fwd_check", "gdr_rmsnorm_gate",
+                     "gdr_gate_cumsum", "gdr_chunk_fwd_check", "gdr_chunk_bwd_check", "gdr_rmsnorm_gate",
                      "gdr_chunk_bwd_workspace", "gdr_chunk_bwd", "gdr_chunk_fwd_gated",
                      "gdr_chunk_fwd_gated_pipelined", "gdr_token_fwd"):
             getattr(L, name).restype = ctypes.c_int
@@ -440,11 +441,27 @@ def chunk_bwd_workspace_bytes(shape):
     return n.value
 
 
+def chunk_bwd_check(workspace, stream=None):
+    """Status a chunk_bwd call left in its workspace (synchronises the stream):
+    None, or GdrError(GDR_ERR_RANGE) when a chunk's log-decay left the
+    backward's range (the gradients are then not to be used)."""
+    detail = (ctypes.c_int * 2)()
+    with torch.cuda.device(workspace.device):
+        st = lib().gdr_chunk_bwd_check(_ptr(workspace), _stream(stream, workspace.device), detail)
+    if st == 6:
+        raise GdrError(st, "gdr_chunk_bwd (sequence %d, chunk %d)" % (detail[0], detail[1]))
+    if st:
+        raise GdrError(st, "gdr_chunk_bwd_check")
+    return None
+
+
 def chunk_bwd(q, k, v, g, dO, beta=None, lam=None, b=None, w=None, h0=None, dhT=None, *,
-              scale=None, flags=None, workspace=None, stream=None):
+              scale=None, flags=None, workspace=None, stream=None, check=False):
     """Gradients of <dO, o> + <dhT, hT> for ``chunk_fwd`` on the same inputs
     (``gdr_chunk_bwd``). Returns a dict of fp32 tensors: q, k, v, g, and beta,
-    lam, b, w, h0 where they apply (None otherwise)."""
+    lam, b, w, h0 where they apply (None otherwise). With check=True the call
+    synchronises and raises GdrError(GDR_ERR_RANGE) for inputs past the
+    backward's decay range (chunk_bwd_check)."""
     B, T, H, dk = q.shape
     dv = v.shape[-1]
     dev, dt = q.device, q.dtype
@@ -475,4 +492,6 @@ def chunk_bwd(q, k, v, g, dO, beta=None, lam=None, b=None, w=None, h0=None, dhT=
                                  _stream(stream, dev))
     if st:
         raise GdrError(st, "gdr_chunk_bwd")
+    if check:
+        chunk_bwd_check(workspace, stream)
     return out

@@ -37,6 +37,12 @@ namespace {
 
 constexpr int kC = 64;            // chunk length
 constexpr int kBwdThreads = 256;
+// The records hold K_bar = k / gamma and E_bar = gamma E with gamma = e^{G} taken
+// from the chunk's first row, so an in-chunk log-decay sum below this leaves
+// 1 / gamma outside the fp32 range (e^{88.7}) with margin; such a chunk is
+// reported as GDR_ERR_RANGE in the status words ([1] = batch * H + head,
+// [2] = chunk; the first report wins) and its gradients are not to be used.
+constexpr float kBwdDecayFloor = -80.f;
 
 constexpr int kKT = 32;           // K slice of the staged products
 constexpr int kU = 4;             // elements per thread whose loads are issued together
@@ -268,6 +274,7 @@ struct BwdPtrs {
   float* dS;       // [B, H, Nc, dk, dv] gradient leaving each chunk (dS_{n+1})
   float* dW;       // [B, H, Nc, 64, dv]
   float* scr;      // [chunks] per-chunk scratch of the gradient kernel
+  int* status;     // kStatusWords status words (the start of the workspace)
   int B, T, H, dk, dv, Nc;
   unsigned flags;
   float scale;
@@ -315,12 +322,14 @@ __global__ void __launch_bounds__(kBwdThreads, 3) bwd_chunk_prep(const BwdPtrs p
     sG[tid] = tid < Lr ? p.g[tok(tid)] : 0.f;
   }
   __syncthreads();
+  bool low = false;   // some G below the range of the records (kBwdDecayFloor)
   if (CH) {
     for (int c = tid; c < dk; c += bd) {
       float acc = 0.f;
       for (int i = 0; i < kC; ++i) {
         acc += sG[i * dk + c];
         sG[i * dk + c] = acc;
+        low |= acc < kBwdDecayFloor;
       }
       sGC[c] = expf(acc);
     }
@@ -329,7 +338,12 @@ __global__ void __launch_bounds__(kBwdThreads, 3) bwd_chunk_prep(const BwdPtrs p
     for (int i = 0; i < kC; ++i) {
       acc += sG[i];
       sG[i] = acc;
+      low |= acc < kBwdDecayFloor;
     }
+  }
+  if (low && atomicCAS(p.status, 0, 6) == 0) {   // GDR_ERR_RANGE
+    p.status[1] = bh;
+    p.status[2] = n;
   }
   __syncthreads();
   if (!CH)
@@ -1117,7 +1131,7 @@ size_t chunk_bwd_workspace_bytes(int B, int T, int H, int dk, int dv) {
   const Scr Q{dk, dv};
   const size_t floats = chunks * (R.size() + Q.size() + 2 * static_cast<size_t>(dk) * dv +
                                   2 * static_cast<size_t>(kC) * dv);
-  return floats * sizeof(float);
+  return kChunkWorkspaceBytes + floats * sizeof(float);   // status words, then the records
 }
 
 cudaError_t launch_chunk_bwd(const ChunkBwdArgs& a, bool f32, cudaStream_t stream) {
@@ -1133,7 +1147,11 @@ cudaError_t launch_chunk_bwd(const ChunkBwdArgs& a, bool f32, cudaStream_t strea
   const size_t chunks = static_cast<size_t>(p.B) * p.H * p.Nc;
   const Rec R{p.dk, p.dv};
   const Scr Q{p.dk, p.dv};
-  float* base = static_cast<float*>(a.workspace);
+  p.status = static_cast<int*>(a.workspace);
+  cudaError_t err = cudaMemsetAsync(p.status, 0, kStatusWords * sizeof(int), stream);
+  if (err != cudaSuccess) return err;
+  float* base = reinterpret_cast<float*>(static_cast<unsigned char*>(a.workspace) +
+                                         kChunkWorkspaceBytes);
   p.rec = base;
   p.scr = p.rec + chunks * R.size();
   p.S = p.scr + chunks * Q.size();

@@ -199,8 +199,22 @@ gdr_status gdr_chunk_fwd_workspace_split(const gdr_shape* shape, int segments, s
 
 namespace {
 
-// The chunked forward with `segments` runs per (batch, head) for the two-kernel
-// path (0: the default policy).
+// Status words a chunked call left at the start of its workspace.
+gdr_status read_status(const void* workspace, gdr_stream_t stream, int* detail) {
+  if (!workspace || !aligned(workspace, 16)) return GDR_ERR_INVALID_ARG;
+  int words[gdr::kStatusWords] = {0, 0, 0, 0};
+  const cudaStream_t st_ = reinterpret_cast<cudaStream_t>(stream);
+  if (cudaMemcpyAsync(words, workspace, sizeof(words), cudaMemcpyDeviceToHost, st_) !=
+          cudaSuccess ||
+      cudaStreamSynchronize(st_) != cudaSuccess)
+    return GDR_ERR_CUDA;
+  if (detail) {
+    detail[0] = words[1];
+    detail[1] = words[2];
+  }
+  return words[0] == 0 ? GDR_OK : static_cast<gdr_status>(words[0]);
+}
+
 // The output epilogue's arguments: valid, and y apart from z.
 gdr_status check_out_gate(const gdr_shape* s, const gdr_out_gate* gate, const void* y) {
   if (!gate || !gate->z || !gate->weight) return GDR_ERR_INVALID_ARG;
@@ -607,18 +621,11 @@ gdr_status gdr_chunk_bwd(const gdr_shape* shape, const void* q, const void* k, c
 }
 
 gdr_status gdr_chunk_fwd_check(const void* workspace, gdr_stream_t stream, int* detail) {
-  if (!workspace || !aligned(workspace, 16)) return GDR_ERR_INVALID_ARG;
-  int words[gdr::kStatusWords] = {0, 0, 0, 0};
-  const cudaStream_t st_ = reinterpret_cast<cudaStream_t>(stream);
-  if (cudaMemcpyAsync(words, workspace, sizeof(words), cudaMemcpyDeviceToHost, st_) !=
-          cudaSuccess ||
-      cudaStreamSynchronize(st_) != cudaSuccess)
-    return GDR_ERR_CUDA;
-  if (detail) {
-    detail[0] = words[1];
-    detail[1] = words[2];
-  }
-  return words[0] == 0 ? GDR_OK : static_cast<gdr_status>(words[0]);
+  return read_status(workspace, stream, detail);
+}
+
+gdr_status gdr_chunk_bwd_check(const void* workspace, gdr_stream_t stream, int* detail) {
+  return read_status(workspace, stream, detail);
 }
 
 gdr_status gdr_recurrent_step(const gdr_shape* shape, const void* q, const void* k,

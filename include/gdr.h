@@ -78,8 +78,13 @@
  *    return GDR_ERR_RANGE (detail[0] = b * H + h of the first such sequence
  *    seen, detail[1] = its chunk) and its outputs are not to be used;
  *    gdr_token_fwd computes such inputs without the limit. Scalar
- *    gates, GDR_BETA_CHANNEL and the recurrent step have no such limit. The
- *    chunk backward assumes every in-chunk sum above -80.
+ *    gates, GDR_BETA_CHANNEL and the recurrent step have no such limit.
+ *  - Decay range of the chunk backward (every gate variant): within one chunk
+ *    the running sum of the log-decay (per key channel, or per row for a
+ *    scalar decay) must stay above -80, since the backward's records hold
+ *    k / e^{G}. A chunk past it makes gdr_chunk_bwd_check return
+ *    GDR_ERR_RANGE (detail as above) and the gradients are not to be used;
+ *    there is no backward without the limit.
  */
 #ifndef GDR_H_
 #define GDR_H_
@@ -287,9 +292,10 @@ gdr_status gdr_chunk_fwd_pipeline_segments(const gdr_shape* shape, int* segments
  * in `workspace` (at least
  * gdr_chunk_bwd_workspace() bytes, 16-byte aligned; about 0.9 MB per chunk at
  * d_k = d_v = 128): the chunk's forward quantities, the state entering and
- * the gradient leaving every chunk. It assumes each in-chunk log-decay sum
- * stays above -80 (1 / gamma within fp32). GDR_BETA_CHANNEL returns
- * GDR_ERR_UNSUPPORTED.
+ * the gradient leaving every chunk. The workspace starts with
+ * status words: a chunk whose running log-decay sum falls below -80 (the
+ * range of 1 / gamma in fp32) is reported there as GDR_ERR_RANGE, read by
+ * gdr_chunk_bwd_check. GDR_BETA_CHANNEL returns GDR_ERR_UNSUPPORTED.
  */
 gdr_status gdr_chunk_bwd_workspace(const gdr_shape* shape, size_t* bytes);
 gdr_status gdr_chunk_bwd(const gdr_shape* shape, const void* q, const void* k, const void* v,
@@ -310,6 +316,15 @@ gdr_status gdr_chunk_bwd(const gdr_shape* shape, const void* q, const void* k, c
  * report wins. Workspaces of 0 bytes need no check.
  */
 gdr_status gdr_chunk_fwd_check(const void* workspace, gdr_stream_t stream,
+                               int* detail);
+
+/*
+ * The same for a gdr_chunk_bwd call's workspace: GDR_OK, or GDR_ERR_RANGE
+ * when a chunk's log-decay left the backward's range (detail[0] = b * H + h
+ * of the first such sequence seen, detail[1] = its chunk). Synchronises
+ * `stream`.
+ */
+gdr_status gdr_chunk_bwd_check(const void* workspace, gdr_stream_t stream,
                                int* detail);
 
 /*

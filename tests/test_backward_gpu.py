@@ -116,3 +116,40 @@ def test_backward_against_autograd(flags, dtype):
             e = rel_err(grads[n][0, :, h].cpu(), ref[n])
             assert e <= tol, (n, h, e)
         assert rel_err(grads["h0"][0, h].cpu(), ref["S0"]) <= tol
+
+
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16], ids=["f32", "bf16"])
+@pytest.mark.parametrize("variant", ["gdn", "kda", "gdn2"])
+def test_backward_decay_past_its_range_is_reported(variant, dtype):
+    """A chunk whose running log-decay sum falls below -80 (per row for the
+    scalar decay, per key channel otherwise) makes the backward's status
+    GDR_ERR_RANGE, naming the first such sequence and its chunk."""
+    B, T, H = 2, 64 * 3 + 7, 2
+    x = wl.make_inputs(variant, B, T, H, 128, 128, dtype, seed=71, h0_std=0.02)
+    if x["g"].dim() == 4:
+        x["g"][1, 64:128, 0, 9] = -1.5       # sequence b=1, h=0, chunk 1: -96 on one channel
+    else:
+        x["g"][1, 64:128, 0] = -1.5
+    dO, dhT = _cotangents(x, 7)
+    d = to_dev(x)
+    with pytest.raises(gdr.GdrError) as e:
+        gdr.chunk_bwd(d["q"], d["k"], d["v"], d["g"], dO.cuda(), d["beta"], d["lam"], d["b"],
+                      d["w"], d["h0"], dhT.cuda(), scale=x["scale"], flags=x["flags"],
+                      check=True)
+    assert e.value.code == 6
+    assert "sequence 2, chunk 1" in str(e.value)
+
+
+@pytest.mark.parametrize("variant", ["gdn", "kda"])
+def test_backward_decay_inside_its_range(variant):
+    """Running sums down to about -74 within a chunk: no report, and the
+    gradients keep the fp32 bar against the oracle."""
+    x = wl.make_inputs(variant, 1, 64 * 2, 2, 128, 128, torch.float32, seed=72, h0_std=0.05)
+    x["g"] = torch.full_like(x["g"], -1.15)   # -73.6 over a full chunk
+    if x["g"].dim() == 4:
+        x["g"][..., ::2] = -0.01
+    dO, dhT = _cotangents(x, 8)
+    d = to_dev(x)
+    gdr.chunk_bwd(d["q"], d["k"], d["v"], d["g"], dO.cuda(), d["beta"], d["lam"], d["b"], d["w"],
+                  d["h0"], dhT.cuda(), scale=x["scale"], flags=x["flags"], check=True)
+    check(x, seed=8)
