@@ -247,6 +247,16 @@ __global__ void __launch_bounds__(Roles<CW>::kThreads, 1)
       for (int j = 0; j < KH; ++j) S[j] *= e0[j];
     }
     if (ok0) store_sa();
+    // RF, warp 1: e^{rho} of the chunk after the current one, read from the
+    // packets in global memory (complete before this launch) two chunks ahead,
+    // so that the update factor never waits for the packet ring
+    float rho_next[DK / 32];
+    auto load_rho = [&](int m) {   // chunk m of this run, m < cnt
+      const float* src = reinterpret_cast<const float*>(pk0 + size_t(m) * P::bytes + P::oGc) + DK;
+#pragma unroll
+      for (int i = 0; i < DK / 32; ++i) rho_next[i] = __ldg(src + 32 * i + lane);
+    };
+    if (rf && warp == 1 && cnt > 1) load_rho(1);
     tc::fence_before_sync();
     if (tc::named_any(kChainBar, kChainThreads, !ok0)) fail = 0;
     for (int n = 0; n < (fail < 0 ? cnt : 0); ++n) {
@@ -308,23 +318,16 @@ __global__ void __launch_bounds__(Roles<CW>::kThreads, 1)
       }
       if (rf && warp == 1 && ok) {
         // m = e^{rho_n} e^{rho_{n+1}} per key channel for this chunk's update (the
-        // next chunk's factor is 1 after the last chunk)
+        // next chunk's factor is 1 after the last chunk); then e^{rho_{n+2}}
         const float* en = reinterpret_cast<const float*>(sst + P::oGc) + DK;
         float mv[DK / 32];
-        if (n + 1 < cnt) {
-          const int s1 = (n + 1) % kStages;
-          if (!spin_test(bar(kFull0 + s1), ((n + 1) / kStages) & 1, 4096))
-            ok = wait_or_abort(bar(kFull0 + s1), ((n + 1) / kStages) & 1, abort_flag);
-          const float* e1 = reinterpret_cast<const float*>(smem + s1 * L::kStage + P::oGc) + DK;
 #pragma unroll
-          for (int i = 0; i < DK / 32; ++i) mv[i] = en[32 * i + lane] * e1[32 * i + lane];
-        } else {
-#pragma unroll
-          for (int i = 0; i < DK / 32; ++i) mv[i] = en[32 * i + lane];
-        }
+        for (int i = 0; i < DK / 32; ++i)
+          mv[i] = n + 1 < cnt ? en[32 * i + lane] * rho_next[i] : en[32 * i + lane];
         float* sm = reinterpret_cast<float*>(smem + L::oM);
 #pragma unroll
         for (int i = 0; i < DK / 32; ++i) sm[32 * i + lane] = mv[i];
+        if (n + 2 < cnt) load_rho(n + 2);
       }
       if (tid == 0 && n + 1 < cnt && ok) {
         // meanwhile: the next chunk's packet and its D1 buffer (read out for chunk n-1)
