@@ -294,7 +294,7 @@ __global__ void __launch_bounds__(kBwdThreads, 3) bwd_chunk_prep(const BwdPtrs p
   const int dk = p.dk, dv = p.dv, tid = threadIdx.x;
   float* r = p.rec + static_cast<size_t>(cid) * R.size();
   const bool CH = p.flags & 1u, ER = p.flags & 2u, WR = p.flags & 4u, QM = p.flags & 8u;
-  extern __shared__ float sg[];
+  extern __shared__ __align__(16) float sg[];
   const T* q = static_cast<const T*>(p.q);
   const T* k = static_cast<const T*>(p.k);
   const T* v = static_cast<const T*>(p.v);
@@ -905,7 +905,7 @@ __global__ void __launch_bounds__(kBwdThreads, 3) bwd_chunk_grad(const BwdPtrs p
   const bool CH = p.flags & 1u, ER = p.flags & 2u, WR = p.flags & 4u, QM = p.flags & 8u;
   const float* r = p.rec + static_cast<size_t>(cid) * R.size();
   float* s = p.scr + static_cast<size_t>(cid) * Q.size();
-  extern __shared__ float sg[];
+  extern __shared__ __align__(16) float sg[];
   const float* S = p.S + static_cast<size_t>(cid) * dk * dv;
   const float* dSn = p.dS + static_cast<size_t>(cid) * dk * dv;
   const float* W = p.W + static_cast<size_t>(cid) * kC * dv;

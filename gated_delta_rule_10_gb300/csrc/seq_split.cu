@@ -27,7 +27,7 @@ __global__ void __launch_bounds__(kCombThreads)
                            const float* __restrict__ h0, float* __restrict__ S, int P, int dv) {
   constexpr int RPT = DK * kCombCols / kCombThreads;   // rows per thread (4 or 2)
   constexpr int LD = DK + kCombPad;
-  extern __shared__ float smc[];
+  extern __shared__ __align__(16) float smc[];
   float* sM = smc;                           // [DK][LD]
   float* sS = sM + DK * LD;                  // [DK][kCombCols]
   const int tid = threadIdx.x;

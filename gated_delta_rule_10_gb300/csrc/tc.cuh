@@ -246,6 +246,15 @@ __device__ __forceinline__ void tma_store_4d(const void* tmap, int c0, int c1, i
       ::"l"(reinterpret_cast<uint64_t>(tmap)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(src)
       : "memory");
 }
+// Plain (untiled) bulk copy of `bytes` contiguous bytes from shared to global
+// memory, completion tracked as a bulk group (bulk_commit, bulk_wait_*). Both
+// addresses 16-byte aligned, size a multiple of 16.
+__device__ __forceinline__ void bulk_store(void* dst, uint32_t src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;\n" ::"l"(
+                   reinterpret_cast<uint64_t>(dst)),
+               "r"(src), "r"(bytes)
+               : "memory");
+}
 __device__ __forceinline__ void bulk_commit() {
   asm volatile("cp.async.bulk.commit_group;\n" ::: "memory");
 }

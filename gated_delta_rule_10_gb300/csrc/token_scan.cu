@@ -27,7 +27,12 @@ constexpr int kRG = kScanThreads / kCG;   // row groups (32)
 template <int DK, int DV, typename TIn>
 __global__ void __launch_bounds__(kScanThreads) token_scan_kernel(const ChunkArgs a) {
   constexpr int RPT = DK / kRG;           // state rows per thread
-  __shared__ float s_alpha[2][DK], s_e[2][DK], s_k[2][DK], s_q[2][DK], s_z[2][kCols];
+  // every array 16-byte aligned: z is read as float4
+  __shared__ __align__(16) float s_alpha[2][DK];
+  __shared__ __align__(16) float s_e[2][DK];
+  __shared__ __align__(16) float s_k[2][DK];
+  __shared__ __align__(16) float s_q[2][DK];
+  __shared__ __align__(16) float s_z[2][kCols];
   __shared__ float4 s_red[2][kRG][kCG];
   __shared__ float s_kq[2][kScanThreads / 32];
 

@@ -105,7 +105,7 @@ __global__ void __launch_bounds__(32 * NW)
   using EL = Elem<T>;
   constexpr int kVBThreads = L::kThreads;
   constexpr int R = L::R, E = L::E;
-  extern __shared__ float sm[];
+  extern __shared__ __align__(16) float sm[];
   float* sK = sm + L::oK;
   float* sQ = sm + L::oQ;
   float* sV = sm + L::oV;
