@@ -227,13 +227,15 @@ gdr_status gdr_chunk_fwd_workspace_split(const gdr_shape* shape, int segments,
 /*
  * gdr_chunk_fwd for long sequences with few (batch, head) pairs, bf16 only,
  * overlapping the two kernels of the two-kernel path in time. The chunks of
- * every sequence are cut into `segments` time segments of equal whole chunks
- * (fewer when there are fewer chunks). The chunk preparation of segment s runs
+ * every sequence are cut into `segments` time segments of whole chunks (fewer
+ * when there are fewer chunks): up to three segments shrink by 5/8 from each to
+ * the next, more are equal. The chunk preparation of segment s runs
  * on `stream`; the state pass of segment s runs on `aux_stream` once those
  * packets exist, continuing from the state segment s - 1 left in the
  * workspace, while the preparation of segment s + 1 runs on the SMs the state
  * pass leaves free (it walks the chunks of each (batch, head) in order and
- * takes one SM per (batch, head, 64 value columns)). The state update and the
+ * takes one SM per (batch, head) at d_k = d_v = 128, per (batch, head, 64
+ * value columns) otherwise). The state update and the
  * read-out are those of gdr_chunk_fwd (Gated DeltaNet-2 notes, key design 2);
  * only the order of the launches differs, so the result is the same up to
  * rounding. Each preparation CTA claims one chunk from a counter and exits,
@@ -268,8 +270,10 @@ gdr_status gdr_chunk_fwd_workspace_pipelined(const gdr_shape* shape, int segment
 /* The number of time segments gdr_chunk_fwd_pipelined should use on `shape`;
  * 1 means that the overlap is not expected to pay and gdr_chunk_fwd is the
  * call to make. It is above 1 for bf16 when the state pass takes at most half
- * of 152 SMs (B * H * d_v / 64 <= 76), gdr_chunk_fwd would not split the
- * sequences, and every segment keeps at least 32 chunks (up to 8 segments). */
+ * of 152 SMs (its CTAs as above), gdr_chunk_fwd would not split the
+ * sequences, and there are at least 64 chunks: up to 8 segments of at least
+ * 32 chunks when the state pass takes at most a quarter of the SMs, else up to
+ * 3 (one per 32 chunks). */
 gdr_status gdr_chunk_fwd_pipeline_segments(const gdr_shape* shape, int* segments);
 
 /*

@@ -283,11 +283,13 @@ def test_pipelined_forward_workspace_policy_and_argument_rules(L):
                                                ctypes.byref(n)) == 2
     assert L.gdr_chunk_fwd_workspace_pipelined(ctypes.byref(s), 2, None) == 1
     # policy: the Gated DeltaNet-2 prefill (B*H = 32, 1024 chunks) is pipelined in 8
-    # segments, B*H = 64 (the transposed state pass takes 64 SMs) in 2; workloads
-    # that the sequence split takes, that are short or fp32 are not
+    # segments, B*H = 64 (the transposed state pass takes 64 SMs) in up to 3 (one
+    # per 32 chunks); workloads that the sequence split takes, that are short or
+    # fp32 are not
     for (B, T, H, dt), want in (((1, 65536, 32, _binding.GDR_BF16), 8),
                                 ((4, 4096, 16, _binding.GDR_BF16), 2),
-                                ((2, 16384, 32, _binding.GDR_BF16), 2),
+                                ((4, 8192, 16, _binding.GDR_BF16), 3),
+                                ((2, 16384, 32, _binding.GDR_BF16), 3),
                                 ((8, 16384, 32, _binding.GDR_BF16), 1),
                                 ((1, 65536, 4, _binding.GDR_BF16), 1),
                                 ((1, 2048, 8, _binding.GDR_BF16), 1),
