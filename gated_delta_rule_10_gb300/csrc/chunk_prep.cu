@@ -971,7 +971,59 @@ __global__ void __launch_bounds__(kThreads, LEAN ? 3 : 2)
       ++k_issued;
     }
 
-    if constexpr (LEAN) {
+    if constexpr (LEAN && UT) {
+      // ---- M2 as one group within 128 TMEM columns, both products M = 128,
+      // N = 64 with the A tile as the K-major B: U^T = Z^T A^T into columns
+      // 0..63 and Y^T = E_abs^T A^T into 64..127 (Z and E_abs as MN-major A) ----
+      const uint64_t dA = tc::smem_desc(sbase + L::oA, 16, 1024);
+      if (vlate) {
+        if (__syncthreads_or(!tc::mbar_wait(bar(kBarV), par))) { fail_at = 4 * n + 2; break; }
+        v_done = v_issued;
+      }
+      if (tid == 0) {
+        tc::fence_after_sync();
+        const uint64_t dZ = tc::smem_desc(sbase + L::oV, 64 * 128, 1024);
+        const uint64_t dE = tc::smem_desc(sbase + L::oEa, 64 * 128, 1024);
+        constexpr uint32_t idu = tc::idesc_bf16(128, 64, 1, 0);
+#pragma unroll
+        for (int k0 = 0; k0 < 64; k0 += 16)
+          tc::mma_bf16(tmem, dZ + (((k0 / 8) * 1024) >> 4), dA + ((k0 * 2) >> 4), idu, k0 > 0);
+#pragma unroll
+        for (int k0 = 0; k0 < 64; k0 += 16)
+          tc::mma_bf16(tmem + 64, dE + (((k0 / 8) * 1024) >> 4), dA + ((k0 * 2) >> 4), idu,
+                       k0 > 0);
+        tc::commit(bar(kBarM2));
+      }
+      if (__syncthreads_or(!tc::mbar_wait(bar(kBarM2), par))) { fail_at = 4 * n + 2; break; }
+      tc::fence_after_sync();
+      // v, the A tile and E_abs are consumed: the next chunk's value side
+      // (under QMIX after its M1) and its key side may land now
+      if (!vlate && wn < total) {
+        if (tid == 64) load_values(wn, wa);
+        ++v_issued;
+      }
+      if (wn < total) {
+        if (tid == 64) load_keys(wn, wa);
+        ++k_issued;
+      }
+      store_ut(pkt, tmem, warp, lane);
+      {
+        // -Y into rows 64..127 of the packet's [Q_gamma; -Y] tile: lane c of
+        // quadrant w % 4 holds key channel c, tokens 32 (w / 4) .. +31; a warp's
+        // store covers 32 adjacent channels of one row (64 bytes)
+        const int q = warp & 3, half = warp >> 2, c = 32 * q + lane;
+#pragma unroll
+        for (int p16 = 0; p16 < 2; ++p16) {
+          const int t0 = 32 * half + 16 * p16;
+          float x[16];
+          tc::tmem_ld16(tmem + (static_cast<uint32_t>(32 * q) << 16) + 64 + t0, x);
+#pragma unroll
+          for (int j = 0; j < 16; ++j)
+            *reinterpret_cast<__nv_bfloat16*>(pkt + P::oQY + tc::tile_off(128, 64 + t0 + j, c)) =
+                __float2bfloat16_rn(-x[j]);
+        }
+      }
+    } else if constexpr (LEAN) {
       // ---- M2 in two groups within 128 TMEM columns: U = A Z (N = DV), read
       // out, then Y = A E_abs (N = DK), read out ----
       const uint64_t dA = tc::smem_desc(sbase + L::oA, 16, 1024);
