@@ -620,6 +620,37 @@ def measure_value_beta(gdr, dev, stream, flush, K, pk, clk):
                              "unit": "TFLOP/s", "frac": round(tf / alu_peak, 4),
                              "peak_source": "derived: 152 SMs x 128 FP32 lanes x 2 x SM clock"}
         out[name] = r
+    # the backward of the same workload (the token-order backward with chunk
+    # checkpoints: a forward pass, then every chunk re-run and walked back);
+    # against the FP32 pipe with about 3 x 7 + 12 d_k d_v flops per token-head
+    gen = torch.Generator(device=dev).manual_seed(11)
+    dO = torch.randn(B, T, H, dv, generator=gen, device=dev).to(c["dtype"])
+    dhT = torch.randn(B, H, dk, dv, generator=gen, device=dev) * 0.1
+    bws = torch.empty(gdr.chunk_bwd_workspace_bytes(shape), dtype=torch.uint8, device=dev)
+
+    def bwd():
+        gdr.chunk_bwd(x["q"], x["k"], x["v"], x["g"], dO, x["beta"], h0=x["h0"], dhT=dhT,
+                      scale=x["scale"], flags=x["flags"], workspace=bws)
+
+    for _ in range(2):
+        bwd()
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(K)]
+    torch.cuda.synchronize()
+    for i in range(K):
+        flush.fill_(float(i))
+        ev[i][0].record(stream)
+        bwd()
+        ev[i][1].record(stream)
+    torch.cuda.synchronize()
+    ms = statistics.mean(ev[i][0].elapsed_time(ev[i][1]) for i in range(K))
+    bflops = 33.0 * dk * dv * th
+    tf = bflops / (ms / 1e3) / 1e12
+    out["backward"] = {"ms_mean": round(ms, 4), "token_heads_per_s": round(th / (ms / 1e3), 1),
+                       "kernels": "value_beta_bwd_kernel", "workspace_bytes": bws.numel(),
+                       "roofline": {"bound": "alu", "achieved": round(tf, 2),
+                                    "peak": round(alu_peak, 2), "unit": "TFLOP/s",
+                                    "frac": round(tf / alu_peak, 4),
+                                    "peak_source": "derived: 152 SMs x 128 FP32 lanes x 2 x SM clock"}}
     return out
 
 

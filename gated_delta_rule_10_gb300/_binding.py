@@ -466,7 +466,7 @@ def chunk_bwd(q, k, v, g, dO, beta=None, lam=None, b=None, w=None, h0=None, dhT=
     dv = v.shape[-1]
     dev, dt = q.device, q.dtype
     if flags is None:
-        flags = _infer_flags(g.dim() == 4, b, w, lam)
+        flags = _infer_flags(g.dim() == 4, b, w, lam, beta is not None and beta.dim() == 4)
     if scale is None:
         scale = dk ** -0.5
     _check(dO, "dO", dt, dev, (B, T, H, dv))
@@ -474,7 +474,7 @@ def chunk_bwd(q, k, v, g, dO, beta=None, lam=None, b=None, w=None, h0=None, dhT=
     f32 = dict(dtype=torch.float32, device=dev)
     out = {"q": torch.empty(B, T, H, dk, **f32), "k": torch.empty(B, T, H, dk, **f32),
            "v": torch.empty(B, T, H, dv, **f32), "g": torch.empty(tuple(g.shape), **f32),
-           "beta": None if beta is None else torch.empty(B, T, H, **f32),
+           "beta": None if beta is None else torch.empty(tuple(beta.shape), **f32),
            "lam": None if lam is None else torch.empty(B, T, H, **f32),
            "b": None if b is None else torch.empty(B, T, H, dk, **f32),
            "w": None if w is None else torch.empty(B, T, H, dv, **f32),

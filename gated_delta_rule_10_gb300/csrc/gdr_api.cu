@@ -603,7 +603,11 @@ gdr_status gdr_chunk_bwd_workspace(const gdr_shape* shape, size_t* bytes) {
   if (!bytes) return GDR_ERR_INVALID_ARG;
   const gdr_status st = check_shape(shape, false);
   if (st != GDR_OK) return st;
-  if (shape->flags & GDR_BETA_CHANNEL) return GDR_ERR_UNSUPPORTED;
+  if (shape->flags & GDR_BETA_CHANNEL) {   // the token-order backward (value_beta_bwd.cu)
+    *bytes = gdr::value_beta_bwd_workspace_bytes(shape->B, shape->T, shape->H, shape->dk,
+                                                 shape->dv);
+    return GDR_OK;
+  }
   *bytes = gdr::chunk_bwd_workspace_bytes(shape->B, shape->T, shape->H, shape->dk, shape->dv);
   return GDR_OK;
 }
@@ -616,7 +620,6 @@ gdr_status gdr_chunk_bwd(const gdr_shape* shape, const void* q, const void* k, c
                          gdr_stream_t stream) {
   gdr_status st = check_shape(shape, false);
   if (st != GDR_OK) return st;
-  if (shape->flags & GDR_BETA_CHANNEL) return GDR_ERR_UNSUPPORTED;
   st = check_gates(shape, q, k, v, g, beta, lam, b, w, dO);   // dO takes o's rules
   if (st != GDR_OK) return st;
   const unsigned f = shape->flags;
@@ -634,6 +637,20 @@ gdr_status gdr_chunk_bwd(const gdr_shape* shape, const void* q, const void* k, c
   size_t need = 0;
   gdr_chunk_bwd_workspace(shape, &need);
   if (!workspace || ws_bytes < need || !aligned(workspace, 16)) return GDR_ERR_WORKSPACE;
+  if (f & GDR_BETA_CHANNEL) {
+    // the write strength per value channel: the token-order backward with
+    // chunk checkpoints; no range limit, so the status words stay clear
+    gdr::ValueBetaBwdArgs a;
+    a.q = q; a.k = k; a.v = v; a.dO = dO; a.g = g; a.beta = beta; a.h0 = h0; a.dhT = dhT;
+    a.dq = dq; a.dk = dk; a.dv = dv; a.dg = dg; a.dbeta = dbeta; a.dh0 = dh0;
+    a.workspace = workspace;
+    a.B = shape->B; a.T = shape->T; a.H = shape->H; a.nk = shape->dk; a.nv = shape->dv;
+    a.scale = shape->scale;
+    const cudaStream_t st_ = reinterpret_cast<cudaStream_t>(stream);
+    cudaError_t err = cudaMemsetAsync(workspace, 0, gdr::kStatusWords * sizeof(int), st_);
+    if (err == cudaSuccess) err = gdr::launch_value_beta_bwd(a, shape->dtype == GDR_F32, st_);
+    return err == cudaSuccess ? GDR_OK : GDR_ERR_CUDA;
+  }
   gdr::ChunkBwdArgs a;
   a.q = q; a.k = k; a.v = v; a.dO = dO; a.g = g; a.beta = beta; a.lam = lam; a.b = b; a.w = w;
   a.h0 = h0; a.dhT = dhT;

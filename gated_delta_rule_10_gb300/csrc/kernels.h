@@ -159,6 +159,21 @@ cudaError_t launch_token_scan(const ChunkArgs& a, int dk, bool f32, cudaStream_t
 // Write strength per value channel (flag 16): token-order scan, fp32 state.
 cudaError_t launch_value_beta_scan(const ValueBetaArgs& a, int dk, int dv, bool f32,
                                    cudaStream_t stream);
+// Gradients of the token-order scan with a write strength per value channel
+// (flag 16): inputs as ValueBetaArgs plus dO (the call's dtype) and dhT (fp32,
+// or null); fp32 outputs dq, dk [B,T,H,nk], dv, dbeta [B,T,H,nv], dg [B,T,H],
+// dh0 [B,H,nk,nv] (or null); value_beta_bwd_workspace_bytes of workspace
+// (16-byte aligned). nv must be a multiple of 32.
+struct ValueBetaBwdArgs {
+  const void *q, *k, *v, *dO;
+  const float *g, *beta, *h0, *dhT;
+  float *dq, *dk, *dv, *dg, *dbeta, *dh0;
+  void* workspace;
+  int B, T, H, nk, nv;
+  float scale;
+};
+size_t value_beta_bwd_workspace_bytes(int B, int T, int H, int dk, int dv);
+cudaError_t launch_value_beta_bwd(const ValueBetaBwdArgs& a, bool f32, cudaStream_t stream);
 cudaError_t launch_gate_cumsum(const float* g, float* G, int B, int T, int X,
                                cudaStream_t stream);
 

@@ -285,7 +285,8 @@ gdr_status gdr_chunk_fwd_pipeline_segments(const gdr_shape* shape, int* segments
  *
  *   dq, dk [B,T,H,d_k] fp32     dv [B,T,H,d_v] fp32
  *   dg     [B,T,H] fp32, or [B,T,H,d_k] under GDR_DECAY_CHANNEL
- *   dbeta  [B,T,H] fp32 (required unless both ERASE and WRITE are set)
+ *   dbeta  [B,T,H] fp32 (required unless both ERASE and WRITE are set;
+ *          [B,T,H,d_v] under GDR_BETA_CHANNEL)
  *   dlam   [B,T,H] fp32 (GDR_QMIX)   db [B,T,H,d_k] fp32 (GDR_ERASE_CHANNEL)
  *   dw     [B,T,H,d_v] fp32 (GDR_WRITE_CHANNEL)
  *   dh0    [B,H,d_k,d_v] fp32, or NULL
@@ -299,7 +300,17 @@ gdr_status gdr_chunk_fwd_pipeline_segments(const gdr_shape* shape, int* segments
  * the gradient leaving every chunk. The workspace starts with
  * status words: a chunk whose running log-decay sum falls below -80 (the
  * range of 1 / gamma in fp32) is reported there as GDR_ERR_RANGE, read by
- * gdr_chunk_bwd_check. GDR_BETA_CHANNEL returns GDR_ERR_UNSUPPORTED.
+ * gdr_chunk_bwd_check.
+ *
+ * GDR_BETA_CHANNEL (the write strength per value channel; LLMs from scratch
+ * ch. 11, section 11.3) takes a token-order backward instead, the reverse of
+ * the recurrence token by token in fp32: the state entering every 64-token
+ * chunk is kept on a forward pass, and each chunk is re-run from it before it
+ * is walked backward. Its workspace (gdr_chunk_bwd_workspace) holds those
+ * states, 64 KB per (batch, head, chunk) at d_k = d_v = 128, and one chunk's
+ * states per (batch, head); it has no decay range limit. dq, dk and dg are
+ * sums over blocks of 32 value columns, added with atomics, so their last bits
+ * may differ between calls; every other output is deterministic.
  */
 gdr_status gdr_chunk_bwd_workspace(const gdr_shape* shape, size_t* bytes);
 gdr_status gdr_chunk_bwd(const gdr_shape* shape, const void* q, const void* k, const void* v,

@@ -153,3 +153,46 @@ def test_backward_decay_inside_its_range(variant):
     gdr.chunk_bwd(d["q"], d["k"], d["v"], d["g"], dO.cuda(), d["beta"], d["lam"], d["b"], d["w"],
                   d["h0"], dhT.cuda(), scale=x["scale"], flags=x["flags"], check=True)
     check(x, seed=8)
+
+
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16], ids=["f32", "bf16"])
+@pytest.mark.parametrize("dk,dv", [(64, 64), (128, 128), (64, 128), (128, 64)])
+def test_backward_write_strength_per_value_channel(dk, dv, dtype):
+    """GDR_BETA_CHANNEL (token-order backward): every gradient against float64
+    autograd through the token recurrence, over several chunks with a ragged
+    tail, from an initial state and with a final-state cotangent."""
+    x = wl.make_inputs("vbeta", 2, 64 * 2 + 9, 2, dk, dv, dtype, seed=500 + dk + dv, h0_std=0.05)
+    assert x["flags"] == gdr.BETA_CHANNEL and x["beta"].dim() == 4
+    dO, dhT = _cotangents(x, 50 + dk)
+    d = to_dev(x)
+    grads = gdr.chunk_bwd(d["q"], d["k"], d["v"], d["g"], dO.cuda(), d["beta"], None, None, None,
+                          d["h0"], dhT.cuda(), scale=x["scale"], flags=x["flags"], check=True)
+    torch.cuda.synchronize()
+    tol = TOL[dtype]
+    for b in range(2):
+        for h in range(2):
+            sel = lambda t: None if t is None else f64(t[b, :, h])
+            ref = obw.grad_autograd(*(sel(x[n]) for n in ("q", "k", "v", "g", "beta")),
+                                    S0=f64(x["h0"][b, h]), scale=x["scale"], flags=x["flags"],
+                                    dO=sel(dO), dST=f64(dhT[b, h]))
+            for n in ("q", "k", "v", "g", "beta"):
+                e = rel_err(grads[n][b, :, h].cpu(), ref[n])
+                assert e <= tol, (n, b, h, e)
+            assert rel_err(grads["h0"][b, h].cpu(), ref["S0"]) <= tol
+
+
+def test_backward_write_strength_without_states():
+    """No initial state and no final-state cotangent (both zero), one short chunk."""
+    x = wl.make_inputs("vbeta", 1, 23, 3, 128, 128, torch.float32, seed=77, h0_std=None)
+    dO, _ = _cotangents(x, 9)
+    d = to_dev(x)
+    grads = gdr.chunk_bwd(d["q"], d["k"], d["v"], d["g"], dO.cuda(), d["beta"], scale=x["scale"],
+                          flags=x["flags"])
+    torch.cuda.synchronize()
+    for h in range(3):
+        sel = lambda t: None if t is None else f64(t[0, :, h])
+        ref = obw.grad_autograd(*(sel(x[n]) for n in ("q", "k", "v", "g", "beta")), S0=None,
+                                scale=x["scale"], flags=x["flags"], dO=sel(dO), dST=None)
+        for n in ("q", "k", "v", "g", "beta"):
+            assert rel_err(grads[n][0, :, h].cpu(), ref[n]) <= TOL[torch.float32], n
+        assert rel_err(grads["h0"][0, h].cpu(), ref["S0"]) <= TOL[torch.float32]
