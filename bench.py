@@ -66,6 +66,8 @@ def parse():
                    help="skip the per-value-channel write strength measurement")
     p.add_argument("--no-split", action="store_true",
                    help="skip the sequence-split measurement")
+    p.add_argument("--no-graph", action="store_true",
+                   help="launch the decode steps one by one instead of replaying a CUDA graph")
     p.add_argument("--no-backward", action="store_true",
                    help="skip the backward measurement")
     p.add_argument("--pipeline", type=int, default=None,
@@ -323,6 +325,25 @@ def run_ours(args):
         prefill()
         decode()
     torch.cuda.synchronize()
+    # the decode phase's launches, recorded once into a CUDA graph and replayed
+    # every step (the same kernels, without one host launch per token)
+    graph = None
+    if dec_steps > 0 and not args.no_graph:
+        side = torch.cuda.Stream(dev)
+        side.wait_stream(stream)
+        with torch.cuda.stream(side):
+            decode()
+        stream.wait_stream(side)
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            decode()
+        torch.cuda.synchronize()
+
+    def decode_phase():
+        if graph is not None:
+            graph.replay()
+        else:
+            decode()
 
     K = args.steps
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
@@ -337,7 +358,7 @@ def run_ours(args):
         ev[i][0].record(stream)
         prefill()
         ev[i][1].record(stream)
-        decode()
+        decode_phase()
         ev[i][2].record(stream)
     torch.cuda.synchronize()
     clk = clocks.stop()
@@ -372,6 +393,8 @@ def run_ours(args):
                                                       "w")), o_dec[0]) + 2 * tensor_bytes(state))
         droof = roofline_obj(dbytes, 5.0 * dk * dv * N * H, per, pk, pk_kind)
         decode_info = {"kernel": "recurrent_step_kernel", "steps": dec_steps, "N": N, "H": H,
+                       "launch": ("one CUDA graph of the steps' launches, replayed"
+                                  if graph is not None else "one launch per step"),
                        "from": "random fp32 states" if y["h0"] is not None else
                                "the prefill's final state",
                        "ms_per_phase": round(statistics.mean(dec_ms), 4),

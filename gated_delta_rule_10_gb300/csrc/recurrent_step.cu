@@ -197,20 +197,49 @@ __global__ void __launch_bounds__(kStepThreads, 1) recurrent_step_kernel(const S
   if (tid == 0) tc::bulk_wait_all<0>();
 }
 
-template <int DK, int DV>
-cudaError_t launch_step(const StepArgs& a, bool f32, cudaStream_t stream) {
+// The kernel's shared-memory opt-in and the SM count, set and read once per
+// device and instance, so that a launch inside a CUDA graph capture makes no
+// other runtime call than the launch itself.
+constexpr int kMaxDevices = 64;
+
+template <int DK, int DV, typename TIn>
+cudaError_t launch_step_t(const StepArgs& a, cudaStream_t stream) {
   constexpr int kSmem = kStepStages * DK * DV * 4;
-  auto kern = f32 ? recurrent_step_kernel<DK, DV, float> : recurrent_step_kernel<DK, DV, __nv_bfloat16>;
-  cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
-  if (err != cudaSuccess) return err;
+  auto kern = recurrent_step_kernel<DK, DV, TIn>;
+  static int sms_of[kMaxDevices] = {};   // 0: not yet set up on that device
   int dev = 0, sms = 0;
-  if ((err = cudaGetDevice(&dev)) != cudaSuccess) return err;
-  if ((err = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
-    return err;
+  cudaError_t err = cudaGetDevice(&dev);
+  if (err != cudaSuccess) return err;
+  if (dev >= 0 && dev < kMaxDevices && sms_of[dev] > 0) {
+    sms = sms_of[dev];
+  } else {
+    if ((err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem)) !=
+            cudaSuccess ||
+        (err = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
+      return err;
+    if (dev >= 0 && dev < kMaxDevices) sms_of[dev] = sms;
+  }
   const long long items = static_cast<long long>(a.N) * a.H;
   const unsigned grid = static_cast<unsigned>(items < sms ? items : sms);   // one CTA per SM
   kern<<<grid, kStepThreads, kSmem, stream>>>(a);
-  return cudaGetLastError();
+  err = cudaGetLastError();
+  if (err == cudaErrorInvalidValue && dev >= 0 && dev < kMaxDevices && sms_of[dev] > 0) {
+    // the opt-in is gone (the device was reset since): set it up again, once
+    sms_of[dev] = 0;
+    if ((err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem)) !=
+        cudaSuccess)
+      return err;
+    sms_of[dev] = sms;
+    kern<<<grid, kStepThreads, kSmem, stream>>>(a);
+    err = cudaGetLastError();
+  }
+  return err;
+}
+
+template <int DK, int DV>
+cudaError_t launch_step(const StepArgs& a, bool f32, cudaStream_t stream) {
+  return f32 ? launch_step_t<DK, DV, float>(a, stream)
+             : launch_step_t<DK, DV, __nv_bfloat16>(a, stream);
 }
 
 }  // namespace
