@@ -76,6 +76,8 @@ def lib():
         L.gdr_chunk_bwd_check.argtypes = [_vp, _vp, ctypes.POINTER(ctypes.c_int)]
         L.gdr_chunk_bwd_workspace.argtypes = [sp, ctypes.POINTER(ctypes.c_size_t)]
         L.gdr_chunk_bwd.argtypes = [sp] + [_vp] * 20 + [_vp, ctypes.c_size_t, _vp]
+        L.gdr_token_bwd_workspace.argtypes = [sp, ctypes.POINTER(ctypes.c_size_t)]
+        L.gdr_token_bwd.argtypes = [sp] + [_vp] * 20 + [_vp, ctypes.c_size_t, _vp]
         L.gdr_rmsnorm_gate.argtypes = [ctypes.c_longlong, ctypes.c_int, ctypes.c_int, _vp, _vp,
                                        _vp, ctypes.c_float, _vp, _vp]
         L.gdr_token_fwd.argtypes = [sp] + [_vp] * 11 + [_vp]
@@ -93,7 +95,7 @@ def lib():
                      "gdr_chunk_fwd_pipelined", "gdr_chunk_fwd_workspace_pipelined",
                      "gdr_chunk_fwd_pipeline_segments", "gdr_recurrent_step",
                      "gdr_gate_cumsum", "gdr_chunk_fwd_check", "gdr_chunk_bwd_check", "gdr_rmsnorm_gate",
-                     "gdr_chunk_bwd_workspace", "gdr_chunk_bwd", "gdr_chunk_fwd_gated",
+                     "gdr_chunk_bwd_workspace", "gdr_chunk_bwd", "gdr_token_bwd_workspace", "gdr_token_bwd", "gdr_chunk_fwd_gated",
                      "gdr_chunk_fwd_gated_pipelined", "gdr_token_fwd"):
             getattr(L, name).restype = ctypes.c_int
         _lib = L
@@ -455,13 +457,9 @@ def chunk_bwd_check(workspace, stream=None):
     return None
 
 
-def chunk_bwd(q, k, v, g, dO, beta=None, lam=None, b=None, w=None, h0=None, dhT=None, *,
-              scale=None, flags=None, workspace=None, stream=None, check=False):
-    """Gradients of <dO, o> + <dhT, hT> for ``chunk_fwd`` on the same inputs
-    (``gdr_chunk_bwd``). Returns a dict of fp32 tensors: q, k, v, g, and beta,
-    lam, b, w, h0 where they apply (None otherwise). With check=True the call
-    synchronises and raises GdrError(GDR_ERR_RANGE) for inputs past the
-    backward's decay range (chunk_bwd_check)."""
+def _bwd(token, q, k, v, g, dO, beta=None, lam=None, b=None, w=None, h0=None, dhT=None, *,
+         scale=None, flags=None, workspace=None, stream=None, check=False):
+    """Shared body of chunk_bwd and token_bwd."""
     B, T, H, dk = q.shape
     dv = v.shape[-1]
     dev, dt = q.device, q.dtype
@@ -481,9 +479,11 @@ def chunk_bwd(q, k, v, g, dO, beta=None, lam=None, b=None, w=None, h0=None, dhT=
            "h0": torch.empty(B, H, dk, dv, **f32)}
     shape = make_shape(B, T, H, dk, dv, dt, flags, scale)
     if workspace is None:
-        workspace = torch.empty(chunk_bwd_workspace_bytes(shape), dtype=torch.uint8, device=dev)
+        nbytes = (token_bwd_workspace_bytes if token else chunk_bwd_workspace_bytes)(shape)
+        workspace = torch.empty(nbytes, dtype=torch.uint8, device=dev)
     with torch.cuda.device(dev):
-        st = lib().gdr_chunk_bwd(ctypes.byref(shape), _ptr(q), _ptr(k), _ptr(v), _ptr(g),
+        fn = lib().gdr_token_bwd if token else lib().gdr_chunk_bwd
+        st = fn(ctypes.byref(shape), _ptr(q), _ptr(k), _ptr(v), _ptr(g),
                                  _ptr(beta), _ptr(lam), _ptr(b), _ptr(w), _ptr(h0), _ptr(dO),
                                  _ptr(dhT), *(_ptr(out[n]) for n in
                                               ("q", "k", "v", "g", "beta", "lam", "b", "w",
@@ -491,7 +491,35 @@ def chunk_bwd(q, k, v, g, dO, beta=None, lam=None, b=None, w=None, h0=None, dhT=
                                  _ptr(workspace), ctypes.c_size_t(workspace.numel()),
                                  _stream(stream, dev))
     if st:
-        raise GdrError(st, "gdr_chunk_bwd")
+        raise GdrError(st, "gdr_token_bwd" if token else "gdr_chunk_bwd")
     if check:
         chunk_bwd_check(workspace, stream)
     return out
+
+
+def chunk_bwd(q, k, v, g, dO, beta=None, lam=None, b=None, w=None, h0=None, dhT=None, *,
+              scale=None, flags=None, workspace=None, stream=None, check=False):
+    """Gradients of <dO, o> + <dhT, hT> for ``chunk_fwd`` on the same inputs
+    (``gdr_chunk_bwd``). Returns a dict of fp32 tensors: q, k, v, g, and beta,
+    lam, b, w, h0 where they apply (None otherwise). With check=True the call
+    synchronises and raises GdrError(GDR_ERR_RANGE) for inputs past the
+    backward's decay range (chunk_bwd_check)."""
+    return _bwd(False, q, k, v, g, dO, beta, lam, b, w, h0, dhT, scale=scale, flags=flags,
+                workspace=workspace, stream=stream, check=check)
+
+
+def token_bwd_workspace_bytes(shape):
+    n = ctypes.c_size_t(0)
+    st = lib().gdr_token_bwd_workspace(ctypes.byref(shape), ctypes.byref(n))
+    if st:
+        raise GdrError(st, "gdr_token_bwd_workspace")
+    return n.value
+
+
+def token_bwd(q, k, v, g, dO, beta=None, lam=None, b=None, w=None, h0=None, dhT=None, *,
+              scale=None, flags=None, workspace=None, stream=None):
+    """chunk_bwd's gradients walked token by token (``gdr_token_bwd``): no decay
+    range limit, for inputs chunk_bwd reports as GDR_ERR_RANGE. Same arguments
+    and result."""
+    return _bwd(True, q, k, v, g, dO, beta, lam, b, w, h0, dhT, scale=scale, flags=flags,
+                workspace=workspace, stream=stream)

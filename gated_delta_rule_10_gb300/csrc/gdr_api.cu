@@ -612,7 +612,7 @@ gdr_status gdr_chunk_bwd_workspace(const gdr_shape* shape, size_t* bytes) {
   return GDR_OK;
 }
 
-gdr_status gdr_chunk_bwd(const gdr_shape* shape, const void* q, const void* k, const void* v,
+static gdr_status bwd_impl(bool token, const gdr_shape* shape, const void* q, const void* k, const void* v,
                          const float* g, const float* beta, const float* lam, const void* b,
                          const void* w, const float* h0, const void* dO, const float* dhT,
                          float* dq, float* dk, float* dv, float* dg, float* dbeta, float* dlam,
@@ -635,7 +635,11 @@ gdr_status gdr_chunk_bwd(const gdr_shape* shape, const void* q, const void* k, c
                           static_cast<const void*>(dh0)})
     if (ptr && !aligned(ptr, 4)) return GDR_ERR_INVALID_ARG;
   size_t need = 0;
-  gdr_chunk_bwd_workspace(shape, &need);
+  if (token) {
+    gdr_token_bwd_workspace(shape, &need);
+  } else {
+    gdr_chunk_bwd_workspace(shape, &need);
+  }
   if (!workspace || ws_bytes < need || !aligned(workspace, 16)) return GDR_ERR_WORKSPACE;
   if (f & GDR_BETA_CHANNEL) {
     // the write strength per value channel: the token-order backward with
@@ -658,9 +662,47 @@ gdr_status gdr_chunk_bwd(const gdr_shape* shape, const void* q, const void* k, c
   a.dlam = dlam; a.db = db; a.dw = dw; a.dh0 = dh0; a.workspace = workspace;
   a.B = shape->B; a.T = shape->T; a.H = shape->H; a.dk_dim = shape->dk; a.dv_dim = shape->dv;
   a.flags = f; a.scale = shape->scale;
-  const cudaError_t err = gdr::launch_chunk_bwd(a, shape->dtype == GDR_F32,
-                                                reinterpret_cast<cudaStream_t>(stream));
+  const cudaStream_t st_ = reinterpret_cast<cudaStream_t>(stream);
+  cudaError_t err;
+  if (token) {   // the token-order backward: no range limit, the status words stay clear
+    err = cudaMemsetAsync(workspace, 0, gdr::kStatusWords * sizeof(int), st_);
+    if (err == cudaSuccess) err = gdr::launch_token_bwd(a, shape->dtype == GDR_F32, st_);
+  } else {
+    err = gdr::launch_chunk_bwd(a, shape->dtype == GDR_F32, st_);
+  }
   return err == cudaSuccess ? GDR_OK : GDR_ERR_CUDA;
+}
+
+gdr_status gdr_chunk_bwd(const gdr_shape* shape, const void* q, const void* k, const void* v,
+                         const float* g, const float* beta, const float* lam, const void* b,
+                         const void* w, const float* h0, const void* dO, const float* dhT,
+                         float* dq, float* dk, float* dv, float* dg, float* dbeta, float* dlam,
+                         float* db, float* dw, float* dh0, void* workspace, size_t ws_bytes,
+                         gdr_stream_t stream) {
+  return bwd_impl(false, shape, q, k, v, g, beta, lam, b, w, h0, dO, dhT, dq, dk, dv, dg, dbeta,
+                  dlam, db, dw, dh0, workspace, ws_bytes, stream);
+}
+
+gdr_status gdr_token_bwd_workspace(const gdr_shape* shape, size_t* bytes) {
+  if (!bytes) return GDR_ERR_INVALID_ARG;
+  const gdr_status st = check_shape(shape, false);
+  if (st != GDR_OK) return st;
+  *bytes = (shape->flags & GDR_BETA_CHANNEL)
+               ? gdr::value_beta_bwd_workspace_bytes(shape->B, shape->T, shape->H, shape->dk,
+                                                     shape->dv)
+               : gdr::token_bwd_workspace_bytes(shape->B, shape->T, shape->H, shape->dk,
+                                                shape->dv);
+  return GDR_OK;
+}
+
+gdr_status gdr_token_bwd(const gdr_shape* shape, const void* q, const void* k, const void* v,
+                         const float* g, const float* beta, const float* lam, const void* b,
+                         const void* w, const float* h0, const void* dO, const float* dhT,
+                         float* dq, float* dk, float* dv, float* dg, float* dbeta, float* dlam,
+                         float* db, float* dw, float* dh0, void* workspace, size_t ws_bytes,
+                         gdr_stream_t stream) {
+  return bwd_impl(true, shape, q, k, v, g, beta, lam, b, w, h0, dO, dhT, dq, dk, dv, dg, dbeta,
+                  dlam, db, dw, dh0, workspace, ws_bytes, stream);
 }
 
 gdr_status gdr_chunk_fwd_check(const void* workspace, gdr_stream_t stream, int* detail) {

@@ -152,6 +152,12 @@ struct ChunkBwdArgs {
 };
 size_t chunk_bwd_workspace_bytes(int B, int T, int H, int dk, int dv);
 cudaError_t launch_chunk_bwd(const ChunkBwdArgs& a, bool f32, cudaStream_t stream);
+// The same gradients walked token by token (every flag but 16; no decay
+// factoring, so no range limit): token_bwd_workspace_bytes of workspace,
+// d_v a multiple of 16; dq, dk, dg, db, dbeta and dlam are summed with atomics
+// into outputs the launch zeroes first.
+size_t token_bwd_workspace_bytes(int B, int T, int H, int dk, int dv);
+cudaError_t launch_token_bwd(const ChunkBwdArgs& a, bool f32, cudaStream_t stream);
 
 // Token-order scan for every flag but 16 (no decay factoring: the path past the
 // chunked path's channel-decay range); o and hT as in the chunked forward.

@@ -84,7 +84,7 @@
  *    scalar decay) must stay above -80, since the backward's records hold
  *    k / e^{G}. A chunk past it makes gdr_chunk_bwd_check return
  *    GDR_ERR_RANGE (detail as above) and the gradients are not to be used;
- *    there is no backward without the limit.
+ *    gdr_token_bwd computes them without the limit.
  */
 #ifndef GDR_H_
 #define GDR_H_
@@ -332,6 +332,30 @@ gdr_status gdr_chunk_bwd(const gdr_shape* shape, const void* q, const void* k, c
  */
 gdr_status gdr_chunk_fwd_check(const void* workspace, gdr_stream_t stream,
                                int* detail);
+
+/*
+ * gdr_chunk_bwd's gradients walked token by token (the reverse of the
+ * recurrence in fp32, no decay factoring): the backward for inputs past the
+ * chunk backward's decay range (gdr_chunk_bwd_check returning GDR_ERR_RANGE),
+ * the counterpart of gdr_token_fwd. Arguments, outputs and rules as
+ * gdr_chunk_bwd; GDR_BETA_CHANNEL takes the same token-order backward as
+ * there. A forward pass keeps the state entering every 64-token chunk, and
+ * each chunk is re-run from it before it is walked backward; one CTA per
+ * (batch, head, 16 value columns), sequential in the tokens, so it is much
+ * slower than gdr_chunk_bwd on long sequences. dq, dk, dg, db, dbeta and dlam
+ * are sums over the column blocks added with atomics (their last bits may
+ * differ between calls); dv, dw and dh0 are deterministic. workspace: at least
+ * gdr_token_bwd_workspace() bytes, 16-byte aligned (status words, then the
+ * chunk-start states: 64 KB per (batch, head, chunk) at d_k = d_v = 128, and
+ * one chunk's states per (batch, head)).
+ */
+gdr_status gdr_token_bwd_workspace(const gdr_shape* shape, size_t* bytes);
+gdr_status gdr_token_bwd(const gdr_shape* shape, const void* q, const void* k, const void* v,
+                         const float* g, const float* beta, const float* lam, const void* b,
+                         const void* w, const float* h0, const void* dO, const float* dhT,
+                         float* dq, float* dk, float* dv, float* dg, float* dbeta, float* dlam,
+                         float* db, float* dw, float* dh0, void* workspace, size_t ws_bytes,
+                         gdr_stream_t stream);
 
 /*
  * The same for a gdr_chunk_bwd call's workspace: GDR_OK, or GDR_ERR_RANGE

@@ -196,3 +196,61 @@ def test_backward_write_strength_without_states():
         for n in ("q", "k", "v", "g", "beta"):
             assert rel_err(grads[n][0, :, h].cpu(), ref[n]) <= TOL[torch.float32], n
         assert rel_err(grads["h0"][0, h].cpu(), ref["S0"]) <= TOL[torch.float32]
+
+
+def _token_bwd_check(x, seed, seqs=None):
+    dO, dhT = _cotangents(x, seed)
+    d = to_dev(x)
+    grads = gdr.token_bwd(d["q"], d["k"], d["v"], d["g"], dO.cuda(), d["beta"], d["lam"], d["b"],
+                          d["w"], d["h0"], dhT.cuda(), scale=x["scale"], flags=x["flags"])
+    torch.cuda.synchronize()
+    B, H = x["q"].shape[0], x["q"].shape[2]
+    tol = TOL[x["q"].dtype]
+    for b, h in (seqs or [(bb, hh) for bb in range(B) for hh in range(H)]):
+        sel = lambda t: None if t is None else f64(t[b, :, h])
+        S0 = None if x["h0"] is None else f64(x["h0"][b, h])
+        ref = obw.grad_autograd(*(sel(x[n]) for n in NAMES), S0=S0, scale=x["scale"],
+                                flags=x["flags"], dO=sel(dO), dST=f64(dhT[b, h]))
+        for n in NAMES:
+            if x[n] is None:
+                continue
+            e = rel_err(grads[n][b, :, h].cpu(), ref[n])
+            assert e <= tol, (n, b, h, e)
+        assert rel_err(grads["h0"][b, h].cpu(), ref["S0"]) <= tol, ("h0", b, h)
+
+
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16], ids=["f32", "bf16"])
+@pytest.mark.parametrize("flags", range(17))
+def test_token_backward_every_flag(flags, dtype):
+    """gdr_token_bwd (the recurrence reversed token by token) against float64
+    autograd, every flag combination (16: the per-value-channel write strength)."""
+    x = wl.make_inputs(flags, 2, 64 * 2 + 9, 2, 128, 128, dtype, seed=700 + flags, h0_std=0.05)
+    _token_bwd_check(x, 70 + flags)
+
+
+@pytest.mark.parametrize("dk,dv", [(64, 64), (64, 128), (128, 64)])
+@pytest.mark.parametrize("flags", [0, 7, 15])
+def test_token_backward_widths(flags, dk, dv):
+    x = wl.make_inputs(flags, 1, 64 + 23, 3, dk, dv, torch.float32, seed=800 + flags + dk + dv,
+                       h0_std=0.05)
+    _token_bwd_check(x, 90 + flags)
+
+
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16], ids=["f32", "bf16"])
+@pytest.mark.parametrize("variant", ["kda", "gdn2"])
+def test_backward_channel_decay_minus_300_per_chunk(variant, dtype):
+    """Per-channel in-chunk log-decay sums of -300: the chunk backward reports
+    GDR_ERR_RANGE for them, and the token-order backward keeps the bar against
+    float64 autograd."""
+    x = wl.make_inputs(variant, 1, 64 * 2 + 5, 2, 128, 128, dtype, seed=41, h0_std=0.1)
+    g = -300.0 / 64 * torch.ones_like(x["g"])
+    g[..., 1::3] = -0.02                      # some channels keep their memory
+    x["g"] = g.contiguous()
+    dO, dhT = _cotangents(x, 42)
+    d = to_dev(x)
+    with pytest.raises(gdr.GdrError) as e:
+        gdr.chunk_bwd(d["q"], d["k"], d["v"], d["g"], dO.cuda(), d["beta"], d["lam"], d["b"],
+                      d["w"], d["h0"], dhT.cuda(), scale=x["scale"], flags=x["flags"],
+                      check=True)
+    assert e.value.code == 6
+    _token_bwd_check(x, 42)
