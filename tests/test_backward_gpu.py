@@ -254,3 +254,10 @@ def test_backward_channel_decay_minus_300_per_chunk(variant, dtype):
                       check=True)
     assert e.value.code == 6
     _token_bwd_check(x, 42)
+
+
+@pytest.mark.parametrize("flags", [0, 7, 16])
+def test_token_backward_single_token(flags):
+    """T = 1: one chunk of one token (the checkpoint is the initial state)."""
+    x = wl.make_inputs(flags, 2, 1, 2, 128, 128, torch.float32, seed=900 + flags, h0_std=0.05)
+    _token_bwd_check(x, 95 + flags)

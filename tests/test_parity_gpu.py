@@ -407,3 +407,24 @@ def test_calls_on_two_streams():
         ro, rh = oracle_forward(x)
         assert rel_err(o.float().cpu(), ro) <= TOL[torch.bfloat16]
         assert rel_err(hT.cpu(), rh) <= TOL[torch.bfloat16]
+
+
+@pytest.mark.parametrize("N,H", [(1, 1), (153, 1), (19, 16)])
+def test_recurrent_step_item_counts(N, H):
+    """The decode stream with one item, with one item more than the SMs (one CTA
+    takes two), and with several items per CTA: every output and state against
+    the oracle over a few steps."""
+    flags, dk, dv, dtype, steps = 7, 128, 128, torch.bfloat16, 3
+    gen = torch.Generator().manual_seed(N * 31 + H)
+    h0 = torch.randn(N, H, dk, dv, generator=gen) * 0.05
+    state = h0.cuda()
+    ys = [_step_inputs(flags, N, H, dk, dv, dtype, seed=5000 + 10 * N + s) for s in range(steps)]
+    outs = [_gpu_step(y, state) for y in ys]
+    torch.cuda.synchronize()
+    cat = {n: (torch.cat([y[n] for y in ys], dim=1) if ys[0][n] is not None else None)
+           for n in ("q", "k", "v", "g", "beta", "lam", "b", "w")}
+    cat.update(h0=h0, scale=ys[0]["scale"], flags=flags)
+    ro, rh = oracle_forward(cat)
+    got = torch.stack([o.float().cpu() for o in outs], dim=1)
+    tol = TOL[dtype]
+    assert rel_err(got, ro) <= tol and rel_err(state.cpu(), rh) <= tol
