@@ -44,6 +44,50 @@ constexpr int kTbChunk = 64;
 __device__ __forceinline__ float to_f(float x) { return x; }
 __device__ __forceinline__ float to_f(__nv_bfloat16 x) { return __bfloat162float(x); }
 
+// N consecutive elements from p (aligned to their size in bytes) as floats, by
+// 16- or 8-byte loads
+template <int N>
+__device__ __forceinline__ void load_run(const float* p, float (&x)[N]) {
+  static_assert(N % 4 == 0, "float4 loads");
+#pragma unroll
+  for (int i = 0; i < N; i += 4) {
+    const float4 f = *reinterpret_cast<const float4*>(p + i);
+    x[i] = f.x; x[i + 1] = f.y; x[i + 2] = f.z; x[i + 3] = f.w;
+  }
+}
+template <int N>
+__device__ __forceinline__ void load_run(const __nv_bfloat16* p, float (&x)[N]) {
+  static_assert(N % 4 == 0, "8-byte loads at least");
+  if constexpr (N % 8 == 0) {
+#pragma unroll
+    for (int i = 0; i < N; i += 8) {
+      const uint4 u = *reinterpret_cast<const uint4*>(p + i);
+      const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        x[i + 2 * j] = __uint_as_float(w[j] << 16);
+        x[i + 2 * j + 1] = __uint_as_float(w[j] & 0xffff0000u);
+      }
+    }
+  } else {
+#pragma unroll
+    for (int i = 0; i < N; i += 4) {
+      const uint2 u = *reinterpret_cast<const uint2*>(p + i);
+      x[i] = __uint_as_float(u.x << 16);
+      x[i + 1] = __uint_as_float(u.x & 0xffff0000u);
+      x[i + 2] = __uint_as_float(u.y << 16);
+      x[i + 3] = __uint_as_float(u.y & 0xffff0000u);
+    }
+  }
+}
+// two consecutive elements (an aligned pair)
+__device__ __forceinline__ float2 load_pair(const float* p) {
+  return *reinterpret_cast<const float2*>(p);
+}
+__device__ __forceinline__ float2 load_pair(const __nv_bfloat16* p) {
+  return __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(p));
+}
+
 template <int R>
 struct TbToken {
   float k[R], q[R], b[R], g[R];
@@ -80,19 +124,26 @@ __global__ void __launch_bounds__(kTbThreads)
 
   auto fetch = [&](int t, TbToken<R>& x) {
     const size_t tk = (static_cast<size_t>(bb) * T + t) * H + h;
+    static_assert(kTbCL == 2, "column pairs");
+    load_run<R>(kg + tk * DK + r0, x.k);
+    load_run<R>(qg + tk * DK + r0, x.q);
+    if (ER) {
+      load_run<R>(bg + tk * DK + r0, x.b);
+    } else {
 #pragma unroll
-    for (int i = 0; i < R; ++i) {
-      x.k[i] = to_f(kg[tk * DK + r0 + i]);
-      x.q[i] = to_f(qg[tk * DK + r0 + i]);
-      x.b[i] = ER ? to_f(bg[tk * DK + r0 + i]) : 0.f;
-      x.g[i] = CH ? a.g[tk * DK + r0 + i] : 0.f;
+      for (int i = 0; i < R; ++i) x.b[i] = 0.f;
     }
+    if (CH) {
+      load_run<R>(a.g + tk * DK + r0, x.g);
+    } else {
 #pragma unroll
-    for (int c = 0; c < kTbCL; ++c) {
-      x.v[c] = to_f(vg[tk * DV + c0 + c]);
-      x.w[c] = WR ? to_f(wg[tk * DV + c0 + c]) : 0.f;
-      x.dO[c] = to_f(dOg[tk * DV + c0 + c]);
+      for (int i = 0; i < R; ++i) x.g[i] = 0.f;
     }
+    const float2 v2 = load_pair(vg + tk * DV + c0), o2 = load_pair(dOg + tk * DV + c0);
+    const float2 w2 = WR ? load_pair(wg + tk * DV + c0) : make_float2(0.f, 0.f);
+    x.v[0] = v2.x; x.v[1] = v2.y;
+    x.w[0] = w2.x; x.w[1] = w2.y;
+    x.dO[0] = o2.x; x.dO[1] = o2.y;
     x.gs = CH ? 0.f : a.g[tk];
     x.beta = use_beta ? a.beta[tk] : 0.f;
     x.lam = QM ? a.lam[tk] : 0.f;

@@ -42,6 +42,50 @@ constexpr int kVbChunk = 64;              // tokens between checkpoints
 __device__ __forceinline__ float to_f(float x) { return x; }
 __device__ __forceinline__ float to_f(__nv_bfloat16 x) { return __bfloat162float(x); }
 
+// N consecutive elements from p (aligned to their size in bytes) as floats, by
+// 16- or 8-byte loads
+template <int N>
+__device__ __forceinline__ void load_run(const float* p, float (&x)[N]) {
+  static_assert(N % 4 == 0, "float4 loads");
+#pragma unroll
+  for (int i = 0; i < N; i += 4) {
+    const float4 f = *reinterpret_cast<const float4*>(p + i);
+    x[i] = f.x; x[i + 1] = f.y; x[i + 2] = f.z; x[i + 3] = f.w;
+  }
+}
+template <int N>
+__device__ __forceinline__ void load_run(const __nv_bfloat16* p, float (&x)[N]) {
+  static_assert(N % 4 == 0, "8-byte loads at least");
+  if constexpr (N % 8 == 0) {
+#pragma unroll
+    for (int i = 0; i < N; i += 8) {
+      const uint4 u = *reinterpret_cast<const uint4*>(p + i);
+      const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        x[i + 2 * j] = __uint_as_float(w[j] << 16);
+        x[i + 2 * j + 1] = __uint_as_float(w[j] & 0xffff0000u);
+      }
+    }
+  } else {
+#pragma unroll
+    for (int i = 0; i < N; i += 4) {
+      const uint2 u = *reinterpret_cast<const uint2*>(p + i);
+      x[i] = __uint_as_float(u.x << 16);
+      x[i + 1] = __uint_as_float(u.x & 0xffff0000u);
+      x[i + 2] = __uint_as_float(u.y << 16);
+      x[i + 3] = __uint_as_float(u.y & 0xffff0000u);
+    }
+  }
+}
+// two consecutive elements (an aligned pair)
+__device__ __forceinline__ float2 load_pair(const float* p) {
+  return *reinterpret_cast<const float2*>(p);
+}
+__device__ __forceinline__ float2 load_pair(const __nv_bfloat16* p) {
+  return __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(p));
+}
+
 template <int R>
 struct VbToken {
   float k[R], q[R];
@@ -74,17 +118,14 @@ __global__ void __launch_bounds__(kVbThreads)
 
   auto fetch = [&](int t, VbToken<R>& x) {
     const size_t tk = (static_cast<size_t>(bb) * T + t) * H + h;
-#pragma unroll
-    for (int i = 0; i < R; ++i) {
-      x.k[i] = to_f(kg[tk * DK + r0 + i]);
-      x.q[i] = to_f(qg[tk * DK + r0 + i]);
-    }
-#pragma unroll
-    for (int c = 0; c < kVbCL; ++c) {
-      x.v[c] = to_f(vg[tk * DV + c0 + c]);
-      x.be[c] = a.beta[tk * DV + c0 + c];
-      x.dO[c] = to_f(dOg[tk * DV + c0 + c]);
-    }
+    static_assert(kVbCL == 2, "column pairs");
+    load_run<R>(kg + tk * DK + r0, x.k);
+    load_run<R>(qg + tk * DK + r0, x.q);
+    const float2 v2 = load_pair(vg + tk * DV + c0), b2 = load_pair(a.beta + tk * DV + c0),
+                 o2 = load_pair(dOg + tk * DV + c0);
+    x.v[0] = v2.x; x.v[1] = v2.y;
+    x.be[0] = b2.x; x.be[1] = b2.y;
+    x.dO[0] = o2.x; x.dO[1] = o2.y;
     x.al = expf(a.g[tk]);
   };
   auto group_sum = [&](float x) {
