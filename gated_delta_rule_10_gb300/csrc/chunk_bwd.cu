@@ -19,9 +19,10 @@
 //      notes' adjoint of the triangular inverse dT = -tril(A^T dA A^T, -1), then
 //      the chain through the decay factors, the cumulative sum and the erase /
 //      write vectors to the inputs.
-// The per-chunk kernels run their products on the tensor cores (warp-level MMA
-// with every fp32 operand split into tf32 hi + lo, about fp32 accuracy), their
-// operands staged through shared memory a 32-wide K slice at a time; the state
+// The per-chunk kernels run their products on the tensor cores (warp-level MMA;
+// for fp32 inputs every fp32 operand is split into tf32 hi + lo, about fp32
+// accuracy; for bf16 inputs one tf32 product), their operands staged through
+// shared memory a 32-wide K slice at a time; the state
 // passes keep the state in MMA accumulators and multiply on warp-level MMAs
 // with bf16 hi + lo split operands, the next chunk's operands copied in while
 // the current one is used. Chunks
@@ -93,12 +94,16 @@ __device__ __forceinline__ void mma_tf32(float (&d)[4], const uint32_t (&a)[4], 
 // next slice in flight while the current one is used. Each operand keeps its
 // global layout in shared memory: AK / BK say that A / B is contiguous along k
 // (else along m / n); every base, stride and offset is a multiple of 4 floats.
-// The products run on the tensor cores with each fp32 operand split into tf32
-// hi + lo and the three products lo*hi + hi*lo + hi*hi accumulated in fp32,
-// which keeps about fp32 accuracy (the dropped lo*lo term is ~2^-22 relative).
+// The products run on the tensor cores. With NP = 3 each fp32 operand is split
+// into tf32 hi + lo and the three products lo*hi + hi*lo + hi*hi are accumulated
+// in fp32, which keeps about fp32 accuracy (the dropped lo*lo term is ~2^-22
+// relative); with NP = 1 the operands are rounded to tf32 (2^-11 relative) and
+// hi*hi alone is accumulated.
 // mask: 0 none, 1 keep n <= m, 2 keep n < m (others written as 0).
-template <int TN, bool AK, bool BK>
-__device__ void gemm64_t(float* C, int ldc, const float* A, int sam, int sak, const float* B,
+// Kept out of line: one body per layout instead of one per call site keeps the
+// per-chunk kernels' code small enough for the instruction cache.
+template <int NP, int TN, bool AK, bool BK>
+__device__ __noinline__ void gemm64_t(float* C, int ldc, const float* A, int sam, int sak, const float* B,
                          int sbk, int sbn, int K, float alpha, float beta, int mask,
                          float* sbuf) {
   constexpr int M = 64, N = 16 * TN;
@@ -159,26 +164,36 @@ __device__ void gemm64_t(float* C, int ldc, const float* A, int sam, int sak, co
     for (int k8 = 0; k8 < kKT; k8 += 8) {
       // fragments: A rows g, g + 8 and columns t, t + 4; B rows t, t + 4 and column g
       uint32_t ah[WM][4], al[WM][4], bh[WN][2], bl[WN][2];
+      auto split = [](float x, uint32_t& hi, uint32_t& lo) {
+        if constexpr (NP == 3) {
+          split_tf32(x, hi, lo);
+        } else {
+          hi = tf32_rna(x);
+          lo = 0u;
+        }
+      };
 #pragma unroll
       for (int i = 0; i < WM; ++i) {
         const int r = m0 + 16 * i + g, k = k8 + t;
-        split_tf32(a_at(r, k), ah[i][0], al[i][0]);
-        split_tf32(a_at(r + 8, k), ah[i][1], al[i][1]);
-        split_tf32(a_at(r, k + 4), ah[i][2], al[i][2]);
-        split_tf32(a_at(r + 8, k + 4), ah[i][3], al[i][3]);
+        split(a_at(r, k), ah[i][0], al[i][0]);
+        split(a_at(r + 8, k), ah[i][1], al[i][1]);
+        split(a_at(r, k + 4), ah[i][2], al[i][2]);
+        split(a_at(r + 8, k + 4), ah[i][3], al[i][3]);
       }
 #pragma unroll
       for (int j = 0; j < WN; ++j) {
         const int n = n0 + 8 * j + g, k = k8 + t;
-        split_tf32(b_at(k, n), bh[j][0], bl[j][0]);
-        split_tf32(b_at(k + 4, n), bh[j][1], bl[j][1]);
+        split(b_at(k, n), bh[j][0], bl[j][0]);
+        split(b_at(k + 4, n), bh[j][1], bl[j][1]);
       }
 #pragma unroll
       for (int i = 0; i < WM; ++i)
 #pragma unroll
         for (int j = 0; j < WN; ++j) {
-          mma_tf32(acc[i][j], al[i], bh[j][0], bh[j][1]);
-          mma_tf32(acc[i][j], ah[i], bl[j][0], bl[j][1]);
+          if constexpr (NP == 3) {
+            mma_tf32(acc[i][j], al[i], bh[j][0], bh[j][1]);
+            mma_tf32(acc[i][j], ah[i], bl[j][0], bl[j][1]);
+          }
           mma_tf32(acc[i][j], ah[i], bh[j][0], bh[j][1]);
         }
     }
@@ -206,27 +221,36 @@ __device__ void gemm64_t(float* C, int ldc, const float* A, int sam, int sak, co
   __syncthreads();
 }
 
-template <int TN>
+template <int NP, int TN>
 __device__ void gemm64_n(float* C, int ldc, const float* A, int sam, int sak, const float* B,
                          int sbk, int sbn, int K, float alpha, float beta, int mask, float* sbuf) {
   if (sak == 1) {
-    if (sbk == 1) gemm64_t<TN, true, true>(C, ldc, A, sam, sak, B, sbk, sbn, K, alpha, beta, mask, sbuf);
-    else gemm64_t<TN, true, false>(C, ldc, A, sam, sak, B, sbk, sbn, K, alpha, beta, mask, sbuf);
+    if (sbk == 1) gemm64_t<NP, TN, true, true>(C, ldc, A, sam, sak, B, sbk, sbn, K, alpha, beta, mask, sbuf);
+    else gemm64_t<NP, TN, true, false>(C, ldc, A, sam, sak, B, sbk, sbn, K, alpha, beta, mask, sbuf);
   } else {
-    if (sbk == 1) gemm64_t<TN, false, true>(C, ldc, A, sam, sak, B, sbk, sbn, K, alpha, beta, mask, sbuf);
-    else gemm64_t<TN, false, false>(C, ldc, A, sam, sak, B, sbk, sbn, K, alpha, beta, mask, sbuf);
+    if (sbk == 1) gemm64_t<NP, TN, false, true>(C, ldc, A, sam, sak, B, sbk, sbn, K, alpha, beta, mask, sbuf);
+    else gemm64_t<NP, TN, false, false>(C, ldc, A, sam, sak, B, sbk, sbn, K, alpha, beta, mask, sbuf);
   }
 }
 
 // M = 64 products with N = 64 or 128 (the only shapes of the chunk algebra).
+template <int NP>
 __device__ void gemm64(float* C, int ldc, const float* A, int sam, int sak, const float* B,
                        int sbk, int sbn, int N, int K, float alpha, float beta, float* sbuf,
                        int mask = 0) {
   if (N == 128)
-    gemm64_n<8>(C, ldc, A, sam, sak, B, sbk, sbn, K, alpha, beta, mask, sbuf);
+    gemm64_n<NP, 8>(C, ldc, A, sam, sak, B, sbk, sbn, K, alpha, beta, mask, sbuf);
   else
-    gemm64_n<4>(C, ldc, A, sam, sak, B, sbk, sbn, K, alpha, beta, mask, sbuf);
+    gemm64_n<NP, 4>(C, ldc, A, sam, sak, B, sbk, sbn, K, alpha, beta, mask, sbuf);
 }
+
+// tf32 products per product of the per-chunk kernels: three (split operands,
+// about fp32 accuracy) for fp32 inputs; one for bf16 inputs, whose 2^-8
+// rounding already bounds the result's accuracy well above tf32's 2^-11
+template <typename T>
+constexpr int kProducts = 3;
+template <>
+constexpr int kProducts<__nv_bfloat16> = 1;
 
 // two stages of the largest slices: A [64][36] (or [kKT][72]), B [128][36] (or [kKT][136])
 constexpr size_t kGemmSmem = static_cast<size_t>(2) * (64 * 36 + 128 * 36) * sizeof(float);
@@ -287,6 +311,7 @@ __device__ __forceinline__ size_t chunk_id(const BwdPtrs& p, int bb, int h, int 
 // ---------------------------------------------------------------- 1. records
 template <typename T>
 __global__ void __launch_bounds__(kBwdThreads, 3) bwd_chunk_prep(const BwdPtrs p) {
+  constexpr int kNP = kProducts<T>;
   const Rec R{p.dk, p.dv};
   const int cid = blockIdx.x;
   const int n = cid % p.Nc, bh = cid / p.Nc, h = bh % p.H, bb = bh / p.H;
@@ -394,8 +419,8 @@ __global__ void __launch_bounds__(kBwdThreads, 3) bwd_chunk_prep(const BwdPtrs p
   }
   __syncthreads();
   // T = tril(E_bar K_bar^T, -1), A_qk = tril(Q_gamma K_bar^T, 0)
-  gemm64(r + R.oT(), kC, r + R.oEb(), dk, 1, r + R.oKb(), 1, dk, kC, dk, 1.f, 0.f, sg, 2);
-  gemm64(r + R.oAqk(), kC, r + R.oQg(), dk, 1, r + R.oKb(), 1, dk, kC, dk, 1.f, 0.f, sg, 1);
+  gemm64<kNP>(r + R.oT(), kC, r + R.oEb(), dk, 1, r + R.oKb(), 1, dk, kC, dk, 1.f, 0.f, sg, 2);
+  gemm64<kNP>(r + R.oAqk(), kC, r + R.oQg(), dk, 1, r + R.oKb(), 1, dk, kC, dk, 1.f, 0.f, sg, 1);
   // A = (I + T)^{-1}: row i of (I + T) A = I gives A_i = e_i - sum_{j<i} T_ij A_j.
   // T and A sit in shared memory; thread c owns column c (two accumulators).
   {
@@ -426,8 +451,8 @@ __global__ void __launch_bounds__(kBwdThreads, 3) bwd_chunk_prep(const BwdPtrs p
     __syncthreads();
   }
   // Y = A E_bar, U = A Z
-  gemm64(r + R.oY(), dk, r + R.oA(), kC, 1, r + R.oEb(), dk, 1, dk, kC, 1.f, 0.f, sg);
-  gemm64(r + R.oU(), dv, r + R.oA(), kC, 1, r + R.oZ(), dv, 1, dv, kC, 1.f, 0.f, sg);
+  gemm64<kNP>(r + R.oY(), dk, r + R.oA(), kC, 1, r + R.oEb(), dk, 1, dk, kC, 1.f, 0.f, sg);
+  gemm64<kNP>(r + R.oU(), dv, r + R.oA(), kC, 1, r + R.oZ(), dv, 1, dv, kC, 1.f, 0.f, sg);
 }
 
 // ------------------------------------------------------- 2. forward states
@@ -874,28 +899,34 @@ __global__ void __launch_bounds__(kPassThreads, 1) bwd_dstate_pass(const BwdPtrs
 }
 
 // ------------------------------------------------------- 4. gradients
+// Buffers whose lifetimes do not overlap share space (every product ends on a
+// CTA barrier, so a buffer's next occupant is written only after its last
+// reader): dA_qk -> dA -> dT in one 64 x 64 region, the fp32 copy of dO ->
+// dY -> X in one 64 x max(d_k, d_v) region.
 struct Scr {
   int dk, dv;
   __host__ __device__ size_t mk() const { return static_cast<size_t>(kC) * dk; }
   __host__ __device__ size_t mv() const { return static_cast<size_t>(kC) * dv; }
-  __host__ __device__ size_t oDAqk() const { return 0; }
-  __host__ __device__ size_t oDA() const { return oDAqk() + kC * kC; }
-  __host__ __device__ size_t oX() const { return oDA() + kC * kC; }
-  __host__ __device__ size_t oDT() const { return oX() + kC * kC; }
-  __host__ __device__ size_t oDQg() const { return oDT() + kC * kC; }
+  __host__ __device__ size_t oR1() const { return 0; }
+  __host__ __device__ size_t oR2() const { return oR1() + kC * kC; }
+  __host__ __device__ size_t oDAqk() const { return oR1(); }
+  __host__ __device__ size_t oDA() const { return oR1(); }
+  __host__ __device__ size_t oDT() const { return oR1(); }
+  __host__ __device__ size_t oDO() const { return oR2(); }
+  __host__ __device__ size_t oDY() const { return oR2(); }
+  __host__ __device__ size_t oX() const { return oR2(); }
+  __host__ __device__ size_t oDQg() const { return oR2() + (mk() > mv() ? mk() : mv()); }
   __host__ __device__ size_t oDKb() const { return oDQg() + mk(); }
   __host__ __device__ size_t oDKt() const { return oDKb() + mk(); }
-  __host__ __device__ size_t oDY() const { return oDKt() + mk(); }
-  __host__ __device__ size_t oDEb() const { return oDY() + mk(); }
-  __host__ __device__ size_t oDG() const { return oDEb() + mk(); }
-  __host__ __device__ size_t oDZ() const { return oDG() + mk(); }
-  __host__ __device__ size_t oDO() const { return oDZ() + mv(); }
-  __host__ __device__ size_t oDgC() const { return oDO() + mv(); }
+  __host__ __device__ size_t oDEb() const { return oDKt() + mk(); }
+  __host__ __device__ size_t oDZ() const { return oDEb() + mk(); }
+  __host__ __device__ size_t oDgC() const { return oDZ() + mv(); }
   __host__ __device__ size_t size() const { return oDgC() + dk; }
 };
 
 template <typename T>
 __global__ void __launch_bounds__(kBwdThreads, 3) bwd_chunk_grad(const BwdPtrs p) {
+  constexpr int kNP = kProducts<T>;
   const Rec R{p.dk, p.dv};
   const Scr Q{p.dk, p.dv};
   const int cid = blockIdx.x;
@@ -944,25 +975,25 @@ __global__ void __launch_bounds__(kBwdThreads, 3) bwd_chunk_grad(const BwdPtrs p
   }
   __syncthreads();
   // dA_qk = tril(dO W^T, 0); dQ_gamma = dO S^T + dA_qk K_bar; dK_bar = dA_qk^T Q_gamma
-  gemm64(s + Q.oDAqk(), kC, dO, dv, 1, W, 1, dv, kC, dv, 1.f, 0.f, sg, 1);
-  gemm64(s + Q.oDQg(), dk, dO, dv, 1, S, 1, dv, dk, dv, 1.f, 0.f, sg);
-  gemm64(s + Q.oDQg(), dk, s + Q.oDAqk(), kC, 1, r + R.oKb(), dk, 1, dk, kC, 1.f, 1.f, sg);
-  gemm64(s + Q.oDKb(), dk, s + Q.oDAqk(), 1, kC, r + R.oQg(), dk, 1, dk, kC, 1.f, 0.f, sg);
+  gemm64<kNP>(s + Q.oDAqk(), kC, dO, dv, 1, W, 1, dv, kC, dv, 1.f, 0.f, sg, 1);
+  gemm64<kNP>(s + Q.oDQg(), dk, dO, dv, 1, S, 1, dv, dk, dv, 1.f, 0.f, sg);
+  gemm64<kNP>(s + Q.oDQg(), dk, s + Q.oDAqk(), kC, 1, r + R.oKb(), dk, 1, dk, kC, 1.f, 1.f, sg);
+  gemm64<kNP>(s + Q.oDKb(), dk, s + Q.oDAqk(), 1, kC, r + R.oQg(), dk, 1, dk, kC, 1.f, 0.f, sg);
   // dK_tail = W dS'^T; dY = -dW S^T
-  gemm64(s + Q.oDKt(), dk, W, dv, 1, dSn, 1, dv, dk, dv, 1.f, 0.f, sg);
-  gemm64(s + Q.oDY(), dk, dW, dv, 1, S, 1, dv, dk, dv, -1.f, 0.f, sg);
+  gemm64<kNP>(s + Q.oDKt(), dk, W, dv, 1, dSn, 1, dv, dk, dv, 1.f, 0.f, sg);
+  gemm64<kNP>(s + Q.oDY(), dk, dW, dv, 1, S, 1, dv, dk, dv, -1.f, 0.f, sg);
   // the notes' gate-aware dA = dU Z^T + dY E_bar^T (dU = dW)
-  gemm64(s + Q.oDA(), kC, dW, dv, 1, r + R.oZ(), 1, dv, kC, dv, 1.f, 0.f, sg);
-  gemm64(s + Q.oDA(), kC, s + Q.oDY(), dk, 1, r + R.oEb(), 1, dk, kC, dk, 1.f, 1.f, sg);
+  gemm64<kNP>(s + Q.oDA(), kC, dW, dv, 1, r + R.oZ(), 1, dv, kC, dv, 1.f, 0.f, sg);
+  gemm64<kNP>(s + Q.oDA(), kC, s + Q.oDY(), dk, 1, r + R.oEb(), 1, dk, kC, dk, 1.f, 1.f, sg);
   // dZ = A^T dU; dE_bar = A^T dY
-  gemm64(s + Q.oDZ(), dv, r + R.oA(), 1, kC, dW, dv, 1, dv, kC, 1.f, 0.f, sg);
-  gemm64(s + Q.oDEb(), dk, r + R.oA(), 1, kC, s + Q.oDY(), dk, 1, dk, kC, 1.f, 0.f, sg);
+  gemm64<kNP>(s + Q.oDZ(), dv, r + R.oA(), 1, kC, dW, dv, 1, dv, kC, 1.f, 0.f, sg);
+  gemm64<kNP>(s + Q.oDEb(), dk, r + R.oA(), 1, kC, s + Q.oDY(), dk, 1, dk, kC, 1.f, 0.f, sg);
   // the notes' adjoint of the inverse: dT = -tril(A^T dA A^T, -1)
-  gemm64(s + Q.oX(), kC, r + R.oA(), 1, kC, s + Q.oDA(), kC, 1, kC, kC, 1.f, 0.f, sg);
-  gemm64(s + Q.oDT(), kC, s + Q.oX(), kC, 1, r + R.oA(), 1, kC, kC, kC, -1.f, 0.f, sg, 2);
+  gemm64<kNP>(s + Q.oX(), kC, r + R.oA(), 1, kC, s + Q.oDA(), kC, 1, kC, kC, 1.f, 0.f, sg);
+  gemm64<kNP>(s + Q.oDT(), kC, s + Q.oX(), kC, 1, r + R.oA(), 1, kC, kC, kC, -1.f, 0.f, sg, 2);
   // dE_bar += dT K_bar; dK_bar += dT^T E_bar
-  gemm64(s + Q.oDEb(), dk, s + Q.oDT(), kC, 1, r + R.oKb(), dk, 1, dk, kC, 1.f, 1.f, sg);
-  gemm64(s + Q.oDKb(), dk, s + Q.oDT(), 1, kC, r + R.oEb(), dk, 1, dk, kC, 1.f, 1.f, sg);
+  gemm64<kNP>(s + Q.oDEb(), dk, s + Q.oDT(), kC, 1, r + R.oKb(), dk, 1, dk, kC, 1.f, 1.f, sg);
+  gemm64<kNP>(s + Q.oDKb(), dk, s + Q.oDT(), 1, kC, r + R.oEb(), dk, 1, dk, kC, 1.f, 1.f, sg);
   // the decay factors: dG = gamma dgamma with
   //   dgamma = dE_bar E - dK_bar K_bar / gamma - dK_tail K_tail / gamma + dQ_gamma Q_gamma / gamma,
   // dgamma_C += sum_r dK_tail k / gamma (= dK_tail K_bar), and dG of the last row

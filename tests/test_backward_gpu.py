@@ -4,7 +4,9 @@ finite differences).
 
 Bar, per gradient tensor on the same seeded inputs (the oracle sees the
 dtype-rounded inputs and dO): max|d| / max|ref| <= 1e-4 for fp32 inputs and
-2e-2 for bf16 inputs, as for the forward; the arithmetic is fp32 throughout.
+2e-2 for bf16 inputs, as for the forward; the arithmetic is fp32, the
+per-chunk products of bf16 inputs on single tf32 products (worst measured
+error over the flag sweep ~2.3e-3).
 """
 import numpy as np
 import pytest
