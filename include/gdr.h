@@ -293,9 +293,10 @@ gdr_status gdr_chunk_fwd_pipeline_segments(const gdr_shape* shape, int* segments
  *
  * dO is [B,T,H,d_v] in the call's dtype (16-byte aligned); dhT [B,H,d_k,d_v]
  * fp32 or NULL (zero). Inputs as gdr_chunk_fwd. The arithmetic is fp32 (products
- * on warp-level tensor-core MMAs with split operands), through per-chunk records
- * in `workspace` (at least
- * gdr_chunk_bwd_workspace() bytes, 16-byte aligned; about 0.9 MB per chunk at
+ * on warp-level tensor-core MMAs: split tf32 operands for fp32 inputs, single
+ * tf32 products in the per-chunk work for bf16 inputs), through per-chunk
+ * records in `workspace` (at least
+ * gdr_chunk_bwd_workspace() bytes, 16-byte aligned; about 0.79 MB per chunk at
  * d_k = d_v = 128): the chunk's forward quantities, the state entering and
  * the gradient leaving every chunk. The workspace starts with
  * status words: a chunk whose running log-decay sum falls below -80 (the
