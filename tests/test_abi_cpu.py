@@ -318,3 +318,57 @@ def test_pipelined_forward_workspace_policy_and_argument_rules(L):
     assert call(s, 4, FAKE, full, q=None) == 1
     assert call(s, 4, FAKE, full, hT=FAKE + 4) == 1
     assert call(_shape(dtype=_binding.GDR_F32), 2, FAKE, full) == 2
+
+
+def _bwd_ws(fn, **kw):
+    n = ctypes.c_size_t(0)
+    st = fn(ctypes.byref(_shape(**kw)), ctypes.byref(n))
+    return st, n.value
+
+
+@pytest.mark.parametrize("name", ["gdr_chunk_bwd_workspace", "gdr_token_bwd_workspace"])
+def test_backward_workspace_queries(L, name):
+    """The backwards' workspace sizes: a fixed head (status words), then a share
+    per 64-token chunk of every (batch, head) sequence (the token-order one also
+    holds one chunk of token states per sequence), so they grow by equal steps
+    in B and H, a ragged tail costs a whole chunk, and invalid shapes are
+    refused like the forward's."""
+    fn = getattr(L, name)
+    st, one = _bwd_ws(fn, dk=128, dv=128)
+    assert st == 0 and one > 0
+    sizes = [_bwd_ws(fn, B=b, dk=128, dv=128)[1] for b in (1, 2, 3)]
+    assert sizes[1] - sizes[0] == sizes[2] - sizes[1] > 0
+    assert _bwd_ws(fn, H=3, dk=128, dv=128)[1] == sizes[2]
+    assert _bwd_ws(fn, T=65, dk=128, dv=128)[1] == _bwd_ws(fn, T=128, dk=128, dv=128)[1]
+    step_t = _bwd_ws(fn, T=128, dk=128, dv=128)[1] - one   # one more chunk
+    if name == "gdr_chunk_bwd_workspace":
+        assert step_t == sizes[1] - sizes[0]                 # everything is per chunk
+    else:
+        assert 0 < step_t < sizes[1] - sizes[0]              # a checkpoint, not a sequence
+    # wider states take more per chunk
+    assert _bwd_ws(fn, dk=64, dv=64)[1] < one
+    # refusals: no output pointer, no shape, unsupported width, empty sequence
+    n = ctypes.c_size_t(0)
+    assert fn(ctypes.byref(_shape()), None) == 1
+    assert fn(None, ctypes.byref(n)) == 1
+    assert _bwd_ws(fn, dk=96)[0] == 2
+    assert _bwd_ws(fn, T=0)[0] == 1
+
+
+def test_chunk_backward_workspace_per_chunk(L):
+    """gdr.h states about 0.79 MB of chunk-backward workspace per chunk at
+    d_k = d_v = 128 (records, scratch, the states and their gradients)."""
+    _, a = _bwd_ws(L.gdr_chunk_bwd_workspace, B=1, T=64 * 64, dk=128, dv=128)
+    _, b = _bwd_ws(L.gdr_chunk_bwd_workspace, B=2, T=64 * 64, dk=128, dv=128)
+    per_chunk = (b - a) / 64
+    assert 0.75e6 < per_chunk < 0.83e6
+
+
+def test_value_beta_backward_workspace_is_the_token_order_one(L):
+    """The per-value-channel write strength has no chunk backward of its own:
+    both queries give the token-order backward's workspace for it."""
+    bc = gdr.BETA_CHANNEL
+    for dk, dv in ((64, 64), (128, 128), (64, 128)):
+        st1, a = _bwd_ws(L.gdr_chunk_bwd_workspace, T=1000, dk=dk, dv=dv, flags=bc)
+        st2, b = _bwd_ws(L.gdr_token_bwd_workspace, T=1000, dk=dk, dv=dv, flags=bc)
+        assert st1 == st2 == 0 and a == b > 0
