@@ -735,7 +735,8 @@ def measure_backward(gdr, dev, stream, flush, K, pk, clk, cfg=2):
     """gdr_chunk_bwd on the Gated DeltaNet workload (4 x 4096 x 16 x 128 bf16;
     gradients of <dO, o> + <dhT, hT>), timed alone: K calls, L2 flushed before
     each, CUDA events on the launching stream. Not part of the step or its
-    metric; fp32 arithmetic."""
+    metric; fp32 accumulation (bf16 inputs: single tf32 products in the per-chunk
+    kernels)."""
     c = wl.CONFIGS[cfg]
     xd = wl.config_inputs(cfg, gen_device=dev)
     B, T, H, dk, dv = c["B"], c["T"], c["H"], c["dk"], c["dv"]
