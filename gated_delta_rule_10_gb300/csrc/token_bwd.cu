@@ -31,6 +31,7 @@
 #include <stdint.h>
 
 #include "kernels.h"
+#include "token_io.cuh"
 
 namespace gdr {
 namespace {
@@ -40,53 +41,6 @@ constexpr int kTbCL = 2;
 constexpr int kTbCols = 2 * kTbNW * kTbCL;   // value columns per CTA (16)
 constexpr int kTbThreads = 32 * kTbNW;
 constexpr int kTbChunk = 64;
-
-__device__ __forceinline__ float to_f(float x) { return x; }
-__device__ __forceinline__ float to_f(__nv_bfloat16 x) { return __bfloat162float(x); }
-
-// N consecutive elements from p (aligned to their size in bytes) as floats, by
-// 16- or 8-byte loads
-template <int N>
-__device__ __forceinline__ void load_run(const float* p, float (&x)[N]) {
-  static_assert(N % 4 == 0, "float4 loads");
-#pragma unroll
-  for (int i = 0; i < N; i += 4) {
-    const float4 f = *reinterpret_cast<const float4*>(p + i);
-    x[i] = f.x; x[i + 1] = f.y; x[i + 2] = f.z; x[i + 3] = f.w;
-  }
-}
-template <int N>
-__device__ __forceinline__ void load_run(const __nv_bfloat16* p, float (&x)[N]) {
-  static_assert(N % 4 == 0, "8-byte loads at least");
-  if constexpr (N % 8 == 0) {
-#pragma unroll
-    for (int i = 0; i < N; i += 8) {
-      const uint4 u = *reinterpret_cast<const uint4*>(p + i);
-      const uint32_t w[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        x[i + 2 * j] = __uint_as_float(w[j] << 16);
-        x[i + 2 * j + 1] = __uint_as_float(w[j] & 0xffff0000u);
-      }
-    }
-  } else {
-#pragma unroll
-    for (int i = 0; i < N; i += 4) {
-      const uint2 u = *reinterpret_cast<const uint2*>(p + i);
-      x[i] = __uint_as_float(u.x << 16);
-      x[i + 1] = __uint_as_float(u.x & 0xffff0000u);
-      x[i + 2] = __uint_as_float(u.y << 16);
-      x[i + 3] = __uint_as_float(u.y & 0xffff0000u);
-    }
-  }
-}
-// two consecutive elements (an aligned pair)
-__device__ __forceinline__ float2 load_pair(const float* p) {
-  return *reinterpret_cast<const float2*>(p);
-}
-__device__ __forceinline__ float2 load_pair(const __nv_bfloat16* p) {
-  return __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(p));
-}
 
 template <int R>
 struct TbToken {
