@@ -206,7 +206,6 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     chunk_fwd_tc_kernel(const ChunkArgs a, int* status) {
   using L = TcLayout<DK>;
   using TM = TmemMap<DK>;
-  constexpr int VK = DK / 8;
   extern __shared__ unsigned char smem_raw[];
   // aligned by pointer arithmetic on the shared array, so the compiler keeps
   // every access below in the shared state space
@@ -216,7 +215,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int slice = blockIdx.x, h = blockIdx.y, bb = blockIdx.z;
   const int T = a.T, H = a.H, DV = a.dv;
-  const bool CH = a.flags & 1u, ER = a.flags & 2u, WR = a.flags & 4u, QM = a.flags & 8u;
+  const bool CH = a.flags & 1u, WR = a.flags & 4u, QM = a.flags & 8u;
   const int col0 = slice * kNV;
 
   float* sT = reinterpret_cast<float*>(smem + L::oT);
