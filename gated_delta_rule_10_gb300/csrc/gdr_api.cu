@@ -252,6 +252,8 @@ gdr_status chunk_fwd_impl(const gdr_shape* shape, int segments, const void* q, c
   if (forced && segments > 1 && !split_allowed(shape)) return GDR_ERR_UNSUPPORTED;
   if (forced && static_cast<long long>(shape->B) * segments > 65535)
     return GDR_ERR_UNSUPPORTED;   // grid z extent of the split scan
+  if (forced && segments > 1 && static_cast<long long>(shape->B) * shape->H > 65535)
+    return GDR_ERR_UNSUPPORTED;   // grid y extent of the run combination
   const int P = forced ? segments : default_segments(shape);
   size_t need_min = 0, need_full = 0;
   gdr_chunk_fwd_workspace_min(shape, &need_min);

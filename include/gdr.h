@@ -65,7 +65,8 @@
  *    anything is enqueued, and the outputs are left untouched. A launch
  *    failure reported by the CUDA runtime returns GDR_ERR_CUDA. Non-finite
  *    inputs propagate to the outputs; they are not detected.
- *  - Supported sizes: d_k, d_v in {64, 128}; any B, H >= 1 and T >= 1 with
+ *  - Supported sizes: d_k, d_v in {64, 128}; 1 <= B, H <= 65535 (launch grid
+ *    extents, GDR_ERR_UNSUPPORTED beyond) and T >= 1 with
  *    B*T*H*max(d_k, d_v) < 2^31 elements per tensor; a ragged last chunk is
  *    handled. 16-byte alignment is required for q, k, v, o, b, w, h0, hT and
  *    state; 4-byte alignment for g, beta and lam.
@@ -208,8 +209,9 @@ gdr_status gdr_chunk_fwd(const gdr_shape* shape, const void* q, const void* k,
  *
  * workspace: at least gdr_chunk_fwd_workspace_split(shape, segments) bytes,
  * else GDR_ERR_WORKSPACE. segments < 1 is GDR_ERR_INVALID_ARG; segments > 1
- * with fp32 or GDR_BETA_CHANNEL is GDR_ERR_UNSUPPORTED. Other arguments as
- * gdr_chunk_fwd.
+ * with fp32 or GDR_BETA_CHANNEL, B * segments > 65535, or segments > 1 with
+ * B * H > 65535 (launch grid extents) is GDR_ERR_UNSUPPORTED. Other arguments
+ * as gdr_chunk_fwd.
  */
 gdr_status gdr_chunk_fwd_split(const gdr_shape* shape, int segments, const void* q,
                                const void* k, const void* v, const float* g,

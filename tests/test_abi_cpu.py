@@ -267,6 +267,17 @@ def test_sequence_split_workspace_and_policy(L):
                                  vp(FAKE), None, vp(FAKE), ctypes.c_size_t(two), None) == 4
     assert L.gdr_chunk_fwd_split(ctypes.byref(s), 0, *(vp(FAKE),) * 5, None, None, None, None,
                                  vp(FAKE), None, vp(FAKE), ctypes.c_size_t(two), None) == 1
+    # a forced split past the launch grid's extents is unsupported, not a failed launch:
+    # B * segments (the split scan's grid z) and B * H (the run combination's grid y)
+    for B, H, P in ((40000, 1, 2), (300, 300, 2)):
+        big = _shape(B=B, T=64, H=H)
+        assert L.gdr_chunk_fwd_split(ctypes.byref(big), P, *(vp(FAKE),) * 5, None, None, None,
+                                     None, vp(FAKE), None, vp(FAKE), ctypes.c_size_t(1 << 40),
+                                     None) == 2
+    # one run stays the plain path at the same B * H
+    big = _shape(B=300, T=64, H=300)
+    n300 = ctypes.c_size_t(0)
+    assert L.gdr_chunk_fwd_workspace_split(ctypes.byref(big), 1, ctypes.byref(n300)) == 0
 
 
 def test_pipelined_forward_workspace_policy_and_argument_rules(L):
